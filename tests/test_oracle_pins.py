@@ -1,0 +1,507 @@
+"""Pins of the CPU oracle to what the formats and the mathematics fix.
+
+Each pin is checked against something other than the oracle itself: bit-field
+definitions of the element formats, exact rational brute force written here
+with Python integers and Fractions, fixtures printed on the pages, library
+routines (torch bf16 conversion, numpy integer matmul, scipy's logistic), and
+invariants. The mutation tests at the end plant plausible mistakes in the
+oracle (on the CPU) and check that at least one pin fails for each.
+"""
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.qmv_oracle as O
+import qmv_inputs as qi
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# Independent element-format definitions (bit fields, exact rationals)
+# ---------------------------------------------------------------------------
+
+def bf_e2m1(nib: int) -> Fraction:
+    """E2M1: sign bit 3, 2-bit exponent (bias 1) in bits 2..1, 1-bit mantissa in bit 0."""
+    s = (nib >> 3) & 1
+    e = (nib >> 1) & 3
+    m = nib & 1
+    if e == 0:
+        v = Fraction(m, 2)                        # subnormal: m * 2**(1-1) * 1/2
+    else:
+        v = Fraction(2) ** (e - 1) * (1 + Fraction(m, 2))
+    return -v if s else v
+
+
+def bf_e8m0(e: int) -> Fraction:
+    return Fraction(2) ** (e - 127)
+
+
+def bf_bf16(bits: int) -> Fraction:
+    s = (bits >> 15) & 1
+    ex = (bits >> 7) & 0xFF
+    man = bits & 0x7F
+    assert ex != 0xFF
+    if ex == 0:
+        v = Fraction(man, 128) * Fraction(2) ** (-126)
+    else:
+        v = (1 + Fraction(man, 128)) * Fraction(2) ** (ex - 127)
+    return -v if s else v
+
+
+def bf_fp16(bits: int) -> Fraction:
+    s = (bits >> 15) & 1
+    ex = (bits >> 10) & 0x1F
+    man = bits & 0x3FF
+    if ex == 0:
+        v = Fraction(man, 1024) * Fraction(2) ** (-14)
+    else:
+        v = (1 + Fraction(man, 1024)) * Fraction(2) ** (ex - 15)
+    return -v if s else v
+
+
+def fp32_round(x) -> float:
+    """Round an exact rational to the nearest fp32 (ties to even), no double rounding."""
+    v = Fraction(x)
+    if v == 0:
+        return 0.0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    n, rem = divmod(a, quantum)
+    n = int(n)
+    if rem > quantum / 2 or (rem == quantum / 2 and n % 2 == 1):
+        n += 1
+    r = float(n * quantum)
+    return -r if v < 0 else r
+
+
+def codes_from_packed(fmt: str, row: bytes, K: int):
+    """Canonical packed bytes of one row -> list of K codes, with Python ints."""
+    out = []
+    if fmt in ("mxfp4", "cb4"):
+        for k in range(K):
+            out.append((row[k // 2] >> (4 * (k % 2))) & 0xF)
+    elif fmt == "cb2":
+        for k in range(K):
+            out.append((row[k // 4] >> (2 * (k % 4))) & 3)
+    elif fmt == "cb3":
+        for k in range(K):
+            grp = k // 8
+            word = int.from_bytes(row[3 * grp:3 * grp + 3], "little")
+            out.append((word >> (3 * (k % 8))) & 7)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Pins (functions, so the mutation tests can re-run them)
+# ---------------------------------------------------------------------------
+
+def pin_e2m1_table():
+    got = O.e2m1_decode(np.arange(16))
+    for n in range(16):
+        assert Fraction(float(got[n])) == bf_e2m1(n), n
+        # every value is exactly representable in fp16 and bf16
+        assert float(np.float16(got[n])) == float(got[n])
+
+
+def pin_e2m1_stated_values():
+    # magnitudes {0,.5,1,1.5,2,3,4,6} for codes 0..7, negated for 8..15
+    mags = sorted({abs(bf_e2m1(n)) for n in range(16)})
+    assert mags == [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2),
+                    Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+    got = O.e2m1_decode(np.arange(16))
+    assert all(got[8 + i] == -got[i] for i in range(8))
+
+
+def pin_e8m0():
+    e = np.arange(256)
+    got = O.e8m0_decode(e)
+    for i in range(1, 255):
+        # fp32 with biased exponent field i and zero mantissa is exactly 2**(i-127)
+        f = struct.unpack("<f", struct.pack("<I", i << 23))[0]
+        assert got[i] == f, i
+        assert Fraction(float(got[i])) == bf_e8m0(i)
+    # e = 0: 2**-127, the fp32 subnormal with only mantissa bit 22 set
+    assert got[0] == struct.unpack("<f", struct.pack("<I", 0x00400000))[0]
+    assert np.isnan(got[255])
+
+
+def pin_bf16_conversions():
+    torch = pytest.importorskip("torch")
+    g = qi.rng(11)
+    bits = g.integers(0, 1 << 16, size=4096, dtype=np.uint16)
+    ex = (bits >> 7) & 0xFF
+    bits = bits[ex != 0xFF]
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_bits_to_f64(bits), ref)
+    # rounding: fp32 values round to bf16 exactly as torch does (single rounding)
+    f = (g.standard_normal(4096) * np.exp2(g.integers(-20, 20, 4096))).astype(np.float32)
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.f64_to_bf16_bits(f.astype(np.float64)), want)
+    # ties go to even: 1 + 2**-8 lies halfway between 1 and 1 + 2**-7
+    assert O.f64_to_bf16_bits(np.array([1 + 2.0 ** -8]))[0] == 0x3F80
+    assert O.f64_to_bf16_bits(np.array([1 + 3 * 2.0 ** -8]))[0] == 0x3F82
+    assert O.f64_to_bf16_bits(np.array([-(1 + 2.0 ** -8)]))[0] == 0xBF80
+
+
+def pin_packings():
+    g = qi.rng(12)
+    for fmt, bits in (("mxfp4", 4), ("cb4", 4), ("cb2", 2), ("cb3", 3)):
+        c = qi.codes(g, (3, 64), bits)
+        p = O.pack_codes(fmt, c)
+        assert p.shape == (3, 64 * bits // 8)
+        assert np.array_equal(O.unpack_codes(fmt, p), c)
+        for r in range(3):
+            assert codes_from_packed(fmt, bytes(p[r]), 64) == c[r].tolist()
+    # MXFP4: a little-endian uint32 read at byte k/2 holds elements k..k+7 in nibbles 0..7
+    c = qi.codes(g, (1, 64), 4)
+    p = bytes(O.pack_codes("mxfp4", c)[0])
+    for k in range(0, 64, 8):
+        word = int.from_bytes(p[k // 2:k // 2 + 4], "little")
+        assert [(word >> (4 * j)) & 0xF for j in range(8)] == c[0, k:k + 8].tolist()
+    # CB3 fixture; a 16-weight half-block is one 48-bit window of 6 bytes
+    with open(os.path.join(GOLDEN, "cb3_packing_example.txt")) as fh:
+        for line in fh:
+            if line.startswith("#") or not line.strip():
+                continue
+            lhs, rhs = line.split(":")
+            codes = np.array([int(t) for t in lhs.split()], dtype=np.uint8)
+            want = [int(t, 16) for t in rhs.split()]
+            assert O.pack_cb3(codes[None])[0].tolist() == want
+    c = qi.codes(g, (1, 64), 3)
+    p = bytes(O.pack_cb3(c)[0])
+    for h in range(4):
+        window = int.from_bytes(p[6 * h:6 * h + 6], "little")
+        assert [(window >> (3 * j)) & 7 for j in range(16)] == c[0, 16 * h:16 * h + 16].tolist()
+
+
+def read_page_tables():
+    tables = {}
+    with open(os.path.join(GOLDEN, "rocmfpx_code_tables.txt")) as fh:
+        for line in fh:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, *vals = line.split()
+            tables[name] = [int(v) for v in vals]
+    return tables
+
+
+def pin_decode_contract():
+    """Unpacked code -> value x half-block scale (e[i >= QK/2]) equals the dequantizer, bit-exact."""
+    tables = read_page_tables()
+    g = qi.rng(13)
+    for fmt, name in (("cb3", "fp3"), ("cb2", "fp2")):
+        lut = tables[name]
+        bits = qi.FORMAT_BITS[fmt]
+        c = qi.codes(g, (4, 64), bits)
+        e = qi.e8m0(g, (4, 4))                      # 2 half-block scales per 32-block
+        p = O.pack_codes(fmt, c)
+        W = O.cb_dequant(O.unpack_codes(fmt, p), e, lut, 16)
+        for r in range(4):
+            codes_r = codes_from_packed(fmt, bytes(p[r]), 64)
+            for i in range(64):
+                blk, within = divmod(i, 32)
+                half = 1 if within >= 16 else 0
+                want = lut[codes_r[i]] * bf_e8m0(int(e[r, 2 * blk + half]))
+                assert Fraction(float(W[r, i])) == want
+
+
+def brute_mxfp4(packed_rows, scales, x_bits, K):
+    out = []
+    for r, row in enumerate(packed_rows):
+        cs = codes_from_packed("mxfp4", bytes(row), K)
+        acc = Fraction(0)
+        for k in range(K):
+            acc += bf_e2m1(cs[k]) * bf_e8m0(int(scales[r, k // 32])) * bf_bf16(int(x_bits[k]))
+        out.append(acc)
+    return out
+
+
+def brute_cb(fmt, packed_rows, scales, lut, group, q, d_bits, K):
+    out = []
+    for r, row in enumerate(packed_rows):
+        cs = codes_from_packed(fmt, bytes(row), K)
+        acc = Fraction(0)
+        for k in range(K):
+            acc += (lut[cs[k]] * bf_e8m0(int(scales[r, k // group]))
+                    * int(q[k]) * bf_fp16(int(d_bits[k // 32])))
+        out.append(acc)
+    return out
+
+
+def pin_brute_force_mxfp4():
+    g = qi.rng(14)
+    for N, K in ((1, 32), (4, 64)):
+        c = qi.codes(g, (N, K), 4)
+        s = qi.e8m0(g, (N, K // 32))
+        x = qi.normal_bf16_bits(g, (1, K))
+        y = O.mxfp4_matvec(c, s, x)[0]
+        want = brute_mxfp4(O.pack_nibbles(c), s, x[0], K)
+        absum = O.mxfp4_abs_products(c, s, x)[0]
+        for r in range(N):
+            assert abs(Fraction(float(y[r])) - want[r]) <= Fraction(float(absum[r])) * Fraction(1, 10 ** 13)
+
+
+def pin_brute_force_cb():
+    g = qi.rng(15)
+    for fmt, lut in (("cb2", qi.LUT_CB2), ("cb3", qi.LUT_CB3), ("cb4", qi.LUT_CB4)):
+        group = qi.FORMAT_GROUP[fmt]
+        for N, K in ((1, 32), (4, 64)):
+            c = qi.codes(g, (N, K), qi.FORMAT_BITS[fmt])
+            s = qi.e8m0(g, (N, K // group))
+            q, d = O.q8_1_quantize(qi.normal_f32(g, (1, K)))
+            y = O.cb_matvec(c, s, lut, group, q, d)[0]
+            want = brute_cb(fmt, O.pack_codes(fmt, c), s, lut, group, q[0], d[0], K)
+            absum = O.cb_abs_products(c, s, lut, group, q, d)[0]
+            for r in range(N):
+                assert abs(Fraction(float(y[r])) - want[r]) <= Fraction(float(absum[r])) * Fraction(1, 10 ** 13)
+
+
+def pin_block_sums_exact():
+    g = qi.rng(16)
+    for fmt, lut in (("cb2", qi.LUT_CB2), ("cb3", qi.LUT_CB3), ("cb4", qi.LUT_CB4)):
+        span = qi.FORMAT_GROUP[fmt]
+        c = qi.codes(g, (4, 64), qi.FORMAT_BITS[fmt])
+        q = g.integers(-127, 128, size=(2, 64)).astype(np.int8)
+        got = O.cb_block_sums(c, lut, q, span)
+        for v in range(2):
+            for r in range(4):
+                cs = codes_from_packed(fmt, bytes(O.pack_codes(fmt, c)[r]), 64)
+                for h in range(64 // span):
+                    want = sum(lut[cs[i]] * int(q[v, i]) for i in range(h * span, (h + 1) * span))
+                    assert int(got[v, r, h]) == want
+
+
+def pin_identity_special_case():
+    """LUT = identity and all scales 2**0: the codebook matvec is an integer matmul."""
+    g = qi.rng(17)
+    for fmt in ("cb2", "cb3", "cb4"):
+        bits = qi.FORMAT_BITS[fmt]
+        group = qi.FORMAT_GROUP[fmt]
+        lut = list(range(1 << bits))
+        c = qi.codes(g, (8, 96), bits)
+        s = np.full((8, 96 // group), 127, dtype=np.uint8)
+        q = g.integers(-127, 128, size=(3, 96)).astype(np.int8)
+        d = np.full((3, 3), 0x3C00, dtype=np.uint16)            # fp16 1.0
+        want = q.astype(np.int64) @ c.astype(np.int64).T
+        assert np.array_equal(O.cb_matvec(c, s, lut, group, q, d), want.astype(np.float64))
+        sums = O.cb_block_sums(c, lut, q, group)
+        blocks = np.einsum("vkb,nkb->vnk", q.astype(np.int64).reshape(3, -1, group),
+                           c.astype(np.int64).reshape(8, -1, group))
+        assert np.array_equal(sums, blocks)
+    # MXFP4 with scale 2**0 and x = unit vectors picks single decoded weights
+    c = qi.codes(g, (5, 64), 4)
+    s = np.full((5, 2), 127, dtype=np.uint8)
+    eye = np.zeros((64, 64), dtype=np.uint16)
+    eye[np.arange(64), np.arange(64)] = 0x3F80                      # bf16 1.0
+    got = O.mxfp4_matvec(c, s, eye)                                 # [64, 5]
+    assert np.array_equal(got.T, O.e2m1_decode(c))
+
+
+def pin_q8_quantizer():
+    g = qi.rng(18)
+    x = qi.normal_f32(g, (3, 256)) * np.float32(3.0)
+    x[1, 32:64] = 0.0                                               # an all-zero block
+    q, d = O.q8_1_quantize(x)
+    qb = q.reshape(3, 8, 32).astype(np.int64)
+    xb = x.reshape(3, 8, 32)
+    assert np.all(np.abs(qb) <= 127)
+    for t in range(3):
+        for b in range(8):
+            amax = float(np.max(np.abs(xb[t, b])))
+            if amax == 0:
+                assert np.all(qb[t, b] == 0) and d[t, b] == 0
+                continue
+            i = int(np.argmax(np.abs(xb[t, b])))
+            assert abs(qb[t, b, i]) == 127
+            dd = fp32_round(Fraction(amax) / 127)
+            assert d[t, b] == np.float16(dd).view(np.uint16)
+            inv = fp32_round(Fraction(1) / Fraction(dd))
+            for k in range(32):
+                v = Fraction(fp32_round(Fraction(float(xb[t, b, k])) * Fraction(inv)))
+                mag = abs(v)
+                r = int(mag) + (1 if mag - int(mag) >= Fraction(1, 2) else 0)
+                r = min(r, 127)
+                assert int(qb[t, b, k]) == (-r if v < 0 else r)
+    # exact ties round away from zero: amax 127 gives d = 1, id = 1
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, :6] = [127.0, 2.5, -2.5, 0.5, -0.5, 1.5]
+    q, d = O.q8_1_quantize(x)
+    assert q[0, :6].tolist() == [127, 3, -3, 1, -1, 2]
+    assert d[0, 0] == 0x3C00
+
+
+def pin_gather():
+    g = qi.rng(19)
+    E, N, K = 5, 8, 64
+    c = qi.codes(g, (E, N, K), 4)
+    s = qi.e8m0(g, (E, N, K // 32))
+    x = qi.normal_bf16_bits(g, (2 * 3, K))
+    ids = np.array([[4, 0, 7], [2, -1, 2]], dtype=np.int32)      # 7 and -1 are invalid
+    for per_slot in (False, True):
+        y = O.mxfp4_moe_gather(c, s, x, ids, per_slot)
+        for t in range(2):
+            for j in range(3):
+                e = int(ids[t, j])
+                v = t * 3 + j if per_slot else t
+                if 0 <= e < E:
+                    want = O.mxfp4_dequant(c[e], s[e]) @ O.bf16_bits_to_f64(x[v])
+                    assert np.array_equal(y[t, j], want)
+                else:
+                    assert np.all(y[t, j] == 0)
+
+
+def pin_silu():
+    special = pytest.importorskip("scipy.special")
+    z = np.linspace(-30, 30, 1201)
+    assert np.allclose(O.silu(z), z * special.expit(z), rtol=1e-15, atol=1e-300)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    assert np.allclose(O.silu(z) - O.silu(-z), z, rtol=1e-13, atol=1e-13)
+    g = np.array([1.0, -2.0, 0.5])
+    u = np.array([3.0, 0.25, -4.0])
+    assert np.allclose(O.swiglu(g, u), u * g * special.expit(g), rtol=1e-15)
+
+
+ALL_PINS = [pin_e2m1_table, pin_e2m1_stated_values, pin_e8m0, pin_bf16_conversions,
+            pin_packings, pin_decode_contract, pin_brute_force_mxfp4, pin_brute_force_cb,
+            pin_block_sums_exact, pin_identity_special_case, pin_q8_quantizer, pin_gather,
+            pin_silu]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_page_tables_decode():
+    """The page's fp3/fp2 tables, used as LUTs, decode codes to exactly those values."""
+    tables = read_page_tables()
+    assert tables["fp3"] == [0, 1, 2, 4, 0, -1, -2, -4]
+    for name, bits in (("fp3", 3), ("fp2", 2)):
+        c = np.arange(1 << bits, dtype=np.uint8)[None, :].repeat(1, 0)
+        c = np.tile(c, (1, 32 // (1 << bits) * 2))[:, :32]
+        s = np.full((1, 2), 127, dtype=np.uint8)
+        W = O.cb_dequant(c, s, tables[name], 16)
+        assert W[0].tolist() == [float(tables[name][int(k)]) for k in c[0]]
+
+
+# ---------------------------------------------------------------------------
+# Mutation tests: a planted oracle mistake must fail at least one pin
+# ---------------------------------------------------------------------------
+
+def _fails_some_pin(pins):
+    for p in pins:
+        try:
+            p()
+        except Exception:
+            return True
+    return False
+
+
+def test_mutation_sign_bit_dropped(monkeypatch):
+    real = O.e2m1_decode
+    monkeypatch.setattr(O, "e2m1_decode", lambda c: np.abs(real(c)))
+    assert _fails_some_pin([pin_e2m1_table, pin_brute_force_mxfp4])
+
+
+def test_mutation_nibble_order(monkeypatch):
+    monkeypatch.setattr(O, "pack_nibbles",
+                        lambda c: (np.asarray(c)[..., 1::2] | (np.asarray(c)[..., 0::2] << 4)).astype(np.uint8))
+    assert _fails_some_pin([pin_packings])
+
+
+def test_mutation_e8m0_bias(monkeypatch):
+    monkeypatch.setattr(O, "e8m0_decode", lambda e: np.ldexp(1.0, np.asarray(e).astype(np.int64) - 126))
+    assert _fails_some_pin([pin_e8m0, pin_brute_force_mxfp4, pin_brute_force_cb])
+
+
+def test_mutation_cb3_bit_order(monkeypatch):
+    def bad_pack(codes):
+        c = np.asarray(codes, dtype=np.uint32)
+        lead = c.shape[:-1]
+        gg = c.reshape(lead + (-1, 8))
+        word = np.zeros(gg.shape[:-1], dtype=np.uint32)
+        for j in range(8):
+            word |= gg[..., j] << (21 - 3 * j)
+        out = np.stack([(word >> (8 * b)) & 0xFF for b in range(3)], -1).astype(np.uint8)
+        return out.reshape(lead + (-1,))
+    monkeypatch.setattr(O, "pack_cb3", bad_pack)
+    assert _fails_some_pin([pin_packings])
+
+
+def test_mutation_q8_half_even(monkeypatch):
+    real = O.q8_1_quantize
+
+    def half_even(x):
+        x = np.asarray(x, dtype=np.float32)
+        lead, K = x.shape[:-1], x.shape[-1]
+        xb = x.reshape(lead + (K // 32, 32))
+        d = (np.max(np.abs(xb), -1) / np.float32(127)).astype(np.float32)
+        with np.errstate(divide="ignore"):
+            inv = np.where(d != 0, np.float32(1) / d, np.float32(0)).astype(np.float32)
+        v = (xb * inv[..., None]).astype(np.float32)
+        q = np.clip(np.rint(v), -127, 127).astype(np.int8).reshape(lead + (K,))
+        return q, real(x)[1]
+    monkeypatch.setattr(O, "q8_1_quantize", half_even)
+    assert _fails_some_pin([pin_q8_quantizer])
+
+
+def test_mutation_transposed_operand(monkeypatch):
+    monkeypatch.setattr(O, "mxfp4_matvec",
+                        lambda c, s, x: O.bf16_bits_to_f64(x) @ O.mxfp4_dequant(c, s))
+    assert _fails_some_pin([pin_brute_force_mxfp4])
+
+
+def test_mutation_mxfp4_group_16(monkeypatch):
+    def bad(codes, scales):
+        K = codes.shape[-1]
+        gidx = np.minimum(np.arange(K) // 16, scales.shape[-1] - 1)
+        return O.e2m1_decode(codes) * O.e8m0_decode(scales)[..., gidx]
+    monkeypatch.setattr(O, "mxfp4_dequant", bad)
+    assert _fails_some_pin([pin_brute_force_mxfp4])
+
+
+def test_mutation_half_block_scale_ignored(monkeypatch):
+    real = O.cb_dequant
+
+    def bad(codes, scales, lut, group):
+        s = np.asarray(scales).copy()
+        if group == 16:
+            s[..., 1::2] = s[..., 0::2]                # use the first half-block scale for both
+        return real(codes, s, lut, group)
+    monkeypatch.setattr(O, "cb_dequant", bad)
+    assert _fails_some_pin([pin_decode_contract])
+
+
+def test_mutation_block_sum_span(monkeypatch):
+    real = O.cb_block_sums
+    monkeypatch.setattr(O, "cb_block_sums",
+                        lambda c, lut, q, span: real(c, lut, q, span) + (1 if span == 16 else 0))
+    assert _fails_some_pin([pin_block_sums_exact, pin_brute_force_cb])
+
+
+def test_mutation_fp16_d_ignored(monkeypatch):
+    real = O.cb_matvec
+
+    def bad(codes, scales, lut, group, q, d_bits):
+        return real(codes, scales, lut, group, q, np.full_like(d_bits, 0x3C00))
+    monkeypatch.setattr(O, "cb_matvec", bad)
+    assert _fails_some_pin([pin_brute_force_cb])
+
+
+def test_mutation_invalid_id_not_zeroed(monkeypatch):
+    real = O.moe_gather
+
+    def bad(matvec, n_experts, ids, per_slot, N):
+        return real(matvec, n_experts, np.clip(ids, 0, n_experts - 1), per_slot, N)
+    monkeypatch.setattr(O, "moe_gather", bad)
+    assert _fails_some_pin([pin_gather])
