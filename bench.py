@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark: weight-stream GB/s of the MXFP4 MoE decode layer sweep on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one decode token through 24 gpt-oss-style MoE layers. Each layer
+gathers 4 of 32 experts for gate and up (2880 x 2880 MXFP4, shared bf16
+activation), applies SwiGLU, and gathers the same 4 experts of down (per-slot
+activation) -- 12 expert matrices, 52,876,800 weight bytes per layer. Router
+ids are fresh each step. The weight bytes of a step (1.27 GB) exceed L2, so
+nothing is served from L2 across steps. `value` = weight bytes of all steps on
+all ranks / max-over-ranks device time (CUDA events, CUDA-graph replay).
+
+Multi-GPU: the workload does not shard; every rank runs an independent replica
+(weak scaling) and rank 0 reports the aggregate.
+
+--impl reference times the CPU oracle (single-threaded numpy, the repository's
+reference definition of the method) on the same workload, one expert matvec
+per step.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU legs time the oracle single-threaded; pin BLAS before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qmv_inputs as qi  # noqa: E402
+
+LAYERS = qi.CONFIG1_LAYERS
+E, N, K, TOP_K = 32, 2880, 2880, 4
+MATRIX_BYTES = 4406400                     # 2880*1440 code bytes + 2880*90 E8M0 bytes
+LAYER_BYTES = 12 * MATRIX_BYTES            # gate, up, down x 4 experts
+STEP_BYTES = LAYERS * LAYER_BYTES
+GATHER_BYTES = TOP_K * MATRIX_BYTES        # one gather launch (4 distinct experts)
+
+WORKLOAD = ("gpt-oss MoE decode layer sweep: 24 layers x (gate, up, down) MXFP4 E2M1/E8M0-g32 "
+            "2880x2880 expert gathers, E=32, top_k=4 fresh ids per step, 1 token, bf16 activations, "
+            "SwiGLU between")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling (nvidia-smi) during the timed window
+# ---------------------------------------------------------------------------
+
+def gpu_uuid(dev) -> str:
+    import torch
+    u = str(torch.cuda.get_device_properties(dev).uuid)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [r for t, r in self.rows if t0 <= t <= t1] or [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+def oracle_expert_matvecs(canon, scales, x_bits, budget_s: float, min_calls: int = 1):
+    """Run the oracle's MXFP4 matvec on consecutive pool experts until the time budget is spent.
+
+    The oracle decodes the canonical bytes itself (unpack, E2M1, E8M0) inside
+    the timed loop, as a CPU implementation of the same call would.
+    """
+    import oracle
+    calls, t0 = 0, time.perf_counter()
+    while calls < min_calls or time.perf_counter() - t0 < budget_s:
+        e = calls % len(canon)
+        oracle.mxfp4_matvec(oracle.unpack_nibbles(canon[e]), scales[e], x_bits)
+        calls += 1
+    return calls, time.perf_counter() - t0
+
+
+def cpu_baseline(canon, scales, x_bits, budget_s=12.0):
+    calls, dt = oracle_expert_matvecs(canon, scales, x_bits, budget_s)
+    return {"value": calls * MATRIX_BYTES / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} expert matvecs of the config workload (2880x2880 MXFP4 x bf16, float64 "
+                      f"oracle incl. decode) in {dt:.1f} s, single-threaded numpy"}
+
+
+def make_pool(n: int, seed: int):
+    """n experts of canonical MXFP4 code bytes [n][N][K/2], E8M0 scales and one bf16 activation."""
+    g = qi.rng(seed)
+    canon = qi.canonical_uniform_codes(g, (n, N), K, 4)
+    scales = qi.e8m0(g, (n, N, K // 32))
+    x = qi.normal_bf16_bits(g, (1, K))
+    return canon, scales, x
+
+
+# ---------------------------------------------------------------------------
+# Distributed helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over the process group (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(bytes_per_step_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job GB/s: the bytes every rank streamed over the slowest rank's time."""
+    return bytes_per_step_per_rank * steps * world / max_seconds / 1e9
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    canon, scales, x = make_pool(4, qi.CONFIG1_GATE.seed)
+    for _ in range(args.warmup):
+        oracle_expert_matvecs(canon, scales, x, 0.0)
+    t0 = time.perf_counter()
+    calls, _ = oracle_expert_matvecs(canon, scales, x, 0.0, min_calls=args.steps)
+    dt = time.perf_counter() - t0
+    value = calls * MATRIX_BYTES / dt / 1e9
+    sample = (f"one 2880x2880 MXFP4 expert matvec (4,406,400 weight bytes) per step, float64 oracle, "
+              f"single-threaded numpy, {calls} steps in {dt:.1f} s")
+    line = {
+        "impl": "reference", "metric": "quantized matvec weight-stream GB/s (MXFP4 MoE decode layer sweep)",
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / calls * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded uniform codes, E8M0 in [120,130], N(0,1) bf16 activations)",
+        "config": {"workload": WORKLOAD, "step": "one expert matvec of the workload"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import bit_quantized_moe_gb300 as qmv
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # --- weights: a pool of distinct packed experts replicated over 24 layers x 3 projections x 32 experts
+    pool_n = 32
+    pool_canon, pool_scales, x_bits = make_pool(pool_n, qi.CONFIG1_GATE.seed)
+    desc_pool = qmv.wdesc("mxfp4", N, K, pool_n)
+    packed_pool = qmv.qmv_pack_weights(desc_pool, pool_canon, pool_scales)
+    desc = qmv.wdesc("mxfp4", N, K, E)
+    eb = qmv.qmv_packed_expert_bytes(desc)
+    pool_dev = torch.from_numpy(packed_pool).to(dev).view(pool_n, eb)
+    W = torch.empty(LAYERS * 3 * E, eb, dtype=torch.uint8, device=dev)
+    W.view(-1, pool_n, eb).copy_(pool_dev.unsqueeze(0).expand(LAYERS * 3 * E // pool_n, pool_n, eb))
+    W = W.view(LAYERS, 3, E * eb)
+    del pool_dev
+
+    x_dev = torch.from_numpy(x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    total_steps = args.warmup + args.steps
+    g = qi.rng(1000 + rank)
+    ids_host = np.stack([np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(LAYERS)]) for _ in range(total_steps)])
+    ids_all = torch.from_numpy(ids_host).to(dev)               # [steps][layers][1][4]
+    ids_buf = torch.empty(LAYERS, 1, TOP_K, dtype=torch.int32, device=dev)
+    yg = torch.empty(LAYERS, 1, TOP_K, N, dtype=torch.bfloat16, device=dev)
+    yu = torch.empty_like(yg)
+    h = torch.empty_like(yg)
+    y = torch.empty_like(yg)
+
+    def gather(w, xin, per_slot, ids, out, events):
+        if events is not None:
+            events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+            events[-1][0].record()
+        qmv.qmv_moe_gather(desc, w, xin, per_slot, ids, 1, TOP_K, out)
+        if events is not None:
+            events[-1][1].record()
+
+    def step(events=None):
+        """One decode token through all layers: gate, up, SwiGLU, down per layer."""
+        for l in range(LAYERS):
+            gather(W[l, 0], x_dev, 0, ids_buf[l], yg[l], events)
+            gather(W[l, 1], x_dev, 0, ids_buf[l], yu[l], events)
+            qmv.qmv_swiglu_bf16(yg[l], yu[l], h[l], TOP_K * N)
+            gather(W[l, 2], h[l], 1, ids_buf[l], y[l], events)
+
+    # eager warm-up (sets kernel attributes), then capture one step in a CUDA graph
+    ids_buf.copy_(ids_all[0])
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(dev))
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        ids_buf.copy_(ids_all[i])
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    ev0.record()
+    for i in range(args.steps):
+        ids_buf.copy_(ids_all[args.warmup + i])
+        graph.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier()
+    wall1 = time.time()
+    # keep the same work running until the sampler has seen >= 1.5 s of it
+    while time.time() - wall0 < 1.5:
+        for i in range(20):
+            ids_buf.copy_(ids_all[i % total_steps])
+            graph.replay()
+        torch.cuda.synchronize()
+    wall2 = time.time()
+    sampler.stop()
+    dt_ms = ev0.elapsed_time(ev1)
+    dt_max = max_over_ranks(dt_ms / 1e3, world, dev)
+    value = aggregate_value(STEP_BYTES, args.steps, world, dt_max)
+    clocks = sampler.summary(wall0, wall2)
+    clocks["window_s"] = round(wall2 - wall0, 3)
+    clocks["timed_s"] = round(wall1 - wall0, 3)
+
+    # --- dominant kernel: per-launch device time of the gather, eager, one event pair per launch
+    events = []
+    n_roof = min(args.steps, 20)
+    for i in range(n_roof):
+        ids_buf.copy_(ids_all[args.warmup + i])
+        step(events)
+    torch.cuda.synchronize()
+    durs = [a.elapsed_time(b) for a, b in events]
+    gather_ms = statistics.mean(durs)
+    hbm, peak_kind = peaks()
+    achieved = GATHER_BYTES / (gather_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": args.traffic, "kernel": "matvec_kernel<MXFP4,1> (qmv_moe_gather)",
+                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "launch_ms_mean": gather_ms,
+                "launch_ms_median": statistics.median(durs), "launches_timed": len(durs),
+                "algorithmic_bytes_per_launch": GATHER_BYTES}
+
+    # --- e2e: host buffers, h2d of x and ids, graph step, d2h of every layer's output
+    x_host = torch.from_numpy(x_bits.view(np.int16)).pin_memory()
+    ids_host_p = torch.from_numpy(ids_host).pin_memory()
+    y_host = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
+    n_e2e = min(args.steps, 50)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        x_dev.view(torch.int16).copy_(x_host, non_blocking=True)
+        ids_buf.copy_(ids_host_p[args.warmup + i], non_blocking=True)
+        graph.replay()
+        y_host.copy_(y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    t_e2e = time.perf_counter() - t0
+    t_e2e = max_over_ranks(t_e2e, world, dev)
+    e2e = {"value": aggregate_value(STEP_BYTES, n_e2e, world, t_e2e), "unit": "GB/s",
+           "h2d_bytes_per_step": x_host.numel() * 2 + ids_buf.numel() * 4,
+           "d2h_bytes_per_step": y_host.numel() * 2, "steps": n_e2e}
+    status = qmv.qmv_device_status(clear=True)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(pool_canon[:4], pool_scales[:4], x_bits)
+
+    if rank == 0:
+        line = {
+            "metric": "quantized matvec weight-stream GB/s (MXFP4 MoE decode layer sweep)",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt_max * 1e3 / args.steps, "us_per_moe_layer": dt_max * 1e6 / args.steps / LAYERS,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "frac_of_hbm_peak": value / world / hbm,
+            "dtype": "mxfp4(e2m1,e8m0) x bf16 -> f32 accumulate",
+            "data": "synthetic (seeded uniform E2M1 codes, E8M0 in [120,130], N(0,1) bf16 activations)",
+            "config": {"workload": WORKLOAD, "layers": LAYERS, "experts": E, "top_k": TOP_K, "N": N, "K": K,
+                       "ntok": 1, "weight_bytes_per_step": STEP_BYTES,
+                       "l2": "inputs larger than L2: 1.27 GB of expert weights per step, fresh ids every step",
+                       "launch": "CUDA graph of 96 kernels per step (72 gathers + 24 SwiGLU), PDL between kernels",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": args.steps * LAYERS * 4, "cpu_baseline": cpu, "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per gather launch from an ncu capture of the current kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,328 @@
+// qmv_api.cpp -- the C ABI (include/qmv.h): argument checks, error reporting,
+// dispatch to the launchers. Nothing here reads device memory or synchronizes,
+// except qmv_device_status.
+#include "../../include/qmv.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "qmv_internal.h"
+#include "qmv_layout.h"
+
+namespace qmv {
+void pack_expert(const Geometry& g, const uint8_t* codes, const uint8_t* scales, uint8_t* out);
+void unpack_expert(const Geometry& g, const uint8_t* in, uint8_t* codes, uint8_t* scales);
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return QMV_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  cudaGetLastError();  // clear a non-sticky error so later calls start clean
+  return fail(QMV_ECUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_desc(const qmv_wdesc* d) {
+  if (d == nullptr) return fail(QMV_EINVAL, "descriptor is NULL");
+  if (d->fmt < QMV_MXFP4 || d->fmt > QMV_CB4) return fail(QMV_EINVAL, "unknown format %d", d->fmt);
+  if (d->N < 1 || d->N > QMV_MAX_N) return fail(QMV_ESHAPE, "N=%d outside [1, %d]", d->N, QMV_MAX_N);
+  if (d->K < 32 || d->K > QMV_MAX_K || d->K % 32 != 0)
+    return fail(QMV_ESHAPE, "K=%d must be a multiple of 32 in [32, %d]", d->K, QMV_MAX_K);
+  if (d->n_experts < 1) return fail(QMV_EINVAL, "n_experts=%d must be >= 1", d->n_experts);
+  return QMV_OK;
+}
+
+void lut_words(const qmv_wdesc* d, uint32_t out[4]) {
+  for (int w = 0; w < 4; ++w) {
+    uint32_t v = 0;
+    for (int b = 0; b < 4; ++b) v |= (uint32_t)(uint8_t)d->lut[4 * w + b] << (8 * b);
+    out[w] = v;
+  }
+}
+
+struct DevInfo {
+  int sm_count = 0;
+  size_t smem_optin = 0;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+const DevInfo* dev_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& di = g_dev[dev];
+  if (di.sm_count == 0) {
+    int sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return nullptr;
+    di.sm_count = sms;
+    di.smem_optin = (size_t)smem;
+  }
+  return &di;
+}
+
+cudaError_t launch_for(const MatvecArgs& a) {
+  switch (a.fmt) {
+    case MXFP4: return launch_matvec_mxfp4(a);
+    case CB2: return launch_matvec_cb2(a);
+    case CB3: return launch_matvec_cb3(a);
+    default: return launch_matvec_cb4(a);
+  }
+}
+
+int run_matvec(const qmv_wdesc* desc, const void* w, const void* x, int per_slot, const int32_t* ids,
+               int ntok, int top_k, void* y, int32_t* dbg, size_t dbg_bytes, cudaStream_t stream,
+               const char* name) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (w == nullptr || x == nullptr || y == nullptr)
+    return fail(QMV_EINVAL, "%s: weight, activation and output pointers must be non-NULL", name);
+  if (ntok < 1 || ntok > QMV_MAX_NTOK) return fail(QMV_EINVAL, "%s: ntok=%d outside [1, %d]", name, ntok, QMV_MAX_NTOK);
+  const bool gather = ids != nullptr;
+  if (gather) {
+    if (top_k < 1 || top_k > QMV_MAX_TOPK)
+      return fail(QMV_EINVAL, "%s: top_k=%d outside [1, %d]", name, top_k, QMV_MAX_TOPK);
+  } else if (desc->n_experts != 1) {
+    return fail(QMV_EINVAL, "%s: a dense matvec needs n_experts == 1 (got %d)", name, desc->n_experts);
+  }
+  if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (gather && !aligned16(ids)))
+    return fail(QMV_EALIGN, "%s: device pointers must be 16-byte aligned", name);
+  if (dbg != nullptr) {
+    if (desc->fmt == QMV_MXFP4) return fail(QMV_EINVAL, "%s: block sums exist only for codebook formats", name);
+    if (!aligned16(dbg)) return fail(QMV_EALIGN, "%s: sums pointer must be 16-byte aligned", name);
+    const int span = fmt_group(desc->fmt);
+    const size_t slots = gather ? (size_t)ntok * top_k : (size_t)ntok;
+    const size_t need = slots * desc->N * (desc->K / span) * sizeof(int32_t);
+    if (dbg_bytes < need) return fail(QMV_ESIZE, "%s: sums buffer %zu bytes < %zu", name, dbg_bytes, need);
+  }
+  const Geometry g = make_geometry(desc->fmt, desc->N, desc->K);
+  MatvecArgs a;
+  a.fmt = desc->fmt;
+  a.N = desc->N;
+  a.K = desc->K;
+  a.n_experts = desc->n_experts;
+  a.w = w;
+  a.expert_stride = g.expert;
+  a.x = x;
+  a.per_slot = gather ? (per_slot != 0) : 0;
+  a.nvec = (gather && a.per_slot) ? ntok * top_k : ntok;
+  a.ids = ids;
+  a.ntok = ntok;
+  a.top_k = gather ? top_k : 1;
+  a.y = y;
+  a.dbg = dbg;
+  lut_words(desc, a.lut);
+  a.stream = stream;
+  const DevInfo* di = dev_info();
+  if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
+  const size_t smem = matvec_smem_bytes(a);
+  if (smem == 0 || smem > di->smem_optin)
+    return fail(QMV_ESHAPE, "%s: %d activation vectors of K=%d do not fit in shared memory", name, a.nvec,
+                desc->K);
+  cudaError_t e = launch_for(a);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+}  // namespace
+
+int device_sm_count() {
+  const DevInfo* di = dev_info();
+  return di ? di->sm_count : 1;
+}
+
+size_t device_max_smem_optin() {
+  const DevInfo* di = dev_info();
+  return di ? di->smem_optin : 0;
+}
+
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+int32_t qmv_scale_group(int32_t fmt) { return (fmt >= 0 && fmt <= 3) ? fmt_group(fmt) : 0; }
+
+int32_t qmv_code_bits(int32_t fmt) { return (fmt >= 0 && fmt <= 3) ? fmt_bits(fmt) : 0; }
+
+size_t qmv_canonical_code_bytes(const qmv_wdesc* d) {
+  if (check_desc(d)) return 0;
+  return (size_t)d->N * d->K * fmt_bits(d->fmt) / 8;
+}
+
+size_t qmv_canonical_scale_bytes(const qmv_wdesc* d) {
+  if (check_desc(d)) return 0;
+  return (size_t)d->N * (d->K / fmt_group(d->fmt));
+}
+
+size_t qmv_packed_expert_bytes(const qmv_wdesc* d) {
+  if (check_desc(d)) return 0;
+  return (size_t)make_geometry(d->fmt, d->N, d->K).expert;
+}
+
+size_t qmv_packed_bytes(const qmv_wdesc* d) {
+  if (check_desc(d)) return 0;
+  return (size_t)make_geometry(d->fmt, d->N, d->K).expert * d->n_experts;
+}
+
+int qmv_pack_weights(const qmv_wdesc* d, const uint8_t* codes, const uint8_t* scales, void* out,
+                     size_t out_bytes) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!codes || !scales || !out) return fail(QMV_EINVAL, "qmv_pack_weights: NULL buffer");
+  const Geometry g = make_geometry(d->fmt, d->N, d->K);
+  const size_t need = (size_t)g.expert * d->n_experts;
+  if (out_bytes < need) return fail(QMV_ESIZE, "qmv_pack_weights: output %zu bytes < %zu", out_bytes, need);
+  const size_t cb = (size_t)d->N * d->K * fmt_bits(d->fmt) / 8;
+  const size_t sb = (size_t)d->N * (d->K / fmt_group(d->fmt));
+  for (int e = 0; e < d->n_experts; ++e) {
+    pack_expert(g, codes + e * cb, scales + e * sb, static_cast<uint8_t*>(out) + (size_t)e * g.expert);
+  }
+  return ok();
+}
+
+int qmv_unpack_weights(const qmv_wdesc* d, const void* packed, size_t packed_bytes, uint8_t* codes,
+                       uint8_t* scales) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!codes || !scales || !packed) return fail(QMV_EINVAL, "qmv_unpack_weights: NULL buffer");
+  const Geometry g = make_geometry(d->fmt, d->N, d->K);
+  const size_t need = (size_t)g.expert * d->n_experts;
+  if (packed_bytes < need)
+    return fail(QMV_ESIZE, "qmv_unpack_weights: input %zu bytes < %zu", packed_bytes, need);
+  const size_t cb = (size_t)d->N * d->K * fmt_bits(d->fmt) / 8;
+  const size_t sb = (size_t)d->N * (d->K / fmt_group(d->fmt));
+  for (int e = 0; e < d->n_experts; ++e) {
+    unpack_expert(g, static_cast<const uint8_t*>(packed) + (size_t)e * g.expert, codes + e * cb, scales + e * sb);
+  }
+  return ok();
+}
+
+size_t qmv_act_q8_vec_bytes(int32_t K) {
+  if (K < 32 || K > QMV_MAX_K || K % 32) return 0;
+  return (size_t)q8_vec_bytes(K);
+}
+
+size_t qmv_act_q8_bytes(int32_t nvec, int32_t K) {
+  if (nvec < 1) return 0;
+  return (size_t)nvec * qmv_act_q8_vec_bytes(K);
+}
+
+int qmv_quantize_act_q8(const float* x, int32_t nvec, int32_t K, void* xq, size_t xq_bytes, void* stream) {
+  if (!x || !xq) return fail(QMV_EINVAL, "qmv_quantize_act_q8: NULL pointer");
+  if (nvec < 1 || nvec > QMV_MAX_NTOK * QMV_MAX_TOPK)
+    return fail(QMV_EINVAL, "qmv_quantize_act_q8: nvec=%d outside [1, %d]", nvec, QMV_MAX_NTOK * QMV_MAX_TOPK);
+  if (K < 32 || K > QMV_MAX_K || K % 32)
+    return fail(QMV_ESHAPE, "qmv_quantize_act_q8: K=%d must be a multiple of 32 in [32, %d]", K, QMV_MAX_K);
+  if (!aligned16(x) || !aligned16(xq)) return fail(QMV_EALIGN, "qmv_quantize_act_q8: pointers must be 16-byte aligned");
+  const size_t need = qmv_act_q8_bytes(nvec, K);
+  if (xq_bytes < need) return fail(QMV_ESIZE, "qmv_quantize_act_q8: output %zu bytes < %zu", xq_bytes, need);
+  cudaError_t e = launch_quantize_q8(x, nvec, K, xq, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmv_quantize_act_q8");
+  return ok();
+}
+
+int qmv_act_q8_unpack(const void* xq, int32_t nvec, int32_t K, int8_t* q, uint16_t* d) {
+  if (!xq || !q || !d) return fail(QMV_EINVAL, "qmv_act_q8_unpack: NULL pointer");
+  if (nvec < 1 || K < 32 || K > QMV_MAX_K || K % 32) return fail(QMV_ESHAPE, "qmv_act_q8_unpack: bad shape");
+  const size_t vb = (size_t)q8_vec_bytes(K);
+  for (int v = 0; v < nvec; ++v) {
+    const uint8_t* src = static_cast<const uint8_t*>(xq) + v * vb;
+    std::memcpy(q + (size_t)v * K, src, K);
+    std::memcpy(d + (size_t)v * (K / 32), src + K, (size_t)(K / 32) * 2);
+  }
+  return ok();
+}
+
+int qmv_dense(const qmv_wdesc* desc, const void* w, const void* x, int32_t ntok, void* y, void* stream) {
+  return run_matvec(desc, w, x, 0, nullptr, ntok, 1, y, nullptr, 0, static_cast<cudaStream_t>(stream),
+                    "qmv_dense");
+}
+
+int qmv_moe_gather(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x, const int32_t* ids,
+                   int32_t ntok, int32_t top_k, void* y, void* stream) {
+  if (ids == nullptr) return fail(QMV_EINVAL, "qmv_moe_gather: ids must be non-NULL");
+  return run_matvec(desc, w, x, per_slot_x, ids, ntok, top_k, y, nullptr, 0, static_cast<cudaStream_t>(stream),
+                    "qmv_moe_gather");
+}
+
+int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
+                         const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
+                         size_t sums_bytes, void* stream) {
+  if (sums == nullptr) return fail(QMV_EINVAL, "qmv_debug_block_sums: sums must be non-NULL");
+  return run_matvec(desc, w, x, per_slot_x, ids, ntok, top_k, y, sums, sums_bytes,
+                    static_cast<cudaStream_t>(stream), "qmv_debug_block_sums");
+}
+
+int qmv_swiglu_bf16(const void* g, const void* u, void* h, int64_t n, void* stream) {
+  if (!g || !u || !h) return fail(QMV_EINVAL, "qmv_swiglu_bf16: NULL pointer");
+  if (n < 0) return fail(QMV_EINVAL, "qmv_swiglu_bf16: n=%lld < 0", (long long)n);
+  if (!aligned16(g) || !aligned16(u) || !aligned16(h))
+    return fail(QMV_EALIGN, "qmv_swiglu_bf16: pointers must be 16-byte aligned");
+  if (n == 0) return ok();
+  cudaError_t e = launch_swiglu_bf16(g, u, h, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmv_swiglu_bf16");
+  return ok();
+}
+
+int qmv_debug_dequant(const qmv_wdesc* desc, const void* w, int32_t expert, float* out, size_t out_bytes,
+                      void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (!w || !out) return fail(QMV_EINVAL, "qmv_debug_dequant: NULL pointer");
+  if (expert < 0 || expert >= desc->n_experts) return fail(QMV_EINVAL, "qmv_debug_dequant: expert %d out of range", expert);
+  if (!aligned16(w) || !aligned16(out)) return fail(QMV_EALIGN, "qmv_debug_dequant: pointers must be 16-byte aligned");
+  const size_t need = (size_t)desc->N * desc->K * sizeof(float);
+  if (out_bytes < need) return fail(QMV_ESIZE, "qmv_debug_dequant: output %zu bytes < %zu", out_bytes, need);
+  const Geometry g = make_geometry(desc->fmt, desc->N, desc->K);
+  uint32_t lut[4];
+  lut_words(desc, lut);
+  cudaError_t e = launch_dequant(desc->fmt, desc->N, desc->K, static_cast<const uint8_t*>(w) + (size_t)expert * g.expert,
+                                 lut, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmv_debug_dequant");
+  return ok();
+}
+
+int qmv_device_status(uint32_t* flags, int32_t clear) {
+  if (!flags) return fail(QMV_EINVAL, "qmv_device_status: NULL pointer");
+  uint32_t v = 0;
+  const uint32_t parts[4] = {status_mxfp4(clear), status_cb2(clear), status_cb3(clear), status_cb4(clear)};
+  for (uint32_t p : parts) {
+    if (p == 0xffffffffu) return cuda_fail(cudaGetLastError(), "qmv_device_status");
+    v |= p;
+  }
+  *flags = v;
+  return ok();
+}
+
+const char* qmv_last_error(void) { return g_last_error.c_str(); }
+
+const char* qmv_version(void) { return "qmv 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// qmv_internal.h -- host-side interface between the C ABI and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qmv_layout.h"
+
+namespace qmv {
+
+// Everything a matvec launch needs; filled and validated by the C ABI layer.
+struct MatvecArgs {
+  int fmt = 0;
+  int N = 0, K = 0, n_experts = 1;
+  const void* w = nullptr;        // GPU weight layout, expert 0
+  uint64_t expert_stride = 0;     // bytes between experts
+  const void* x = nullptr;        // bf16 vectors (MXFP4) or q8_1 vectors
+  int nvec = 0;                   // activation vectors in x
+  int per_slot = 0;
+  const int32_t* ids = nullptr;   // null: dense
+  int ntok = 1, top_k = 1;
+  void* y = nullptr;
+  int32_t* dbg = nullptr;         // integer block sums (CB formats) or null
+  uint32_t lut[4] = {0, 0, 0, 0}; // 16 int8 codebook bytes
+  cudaStream_t stream = nullptr;
+};
+
+// Dynamic shared memory a launch of `a` needs (0 if it exceeds the device limit).
+size_t matvec_smem_bytes(const MatvecArgs& a);
+
+cudaError_t launch_matvec_mxfp4(const MatvecArgs& a);
+cudaError_t launch_matvec_cb2(const MatvecArgs& a);
+cudaError_t launch_matvec_cb3(const MatvecArgs& a);
+cudaError_t launch_matvec_cb4(const MatvecArgs& a);
+
+cudaError_t launch_quantize_q8(const float* x, int nvec, int K, void* xq, cudaStream_t s);
+cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n, cudaStream_t s);
+cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t lut[4], float* out,
+                           cudaStream_t s);
+
+uint32_t status_mxfp4(int clear);
+uint32_t status_cb2(int clear);
+uint32_t status_cb3(int clear);
+uint32_t status_cb4(int clear);
+
+// Per-device cached properties.
+int device_sm_count();
+size_t device_max_smem_optin();
+
+}  // namespace qmv

@@ -1,0 +1,655 @@
+// qmv_matvec.cuh -- the decode matvec kernel (dense and expert-gathered), one
+// template for all weight formats.
+//
+// Work decomposition. A "work item" is one row tile (kRows rows) of one
+// matrix applied to up to NV activation vectors (the "entry": an expert and
+// the (token, slot) pairs routed to it). Items are dealt round-robin to every
+// warp of the grid. A warp streams its items' tiles -- one tile per K chunk --
+// through a private ring of kStages shared-memory stages filled by bulk
+// asynchronous copies (one elected lane issues them, an mbarrier per stage
+// tracks completion). Lane l of the warp owns columns [32 l, 32 l + 32) of
+// every chunk for all kRows rows, so the activations it needs are loaded into
+// registers once per chunk and reused for kRows rows. After the last chunk a
+// warp reduce-scatter (shuffles) leaves each (row, vector) sum in one lane,
+// which applies nothing further and stores it.
+//
+// Per format (lane-block encodings are defined in qmv_layout.h):
+//   MXFP4: E2M1 nibbles -> f16x2 with cvt.rn.f16x2.e2m1x2, fp32 FMA against
+//          the bf16 activations, fp32 group sum times 2^(e-127) per 32
+//          weights ("perf(rocm): add an mxfp4 arm to the warp-shared
+//          gather_qmv kernel ...", "Proposed Solution" item 1).
+//   CB2/CB3/CB4: codes -> int8 through byte permutes (prmt) over the codebook
+//          held in registers, dp4a against q8_1 activations, integer sums per
+//          16-weight half-block (CB2, CB3) or 32-weight block (CB4), then
+//          d_b * 2^(e-127) * isum in fp32 ("perf(ggml/hip): optimize ROCMFPX
+//          fp3/fp2 MMVQ on RDNA ...", "Changes" items 1, 2, 4 and the review
+//          reply's dot structure).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "qmv_device.cuh"
+#include "qmv_internal.h"
+#include "qmv_layout.h"
+
+namespace qmv {
+
+constexpr int kWarps = 4;        // warps per CTA
+constexpr int kStages = 2;       // shared-memory stages per warp
+constexpr int kMaxEntries = 32;  // ntok * top_k <= 4 * 8
+constexpr int kMaxDevices = 64;
+
+struct Entry {
+  int expert;
+  int nv;
+  int vec[4];   // activation vector index per routed pair
+  int slot[4];  // output slot (t for dense, t * top_k + j for gather)
+};
+
+struct KParams {
+  const uint8_t* w;
+  uint64_t expert_stride;
+  const uint8_t* x;
+  uint32_t x_vec_bytes;   // bytes per activation vector (global and shared)
+  int nvec;
+  const int32_t* ids;
+  int ntok, top_k, per_slot, n_experts;
+  int N, K, row_tiles, chunks, last_lanes;
+  uint32_t full_tile, last_tile;
+  uint64_t rowtile;
+  void* y;
+  int32_t* dbg;
+  uint32_t lut[4];
+};
+
+// Largest number of activation vectors one work item applies a tile to.
+template <int FMT>
+struct MaxVectors {
+  static constexpr int value = (FMT == MXFP4) ? 2 : 4;
+};
+
+__host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
+  return (v + a - 1) / a * a;
+}
+
+struct SmemLayout {
+  uint32_t x_off, ring_off, bar_off, ent_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(uint32_t nvec, uint32_t x_vec_bytes,
+                                                  uint32_t full_tile) {
+  SmemLayout L;
+  L.x_off = 0;
+  L.ring_off = round_up_u32(nvec * x_vec_bytes, 128);
+  L.bar_off = L.ring_off + kWarps * kStages * full_tile;
+  L.ent_off = round_up_u32(L.bar_off + (kWarps * kStages + 1) * 8, 16);
+  L.total = L.ent_off + kMaxEntries * (uint32_t)sizeof(Entry);
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Work list
+// ---------------------------------------------------------------------------
+
+template <int NV>
+__device__ int build_entries(const KParams& p, Entry* ent) {
+  int n = 0;
+  if (p.ids == nullptr) {
+    for (int t = 0; t < p.ntok; t += NV) {
+      Entry& e = ent[n++];
+      e.expert = 0;
+      e.nv = min(NV, p.ntok - t);
+      for (int i = 0; i < 4; ++i) {
+        const int tt = t + min(i, e.nv - 1);
+        e.vec[i] = tt;
+        e.slot[i] = tt;
+      }
+    }
+    return n;
+  }
+  for (int t = 0; t < p.ntok; ++t) {
+    for (int j = 0; j < p.top_k; ++j) {
+      const int s = t * p.top_k + j;
+      const int ex = p.ids[s];
+      if (ex < 0 || ex >= p.n_experts) continue;
+      const int v = p.per_slot ? s : t;
+      int f = -1;
+      for (int i = 0; i < n; ++i) {
+        if (ent[i].expert == ex && ent[i].nv < NV) {
+          f = i;
+          break;
+        }
+      }
+      if (f < 0) {
+        f = n++;
+        ent[f].expert = ex;
+        ent[f].nv = 0;
+        for (int i = 0; i < 4; ++i) {
+          ent[f].vec[i] = v;
+          ent[f].slot[i] = s;
+        }
+      }
+      Entry& e = ent[f];
+      e.vec[e.nv] = v;
+      e.slot[e.nv] = s;
+      e.nv += 1;
+    }
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// Tile loads
+// ---------------------------------------------------------------------------
+
+struct WarpPipe {
+  uint32_t ring;      // shared address of this warp's stage 0
+  uint32_t bars;      // shared address of this warp's mbarrier 0
+  const uint8_t* ring_ptr;
+  int gw, nw, n_items;
+  uint64_t policy;
+};
+
+// Issues the copy of the tile at position q of this warp's sequence
+// (item = gw + (q / chunks) * nw, chunk = q % chunks) into stage q % kStages.
+__device__ __forceinline__ void issue_tile(const KParams& p, const Entry* ent, const WarpPipe& wp,
+                                           int q) {
+  const int item = wp.gw + (q / p.chunks) * wp.nw;
+  if (item >= wp.n_items) return;
+  const int c = q % p.chunks;
+  const int rt = item % p.row_tiles;
+  const Entry& e = ent[item / p.row_tiles];
+  const uint8_t* src = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)rt * p.rowtile +
+                       (uint64_t)c * p.full_tile;
+  const uint32_t bytes = (c == p.chunks - 1) ? p.last_tile : p.full_tile;
+  const int s = q % kStages;
+  const uint32_t bar = wp.bars + 8u * s;
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_copy_g2s_hint(wp.ring + (uint32_t)s * p.full_tile, src, bytes, bar, wp.policy);
+}
+
+// ---------------------------------------------------------------------------
+// Decoders: 32 codes of one lane and one row -> 8 words of int8x4 (CB) in
+// column order: word i holds columns 4i..4i+3.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void decode_cb2(uint32_t w0, uint32_t w1, uint32_t l0, uint32_t (&v)[8]) {
+  uint32_t s;
+  s = w0 & 0x33333333u;
+  v[0] = prmt(l0, l0, s);
+  v[1] = prmt(l0, l0, s >> 16);
+  s = (w0 >> 2) & 0x33333333u;
+  v[2] = prmt(l0, l0, s);
+  v[3] = prmt(l0, l0, s >> 16);
+  s = w1 & 0x33333333u;
+  v[4] = prmt(l0, l0, s);
+  v[5] = prmt(l0, l0, s >> 16);
+  s = (w1 >> 2) & 0x33333333u;
+  v[6] = prmt(l0, l0, s);
+  v[7] = prmt(l0, l0, s >> 16);
+}
+
+__device__ __forceinline__ void decode_cb3(uint32_t a, uint32_t b, uint32_t c, uint32_t l0,
+                                           uint32_t l1, uint32_t (&v)[8]) {
+  uint32_t s;
+  s = (a & 0x33333333u) | ((c << 2) & 0x44444444u);
+  v[0] = prmt(l0, l1, s);
+  v[1] = prmt(l0, l1, s >> 16);
+  s = ((a >> 2) & 0x33333333u) | ((c << 1) & 0x44444444u);
+  v[2] = prmt(l0, l1, s);
+  v[3] = prmt(l0, l1, s >> 16);
+  s = (b & 0x33333333u) | (c & 0x44444444u);
+  v[4] = prmt(l0, l1, s);
+  v[5] = prmt(l0, l1, s >> 16);
+  s = ((b >> 2) & 0x33333333u) | ((c >> 1) & 0x44444444u);
+  v[6] = prmt(l0, l1, s);
+  v[7] = prmt(l0, l1, s >> 16);
+}
+
+// 16-entry codebook: two 8-entry lookups (codes 0..7 and 8..15) and a byte
+// select by bit 3 of each code.
+__device__ __forceinline__ uint32_t cb4_quad(uint32_t sel_lo, uint32_t hi_bits, const uint32_t (&t)[4]) {
+  const uint32_t a = prmt(t[0], t[1], sel_lo);
+  const uint32_t b = prmt(t[2], t[3], sel_lo);
+  const uint32_t pick = (hi_bits & 0x4444u) | 0x3210u;
+  return prmt(a, b, pick);
+}
+
+__device__ __forceinline__ void decode_cb4(const uint32_t (&w)[4], const uint32_t (&t)[4], uint32_t (&v)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = w[i] & 0x77777777u;
+    v[2 * i] = cb4_quad(lo, w[i] >> 1, t);
+    v[2 * i + 1] = cb4_quad(lo >> 16, w[i] >> 17, t);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per-chunk compute
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+template <int NVV, int NVP>
+__device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, int c, int L,
+                                            const uint8_t* st, const uint8_t* xs, float* acc) {
+  const int lane = threadIdx.x & 31;
+  float xf[NVV][32];
+#pragma unroll
+  for (int v = 0; v < NVV; ++v) {
+    const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)e.vec[v] * p.x_vec_bytes +
+                                                     (size_t)(c * kChunkK + lane * kLaneK) * 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = xp[q];
+      xf[v][8 * q + 0] = bf16_lo(u.x);
+      xf[v][8 * q + 1] = bf16_hi(u.x);
+      xf[v][8 * q + 2] = bf16_lo(u.y);
+      xf[v][8 * q + 3] = bf16_hi(u.y);
+      xf[v][8 * q + 4] = bf16_lo(u.z);
+      xf[v][8 * q + 5] = bf16_hi(u.z);
+      xf[v][8 * q + 6] = bf16_lo(u.w);
+      xf[v][8 * q + 7] = bf16_hi(u.w);
+    }
+  }
+  const uint4 sc = *reinterpret_cast<const uint4*>(st + tile_code_bytes(MXFP4, L) + lane * kRows);
+  const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const uint4 cw = *reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 16);
+    const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+    float dot[NVV];
+#pragma unroll
+    for (int v = 0; v < NVV; ++v) dot[v] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t h[4];
+      e2m1x8_to_f16x2(w4[q], h);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
+        const int k = 8 * q + 2 * b;
+#pragma unroll
+        for (int v = 0; v < NVV; ++v) {
+          dot[v] = fmaf(f.x, xf[v][k], dot[v]);
+          dot[v] = fmaf(f.y, xf[v][k + 1], dot[v]);
+        }
+      }
+    }
+    const float s = e8m0_to_f32((scw[r >> 2] >> (8 * (r & 3))) & 0xffu);
+#pragma unroll
+    for (int v = 0; v < NVV; ++v) acc[r * NVP + v] = fmaf(s, dot[v], acc[r * NVP + v]);
+  }
+}
+
+template <int FMT, int NVV, int NVP, bool DBG>
+__device__ __forceinline__ void chunk_cb(const KParams& p, const Entry& e, int rt, int c, int L,
+                                         const uint8_t* st, const uint8_t* xs, float* acc) {
+  const int lane = threadIdx.x & 31;
+  constexpr int SPL = lane_scale_bytes(FMT);  // 2 (half-blocks) or 1
+  uint32_t qx[NVV][8];
+  float dv[NVV];
+#pragma unroll
+  for (int v = 0; v < NVV; ++v) {
+    const uint8_t* xv = xs + (size_t)e.vec[v] * p.x_vec_bytes;
+    const uint4* qp = reinterpret_cast<const uint4*>(xv + c * kChunkK + lane * kLaneK);
+    const uint4 a = qp[0], b = qp[1];
+    qx[v][0] = a.x; qx[v][1] = a.y; qx[v][2] = a.z; qx[v][3] = a.w;
+    qx[v][4] = b.x; qx[v][5] = b.y; qx[v][6] = b.z; qx[v][7] = b.w;
+    dv[v] = __half2float(reinterpret_cast<const __half*>(xv + p.K)[c * 32 + lane]);
+  }
+  const uint8_t* scl = st + tile_code_bytes(FMT, L) + lane * kRows * SPL;
+  uint32_t sw[kRows * SPL / 4];
+#pragma unroll
+  for (int i = 0; i < kRows * SPL / 16; ++i) {
+    const uint4 u = reinterpret_cast<const uint4*>(scl)[i];
+    sw[4 * i] = u.x; sw[4 * i + 1] = u.y; sw[4 * i + 2] = u.z; sw[4 * i + 3] = u.w;
+  }
+  uint32_t t[4] = {p.lut[0], p.lut[1], p.lut[2], p.lut[3]};
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    uint32_t wv[8];
+    if constexpr (FMT == CB2) {
+      const uint2 u = *reinterpret_cast<const uint2*>(st + (size_t)(r * L + lane) * 8);
+      decode_cb2(u.x, u.y, t[0], wv);
+    } else if constexpr (FMT == CB3) {
+      const uint2 u = *reinterpret_cast<const uint2*>(st + (size_t)(r * L + lane) * 8);
+      const uint32_t hc = *reinterpret_cast<const uint32_t*>(st + (size_t)kRows * L * 8 +
+                                                             (size_t)(r * L + lane) * 4);
+      decode_cb3(u.x, u.y, hc, t[0], t[1], wv);
+    } else {
+      const uint4 u = *reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 16);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      decode_cb4(w4, t, wv);
+    }
+    const int row = r + rt * kRows;
+    if constexpr (SPL == 2) {
+      const uint32_t sb = sw[r >> 1] >> (16 * (r & 1));
+      const float s0 = e8m0_to_f32(sb & 0xffu);
+      const float s1 = e8m0_to_f32((sb >> 8) & 0xffu);
+#pragma unroll
+      for (int v = 0; v < NVV; ++v) {
+        int i0 = 0, i1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          i0 = dp4a(wv[i], qx[v][i], i0);
+          i1 = dp4a(wv[4 + i], qx[v][4 + i], i1);
+        }
+        acc[r * NVP + v] = fmaf(dv[v], fmaf(s0, (float)i0, s1 * (float)i1), acc[r * NVP + v]);
+        if constexpr (DBG) {
+          if (row < p.N) {
+            int32_t* o = p.dbg + ((size_t)e.slot[v] * p.N + row) * (p.K / 16) + (c * kChunkK + lane * kLaneK) / 16;
+            o[0] = i0;
+            o[1] = i1;
+          }
+        }
+      }
+    } else {
+      const float s = e8m0_to_f32((sw[r >> 2] >> (8 * (r & 3))) & 0xffu);
+#pragma unroll
+      for (int v = 0; v < NVV; ++v) {
+        int i0 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) i0 = dp4a(wv[i], qx[v][i], i0);
+        acc[r * NVP + v] = fmaf(dv[v], s * (float)i0, acc[r * NVP + v]);
+        if constexpr (DBG) {
+          if (row < p.N) {
+            p.dbg[((size_t)e.slot[v] * p.N + row) * (p.K / 32) + (c * kChunkK + lane * kLaneK) / 32] = i0;
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Warp reduce-scatter: after rs_step<M, 16>, lane l holds value index
+// l / (32 / M) when M <= 32, or 2 l + i (i = 0, 1) when M = 64, each summed
+// over all 32 lanes.
+// ---------------------------------------------------------------------------
+
+template <int M, int O>
+__device__ __forceinline__ void rs_step(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (M >= 2) {
+      constexpr int H = M / 2;
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float send = up ? v[i] : v[i + H];
+        const float keep = up ? v[i + H] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      rs_step<H, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      rs_step<1, O / 2>(v, lane);
+    }
+  }
+}
+
+template <int FMT, int NVV, int NVP>
+__device__ __forceinline__ void reduce_store(const KParams& p, const Entry& e, int rt, float* acc) {
+  const int lane = threadIdx.x & 31;
+  constexpr int M = kRows * NVP;
+  rs_step<M, 16>(acc, lane);
+  auto store = [&](int idx, float val) {
+    const int r = idx / NVP, v = idx % NVP;
+    const int row = rt * kRows + r;
+    if (v < NVV && row < p.N) {
+      const size_t o = (size_t)e.slot[v] * p.N + row;
+      if constexpr (FMT == MXFP4) {
+        reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(val);
+      } else {
+        reinterpret_cast<float*>(p.y)[o] = val;
+      }
+    }
+  };
+  if constexpr (M <= 32) {
+    constexpr int S = 32 / M;
+    if (lane % S == 0) store(lane / S, acc[0]);
+  } else {
+    store(2 * lane, acc[0]);
+    store(2 * lane + 1, acc[1]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One work item: all chunks of one row tile, applied to NVV vectors.
+// ---------------------------------------------------------------------------
+
+template <int FMT, int NVV, bool DBG>
+__device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, const Entry& e, int rt,
+                                         int& q, const WarpPipe& wp, const uint8_t* xs) {
+  constexpr int NVP = (NVV == 3) ? 4 : NVV;
+  const int lane = threadIdx.x & 31;
+  float acc[kRows * NVP];
+#pragma unroll
+  for (int i = 0; i < kRows * NVP; ++i) acc[i] = 0.f;
+  for (int c = 0; c < p.chunks; ++c, ++q) {
+    const int s = q % kStages;
+    const uint32_t parity = (uint32_t)(q / kStages) & 1u;
+    bool ok = mbar_wait_bounded(wp.bars + 8u * s, parity, kWaitLimitNs);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    const int L = (c == p.chunks - 1) ? p.last_lanes : 32;
+    const uint8_t* st = wp.ring_ptr + (size_t)s * p.full_tile;
+    if (lane < L) {
+      if constexpr (FMT == MXFP4) {
+        chunk_mxfp4<NVV, NVP>(p, e, c, L, st, xs, acc);
+      } else {
+        chunk_cb<FMT, NVV, NVP, DBG>(p, e, rt, c, L, st, xs, acc);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) issue_tile(p, ent, wp, q + kStages);
+  }
+  reduce_store<FMT, NVV, NVP>(p, e, rt, acc);
+  return true;
+}
+
+template <int FMT, int NV, bool DBG>
+__global__ void __launch_bounds__(kWarps * 32) matvec_kernel(const KParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const SmemLayout sl = smem_layout((uint32_t)p.nvec, p.x_vec_bytes, p.full_tile);
+  uint8_t* xs = smem + sl.x_off;
+  uint8_t* ring = smem + sl.ring_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bar_off);
+  Entry* ent = reinterpret_cast<Entry*>(smem + sl.ent_off);
+  __shared__ int s_nent;
+
+  // Inputs (activations, ids) may be produced by the preceding kernel.
+  pdl_wait();
+  const uint32_t xbar = smem_addr(&bars[kWarps * kStages]);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * kStages + 1; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    fence_mbar_init();
+    const uint32_t xbytes = (uint32_t)p.nvec * p.x_vec_bytes;
+    mbar_arrive_expect_tx(xbar, xbytes);
+    for (int v = 0; v < p.nvec; ++v) {
+      bulk_copy_g2s(smem_addr(xs + (size_t)v * p.x_vec_bytes), p.x + (size_t)v * p.x_vec_bytes,
+                    p.x_vec_bytes, xbar);
+    }
+    s_nent = build_entries<NV>(p, ent);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  WarpPipe wp;
+  wp.gw = blockIdx.x * kWarps + warp;
+  wp.nw = gridDim.x * kWarps;
+  wp.n_items = s_nent * p.row_tiles;
+  wp.ring_ptr = ring + (size_t)warp * kStages * p.full_tile;
+  wp.ring = smem_addr(wp.ring_ptr);
+  wp.bars = smem_addr(&bars[warp * kStages]);
+  wp.policy = l2_evict_first_policy();
+  if (lane == 0) {
+    for (int q = 0; q < kStages; ++q) issue_tile(p, ent, wp, q);
+  }
+
+  // Gather slots with an invalid id produce zero rows.
+  if (p.ids != nullptr) {
+    const int nslots = p.ntok * p.top_k;
+    for (int s = 0; s < nslots; ++s) {
+      const int ex = p.ids[s];
+      if (ex >= 0 && ex < p.n_experts) continue;
+      for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < p.N; row += gridDim.x * blockDim.x) {
+        if constexpr (FMT == MXFP4) {
+          reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)s * p.N + row] = __float2bfloat16_rn(0.f);
+        } else {
+          reinterpret_cast<float*>(p.y)[(size_t)s * p.N + row] = 0.f;
+        }
+      }
+    }
+  }
+
+  bool ok = mbar_wait_bounded(xbar, 0, kWaitLimitNs);
+  if (!__all_sync(0xffffffffu, ok)) {
+    if (lane == 0) set_status(kStatusWaitX);
+    if (!mbar_wait_bounded(xbar, 0, kDrainLimitNs) && lane == 0) set_status(kStatusDrain);
+    ok = false;
+  }
+
+  int q = 0;
+  if (ok) {
+    for (int item = wp.gw; item < wp.n_items; item += wp.nw) {
+      const Entry& e = ent[item / p.row_tiles];
+      const int rt = item % p.row_tiles;
+      switch (e.nv) {
+        case 1: ok = run_item<FMT, 1, DBG>(p, ent, e, rt, q, wp, xs); break;
+        case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG>(p, ent, e, rt, q, wp, xs); break;
+        case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG>(p, ent, e, rt, q, wp, xs); break;
+        case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG>(p, ent, e, rt, q, wp, xs); break;
+        default: break;
+      }
+      if (!ok) {
+        if (lane == 0) set_status(kStatusWaitTile);
+        break;
+      }
+    }
+  }
+  if (!ok) {
+    // Let every copy this warp issued land (bounded) before the CTA's shared
+    // memory can be released.
+    const int total = ((wp.n_items - wp.gw + wp.nw - 1) / wp.nw) * p.chunks;
+    for (int qq = q; qq < min(total, q + kStages); ++qq) {
+      const int s = qq % kStages;
+      if (!mbar_wait_bounded(wp.bars + 8u * s, (uint32_t)(qq / kStages) & 1u, kDrainLimitNs)) {
+        if (lane == 0) set_status(kStatusDrain);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launcher
+// ---------------------------------------------------------------------------
+
+template <int FMT>
+struct KernelSet {
+  template <int NV, bool DBG>
+  static void* fn() {
+    return reinterpret_cast<void*>(&matvec_kernel<FMT, NV, DBG>);
+  }
+};
+
+inline KParams make_params(const MatvecArgs& a) {
+  const Geometry g = make_geometry(a.fmt, a.N, a.K);
+  KParams p;
+  p.w = static_cast<const uint8_t*>(a.w);
+  p.expert_stride = a.expert_stride;
+  p.x = static_cast<const uint8_t*>(a.x);
+  p.x_vec_bytes = (a.fmt == MXFP4) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
+  p.nvec = a.nvec;
+  p.ids = a.ids;
+  p.ntok = a.ntok;
+  p.top_k = a.ids ? a.top_k : 1;
+  p.per_slot = a.per_slot;
+  p.n_experts = a.n_experts;
+  p.N = a.N;
+  p.K = a.K;
+  p.row_tiles = g.row_tiles;
+  p.chunks = g.chunks;
+  p.last_lanes = g.last_lanes;
+  p.full_tile = g.full_tile;
+  p.last_tile = g.last_tile;
+  p.rowtile = g.rowtile;
+  p.y = a.y;
+  p.dbg = a.dbg;
+  for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i];
+  return p;
+}
+
+template <int FMT>
+cudaError_t launch_matvec(const MatvecArgs& a) {
+  constexpr int NVMAX = MaxVectors<FMT>::value;
+  const KParams p = make_params(a);
+  const SmemLayout sl = smem_layout((uint32_t)p.nvec, p.x_vec_bytes, p.full_tile);
+  const int want_nv = a.ids ? (a.ntok < NVMAX ? a.ntok : NVMAX) : (a.ntok < NVMAX ? a.ntok : NVMAX);
+  void* fn = nullptr;
+  const bool dbg = a.dbg != nullptr;
+  switch (want_nv) {
+    case 1: fn = dbg ? KernelSet<FMT>::template fn<1, true>() : KernelSet<FMT>::template fn<1, false>(); break;
+    case 2: fn = dbg ? KernelSet<FMT>::template fn<2, true>() : KernelSet<FMT>::template fn<2, false>(); break;
+    case 3:
+      if constexpr (NVMAX >= 3) fn = dbg ? KernelSet<FMT>::template fn<3, true>() : KernelSet<FMT>::template fn<3, false>();
+      break;
+    default:
+      if constexpr (NVMAX >= 4) fn = dbg ? KernelSet<FMT>::template fn<4, true>() : KernelSet<FMT>::template fn<4, false>();
+      break;
+  }
+  if (fn == nullptr) return cudaErrorInvalidValue;
+
+  // Opt in to the shared memory this launch needs, once per kernel and size.
+  static std::mutex mu;
+  static size_t configured[kMaxDevices][5][2] = {};
+  int dev = 0;
+  cudaError_t derr = cudaGetDevice(&dev);
+  if (derr != cudaSuccess) return derr;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = configured[dev][want_nv][dbg ? 1 : 0];
+    if (have < sl.total) {
+      const size_t target = device_max_smem_optin();
+      cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)target);
+      if (err != cudaSuccess) return err;
+      have = target;
+    }
+  }
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWarps * 32, sl.total);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // Upper bound on work items: every routed pair its own entry.
+  const int entries_max = a.ids ? a.ntok * a.top_k : (a.ntok + want_nv - 1) / want_nv;
+  const long items = (long)entries_max * p.row_tiles;
+  long grid = (items + kWarps - 1) / kWarps;
+  const long cap = (long)device_sm_count() * per_sm;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = sl.total;
+  cfg.stream = a.stream;
+  // Programmatic dependent launch lets this grid start while the previous
+  // kernel in the stream drains; the kernel waits (griddepcontrol.wait) before
+  // it reads any input. Not used on the legacy NULL stream.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (a.stream != nullptr) ? 1 : 0;
+  void* args[] = {const_cast<KParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace qmv

@@ -1,0 +1,231 @@
+/*
+ * qmv.h -- C ABI of libqmv: block-quantized decode matrix-vector products on
+ * NVIDIA GB300 (sm_103a), dense and MoE expert-gathered.
+ *
+ * Operation. For a weight matrix W (N rows x K columns) stored block-quantized
+ * and 1..4 decode tokens, y = W . x per token. Weight formats:
+ *
+ *   QMV_MXFP4  E2M1 4-bit codes, one E8M0 scale per 32 weights along K,
+ *              times bf16 activations, fp32 accumulation, bf16 output.
+ *              Source: "perf(rocm): add an mxfp4 arm to the warp-shared
+ *              gather_qmv kernel for gpt-oss decode" (mlxcel #2178),
+ *              "Current Behavior" and "Proposed Solution" item 1.
+ *   QMV_CB2    2-bit codes into a 4-entry int8 codebook, E8M0 per 16 weights.
+ *   QMV_CB3    3-bit codes into an 8-entry int8 codebook, E8M0 per 16 weights.
+ *   QMV_CB4    4-bit codes into a 16-entry int8 codebook, E8M0 per 32 weights.
+ *              The codebook formats multiply q8_1 activations (int8 blocks of
+ *              32 with an fp16 scale d) and reduce with integer dot products:
+ *              y = sum_b d_b * sum_{h in b} 2^(e_h - 127) * sum_{i in h} lut[c_i] * q_i.
+ *              Source: "perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA
+ *              (perm-LUT + VDR=4 + fp2)" (lucebox-hub #21), "Changes" and
+ *              the review reply's "dot structure"; "DS4 H200: rocmfp2_mix MoE
+ *              matvec 3.31x + ROCmFP4 dense matvec 1.53x" (geo-lucebox #31),
+ *              "Headline" and "Caveats" (quantize_q8_1).
+ *
+ * E8M0 scale byte e means 2^(e-127); e = 255 means NaN.
+ *
+ * Conventions for every entry point:
+ *  - Return 0 (QMV_OK) on success or a negative QMV_E* code. The message of
+ *    the last failure on the calling thread is returned by qmv_last_error().
+ *  - "_dev" pointers are CUDA device pointers owned by the caller; "_host"
+ *    pointers are host memory owned by the caller. The library allocates no
+ *    device memory and keeps no per-call state.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). GPU entry
+ *    points only enqueue work: they never synchronize and never read device
+ *    memory on the host. Argument errors are reported before anything is
+ *    enqueued; launch errors come back as QMV_ECUDA.
+ *  - Device pointers must be 16-byte aligned (QMV_EALIGN otherwise).
+ *  - Invalid data on the device is not an error: an expert id outside
+ *    [0, n_experts) yields a zero output row block; E8M0 = 255 yields NaN.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMV_OK 0
+#define QMV_EINVAL (-1)  /* null pointer, bad format, ntok/top_k out of range */
+#define QMV_ESHAPE (-2)  /* K % 32 != 0, N or K out of range, too many activation vectors */
+#define QMV_EALIGN (-3)  /* a device pointer that is not 16-byte aligned */
+#define QMV_ESIZE (-4)   /* a caller buffer smaller than the required size */
+#define QMV_ECUDA (-5)   /* a CUDA runtime error (message in qmv_last_error) */
+
+typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3 } qmv_fmt;
+
+/* Limits checked by every entry point. */
+#define QMV_MAX_NTOK 4      /* decode tokens per call */
+#define QMV_MAX_TOPK 8      /* experts per token */
+#define QMV_MAX_N (1 << 20)
+#define QMV_MAX_K (1 << 16)
+
+/*
+ * Weight descriptor. `lut` holds the codebook value of code c in lut[c] for
+ * the CB formats (entries at or beyond 2^bits are ignored; unused for
+ * MXFP4). n_experts = 1 describes a dense matrix.
+ */
+typedef struct {
+  int32_t fmt;        /* qmv_fmt */
+  int32_t N;          /* output rows of each matrix, 1 <= N <= QMV_MAX_N */
+  int32_t K;          /* reduction length, multiple of 32, <= QMV_MAX_K */
+  int32_t n_experts;  /* >= 1 */
+  int8_t lut[16];
+} qmv_wdesc;
+
+/* Weights per E8M0 scale along K: 32 for MXFP4 and CB4, 16 for CB2 and CB3. */
+int32_t qmv_scale_group(int32_t fmt);
+
+/* Bits per weight code: 4, 2, 3, 4 for MXFP4, CB2, CB3, CB4. */
+int32_t qmv_code_bits(int32_t fmt);
+
+/*
+ * Canonical (storage-order) sizes of ONE expert matrix, in bytes:
+ *   codes:  N * K * bits / 8, row-major, each row packed as
+ *           MXFP4/CB4: element k in byte k/2, low nibble first (a
+ *             little-endian uint32 at byte k/2 holds elements k..k+7; mlxcel
+ *             #2178, "Proposed Solution" item 1);
+ *           CB2: code j of each byte at bits [2j, 2j+2);
+ *           CB3: 8 codes per 3 bytes, code j at bits [3j, 3j+3) of the
+ *             little-endian 24-bit word (a 16-weight half-block is one
+ *             48-bit window; lucebox-hub #21, "Changes" item 2).
+ *   scales: N * (K / group) E8M0 bytes, row-major.
+ * Return 0 for an invalid descriptor.
+ */
+size_t qmv_canonical_code_bytes(const qmv_wdesc* desc);
+size_t qmv_canonical_scale_bytes(const qmv_wdesc* desc);
+
+/*
+ * Size in bytes of the GPU weight layout of one expert (a multiple of 256)
+ * and of all n_experts (expert e starts at e * qmv_packed_expert_bytes()).
+ * Rows are padded to whole row tiles, so no kernel load goes past the
+ * buffer. Return 0 for an invalid descriptor.
+ */
+size_t qmv_packed_expert_bytes(const qmv_wdesc* desc);
+size_t qmv_packed_bytes(const qmv_wdesc* desc);
+
+/*
+ * Host packer (offline, not on the timed path). Converts canonical codes
+ * [n_experts][canonical code bytes] and E8M0 scales [n_experts][N][K/group]
+ * into the GPU weight layout in `out_host` (out_bytes >= qmv_packed_bytes).
+ * Padding bytes are zero. The layout is private to this library: upload it
+ * unchanged and pass it to qmv_dense / qmv_moe_gather.
+ * Errors: QMV_EINVAL (null pointer, bad descriptor), QMV_ESHAPE, QMV_ESIZE.
+ */
+int qmv_pack_weights(const qmv_wdesc* desc, const uint8_t* codes_host, const uint8_t* scales_host,
+                     void* out_host, size_t out_bytes);
+
+/*
+ * Inverse of qmv_pack_weights: GPU layout -> canonical codes and scales
+ * (same shapes as qmv_pack_weights' inputs). Used to check the packer.
+ */
+int qmv_unpack_weights(const qmv_wdesc* desc, const void* packed_host, size_t packed_bytes,
+                       uint8_t* codes_host, uint8_t* scales_host);
+
+/*
+ * q8_1 activation buffer: per vector, K int8 codes followed by K/32 fp16
+ * scales d, the vector padded to a multiple of 16 bytes. Vector v starts at
+ * v * qmv_act_q8_vec_bytes(K). qmv_act_q8_bytes(nvec, K) is the total.
+ */
+size_t qmv_act_q8_vec_bytes(int32_t K);
+size_t qmv_act_q8_bytes(int32_t nvec, int32_t K);
+
+/*
+ * Quantize fp32 activations x_dev [nvec][K] to q8_1 (xq_dev, layout above).
+ * Per block of 32, in fp32: amax = max|x|, d = amax / 127, q = x * (1/d)
+ * rounded half away from zero and clamped to [-127, 127] (q = 0 when d = 0);
+ * d is stored as fp16 (round to nearest even). One launch quantizes every
+ * vector (geo-lucebox #31, "Caveats": quantize_q8_1).
+ * Errors: QMV_EINVAL, QMV_ESHAPE (K % 32), QMV_EALIGN, QMV_ESIZE, QMV_ECUDA.
+ */
+int qmv_quantize_act_q8(const float* x_dev, int32_t nvec, int32_t K, void* xq_dev, size_t xq_bytes,
+                        void* stream);
+
+/*
+ * Host helper: split a q8_1 buffer (host copy) into q [nvec][K] int8 and
+ * d [nvec][K/32] fp16 bit patterns.
+ */
+int qmv_act_q8_unpack(const void* xq_host, int32_t nvec, int32_t K, int8_t* q_host, uint16_t* d_host);
+
+/*
+ * Dense decode matvec: y[t] = W . x[t] for t < ntok (1..4).
+ *   w_dev: GPU layout of one matrix (desc->n_experts must be 1).
+ *   x_dev: MXFP4: bf16 [ntok][K]; CB formats: q8_1 buffer of ntok vectors.
+ *   y_dev: MXFP4: bf16 [ntok][N]; CB formats: fp32 [ntok][N].
+ * The kernel streams every packed weight byte once per call and applies it
+ * to all ntok tokens.
+ * Errors: QMV_EINVAL, QMV_ESHAPE, QMV_EALIGN, QMV_ECUDA.
+ */
+int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t ntok, void* y_dev,
+              void* stream);
+
+/*
+ * MoE expert-gathered decode matvec (the unsorted decode gather):
+ *   y[t][j] = W[ids[t][j]] . x(t, j)   for t < ntok, j < top_k,
+ * with x(t, j) = x[t] when per_slot_x == 0 (gate/up projections share the
+ * token's activation) and x[t * top_k + j] when per_slot_x != 0 (down
+ * projection: one activation per slot).
+ *   w_dev:   n_experts matrices in GPU layout, expert e at e * qmv_packed_expert_bytes().
+ *   ids_dev: int32 [ntok][top_k] expert ids, read on the device. An id outside
+ *            [0, n_experts) writes a zero row block (mlxcel #2178,
+ *            "Implementation Notes", edge cases). A matrix used by several
+ *            (token, slot) pairs is streamed once per call for up to 4 of them.
+ *   x_dev:   MXFP4: bf16 vectors of K; CB formats: q8_1 buffer.
+ *   y_dev:   MXFP4: bf16 [ntok][top_k][N]; CB formats: fp32 [ntok][top_k][N].
+ * Errors: QMV_EINVAL (ntok not in 1..4, top_k not in 1..8), QMV_ESHAPE,
+ * QMV_EALIGN, QMV_ECUDA.
+ */
+int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,
+                   const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, void* stream);
+
+/*
+ * SwiGLU between the gate/up and down gathers of a gpt-oss-style MoE layer:
+ * h[i] = silu(g[i]) * u[i], silu(z) = z / (1 + exp(-z)), bf16 in and out,
+ * fp32 arithmetic, n elements ("perf(rocm): add an mxfp4 arm ...", "Problem /
+ * Background": 24 layers times gate, up and down).
+ * Errors: QMV_EINVAL, QMV_EALIGN, QMV_ECUDA.
+ */
+int qmv_swiglu_bf16(const void* g_dev, const void* u_dev, void* h_dev, int64_t n, void* stream);
+
+/*
+ * Test export: the same kernels as qmv_dense / qmv_moe_gather for the CB
+ * formats, additionally writing every integer block sum
+ *   sums[slot][n][h] = sum_{i in h} lut[c_{n,i}] * q_i      (int32)
+ * with h a 16-weight half-block (CB2, CB3) or 32-weight block (CB4), slot =
+ * t (dense) or t * top_k + j (gather), sums_bytes >= slots * N * (K/span) * 4.
+ * ids_dev = NULL selects the dense path (top_k and per_slot_x ignored).
+ * Slots with an invalid id are left untouched.
+ */
+int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w_dev, const void* x_dev,
+                         int32_t per_slot_x, const int32_t* ids_dev, int32_t ntok, int32_t top_k,
+                         void* y_dev, int32_t* sums_dev, size_t sums_bytes, void* stream);
+
+/*
+ * Test export: decode the GPU weight layout of one matrix with the kernels'
+ * device decode routines to fp32 w_dev [N][K] = value(code) * 2^(e-127).
+ * For the CB formats value(code) = lut[code].
+ */
+int qmv_debug_dequant(const qmv_wdesc* desc, const void* w_dev, int32_t expert, float* out_dev,
+                      size_t out_bytes, void* stream);
+
+/*
+ * Device-side status: bit flags set by kernels whose bounded waits gave up
+ * (no kernel here waits on another kernel, so a set flag indicates a lost
+ * asynchronous copy). Synchronizes the device. clear != 0 resets the flags.
+ */
+int qmv_device_status(uint32_t* flags_host, int32_t clear);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* qmv_last_error(void);
+
+/* Library version string. */
+const char* qmv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

@@ -41,6 +41,16 @@ def codes(g: np.random.Generator, shape, bits: int) -> np.ndarray:
     return g.integers(0, 1 << bits, size=shape, dtype=np.uint8)
 
 
+def canonical_uniform_codes(g: np.random.Generator, lead_shape, K: int, bits: int) -> np.ndarray:
+    """Canonical packed code bytes of uniform codes: [..., K * bits / 8] uniform bytes.
+
+    Every canonical packing used here (two nibbles per byte, four 2-bit codes
+    per byte, eight 3-bit codes per three bytes) maps uniform random bytes to
+    independent uniform codes, so no packing step is needed to draw them.
+    """
+    return g.integers(0, 256, size=tuple(lead_shape) + (K * bits // 8,), dtype=np.uint8)
+
+
 def e8m0(g: np.random.Generator, shape, lo: int = 120, hi: int = 130) -> np.ndarray:
     """Uniform E8M0 exponent bytes in [lo, hi] (inclusive)."""
     return g.integers(lo, hi + 1, size=shape, dtype=np.uint8)

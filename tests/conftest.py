@@ -4,10 +4,16 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-if ROOT not in sys.path:
-    sys.path.insert(0, ROOT)
+TESTS = os.path.dirname(os.path.abspath(__file__))
+for p in (ROOT, TESTS):
+    if p not in sys.path:
+        sys.path.insert(0, p)
 
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: full-size cases")
+    # Build the native library in-tree if it is missing (nvcc cross-compiles
+    # here and builds natively on the GPU machine).
+    from bit_quantized_moe_gb300 import build as qbuild
+    if not os.path.exists(qbuild.LIB):
+        qbuild.build()

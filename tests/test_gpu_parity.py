@@ -1,0 +1,363 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bar: bit-exact for the decoded weights, q8_1 codes and scales, and every
+integer block sum; max|gpu - oracle| <= 1e-3 * sum|w x| per output element for
+the floating-point outputs (plus one bf16 ulp of the result where the output
+is bf16). Shapes span several row tiles, ragged row tiles (N = 516, 17, 1) and
+ragged K chunks (K = 2880, 96, 32)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import qmv_inputs as qi
+
+pytestmark = pytest.mark.gpu
+
+qmv = pytest.importorskip("bit_quantized_moe_gb300")
+from qmv_testutil import (DEV, Matrices, assert_close, bf16_to_np, quantize_on_gpu,  # noqa: E402
+                          status_clean, to_dev)
+
+LUTS = {"cb2": qi.LUT_CB2, "cb3": qi.LUT_CB3, "cb4": qi.LUT_CB4}
+
+
+# ---------------------------------------------------------------------------
+# Decode of the packed layout and the activation quantizer (bit-exact)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "cb2", "cb3", "cb4"])
+@pytest.mark.parametrize("N,K", [(17, 96), (516, 2880), (16, 2048)])
+def test_dequant_bit_exact(fmt, N, K):
+    m = Matrices(fmt, N, K, 1, [0], seed=N + K, lut=LUTS.get(fmt), scale_lo=0, scale_hi=255)
+    out = torch.empty(N, K, dtype=torch.float32, device=DEV)
+    qmv.qmv_debug_dequant(m.desc, m.w, 0, out)
+    got = out.cpu().numpy()
+    if fmt == "mxfp4":
+        ref = oracle.mxfp4_dequant(m.codes[0], m.scales[0])
+    else:
+        ref = oracle.cb_dequant(m.codes[0], m.scales[0], m.lut, qi.FORMAT_GROUP[fmt])
+    with np.errstate(over="ignore"):
+        ref32 = ref.astype(np.float32)        # fp32 overflow of 6 * 2^127 matches the kernel's fp32 product
+    same = (got == ref32) | (np.isnan(got) & np.isnan(ref32))
+    assert same.all(), f"{(~same).sum()} decoded weights differ"
+    assert status_clean()
+
+
+def test_dequant_page_tables():
+    """The fp3/fp2 code tables printed on the ROCMFPX PR decode exactly through the device LUT path."""
+    tables = {"cb3": [0, 1, 2, 4, 0, -1, -2, -4], "cb2": [-1, 0, 1, 2]}
+    for fmt, lut in tables.items():
+        m = Matrices(fmt, 16, 64, 1, [], seed=1, lut=lut)
+        codes = np.tile(np.arange(1 << qi.FORMAT_BITS[fmt], dtype=np.uint8), (16, 64 // (1 << qi.FORMAT_BITS[fmt])))
+        m.set_expert(0, codes, np.full((16, 4), 127, dtype=np.uint8))
+        out = torch.empty(16, 64, dtype=torch.float32, device=DEV)
+        qmv.qmv_debug_dequant(m.desc, m.w, 0, out)
+        assert out.cpu().numpy().tolist() == [[float(lut[c]) for c in row] for row in codes]
+
+
+@pytest.mark.parametrize("nvec,K", [(1, 32), (4, 2048), (16, 2048), (3, 7168)])
+def test_q8_quantizer_bit_exact(nvec, K):
+    g = qi.rng(nvec * K)
+    x = qi.normal_f32(g, (nvec, K)) * np.float32(2.0) ** g.integers(-8, 8, size=(nvec, 1)).astype(np.float32)
+    x[0, :32] = 0.0                                   # all-zero block
+    if K >= 64:
+        x[0, 32:64] = 0.0
+        x[0, 32:38] = [127.0, 2.5, -2.5, 0.5, -0.5, 1.5]   # exact ties after scaling by 1
+        x[0, 64 % K:64 % K + 4] = [1e-40, -3e-39, 2e-38, 5e-39] if K > 64 else x[0, 0:4]
+    _, q, d = quantize_on_gpu(x)
+    q_ref, d_ref = oracle.q8_1_quantize(x)
+    assert np.array_equal(q, q_ref)
+    assert np.array_equal(d, d_ref)
+    if K >= 64:
+        assert q[0, 32:38].tolist() == [127, 3, -3, 1, -1, 2]
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 x bf16
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(1, 32), (17, 96), (516, 2880), (2880, 2880), (48, 4096)])
+@pytest.mark.parametrize("ntok", [1, 2, 3, 4])
+def test_mxfp4_dense(N, K, ntok):
+    m = Matrices("mxfp4", N, K, 1, [0], seed=7 * N + K)
+    x = qi.normal_bf16_bits(qi.rng(ntok + N), (ntok, K))
+    y = torch.empty(ntok, N, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_dense(m.desc, m.w, to_dev(x), ntok, y)
+    ref = oracle.mxfp4_matvec(m.codes[0], m.scales[0], x)
+    absum = oracle.mxfp4_abs_products(m.codes[0], m.scales[0], x)
+    assert_close(bf16_to_np(y), ref, absum, True, f"mxfp4 dense {N}x{K} ntok={ntok}")
+    assert status_clean()
+
+
+@pytest.mark.parametrize("N,K", [(516, 2880), (2880, 2880)])
+@pytest.mark.parametrize("ntok,top_k,per_slot", [(1, 4, False), (1, 4, True), (4, 4, False), (4, 4, True),
+                                                 (2, 8, True), (3, 1, False)])
+def test_mxfp4_gather(N, K, ntok, top_k, per_slot):
+    E = 32
+    g = qi.rng(N + 10 * ntok + top_k)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    m = Matrices("mxfp4", N, K, E, ids.reshape(-1), seed=N + top_k)
+    nvec = ntok * top_k if per_slot else ntok
+    x = qi.normal_bf16_bits(g, (nvec, K))
+    y = torch.empty(ntok, top_k, N, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), int(per_slot), to_dev(ids), ntok, top_k, y)
+    got = bf16_to_np(y)
+    for t in range(ntok):
+        for j in range(top_k):
+            e = int(ids[t, j])
+            v = t * top_k + j if per_slot else t
+            ref = oracle.mxfp4_matvec(m.codes[e], m.scales[e], x[v:v + 1])[0]
+            absum = oracle.mxfp4_abs_products(m.codes[e], m.scales[e], x[v:v + 1])[0]
+            assert_close(got[t, j], ref, absum, True, f"slot ({t},{j}) expert {e}")
+    assert status_clean()
+
+
+def test_mxfp4_gather_invalid_and_repeated_ids():
+    """Invalid ids give zero rows; an expert repeated across slots or tokens is still right."""
+    E, N, K = 8, 516, 2880
+    ids = np.array([[3, 3, -1, 8], [3, 5, 7, 100]], dtype=np.int32)
+    m = Matrices("mxfp4", N, K, E, ids.reshape(-1), seed=5)
+    x = qi.normal_bf16_bits(qi.rng(9), (8, K))
+    for per_slot in (0, 1):
+        y = torch.full((2, 4, N), 7.0, dtype=torch.bfloat16, device=DEV)
+        qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), per_slot, to_dev(ids), 2, 4, y)
+        ref = oracle.mxfp4_moe_gather(np.stack([m.codes.get(e, np.zeros((N, K), np.uint8)) for e in range(E)]),
+                                      np.stack([m.scales.get(e, np.zeros((N, K // 32), np.uint8)) for e in range(E)]),
+                                      x, ids, bool(per_slot))
+        got = bf16_to_np(y)
+        for t in range(2):
+            for j in range(4):
+                e = int(ids[t, j])
+                if 0 <= e < E:
+                    v = t * 4 + j if per_slot else t
+                    absum = oracle.mxfp4_abs_products(m.codes[e], m.scales[e], x[v:v + 1])[0]
+                    assert_close(got[t, j], ref[t, j], absum, True, f"({t},{j})")
+                else:
+                    assert np.all(got[t, j] == 0.0)
+    assert status_clean()
+
+
+def test_mxfp4_special_scales():
+    """E8M0 255 decodes to NaN; 0 to 2^-127 (kept, not flushed)."""
+    N, K = 16, 64
+    m = Matrices("mxfp4", N, K, 1, [], seed=3)
+    codes = np.full((N, K), 2, dtype=np.uint8)          # every weight 1.0
+    scales = np.full((N, 2), 127, dtype=np.uint8)
+    scales[3, :] = 255
+    scales[5, :] = 0
+    m.set_expert(0, codes, scales)
+    x = np.full((1, K), 0x3F80, dtype=np.uint16)         # all ones
+    y = torch.empty(1, N, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_dense(m.one, m.w, to_dev(x), 1, y)
+    got = bf16_to_np(y)[0]
+    assert np.isnan(got[3])
+    assert got[0] == 64.0
+    ref5 = 64.0 * 2.0 ** -127
+    assert abs(got[5] - ref5) <= ref5 * 2 ** -8
+
+
+# ---------------------------------------------------------------------------
+# Codebook formats x q8_1 (integer block sums bit-exact)
+# ---------------------------------------------------------------------------
+
+def _cb_check(fmt, m, x, ids, per_slot, ntok, top_k, what):
+    group = qi.FORMAT_GROUP[fmt]
+    xq, q, d = quantize_on_gpu(x)
+    q_ref, d_ref = oracle.q8_1_quantize(x)
+    assert np.array_equal(q, q_ref) and np.array_equal(d, d_ref)
+    N, K = m.N, m.K
+    slots = ntok * top_k if ids is not None else ntok
+    y = torch.empty(slots, N, dtype=torch.float32, device=DEV)
+    sums = torch.full((slots, N, K // group), -7, dtype=torch.int32, device=DEV)
+    y2 = torch.empty_like(y)
+    if ids is None:
+        qmv.qmv_dense(m.desc, m.w, xq, ntok, y2)
+        qmv.qmv_debug_block_sums(m.desc, m.w, xq, 0, None, ntok, 1, y, sums)
+    else:
+        qmv.qmv_moe_gather(m.desc, m.w, xq, int(per_slot), to_dev(ids), ntok, top_k, y2)
+        qmv.qmv_debug_block_sums(m.desc, m.w, xq, int(per_slot), to_dev(ids), ntok, top_k, y, sums)
+    got_y, got_y2, got_s = y.cpu().numpy(), y2.cpu().numpy(), sums.cpu().numpy()
+    assert np.array_equal(got_y, got_y2), "debug and production kernels disagree"
+    for s in range(slots):
+        if ids is None:
+            e, v = 0, s
+        else:
+            t, j = divmod(s, top_k)
+            e = int(ids[t, j])
+            v = s if per_slot else t
+            if not (0 <= e < m.E):
+                assert np.all(got_y2[s] == 0.0)
+                continue
+        ref_s = oracle.cb_block_sums(m.codes[e], m.lut, q_ref[v:v + 1], group)[0]
+        assert np.array_equal(got_s[s], ref_s), f"{what}: block sums differ for slot {s}"
+        ref = oracle.cb_matvec(m.codes[e], m.scales[e], m.lut, group, q_ref[v:v + 1], d_ref[v:v + 1])[0]
+        absum = oracle.cb_abs_products(m.codes[e], m.scales[e], m.lut, group, q_ref[v:v + 1], d_ref[v:v + 1])[0]
+        assert_close(got_y2[s], ref, absum, False, f"{what} slot {s}")
+
+
+@pytest.mark.parametrize("fmt", ["cb2", "cb3", "cb4"])
+@pytest.mark.parametrize("N,K", [(1, 32), (17, 96), (516, 2880), (64, 7168)])
+@pytest.mark.parametrize("ntok", [1, 4])
+def test_cb_dense(fmt, N, K, ntok):
+    m = Matrices(fmt, N, K, 1, [0], seed=N + K + ntok, lut=LUTS[fmt])
+    x = qi.normal_f32(qi.rng(N * ntok), (ntok, K))
+    _cb_check(fmt, m, x, None, False, ntok, 1, f"{fmt} dense {N}x{K}")
+    assert status_clean()
+
+
+@pytest.mark.parametrize("fmt", ["cb2", "cb3", "cb4"])
+@pytest.mark.parametrize("ntok,top_k,per_slot", [(1, 4, False), (4, 4, True), (2, 3, False)])
+def test_cb_gather(fmt, ntok, top_k, per_slot):
+    E, N, K = 64, 272, 2048
+    g = qi.rng(ntok * 10 + top_k)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    if ntok == 4:
+        ids[2, 1] = ids[0, 0]           # an expert shared by two tokens
+        ids[3, 0] = -5                  # an invalid id
+    m = Matrices(fmt, N, K, E, ids.reshape(-1), seed=E + ntok, lut=LUTS[fmt])
+    nvec = ntok * top_k if per_slot else ntok
+    x = qi.normal_f32(g, (nvec, K))
+    _cb_check(fmt, m, x, ids, per_slot, ntok, top_k, f"{fmt} gather")
+    assert status_clean()
+
+
+@pytest.mark.parametrize("fmt,lut", [("cb3", [0, 1, 2, 4, 0, -1, -2, -4]), ("cb2", [-1, 0, 1, 2]),
+                                     ("cb4", [-128, -100, -7, -5, -4, -3, -2, -1, 0, 2, 3, 4, 5, 7, 99, 127])])
+def test_cb_other_codebooks(fmt, lut):
+    """The page's fp3/fp2 tables and a full-range int8 16-entry table."""
+    m = Matrices(fmt, 48, 1024, 1, [0], seed=11, lut=lut)
+    x = qi.normal_f32(qi.rng(12), (2, 1024))
+    _cb_check(fmt, m, x, None, False, 2, 1, f"{fmt} lut {lut}")
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU and one MXFP4 MoE layer
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 8, 11520, 11527])
+def test_swiglu(n):
+    g = qi.rng(n)
+    gb = qi.normal_bf16_bits(g, (n,))
+    ub = qi.normal_bf16_bits(g, (n,))
+    h = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_swiglu_bf16(to_dev(gb), to_dev(ub), h, n)
+    ref = oracle.swiglu(oracle.bf16_bits_to_f64(gb), oracle.bf16_bits_to_f64(ub))
+    got = bf16_to_np(h)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+
+
+def test_mxfp4_moe_layer_chain():
+    """gate, up (gather, shared x) -> SwiGLU -> down (gather, per-slot h): a full layer at 2880."""
+    E, N, K, top_k = 32, 2880, 2880, 4
+    g = qi.rng(21)
+    ids = qi.topk_ids(g, 1, top_k, E)
+    gate = Matrices("mxfp4", N, K, E, ids[0], seed=22)
+    up = Matrices("mxfp4", N, K, E, ids[0], seed=23)
+    down = Matrices("mxfp4", N, K, E, ids[0], seed=24)
+    x = qi.normal_bf16_bits(g, (1, K))
+    ids_d, x_d = to_dev(ids), to_dev(x)
+    yg = torch.empty(1, top_k, N, dtype=torch.bfloat16, device=DEV)
+    yu = torch.empty_like(yg)
+    h = torch.empty_like(yg)
+    y = torch.empty_like(yg)
+    qmv.qmv_moe_gather(gate.desc, gate.w, x_d, 0, ids_d, 1, top_k, yg)
+    qmv.qmv_moe_gather(up.desc, up.w, x_d, 0, ids_d, 1, top_k, yu)
+    qmv.qmv_swiglu_bf16(yg, yu, h, top_k * N)
+    qmv.qmv_moe_gather(down.desc, down.w, h, 1, ids_d, 1, top_k, y)
+
+    def full(mm):
+        cs = np.zeros((E, N, K), np.uint8)
+        ss = np.zeros((E, N, K // 32), np.uint8)
+        for e in mm.codes:
+            cs[e], ss[e] = mm.codes[e], mm.scales[e]
+        return cs, ss
+    ref = oracle.mxfp4_moe_layer(full(gate), full(up), full(down), x, ids)
+    # gate/up: per-output tolerance
+    for name, got, refv, mm in (("gate", yg, ref["g_bits"], gate), ("up", yu, ref["u_bits"], up)):
+        for j in range(top_k):
+            e = int(ids[0, j])
+            r = oracle.mxfp4_matvec(mm.codes[e], mm.scales[e], x)[0]
+            absum = oracle.mxfp4_abs_products(mm.codes[e], mm.scales[e], x)[0]
+            assert_close(bf16_to_np(got)[0, j], r, absum, True, f"{name} slot {j}")
+    # h: bf16 of silu(g)*u; g/u may differ from the oracle's by a bf16 rounding step
+    hg = bf16_to_np(h)[0]
+    href = oracle.bf16_bits_to_f64(ref["h_bits"])[0]
+    assert np.mean(np.abs(hg - href) <= np.abs(href) * 2.0 ** -7 + 1e-6) > 0.999
+    # down: against the oracle chain (its own h)
+    for j in range(top_k):
+        e = int(ids[0, j])
+        absum = oracle.mxfp4_abs_products(down.codes[e], down.scales[e], ref["h_rows_bits"][j:j + 1])[0]
+        assert_close(bf16_to_np(y)[0, j], ref["y"][0, j], absum, True, f"down slot {j}")
+    assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Determinism and full-size configurations (sampled outputs)
+# ---------------------------------------------------------------------------
+
+def test_two_runs_bit_identical():
+    E, N, K = 32, 2880, 2880
+    ids = qi.topk_ids(qi.rng(31), 1, 4, E)
+    m = Matrices("mxfp4", N, K, E, ids[0], seed=32)
+    x = to_dev(qi.normal_bf16_bits(qi.rng(33), (4, K)))
+    outs = []
+    for _ in range(2):
+        y = torch.empty(1, 4, N, dtype=torch.bfloat16, device=DEV)
+        qmv.qmv_moe_gather(m.desc, m.w, x, 1, to_dev(ids), 1, 4, y)
+        outs.append(y.view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    c = Matrices("cb3", 7168, 2048, 1, [0], seed=34, lut=qi.LUT_CB3)
+    xq, _, _ = quantize_on_gpu(qi.normal_f32(qi.rng(35), (4, 2048)))
+    outs = []
+    for _ in range(2):
+        y = torch.empty(4, 7168, dtype=torch.float32, device=DEV)
+        qmv.qmv_dense(c.desc, c.w, xq, 4, y)
+        outs.append(y.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+def test_config2_full_size():
+    """256 experts x 2048 x 7168 CB2 gate and up, 4 ids, ntok = 1 (full shapes)."""
+    r = qi.CONFIG2
+    g = qi.rng(r.seed)
+    ids = qi.topk_ids(g, 1, r.top_k, r.n_experts)
+    x = qi.normal_f32(g, (1, r.K))
+    for proj in ("gate", "up"):
+        m = Matrices("cb2", r.N, r.K, r.n_experts, ids[0], seed=r.seed + (proj == "up"), lut=r.lut)
+        _cb_check("cb2", m, x, ids, False, 1, r.top_k, f"config2 {proj}")
+    assert status_clean()
+
+
+def test_config3_full_size():
+    """256 experts x 7168 x 2048 CB3 down, ntok = 4 tokens x top-4 independent ids, per-slot q8."""
+    r = qi.CONFIG3
+    g = qi.rng(r.seed)
+    ids = qi.topk_ids(g, r.ntok, r.top_k, r.n_experts)
+    m = Matrices("cb3", r.N, r.K, r.n_experts, ids.reshape(-1), seed=r.seed, lut=r.lut)
+    x = qi.normal_f32(g, (r.ntok * r.top_k, r.K))
+    _cb_check("cb3", m, x, ids, True, r.ntok, r.top_k, "config3")
+    assert status_clean()
+
+
+@pytest.mark.parametrize("N,K", qi.CONFIG4_SHAPES)
+def test_config4_full_size_sampled_rows(N, K):
+    """Dense CB4 7168x7168 and 2048x7168 at ntok 1..4: every output compared on sampled rows,
+    block sums on the same rows bit-exact."""
+    r = qi.config4(N, K, 4)
+    m = Matrices("cb4", N, K, 1, [0], seed=r.seed + N, lut=r.lut)
+    g = qi.rng(N)
+    rows = np.unique(np.concatenate([g.choice(N, 256, replace=False), [0, 15, 16, N - 1]]))
+    for ntok in qi.CONFIG4_NTOKS:
+        x = qi.normal_f32(g, (ntok, K))
+        xq, q, d = quantize_on_gpu(x)
+        y = torch.empty(ntok, N, dtype=torch.float32, device=DEV)
+        sums = torch.empty(ntok, N, K // 32, dtype=torch.int32, device=DEV)
+        qmv.qmv_debug_block_sums(m.desc, m.w, xq, 0, None, ntok, 1, y, sums)
+        got_s = sums.cpu().numpy()[:, rows]
+        got_y = y.cpu().numpy()[:, rows]
+        cs, ss = m.codes[0][rows], m.scales[0][rows]
+        assert np.array_equal(got_s, oracle.cb_block_sums(cs, m.lut, q, 32))
+        ref = oracle.cb_matvec(cs, ss, m.lut, 32, q, d)
+        absum = oracle.cb_abs_products(cs, ss, m.lut, 32, q, d)
+        assert_close(got_y, ref, absum, False, f"config4 {N}x{K} ntok={ntok}")
+    assert status_clean()

@@ -1,0 +1,195 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared
+symbol, packs and unpacks every format bit-exactly, and rejects bad arguments
+with the documented error codes before touching a GPU."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import qmv_inputs as qi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmv.h")
+
+qmv = pytest.importorskip("bit_quantized_moe_gb300", reason="libqmv not built")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(qmv.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    out = subprocess.run(["nm", "-D", "--defined-only", qmv.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\sT\s+(qmv_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(qmv.lib, name)
+
+
+def test_version_and_format_constants():
+    assert "sm_103a" in qmv.qmv_version()
+    assert [qmv.qmv_scale_group(f) for f in ("mxfp4", "cb2", "cb3", "cb4")] == [32, 16, 16, 32]
+    assert [qmv.qmv_code_bits(f) for f in ("mxfp4", "cb2", "cb3", "cb4")] == [4, 2, 3, 4]
+    assert qmv.qmv_scale_group(7) == 0
+
+
+SHAPES = [(1, 32), (5, 96), (16, 1024), (17, 1056), (40, 2048), (516, 2880)]
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "cb2", "cb3", "cb4"])
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_pack_roundtrip_bit_exact(fmt, N, K):
+    E = 2
+    g = qi.rng(100 + N + K)
+    codes = qi.codes(g, (E, N, K), qi.FORMAT_BITS[fmt])
+    scales = qi.e8m0(g, (E, N, K // qi.FORMAT_GROUP[fmt]), 0, 255)
+    canon = oracle.pack_codes(fmt, codes)
+    d = qmv.wdesc(fmt, N, K, E)
+    assert qmv.qmv_canonical_code_bytes(d) == canon[0].nbytes
+    assert qmv.qmv_canonical_scale_bytes(d) == scales[0].nbytes
+    packed = qmv.qmv_pack_weights(d, canon, scales)
+    assert packed.nbytes == qmv.qmv_packed_bytes(d) == E * qmv.qmv_packed_expert_bytes(d)
+    assert qmv.qmv_packed_expert_bytes(d) % 256 == 0
+    c2, s2 = qmv.qmv_unpack_weights(d, packed)
+    assert np.array_equal(c2.reshape(canon.shape), canon)
+    assert np.array_equal(s2.reshape(scales.shape), scales)
+    assert np.array_equal(oracle.unpack_codes(fmt, c2.reshape(canon.shape)), codes)
+
+
+def test_pack_changes_with_every_code():
+    """Every canonical code bit lands somewhere in the GPU layout (no dropped bits)."""
+    for fmt in ("mxfp4", "cb2", "cb3", "cb4"):
+        N, K = 3, 64
+        d = qmv.wdesc(fmt, N, K)
+        codes = np.zeros((1, N, K), dtype=np.uint8)
+        scales = np.zeros((1, N, K // qi.FORMAT_GROUP[fmt]), dtype=np.uint8)
+        base = qmv.qmv_pack_weights(d, oracle.pack_codes(fmt, codes), scales)
+        seen = set()
+        for n in range(N):
+            for k in range(K):
+                for b in range(qi.FORMAT_BITS[fmt]):
+                    c = codes.copy()
+                    c[0, n, k] = 1 << b
+                    p = qmv.qmv_pack_weights(d, oracle.pack_codes(fmt, c), scales)
+                    diff = np.nonzero(p != base)[0]
+                    assert len(diff) == 1
+                    bit = (int(diff[0]), int(p[diff[0]] ^ base[diff[0]]))
+                    assert bit not in seen
+                    seen.add(bit)
+
+
+def test_packed_bytes_match_algorithmic_bytes():
+    # 2880 x 2880 MXFP4: 1440 code bytes + 90 scale bytes per row, no padding
+    # besides rounding the expert stride to 256 bytes.
+    d = qmv.wdesc("mxfp4", 2880, 2880)
+    alg = 2880 * 1440 + 2880 * 90
+    assert alg == 4406400
+    assert alg <= qmv.qmv_packed_expert_bytes(d) < alg + 256
+    d = qmv.wdesc("cb3", 7168, 2048)
+    alg = 7168 * 2048 * 3 // 8 + 7168 * 128
+    assert alg == 6422528
+    assert alg <= qmv.qmv_packed_expert_bytes(d) < alg + 256
+    d = qmv.wdesc("cb2", 2048, 7168)
+    assert 2048 * 7168 // 4 + 2048 * 448 == 4587520
+    assert qmv.qmv_packed_expert_bytes(d) == 4587520
+    d = qmv.wdesc("cb4", 7168, 7168)
+    assert qmv.qmv_packed_expert_bytes(d) == 27295744
+
+
+def test_q8_sizes_and_unpack():
+    assert qmv.qmv_act_q8_vec_bytes(32) == 48           # 32 + 2 -> 48
+    assert qmv.qmv_act_q8_vec_bytes(7168) == 7168 + 448
+    assert qmv.qmv_act_q8_vec_bytes(33) == 0
+    assert qmv.qmv_act_q8_bytes(3, 2048) == 3 * (2048 + 128)
+    vb = qmv.qmv_act_q8_vec_bytes(64)
+    buf = np.arange(2 * vb, dtype=np.uint8)
+    q, d = qmv.qmv_act_q8_unpack(buf, 2, 64)
+    assert np.array_equal(q[1].view(np.uint8), buf[vb:vb + 64])
+    assert np.array_equal(d[1], buf[vb + 64:vb + 68].view(np.uint16))
+
+
+FAKE = 1 << 40          # 16-byte aligned address that is never dereferenced
+
+
+@pytest.mark.parametrize("case,code", [
+    ("K not multiple of 32", qmv.QMV_ESHAPE),
+    ("N zero", qmv.QMV_ESHAPE),
+    ("bad format", qmv.QMV_EINVAL),
+    ("ntok 5", qmv.QMV_EINVAL),
+    ("ntok 0", qmv.QMV_EINVAL),
+    ("misaligned x", qmv.QMV_EALIGN),
+    ("null y", qmv.QMV_EINVAL),
+    ("dense with experts", qmv.QMV_EINVAL),
+])
+def test_dense_argument_errors(case, code):
+    d = qmv.wdesc("cb4", 64, 64)
+    w, x, y, ntok = FAKE, FAKE, FAKE, 1
+    if case == "K not multiple of 32":
+        d.K = 48
+    elif case == "N zero":
+        d.N = 0
+    elif case == "bad format":
+        d.fmt = 9
+    elif case == "ntok 5":
+        ntok = 5
+    elif case == "ntok 0":
+        ntok = 0
+    elif case == "misaligned x":
+        x = FAKE + 4
+    elif case == "null y":
+        y = None
+    elif case == "dense with experts":
+        d.n_experts = 3
+    with pytest.raises(qmv.QmvError) as ei:
+        qmv.qmv_dense(d, w, x, ntok, y, stream=0)
+    assert ei.value.code == code
+    assert qmv.qmv_last_error()
+
+
+@pytest.mark.parametrize("top_k,ids,code", [(9, FAKE, qmv.QMV_EINVAL), (0, FAKE, qmv.QMV_EINVAL),
+                                            (4, None, qmv.QMV_EINVAL), (4, FAKE + 8, qmv.QMV_EALIGN)])
+def test_gather_argument_errors(top_k, ids, code):
+    d = qmv.wdesc("mxfp4", 64, 64, 8)
+    with pytest.raises(qmv.QmvError) as ei:
+        qmv.qmv_moe_gather(d, FAKE, FAKE, 0, ids, 1, top_k, FAKE, stream=0)
+    assert ei.value.code == code
+
+
+def test_debug_sums_size_error():
+    d = qmv.wdesc("cb2", 64, 64)
+    small = np.zeros(4, dtype=np.int32)
+    rc = qmv.lib.qmv_debug_block_sums(qmv.ctypes.byref(d), FAKE, FAKE, 0, None, 1, 1, FAKE, FAKE, small.nbytes, 0)
+    assert rc == qmv.QMV_ESIZE
+    d = qmv.wdesc("mxfp4", 64, 64)
+    rc = qmv.lib.qmv_debug_block_sums(qmv.ctypes.byref(d), FAKE, FAKE, 0, None, 1, 1, FAKE, FAKE, 1 << 20, 0)
+    assert rc == qmv.QMV_EINVAL
+
+
+def test_pack_size_errors():
+    d = qmv.wdesc("cb3", 16, 64)
+    codes = np.zeros(qmv.qmv_canonical_code_bytes(d), dtype=np.uint8)
+    scales = np.zeros(qmv.qmv_canonical_scale_bytes(d), dtype=np.uint8)
+    out = np.zeros(qmv.qmv_packed_bytes(d) - 16, dtype=np.uint8)
+    rc = qmv.lib.qmv_pack_weights(qmv.ctypes.byref(d), codes.ctypes.data, scales.ctypes.data, out.ctypes.data,
+                                  out.nbytes)
+    assert rc == qmv.QMV_ESIZE
+    rc = qmv.lib.qmv_pack_weights(qmv.ctypes.byref(d), None, scales.ctypes.data, out.ctypes.data, out.nbytes)
+    assert rc == qmv.QMV_EINVAL
+
+
+def test_quantize_and_swiglu_argument_errors():
+    assert qmv.lib.qmv_quantize_act_q8(FAKE, 1, 33, FAKE, 1 << 20, 0) == qmv.QMV_ESHAPE
+    assert qmv.lib.qmv_quantize_act_q8(FAKE, 1, 64, FAKE, 8, 0) == qmv.QMV_ESIZE
+    assert qmv.lib.qmv_quantize_act_q8(FAKE + 4, 1, 64, FAKE, 1 << 20, 0) == qmv.QMV_EALIGN
+    assert qmv.lib.qmv_swiglu_bf16(FAKE, FAKE, None, 16, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_swiglu_bf16(FAKE, FAKE + 2, FAKE, 16, 0) == qmv.QMV_EALIGN
