@@ -5,7 +5,7 @@ library. Device buffers are torch CUDA tensors (or raw device addresses);
 host buffers are numpy arrays. Each function has the name of the C entry
 point it calls and raises QmvError when that entry point returns an error.
 
-The library is built in-tree by ``python -m bit_quantized_moe_gb300.build``
+The library is built in-tree by ``python bit_quantized_moe_gb300/build.py``
 (or ``__graft_entry__.build()``). Importing this package without the built
 library raises ImportError: there is no fallback implementation.
 """
@@ -67,7 +67,7 @@ def wdesc(fmt, N: int, K: int, n_experts: int = 1, lut: Optional[Sequence[int]] 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libqmv is not built ({LIB_PATH} missing); run "
-                          "`python -m bit_quantized_moe_gb300.build`")
+                          "`python bit_quantized_moe_gb300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     D = ctypes.POINTER(WDesc)

@@ -1,6 +1,9 @@
 """Build libqmv.so in-tree for sm_103a with nvcc.
 
-    python -m bit_quantized_moe_gb300.build [--force] [--verbose-ptxas]
+    python bit_quantized_moe_gb300/build.py [--force] [--verbose-ptxas]
+
+(run as a script or loaded by file path: importing the package itself needs
+the built library).
 
 Every translation unit under csrc/ is compiled in parallel to an object file
 under _build/, then linked into _build/libqmv.so (CUDA runtime linked
