@@ -39,7 +39,7 @@ EXPORTS = (
     "qmv_packed_expert_bytes", "qmv_packed_bytes", "qmv_pack_weights", "qmv_unpack_weights",
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
     "qmv_dense", "qmv_moe_gather", "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
-    "qmv_device_status", "qmv_last_error", "qmv_version",
+    "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
 
 
@@ -90,6 +90,7 @@ def _load() -> ctypes.CDLL:
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
         "qmv_debug_dequant": (ctypes.c_int, [D, P, I32, P, SZ, P]),
         "qmv_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32]),
+        "qmv_debug_wait_probe": (ctypes.c_int, [ctypes.c_uint64, P]),
         "qmv_last_error": (ctypes.c_char_p, []),
         "qmv_version": (ctypes.c_char_p, []),
     }
@@ -234,6 +235,10 @@ def qmv_device_status(clear: bool = False) -> int:
     v = ctypes.c_uint32(0)
     _check(lib.qmv_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def qmv_debug_wait_probe(limit_ns: int, stream=None) -> None:
+    _check(lib.qmv_debug_wait_probe(int(limit_ns), _stream(stream)))
 
 
 def qmv_last_error() -> str:

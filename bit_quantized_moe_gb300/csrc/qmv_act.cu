@@ -165,6 +165,29 @@ cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Wait probe: one CTA waits on an mbarrier phase that nothing completes, with
+// the same bounded wait the matvec kernels use, and records the timeout in the
+// status word. Exercises the timeout path without a fault or a hang.
+// ---------------------------------------------------------------------------
+__global__ void wait_probe_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(smem_addr(&bar), 0, limit_ns);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) set_status(kStatusWaitProbe);
+}
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+QMV_DEFINE_STATUS_ACCESSOR(status_act)
+
 size_t matvec_smem_bytes(const MatvecArgs& a) {
   const Geometry g = make_geometry(a.fmt, a.N, a.K);
   const uint32_t xvb = (a.fmt == MXFP4) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);

@@ -15,6 +15,8 @@
 #include "qmv_layout.h"
 
 namespace qmv {
+thread_local const char* g_launch_stage = "";
+
 void pack_expert(const Geometry& g, const uint8_t* codes, const uint8_t* scales, uint8_t* out);
 void unpack_expert(const Geometry& g, const uint8_t* in, uint8_t* codes, uint8_t* scales);
 
@@ -144,8 +146,13 @@ int run_matvec(const qmv_wdesc* desc, const void* w, const void* x, int per_slot
   if (smem == 0 || smem > di->smem_optin)
     return fail(QMV_ESHAPE, "%s: %d activation vectors of K=%d do not fit in shared memory", name, a.nvec,
                 desc->K);
+  g_launch_stage = "";
   cudaError_t e = launch_for(a);
-  if (e != cudaSuccess) return cuda_fail(e, name);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(QMV_ECUDA, "%s: %s failed: %s (%s)", name, g_launch_stage, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  }
   return ok();
 }
 
@@ -312,12 +319,21 @@ int qmv_debug_dequant(const qmv_wdesc* desc, const void* w, int32_t expert, floa
 int qmv_device_status(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(QMV_EINVAL, "qmv_device_status: NULL pointer");
   uint32_t v = 0;
-  const uint32_t parts[4] = {status_mxfp4(clear), status_cb2(clear), status_cb3(clear), status_cb4(clear)};
+  const uint32_t parts[5] = {status_mxfp4(clear), status_cb2(clear), status_cb3(clear), status_cb4(clear),
+                             status_act(clear)};
   for (uint32_t p : parts) {
     if (p == 0xffffffffu) return cuda_fail(cudaGetLastError(), "qmv_device_status");
     v |= p;
   }
   *flags = v;
+  return ok();
+}
+
+int qmv_debug_wait_probe(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull)
+    return fail(QMV_EINVAL, "qmv_debug_wait_probe: limit %llu ns outside (0, 1 s]", (unsigned long long)limit_ns);
+  cudaError_t e = launch_wait_probe(limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qmv_debug_wait_probe");
   return ok();
 }
 

@@ -17,6 +17,7 @@ enum : uint32_t {
   kStatusWaitX = 1u,      // activation staging copy did not complete
   kStatusWaitTile = 2u,   // weight tile copy did not complete
   kStatusDrain = 4u,      // a copy was still in flight when giving up
+  kStatusWaitProbe = 8u,  // the wait probe's barrier (which nothing completes) timed out
 };
 
 // One status word per translation unit; read back by that unit's accessor.

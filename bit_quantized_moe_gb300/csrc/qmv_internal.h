@@ -25,6 +25,9 @@ struct MatvecArgs {
   cudaStream_t stream = nullptr;
 };
 
+// Name of the CUDA call a launcher made last on this thread (for error messages).
+extern thread_local const char* g_launch_stage;
+
 // Dynamic shared memory a launch of `a` needs (0 if it exceeds the device limit).
 size_t matvec_smem_bytes(const MatvecArgs& a);
 
@@ -38,6 +41,9 @@ cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n,
 cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t lut[4], float* out,
                            cudaStream_t s);
 
+cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t s);
+
+uint32_t status_act(int clear);
 uint32_t status_mxfp4(int clear);
 uint32_t status_cb2(int clear);
 uint32_t status_cb3(int clear);

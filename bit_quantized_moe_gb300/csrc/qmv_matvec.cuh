@@ -604,6 +604,7 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
       if constexpr (NVMAX >= 4) fn = dbg ? KernelSet<FMT>::template fn<4, true>() : KernelSet<FMT>::template fn<4, false>();
       break;
   }
+  g_launch_stage = "kernel selection";
   if (fn == nullptr) return cudaErrorInvalidValue;
 
   // Opt in to the shared memory this launch needs, once per kernel and size.
@@ -617,13 +618,24 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
     std::lock_guard<std::mutex> lock(mu);
     size_t& have = configured[dev][want_nv][dbg ? 1 : 0];
     if (have < sl.total) {
-      const size_t target = device_max_smem_optin();
-      cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)target);
+      // The opt-in limit covers static plus dynamic shared memory.
+      cudaFuncAttributes fa;
+      g_launch_stage = "cudaFuncGetAttributes";
+      cudaError_t err = cudaFuncGetAttributes(&fa, fn);
+      if (err != cudaSuccess) return err;
+      const size_t target = device_max_smem_optin() - fa.sharedSizeBytes;
+      if (target < sl.total) {
+        g_launch_stage = "shared memory limit";
+        return cudaErrorInvalidValue;
+      }
+      g_launch_stage = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
+      err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)target);
       if (err != cudaSuccess) return err;
       have = target;
     }
   }
   int per_sm = 0;
+  g_launch_stage = "cudaOccupancyMaxActiveBlocksPerMultiprocessor";
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWarps * 32, sl.total);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -649,6 +661,7 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   cfg.attrs = attr;
   cfg.numAttrs = (a.stream != nullptr) ? 1 : 0;
   void* args[] = {const_cast<KParams*>(&p)};
+  g_launch_stage = "cudaLaunchKernelExC";
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

@@ -212,11 +212,21 @@ int qmv_debug_dequant(const qmv_wdesc* desc, const void* w_dev, int32_t expert, 
                       size_t out_bytes, void* stream);
 
 /*
- * Device-side status: bit flags set by kernels whose bounded waits gave up
- * (no kernel here waits on another kernel, so a set flag indicates a lost
- * asynchronous copy). Synchronizes the device. clear != 0 resets the flags.
+ * Device-side status: bit flags set by kernels whose bounded waits gave up:
+ * 1 activation copy, 2 weight tile copy, 4 copy still in flight when giving
+ * up, 8 the wait probe. No kernel here waits on another kernel, so bits 1-4
+ * indicate a lost asynchronous copy. Synchronizes the device; clear != 0
+ * resets the flags.
  */
 int qmv_device_status(uint32_t* flags_host, int32_t clear);
+
+/*
+ * Test export: launches one CTA that waits, with the kernels' bounded wait and
+ * the given limit (0 < limit_ns <= 1 s), on an mbarrier phase that nothing
+ * completes. The wait gives up, the kernel sets status bit 8 and returns; the
+ * context stays usable. Checks the timeout path without a fault or a hang.
+ */
+int qmv_debug_wait_probe(uint64_t limit_ns, void* stream);
 
 /* Message of the last failure on the calling thread ("" if none). */
 const char* qmv_last_error(void);

@@ -361,3 +361,22 @@ def test_config4_full_size_sampled_rows(N, K):
         absum = oracle.cb_abs_products(cs, ss, m.lut, 32, q, d)
         assert_close(got_y, ref, absum, False, f"config4 {N}x{K} ntok={ntok}")
     assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Failure detection without a fault: a bounded wait runs out
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_times_out_and_context_survives():
+    assert qmv.qmv_device_status(clear=True) == 0
+    qmv.qmv_debug_wait_probe(20_000_000)          # 20 ms on a barrier nothing completes
+    torch.cuda.synchronize()
+    assert qmv.qmv_device_status(clear=True) == 8
+    assert qmv.qmv_device_status() == 0
+    # the context is still usable
+    m = Matrices("mxfp4", 16, 64, 1, [0], seed=1)
+    x = qi.normal_bf16_bits(qi.rng(2), (1, 64))
+    y = torch.empty(1, 16, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_dense(m.desc, m.w, to_dev(x), 1, y)
+    ref = oracle.mxfp4_matvec(m.codes[0], m.scales[0], x)
+    assert_close(bf16_to_np(y), ref, oracle.mxfp4_abs_products(m.codes[0], m.scales[0], x), True, "after probe")

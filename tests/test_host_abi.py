@@ -193,3 +193,8 @@ def test_quantize_and_swiglu_argument_errors():
     assert qmv.lib.qmv_quantize_act_q8(FAKE + 4, 1, 64, FAKE, 1 << 20, 0) == qmv.QMV_EALIGN
     assert qmv.lib.qmv_swiglu_bf16(FAKE, FAKE, None, 16, 0) == qmv.QMV_EINVAL
     assert qmv.lib.qmv_swiglu_bf16(FAKE, FAKE + 2, FAKE, 16, 0) == qmv.QMV_EALIGN
+
+
+def test_wait_probe_argument_errors():
+    assert qmv.lib.qmv_debug_wait_probe(0, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_debug_wait_probe(2_000_000_000, 0) == qmv.QMV_EINVAL
