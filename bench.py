@@ -162,6 +162,33 @@ def make_pool(n: int, seed: int):
     return canon, scales, x
 
 
+def kernel_source_digest() -> str:
+    """sha256 over the CUDA sources and headers of the library (kernel identity)."""
+    import hashlib
+    d = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_moe_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                d.update(f.encode() + b"\0" + fh.read())
+    return d.hexdigest()
+
+
+def traffic_for_current_kernel():
+    """DRAM bytes per gather launch from the committed ncu summary, if it was
+    taken on the current kernel sources; otherwise None."""
+    import re
+    p = os.path.join(ROOT, "profiles", "mxfp4_gather_2880_top4.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h or h.group(1) != kernel_source_digest():
+        return None
+    return float(m.group(1))
+
+
 # ---------------------------------------------------------------------------
 # Distributed helpers
 # ---------------------------------------------------------------------------
@@ -225,6 +252,8 @@ def run_ours(args):
 
     import bit_quantized_moe_gb300 as qmv
 
+    L = args.layers
+    step_bytes = L * LAYER_BYTES
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -244,18 +273,18 @@ def run_ours(args):
     desc = qmv.wdesc("mxfp4", N, K, E)
     eb = qmv.qmv_packed_expert_bytes(desc)
     pool_dev = torch.from_numpy(packed_pool).to(dev).view(pool_n, eb)
-    W = torch.empty(LAYERS * 3 * E, eb, dtype=torch.uint8, device=dev)
-    W.view(-1, pool_n, eb).copy_(pool_dev.unsqueeze(0).expand(LAYERS * 3 * E // pool_n, pool_n, eb))
-    W = W.view(LAYERS, 3, E * eb)
+    W = torch.empty(L * 3 * E, eb, dtype=torch.uint8, device=dev)
+    W.view(-1, pool_n, eb).copy_(pool_dev.unsqueeze(0).expand(L * 3 * E // pool_n, pool_n, eb))
+    W = W.view(L, 3, E * eb)
     del pool_dev
 
     x_dev = torch.from_numpy(x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     total_steps = args.warmup + args.steps
     g = qi.rng(1000 + rank)
-    ids_host = np.stack([np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(LAYERS)]) for _ in range(total_steps)])
+    ids_host = np.stack([np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(L)]) for _ in range(total_steps)])
     ids_all = torch.from_numpy(ids_host).to(dev)               # [steps][layers][1][4]
-    ids_buf = torch.empty(LAYERS, 1, TOP_K, dtype=torch.int32, device=dev)
-    yg = torch.empty(LAYERS, 1, TOP_K, N, dtype=torch.bfloat16, device=dev)
+    ids_buf = torch.empty(L, 1, TOP_K, dtype=torch.int32, device=dev)
+    yg = torch.empty(L, 1, TOP_K, N, dtype=torch.bfloat16, device=dev)
     yu = torch.empty_like(yg)
     h = torch.empty_like(yg)
     y = torch.empty_like(yg)
@@ -270,7 +299,7 @@ def run_ours(args):
 
     def step(events=None):
         """One decode token through all layers: gate, up, SwiGLU, down per layer."""
-        for l in range(LAYERS):
+        for l in range(L):
             gather(W[l, 0], x_dev, 0, ids_buf[l], yg[l], events)
             gather(W[l, 1], x_dev, 0, ids_buf[l], yu[l], events)
             qmv.qmv_swiglu_bf16(yg[l], yu[l], h[l], TOP_K * N)
@@ -280,6 +309,14 @@ def run_ours(args):
     ids_buf.copy_(ids_all[0])
     step()
     torch.cuda.synchronize()
+    if args.profile:
+        for i in range(args.steps):
+            ids_buf.copy_(ids_all[i % total_steps])
+            step()
+        torch.cuda.synchronize()
+        print(f"profile run: {args.steps} eager steps over {L} layers, device status "
+              f"{qmv.qmv_device_status(clear=True)}", flush=True)
+        return 0
     graph = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -320,27 +357,40 @@ def run_ours(args):
     sampler.stop()
     dt_ms = ev0.elapsed_time(ev1)
     dt_max = max_over_ranks(dt_ms / 1e3, world, dev)
-    value = aggregate_value(STEP_BYTES, args.steps, world, dt_max)
+    value = aggregate_value(step_bytes, args.steps, world, dt_max)
     clocks = sampler.summary(wall0, wall2)
     clocks["window_s"] = round(wall2 - wall0, 3)
     clocks["timed_s"] = round(wall1 - wall0, 3)
 
-    # --- dominant kernel: per-launch device time of the gather, eager, one event pair per launch
-    events = []
-    n_roof = min(args.steps, 20)
+    # --- dominant kernel: the 72 gather launches of a step captured alone in a
+    # CUDA graph (same weights, ids and outputs, no SwiGLU), replayed over the
+    # timed steps' ids; average launch duration = elapsed / launches.
+    gather_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gather_graph):
+        for l in range(L):
+            gather(W[l, 0], x_dev, 0, ids_buf[l], yg[l], None)
+            gather(W[l, 1], x_dev, 0, ids_buf[l], yu[l], None)
+            gather(W[l, 2], h[l], 1, ids_buf[l], y[l], None)
+    n_roof = min(args.steps, 100)
+    for i in range(3):
+        ids_buf.copy_(ids_all[i])
+        gather_graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
     for i in range(n_roof):
         ids_buf.copy_(ids_all[args.warmup + i])
-        step(events)
+        gather_graph.replay()
+    g1.record()
     torch.cuda.synchronize()
-    durs = [a.elapsed_time(b) for a, b in events]
-    gather_ms = statistics.mean(durs)
+    gather_ms = g0.elapsed_time(g1) / (n_roof * L * 3)
     hbm, peak_kind = peaks()
     achieved = GATHER_BYTES / (gather_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": args.traffic, "kernel": "matvec_kernel<MXFP4,1> (qmv_moe_gather)",
-                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "launch_ms_mean": gather_ms,
-                "launch_ms_median": statistics.median(durs), "launches_timed": len(durs),
-                "algorithmic_bytes_per_launch": GATHER_BYTES}
+                "traffic": traffic_for_current_kernel(), "kernel": "matvec_kernel<MXFP4,1> (qmv_moe_gather)",
+                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "launch_us_mean": gather_ms * 1e3,
+                "launches_timed": n_roof * L * 3, "algorithmic_bytes_per_launch": GATHER_BYTES,
+                "timing": "CUDA graph of one step's 72 gather launches, events around the replays"}
 
     # --- e2e: host buffers, h2d of x and ids, graph step, d2h of every layer's output
     x_host = torch.from_numpy(x_bits.view(np.int16)).pin_memory()
@@ -357,7 +407,7 @@ def run_ours(args):
         torch.cuda.current_stream().synchronize()
     t_e2e = time.perf_counter() - t0
     t_e2e = max_over_ranks(t_e2e, world, dev)
-    e2e = {"value": aggregate_value(STEP_BYTES, n_e2e, world, t_e2e), "unit": "GB/s",
+    e2e = {"value": aggregate_value(step_bytes, n_e2e, world, t_e2e), "unit": "GB/s",
            "h2d_bytes_per_step": x_host.numel() * 2 + ids_buf.numel() * 4,
            "d2h_bytes_per_step": y_host.numel() * 2, "steps": n_e2e}
     status = qmv.qmv_device_status(clear=True)
@@ -370,18 +420,18 @@ def run_ours(args):
         line = {
             "metric": "quantized matvec weight-stream GB/s (MXFP4 MoE decode layer sweep)",
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": dt_max * 1e3 / args.steps, "us_per_moe_layer": dt_max * 1e6 / args.steps / LAYERS,
+            "ms_per_step": dt_max * 1e3 / args.steps, "us_per_moe_layer": dt_max * 1e6 / args.steps / L,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "frac_of_hbm_peak": value / world / hbm,
             "dtype": "mxfp4(e2m1,e8m0) x bf16 -> f32 accumulate",
             "data": "synthetic (seeded uniform E2M1 codes, E8M0 in [120,130], N(0,1) bf16 activations)",
-            "config": {"workload": WORKLOAD, "layers": LAYERS, "experts": E, "top_k": TOP_K, "N": N, "K": K,
-                       "ntok": 1, "weight_bytes_per_step": STEP_BYTES,
+            "config": {"workload": WORKLOAD, "layers": L, "experts": E, "top_k": TOP_K, "N": N, "K": K,
+                       "ntok": 1, "weight_bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2: 1.27 GB of expert weights per step, fresh ids every step",
-                       "launch": "CUDA graph of 96 kernels per step (72 gathers + 24 SwiGLU), PDL between kernels",
+                       "launch": f"CUDA graph of {4 * L} kernels per step ({3 * L} gathers + {L} SwiGLU), PDL between kernels",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": args.steps * LAYERS * 4, "cpu_baseline": cpu, "device_status": status,
+            "gpu_launches": args.steps * L * 4, "cpu_baseline": cpu, "device_status": status,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -395,10 +445,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="dram bytes per gather launch from an ncu capture of the current kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="eager run of --steps steps over --layers layers for ncu captures; prints no JSON")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers held on the device (the reported workload is 24; smaller for ncu captures)")
+    ap.add_argument("--digest", action="store_true", help="print the kernel source digest and exit")
     args = ap.parse_args(argv)
+    if args.digest:
+        print(kernel_source_digest())
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

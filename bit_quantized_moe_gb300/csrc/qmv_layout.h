@@ -12,9 +12,10 @@
 //            CB3 splits its 12-byte lane block into an 8-byte plane
 //            [row][lane][8] followed by a 4-byte plane [row][lane][4]
 //   scales : [lane][row][scales per lane] E8M0 bytes
-// Every region size is a multiple of 16 bytes, so tiles and regions stay
-// 16-byte aligned. Row tiles past N are zero-filled. Experts follow one another
-// at a stride rounded up to 256 bytes.
+// The code region is a multiple of 16 bytes; the tile is padded to a multiple
+// of 16 bytes, so every tile starts 16-byte aligned. Row tiles past N and the
+// padding are zero-filled. Experts follow one another at a stride rounded up
+// to 256 bytes.
 //
 // The bit order of codes inside a lane block is chosen for the device decode
 // (see the per-format notes below) and is not the canonical storage order.
@@ -25,7 +26,7 @@
 
 namespace qmv {
 
-constexpr int kRows = 16;          // rows per tile
+constexpr int kRows = 8;           // rows per tile
 constexpr int kLaneK = 32;         // columns per lane per chunk
 constexpr int kChunkK = 32 * kLaneK;  // columns per chunk (one warp)
 constexpr int kExpertAlign = 256;
@@ -51,8 +52,9 @@ QMV_HD constexpr uint32_t tile_code_bytes(int f, int lanes) {
 QMV_HD constexpr uint32_t tile_scale_bytes(int f, int lanes) {
   return (uint32_t)lanes * kRows * lane_scale_bytes(f);
 }
+// Padded to 16 bytes: the bulk copy size must be a multiple of 16.
 QMV_HD constexpr uint32_t tile_bytes(int f, int lanes) {
-  return tile_code_bytes(f, lanes) + tile_scale_bytes(f, lanes);
+  return (tile_code_bytes(f, lanes) + tile_scale_bytes(f, lanes) + 15u) / 16u * 16u;
 }
 
 struct Geometry {

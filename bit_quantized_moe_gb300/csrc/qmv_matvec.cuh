@@ -14,8 +14,9 @@
 // which applies nothing further and stores it.
 //
 // Per format (lane-block encodings are defined in qmv_layout.h):
-//   MXFP4: E2M1 nibbles -> f16x2 with cvt.rn.f16x2.e2m1x2, fp32 FMA against
-//          the bf16 activations, fp32 group sum times 2^(e-127) per 32
+//   MXFP4: E2M1 nibbles -> f16x2 with cvt.rn.f16x2.e2m1x2, mixed-precision
+//          FMA (f16 operands, fp32 product and sum) against the activations
+//          staged as group-scaled f16, fp32 group sum times 2^(e-127) per 32
 //          weights ("perf(rocm): add an mxfp4 arm to the warp-shared
 //          gather_qmv kernel ...", "Proposed Solution" item 1).
 //   CB2/CB3/CB4: codes -> int8 through byte permutes (prmt) over the codebook
@@ -37,8 +38,8 @@
 
 namespace qmv {
 
-constexpr int kWarps = 4;        // warps per CTA
-constexpr int kStages = 2;       // shared-memory stages per warp
+constexpr int kWarps = 6;        // warps per CTA
+constexpr int kStages = 3;       // shared-memory stages per warp (3 chunks cover K <= 3072)
 constexpr int kMaxEntries = 32;  // ntok * top_k <= 4 * 8
 constexpr int kMaxDevices = 64;
 
@@ -68,7 +69,7 @@ struct KParams {
 // Largest number of activation vectors one work item applies a tile to.
 template <int FMT>
 struct MaxVectors {
-  static constexpr int value = (FMT == MXFP4) ? 2 : 4;
+  static constexpr int value = 4;
 };
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
@@ -76,14 +77,18 @@ __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
 }
 
 struct SmemLayout {
-  uint32_t x_off, ring_off, bar_off, ent_off, total;
+  uint32_t x_off, xinv_off, ring_off, bar_off, ent_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(uint32_t nvec, uint32_t x_vec_bytes,
-                                                  uint32_t full_tile) {
+// x region: the activation vectors as copied; for MXFP4 they are rewritten in
+// place as f16 (see stage_x_mxfp4) and xinv holds one float per 32-group.
+__host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32_t x_vec_bytes,
+                                                  uint32_t full_tile, int K) {
   SmemLayout L;
   L.x_off = 0;
-  L.ring_off = round_up_u32(nvec * x_vec_bytes, 128);
+  L.xinv_off = round_up_u32(nvec * x_vec_bytes, 16);
+  const uint32_t xinv_bytes = (fmt == MXFP4) ? nvec * (uint32_t)(K / 32) * 4u : 0u;
+  L.ring_off = round_up_u32(L.xinv_off + xinv_bytes, 128);
   L.bar_off = L.ring_off + kWarps * kStages * full_tile;
   L.ent_off = round_up_u32(L.bar_off + (kWarps * kStages + 1) * 8, 16);
   L.total = L.ent_off + kMaxEntries * (uint32_t)sizeof(Entry);
@@ -95,7 +100,7 @@ __host__ __device__ inline SmemLayout smem_layout(uint32_t nvec, uint32_t x_vec_
 // ---------------------------------------------------------------------------
 
 template <int NV>
-__device__ int build_entries(const KParams& p, Entry* ent) {
+__device__ int build_entries(const KParams& p, const int* ids, Entry* ent) {
   int n = 0;
   if (p.ids == nullptr) {
     for (int t = 0; t < p.ntok; t += NV) {
@@ -113,7 +118,7 @@ __device__ int build_entries(const KParams& p, Entry* ent) {
   for (int t = 0; t < p.ntok; ++t) {
     for (int j = 0; j < p.top_k; ++j) {
       const int s = t * p.top_k + j;
-      const int ex = p.ids[s];
+      const int ex = ids[s];
       if (ex < 0 || ex >= p.n_experts) continue;
       const int v = p.per_slot ? s : t;
       int f = -1;
@@ -231,14 +236,74 @@ __device__ __forceinline__ void decode_cb4(const uint32_t (&w)[4], const uint32_
 // Per-chunk compute
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+// acc += lo(w2) * lo(x2) + hi(w2) * hi(x2): f16 operands, products and sums in
+// fp32 (mixed-precision FMA, sm_100 and later).
+__device__ __forceinline__ float fma_f16x2_f32(uint32_t w2, uint32_t x2, float acc) {
+  asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+      " fma.rn.f32.f16 %0, wl, xl, %0;\n fma.rn.f32.f16 %0, wh, xh, %0;\n}"
+      : "+f"(acc)
+      : "r"(w2), "r"(x2));
+  return acc;
+}
+
+// Exact 2^e as an fp32 for e in [-149, 127].
+__device__ __forceinline__ float pow2f(int e) {
+  return (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
+
+// MXFP4 activations are staged once per CTA: each 32-element group (one E8M0
+// group of the weights) is scaled by 2^s, s chosen so that the group's largest
+// magnitude lands in [2^14, 2^15), and stored as f16 in place of the bf16
+// input; xinv holds 2^-s. A bf16 value v of the group is then exact in f16
+// whenever |v| >= max|group| * 2^-31, so every product w * x' (E2M1 times
+// f16) and its fp32 accumulation match fp32 arithmetic on the bf16 input, and
+// dot * 2^-s undoes the shift exactly. One thread converts one group.
+__device__ __forceinline__ void stage_x_mxfp4(uint8_t* xs, float* xinv, int nvec, int K, uint32_t vec_bytes) {
+  const int groups = K / 32;
+  for (int gi = threadIdx.x; gi < nvec * groups; gi += blockDim.x) {
+    const int v = gi / groups, g = gi % groups;
+    uint4* xv = reinterpret_cast<uint4*>(xs + (size_t)v * vec_bytes + (size_t)g * 64);
+    uint32_t w[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = xv[q];
+      w[4 * q] = u.x; w[4 * q + 1] = u.y; w[4 * q + 2] = u.z; w[4 * q + 3] = u.w;
+    }
+    uint32_t m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t a = w[2 * i] & 0x7fff7fffu, b = w[2 * i + 1] & 0x7fff7fffu;
+      m8[i] = max(max(a & 0xffffu, a >> 16), max(b & 0xffffu, b >> 16));
+    }
+    const uint32_t mx = max(max(max(m8[0], m8[1]), max(m8[2], m8[3])), max(max(m8[4], m8[5]), max(m8[6], m8[7])));
+    int sh = 0;
+    if (mx != 0 && mx < 0x7f80u) {
+      const int ex = (int)(mx >> 7);
+      const int lg = (ex != 0) ? ex - 127 : -133 + (31 - __clz((int)(mx & 0x7fu)));   // floor(log2 max)
+      sh = 14 - lg;                                                                  // in [-113, 147]
+    }
+    const float m1 = pow2f(sh > 127 ? 127 : sh);
+    const float m2 = pow2f(sh > 127 ? sh - 127 : 0);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float lo = __fmul_rn(__fmul_rn(__uint_as_float(w[i] << 16), m1), m2);
+      const float hi = __fmul_rn(__fmul_rn(__uint_as_float(w[i] & 0xffff0000u), m1), m2);
+      const __half2 h2 = __floats2half2_rn(lo, hi);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xv[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    xinv[gi] = pow2f(-sh);
+  }
+}
 
 template <int NVV, int NVP>
 __device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, int c, int L,
-                                            const uint8_t* st, const uint8_t* xs, float* acc) {
+                                            const uint8_t* st, const uint8_t* xs, const float* xinv,
+                                            float* acc) {
   const int lane = threadIdx.x & 31;
-  float xf[NVV][32];
+  uint32_t xh[NVV][16];   // f16 pairs (k = 2j, 2j + 1) of the lane's 32 columns
+  float inv[NVV];
 #pragma unroll
   for (int v = 0; v < NVV; ++v) {
     const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)e.vec[v] * p.x_vec_bytes +
@@ -246,18 +311,12 @@ __device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, in
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 u = xp[q];
-      xf[v][8 * q + 0] = bf16_lo(u.x);
-      xf[v][8 * q + 1] = bf16_hi(u.x);
-      xf[v][8 * q + 2] = bf16_lo(u.y);
-      xf[v][8 * q + 3] = bf16_hi(u.y);
-      xf[v][8 * q + 4] = bf16_lo(u.z);
-      xf[v][8 * q + 5] = bf16_hi(u.z);
-      xf[v][8 * q + 6] = bf16_lo(u.w);
-      xf[v][8 * q + 7] = bf16_hi(u.w);
+      xh[v][4 * q] = u.x; xh[v][4 * q + 1] = u.y; xh[v][4 * q + 2] = u.z; xh[v][4 * q + 3] = u.w;
     }
+    inv[v] = xinv[e.vec[v] * (p.K / 32) + c * 32 + lane];
   }
-  const uint4 sc = *reinterpret_cast<const uint4*>(st + tile_code_bytes(MXFP4, L) + lane * kRows);
-  const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+  const uint2 sc = *reinterpret_cast<const uint2*>(st + tile_code_bytes(MXFP4, L) + lane * kRows);
+  const uint32_t scw[2] = {sc.x, sc.y};
 #pragma unroll
   for (int r = 0; r < kRows; ++r) {
     const uint4 cw = *reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 16);
@@ -271,18 +330,13 @@ __device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, in
       e2m1x8_to_f16x2(w4[q], h);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
-        const int k = 8 * q + 2 * b;
 #pragma unroll
-        for (int v = 0; v < NVV; ++v) {
-          dot[v] = fmaf(f.x, xf[v][k], dot[v]);
-          dot[v] = fmaf(f.y, xf[v][k + 1], dot[v]);
-        }
+        for (int v = 0; v < NVV; ++v) dot[v] = fma_f16x2_f32(h[b], xh[v][4 * q + b], dot[v]);
       }
     }
     const float s = e8m0_to_f32((scw[r >> 2] >> (8 * (r & 3))) & 0xffu);
 #pragma unroll
-    for (int v = 0; v < NVV; ++v) acc[r * NVP + v] = fmaf(s, dot[v], acc[r * NVP + v]);
+    for (int v = 0; v < NVV; ++v) acc[r * NVP + v] = fmaf(s, dot[v] * inv[v], acc[r * NVP + v]);
   }
 }
 
@@ -303,11 +357,14 @@ __device__ __forceinline__ void chunk_cb(const KParams& p, const Entry& e, int r
     dv[v] = __half2float(reinterpret_cast<const __half*>(xv + p.K)[c * 32 + lane]);
   }
   const uint8_t* scl = st + tile_code_bytes(FMT, L) + lane * kRows * SPL;
+  static_assert(kRows * SPL == 8 || kRows * SPL == 16, "scale block of 8 or 16 bytes");
   uint32_t sw[kRows * SPL / 4];
-#pragma unroll
-  for (int i = 0; i < kRows * SPL / 16; ++i) {
-    const uint4 u = reinterpret_cast<const uint4*>(scl)[i];
-    sw[4 * i] = u.x; sw[4 * i + 1] = u.y; sw[4 * i + 2] = u.z; sw[4 * i + 3] = u.w;
+  if constexpr (kRows * SPL == 16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(scl);
+    sw[0] = u.x; sw[1] = u.y; sw[2] = u.z; sw[3] = u.w;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(scl);
+    sw[0] = u.x; sw[1] = u.y;
   }
   uint32_t t[4] = {p.lut[0], p.lut[1], p.lut[2], p.lut[3]};
 #pragma unroll
@@ -424,7 +481,7 @@ __device__ __forceinline__ void reduce_store(const KParams& p, const Entry& e, i
 
 template <int FMT, int NVV, bool DBG>
 __device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, const Entry& e, int rt,
-                                         int& q, const WarpPipe& wp, const uint8_t* xs) {
+                                         int& q, const WarpPipe& wp, const uint8_t* xs, const float* xinv) {
   constexpr int NVP = (NVV == 3) ? 4 : NVV;
   const int lane = threadIdx.x & 31;
   float acc[kRows * NVP];
@@ -439,7 +496,7 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, con
     const uint8_t* st = wp.ring_ptr + (size_t)s * p.full_tile;
     if (lane < L) {
       if constexpr (FMT == MXFP4) {
-        chunk_mxfp4<NVV, NVP>(p, e, c, L, st, xs, acc);
+        chunk_mxfp4<NVV, NVP>(p, e, c, L, st, xs, xinv, acc);
       } else {
         chunk_cb<FMT, NVV, NVP, DBG>(p, e, rt, c, L, st, xs, acc);
       }
@@ -453,30 +510,39 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, con
 }
 
 template <int FMT, int NV, bool DBG>
-__global__ void __launch_bounds__(kWarps * 32) matvec_kernel(const KParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SmemLayout sl = smem_layout((uint32_t)p.nvec, p.x_vec_bytes, p.full_tile);
+  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K);
   uint8_t* xs = smem + sl.x_off;
+  float* xinv = reinterpret_cast<float*>(smem + sl.xinv_off);
   uint8_t* ring = smem + sl.ring_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bar_off);
   Entry* ent = reinterpret_cast<Entry*>(smem + sl.ent_off);
   __shared__ int s_nent;
 
-  // Inputs (activations, ids) may be produced by the preceding kernel.
-  pdl_wait();
+  __shared__ int s_ids[kMaxEntries];
   const uint32_t xbar = smem_addr(&bars[kWarps * kStages]);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWarps * kStages + 1; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
-    const uint32_t xbytes = (uint32_t)p.nvec * p.x_vec_bytes;
-    mbar_arrive_expect_tx(xbar, xbytes);
-    for (int v = 0; v < p.nvec; ++v) {
-      bulk_copy_g2s(smem_addr(xs + (size_t)v * p.x_vec_bytes), p.x + (size_t)v * p.x_vec_bytes,
-                    p.x_vec_bytes, xbar);
+  }
+  // Inputs (activations, ids) may be produced by the preceding kernel.
+  pdl_wait();
+  if (warp == 0) {
+    const int nslots = p.ids ? p.ntok * p.top_k : 0;
+    if (lane < nslots) s_ids[lane] = p.ids[lane];
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t xbytes = (uint32_t)p.nvec * p.x_vec_bytes;
+      mbar_arrive_expect_tx(xbar, xbytes);
+      for (int v = 0; v < p.nvec; ++v) {
+        bulk_copy_g2s(smem_addr(xs + (size_t)v * p.x_vec_bytes), p.x + (size_t)v * p.x_vec_bytes,
+                      p.x_vec_bytes, xbar);
+      }
+      s_nent = build_entries<NV>(p, s_ids, ent);
     }
-    s_nent = build_entries<NV>(p, ent);
   }
   __syncthreads();
   pdl_launch_dependents();
@@ -497,7 +563,7 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_kernel(const KParams p) {
   if (p.ids != nullptr) {
     const int nslots = p.ntok * p.top_k;
     for (int s = 0; s < nslots; ++s) {
-      const int ex = p.ids[s];
+      const int ex = s_ids[s];
       if (ex >= 0 && ex < p.n_experts) continue;
       for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < p.N; row += gridDim.x * blockDim.x) {
         if constexpr (FMT == MXFP4) {
@@ -515,6 +581,12 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_kernel(const KParams p) {
     if (!mbar_wait_bounded(xbar, 0, kDrainLimitNs) && lane == 0) set_status(kStatusDrain);
     ok = false;
   }
+  if constexpr (FMT == MXFP4) {
+    // every thread reaches this barrier: a warp whose x wait failed still
+    // takes part, then skips its work items below
+    if (ok) stage_x_mxfp4(xs, xinv, p.nvec, p.K, p.x_vec_bytes);
+    __syncthreads();
+  }
 
   int q = 0;
   if (ok) {
@@ -522,10 +594,10 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_kernel(const KParams p) {
       const Entry& e = ent[item / p.row_tiles];
       const int rt = item % p.row_tiles;
       switch (e.nv) {
-        case 1: ok = run_item<FMT, 1, DBG>(p, ent, e, rt, q, wp, xs); break;
-        case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG>(p, ent, e, rt, q, wp, xs); break;
-        case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG>(p, ent, e, rt, q, wp, xs); break;
-        case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG>(p, ent, e, rt, q, wp, xs); break;
+        case 1: ok = run_item<FMT, 1, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
+        case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
+        case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
+        case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
         default: break;
       }
       if (!ok) {
@@ -590,7 +662,7 @@ template <int FMT>
 cudaError_t launch_matvec(const MatvecArgs& a) {
   constexpr int NVMAX = MaxVectors<FMT>::value;
   const KParams p = make_params(a);
-  const SmemLayout sl = smem_layout((uint32_t)p.nvec, p.x_vec_bytes, p.full_tile);
+  const SmemLayout sl = smem_layout(a.fmt, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K);
   const int want_nv = a.ids ? (a.ntok < NVMAX ? a.ntok : NVMAX) : (a.ntok < NVMAX ? a.ntok : NVMAX);
   void* fn = nullptr;
   const bool dbg = a.dbg != nullptr;
