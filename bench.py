@@ -293,7 +293,10 @@ def run_ours(args):
         if events is not None:
             events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
             events[-1][0].record()
-        qmv.qmv_moe_gather(desc, w, xin, per_slot, ids, 1, TOP_K, out)
+        # The step's weights and ids are never written by a kernel of the step
+        # (ids are copied in before it), so every gather may prefetch them
+        # while the preceding kernel drains.
+        qmv.qmv_moe_gather_ex(desc, w, xin, per_slot, ids, 1, TOP_K, out, qmv.QMV_FLAG_PREFETCH_INPUTS)
         if events is not None:
             events[-1][1].record()
 
@@ -428,7 +431,7 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "layers": L, "experts": E, "top_k": TOP_K, "N": N, "K": K,
                        "ntok": 1, "weight_bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2: 1.27 GB of expert weights per step, fresh ids every step",
-                       "launch": f"CUDA graph of {4 * L} kernels per step ({3 * L} gathers + {L} SwiGLU), PDL between kernels",
+                       "launch": f"CUDA graph of {4 * L} kernels per step ({3 * L} gathers + {L} SwiGLU), programmatic dependent launch with weight/id prefetch",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "clocks": clocks, "e2e": e2e,
             "gpu_launches": args.steps * L * 4, "cpu_baseline": cpu, "device_status": status,

@@ -27,6 +27,7 @@ QMV_ESHAPE = -2
 QMV_EALIGN = -3
 QMV_ESIZE = -4
 QMV_ECUDA = -5
+QMV_FLAG_PREFETCH_INPUTS = 1
 
 MXFP4, CB2, CB3, CB4 = 0, 1, 2, 3
 FORMATS = {"mxfp4": MXFP4, "cb2": CB2, "cb3": CB3, "cb4": CB4}
@@ -38,7 +39,7 @@ EXPORTS = (
     "qmv_scale_group", "qmv_code_bits", "qmv_canonical_code_bytes", "qmv_canonical_scale_bytes",
     "qmv_packed_expert_bytes", "qmv_packed_bytes", "qmv_pack_weights", "qmv_unpack_weights",
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
-    "qmv_dense", "qmv_moe_gather", "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
+    "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
 
@@ -86,6 +87,8 @@ def _load() -> ctypes.CDLL:
         "qmv_act_q8_unpack": (ctypes.c_int, [P, I32, I32, P, P]),
         "qmv_dense": (ctypes.c_int, [D, P, P, I32, P, P]),
         "qmv_moe_gather": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P]),
+        "qmv_dense_ex": (ctypes.c_int, [D, P, P, I32, P, ctypes.c_uint32, P]),
+        "qmv_moe_gather_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
         "qmv_debug_dequant": (ctypes.c_int, [D, P, I32, P, SZ, P]),
@@ -214,6 +217,16 @@ def qmv_dense(desc: WDesc, w, x, ntok: int, y, stream=None) -> None:
 def qmv_moe_gather(desc: WDesc, w, x, per_slot_x: int, ids, ntok: int, top_k: int, y, stream=None) -> None:
     _check(lib.qmv_moe_gather(ctypes.byref(desc), _ptr(w), _ptr(x), int(per_slot_x), _ptr(ids), ntok,
                               top_k, _ptr(y), _stream(stream)))
+
+
+def qmv_dense_ex(desc: WDesc, w, x, ntok: int, y, flags: int, stream=None) -> None:
+    _check(lib.qmv_dense_ex(ctypes.byref(desc), _ptr(w), _ptr(x), ntok, _ptr(y), int(flags), _stream(stream)))
+
+
+def qmv_moe_gather_ex(desc: WDesc, w, x, per_slot_x: int, ids, ntok: int, top_k: int, y, flags: int,
+                      stream=None) -> None:
+    _check(lib.qmv_moe_gather_ex(ctypes.byref(desc), _ptr(w), _ptr(x), int(per_slot_x), _ptr(ids), ntok, top_k,
+                                 _ptr(y), int(flags), _stream(stream)))
 
 
 def qmv_swiglu_bf16(g, u, h, n: int, stream=None) -> None:

@@ -99,9 +99,10 @@ cudaError_t launch_for(const MatvecArgs& a) {
 
 int run_matvec(const qmv_wdesc* desc, const void* w, const void* x, int per_slot, const int32_t* ids,
                int ntok, int top_k, void* y, int32_t* dbg, size_t dbg_bytes, cudaStream_t stream,
-               const char* name) {
+               const char* name, uint32_t flags = 0) {
   int rc = check_desc(desc);
   if (rc) return rc;
+  if (flags & ~(uint32_t)QMV_FLAG_PREFETCH_INPUTS) return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
   if (w == nullptr || x == nullptr || y == nullptr)
     return fail(QMV_EINVAL, "%s: weight, activation and output pointers must be non-NULL", name);
   if (ntok < 1 || ntok > QMV_MAX_NTOK) return fail(QMV_EINVAL, "%s: ntok=%d outside [1, %d]", name, ntok, QMV_MAX_NTOK);
@@ -139,6 +140,7 @@ int run_matvec(const qmv_wdesc* desc, const void* w, const void* x, int per_slot
   a.y = y;
   a.dbg = dbg;
   lut_words(desc, a.lut);
+  a.flags = flags;
   a.stream = stream;
   const DevInfo* di = dev_info();
   if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
@@ -277,6 +279,19 @@ int qmv_moe_gather(const qmv_wdesc* desc, const void* w, const void* x, int32_t 
   if (ids == nullptr) return fail(QMV_EINVAL, "qmv_moe_gather: ids must be non-NULL");
   return run_matvec(desc, w, x, per_slot_x, ids, ntok, top_k, y, nullptr, 0, static_cast<cudaStream_t>(stream),
                     "qmv_moe_gather");
+}
+
+int qmv_dense_ex(const qmv_wdesc* desc, const void* w, const void* x, int32_t ntok, void* y, uint32_t flags,
+                 void* stream) {
+  return run_matvec(desc, w, x, 0, nullptr, ntok, 1, y, nullptr, 0, static_cast<cudaStream_t>(stream),
+                    "qmv_dense_ex", flags);
+}
+
+int qmv_moe_gather_ex(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x, const int32_t* ids,
+                      int32_t ntok, int32_t top_k, void* y, uint32_t flags, void* stream) {
+  if (ids == nullptr) return fail(QMV_EINVAL, "qmv_moe_gather_ex: ids must be non-NULL");
+  return run_matvec(desc, w, x, per_slot_x, ids, ntok, top_k, y, nullptr, 0, static_cast<cudaStream_t>(stream),
+                    "qmv_moe_gather_ex", flags);
 }
 
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,

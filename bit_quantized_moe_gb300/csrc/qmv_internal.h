@@ -22,6 +22,7 @@ struct MatvecArgs {
   void* y = nullptr;
   int32_t* dbg = nullptr;         // integer block sums (CB formats) or null
   uint32_t lut[4] = {0, 0, 0, 0}; // 16 int8 codebook bytes
+  uint32_t flags = 0;             // QMV_FLAG_* of the call
   cudaStream_t stream = nullptr;
 };
 

@@ -3,8 +3,8 @@
 //
 // Work decomposition. A "work item" is one row tile (kRows rows) of one
 // matrix applied to up to NV activation vectors (the "entry": an expert and
-// the (token, slot) pairs routed to it). Items are dealt round-robin to every
-// warp of the grid. A warp streams its items' tiles -- one tile per K chunk --
+// the (token, slot) pairs routed to it). Items are dealt round-robin over the
+// CTAs of a one-wave grid, then over each CTA's warps. A warp streams its items' tiles -- one tile per K chunk --
 // through a private ring of kStages shared-memory stages filled by bulk
 // asynchronous copies (one elected lane issues them, an mbarrier per stage
 // tracks completion). Lane l of the warp owns columns [32 l, 32 l + 32) of
@@ -64,7 +64,11 @@ struct KParams {
   void* y;
   int32_t* dbg;
   uint32_t lut[4];
+  uint32_t flags;
 };
+
+// KParams::flags
+constexpr uint32_t kFlagPrefetch = 1u;   // weights and ids are not written by the preceding kernel
 
 // Largest number of activation vectors one work item applies a tile to.
 template <int FMT>
@@ -236,13 +240,10 @@ __device__ __forceinline__ void decode_cb4(const uint32_t (&w)[4], const uint32_
 // Per-chunk compute
 // ---------------------------------------------------------------------------
 
-// acc += lo(w2) * lo(x2) + hi(w2) * hi(x2): f16 operands, products and sums in
-// fp32 (mixed-precision FMA, sm_100 and later).
-__device__ __forceinline__ float fma_f16x2_f32(uint32_t w2, uint32_t x2, float acc) {
-  asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
-      " fma.rn.f32.f16 %0, wl, xl, %0;\n fma.rn.f32.f16 %0, wh, xh, %0;\n}"
-      : "+f"(acc)
-      : "r"(w2), "r"(x2));
+// acc + w * x with f16 operands, product and sum in fp32 (mixed-precision FMA,
+// sm_100 and later).
+__device__ __forceinline__ float fma_f16_f32(uint16_t w, uint16_t x, float acc) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(w), "h"(x));
   return acc;
 }
 
@@ -302,7 +303,9 @@ __device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, in
                                             const uint8_t* st, const uint8_t* xs, const float* xinv,
                                             float* acc) {
   const int lane = threadIdx.x & 31;
-  uint32_t xh[NVV][16];   // f16 pairs (k = 2j, 2j + 1) of the lane's 32 columns
+  // The lane's 32 activations as separate f16 values, unpacked once per chunk
+  // and reused for all kRows rows.
+  uint16_t xv16[NVV][32];
   float inv[NVV];
 #pragma unroll
   for (int v = 0; v < NVV; ++v) {
@@ -311,32 +314,44 @@ __device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, in
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 u = xp[q];
-      xh[v][4 * q] = u.x; xh[v][4 * q + 1] = u.y; xh[v][4 * q + 2] = u.z; xh[v][4 * q + 3] = u.w;
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv16[v][8 * q + 2 * i] = (uint16_t)(w4[i] & 0xffffu);
+        xv16[v][8 * q + 2 * i + 1] = (uint16_t)(w4[i] >> 16);
+      }
     }
     inv[v] = xinv[e.vec[v] * (p.K / 32) + c * 32 + lane];
   }
   const uint2 sc = *reinterpret_cast<const uint2*>(st + tile_code_bytes(MXFP4, L) + lane * kRows);
   const uint32_t scw[2] = {sc.x, sc.y};
+  uint4 cw[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) cw[r] = *reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 16);
 #pragma unroll
   for (int r = 0; r < kRows; ++r) {
-    const uint4 cw = *reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 16);
-    const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
-    float dot[NVV];
+    const uint32_t w4[4] = {cw[r].x, cw[r].y, cw[r].z, cw[r].w};
+    float d0[NVV], d1[NVV];   // even / odd columns: two independent chains
 #pragma unroll
-    for (int v = 0; v < NVV; ++v) dot[v] = 0.f;
+    for (int v = 0; v < NVV; ++v) d0[v] = d1[v] = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint32_t h[4];
       e2m1x8_to_f16x2(w4[q], h);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
+        const int k = 8 * q + 2 * b;
+        const uint16_t wl = (uint16_t)(h[b] & 0xffffu), wh = (uint16_t)(h[b] >> 16);
 #pragma unroll
-        for (int v = 0; v < NVV; ++v) dot[v] = fma_f16x2_f32(h[b], xh[v][4 * q + b], dot[v]);
+        for (int v = 0; v < NVV; ++v) {
+          d0[v] = fma_f16_f32(wl, xv16[v][k], d0[v]);
+          d1[v] = fma_f16_f32(wh, xv16[v][k + 1], d1[v]);
+        }
       }
     }
     const float s = e8m0_to_f32((scw[r >> 2] >> (8 * (r & 3))) & 0xffu);
 #pragma unroll
-    for (int v = 0; v < NVV; ++v) acc[r * NVP + v] = fmaf(s, dot[v] * inv[v], acc[r * NVP + v]);
+    for (int v = 0; v < NVV; ++v) acc[r * NVP + v] = fmaf(s, (d0[v] + d1[v]) * inv[v], acc[r * NVP + v]);
   }
 }
 
@@ -528,27 +543,37 @@ __global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p)
     for (int i = 0; i < kWarps * kStages + 1; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
   }
-  // Inputs (activations, ids) may be produced by the preceding kernel.
-  pdl_wait();
+  // Programmatic dependent launch. Activations may be produced by the kernel
+  // that precedes this one in the stream, so they are read only after
+  // griddepcontrol.wait. Without kFlagPrefetch the ids are read after the wait
+  // too. With it, the caller guarantees that the weights and ids were not
+  // written by that preceding kernel; every kernel of this library signals its
+  // dependents only after its own wait, so everything older is complete, and
+  // the ids and the first weight tiles are fetched while the preceding kernel
+  // drains.
+  const bool early = (p.flags & kFlagPrefetch) != 0;
+  auto issue_x = [&]() {
+    const uint32_t xbytes = (uint32_t)p.nvec * p.x_vec_bytes;
+    mbar_arrive_expect_tx(xbar, xbytes);
+    for (int v = 0; v < p.nvec; ++v) {
+      bulk_copy_g2s(smem_addr(xs + (size_t)v * p.x_vec_bytes), p.x + (size_t)v * p.x_vec_bytes,
+                    p.x_vec_bytes, xbar);
+    }
+  };
+  if (!early) pdl_wait();
   if (warp == 0) {
+    if (!early && lane == 0) issue_x();
     const int nslots = p.ids ? p.ntok * p.top_k : 0;
     if (lane < nslots) s_ids[lane] = p.ids[lane];
     __syncwarp();
-    if (lane == 0) {
-      const uint32_t xbytes = (uint32_t)p.nvec * p.x_vec_bytes;
-      mbar_arrive_expect_tx(xbar, xbytes);
-      for (int v = 0; v < p.nvec; ++v) {
-        bulk_copy_g2s(smem_addr(xs + (size_t)v * p.x_vec_bytes), p.x + (size_t)v * p.x_vec_bytes,
-                      p.x_vec_bytes, xbar);
-      }
-      s_nent = build_entries<NV>(p, s_ids, ent);
-    }
+    if (lane == 0) s_nent = build_entries<NV>(p, s_ids, ent);
   }
   __syncthreads();
-  pdl_launch_dependents();
 
   WarpPipe wp;
-  wp.gw = blockIdx.x * kWarps + warp;
+  // Items are dealt to CTAs first (item i -> CTA i % gridDim.x), so every CTA,
+  // and with a full grid every SM, gets the same number of items within one.
+  wp.gw = blockIdx.x + gridDim.x * warp;
   wp.nw = gridDim.x * kWarps;
   wp.n_items = s_nent * p.row_tiles;
   wp.ring_ptr = ring + (size_t)warp * kStages * p.full_tile;
@@ -558,6 +583,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p)
   if (lane == 0) {
     for (int q = 0; q < kStages; ++q) issue_tile(p, ent, wp, q);
   }
+  if (early) {
+    pdl_wait();
+    if (threadIdx.x == 0) issue_x();
+  }
+  pdl_launch_dependents();
 
   // Gather slots with an invalid id produce zero rows.
   if (p.ids != nullptr) {
@@ -655,6 +685,7 @@ inline KParams make_params(const MatvecArgs& a) {
   p.y = a.y;
   p.dbg = a.dbg;
   for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i];
+  p.flags = a.flags;
   return p;
 }
 
@@ -714,9 +745,9 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   // Upper bound on work items: every routed pair its own entry.
   const int entries_max = a.ids ? a.ntok * a.top_k : (a.ntok + want_nv - 1) / want_nv;
   const long items = (long)entries_max * p.row_tiles;
-  long grid = (items + kWarps - 1) / kWarps;
-  const long cap = (long)device_sm_count() * per_sm;
-  if (grid > cap) grid = cap;
+  // One wave on every SM; no CTA without an item.
+  long grid = (long)device_sm_count() * per_sm;
+  if (grid > items) grid = items;
   if (grid < 1) grid = 1;
 
   cudaLaunchConfig_t cfg = {};

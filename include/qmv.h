@@ -182,6 +182,28 @@ int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, 
                    const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, void* stream);
 
 /*
+ * Launch flags of qmv_dense_ex / qmv_moe_gather_ex.
+ *
+ * QMV_FLAG_PREFETCH_INPUTS: the caller guarantees that the weights and the
+ * router ids were not written by the kernel immediately preceding this call
+ * in the stream (they were ready before it started). The kernel then reads the
+ * ids and starts streaming weight tiles while that kernel drains, and waits
+ * for it (programmatic dependent launch) only before reading the activations
+ * and writing outputs. Typical use: the up and down projections of a MoE
+ * layer, whose ids the router produced before the gate projection ran.
+ */
+#define QMV_FLAG_PREFETCH_INPUTS 1u
+
+/* qmv_dense with launch flags (QMV_FLAG_*); flags = 0 is qmv_dense. */
+int qmv_dense_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t ntok, void* y_dev,
+                 uint32_t flags, void* stream);
+
+/* qmv_moe_gather with launch flags (QMV_FLAG_*); flags = 0 is qmv_moe_gather. */
+int qmv_moe_gather_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,
+                      const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, uint32_t flags,
+                      void* stream);
+
+/*
  * SwiGLU between the gate/up and down gathers of a gpt-oss-style MoE layer:
  * h[i] = silu(g[i]) * u[i], silu(z) = z / (1 + exp(-z)), bf16 in and out,
  * fp32 arithmetic, n elements ("perf(rocm): add an mxfp4 arm ...", "Problem /

@@ -380,3 +380,47 @@ def test_bounded_wait_times_out_and_context_survives():
     qmv.qmv_dense(m.desc, m.w, to_dev(x), 1, y)
     ref = oracle.mxfp4_matvec(m.codes[0], m.scales[0], x)
     assert_close(bf16_to_np(y), ref, oracle.mxfp4_abs_products(m.codes[0], m.scales[0], x), True, "after probe")
+
+
+# ---------------------------------------------------------------------------
+# Launch flags: prefetching weights/ids before the dependent-launch wait
+# ---------------------------------------------------------------------------
+
+def test_prefetch_flag_matches_plain_path_in_a_dependent_chain():
+    """gate, up (prefetch), SwiGLU, down (prefetch, reads the SwiGLU output) on
+    one stream: results bit-identical to the same chain without the flag."""
+    E, N, K, N_down, top_k = 16, 2880, 2880, 516, 4
+    g = qi.rng(41)
+    ids = to_dev(qi.topk_ids(g, 1, top_k, E))
+    mats = [Matrices("mxfp4", N, K, E, range(E), seed=42 + i) for i in range(2)]
+    mats.append(Matrices("mxfp4", N_down, N, E, range(E), seed=44))
+    x = to_dev(qi.normal_bf16_bits(g, (1, K)))
+    outs = []
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for flags in (0, qmv.QMV_FLAG_PREFETCH_INPUTS, 0, qmv.QMV_FLAG_PREFETCH_INPUTS):
+            yg = torch.empty(1, top_k, N, dtype=torch.bfloat16, device=DEV)
+            yu, h = torch.empty_like(yg), torch.empty_like(yg)
+            y = torch.empty(1, top_k, N_down, dtype=torch.bfloat16, device=DEV)
+            qmv.qmv_moe_gather(mats[0].desc, mats[0].w, x, 0, ids, 1, top_k, yg)
+            qmv.qmv_moe_gather_ex(mats[1].desc, mats[1].w, x, 0, ids, 1, top_k, yu, flags)
+            qmv.qmv_swiglu_bf16(yg, yu, h, top_k * N)
+            qmv.qmv_moe_gather_ex(mats[2].desc, mats[2].w, h, 1, ids, 1, top_k, y, flags)
+            outs.append(y.view(torch.int16).clone())
+    s.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert status_clean()
+
+
+def test_dense_ex_prefetch_matches():
+    m = Matrices("cb4", 520, 7168, 1, [0], seed=43, lut=qi.LUT_CB4)
+    xq, _, _ = quantize_on_gpu(qi.normal_f32(qi.rng(44), (3, 7168)))
+    y0 = torch.empty(3, 520, dtype=torch.float32, device=DEV)
+    y1 = torch.empty_like(y0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qmv.qmv_dense(m.desc, m.w, xq, 3, y0)
+        qmv.qmv_dense_ex(m.desc, m.w, xq, 3, y1, qmv.QMV_FLAG_PREFETCH_INPUTS)
+    s.synchronize()
+    assert torch.equal(y0.view(torch.int32), y1.view(torch.int32))

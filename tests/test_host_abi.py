@@ -198,3 +198,11 @@ def test_quantize_and_swiglu_argument_errors():
 def test_wait_probe_argument_errors():
     assert qmv.lib.qmv_debug_wait_probe(0, 0) == qmv.QMV_EINVAL
     assert qmv.lib.qmv_debug_wait_probe(2_000_000_000, 0) == qmv.QMV_EINVAL
+
+
+def test_unknown_launch_flags_rejected():
+    d = qmv.wdesc("mxfp4", 64, 64, 4)
+    rc = qmv.lib.qmv_moe_gather_ex(qmv.ctypes.byref(d), FAKE, FAKE, 0, FAKE, 1, 4, FAKE, 6, 0)
+    assert rc == qmv.QMV_EINVAL
+    d = qmv.wdesc("cb2", 64, 64)
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 2, 0) == qmv.QMV_EINVAL
