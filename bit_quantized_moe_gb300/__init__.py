@@ -39,7 +39,8 @@ EXPORTS = (
     "qmv_scale_group", "qmv_code_bits", "qmv_canonical_code_bytes", "qmv_canonical_scale_bytes",
     "qmv_packed_expert_bytes", "qmv_packed_bytes", "qmv_pack_weights", "qmv_unpack_weights",
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
-    "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
+    "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
+    "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
 
@@ -88,6 +89,9 @@ def _load() -> ctypes.CDLL:
         "qmv_dense": (ctypes.c_int, [D, P, P, I32, P, P]),
         "qmv_moe_gather": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P]),
         "qmv_dense_ex": (ctypes.c_int, [D, P, P, I32, P, ctypes.c_uint32, P]),
+        "qmv_packed_gate_up_expert_bytes": (SZ, [D]),
+        "qmv_pack_gate_up": (ctypes.c_int, [D, P, P, P, P, P, SZ]),
+        "qmv_moe_gate_up_swiglu": (ctypes.c_int, [D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_moe_gather_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
@@ -186,6 +190,22 @@ def qmv_pack_weights(desc: WDesc, codes: np.ndarray, scales: np.ndarray) -> np.n
     return out
 
 
+def qmv_packed_gate_up_expert_bytes(desc: WDesc) -> int:
+    return lib.qmv_packed_gate_up_expert_bytes(ctypes.byref(desc))
+
+
+def qmv_pack_gate_up(desc: WDesc, gate_codes, gate_scales, up_codes, up_scales) -> np.ndarray:
+    """Canonical gate and up codes/scales (each as for qmv_pack_weights) -> fused GPU layout bytes."""
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (gate_codes, gate_scales, up_codes, up_scales)]
+    E = desc.n_experts
+    if (arrs[0].nbytes != E * qmv_canonical_code_bytes(desc) or arrs[2].nbytes != arrs[0].nbytes
+            or arrs[1].nbytes != E * qmv_canonical_scale_bytes(desc) or arrs[3].nbytes != arrs[1].nbytes):
+        raise ValueError("gate/up codes or scales do not match the descriptor's canonical sizes")
+    out = np.empty(E * qmv_packed_gate_up_expert_bytes(desc), dtype=np.uint8)
+    _check(lib.qmv_pack_gate_up(ctypes.byref(desc), *[a.ctypes.data for a in arrs], out.ctypes.data, out.nbytes))
+    return out
+
+
 def qmv_unpack_weights(desc: WDesc, packed: np.ndarray):
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     E = desc.n_experts
@@ -227,6 +247,12 @@ def qmv_moe_gather_ex(desc: WDesc, w, x, per_slot_x: int, ids, ntok: int, top_k:
                       stream=None) -> None:
     _check(lib.qmv_moe_gather_ex(ctypes.byref(desc), _ptr(w), _ptr(x), int(per_slot_x), _ptr(ids), ntok, top_k,
                                  _ptr(y), int(flags), _stream(stream)))
+
+
+def qmv_moe_gate_up_swiglu(desc: WDesc, w, x, ids, ntok: int, top_k: int, h, flags: int = 0,
+                           stream=None) -> None:
+    _check(lib.qmv_moe_gate_up_swiglu(ctypes.byref(desc), _ptr(w), _ptr(x), _ptr(ids), ntok, top_k, _ptr(h),
+                                      int(flags), _stream(stream)))
 
 
 def qmv_swiglu_bf16(g, u, h, n: int, stream=None) -> None:

@@ -56,8 +56,6 @@ cudaError_t launch_quantize_q8(const float* x, int nvec, int K, void* xq, cudaSt
 // ---------------------------------------------------------------------------
 // SwiGLU: h = silu(g) * u, silu(z) = z / (1 + exp(-z)), fp32 arithmetic.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
-
 __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ u,
                               __nv_bfloat16* __restrict__ h, int64_t n) {
   pdl_wait();

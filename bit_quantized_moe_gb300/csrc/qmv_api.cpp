@@ -18,6 +18,8 @@ namespace qmv {
 thread_local const char* g_launch_stage = "";
 
 void pack_expert(const Geometry& g, const uint8_t* codes, const uint8_t* scales, uint8_t* out);
+void pack_gate_up_expert(const Geometry& g, int N, const uint8_t* gate_codes, const uint8_t* gate_scales,
+                         const uint8_t* up_codes, const uint8_t* up_scales, uint8_t* out);
 void unpack_expert(const Geometry& g, const uint8_t* in, uint8_t* codes, uint8_t* scales);
 
 namespace {
@@ -97,11 +99,22 @@ cudaError_t launch_for(const MatvecArgs& a) {
   }
 }
 
-int run_matvec(const qmv_wdesc* desc, const void* w, const void* x, int per_slot, const int32_t* ids,
+// Rows of the gate/up-interleaved matrix of a projection with N rows.
+int gate_up_rows(int N) { return 2 * ((N + kRows / 2 - 1) / (kRows / 2) * (kRows / 2)); }
+
+int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_slot, const int32_t* ids,
                int ntok, int top_k, void* y, int32_t* dbg, size_t dbg_bytes, cudaStream_t stream,
-               const char* name, uint32_t flags = 0) {
-  int rc = check_desc(desc);
+               const char* name, uint32_t flags = 0, bool glu = false) {
+  int rc = check_desc(desc_in);
   if (rc) return rc;
+  qmv_wdesc glu_desc;
+  const qmv_wdesc* desc = desc_in;
+  if (glu) {
+    if (desc_in->N > QMV_MAX_N / 2) return fail(QMV_ESHAPE, "%s: N=%d too large for gate/up fusion", name, desc_in->N);
+    glu_desc = *desc_in;
+    glu_desc.N = gate_up_rows(desc_in->N);
+    desc = &glu_desc;
+  }
   if (flags & ~(uint32_t)QMV_FLAG_PREFETCH_INPUTS) return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
   if (w == nullptr || x == nullptr || y == nullptr)
     return fail(QMV_EINVAL, "%s: weight, activation and output pointers must be non-NULL", name);
@@ -141,6 +154,8 @@ int run_matvec(const qmv_wdesc* desc, const void* w, const void* x, int per_slot
   a.dbg = dbg;
   lut_words(desc, a.lut);
   a.flags = flags;
+  a.glu = glu;
+  a.out_n = desc_in->N;
   a.stream = stream;
   const DevInfo* di = dev_info();
   if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
@@ -292,6 +307,38 @@ int qmv_moe_gather_ex(const qmv_wdesc* desc, const void* w, const void* x, int32
   if (ids == nullptr) return fail(QMV_EINVAL, "qmv_moe_gather_ex: ids must be non-NULL");
   return run_matvec(desc, w, x, per_slot_x, ids, ntok, top_k, y, nullptr, 0, static_cast<cudaStream_t>(stream),
                     "qmv_moe_gather_ex", flags);
+}
+
+size_t qmv_packed_gate_up_expert_bytes(const qmv_wdesc* d) {
+  if (check_desc(d)) return 0;
+  if (d->N > QMV_MAX_N / 2) return 0;
+  return (size_t)make_geometry(d->fmt, gate_up_rows(d->N), d->K).expert;
+}
+
+int qmv_pack_gate_up(const qmv_wdesc* d, const uint8_t* gate_codes, const uint8_t* gate_scales,
+                     const uint8_t* up_codes, const uint8_t* up_scales, void* out, size_t out_bytes) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!gate_codes || !gate_scales || !up_codes || !up_scales || !out)
+    return fail(QMV_EINVAL, "qmv_pack_gate_up: NULL buffer");
+  if (d->N > QMV_MAX_N / 2) return fail(QMV_ESHAPE, "qmv_pack_gate_up: N=%d too large", d->N);
+  const Geometry g = make_geometry(d->fmt, gate_up_rows(d->N), d->K);
+  const size_t need = (size_t)g.expert * d->n_experts;
+  if (out_bytes < need) return fail(QMV_ESIZE, "qmv_pack_gate_up: output %zu bytes < %zu", out_bytes, need);
+  const size_t cb = (size_t)d->N * d->K * fmt_bits(d->fmt) / 8;
+  const size_t sb = (size_t)d->N * (d->K / fmt_group(d->fmt));
+  for (int e = 0; e < d->n_experts; ++e) {
+    pack_gate_up_expert(g, d->N, gate_codes + e * cb, gate_scales + e * sb, up_codes + e * cb, up_scales + e * sb,
+                        static_cast<uint8_t*>(out) + (size_t)e * g.expert);
+  }
+  return ok();
+}
+
+int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, const int32_t* ids, int32_t ntok,
+                           int32_t top_k, void* h, uint32_t flags, void* stream) {
+  if (ids == nullptr) return fail(QMV_EINVAL, "qmv_moe_gate_up_swiglu: ids must be non-NULL");
+  return run_matvec(desc, w, x, 0, ids, ntok, top_k, h, nullptr, 0, static_cast<cudaStream_t>(stream),
+                    "qmv_moe_gate_up_swiglu", flags, true);
 }
 
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,

@@ -23,6 +23,8 @@ struct MatvecArgs {
   int32_t* dbg = nullptr;         // integer block sums (CB formats) or null
   uint32_t lut[4] = {0, 0, 0, 0}; // 16 int8 codebook bytes
   uint32_t flags = 0;             // QMV_FLAG_* of the call
+  bool glu = false;               // gate/up-interleaved matrix, store silu(gate) * up
+  int out_n = 0;                  // output rows per slot (0: N)
   cudaStream_t stream = nullptr;
 };
 

@@ -65,10 +65,12 @@ struct KParams {
   int32_t* dbg;
   uint32_t lut[4];
   uint32_t flags;
+  int out_n;              // rows of each output vector (N, or N / 2 rounded for gate/up fusion)
 };
 
 // KParams::flags
 constexpr uint32_t kFlagPrefetch = 1u;   // weights and ids are not written by the preceding kernel
+constexpr uint32_t kFlagGlu = 2u;        // gate/up-interleaved matrix: store silu(gate) * up
 
 // Largest number of activation vectors one work item applies a tile to.
 template <int FMT>
@@ -464,29 +466,41 @@ __device__ __forceinline__ void rs_step(float* v, int lane) {
   }
 }
 
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+template <int FMT>
+__device__ __forceinline__ void store_out(const KParams& p, size_t o, float val) {
+  if constexpr (FMT == MXFP4) {
+    reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(val);
+  } else {
+    reinterpret_cast<float*>(p.y)[o] = val;
+  }
+}
+
+// After the reduce-scatter, lane l holds (row, vector) index l / (32 / M).
+// Plain: store y[slot][rt * kRows + row]. Gate/up fusion (kFlagGlu): rows
+// 0..3 of the tile are gate rows 4 rt .. 4 rt + 3 and rows 4..7 the matching
+// up rows; the lane of gate row r takes up row r from lane l + 16 and stores
+// silu(g) * u at h[slot][4 rt + r] (mlxcel-2178, "Problem / Background":
+// gate, up and down per layer, SwiGLU between them).
 template <int FMT, int NVV, int NVP>
 __device__ __forceinline__ void reduce_store(const KParams& p, const Entry& e, int rt, float* acc) {
   const int lane = threadIdx.x & 31;
   constexpr int M = kRows * NVP;
+  static_assert(M <= 32, "one value per lane group after the reduce-scatter");
+  constexpr int S = 32 / M;
   rs_step<M, 16>(acc, lane);
-  auto store = [&](int idx, float val) {
-    const int r = idx / NVP, v = idx % NVP;
-    const int row = rt * kRows + r;
-    if (v < NVV && row < p.N) {
-      const size_t o = (size_t)e.slot[v] * p.N + row;
-      if constexpr (FMT == MXFP4) {
-        reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(val);
-      } else {
-        reinterpret_cast<float*>(p.y)[o] = val;
-      }
+  const int idx = lane / S;
+  const int r = idx / NVP, v = idx % NVP;
+  if (p.flags & kFlagGlu) {
+    const float up = __shfl_xor_sync(0xffffffffu, acc[0], 16);   // row r + 4 (same vector) lives 16 lanes up
+    const int row = rt * (kRows / 2) + r;
+    if (lane % S == 0 && r < kRows / 2 && v < NVV && row < p.out_n) {
+      store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, silu_f32(acc[0]) * up);
     }
-  };
-  if constexpr (M <= 32) {
-    constexpr int S = 32 / M;
-    if (lane % S == 0) store(lane / S, acc[0]);
   } else {
-    store(2 * lane, acc[0]);
-    store(2 * lane + 1, acc[1]);
+    const int row = rt * kRows + r;
+    if (lane % S == 0 && v < NVV && row < p.out_n) store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, acc[0]);
   }
 }
 
@@ -595,12 +609,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p)
     for (int s = 0; s < nslots; ++s) {
       const int ex = s_ids[s];
       if (ex >= 0 && ex < p.n_experts) continue;
-      for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < p.N; row += gridDim.x * blockDim.x) {
-        if constexpr (FMT == MXFP4) {
-          reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)s * p.N + row] = __float2bfloat16_rn(0.f);
-        } else {
-          reinterpret_cast<float*>(p.y)[(size_t)s * p.N + row] = 0.f;
-        }
+      for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < p.out_n; row += gridDim.x * blockDim.x) {
+        store_out<FMT>(p, (size_t)s * p.out_n + row, 0.f);
       }
     }
   }
@@ -685,7 +695,8 @@ inline KParams make_params(const MatvecArgs& a) {
   p.y = a.y;
   p.dbg = a.dbg;
   for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i];
-  p.flags = a.flags;
+  p.flags = a.flags | (a.glu ? kFlagGlu : 0u);
+  p.out_n = a.out_n > 0 ? a.out_n : a.N;
   return p;
 }
 

@@ -5,6 +5,7 @@
 // three bytes, code j at bits [3j, 3j+3) of the little-endian 24-bit word.
 // The GPU layout is described in qmv_layout.h.
 #include <cstring>
+#include <vector>
 
 #include "qmv_layout.h"
 
@@ -132,6 +133,26 @@ void unpack_expert(const Geometry& g, const uint8_t* in, uint8_t* codes, uint8_t
       }
     }
   }
+}
+
+// Gate and up projections of one expert (each N x K, canonical) packed as one
+// matrix of 2 * round_up(N, 4) rows whose 8-row tile i holds gate rows
+// 4i..4i+3 then up rows 4i..4i+3 (rows past N are zero). `g` is the geometry
+// of that interleaved matrix.
+void pack_gate_up_expert(const Geometry& g, int N, const uint8_t* gate_codes, const uint8_t* gate_scales,
+                         const uint8_t* up_codes, const uint8_t* up_scales, uint8_t* out) {
+  const size_t rcb = (size_t)g.K * fmt_bits(g.fmt) / 8;
+  const size_t rsb = (size_t)(g.K / fmt_group(g.fmt));
+  std::vector<uint8_t> codes((size_t)g.N * rcb, 0), scales((size_t)g.N * rsb, 0);
+  for (int row = 0; row < g.N; ++row) {
+    const int tile = row / kRows, r = row % kRows;
+    const int src = tile * (kRows / 2) + (r % (kRows / 2));
+    if (src >= N) continue;
+    const bool up = r >= kRows / 2;
+    std::memcpy(&codes[(size_t)row * rcb], (up ? up_codes : gate_codes) + (size_t)src * rcb, rcb);
+    std::memcpy(&scales[(size_t)row * rsb], (up ? up_scales : gate_scales) + (size_t)src * rsb, rsb);
+  }
+  pack_expert(g, codes.data(), scales.data(), out);
 }
 
 }  // namespace qmv

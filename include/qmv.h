@@ -57,6 +57,19 @@ extern "C" {
 
 typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3 } qmv_fmt;
 
+/*
+ * Launch flags of qmv_dense_ex, qmv_moe_gather_ex and qmv_moe_gate_up_swiglu.
+ *
+ * QMV_FLAG_PREFETCH_INPUTS: the caller guarantees that the weights and the
+ * router ids were not written by the kernel immediately preceding this call
+ * in the stream (they were ready before it started). The kernel then reads the
+ * ids and starts streaming weight tiles while that kernel drains, and waits
+ * for it (programmatic dependent launch) only before reading the activations
+ * and writing outputs. Typical use: the up and down projections of a MoE
+ * layer, whose ids the router produced before the gate projection ran.
+ */
+#define QMV_FLAG_PREFETCH_INPUTS 1u
+
 /* Limits checked by every entry point. */
 #define QMV_MAX_NTOK 4      /* decode tokens per call */
 #define QMV_MAX_TOPK 8      /* experts per token */
@@ -181,19 +194,6 @@ int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32
 int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,
                    const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, void* stream);
 
-/*
- * Launch flags of qmv_dense_ex / qmv_moe_gather_ex.
- *
- * QMV_FLAG_PREFETCH_INPUTS: the caller guarantees that the weights and the
- * router ids were not written by the kernel immediately preceding this call
- * in the stream (they were ready before it started). The kernel then reads the
- * ids and starts streaming weight tiles while that kernel drains, and waits
- * for it (programmatic dependent launch) only before reading the activations
- * and writing outputs. Typical use: the up and down projections of a MoE
- * layer, whose ids the router produced before the gate projection ran.
- */
-#define QMV_FLAG_PREFETCH_INPUTS 1u
-
 /* qmv_dense with launch flags (QMV_FLAG_*); flags = 0 is qmv_dense. */
 int qmv_dense_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t ntok, void* y_dev,
                  uint32_t flags, void* stream);
@@ -202,6 +202,36 @@ int qmv_dense_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, in
 int qmv_moe_gather_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,
                       const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, uint32_t flags,
                       void* stream);
+
+/*
+ * Gate and up projections fused with the SwiGLU between them (one launch).
+ *
+ * Weights: the gate and up matrices of every expert (each N x K, same format,
+ * same codebook) packed together by qmv_pack_gate_up into one matrix of
+ * 2 * round_up(N, 4) rows per expert, at a stride of
+ * qmv_packed_gate_up_expert_bytes(desc). `desc` describes ONE projection
+ * (N rows, K columns, n_experts, format, codebook); the packer's inputs are
+ * the canonical codes and scales of the gate and up sets in the layout of
+ * qmv_pack_weights.
+ *
+ * qmv_moe_gate_up_swiglu computes, for t < ntok, j < top_k,
+ *   g = W_gate[ids[t][j]] . x[t],  u = W_up[ids[t][j]] . x[t],
+ *   h[t][j] = silu(g) * u,  silu(z) = z / (1 + exp(-z)),
+ * with g and u accumulated in fp32 and never rounded to bf16 (the gpt-oss
+ * MoE layer's gate, up and SwiGLU: "perf(rocm): add an mxfp4 arm to the
+ * warp-shared gather_qmv kernel for gpt-oss decode", "Problem / Background"
+ * and "Current Behavior"). x and h follow qmv_moe_gather with per_slot_x = 0:
+ * MXFP4: x bf16 [ntok][K], h bf16 [ntok][top_k][N]; CB formats: x q8_1, h fp32.
+ * An invalid id gives a zero row of h. flags: QMV_FLAG_* (see below).
+ * Errors: as qmv_moe_gather.
+ */
+size_t qmv_packed_gate_up_expert_bytes(const qmv_wdesc* desc);
+int qmv_pack_gate_up(const qmv_wdesc* desc, const uint8_t* gate_codes_host, const uint8_t* gate_scales_host,
+                     const uint8_t* up_codes_host, const uint8_t* up_scales_host, void* out_host,
+                     size_t out_bytes);
+int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w_gate_up_dev, const void* x_dev,
+                           const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* h_dev, uint32_t flags,
+                           void* stream);
 
 /*
  * SwiGLU between the gate/up and down gathers of a gpt-oss-style MoE layer:

@@ -427,3 +427,32 @@ def mxfp4_moe_layer(gate, up, down, x_bits, ids):
     h_rows = h_b.reshape(ntok * top_k, -1)
     y = mxfp4_moe_gather(down[0], down[1], h_rows, ids, per_slot=True)
     return {"g_bits": g_b, "u_bits": u_b, "h_bits": h_b, "h": h, "y": y, "h_rows_bits": h_rows}
+
+
+def moe_gate_up_swiglu(gate_matvec, up_matvec, n_experts: int, ids: np.ndarray, N: int):
+    """Fused gate/up/SwiGLU of one MoE layer: h[t, j] = silu(g) * u with
+    g = W_gate[ids[t, j]] . x[t] and u = W_up[ids[t, j]] . x[t] taken exactly
+    (float64, no intermediate rounding). `gate_matvec(e, t)` / `up_matvec(e, t)`
+    return one expert applied to token t's activation. An invalid id gives a
+    zero row. Returns (h, g, u), float64 [ntok, top_k, N].
+
+    The gate and up gathers share the token's activation and the SwiGLU sits
+    between them and the down gather [mlxcel-2178, "Problem / Background";
+    "Current Behavior": GptOssSwitchGLU]; fusing them changes no definition,
+    only where g and u live (registers instead of bf16 buffers).
+    """
+    g = moe_gather(gate_matvec, n_experts, ids, False, N)
+    u = moe_gather(up_matvec, n_experts, ids, False, N)
+    return swiglu(g, u), g, u
+
+
+def swiglu_tolerance(g, u, tol_g, tol_u):
+    """Propagate absolute bounds on g and u through h = silu(g) * u.
+
+    |d silu / dz| = |s(z) (1 + z (1 - s(z)))| <= 1.1 for all z (s the logistic
+    function), so |dh| <= 1.1 |u| tol_g + |silu(g)| tol_u + 1.1 tol_g tol_u.
+    """
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    return 1.1 * np.abs(u) * tol_g + np.abs(silu(g)) * tol_u + 1.1 * tol_g * tol_u
+

@@ -424,3 +424,81 @@ def test_dense_ex_prefetch_matches():
         qmv.qmv_dense_ex(m.desc, m.w, xq, 3, y1, qmv.QMV_FLAG_PREFETCH_INPUTS)
     s.synchronize()
     assert torch.equal(y0.view(torch.int32), y1.view(torch.int32))
+
+
+# ---------------------------------------------------------------------------
+# Gate/up/SwiGLU fusion
+# ---------------------------------------------------------------------------
+
+class GateUp:
+    """Gate and up expert sets packed together; only `experts` hold data."""
+
+    def __init__(self, fmt, N, K, E, experts, seed, lut=None):
+        self.fmt, self.N, self.K, self.E, self.lut = fmt, N, K, E, (list(lut) if lut else None)
+        self.desc = qmv.wdesc(fmt, N, K, E, lut)
+        one = qmv.wdesc(fmt, N, K, 1, lut)
+        eb = qmv.qmv_packed_gate_up_expert_bytes(self.desc)
+        self.w = torch.zeros(E * eb, dtype=torch.uint8, device=DEV)
+        g = qi.rng(seed)
+        bits, grp = qi.FORMAT_BITS[fmt], qi.FORMAT_GROUP[fmt]
+        self.cg, self.sg, self.cu, self.su = {}, {}, {}, {}
+        for e in sorted(set(int(v) for v in experts if 0 <= int(v) < E)):
+            self.cg[e], self.cu[e] = qi.codes(g, (N, K), bits), qi.codes(g, (N, K), bits)
+            self.sg[e], self.su[e] = qi.e8m0(g, (N, K // grp)), qi.e8m0(g, (N, K // grp))
+            p = qmv.qmv_pack_gate_up(one, oracle.pack_codes(fmt, self.cg[e][None]), self.sg[e][None],
+                                     oracle.pack_codes(fmt, self.cu[e][None]), self.su[e][None])
+            self.w[e * eb:(e + 1) * eb] = torch.from_numpy(p).to(DEV)
+
+    def matvecs(self, xin, q=None, d=None):
+        """(gate, up, gate |w x|, up |w x|) callables of (expert, token) for the oracle."""
+        if self.fmt == "mxfp4":
+            mv = lambda c, s: (lambda e, t: oracle.mxfp4_matvec(c[e], s[e], xin[t:t + 1])[0])
+            ab = lambda c, s: (lambda e, t: oracle.mxfp4_abs_products(c[e], s[e], xin[t:t + 1])[0])
+        else:
+            grp = qi.FORMAT_GROUP[self.fmt]
+            mv = lambda c, s: (lambda e, t: oracle.cb_matvec(c[e], s[e], self.lut, grp, q[t:t + 1], d[t:t + 1])[0])
+            ab = lambda c, s: (lambda e, t: oracle.cb_abs_products(c[e], s[e], self.lut, grp, q[t:t + 1],
+                                                                   d[t:t + 1])[0])
+        return mv(self.cg, self.sg), mv(self.cu, self.su), ab(self.cg, self.sg), ab(self.cu, self.su)
+
+
+def check_gate_up(m, ids, h_gpu, xin, q=None, d=None):
+    gm, um, ga, ua = m.matvecs(xin, q, d)
+    h, gv, uv = oracle.moe_gate_up_swiglu(gm, um, m.E, ids, m.N)
+    tg = oracle.moe_gather(ga, m.E, ids, False, m.N) * 1e-3
+    tu = oracle.moe_gather(ua, m.E, ids, False, m.N) * 1e-3
+    tol = oracle.swiglu_tolerance(gv, uv, tg, tu)
+    if m.fmt == "mxfp4":
+        tol = tol + np.abs(h) * 2.0 ** -8
+    err = np.abs(h_gpu - h)
+    bad = ~(err <= tol + 1e-30)
+    assert not bad.any(), f"{bad.sum()} fused outputs outside tolerance, first {np.argwhere(bad)[0]}"
+
+
+@pytest.mark.parametrize("N,ntok,top_k", [(2880, 1, 4), (516, 2, 4), (515, 1, 3), (64, 4, 2)])
+def test_mxfp4_gate_up_swiglu(N, ntok, top_k):
+    E, K = 32, 2880
+    g = qi.rng(N + ntok)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    if ntok > 1:
+        ids[1, 0] = ids[0, 0]           # shared expert
+        ids[-1, -1] = 77                # invalid id
+    m = GateUp("mxfp4", N, K, E, ids.reshape(-1), seed=N)
+    x = qi.normal_bf16_bits(g, (ntok, K))
+    h = torch.full((ntok, top_k, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_moe_gate_up_swiglu(m.desc, m.w, to_dev(x), to_dev(ids), ntok, top_k, h)
+    check_gate_up(m, ids, bf16_to_np(h), x)
+    assert status_clean()
+
+
+@pytest.mark.parametrize("fmt", ["cb2", "cb3", "cb4"])
+def test_cb_gate_up_swiglu(fmt):
+    E, N, K, ntok, top_k = 64, 2048, 7168 if fmt == "cb2" else 2048, 1, 4
+    g = qi.rng(7)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    m = GateUp(fmt, N, K, E, ids.reshape(-1), seed=8, lut=LUTS[fmt])
+    xq, q, d = quantize_on_gpu(qi.normal_f32(g, (ntok, K)))
+    h = torch.empty(ntok, top_k, N, dtype=torch.float32, device=DEV)
+    qmv.qmv_moe_gate_up_swiglu(m.desc, m.w, xq, to_dev(ids), ntok, top_k, h)
+    check_gate_up(m, ids, h.cpu().numpy().astype(np.float64), None, q, d)
+    assert status_clean()

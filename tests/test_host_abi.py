@@ -206,3 +206,32 @@ def test_unknown_launch_flags_rejected():
     assert rc == qmv.QMV_EINVAL
     d = qmv.wdesc("cb2", 64, 64)
     assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 2, 0) == qmv.QMV_EINVAL
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "cb3"])
+@pytest.mark.parametrize("N", [1, 8, 515, 516])
+def test_pack_gate_up_interleaves_rows(fmt, N):
+    """The fused gate/up layout is the plain layout of a 2*round_up(N,4)-row
+    matrix whose 8-row tile i holds gate rows 4i..4i+3 then up rows 4i..4i+3."""
+    E, K = 2, 96
+    g = qi.rng(N)
+    bits, grp = qi.FORMAT_BITS[fmt], qi.FORMAT_GROUP[fmt]
+    cg, cu = qi.codes(g, (E, N, K), bits), qi.codes(g, (E, N, K), bits)
+    sg, su = qi.e8m0(g, (E, N, K // grp)), qi.e8m0(g, (E, N, K // grp))
+    d = qmv.wdesc(fmt, N, K, E)
+    packed = qmv.qmv_pack_gate_up(d, oracle.pack_codes(fmt, cg), sg, oracle.pack_codes(fmt, cu), su)
+    R = 2 * ((N + 3) // 4 * 4)
+    dm = qmv.wdesc(fmt, R, K, E)
+    assert packed.nbytes == qmv.qmv_packed_bytes(dm) == E * qmv.qmv_packed_gate_up_expert_bytes(d)
+    c2, s2 = qmv.qmv_unpack_weights(dm, packed)
+    codes = oracle.unpack_codes(fmt, c2.reshape(E, R, -1))
+    scales = s2.reshape(E, R, -1)
+    for row in range(R):
+        tile, r = divmod(row, 8)
+        src = 4 * tile + r % 4
+        if src >= N:
+            assert not codes[:, row].any() and not scales[:, row].any()
+            continue
+        want_c, want_s = (cu, su) if r >= 4 else (cg, sg)
+        assert np.array_equal(codes[:, row], want_c[:, src])
+        assert np.array_equal(scales[:, row], want_s[:, src])

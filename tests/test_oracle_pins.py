@@ -371,10 +371,51 @@ def pin_silu():
     assert np.allclose(O.swiglu(g, u), u * g * special.expit(g), rtol=1e-15)
 
 
+def pin_swiglu_tolerance():
+    """The derivative bound used to propagate tolerances: max |silu'(z)| < 1.1,
+    and the propagated bound covers actual perturbations of g and u."""
+    special = pytest.importorskip("scipy.special")
+    z = np.linspace(-40, 40, 200001)
+    s = special.expit(z)
+    assert np.max(np.abs(s * (1 + z * (1 - s)))) < 1.1
+    g = qi.rng(20)
+    gg, uu = g.standard_normal(1000) * 5, g.standard_normal(1000) * 5
+    tg, tu = np.abs(g.standard_normal(1000)) * 0.1, np.abs(g.standard_normal(1000)) * 0.1
+    for sg in (-1, 1):
+        for su in (-1, 1):
+            dh = np.abs(O.swiglu(gg + sg * tg, uu + su * tu) - O.swiglu(gg, uu))
+            assert np.all(dh <= O.swiglu_tolerance(gg, uu, tg, tu) + 1e-12)
+
+
+def pin_fused_gate_up():
+    g = qi.rng(21)
+    E, N, K = 4, 8, 64
+    cg, cu = qi.codes(g, (E, N, K), 4), qi.codes(g, (E, N, K), 4)
+    sg, su = qi.e8m0(g, (E, N, K // 32)), qi.e8m0(g, (E, N, K // 32))
+    x = qi.normal_bf16_bits(g, (2, K))
+    ids = np.array([[1, 3], [0, 9]], dtype=np.int32)
+    h, gv, uv = O.moe_gate_up_swiglu(lambda e, t: O.mxfp4_matvec(cg[e], sg[e], x[t:t + 1])[0],
+                                     lambda e, t: O.mxfp4_matvec(cu[e], su[e], x[t:t + 1])[0], E, ids, N)
+    for t in range(2):
+        for j in range(2):
+            e = int(ids[t, j])
+            if e >= E:
+                assert np.all(h[t, j] == 0)
+                continue
+            xv = [bf_bf16(int(b)) for b in x[t]]
+            for n in range(N):
+                gx = sum(bf_e2m1(int(cg[e, n, k])) * bf_e8m0(int(sg[e, n, k // 32])) * xv[k] for k in range(K))
+                ux = sum(bf_e2m1(int(cu[e, n, k])) * bf_e8m0(int(su[e, n, k // 32])) * xv[k] for k in range(K))
+                assert abs(Fraction(float(gv[t, j, n])) - gx) <= abs(gx) * Fraction(1, 10 ** 12) + Fraction(1, 10 ** 300)
+                assert abs(Fraction(float(uv[t, j, n])) - ux) <= abs(ux) * Fraction(1, 10 ** 12) + Fraction(1, 10 ** 300)
+                want = float(gx) / (1 + np.exp(-float(gx))) * float(ux)
+                assert abs(h[t, j, n] - want) <= 1e-12 * abs(want) + 1e-300
+
+
 ALL_PINS = [pin_e2m1_table, pin_e2m1_stated_values, pin_e8m0, pin_bf16_conversions,
             pin_packings, pin_decode_contract, pin_brute_force_mxfp4, pin_brute_force_cb,
             pin_block_sums_exact, pin_identity_special_case, pin_q8_quantizer, pin_gather,
-            pin_silu]
+            pin_silu, pin_swiglu_tolerance, pin_fused_gate_up]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
