@@ -40,7 +40,8 @@ EXPORTS = (
     "qmv_packed_expert_bytes", "qmv_packed_bytes", "qmv_pack_weights", "qmv_unpack_weights",
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
     "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
-    "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
+    "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
+    "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
 
@@ -92,6 +93,8 @@ def _load() -> ctypes.CDLL:
         "qmv_packed_gate_up_expert_bytes": (SZ, [D]),
         "qmv_pack_gate_up": (ctypes.c_int, [D, P, P, P, P, P, SZ]),
         "qmv_moe_gate_up_swiglu": (ctypes.c_int, [D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
+        "qmv_moe_layer_workspace_bytes": (SZ, [D, I32, I32]),
+        "qmv_moe_layer": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, SZ, P, ctypes.c_uint32, P]),
         "qmv_moe_gather_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
@@ -253,6 +256,17 @@ def qmv_moe_gate_up_swiglu(desc: WDesc, w, x, ids, ntok: int, top_k: int, h, fla
                            stream=None) -> None:
     _check(lib.qmv_moe_gate_up_swiglu(ctypes.byref(desc), _ptr(w), _ptr(x), _ptr(ids), ntok, top_k, _ptr(h),
                                       int(flags), _stream(stream)))
+
+
+def qmv_moe_layer_workspace_bytes(gate_up_desc: WDesc, ntok: int, top_k: int) -> int:
+    return lib.qmv_moe_layer_workspace_bytes(ctypes.byref(gate_up_desc), ntok, top_k)
+
+
+def qmv_moe_layer(gate_up_desc: WDesc, w_gate_up, down_desc: WDesc, w_down, x, ids, ntok: int, top_k: int,
+                  workspace, y, flags: int = 0, stream=None) -> None:
+    _check(lib.qmv_moe_layer(ctypes.byref(gate_up_desc), _ptr(w_gate_up), ctypes.byref(down_desc), _ptr(w_down),
+                             _ptr(x), _ptr(ids), ntok, top_k, _ptr(workspace), _nbytes(workspace), _ptr(y),
+                             int(flags), _stream(stream)))
 
 
 def qmv_swiglu_bf16(g, u, h, n: int, stream=None) -> None:

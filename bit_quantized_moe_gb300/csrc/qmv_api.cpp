@@ -341,6 +341,51 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, 
                     "qmv_moe_gate_up_swiglu", flags, true);
 }
 
+size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gu, int32_t ntok, int32_t top_k) {
+  if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK) return 0;
+  const size_t slots = (size_t)ntok * top_k;
+  if (gu->fmt == QMV_MXFP4) return (slots * gu->N * 2 + 255) / 256 * 256;
+  if (gu->N % 32) return 0;
+  const size_t h32 = (slots * gu->N * 4 + 255) / 256 * 256;
+  return h32 + (slots * q8_vec_bytes(gu->N) + 255) / 256 * 256;
+}
+
+int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, const void* w_down, const void* x,
+                  const int32_t* ids, int32_t ntok, int32_t top_k, void* ws, size_t ws_bytes, void* y,
+                  uint32_t flags, void* stream) {
+  const char* name = "qmv_moe_layer";
+  int rc = check_desc(gu);
+  if (rc) return rc;
+  rc = check_desc(down);
+  if (rc) return rc;
+  if (!ids || !ws) return fail(QMV_EINVAL, "%s: ids and workspace must be non-NULL", name);
+  if ((gu->fmt == QMV_MXFP4) != (down->fmt == QMV_MXFP4))
+    return fail(QMV_EINVAL, "%s: gate/up and down must both be MXFP4 or both codebook formats", name);
+  if (down->K != gu->N) return fail(QMV_ESHAPE, "%s: down K=%d must equal gate/up N=%d", name, down->K, gu->N);
+  if (down->n_experts != gu->n_experts)
+    return fail(QMV_EINVAL, "%s: gate/up and down expert counts differ (%d, %d)", name, gu->n_experts, down->n_experts);
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK)
+    return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
+  const size_t need = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
+  if (ws_bytes < need) return fail(QMV_ESIZE, "%s: workspace %zu bytes < %zu", name, ws_bytes, need);
+  if (!aligned16(ws)) return fail(QMV_EALIGN, "%s: workspace must be 16-byte aligned", name);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint32_t down_flags = flags | QMV_FLAG_PREFETCH_INPUTS;
+  if (gu->fmt == QMV_MXFP4) {
+    rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, ws, nullptr, 0, s, name, flags, true);
+    if (rc) return rc;
+    return run_matvec(down, w_down, ws, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
+  }
+  const size_t slots = (size_t)ntok * top_k;
+  uint8_t* h32 = static_cast<uint8_t*>(ws);
+  uint8_t* hq = h32 + (slots * gu->N * 4 + 255) / 256 * 256;
+  rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, h32, nullptr, 0, s, name, flags, true);
+  if (rc) return rc;
+  cudaError_t e = launch_quantize_q8(reinterpret_cast<const float*>(h32), (int)slots, gu->N, hq, s);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return run_matvec(down, w_down, hq, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
+}
+
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
                          const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
                          size_t sums_bytes, void* stream) {

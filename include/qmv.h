@@ -234,6 +234,31 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w_gate_up_dev, con
                            void* stream);
 
 /*
+ * One MoE decode layer's expert FFN: fused gate/up/SwiGLU, then the down
+ * gather on the per-slot h (the gpt-oss layer of "perf(rocm): add an mxfp4
+ * arm to the warp-shared gather_qmv kernel for gpt-oss decode", "Problem /
+ * Background"; for the codebook formats the DS4 gate/up then down of
+ * "DS4 H200: rocmfp2_mix MoE matvec 3.31x + ROCmFP4 dense matvec 1.53x",
+ * "Caveats", with h quantized to q8_1 in between).
+ *   y[t][j] = W_down[ids[t][j]] . h[t][j],  h as qmv_moe_gate_up_swiglu.
+ * gate_up_desc: one projection (N, K); down_desc: (N_down, K = N). Both MXFP4
+ * or both codebook formats, same n_experts. x as qmv_moe_gate_up_swiglu.
+ * y: MXFP4 bf16 [ntok][top_k][N_down]; codebooks fp32.
+ * MXFP4: h is stored bf16 in the workspace (two launches). Codebooks: h fp32,
+ * then its q8_1 (three launches).
+ * workspace: caller-owned device scratch of at least
+ * qmv_moe_layer_workspace_bytes(gate_up_desc, ntok, top_k) bytes, 16-byte
+ * aligned; its contents on entry do not matter. Calls that share a workspace
+ * must be ordered on one stream.
+ * flags apply to the first launch; the down gather always prefetches its
+ * weights and ids (they were complete before the layer's first launch).
+ */
+size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gate_up_desc, int32_t ntok, int32_t top_k);
+int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, const qmv_wdesc* down_desc,
+                  const void* w_down_dev, const void* x_dev, const int32_t* ids_dev, int32_t ntok, int32_t top_k,
+                  void* workspace_dev, size_t workspace_bytes, void* y_dev, uint32_t flags, void* stream);
+
+/*
  * SwiGLU between the gate/up and down gathers of a gpt-oss-style MoE layer:
  * h[i] = silu(g[i]) * u[i], silu(z) = z / (1 + exp(-z)), bf16 in and out,
  * fp32 arithmetic, n elements ("perf(rocm): add an mxfp4 arm ...", "Problem /

@@ -502,3 +502,84 @@ def test_cb_gate_up_swiglu(fmt):
     qmv.qmv_moe_gate_up_swiglu(m.desc, m.w, xq, to_dev(ids), ntok, top_k, h)
     check_gate_up(m, ids, h.cpu().numpy().astype(np.float64), None, q, d)
     assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# One MoE layer: fused gate/up/SwiGLU, then down on the per-slot h
+# ---------------------------------------------------------------------------
+
+def _layer_expected(gu, down, ids, x=None, q=None, d=None):
+    """Oracle chain and the per-output bound for y. h differs from the GPU's
+    by the propagated SwiGLU bound plus its storage rounding (a bf16 ulp for
+    MXFP4, one q8_1 quantum of its block for the codebooks)."""
+    gm, um, ga, ua = gu.matvecs(x, q, d)
+    h, gv, uv = oracle.moe_gate_up_swiglu(gm, um, gu.E, ids, gu.N)
+    tol_h = oracle.swiglu_tolerance(gv, uv, oracle.moe_gather(ga, gu.E, ids, False, gu.N) * 1e-3,
+                                    oracle.moe_gather(ua, gu.E, ids, False, gu.N) * 1e-3)
+    ntok, top_k = ids.shape
+    rows = h.reshape(ntok * top_k, gu.N)
+    if gu.fmt == "mxfp4":
+        hb = oracle.f64_to_bf16_bits(rows)
+        hx = oracle.bf16_bits_to_f64(hb)
+        dh = tol_h.reshape(rows.shape) + np.abs(hx) * 2.0 ** -8 * 2
+        y = oracle.mxfp4_moe_gather(np.stack([down.codes.get(e, np.zeros((down.N, down.K), np.uint8)) for e in range(down.E)]),
+                                    np.stack([down.scales.get(e, np.zeros((down.N, down.K // 32), np.uint8)) for e in range(down.E)]),
+                                    hb, ids, True)
+    else:
+        hq, hd = oracle.q8_1_quantize(rows.astype(np.float32))
+        dq = oracle.f16_bits_to_f64(hd)
+        dh = tol_h.reshape(rows.shape) + np.repeat(dq, 32, axis=1) * 1.01
+        grp = qi.FORMAT_GROUP[down.fmt]
+        y = oracle.cb_moe_gather(np.stack([down.codes.get(e, np.zeros((down.N, down.K), np.uint8)) for e in range(down.E)]),
+                                 np.stack([down.scales.get(e, np.zeros((down.N, down.K // grp), np.uint8)) for e in range(down.E)]),
+                                 down.lut, grp, hq, hd, ids, True)
+    tol = np.zeros_like(y)
+    for t in range(ntok):
+        for j in range(top_k):
+            e, s = int(ids[t, j]), t * top_k + j
+            if not (0 <= e < down.E):
+                continue
+            if down.fmt == "mxfp4":
+                Wabs = np.abs(oracle.mxfp4_dequant(down.codes[e], down.scales[e]))
+                base = Wabs @ np.abs(oracle.bf16_bits_to_f64(hb[s]))
+            else:
+                Wabs = np.abs(oracle.cb_dequant(down.codes[e], down.scales[e], down.lut, grp))
+                base = Wabs @ np.abs(hq[s].astype(np.float64) * np.repeat(dq[s], 32))
+            tol[t, j] = 1e-3 * base + Wabs @ dh[s]
+    if down.fmt == "mxfp4":
+        tol = tol + np.abs(y) * 2.0 ** -8
+    return y, tol
+
+
+def test_mxfp4_moe_layer():
+    E, N, K, top_k = 32, 2880, 2880, 4
+    for ntok in (1, 2):
+        g = qi.rng(60 + ntok)
+        ids = qi.topk_ids(g, ntok, top_k, E)
+        gu = GateUp("mxfp4", N, K, E, ids.reshape(-1), seed=61)
+        down = Matrices("mxfp4", K, N, E, ids.reshape(-1), seed=62)
+        x = qi.normal_bf16_bits(g, (ntok, K))
+        ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k), dtype=torch.uint8, device=DEV)
+        y = torch.empty(ntok, top_k, K, dtype=torch.bfloat16, device=DEV)
+        qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, to_dev(x), to_dev(ids), ntok, top_k, ws, y)
+        want, tol = _layer_expected(gu, down, ids, x=x)
+        err = np.abs(bf16_to_np(y) - want)
+        assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert status_clean()
+
+
+def test_cb_moe_layer_ds4_shapes():
+    """CB2 gate/up 2048 x 7168, q8_1 of h, CB3 down 7168 x 2048 (the DS4 expert shapes)."""
+    E, top_k, ntok = 64, 4, 1
+    g = qi.rng(70)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    gu = GateUp("cb2", 2048, 7168, E, ids.reshape(-1), seed=71, lut=qi.LUT_CB2)
+    down = Matrices("cb3", 7168, 2048, E, ids.reshape(-1), seed=72, lut=qi.LUT_CB3)
+    xq, q, d = quantize_on_gpu(qi.normal_f32(g, (ntok, 7168)))
+    ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k), dtype=torch.uint8, device=DEV)
+    y = torch.empty(ntok, top_k, 7168, dtype=torch.float32, device=DEV)
+    qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xq, to_dev(ids), ntok, top_k, ws, y)
+    want, tol = _layer_expected(gu, down, ids, q=q, d=d)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - want)
+    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert status_clean()

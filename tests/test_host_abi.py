@@ -235,3 +235,18 @@ def test_pack_gate_up_interleaves_rows(fmt, N):
         want_c, want_s = (cu, su) if r >= 4 else (cg, sg)
         assert np.array_equal(codes[:, row], want_c[:, src])
         assert np.array_equal(scales[:, row], want_s[:, src])
+
+
+def test_moe_layer_argument_errors():
+    gu = qmv.wdesc("mxfp4", 2880, 2880, 32)
+    dn = qmv.wdesc("mxfp4", 2880, 2880, 32)
+    need = qmv.qmv_moe_layer_workspace_bytes(gu, 1, 4)
+    assert need == (4 * 2880 * 2 + 255) // 256 * 256
+    L = qmv.lib.qmv_moe_layer
+    B = qmv.ctypes.byref
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need - 16, FAKE, 0, 0) == qmv.QMV_ESIZE
+    bad = qmv.wdesc("mxfp4", 2880, 1024, 32)
+    assert L(B(gu), FAKE, B(bad), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_ESHAPE
+    cb = qmv.wdesc("cb3", 2880, 2880, 32)
+    assert L(B(gu), FAKE, B(cb), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, None, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
