@@ -4,9 +4,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one decode token through 24 gpt-oss-style MoE layers. Each layer
-gathers 4 of 32 experts for gate and up (2880 x 2880 MXFP4, shared bf16
-activation), applies SwiGLU, and gathers the same 4 experts of down (per-slot
-activation) -- 12 expert matrices, 52,876,800 weight bytes per layer. Router
+(qmv_moe_layer) gathers 4 of 32 experts for gate and up (2880 x 2880 MXFP4,
+shared bf16 activation) with SwiGLU fused into that launch, then gathers the
+same 4 experts of down (per-slot activation) -- 12 expert matrices,
+52,876,800 weight bytes per layer. Router
 ids are fresh each step. The weight bytes of a step (1.27 GB) exceed L2, so
 nothing is served from L2 across steps. `value` = weight bytes of all steps on
 all ranks / max-over-ranks device time (CUDA events, CUDA-graph replay).
@@ -265,18 +266,26 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
 
-    # --- weights: a pool of distinct packed experts replicated over 24 layers x 3 projections x 32 experts
+    # --- weights: pools of distinct packed experts (fused gate/up and down)
+    # replicated over the layers; content repeats, addresses do not.
     pool_n = 32
-    pool_canon, pool_scales, x_bits = make_pool(pool_n, qi.CONFIG1_GATE.seed)
-    desc_pool = qmv.wdesc("mxfp4", N, K, pool_n)
-    packed_pool = qmv.qmv_pack_weights(desc_pool, pool_canon, pool_scales)
-    desc = qmv.wdesc("mxfp4", N, K, E)
-    eb = qmv.qmv_packed_expert_bytes(desc)
-    pool_dev = torch.from_numpy(packed_pool).to(dev).view(pool_n, eb)
-    W = torch.empty(L * 3 * E, eb, dtype=torch.uint8, device=dev)
-    W.view(-1, pool_n, eb).copy_(pool_dev.unsqueeze(0).expand(L * 3 * E // pool_n, pool_n, eb))
-    W = W.view(L, 3, E * eb)
-    del pool_dev
+    g_canon, g_scales, x_bits = make_pool(pool_n, qi.CONFIG1_GATE.seed)
+    u_canon, u_scales, _ = make_pool(pool_n, qi.CONFIG1_UP.seed + 100)
+    d_canon, d_scales, _ = make_pool(pool_n, qi.CONFIG1_DOWN.seed + 200)
+    desc_gu = qmv.wdesc("mxfp4", N, K, E)
+    desc_dn = qmv.wdesc("mxfp4", K, N, E)
+    eb_gu = qmv.qmv_packed_gate_up_expert_bytes(desc_gu)
+    eb_dn = qmv.qmv_packed_expert_bytes(desc_dn)
+    pool_gu = torch.from_numpy(qmv.qmv_pack_gate_up(qmv.wdesc("mxfp4", N, K, pool_n), g_canon, g_scales,
+                                                    u_canon, u_scales)).to(dev).view(pool_n, eb_gu)
+    pool_dn = torch.from_numpy(qmv.qmv_pack_weights(qmv.wdesc("mxfp4", K, N, pool_n), d_canon,
+                                                    d_scales)).to(dev).view(pool_n, eb_dn)
+    W_gu = torch.empty(L * E, eb_gu, dtype=torch.uint8, device=dev)
+    W_gu.view(-1, pool_n, eb_gu).copy_(pool_gu.unsqueeze(0).expand(L * E // pool_n, pool_n, eb_gu))
+    W_dn = torch.empty(L * E, eb_dn, dtype=torch.uint8, device=dev)
+    W_dn.view(-1, pool_n, eb_dn).copy_(pool_dn.unsqueeze(0).expand(L * E // pool_n, pool_n, eb_dn))
+    W_gu, W_dn = W_gu.view(L, E * eb_gu), W_dn.view(L, E * eb_dn)
+    del pool_gu, pool_dn
 
     x_dev = torch.from_numpy(x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     total_steps = args.warmup + args.steps
@@ -284,29 +293,17 @@ def run_ours(args):
     ids_host = np.stack([np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(L)]) for _ in range(total_steps)])
     ids_all = torch.from_numpy(ids_host).to(dev)               # [steps][layers][1][4]
     ids_buf = torch.empty(L, 1, TOP_K, dtype=torch.int32, device=dev)
-    yg = torch.empty(L, 1, TOP_K, N, dtype=torch.bfloat16, device=dev)
-    yu = torch.empty_like(yg)
-    h = torch.empty_like(yg)
-    y = torch.empty_like(yg)
+    ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(desc_gu, 1, TOP_K), dtype=torch.uint8, device=dev)
+    y = torch.empty(L, 1, TOP_K, K, dtype=torch.bfloat16, device=dev)
 
-    def gather(w, xin, per_slot, ids, out, events):
-        if events is not None:
-            events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
-            events[-1][0].record()
-        # The step's weights and ids are never written by a kernel of the step
-        # (ids are copied in before it), so every gather may prefetch them
-        # while the preceding kernel drains.
-        qmv.qmv_moe_gather_ex(desc, w, xin, per_slot, ids, 1, TOP_K, out, qmv.QMV_FLAG_PREFETCH_INPUTS)
-        if events is not None:
-            events[-1][1].record()
-
-    def step(events=None):
-        """One decode token through all layers: gate, up, SwiGLU, down per layer."""
+    def step():
+        """One decode token through all layers (fused gate/up/SwiGLU, then down).
+        The step's weights and ids are never written by a kernel of the step
+        (ids are copied in before it), so every layer may prefetch them while
+        the preceding kernel drains."""
         for l in range(L):
-            gather(W[l, 0], x_dev, 0, ids_buf[l], yg[l], events)
-            gather(W[l, 1], x_dev, 0, ids_buf[l], yu[l], events)
-            qmv.qmv_swiglu_bf16(yg[l], yu[l], h[l], TOP_K * N)
-            gather(W[l, 2], h[l], 1, ids_buf[l], y[l], events)
+            qmv.qmv_moe_layer(desc_gu, W_gu[l], desc_dn, W_dn[l], x_dev, ids_buf[l], 1, TOP_K, ws, y[l],
+                              qmv.QMV_FLAG_PREFETCH_INPUTS)
 
     # eager warm-up (sets kernel attributes), then capture one step in a CUDA graph
     ids_buf.copy_(ids_all[0])
@@ -365,35 +362,18 @@ def run_ours(args):
     clocks["window_s"] = round(wall2 - wall0, 3)
     clocks["timed_s"] = round(wall1 - wall0, 3)
 
-    # --- dominant kernel: the 72 gather launches of a step captured alone in a
-    # CUDA graph (same weights, ids and outputs, no SwiGLU), replayed over the
-    # timed steps' ids; average launch duration = elapsed / launches.
-    gather_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gather_graph):
-        for l in range(L):
-            gather(W[l, 0], x_dev, 0, ids_buf[l], yg[l], None)
-            gather(W[l, 1], x_dev, 0, ids_buf[l], yu[l], None)
-            gather(W[l, 2], h[l], 1, ids_buf[l], y[l], None)
-    n_roof = min(args.steps, 100)
-    for i in range(3):
-        ids_buf.copy_(ids_all[i])
-        gather_graph.replay()
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record()
-    for i in range(n_roof):
-        ids_buf.copy_(ids_all[args.warmup + i])
-        gather_graph.replay()
-    g1.record()
-    torch.cuda.synchronize()
-    gather_ms = g0.elapsed_time(g1) / (n_roof * L * 3)
+    # --- dominant kernel: every launch of the step is matvec_kernel<MXFP4,1>
+    # (24 fused gate/up/SwiGLU gathers of 35.25 MB and 24 down gathers of
+    # 17.63 MB), so its average launch time is the step time over 2L launches
+    # and its average algorithmic bytes per launch are LAYER_BYTES / 2.
+    launch_ms = dt_max * 1e3 / args.steps / (2 * L)
     hbm, peak_kind = peaks()
-    achieved = GATHER_BYTES / (gather_ms / 1e3) / 1e9
+    achieved = (LAYER_BYTES / 2) / (launch_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": traffic_for_current_kernel(), "kernel": "matvec_kernel<MXFP4,1> (qmv_moe_gather)",
-                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "launch_us_mean": gather_ms * 1e3,
-                "launches_timed": n_roof * L * 3, "algorithmic_bytes_per_launch": GATHER_BYTES,
-                "timing": "CUDA graph of one step's 72 gather launches, events around the replays"}
+                "traffic": traffic_for_current_kernel(), "kernel": "matvec_kernel<MXFP4,1> (qmv_moe_layer)",
+                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "launch_us_mean": launch_ms * 1e3,
+                "launches_timed": args.steps * 2 * L, "algorithmic_bytes_per_launch": LAYER_BYTES // 2,
+                "timing": "CUDA events around the timed step graphs; every launch in them is this kernel"}
 
     # --- e2e: host buffers, h2d of x and ids, graph step, d2h of every layer's output
     x_host = torch.from_numpy(x_bits.view(np.int16)).pin_memory()
@@ -417,7 +397,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(pool_canon[:4], pool_scales[:4], x_bits)
+        cpu = cpu_baseline(g_canon[:4], g_scales[:4], x_bits)
 
     if rank == 0:
         line = {
@@ -431,10 +411,10 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "layers": L, "experts": E, "top_k": TOP_K, "N": N, "K": K,
                        "ntok": 1, "weight_bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2: 1.27 GB of expert weights per step, fresh ids every step",
-                       "launch": f"CUDA graph of {4 * L} kernels per step ({3 * L} gathers + {L} SwiGLU), programmatic dependent launch with weight/id prefetch",
+                       "launch": f"CUDA graph of {2 * L} kernels per step ({L} fused gate/up/SwiGLU gathers + {L} down gathers, qmv_moe_layer), programmatic dependent launch with weight/id prefetch",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": args.steps * L * 4, "cpu_baseline": cpu, "device_status": status,
+            "gpu_launches": args.steps * L * 2, "cpu_baseline": cpu, "device_status": status,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
