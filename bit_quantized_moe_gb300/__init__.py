@@ -28,6 +28,7 @@ QMV_EALIGN = -3
 QMV_ESIZE = -4
 QMV_ECUDA = -5
 QMV_FLAG_PREFETCH_INPUTS = 1
+QMV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 MXFP4, CB2, CB3, CB4 = 0, 1, 2, 3
 FORMATS = {"mxfp4": MXFP4, "cb2": CB2, "cb3": CB3, "cb4": CB4}
@@ -41,6 +42,7 @@ EXPORTS = (
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
     "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
     "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
+    "qmv_moe_layer_noalloc",
     "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
@@ -95,6 +97,7 @@ def _load() -> ctypes.CDLL:
         "qmv_moe_gate_up_swiglu": (ctypes.c_int, [D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_moe_layer_workspace_bytes": (SZ, [D, I32, I32]),
         "qmv_moe_layer": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, SZ, P, ctypes.c_uint32, P]),
+        "qmv_moe_layer_noalloc": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_moe_gather_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
@@ -267,6 +270,16 @@ def qmv_moe_layer(gate_up_desc: WDesc, w_gate_up, down_desc: WDesc, w_down, x, i
     _check(lib.qmv_moe_layer(ctypes.byref(gate_up_desc), _ptr(w_gate_up), ctypes.byref(down_desc), _ptr(w_down),
                              _ptr(x), _ptr(ids), ntok, top_k, _ptr(workspace), _nbytes(workspace), _ptr(y),
                              int(flags), _stream(stream)))
+
+
+def qmv_moe_layer_noalloc(gate_up_desc: WDesc, w_gate_up, down_desc: WDesc, w_down, x, ids, ntok: int, top_k: int,
+                          y, flags: int = 0, stream=None) -> None:
+    """qmv_moe_layer without a workspace, for callers that may not allocate
+    device memory: the scratch is a static array inside the library (see
+    include/qmv.h for its size, sharing and first-call rules)."""
+    _check(lib.qmv_moe_layer_noalloc(ctypes.byref(gate_up_desc), _ptr(w_gate_up), ctypes.byref(down_desc),
+                                     _ptr(w_down), _ptr(x), _ptr(ids), ntok, top_k, _ptr(y), int(flags),
+                                     _stream(stream)))
 
 
 def qmv_swiglu_bf16(g, u, h, n: int, stream=None) -> None:

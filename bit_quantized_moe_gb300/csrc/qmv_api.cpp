@@ -175,6 +175,16 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
 
 }  // namespace
 
+int record_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
 int device_sm_count() {
   const DevInfo* di = dev_info();
   return di ? di->sm_count : 1;

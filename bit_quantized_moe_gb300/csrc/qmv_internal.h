@@ -52,6 +52,9 @@ uint32_t status_cb2(int clear);
 uint32_t status_cb3(int clear);
 uint32_t status_cb4(int clear);
 
+// Sets the calling thread's qmv_last_error() message and returns `code`.
+int record_error(int code, const char* fmt, ...);
+
 // Per-device cached properties.
 int device_sm_count();
 size_t device_max_smem_optin();

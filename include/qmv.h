@@ -259,6 +259,32 @@ int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, cons
                   void* workspace_dev, size_t workspace_bytes, void* y_dev, uint32_t flags, void* stream);
 
 /*
+ * qmv_moe_layer for callers that cannot allocate device memory. (No
+ * counterpart on the pages this library follows; it exists for how the
+ * library is embedded.) Some callers may not allocate GPU memory while they
+ * decode: an inference server that gives the whole device to its own memory
+ * pool before serving, a plugin living in another application's CUDA context
+ * under a fixed budget, or code running while a stream is being captured,
+ * where allocating is not allowed. This entry point takes the same arguments
+ * as qmv_moe_layer minus the workspace and uses a static scratch array of
+ * QMV_NOALLOC_SCRATCH_BYTES bytes compiled into the library instead; it calls
+ * no allocator.
+ *  - Every GPU that loads the library holds the array until the process exits.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - A layer whose qmv_moe_layer_workspace_bytes exceeds the array is rejected
+ *    with QMV_ESIZE (use qmv_moe_layer with a workspace for it).
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero: every byte the layer reads from it
+ *    is written earlier in the same call. Calls that can overlap on the GPU
+ *    (other streams, other host threads) race on the array: order them.
+ */
+#define QMV_NOALLOC_SCRATCH_BYTES (1u << 20)
+int qmv_moe_layer_noalloc(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, const qmv_wdesc* down_desc,
+                          const void* w_down_dev, const void* x_dev, const int32_t* ids_dev, int32_t ntok,
+                          int32_t top_k, void* y_dev, uint32_t flags, void* stream);
+
+/*
  * SwiGLU between the gate/up and down gathers of a gpt-oss-style MoE layer:
  * h[i] = silu(g[i]) * u[i], silu(z) = z / (1 + exp(-z)), bf16 in and out,
  * fp32 arithmetic, n elements ("perf(rocm): add an mxfp4 arm ...", "Problem /
