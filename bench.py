@@ -4,10 +4,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one decode token through 24 gpt-oss-style MoE layers. Each layer
-(qmv_moe_layer) gathers 4 of 32 experts for gate and up (2880 x 2880 MXFP4,
-shared bf16 activation) with SwiGLU fused into that launch, then gathers the
-same 4 experts of down (per-slot activation) -- 12 expert matrices,
-52,876,800 weight bytes per layer. Router
+(qmv_moe_layer, two kernel launches) gathers 4 of 32 experts for gate and up
+(2880 x 2880 MXFP4, shared bf16 activation) with SwiGLU fused into that
+launch, then gathers the same 4 experts of down (per-slot activation) -- 12
+expert matrices, 52,876,800 weight bytes per layer. Router
 ids are fresh each step. The weight bytes of a step (1.27 GB) exceed L2, so
 nothing is served from L2 across steps. `value` = weight bytes of all steps on
 all ranks / max-over-ranks device time (CUDA events, CUDA-graph replay).
@@ -176,8 +176,8 @@ def kernel_source_digest() -> str:
 
 
 def traffic_for_current_kernel():
-    """DRAM bytes per gather launch from the committed ncu summary, if it was
-    taken on the current kernel sources; otherwise None."""
+    """DRAM bytes per launch of the step's kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; otherwise None."""
     import re
     p = os.path.join(ROOT, "profiles", "mxfp4_gather_2880_top4.md")
     if not os.path.exists(p):
@@ -293,7 +293,9 @@ def run_ours(args):
     ids_host = np.stack([np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(L)]) for _ in range(total_steps)])
     ids_all = torch.from_numpy(ids_host).to(dev)               # [steps][layers][1][4]
     ids_buf = torch.empty(L, 1, TOP_K, dtype=torch.int32, device=dev)
-    ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(desc_gu, 1, TOP_K), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(qmv.qmv_moe_layer_workspace_bytes(desc_gu, 1, TOP_K), dtype=torch.uint8, device=dev)
+    layer_flags = qmv.QMV_FLAG_PREFETCH_INPUTS
+    per_layer = 2
     y = torch.empty(L, 1, TOP_K, K, dtype=torch.bfloat16, device=dev)
 
     def step():
@@ -303,7 +305,7 @@ def run_ours(args):
         the preceding kernel drains."""
         for l in range(L):
             qmv.qmv_moe_layer(desc_gu, W_gu[l], desc_dn, W_dn[l], x_dev, ids_buf[l], 1, TOP_K, ws, y[l],
-                              qmv.QMV_FLAG_PREFETCH_INPUTS)
+                              layer_flags)
 
     # eager warm-up (sets kernel attributes), then capture one step in a CUDA graph
     ids_buf.copy_(ids_all[0])
@@ -363,16 +365,18 @@ def run_ours(args):
     clocks["timed_s"] = round(wall1 - wall0, 3)
 
     # --- dominant kernel: every launch of the step is matvec_kernel<MXFP4,1>
-    # (24 fused gate/up/SwiGLU gathers of 35.25 MB and 24 down gathers of
-    # 17.63 MB), so its average launch time is the step time over 2L launches
-    # and its average algorithmic bytes per launch are LAYER_BYTES / 2.
-    launch_ms = dt_max * 1e3 / args.steps / (2 * L)
+    # (L fused gate/up/SwiGLU gathers of 35.25 MB and L down gathers of
+    # 17.63 MB), so its average launch time is the step time over the step's
+    # 2L launches and its average algorithmic bytes per launch are
+    # LAYER_BYTES / 2.
+    launch_ms = dt_max * 1e3 / args.steps / (per_layer * L)
     hbm, peak_kind = peaks()
-    achieved = (LAYER_BYTES / 2) / (launch_ms / 1e3) / 1e9
+    bytes_per_launch = LAYER_BYTES // per_layer
+    achieved = bytes_per_launch / (launch_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic_for_current_kernel(), "kernel": "matvec_kernel<MXFP4,1> (qmv_moe_layer)",
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "launch_us_mean": launch_ms * 1e3,
-                "launches_timed": args.steps * 2 * L, "algorithmic_bytes_per_launch": LAYER_BYTES // 2,
+                "launches_timed": args.steps * per_layer * L, "algorithmic_bytes_per_launch": bytes_per_launch,
                 "timing": "CUDA events around the timed step graphs; every launch in them is this kernel"}
 
     # --- e2e: host buffers, h2d of x and ids, graph step, d2h of every layer's output
@@ -414,11 +418,196 @@ def run_ours(args):
                        "launch": f"CUDA graph of {2 * L} kernels per step ({L} fused gate/up/SwiGLU gathers + {L} down gathers, qmv_moe_layer), programmatic dependent launch with weight/id prefetch",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": args.steps * L * 2, "cpu_baseline": cpu, "device_status": status,
+            "gpu_launches": args.steps * L * per_layer, "cpu_baseline": cpu, "device_status": status,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Per-config measurements (--configs): every config of the workload set, the
+# same way as the headline line (CUDA-graph replay, inputs larger than L2,
+# CUDA events), one JSON line each. Not the default line.
+# ---------------------------------------------------------------------------
+
+L2_BYTES = 132 * 1000 * 1000
+
+
+def _replicated(qmv, torch, dev, desc_pool, pack, n_total: int, eb: int):
+    """A device buffer of n_total experts (eb bytes each): a packed pool of
+    distinct experts repeated; content repeats, addresses do not."""
+    pool = torch.from_numpy(pack()).to(dev).view(desc_pool.n_experts, eb)
+    w = torch.empty(n_total, eb, dtype=torch.uint8, device=dev)
+    reps = (n_total + desc_pool.n_experts - 1) // desc_pool.n_experts
+    w.copy_(pool.repeat(reps, 1)[:n_total])
+    return w
+
+
+def _graph_time(torch, calls, replays: int = 20):
+    """Seconds per replay of a CUDA graph of `calls` (median of 3 batches)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        calls()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    res = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(replays):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res.append(e0.elapsed_time(e1) / 1e3 / replays)
+    return statistics.median(res), s
+
+
+def run_configs(args):
+    import torch
+
+    import bit_quantized_moe_gb300 as qmv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm, peak_kind = peaks()
+    PF = qmv.QMV_FLAG_PREFETCH_INPUTS
+    g = qi.rng(77)
+    pool = 8
+
+    def emit(cfg, call, bytes_per_call, sec_per_call, extra=None):
+        gbs = bytes_per_call / sec_per_call / 1e9
+        line = {"config": cfg, "call": call, "us_per_call": sec_per_call * 1e6, "GB/s": gbs,
+                "frac_of_hbm_peak": gbs / hbm, "peak": hbm, "peak_kind": f"{peak_kind} hbm_gbs",
+                "weight_bytes_per_call": bytes_per_call, "status": qmv.qmv_device_status(clear=True)}
+        line.update(extra or {})
+        print(json.dumps(line), flush=True)
+
+    def canon(fmt, n, N_, K_):
+        gg = qi.rng(int(g.integers(1 << 30)))
+        return (qi.canonical_uniform_codes(gg, (n, N_), K_, qi.FORMAT_BITS[fmt]),
+                qi.e8m0(gg, (n, N_, K_ // qi.FORMAT_GROUP[fmt])))
+
+    def luts(fmt):
+        return {"cb2": qi.LUT_CB2, "cb3": qi.LUT_CB3, "cb4": qi.LUT_CB4}.get(fmt)
+
+    # --- config 0: dense MXFP4 2880 x 2880, 1 token, copies rotated past L2
+    d0 = qmv.wdesc("mxfp4", 2880, 2880, 1)
+    b0 = qmv.qmv_packed_bytes(d0)
+    n0 = -(-4 * L2_BYTES // b0)
+    c0, s0 = canon("mxfp4", pool, 2880, 2880)
+    W0 = _replicated(qmv, torch, dev, qmv.wdesc("mxfp4", 2880, 2880, pool),
+                     lambda: qmv.qmv_pack_weights(qmv.wdesc("mxfp4", 2880, 2880, pool), c0, s0), n0, b0)
+    x0 = torch.from_numpy(qi.normal_bf16_bits(g, (1, 2880)).view(np.int16)).to(dev).view(torch.bfloat16)
+    y0 = torch.empty(n0, 2880, dtype=torch.bfloat16, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_dense_ex(d0, W0[i], x0, 1, y0[i], PF) for i in range(n0)])
+    emit(0, "qmv_dense MXFP4 2880x2880 ntok=1", 4406400, t / n0, {"calls_per_graph": n0})
+    del W0
+
+    # --- configs 2 and 3 and the DS4 layer: E=256 resident expert sets, fresh ids per call
+    E2, top_k = 256, 4
+    dgu = qmv.wdesc("cb2", 2048, 7168, E2, luts("cb2"))
+    egu = qmv.qmv_packed_gate_up_expert_bytes(dgu)
+    cg, sg = canon("cb2", pool, 2048, 7168)
+    cu, su = canon("cb2", pool, 2048, 7168)
+    Wgu = _replicated(qmv, torch, dev, qmv.wdesc("cb2", 2048, 7168, pool, luts("cb2")),
+                      lambda: qmv.qmv_pack_gate_up(qmv.wdesc("cb2", 2048, 7168, pool, luts("cb2")), cg, sg, cu, su),
+                      E2, egu).view(-1)
+    ddn = qmv.wdesc("cb3", 7168, 2048, E2, luts("cb3"))
+    edn = qmv.qmv_packed_expert_bytes(ddn)
+    cd, sd = canon("cb3", pool, 7168, 2048)
+    Wdn = _replicated(qmv, torch, dev, qmv.wdesc("cb3", 7168, 2048, pool, luts("cb3")),
+                      lambda: qmv.qmv_pack_weights(qmv.wdesc("cb3", 7168, 2048, pool, luts("cb3")), cd, sd),
+                      E2, edn).view(-1)
+    C = 32
+    x2 = torch.from_numpy(qi.normal_f32(g, (1, 7168))).to(dev)
+    xq2 = torch.empty(qmv.qmv_act_q8_bytes(1, 7168), dtype=torch.uint8, device=dev)
+    qmv.qmv_quantize_act_q8(x2, 1, 7168, xq2)
+    ids2 = torch.from_numpy(np.stack([qi.topk_ids(g, 1, top_k, E2) for _ in range(C)])).to(dev)
+    h2 = torch.empty(C, 1, top_k, 2048, dtype=torch.float32, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_gate_up_swiglu(dgu, Wgu, xq2, ids2[i], 1, top_k, h2[i], PF)
+                                       for i in range(C)])
+    emit(2, "qmv_moe_gate_up_swiglu CB2 2048x7168 gate+up E=256 top4 ntok=1, q8_1 x", 8 * 4587520, t / C,
+         {"calls_per_graph": C})
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_gate_up_swiglu(dgu, Wgu, x2, ids2[i], 1, top_k, h2[i],
+                                                                  PF | qmv.QMV_FLAG_X_F32) for i in range(C)])
+    emit(2, "qmv_moe_gate_up_swiglu CB2 2048x7168 gate+up E=256 top4 ntok=1, fp32 x (QMV_FLAG_X_F32)",
+         8 * 4587520, t / C, {"calls_per_graph": C})
+    xqs = torch.empty(C, qmv.qmv_act_q8_bytes(1, 7168), dtype=torch.uint8, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_quantize_act_q8(x2, 1, 7168, xqs[i]) for i in range(C)])
+    emit(2, "qmv_quantize_act_q8 K=7168 ntok=1 (activation bytes, not weights)", 7168 * 4, t / C,
+         {"calls_per_graph": C})
+
+    C3 = 16
+    ids3 = np.stack([qi.topk_ids(g, 4, top_k, E2) for _ in range(C3)])
+    distinct = [len(set(r.reshape(-1).tolist())) for r in ids3]
+    ids3d = torch.from_numpy(ids3).to(dev)
+    xq3 = torch.empty(16, qmv.qmv_act_q8_bytes(1, 2048), dtype=torch.uint8, device=dev)
+    qmv.qmv_quantize_act_q8(torch.from_numpy(qi.normal_f32(g, (16, 2048))).to(dev), 16, 2048, xq3)
+    y3 = torch.empty(C3, 4, top_k, 7168, dtype=torch.float32, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_gather_ex(ddn, Wdn, xq3, 1, ids3d[i], 4, top_k, y3[i], PF)
+                                       for i in range(C3)])
+    emit(3, "qmv_moe_gather CB3 7168x2048 down E=256 top4 ntok=4 per-slot x", sum(distinct) * 6422528 / C3,
+         t / C3, {"calls_per_graph": C3, "distinct_experts_mean": sum(distinct) / C3})
+
+    # DS4 layer (CB2 gate/up -> SwiGLU -> q8_1 -> CB3 down), both launch structures
+    CL = 16
+    idsL = torch.from_numpy(np.stack([qi.topk_ids(g, 1, top_k, E2) for _ in range(CL)])).to(dev)
+    wsL = torch.zeros(qmv.qmv_moe_layer_workspace_bytes(dgu, 1, top_k), dtype=torch.uint8, device=dev)
+    yL = torch.empty(CL, 1, top_k, 7168, dtype=torch.float32, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgu, Wgu, ddn, Wdn, xq2, idsL[i], 1, top_k, wsL,
+                                                         yL[i], PF) for i in range(CL)])
+    emit("ds4-layer", "qmv_moe_layer CB2 gate/up + CB3 down E=256 top4 ntok=1 (2 launches)",
+         8 * 4587520 + 4 * 6422528, t / CL, {"calls_per_graph": CL})
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgu, Wgu, ddn, Wdn, x2, idsL[i], 1, top_k, wsL,
+                                                         yL[i], PF | qmv.QMV_FLAG_X_F32) for i in range(CL)])
+    emit("ds4-layer", "qmv_moe_layer CB2 gate/up + CB3 down E=256 top4 ntok=1, fp32 x (2 launches, no quantize launch)",
+         8 * 4587520 + 4 * 6422528, t / CL, {"calls_per_graph": CL})
+    del Wgu, Wdn
+
+    # --- config 4: dense CB4 7168x7168 and 2048x7168, ntok 1..4, copies rotated past L2
+    for (N4, K4) in qi.CONFIG4_SHAPES:
+        d4 = qmv.wdesc("cb4", N4, K4, 1, luts("cb4"))
+        b4 = qmv.qmv_packed_bytes(d4)
+        alg = N4 * K4 // 2 + N4 * (K4 // 32)
+        n4 = -(-4 * L2_BYTES // b4)
+        c4, s4 = canon("cb4", 2, N4, K4)
+        W4 = _replicated(qmv, torch, dev, qmv.wdesc("cb4", N4, K4, 2, luts("cb4")),
+                         lambda: qmv.qmv_pack_weights(qmv.wdesc("cb4", N4, K4, 2, luts("cb4")), c4, s4), n4, b4)
+        for ntok in qi.CONFIG4_NTOKS:
+            xq4 = torch.empty(qmv.qmv_act_q8_bytes(ntok, K4), dtype=torch.uint8, device=dev)
+            qmv.qmv_quantize_act_q8(torch.from_numpy(qi.normal_f32(g, (ntok, K4))).to(dev), ntok, K4, xq4)
+            y4 = torch.empty(n4, ntok, N4, dtype=torch.float32, device=dev)
+            t, _ = _graph_time(torch, lambda: [qmv.qmv_dense_ex(d4, W4[i], xq4, ntok, y4[i], PF) for i in range(n4)])
+            emit(4, f"qmv_dense CB4 {N4}x{K4} ntok={ntok}", alg, t / n4, {"calls_per_graph": n4})
+        del W4
+
+    # --- config 1 layer, both launch structures (the headline bench line uses the default)
+    dgm, ddm = qmv.wdesc("mxfp4", N, K, E), qmv.wdesc("mxfp4", K, N, E)
+    egm, edm = qmv.qmv_packed_gate_up_expert_bytes(dgm), qmv.qmv_packed_expert_bytes(ddm)
+    Lm = 24
+    gc, gs = canon("mxfp4", pool, N, K)
+    uc, us_ = canon("mxfp4", pool, N, K)
+    dc, ds = canon("mxfp4", pool, K, N)
+    Wgm = _replicated(qmv, torch, dev, qmv.wdesc("mxfp4", N, K, pool),
+                      lambda: qmv.qmv_pack_gate_up(qmv.wdesc("mxfp4", N, K, pool), gc, gs, uc, us_), Lm * E, egm)
+    Wdm = _replicated(qmv, torch, dev, qmv.wdesc("mxfp4", K, N, pool),
+                      lambda: qmv.qmv_pack_weights(qmv.wdesc("mxfp4", K, N, pool), dc, ds), Lm * E, edm)
+    Wgm, Wdm = Wgm.view(Lm, -1), Wdm.view(Lm, -1)
+    xm = torch.from_numpy(qi.normal_bf16_bits(g, (1, K)).view(np.int16)).to(dev).view(torch.bfloat16)
+    idsm = torch.from_numpy(np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(Lm)])).to(dev)
+    wsm = torch.zeros(qmv.qmv_moe_layer_workspace_bytes(dgm, 1, TOP_K), dtype=torch.uint8, device=dev)
+    ym = torch.empty(Lm, 1, TOP_K, K, dtype=torch.bfloat16, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgm, Wgm[l], ddm, Wdm[l], xm, idsm[l], 1, TOP_K, wsm,
+                                                         ym[l], PF) for l in range(Lm)])
+    emit(1, "qmv_moe_layer MXFP4 2880 E=32 top4 ntok=1 (2 launches)", LAYER_BYTES, t / Lm, {"calls_per_graph": Lm})
     return 0
 
 
@@ -434,6 +623,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers held on the device (the reported workload is 24; smaller for ncu captures)")
     ap.add_argument("--digest", action="store_true", help="print the kernel source digest and exit")
+    ap.add_argument("--configs", action="store_true",
+                    help="measure every config of the workload set (one JSON line per call type) and exit")
     args = ap.parse_args(argv)
     if args.digest:
         print(kernel_source_digest())
@@ -442,6 +633,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs:
+        return run_configs(args)
     return run_ours(args)
 
 

@@ -28,6 +28,7 @@ QMV_EALIGN = -3
 QMV_ESIZE = -4
 QMV_ECUDA = -5
 QMV_FLAG_PREFETCH_INPUTS = 1
+QMV_FLAG_X_F32 = 2
 QMV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 MXFP4, CB2, CB3, CB4 = 0, 1, 2, 3

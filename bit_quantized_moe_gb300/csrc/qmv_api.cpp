@@ -102,9 +102,10 @@ cudaError_t launch_for(const MatvecArgs& a) {
 // Rows of the gate/up-interleaved matrix of a projection with N rows.
 int gate_up_rows(int N) { return 2 * ((N + kRows / 2 - 1) / (kRows / 2) * (kRows / 2)); }
 
-int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_slot, const int32_t* ids,
-               int ntok, int top_k, void* y, int32_t* dbg, size_t dbg_bytes, cudaStream_t stream,
-               const char* name, uint32_t flags = 0, bool glu = false) {
+// Validates one matvec call and fills `a` (no launch).
+int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_slot, const int32_t* ids,
+                   int ntok, int top_k, void* y, int32_t* dbg, size_t dbg_bytes, cudaStream_t stream,
+                   const char* name, uint32_t flags, bool glu, MatvecArgs& a) {
   int rc = check_desc(desc_in);
   if (rc) return rc;
   qmv_wdesc glu_desc;
@@ -115,7 +116,10 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
     glu_desc.N = gate_up_rows(desc_in->N);
     desc = &glu_desc;
   }
-  if (flags & ~(uint32_t)QMV_FLAG_PREFETCH_INPUTS) return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32))
+    return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  if ((flags & QMV_FLAG_X_F32) && (desc->fmt == QMV_MXFP4 || dbg != nullptr))
+    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F32 applies to the codebook formats only (not block sums)", name);
   if (w == nullptr || x == nullptr || y == nullptr)
     return fail(QMV_EINVAL, "%s: weight, activation and output pointers must be non-NULL", name);
   if (ntok < 1 || ntok > QMV_MAX_NTOK) return fail(QMV_EINVAL, "%s: ntok=%d outside [1, %d]", name, ntok, QMV_MAX_NTOK);
@@ -137,7 +141,7 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
     if (dbg_bytes < need) return fail(QMV_ESIZE, "%s: sums buffer %zu bytes < %zu", name, dbg_bytes, need);
   }
   const Geometry g = make_geometry(desc->fmt, desc->N, desc->K);
-  MatvecArgs a;
+  a = MatvecArgs();
   a.fmt = desc->fmt;
   a.N = desc->N;
   a.K = desc->K;
@@ -153,7 +157,8 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
   a.y = y;
   a.dbg = dbg;
   lut_words(desc, a.lut);
-  a.flags = flags;
+  a.prefetch = (flags & QMV_FLAG_PREFETCH_INPUTS) != 0;
+  a.x_f32 = (flags & QMV_FLAG_X_F32) != 0;
   a.glu = glu;
   a.out_n = desc_in->N;
   a.stream = stream;
@@ -163,6 +168,16 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
   if (smem == 0 || smem > di->smem_optin)
     return fail(QMV_ESHAPE, "%s: %d activation vectors of K=%d do not fit in shared memory", name, a.nvec,
                 desc->K);
+  return QMV_OK;
+}
+
+int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_slot, const int32_t* ids,
+               int ntok, int top_k, void* y, int32_t* dbg, size_t dbg_bytes, cudaStream_t stream,
+               const char* name, uint32_t flags = 0, bool glu = false) {
+  MatvecArgs a;
+  const int rc = prepare_matvec(desc_in, w, x, per_slot, ids, ntok, top_k, y, dbg, dbg_bytes, stream, name, flags,
+                                glu, a);
+  if (rc) return rc;
   g_launch_stage = "";
   cudaError_t e = launch_for(a);
   if (e != cudaSuccess) {
@@ -351,13 +366,13 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, 
                     "qmv_moe_gate_up_swiglu", flags, true);
 }
 
+// Workspace of qmv_moe_layer: h (MXFP4: bf16; codebooks: fp32).
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gu, int32_t ntok, int32_t top_k) {
   if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK) return 0;
   const size_t slots = (size_t)ntok * top_k;
   if (gu->fmt == QMV_MXFP4) return (slots * gu->N * 2 + 255) / 256 * 256;
   if (gu->N % 32) return 0;
-  const size_t h32 = (slots * gu->N * 4 + 255) / 256 * 256;
-  return h32 + (slots * q8_vec_bytes(gu->N) + 255) / 256 * 256;
+  return (slots * gu->N * 4 + 255) / 256 * 256;
 }
 
 int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, const void* w_down, const void* x,
@@ -380,20 +395,14 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   if (ws_bytes < need) return fail(QMV_ESIZE, "%s: workspace %zu bytes < %zu", name, ws_bytes, need);
   if (!aligned16(ws)) return fail(QMV_EALIGN, "%s: workspace must be 16-byte aligned", name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const uint32_t down_flags = flags | QMV_FLAG_PREFETCH_INPUTS;
-  if (gu->fmt == QMV_MXFP4) {
-    rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, ws, nullptr, 0, s, name, flags, true);
-    if (rc) return rc;
-    return run_matvec(down, w_down, ws, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
-  }
-  const size_t slots = (size_t)ntok * top_k;
-  uint8_t* h32 = static_cast<uint8_t*>(ws);
-  uint8_t* hq = h32 + (slots * gu->N * 4 + 255) / 256 * 256;
-  rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, h32, nullptr, 0, s, name, flags, true);
+  // gate/up with SwiGLU into h, then down on the per-slot h. The down gather
+  // prefetches its weights and ids (they were complete before the layer's
+  // first launch). Codebooks: the down launch quantizes the fp32 h to q8_1 as
+  // it stages it.
+  rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, ws, nullptr, 0, s, name, flags, true);
   if (rc) return rc;
-  cudaError_t e = launch_quantize_q8(reinterpret_cast<const float*>(h32), (int)slots, gu->N, hq, s);
-  if (e != cudaSuccess) return cuda_fail(e, name);
-  return run_matvec(down, w_down, hq, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
+  const uint32_t down_flags = QMV_FLAG_PREFETCH_INPUTS | (gu->fmt == QMV_MXFP4 ? 0u : (uint32_t)QMV_FLAG_X_F32);
+  return run_matvec(down, w_down, ws, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
 }
 
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,

@@ -22,7 +22,8 @@ struct MatvecArgs {
   void* y = nullptr;
   int32_t* dbg = nullptr;         // integer block sums (CB formats) or null
   uint32_t lut[4] = {0, 0, 0, 0}; // 16 int8 codebook bytes
-  uint32_t flags = 0;             // QMV_FLAG_* of the call
+  bool prefetch = false;          // QMV_FLAG_PREFETCH_INPUTS
+  bool x_f32 = false;             // QMV_FLAG_X_F32: fp32 x, quantized to q8_1 in the kernel
   bool glu = false;               // gate/up-interleaved matrix, store silu(gate) * up
   int out_n = 0;                  // output rows per slot (0: N)
   cudaStream_t stream = nullptr;

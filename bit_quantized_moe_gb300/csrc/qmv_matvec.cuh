@@ -38,8 +38,12 @@
 
 namespace qmv {
 
+// One CTA of kWarps warps per SM, each warp with a ring of kStages tiles: 30
+// tiles (130 KB) in flight per SM, enough to request a whole 2880 x 2880
+// top-4 gather's share of weights at once.
 constexpr int kWarps = 6;        // warps per CTA
 constexpr int kStages = 3;       // shared-memory stages per warp (3 chunks cover K <= 3072)
+constexpr int kCtasPerSm = 2;
 constexpr int kMaxEntries = 32;  // ntok * top_k <= 4 * 8
 constexpr int kMaxDevices = 64;
 
@@ -71,6 +75,7 @@ struct KParams {
 // KParams::flags
 constexpr uint32_t kFlagPrefetch = 1u;   // weights and ids are not written by the preceding kernel
 constexpr uint32_t kFlagGlu = 2u;        // gate/up-interleaved matrix: store silu(gate) * up
+constexpr uint32_t kFlagXF32 = 4u;       // codebooks: x is fp32, quantized to q8_1 while staged
 
 // Largest number of activation vectors one work item applies a tile to.
 template <int FMT>
@@ -96,7 +101,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32
   const uint32_t xinv_bytes = (fmt == MXFP4) ? nvec * (uint32_t)(K / 32) * 4u : 0u;
   L.ring_off = round_up_u32(L.xinv_off + xinv_bytes, 128);
   L.bar_off = L.ring_off + kWarps * kStages * full_tile;
-  L.ent_off = round_up_u32(L.bar_off + (kWarps * kStages + 1) * 8, 16);
+  L.ent_off = round_up_u32(L.bar_off + kWarps * kStages * 8, 16);
   L.total = L.ent_off + kMaxEntries * (uint32_t)sizeof(Entry);
   return L;
 }
@@ -105,81 +110,124 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32
 // Work list
 // ---------------------------------------------------------------------------
 
+// Work list, built by the 32 lanes of one warp (lane s = routed slot s):
+// entries in order of their first slot, an expert's slots grouped NV at a time
+// (repeated experts share one tile stream for up to NV vectors). Unused vec /
+// slot positions repeat the entry's first member. Also copies the ids to
+// s_ids. Returns the entry count on every lane.
 template <int NV>
-__device__ int build_entries(const KParams& p, const int* ids, Entry* ent) {
-  int n = 0;
+__device__ int build_entries_warp(const KParams& p, Entry* ent, int* s_ids) {
+  const int lane = threadIdx.x & 31;
   if (p.ids == nullptr) {
-    for (int t = 0; t < p.ntok; t += NV) {
-      Entry& e = ent[n++];
+    const int n = (p.ntok + NV - 1) / NV;
+    if (lane < n) {
+      const int t = lane * NV;
+      Entry e;
       e.expert = 0;
       e.nv = min(NV, p.ntok - t);
-      for (int i = 0; i < 4; ++i) {
-        const int tt = t + min(i, e.nv - 1);
-        e.vec[i] = tt;
-        e.slot[i] = tt;
-      }
+      for (int i = 0; i < 4; ++i) e.vec[i] = e.slot[i] = t + min(i, e.nv - 1);
+      ent[lane] = e;
     }
+    __syncwarp();
     return n;
   }
-  for (int t = 0; t < p.ntok; ++t) {
-    for (int j = 0; j < p.top_k; ++j) {
-      const int s = t * p.top_k + j;
-      const int ex = ids[s];
-      if (ex < 0 || ex >= p.n_experts) continue;
-      const int v = p.per_slot ? s : t;
-      int f = -1;
-      for (int i = 0; i < n; ++i) {
-        if (ent[i].expert == ex && ent[i].nv < NV) {
-          f = i;
-          break;
-        }
-      }
-      if (f < 0) {
-        f = n++;
-        ent[f].expert = ex;
-        ent[f].nv = 0;
-        for (int i = 0; i < 4; ++i) {
-          ent[f].vec[i] = v;
-          ent[f].slot[i] = s;
-        }
-      }
-      Entry& e = ent[f];
-      e.vec[e.nv] = v;
-      e.slot[e.nv] = s;
-      e.nv += 1;
+  const int nslots = p.ntok * p.top_k;
+  const bool in = lane < nslots;
+  const int ex = in ? p.ids[lane] : -1;
+  if (in) s_ids[lane] = ex;
+  const bool valid = in && ex >= 0 && ex < p.n_experts;
+  // invalid slots get keys no valid id or other slot can have
+  const unsigned key = valid ? (unsigned)ex : (0x80000000u | (unsigned)lane);
+  const unsigned match = __match_any_sync(0xffffffffu, key);
+  const int r = __popc(match & ((1u << lane) - 1u));   // rank among the slots of this expert
+  const int c = r / NV, m = r % NV;                    // chunk of NV slots, position in it
+  const unsigned leaders = __ballot_sync(0xffffffffu, valid && m == 0);
+  unsigned rest = match;                               // drop the c * NV earlier slots
+  for (int i = 0; i < c * NV; ++i) rest &= rest - 1u;
+  const int leader_lane = __ffs(rest) - 1;             // first slot of this chunk
+  const int eid = __popc(leaders & ((1u << leader_lane) - 1u));
+  const int v = p.per_slot ? lane : lane / p.top_k;
+  if (valid && m == 0) {
+    ent[eid].expert = ex;
+    ent[eid].nv = min(NV, __popc(match) - c * NV);
+    for (int i = 0; i < 4; ++i) {
+      ent[eid].vec[i] = v;
+      ent[eid].slot[i] = lane;
     }
   }
-  return n;
+  __syncwarp();
+  if (valid && m != 0) {
+    ent[eid].vec[m] = v;
+    ent[eid].slot[m] = lane;
+  }
+  __syncwarp();
+  return __popc(leaders);
 }
 
 // ---------------------------------------------------------------------------
 // Tile loads
 // ---------------------------------------------------------------------------
 
+// A warp's tiles come from one or two "phases" (the items of one matrix each),
+// streamed back to back through the same ring: tile q of the warp's sequence
+// is tile q of phase 0 if q < ph0.nq, else tile q - ph0.nq of phase 1.
+struct PhaseSeq {
+  const KParams* p;   // the matrix (points into kernel parameter space)
+  const Entry* ent;   // its work list
+  int first;          // this warp's first item; it then takes every nw-th
+  int n_items;        // items in the whole list
+  int nq;             // tiles this warp streams in this phase
+};
+
 struct WarpPipe {
   uint32_t ring;      // shared address of this warp's stage 0
   uint32_t bars;      // shared address of this warp's mbarrier 0
   const uint8_t* ring_ptr;
-  int gw, nw, n_items;
+  uint32_t stage_bytes;
+  int nw;             // warps in the grid
+  PhaseSeq ph0, ph1;  // ph1.nq == 0 when there is one phase
   uint64_t policy;
 };
 
-// Issues the copy of the tile at position q of this warp's sequence
-// (item = gw + (q / chunks) * nw, chunk = q % chunks) into stage q % kStages.
-__device__ __forceinline__ void issue_tile(const KParams& p, const Entry* ent, const WarpPipe& wp,
-                                           int q) {
-  const int item = wp.gw + (q / p.chunks) * wp.nw;
-  if (item >= wp.n_items) return;
-  const int c = q % p.chunks;
+__device__ __forceinline__ int warp_item_count(int first, int n_items, int nw) {
+  return first < n_items ? (n_items - first + nw - 1) / nw : 0;
+}
+
+__device__ __forceinline__ PhaseSeq make_phase(const KParams* p, const Entry* ent, int first, int n_items,
+                                               int nw) {
+  PhaseSeq ph;
+  ph.p = p;
+  ph.ent = ent;
+  ph.first = first;
+  ph.n_items = n_items;
+  ph.nq = warp_item_count(first, n_items, nw) * p->chunks;
+  return ph;
+}
+
+// Copies tile t of phase `ph` (item = first + (t / chunks) * nw, chunk =
+// t % chunks) into ring stage qs % kStages.
+__device__ __forceinline__ void issue_phase_tile(const WarpPipe& wp, const PhaseSeq& ph, int t, int qs) {
+  const KParams& p = *ph.p;
+  const int item = ph.first + (t / p.chunks) * wp.nw;
+  const int c = t % p.chunks;
   const int rt = item % p.row_tiles;
-  const Entry& e = ent[item / p.row_tiles];
+  const Entry& e = ph.ent[item / p.row_tiles];
   const uint8_t* src = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)rt * p.rowtile +
                        (uint64_t)c * p.full_tile;
   const uint32_t bytes = (c == p.chunks - 1) ? p.last_tile : p.full_tile;
-  const int s = q % kStages;
+  const int s = qs % kStages;
   const uint32_t bar = wp.bars + 8u * s;
   mbar_arrive_expect_tx(bar, bytes);
-  bulk_copy_g2s_hint(wp.ring + (uint32_t)s * p.full_tile, src, bytes, bar, wp.policy);
+  bulk_copy_g2s_hint(wp.ring + (uint32_t)s * wp.stage_bytes, src, bytes, bar, wp.policy);
+}
+
+// Issues the copy of tile q of this warp's sequence, if there is one.
+__device__ __forceinline__ void issue_tile(const WarpPipe& wp, int q) {
+  if (q < wp.ph0.nq) {
+    issue_phase_tile(wp, wp.ph0, q, q);
+  } else if (q - wp.ph0.nq < wp.ph1.nq) {
+    issue_phase_tile(wp, wp.ph1, q - wp.ph0.nq, q);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -254,49 +302,151 @@ __device__ __forceinline__ float pow2f(int e) {
   return (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 }
 
+// Activation staging. Every thread issues the global loads of up to kStageU
+// units (a group, a block or 16 bytes) before it converts or stores any of
+// them: at the start of a launch the loads queue behind the weight tiles just
+// requested, so each extra dependent round of loads costs a full queued round
+// trip.
+constexpr int kStageU = 2;
+
 // MXFP4 activations are staged once per CTA: each 32-element group (one E8M0
 // group of the weights) is scaled by 2^s, s chosen so that the group's largest
-// magnitude lands in [2^14, 2^15), and stored as f16 in place of the bf16
-// input; xinv holds 2^-s. A bf16 value v of the group is then exact in f16
-// whenever |v| >= max|group| * 2^-31, so every product w * x' (E2M1 times
-// f16) and its fp32 accumulation match fp32 arithmetic on the bf16 input, and
-// dot * 2^-s undoes the shift exactly. One thread converts one group.
-__device__ __forceinline__ void stage_x_mxfp4(uint8_t* xs, float* xinv, int nvec, int K, uint32_t vec_bytes) {
+// magnitude lands in [2^14, 2^15), and stored as f16; xinv holds 2^-s. A bf16
+// value v of the group is then exact in f16 whenever |v| >= max|group| * 2^-31,
+// so every product w * x' (E2M1 times f16) and its fp32 accumulation match
+// fp32 arithmetic on the bf16 input, and dot * 2^-s undoes the shift exactly.
+// One thread converts one group (64 bytes of bf16).
+__device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* dst_bytes, float* xinv_slot) {
+  uint32_t m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = w[2 * i] & 0x7fff7fffu, b = w[2 * i + 1] & 0x7fff7fffu;
+    m8[i] = max(max(a & 0xffffu, a >> 16), max(b & 0xffffu, b >> 16));
+  }
+  const uint32_t mx = max(max(max(m8[0], m8[1]), max(m8[2], m8[3])), max(max(m8[4], m8[5]), max(m8[6], m8[7])));
+  int sh = 0;
+  if (mx != 0 && mx < 0x7f80u) {
+    const int ex = (int)(mx >> 7);
+    const int lg = (ex != 0) ? ex - 127 : -133 + (31 - __clz((int)(mx & 0x7fu)));   // floor(log2 max)
+    sh = 14 - lg;                                                                  // in [-113, 147]
+  }
+  const float m1 = pow2f(sh > 127 ? 127 : sh);
+  const float m2 = pow2f(sh > 127 ? sh - 127 : 0);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float lo = __fmul_rn(__fmul_rn(__uint_as_float(w[i] << 16), m1), m2);
+    const float hi = __fmul_rn(__fmul_rn(__uint_as_float(w[i] & 0xffff0000u), m1), m2);
+    const __half2 h2 = __floats2half2_rn(lo, hi);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(dst_bytes);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  *xinv_slot = pow2f(-sh);
+}
+
+__device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, int nvec, int K,
+                                              uint32_t vec_bytes) {
   const int groups = K / 32;
-  for (int gi = threadIdx.x; gi < nvec * groups; gi += blockDim.x) {
-    const int v = gi / groups, g = gi % groups;
-    uint4* xv = reinterpret_cast<uint4*>(xs + (size_t)v * vec_bytes + (size_t)g * 64);
-    uint32_t w[16];
+  const int n = nvec * groups;
+  for (int g0 = threadIdx.x; g0 < n; g0 += kStageU * blockDim.x) {
+    uint32_t w[kStageU][16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = xv[q];
-      w[4 * q] = u.x; w[4 * q + 1] = u.y; w[4 * q + 2] = u.z; w[4 * q + 3] = u.w;
-    }
-    uint32_t m8[8];
+    for (int u = 0; u < kStageU; ++u) {
+      const int gi = g0 + u * blockDim.x;
+      if (gi < n) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(gi / groups) * vec_bytes +
+                                                          (size_t)(gi % groups) * 64);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t a = w[2 * i] & 0x7fff7fffu, b = w[2 * i + 1] & 0x7fff7fffu;
-      m8[i] = max(max(a & 0xffffu, a >> 16), max(b & 0xffffu, b >> 16));
-    }
-    const uint32_t mx = max(max(max(m8[0], m8[1]), max(m8[2], m8[3])), max(max(m8[4], m8[5]), max(m8[6], m8[7])));
-    int sh = 0;
-    if (mx != 0 && mx < 0x7f80u) {
-      const int ex = (int)(mx >> 7);
-      const int lg = (ex != 0) ? ex - 127 : -133 + (31 - __clz((int)(mx & 0x7fu)));   // floor(log2 max)
-      sh = 14 - lg;                                                                  // in [-113, 147]
-    }
-    const float m1 = pow2f(sh > 127 ? 127 : sh);
-    const float m2 = pow2f(sh > 127 ? sh - 127 : 0);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float lo = __fmul_rn(__fmul_rn(__uint_as_float(w[i] << 16), m1), m2);
-      const float hi = __fmul_rn(__fmul_rn(__uint_as_float(w[i] & 0xffff0000u), m1), m2);
-      const __half2 h2 = __floats2half2_rn(lo, hi);
-      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = src[q];
+          w[u][4 * q] = v.x; w[u][4 * q + 1] = v.y; w[u][4 * q + 2] = v.z; w[u][4 * q + 3] = v.w;
+        }
+      }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) xv[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-    xinv[gi] = pow2f(-sh);
+    for (int u = 0; u < kStageU; ++u) {
+      const int gi = g0 + u * blockDim.x;
+      if (gi < n) {
+        convert_group_mxfp4(w[u], xs + (size_t)(gi / groups) * vec_bytes + (size_t)(gi % groups) * 64, xinv + gi);
+      }
+    }
+  }
+}
+
+// q8_1 quantization of fp32 vectors straight into the shared-memory
+// activation layout (codebook formats with kFlagXF32): one thread per
+// 32-element block, amax = max|x|, d = amax / 127,
+// q = round_half_away(x * (1 / d)) clamped to +-127, d stored as fp16 (RNE);
+// the same IEEE-rounded fp32 operations as the standalone quantizer, so the
+// result equals quantizing first and passing q8_1.
+__device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t* out, int K, int blk) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  uint32_t qw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float r = roundf(__fmul_rn(f[4 * i + j], id));
+      r = fminf(fmaxf(r, -127.0f), 127.0f);
+      word |= ((uint32_t)(uint8_t)(int8_t)(int)r) << (8 * j);
+    }
+    qw[i] = word;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)blk * 32);
+  dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+  dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+  reinterpret_cast<__half*>(out + K)[blk] = __float2half_rn(d);
+}
+
+__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, int nvec, int K, uint32_t vec_bytes) {
+  const int blocks = K / 32;
+  const int n = nvec * blocks;
+  for (int b0 = threadIdx.x; b0 < n; b0 += kStageU * blockDim.x) {
+    float f[kStageU][32];
+#pragma unroll
+    for (int u = 0; u < kStageU; ++u) {
+      const int bi = b0 + u * blockDim.x;
+      if (bi < n) {
+        const float4* src = reinterpret_cast<const float4*>(x + (size_t)(bi / blocks) * K + (size_t)(bi % blocks) * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = src[i];
+          f[u][4 * i] = v.x; f[u][4 * i + 1] = v.y; f[u][4 * i + 2] = v.z; f[u][4 * i + 3] = v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kStageU; ++u) {
+      const int bi = b0 + u * blockDim.x;
+      if (bi < n) quantize_block_q8(f[u], xs + (size_t)(bi / blocks) * vec_bytes, K, bi % blocks);
+    }
+  }
+}
+
+// Codebook activations (q8_1 vectors) are copied to shared memory as they are,
+// four 16-byte loads per thread in flight.
+__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, int nvec, uint32_t vec_bytes) {
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(xs);
+  const int n = (int)((size_t)nvec * vec_bytes / 16);
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) v[u] = src[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n) dst[i] = v[u];
+    }
   }
 }
 
@@ -509,8 +659,8 @@ __device__ __forceinline__ void reduce_store(const KParams& p, const Entry& e, i
 // ---------------------------------------------------------------------------
 
 template <int FMT, int NVV, bool DBG>
-__device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, const Entry& e, int rt,
-                                         int& q, const WarpPipe& wp, const uint8_t* xs, const float* xinv) {
+__device__ __forceinline__ bool run_item(const KParams& p, const Entry& e, int rt, int& q, const WarpPipe& wp,
+                                         const uint8_t* xs, const float* xinv) {
   constexpr int NVP = (NVV == 3) ? 4 : NVV;
   const int lane = threadIdx.x & 31;
   float acc[kRows * NVP];
@@ -522,7 +672,7 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, con
     bool ok = mbar_wait_bounded(wp.bars + 8u * s, parity, kWaitLimitNs);
     if (!__all_sync(0xffffffffu, ok)) return false;
     const int L = (c == p.chunks - 1) ? p.last_lanes : 32;
-    const uint8_t* st = wp.ring_ptr + (size_t)s * p.full_tile;
+    const uint8_t* st = wp.ring_ptr + (size_t)s * wp.stage_bytes;
     if (lane < L) {
       if constexpr (FMT == MXFP4) {
         chunk_mxfp4<NVV, NVP>(p, e, c, L, st, xs, xinv, acc);
@@ -532,14 +682,48 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry* ent, con
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) issue_tile(p, ent, wp, q + kStages);
+    if (lane == 0) issue_tile(wp, q + kStages);
   }
   reduce_store<FMT, NVV, NVP>(p, e, rt, acc);
   return true;
 }
 
+// All items of one phase of this warp. False if a tile wait gave up.
 template <int FMT, int NV, bool DBG>
-__global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p) {
+__device__ __forceinline__ bool run_phase(const KParams& p, const PhaseSeq& ph, int& q, const WarpPipe& wp,
+                                          const uint8_t* xs, const float* xinv) {
+  for (int item = ph.first; item < ph.n_items; item += wp.nw) {
+    const Entry& e = ph.ent[item / p.row_tiles];
+    const int rt = item % p.row_tiles;
+    bool ok = true;
+    switch (e.nv) {
+      case 1: ok = run_item<FMT, 1, DBG>(p, e, rt, q, wp, xs, xinv); break;
+      case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG>(p, e, rt, q, wp, xs, xinv); break;
+      case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG>(p, e, rt, q, wp, xs, xinv); break;
+      case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG>(p, e, rt, q, wp, xs, xinv); break;
+      default: break;
+    }
+    if (!ok) return false;
+  }
+  return true;
+}
+
+// After a failed wait: let every copy this warp still has in flight (tiles
+// q .. q + kStages - 1 of its sequence) land, bounded, before the CTA's shared
+// memory can be released.
+__device__ __forceinline__ void drain_ring(const WarpPipe& wp, int q) {
+  const int lane = threadIdx.x & 31;
+  const int total = wp.ph0.nq + wp.ph1.nq;
+  for (int qq = q; qq < min(total, q + kStages); ++qq) {
+    const int s = qq % kStages;
+    if (!mbar_wait_bounded(wp.bars + 8u * s, (uint32_t)(qq / kStages) & 1u, kDrainLimitNs)) {
+      if (lane == 0) set_status(kStatusDrain);
+    }
+  }
+}
+
+template <int FMT, int NV, bool DBG>
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) matvec_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -552,9 +736,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p)
   __shared__ int s_nent;
 
   __shared__ int s_ids[kMaxEntries];
-  const uint32_t xbar = smem_addr(&bars[kWarps * kStages]);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kWarps * kStages + 1; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
   }
   // Programmatic dependent launch. Activations may be produced by the kernel
@@ -566,41 +749,35 @@ __global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p)
   // the ids and the first weight tiles are fetched while the preceding kernel
   // drains.
   const bool early = (p.flags & kFlagPrefetch) != 0;
-  auto issue_x = [&]() {
-    const uint32_t xbytes = (uint32_t)p.nvec * p.x_vec_bytes;
-    mbar_arrive_expect_tx(xbar, xbytes);
-    for (int v = 0; v < p.nvec; ++v) {
-      bulk_copy_g2s(smem_addr(xs + (size_t)v * p.x_vec_bytes), p.x + (size_t)v * p.x_vec_bytes,
-                    p.x_vec_bytes, xbar);
-    }
-  };
   if (!early) pdl_wait();
   if (warp == 0) {
-    if (!early && lane == 0) issue_x();
-    const int nslots = p.ids ? p.ntok * p.top_k : 0;
-    if (lane < nslots) s_ids[lane] = p.ids[lane];
-    __syncwarp();
-    if (lane == 0) s_nent = build_entries<NV>(p, s_ids, ent);
+    const int n = build_entries_warp<NV>(p, ent, s_ids);
+    if (lane == 0) s_nent = n;
   }
   __syncthreads();
 
   WarpPipe wp;
   // Items are dealt to CTAs first (item i -> CTA i % gridDim.x), so every CTA,
   // and with a full grid every SM, gets the same number of items within one.
-  wp.gw = blockIdx.x + gridDim.x * warp;
   wp.nw = gridDim.x * kWarps;
-  wp.n_items = s_nent * p.row_tiles;
-  wp.ring_ptr = ring + (size_t)warp * kStages * p.full_tile;
+  wp.stage_bytes = p.full_tile;
+  wp.ring_ptr = ring + (size_t)warp * kStages * wp.stage_bytes;
   wp.ring = smem_addr(wp.ring_ptr);
   wp.bars = smem_addr(&bars[warp * kStages]);
   wp.policy = l2_evict_first_policy();
-  if (lane == 0) {
-    for (int q = 0; q < kStages; ++q) issue_tile(p, ent, wp, q);
+  wp.ph0 = make_phase(&p, ent, blockIdx.x + gridDim.x * warp, s_nent * p.row_tiles, wp.nw);
+  wp.ph1 = wp.ph0;
+  wp.ph1.nq = 0;
+  // Stage-major issue order (every warp's first tile, then every warp's
+  // second, ...) so that each warp's first tile arrives early in the burst.
+  for (int q = 0; q < kStages; ++q) {
+    if (lane == 0) issue_tile(wp, q);
+    __syncthreads();
   }
-  if (early) {
-    pdl_wait();
-    if (threadIdx.x == 0) issue_x();
-  }
+  if (early) pdl_wait();
+  // Dependents are released only after this kernel's own wait, so when one
+  // starts, every kernel before this one is complete (what
+  // QMV_FLAG_PREFETCH_INPUTS relies on).
   pdl_launch_dependents();
 
   // Gather slots with an invalid id produce zero rows.
@@ -615,47 +792,21 @@ __global__ void __launch_bounds__(kWarps * 32, 2) matvec_kernel(const KParams p)
     }
   }
 
-  bool ok = mbar_wait_bounded(xbar, 0, kWaitLimitNs);
-  if (!__all_sync(0xffffffffu, ok)) {
-    if (lane == 0) set_status(kStatusWaitX);
-    if (!mbar_wait_bounded(xbar, 0, kDrainLimitNs) && lane == 0) set_status(kStatusDrain);
-    ok = false;
-  }
+  // Activations: plain 16-byte loads by every thread (they do not queue
+  // behind the tile copies), converted on the way for MXFP4.
   if constexpr (FMT == MXFP4) {
-    // every thread reaches this barrier: a warp whose x wait failed still
-    // takes part, then skips its work items below
-    if (ok) stage_x_mxfp4(xs, xinv, p.nvec, p.K, p.x_vec_bytes);
-    __syncthreads();
+    stage_x_mxfp4(p.x, xs, xinv, p.nvec, p.K, p.x_vec_bytes);
+  } else if (p.flags & kFlagXF32) {
+    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, p.nvec, p.K, p.x_vec_bytes);
+  } else {
+    stage_x_copy(p.x, xs, p.nvec, p.x_vec_bytes);
   }
+  __syncthreads();
 
   int q = 0;
-  if (ok) {
-    for (int item = wp.gw; item < wp.n_items; item += wp.nw) {
-      const Entry& e = ent[item / p.row_tiles];
-      const int rt = item % p.row_tiles;
-      switch (e.nv) {
-        case 1: ok = run_item<FMT, 1, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
-        case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
-        case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
-        case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG>(p, ent, e, rt, q, wp, xs, xinv); break;
-        default: break;
-      }
-      if (!ok) {
-        if (lane == 0) set_status(kStatusWaitTile);
-        break;
-      }
-    }
-  }
-  if (!ok) {
-    // Let every copy this warp issued land (bounded) before the CTA's shared
-    // memory can be released.
-    const int total = ((wp.n_items - wp.gw + wp.nw - 1) / wp.nw) * p.chunks;
-    for (int qq = q; qq < min(total, q + kStages); ++qq) {
-      const int s = qq % kStages;
-      if (!mbar_wait_bounded(wp.bars + 8u * s, (uint32_t)(qq / kStages) & 1u, kDrainLimitNs)) {
-        if (lane == 0) set_status(kStatusDrain);
-      }
-    }
+  if (!run_phase<FMT, NV, DBG>(p, wp.ph0, q, wp, xs, xinv)) {
+    if (lane == 0) set_status(kStatusWaitTile);
+    drain_ring(wp, q);
   }
 }
 
@@ -695,7 +846,7 @@ inline KParams make_params(const MatvecArgs& a) {
   p.y = a.y;
   p.dbg = a.dbg;
   for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i];
-  p.flags = a.flags | (a.glu ? kFlagGlu : 0u);
+  p.flags = (a.prefetch ? kFlagPrefetch : 0u) | (a.glu ? kFlagGlu : 0u) | (a.x_f32 ? kFlagXF32 : 0u);
   p.out_n = a.out_n > 0 ? a.out_n : a.N;
   return p;
 }
@@ -756,8 +907,8 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   // Upper bound on work items: every routed pair its own entry.
   const int entries_max = a.ids ? a.ntok * a.top_k : (a.ntok + want_nv - 1) / want_nv;
   const long items = (long)entries_max * p.row_tiles;
-  // One wave on every SM; no CTA without an item.
-  long grid = (long)device_sm_count() * per_sm;
+  // One wave, kCtasPerSm per SM; no CTA without an item.
+  long grid = (long)device_sm_count() * (per_sm < kCtasPerSm ? per_sm : kCtasPerSm);
   if (grid > items) grid = items;
   if (grid < 1) grid = 1;
 

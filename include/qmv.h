@@ -58,7 +58,8 @@ extern "C" {
 typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3 } qmv_fmt;
 
 /*
- * Launch flags of qmv_dense_ex, qmv_moe_gather_ex and qmv_moe_gate_up_swiglu.
+ * Launch flags of qmv_dense_ex, qmv_moe_gather_ex, qmv_moe_gate_up_swiglu and
+ * qmv_moe_layer.
  *
  * QMV_FLAG_PREFETCH_INPUTS: the caller guarantees that the weights and the
  * router ids were not written by the kernel immediately preceding this call
@@ -69,6 +70,17 @@ typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3 } qmv_fmt;
  * layer, whose ids the router produced before the gate projection ran.
  */
 #define QMV_FLAG_PREFETCH_INPUTS 1u
+
+/*
+ * QMV_FLAG_X_F32 (codebook formats): x_dev holds fp32 activations [nvec][K]
+ * (nvec as for the q8_1 buffer it replaces) instead of q8_1. Every CTA
+ * quantizes them to q8_1 while staging them in shared memory, with exactly
+ * the arithmetic of qmv_quantize_act_q8, so the outputs equal those of
+ * qmv_quantize_act_q8 followed by the call, one launch fewer ("DS4 H200:
+ * rocmfp2_mix MoE matvec 3.31x ...", "Caveats": the separate q8_1 quantize
+ * launch per matvec). Not valid for MXFP4 or qmv_debug_block_sums.
+ */
+#define QMV_FLAG_X_F32 2u
 
 /* Limits checked by every entry point. */
 #define QMV_MAX_NTOK 4      /* decode tokens per call */
@@ -244,14 +256,16 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w_gate_up_dev, con
  * gate_up_desc: one projection (N, K); down_desc: (N_down, K = N). Both MXFP4
  * or both codebook formats, same n_experts. x as qmv_moe_gate_up_swiglu.
  * y: MXFP4 bf16 [ntok][top_k][N_down]; codebooks fp32.
- * MXFP4: h is stored bf16 in the workspace (two launches). Codebooks: h fp32,
- * then its q8_1 (three launches).
+ * Two launches: the fused gate/up/SwiGLU gather stores h in the workspace
+ * (MXFP4 bf16, codebooks fp32), then the down gather reads the per-slot h
+ * (codebooks: it quantizes h to q8_1 while staging it, as QMV_FLAG_X_F32).
  * workspace: caller-owned device scratch of at least
  * qmv_moe_layer_workspace_bytes(gate_up_desc, ntok, top_k) bytes, 16-byte
  * aligned; its contents on entry do not matter. Calls that share a workspace
  * must be ordered on one stream.
- * flags apply to the first launch; the down gather always prefetches its
- * weights and ids (they were complete before the layer's first launch).
+ * flags apply to the gate/up launch (QMV_FLAG_X_F32: a codebook layer's x is
+ * fp32); the down gather always prefetches its weights and ids (they were
+ * complete before the layer's first launch).
  */
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gate_up_desc, int32_t ntok, int32_t top_k);
 int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, const qmv_wdesc* down_desc,
@@ -316,7 +330,7 @@ int qmv_debug_dequant(const qmv_wdesc* desc, const void* w_dev, int32_t expert, 
 
 /*
  * Device-side status: bit flags set by kernels whose bounded waits gave up:
- * 1 activation copy, 2 weight tile copy, 4 copy still in flight when giving
+ * 1 (not used), 2 weight tile copy, 4 copy still in flight when giving
  * up, 8 the wait probe. No kernel here waits on another kernel, so bits 1-4
  * indicate a lost asynchronous copy. Synchronizes the device; clear != 0
  * resets the flags.

@@ -433,7 +433,7 @@ def test_dense_ex_prefetch_matches():
 class GateUp:
     """Gate and up expert sets packed together; only `experts` hold data."""
 
-    def __init__(self, fmt, N, K, E, experts, seed, lut=None):
+    def __init__(self, fmt, N, K, E, experts, seed, lut=None, scale_lo=120, scale_hi=130):
         self.fmt, self.N, self.K, self.E, self.lut = fmt, N, K, E, (list(lut) if lut else None)
         self.desc = qmv.wdesc(fmt, N, K, E, lut)
         one = qmv.wdesc(fmt, N, K, 1, lut)
@@ -444,7 +444,8 @@ class GateUp:
         self.cg, self.sg, self.cu, self.su = {}, {}, {}, {}
         for e in sorted(set(int(v) for v in experts if 0 <= int(v) < E)):
             self.cg[e], self.cu[e] = qi.codes(g, (N, K), bits), qi.codes(g, (N, K), bits)
-            self.sg[e], self.su[e] = qi.e8m0(g, (N, K // grp)), qi.e8m0(g, (N, K // grp))
+            self.sg[e] = qi.e8m0(g, (N, K // grp), scale_lo, scale_hi)
+            self.su[e] = qi.e8m0(g, (N, K // grp), scale_lo, scale_hi)
             p = qmv.qmv_pack_gate_up(one, oracle.pack_codes(fmt, self.cg[e][None]), self.sg[e][None],
                                      oracle.pack_codes(fmt, self.cu[e][None]), self.su[e][None])
             self.w[e * eb:(e + 1) * eb] = torch.from_numpy(p).to(DEV)
@@ -582,4 +583,160 @@ def test_cb_moe_layer_ds4_shapes():
     want, tol = _layer_expected(gu, down, ids, q=q, d=d)
     err = np.abs(y.cpu().numpy().astype(np.float64) - want)
     assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Layers across format pairs, token counts and routing edge cases
+# ---------------------------------------------------------------------------
+
+LAYER_PAIRS = [("mxfp4", "mxfp4", 2880, 2880, 32), ("cb2", "cb3", 2048, 7168, 64), ("cb4", "cb4", 1024, 2048, 16)]
+
+
+def _layer_case(fmt_gu, fmt_dn, N, K, E, ntok, top_k, seed):
+    g = qi.rng(seed)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    if ntok > 1:
+        ids[1, 0] = ids[0, 0]       # an expert shared by two tokens
+        ids[-1, -1] = -1            # an invalid id: zero output row
+    gu = GateUp(fmt_gu, N, K, E, ids.reshape(-1), seed=seed + 1, lut=LUTS.get(fmt_gu))
+    down = Matrices(fmt_dn, K, N, E, ids.reshape(-1), seed=seed + 2, lut=LUTS.get(fmt_dn))
+    if fmt_gu == "mxfp4":
+        x = qi.normal_bf16_bits(g, (ntok, K))
+        return ids, gu, down, x, to_dev(x), None, None, None, torch.bfloat16
+    xf = qi.normal_f32(g, (ntok, K))
+    xin, q, d = quantize_on_gpu(xf)
+    return ids, gu, down, None, xin, q, d, to_dev(xf), torch.float32
+
+
+@pytest.mark.parametrize("pair", LAYER_PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+@pytest.mark.parametrize("ntok,top_k", [(1, 4), (2, 4), (4, 2)])
+def test_layer_format_pairs(pair, ntok, top_k):
+    """qmv_moe_layer against the oracle chain; codebook layers also from fp32
+    x (QMV_FLAG_X_F32), which must equal the q8_1 input bit for bit."""
+    fmt_gu, fmt_dn, N, K, E = pair
+    ids, gu, down, x, xin, q, d, xf, dt = _layer_case(fmt_gu, fmt_dn, N, K, E, ntok, top_k, 300 + ntok * 10 + top_k)
+    ids_d = to_dev(ids)
+    ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k), dtype=torch.uint8, device=DEV)
+    y = torch.full((ntok, top_k, K), 7.0, dtype=dt, device=DEV)
+    qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xin, ids_d, ntok, top_k, ws, y)
+    want, tol = _layer_expected(gu, down, ids, x=x, q=q, d=d)
+    got = bf16_to_np(y) if dt == torch.bfloat16 else y.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    if xf is not None:
+        y2 = torch.full_like(y, -7.0)
+        qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xf, ids_d, ntok, top_k, ws, y2, qmv.QMV_FLAG_X_F32)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+    assert status_clean()
+
+
+def test_layer_many_slots():
+    """32 routed slots (4 tokens x top-8), repeated experts and invalid ids."""
+    E, N, K, ntok, top_k = 16, 512, 1024, 4, 8
+    g = qi.rng(420)
+    ids = np.stack([g.permutation(E)[:top_k] for _ in range(ntok)]).astype(np.int32)
+    ids[3, 7] = E          # invalid
+    ids[2, 0] = -5         # invalid
+    gu = GateUp("mxfp4", N, K, E, ids.reshape(-1), seed=421)
+    down = Matrices("mxfp4", K, N, E, ids.reshape(-1), seed=422)
+    x = qi.normal_bf16_bits(g, (ntok, K))
+    ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k), dtype=torch.uint8, device=DEV)
+    y = torch.full((ntok, top_k, K), 5.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, to_dev(x), to_dev(ids), ntok, top_k, ws, y)
+    want, tol = _layer_expected(gu, down, ids, x=x)
+    got = bf16_to_np(y)
+    assert np.all(got[3, 7] == 0) and np.all(got[2, 0] == 0)
+    err = np.abs(got - want)
+    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert status_clean()
+
+
+def test_layer_chain_graph_stream_prefetch():
+    """Consecutive layers sharing one workspace, launched on a side stream
+    (programmatic dependent launch) with QMV_FLAG_PREFETCH_INPUTS and replayed
+    from a CUDA graph, as a decode step runs them, each layer's x the previous
+    layer's output: every replay gives exactly the eager legacy-stream chain
+    (no dependent launch, no prefetch)."""
+    E, N, K, top_k, L = 8, 1024, 1024, 4, 4
+    g = qi.rng(430)
+    layers = []
+    for l in range(L):
+        ids = qi.topk_ids(g, 1, top_k, E)
+        # scales around 2^-7 keep every layer's output O(1) through the chain
+        gu = GateUp("mxfp4", N, K, E, range(E), seed=431 + l, scale_lo=118, scale_hi=122)
+        down = Matrices("mxfp4", K, N, E, range(E), seed=441 + l, scale_lo=118, scale_hi=122)
+        layers.append((gu, down, to_dev(ids)))
+    x = to_dev(qi.normal_bf16_bits(g, (1, K)))
+    nbytes = qmv.qmv_moe_layer_workspace_bytes(layers[0][0].desc, 1, top_k)
+
+    def chain(y, ws, flags, stream):
+        for l, (gu, down, ids_d) in enumerate(layers):
+            xin = x if l == 0 else y[l - 1, 0, 0].view(1, K)
+            qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xin, ids_d, 1, top_k, ws, y[l], flags, stream=stream)
+
+    y_ref = torch.empty(L, 1, top_k, K, dtype=torch.bfloat16, device=DEV)
+    chain(y_ref, torch.empty(nbytes, dtype=torch.uint8, device=DEV), 0, 0)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y_ref.float()).all()
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    y = torch.empty_like(y_ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain(y, ws, qmv.QMV_FLAG_PREFETCH_INPUTS, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        chain(y, ws, qmv.QMV_FLAG_PREFETCH_INPUTS, s)
+    for _ in range(3):
+        y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# QMV_FLAG_X_F32: fp32 activations quantized to q8_1 inside the matvec launch
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,N,K", [("cb2", 2048, 7168), ("cb3", 515, 2080), ("cb4", 1024, 7168)])
+@pytest.mark.parametrize("ntok", [1, 3, 4])
+def test_x_f32_dense_equals_quantize_then_call(fmt, N, K, ntok):
+    g = qi.rng(500 + ntok)
+    m = Matrices(fmt, N, K, 1, [0], seed=501, lut=LUTS[fmt])
+    xf = qi.normal_f32(g, (ntok, K))
+    xf[0, :32] = 0.0                      # an all-zero block: d = 0
+    xf[-1, 64] = 1e4                      # a block dominated by one value
+    xq, _, _ = quantize_on_gpu(xf)
+    y1 = torch.empty(ntok, N, dtype=torch.float32, device=DEV)
+    y2 = torch.full_like(y1, 3.0)
+    qmv.qmv_dense(m.desc, m.w, xq, ntok, y1)
+    qmv.qmv_dense_ex(m.desc, m.w, to_dev(xf), ntok, y2, qmv.QMV_FLAG_X_F32)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert status_clean()
+
+
+@pytest.mark.parametrize("per_slot", [0, 1])
+def test_x_f32_gather_equals_quantize_then_call(per_slot):
+    E, N, K, ntok, top_k = 64, 7168, 2048, 4, 4
+    g = qi.rng(510 + per_slot)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    ids[2, 1] = 99
+    m = Matrices("cb3", N, K, E, ids.reshape(-1), seed=511, lut=LUTS["cb3"])
+    nvec = ntok * top_k if per_slot else ntok
+    xf = qi.normal_f32(g, (nvec, K))
+    xq, _, _ = quantize_on_gpu(xf)
+    y1 = torch.empty(ntok, top_k, N, dtype=torch.float32, device=DEV)
+    y2 = torch.full_like(y1, 3.0)
+    ids_d = to_dev(ids)
+    qmv.qmv_moe_gather(m.desc, m.w, xq, per_slot, ids_d, ntok, top_k, y1)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, to_dev(xf), per_slot, ids_d, ntok, top_k, y2, qmv.QMV_FLAG_X_F32)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert torch.all(y2[2, 1] == 0)
     assert status_clean()

@@ -205,7 +205,7 @@ def test_unknown_launch_flags_rejected():
     rc = qmv.lib.qmv_moe_gather_ex(qmv.ctypes.byref(d), FAKE, FAKE, 0, FAKE, 1, 4, FAKE, 6, 0)
     assert rc == qmv.QMV_EINVAL
     d = qmv.wdesc("cb2", 64, 64)
-    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 2, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 4, 0) == qmv.QMV_EINVAL
 
 
 @pytest.mark.parametrize("fmt", ["mxfp4", "cb3"])
@@ -242,6 +242,8 @@ def test_moe_layer_argument_errors():
     dn = qmv.wdesc("mxfp4", 2880, 2880, 32)
     need = qmv.qmv_moe_layer_workspace_bytes(gu, 1, 4)
     assert need == (4 * 2880 * 2 + 255) // 256 * 256
+    cbd = qmv.wdesc("cb2", 2048, 7168, 64)
+    assert qmv.qmv_moe_layer_workspace_bytes(cbd, 1, 4) == 4 * 2048 * 4
     L = qmv.lib.qmv_moe_layer
     B = qmv.ctypes.byref
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need - 16, FAKE, 0, 0) == qmv.QMV_ESIZE
@@ -250,3 +252,8 @@ def test_moe_layer_argument_errors():
     cb = qmv.wdesc("cb3", 2880, 2880, 32)
     assert L(B(gu), FAKE, B(cb), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, None, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 4, 0) == qmv.QMV_EINVAL   # unknown flag
+    # fp32 activations exist only for the codebook formats
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
+    d = qmv.wdesc("mxfp4", 64, 64)
+    assert qmv.lib.qmv_dense_ex(B(d), FAKE, FAKE, 1, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
