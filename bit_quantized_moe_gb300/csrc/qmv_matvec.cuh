@@ -4,8 +4,9 @@
 // Work decomposition. A "work item" is one row tile (kRows rows) of one
 // matrix applied to up to NV activation vectors (the "entry": an expert and
 // the (token, slot) pairs routed to it). Items are dealt round-robin over the
-// CTAs of a one-wave grid, then over each CTA's warps. A warp streams its items' tiles -- one tile per K chunk --
-// through a private ring of kStages shared-memory stages filled by bulk
+// CTAs of a one-wave grid, then over each CTA's warps. A warp streams its
+// items' tiles -- one tile per K chunk -- through a private ring of
+// shared-memory stages (Shape::stages) filled by bulk
 // asynchronous copies (one elected lane issues them, an mbarrier per stage
 // tracks completion). Lane l of the warp owns columns [32 l, 32 l + 32) of
 // every chunk for all kRows rows, so the activations it needs are loaded into
@@ -38,12 +39,23 @@
 
 namespace qmv {
 
-// One CTA of kWarps warps per SM, each warp with a ring of kStages tiles: 30
-// tiles (130 KB) in flight per SM, enough to request a whole 2880 x 2880
-// top-4 gather's share of weights at once.
-constexpr int kWarps = 6;        // warps per CTA
-constexpr int kStages = 3;       // shared-memory stages per warp (3 chunks cover K <= 3072)
+// Launch shape of the kernel for entries of up to NV vectors: two CTAs per SM;
+// a CTA of `warps` warps, each with a ring of `stages` tiles. One-vector
+// kernels (every decode call at one token) run 10 warps with 2-stage rings:
+// 20 warps per SM give each warp about one 8-row item of a 2880-row gather,
+// and 40 tiles (174 KB) are in flight per SM. Kernels for 2-4 vectors need
+// 110-160 registers per thread and run 6 warps with 3-stage rings.
+template <int NV>
+struct Shape {
+  static constexpr int warps = (NV == 1) ? 10 : 6;
+  static constexpr int stages = (NV == 1) ? 2 : 3;
+};
 constexpr int kCtasPerSm = 2;
+
+inline void launch_shape(int nv, int& warps, int& stages) {
+  warps = (nv == 1) ? Shape<1>::warps : Shape<4>::warps;
+  stages = (nv == 1) ? Shape<1>::stages : Shape<4>::stages;
+}
 constexpr int kMaxEntries = 32;  // ntok * top_k <= 4 * 8
 constexpr int kMaxDevices = 64;
 
@@ -94,14 +106,14 @@ struct SmemLayout {
 // x region: the activation vectors as copied; for MXFP4 they are rewritten in
 // place as f16 (see stage_x_mxfp4) and xinv holds one float per 32-group.
 __host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32_t x_vec_bytes,
-                                                  uint32_t full_tile, int K) {
+                                                  uint32_t full_tile, int K, int warps, int stages) {
   SmemLayout L;
   L.x_off = 0;
   L.xinv_off = round_up_u32(nvec * x_vec_bytes, 16);
   const uint32_t xinv_bytes = (fmt == MXFP4) ? nvec * (uint32_t)(K / 32) * 4u : 0u;
   L.ring_off = round_up_u32(L.xinv_off + xinv_bytes, 128);
-  L.bar_off = L.ring_off + kWarps * kStages * full_tile;
-  L.ent_off = round_up_u32(L.bar_off + kWarps * kStages * 8, 16);
+  L.bar_off = L.ring_off + (uint32_t)(warps * stages) * full_tile;
+  L.ent_off = round_up_u32(L.bar_off + (uint32_t)(warps * stages) * 8, 16);
   L.total = L.ent_off + kMaxEntries * (uint32_t)sizeof(Entry);
   return L;
 }
@@ -168,66 +180,39 @@ __device__ int build_entries_warp(const KParams& p, Entry* ent, int* s_ids) {
 // Tile loads
 // ---------------------------------------------------------------------------
 
-// A warp's tiles come from one or two "phases" (the items of one matrix each),
-// streamed back to back through the same ring: tile q of the warp's sequence
-// is tile q of phase 0 if q < ph0.nq, else tile q - ph0.nq of phase 1.
-struct PhaseSeq {
-  const KParams* p;   // the matrix (points into kernel parameter space)
-  const Entry* ent;   // its work list
-  int first;          // this warp's first item; it then takes every nw-th
-  int n_items;        // items in the whole list
-  int nq;             // tiles this warp streams in this phase
-};
-
+// A warp streams the tiles of its items (item = first + k * nw, all chunks of
+// each) through its ring: tile q is chunk q % chunks of the warp's item
+// q / chunks.
 struct WarpPipe {
+  const KParams* p;   // the matrix (points into kernel parameter space)
+  const Entry* ent;   // the work list
   uint32_t ring;      // shared address of this warp's stage 0
   uint32_t bars;      // shared address of this warp's mbarrier 0
   const uint8_t* ring_ptr;
-  uint32_t stage_bytes;
+  int first;          // this warp's first item
   int nw;             // warps in the grid
-  PhaseSeq ph0, ph1;  // ph1.nq == 0 when there is one phase
+  int n_items;        // items in the whole list
+  int nq;             // tiles this warp streams
   uint64_t policy;
 };
 
-__device__ __forceinline__ int warp_item_count(int first, int n_items, int nw) {
-  return first < n_items ? (n_items - first + nw - 1) / nw : 0;
-}
-
-__device__ __forceinline__ PhaseSeq make_phase(const KParams* p, const Entry* ent, int first, int n_items,
-                                               int nw) {
-  PhaseSeq ph;
-  ph.p = p;
-  ph.ent = ent;
-  ph.first = first;
-  ph.n_items = n_items;
-  ph.nq = warp_item_count(first, n_items, nw) * p->chunks;
-  return ph;
-}
-
-// Copies tile t of phase `ph` (item = first + (t / chunks) * nw, chunk =
-// t % chunks) into ring stage qs % kStages.
-__device__ __forceinline__ void issue_phase_tile(const WarpPipe& wp, const PhaseSeq& ph, int t, int qs) {
-  const KParams& p = *ph.p;
-  const int item = ph.first + (t / p.chunks) * wp.nw;
-  const int c = t % p.chunks;
+// Copies tile q of this warp's sequence into ring stage q % ST, if there is
+// one.
+template <int ST>
+__device__ __forceinline__ void issue_tile(const WarpPipe& wp, int q) {
+  if (q >= wp.nq) return;
+  const KParams& p = *wp.p;
+  const int item = wp.first + (q / p.chunks) * wp.nw;
+  const int c = q % p.chunks;
   const int rt = item % p.row_tiles;
-  const Entry& e = ph.ent[item / p.row_tiles];
+  const Entry& e = wp.ent[item / p.row_tiles];
   const uint8_t* src = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)rt * p.rowtile +
                        (uint64_t)c * p.full_tile;
   const uint32_t bytes = (c == p.chunks - 1) ? p.last_tile : p.full_tile;
-  const int s = qs % kStages;
+  const int s = q % ST;
   const uint32_t bar = wp.bars + 8u * s;
   mbar_arrive_expect_tx(bar, bytes);
-  bulk_copy_g2s_hint(wp.ring + (uint32_t)s * wp.stage_bytes, src, bytes, bar, wp.policy);
-}
-
-// Issues the copy of tile q of this warp's sequence, if there is one.
-__device__ __forceinline__ void issue_tile(const WarpPipe& wp, int q) {
-  if (q < wp.ph0.nq) {
-    issue_phase_tile(wp, wp.ph0, q, q);
-  } else if (q - wp.ph0.nq < wp.ph1.nq) {
-    issue_phase_tile(wp, wp.ph1, q - wp.ph0.nq, q);
-  }
+  bulk_copy_g2s_hint(wp.ring + (uint32_t)s * p.full_tile, src, bytes, bar, wp.policy);
 }
 
 // ---------------------------------------------------------------------------
@@ -302,11 +287,12 @@ __device__ __forceinline__ float pow2f(int e) {
   return (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 }
 
-// Activation staging. Every thread issues the global loads of up to kStageU
-// units (a group, a block or 16 bytes) before it converts or stores any of
-// them: at the start of a launch the loads queue behind the weight tiles just
-// requested, so each extra dependent round of loads costs a full queued round
-// trip.
+// Activation staging. Every thread issues the global loads of several units
+// (kStageU MXFP4 groups, one fp32 block, four 16-byte pieces) before it
+// converts or stores any of them: at the start of a launch the loads queue
+// behind the weight tiles just requested, so each extra dependent round of
+// loads costs a full queued round trip. (One fp32 block, 32 registers, keeps
+// the one-vector codebook kernels within 102 registers per thread.)
 constexpr int kStageU = 2;
 
 // MXFP4 activations are staged once per CTA: each 32-element group (one E8M0
@@ -407,10 +393,11 @@ __device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t*
 __device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, int nvec, int K, uint32_t vec_bytes) {
   const int blocks = K / 32;
   const int n = nvec * blocks;
-  for (int b0 = threadIdx.x; b0 < n; b0 += kStageU * blockDim.x) {
-    float f[kStageU][32];
+  constexpr int U = 1;
+  for (int b0 = threadIdx.x; b0 < n; b0 += U * blockDim.x) {
+    float f[U][32];
 #pragma unroll
-    for (int u = 0; u < kStageU; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int bi = b0 + u * blockDim.x;
       if (bi < n) {
         const float4* src = reinterpret_cast<const float4*>(x + (size_t)(bi / blocks) * K + (size_t)(bi % blocks) * 32);
@@ -422,7 +409,7 @@ __device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, i
       }
     }
 #pragma unroll
-    for (int u = 0; u < kStageU; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int bi = b0 + u * blockDim.x;
       if (bi < n) quantize_block_q8(f[u], xs + (size_t)(bi / blocks) * vec_bytes, K, bi % blocks);
     }
@@ -658,7 +645,7 @@ __device__ __forceinline__ void reduce_store(const KParams& p, const Entry& e, i
 // One work item: all chunks of one row tile, applied to NVV vectors.
 // ---------------------------------------------------------------------------
 
-template <int FMT, int NVV, bool DBG>
+template <int FMT, int NVV, bool DBG, int ST>
 __device__ __forceinline__ bool run_item(const KParams& p, const Entry& e, int rt, int& q, const WarpPipe& wp,
                                          const uint8_t* xs, const float* xinv) {
   constexpr int NVP = (NVV == 3) ? 4 : NVV;
@@ -667,12 +654,12 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry& e, int r
 #pragma unroll
   for (int i = 0; i < kRows * NVP; ++i) acc[i] = 0.f;
   for (int c = 0; c < p.chunks; ++c, ++q) {
-    const int s = q % kStages;
-    const uint32_t parity = (uint32_t)(q / kStages) & 1u;
+    const int s = q % ST;
+    const uint32_t parity = (uint32_t)(q / ST) & 1u;
     bool ok = mbar_wait_bounded(wp.bars + 8u * s, parity, kWaitLimitNs);
     if (!__all_sync(0xffffffffu, ok)) return false;
     const int L = (c == p.chunks - 1) ? p.last_lanes : 32;
-    const uint8_t* st = wp.ring_ptr + (size_t)s * wp.stage_bytes;
+    const uint8_t* st = wp.ring_ptr + (size_t)s * p.full_tile;
     if (lane < L) {
       if constexpr (FMT == MXFP4) {
         chunk_mxfp4<NVV, NVP>(p, e, c, L, st, xs, xinv, acc);
@@ -682,25 +669,25 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry& e, int r
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) issue_tile(wp, q + kStages);
+    if (lane == 0) issue_tile<ST>(wp, q + ST);
   }
   reduce_store<FMT, NVV, NVP>(p, e, rt, acc);
   return true;
 }
 
-// All items of one phase of this warp. False if a tile wait gave up.
-template <int FMT, int NV, bool DBG>
-__device__ __forceinline__ bool run_phase(const KParams& p, const PhaseSeq& ph, int& q, const WarpPipe& wp,
-                                          const uint8_t* xs, const float* xinv) {
-  for (int item = ph.first; item < ph.n_items; item += wp.nw) {
-    const Entry& e = ph.ent[item / p.row_tiles];
+// All items of this warp. False if a tile wait gave up.
+template <int FMT, int NV, bool DBG, int ST>
+__device__ __forceinline__ bool run_items(const KParams& p, int& q, const WarpPipe& wp, const uint8_t* xs,
+                                          const float* xinv) {
+  for (int item = wp.first; item < wp.n_items; item += wp.nw) {
+    const Entry& e = wp.ent[item / p.row_tiles];
     const int rt = item % p.row_tiles;
     bool ok = true;
     switch (e.nv) {
-      case 1: ok = run_item<FMT, 1, DBG>(p, e, rt, q, wp, xs, xinv); break;
-      case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG>(p, e, rt, q, wp, xs, xinv); break;
-      case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG>(p, e, rt, q, wp, xs, xinv); break;
-      case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG>(p, e, rt, q, wp, xs, xinv); break;
+      case 1: ok = run_item<FMT, 1, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
+      case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
+      case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
+      case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
       default: break;
     }
     if (!ok) return false;
@@ -709,25 +696,28 @@ __device__ __forceinline__ bool run_phase(const KParams& p, const PhaseSeq& ph, 
 }
 
 // After a failed wait: let every copy this warp still has in flight (tiles
-// q .. q + kStages - 1 of its sequence) land, bounded, before the CTA's shared
+// q .. q + ST - 1 of its sequence) land, bounded, before the CTA's shared
 // memory can be released.
+template <int ST>
 __device__ __forceinline__ void drain_ring(const WarpPipe& wp, int q) {
   const int lane = threadIdx.x & 31;
-  const int total = wp.ph0.nq + wp.ph1.nq;
-  for (int qq = q; qq < min(total, q + kStages); ++qq) {
-    const int s = qq % kStages;
-    if (!mbar_wait_bounded(wp.bars + 8u * s, (uint32_t)(qq / kStages) & 1u, kDrainLimitNs)) {
+  for (int qq = q; qq < min(wp.nq, q + ST); ++qq) {
+    const int s = qq % ST;
+    if (!mbar_wait_bounded(wp.bars + 8u * s, (uint32_t)(qq / ST) & 1u, kDrainLimitNs)) {
       if (lane == 0) set_status(kStatusDrain);
     }
   }
 }
 
 template <int FMT, int NV, bool DBG>
-__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) matvec_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
+    matvec_kernel(const __grid_constant__ KParams p) {
+  constexpr int W = Shape<NV>::warps;
+  constexpr int ST = Shape<NV>::stages;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K);
+  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K, W, ST);
   uint8_t* xs = smem + sl.x_off;
   float* xinv = reinterpret_cast<float*>(smem + sl.xinv_off);
   uint8_t* ring = smem + sl.ring_off;
@@ -737,7 +727,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) matvec_kernel(const _
 
   __shared__ int s_ids[kMaxEntries];
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    for (int i = 0; i < W * ST; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
   }
   // Programmatic dependent launch. Activations may be produced by the kernel
@@ -759,19 +749,20 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) matvec_kernel(const _
   WarpPipe wp;
   // Items are dealt to CTAs first (item i -> CTA i % gridDim.x), so every CTA,
   // and with a full grid every SM, gets the same number of items within one.
-  wp.nw = gridDim.x * kWarps;
-  wp.stage_bytes = p.full_tile;
-  wp.ring_ptr = ring + (size_t)warp * kStages * wp.stage_bytes;
+  wp.p = &p;
+  wp.ent = ent;
+  wp.nw = gridDim.x * W;
+  wp.first = blockIdx.x + gridDim.x * warp;
+  wp.n_items = s_nent * p.row_tiles;
+  wp.nq = (wp.first < wp.n_items ? (wp.n_items - wp.first + wp.nw - 1) / wp.nw : 0) * p.chunks;
+  wp.ring_ptr = ring + (size_t)warp * ST * p.full_tile;
   wp.ring = smem_addr(wp.ring_ptr);
-  wp.bars = smem_addr(&bars[warp * kStages]);
+  wp.bars = smem_addr(&bars[warp * ST]);
   wp.policy = l2_evict_first_policy();
-  wp.ph0 = make_phase(&p, ent, blockIdx.x + gridDim.x * warp, s_nent * p.row_tiles, wp.nw);
-  wp.ph1 = wp.ph0;
-  wp.ph1.nq = 0;
   // Stage-major issue order (every warp's first tile, then every warp's
   // second, ...) so that each warp's first tile arrives early in the burst.
-  for (int q = 0; q < kStages; ++q) {
-    if (lane == 0) issue_tile(wp, q);
+  for (int q = 0; q < ST; ++q) {
+    if (lane == 0) issue_tile<ST>(wp, q);
     __syncthreads();
   }
   if (early) pdl_wait();
@@ -804,9 +795,9 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) matvec_kernel(const _
   __syncthreads();
 
   int q = 0;
-  if (!run_phase<FMT, NV, DBG>(p, wp.ph0, q, wp, xs, xinv)) {
+  if (!run_items<FMT, NV, DBG, ST>(p, q, wp, xs, xinv)) {
     if (lane == 0) set_status(kStatusWaitTile);
-    drain_ring(wp, q);
+    drain_ring<ST>(wp, q);
   }
 }
 
@@ -855,8 +846,10 @@ template <int FMT>
 cudaError_t launch_matvec(const MatvecArgs& a) {
   constexpr int NVMAX = MaxVectors<FMT>::value;
   const KParams p = make_params(a);
-  const SmemLayout sl = smem_layout(a.fmt, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K);
-  const int want_nv = a.ids ? (a.ntok < NVMAX ? a.ntok : NVMAX) : (a.ntok < NVMAX ? a.ntok : NVMAX);
+  const int want_nv = a.ntok < NVMAX ? a.ntok : NVMAX;
+  int warps = 0, stages = 0;
+  launch_shape(want_nv, warps, stages);
+  const SmemLayout sl = smem_layout(a.fmt, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K, warps, stages);
   void* fn = nullptr;
   const bool dbg = a.dbg != nullptr;
   switch (want_nv) {
@@ -901,7 +894,7 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   }
   int per_sm = 0;
   g_launch_stage = "cudaOccupancyMaxActiveBlocksPerMultiprocessor";
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWarps * 32, sl.total);
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, sl.total);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // Upper bound on work items: every routed pair its own entry.
@@ -914,7 +907,7 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.blockDim = dim3(warps * 32);
   cfg.dynamicSmemBytes = sl.total;
   cfg.stream = a.stream;
   // Programmatic dependent launch lets this grid start while the previous
