@@ -187,13 +187,9 @@ cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t s) {
 QMV_DEFINE_STATUS_ACCESSOR(status_act)
 
 size_t matvec_smem_bytes(const MatvecArgs& a) {
-  const Geometry g = make_geometry(a.fmt, a.N, a.K);
-  const uint32_t xvb = (a.fmt == MXFP4) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
-  int warps = 0, stages = 0;
-  launch_shape(a.ntok < 4 ? a.ntok : 4, warps, stages);
-  const uint64_t total = (uint64_t)smem_layout(a.fmt, (uint32_t)a.nvec, xvb, g.full_tile, a.K, warps, stages).total;
+  const LaunchPlan plan = plan_launch(a, device_sm_count(), kCtasPerSm);
   // room for the kernel's static shared variables (128 bytes with alignment)
-  return (size_t)(total + 256);
+  return (size_t)plan.smem.total + 256;
 }
 
 }  // namespace qmv

@@ -43,18 +43,32 @@ namespace qmv {
 // a CTA of `warps` warps, each with a ring of `stages` tiles. One-vector
 // kernels (every decode call at one token) run 10 warps with 2-stage rings:
 // 20 warps per SM give each warp about one 8-row item of a 2880-row gather,
-// and 40 tiles (174 KB) are in flight per SM. Kernels for 2-4 vectors need
-// 110-160 registers per thread and run 6 warps with 3-stage rings.
+// and 40 tiles (174 KB) are in flight per SM. Two-vector kernels (<= 128
+// registers) run 8 warps with 2-stage rings; 3- and 4-vector kernels need up
+// to 160 registers per thread and run 6 warps with 3-stage rings.
 template <int NV>
 struct Shape {
-  static constexpr int warps = (NV == 1) ? 10 : 6;
-  static constexpr int stages = (NV == 1) ? 2 : 3;
+  static constexpr int warps = (NV == 1) ? 10 : (NV == 2 ? 8 : 6);
+  static constexpr int stages = (NV <= 2) ? 2 : 3;
 };
 constexpr int kCtasPerSm = 2;
 
 inline void launch_shape(int nv, int& warps, int& stages) {
-  warps = (nv == 1) ? Shape<1>::warps : Shape<4>::warps;
-  stages = (nv == 1) ? Shape<1>::stages : Shape<4>::stages;
+  switch (nv) {
+    case 1: warps = Shape<1>::warps; stages = Shape<1>::stages; break;
+    case 2: warps = Shape<2>::warps; stages = Shape<2>::stages; break;
+    default: warps = Shape<4>::warps; stages = Shape<4>::stages; break;
+  }
+}
+
+// Vectors per entry of a launch's kernel. Dense calls put every token in each
+// entry (up to 4). Gathers group the routed pairs of one expert; with
+// independently routed tokens that is almost always one pair, so gathers use
+// at most the two-vector kernel (its launch shape keeps more warps per SM) and
+// an expert shared by more pairs is streamed once per two of them.
+inline int launch_vectors(bool gather, int ntok) {
+  const int cap = gather ? 2 : 4;
+  return ntok < cap ? ntok : cap;
 }
 constexpr int kMaxEntries = 32;  // ntok * top_k <= 4 * 8
 constexpr int kMaxDevices = 64;
@@ -82,6 +96,9 @@ struct KParams {
   uint32_t lut[4];
   uint32_t flags;
   int out_n;              // rows of each output vector (N, or N / 2 rounded for gate/up fusion)
+  int splits;             // K ranges per item (split-K inside a CTA), >= 1
+  int split_chunks;       // chunks per K range (the last may be shorter)
+  int items_per_cta;      // upper bound on items per CTA (split-K partial slots)
 };
 
 // KParams::flags
@@ -100,13 +117,19 @@ __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
 }
 
 struct SmemLayout {
-  uint32_t x_off, xinv_off, ring_off, bar_off, ent_off, total;
+  uint32_t x_off, xinv_off, ring_off, bar_off, ent_off, part_off, cnt_off, total;
 };
+
+// Split-K partial sums: 32 floats (8 rows x up to 4 vectors, after the
+// warp reduction) per (item of the CTA, K range), and one counter per item.
+constexpr uint32_t kPartFloats = 32;
+constexpr int kMaxSplits = 8;
 
 // x region: the activation vectors as copied; for MXFP4 they are rewritten in
 // place as f16 (see stage_x_mxfp4) and xinv holds one float per 32-group.
 __host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32_t x_vec_bytes,
-                                                  uint32_t full_tile, int K, int warps, int stages) {
+                                                  uint32_t full_tile, int K, int warps, int stages,
+                                                  int splits, int items_per_cta) {
   SmemLayout L;
   L.x_off = 0;
   L.xinv_off = round_up_u32(nvec * x_vec_bytes, 16);
@@ -114,7 +137,10 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32
   L.ring_off = round_up_u32(L.xinv_off + xinv_bytes, 128);
   L.bar_off = L.ring_off + (uint32_t)(warps * stages) * full_tile;
   L.ent_off = round_up_u32(L.bar_off + (uint32_t)(warps * stages) * 8, 16);
-  L.total = L.ent_off + kMaxEntries * (uint32_t)sizeof(Entry);
+  L.part_off = L.ent_off + kMaxEntries * (uint32_t)sizeof(Entry);
+  const uint32_t slots = (splits > 1) ? (uint32_t)items_per_cta : 0u;
+  L.cnt_off = L.part_off + slots * (uint32_t)splits * kPartFloats * 4u;
+  L.total = L.cnt_off + slots * 4u;
   return L;
 }
 
@@ -180,39 +206,61 @@ __device__ int build_entries_warp(const KParams& p, Entry* ent, int* s_ids) {
 // Tile loads
 // ---------------------------------------------------------------------------
 
-// A warp streams the tiles of its items (item = first + k * nw, all chunks of
-// each) through its ring: tile q is chunk q % chunks of the warp's item
-// q / chunks.
+// Work of a CTA: its items are b, b + G, b + 2G, ... (b = blockIdx.x, G =
+// gridDim.x: every CTA, and with a full grid every SM, gets the same number
+// within one); item k of the CTA is split into `splits` K ranges, and task
+// lt = k * splits + r (range r of item k) goes to warp lt % W. A warp streams
+// the tiles of its tasks, in order, through its ring. Lane 0 keeps the issue
+// cursor (the next task and chunk to copy).
 struct WarpPipe {
   const KParams* p;   // the matrix (points into kernel parameter space)
   const Entry* ent;   // the work list
   uint32_t ring;      // shared address of this warp's stage 0
   uint32_t bars;      // shared address of this warp's mbarrier 0
   const uint8_t* ring_ptr;
-  int first;          // this warp's first item
-  int nw;             // warps in the grid
-  int n_items;        // items in the whole list
-  int nq;             // tiles this warp streams
+  int n_tasks;        // tasks of this CTA
+  int warps;          // W
+  int iss_n;          // tiles issued so far
+  int iss_lt, iss_c, iss_c1;  // issue cursor: task, next chunk, end chunk
+  const uint8_t* iss_base;    // global address of the cursor task's row tile
   uint64_t policy;
 };
 
-// Copies tile q of this warp's sequence into ring stage q % ST, if there is
-// one.
-template <int ST>
-__device__ __forceinline__ void issue_tile(const WarpPipe& wp, int q) {
-  if (q >= wp.nq) return;
+__device__ __forceinline__ int task_item(const KParams& p, int lt) {
+  return blockIdx.x + (lt / p.splits) * gridDim.x;
+}
+
+__device__ __forceinline__ void task_chunks(const KParams& p, int lt, int& c0, int& c1) {
+  c0 = (lt % p.splits) * p.split_chunks;
+  c1 = min(p.chunks, c0 + p.split_chunks);
+}
+
+// Moves the issue cursor to task lt (the divisions happen once per task).
+__device__ __forceinline__ void cursor_to(WarpPipe& wp, int lt) {
+  wp.iss_lt = lt;
+  if (lt >= wp.n_tasks) return;
   const KParams& p = *wp.p;
-  const int item = wp.first + (q / p.chunks) * wp.nw;
-  const int c = q % p.chunks;
-  const int rt = item % p.row_tiles;
+  task_chunks(p, lt, wp.iss_c, wp.iss_c1);
+  const int item = task_item(p, lt);
   const Entry& e = wp.ent[item / p.row_tiles];
-  const uint8_t* src = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)rt * p.rowtile +
-                       (uint64_t)c * p.full_tile;
+  wp.iss_base = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)(item % p.row_tiles) * p.rowtile;
+}
+
+// Lane 0: copies the next tile of this warp's task sequence into ring stage
+// (tiles issued) % ST, if there is one.
+template <int ST>
+__device__ __forceinline__ void issue_next(WarpPipe& wp) {
+  if (wp.iss_lt >= wp.n_tasks) return;
+  const KParams& p = *wp.p;
+  const int c = wp.iss_c;
+  const uint8_t* src = wp.iss_base + (uint64_t)c * p.full_tile;
   const uint32_t bytes = (c == p.chunks - 1) ? p.last_tile : p.full_tile;
-  const int s = q % ST;
+  const int s = wp.iss_n % ST;
   const uint32_t bar = wp.bars + 8u * s;
   mbar_arrive_expect_tx(bar, bytes);
   bulk_copy_g2s_hint(wp.ring + (uint32_t)s * p.full_tile, src, bytes, bar, wp.policy);
+  ++wp.iss_n;
+  if (++wp.iss_c == wp.iss_c1) cursor_to(wp, wp.iss_lt + wp.warps);
 }
 
 // ---------------------------------------------------------------------------
@@ -614,46 +662,59 @@ __device__ __forceinline__ void store_out(const KParams& p, size_t o, float val)
   }
 }
 
-// After the reduce-scatter, lane l holds (row, vector) index l / (32 / M).
-// Plain: store y[slot][rt * kRows + row]. Gate/up fusion (kFlagGlu): rows
-// 0..3 of the tile are gate rows 4 rt .. 4 rt + 3 and rows 4..7 the matching
-// up rows; the lane of gate row r takes up row r from lane l + 16 and stores
-// silu(g) * u at h[slot][4 rt + r] (mlxcel-2178, "Problem / Background":
-// gate, up and down per layer, SwiGLU between them).
-template <int FMT, int NVV, int NVP>
-__device__ __forceinline__ void reduce_store(const KParams& p, const Entry& e, int rt, float* acc) {
-  const int lane = threadIdx.x & 31;
+// After the reduce-scatter (rs_step), each group of 32 / M lanes holds the
+// sum of (row, vector) index l / (32 / M), M = kRows * NVP.
+template <int NVP>
+__device__ __forceinline__ float reduce_lanes(float* acc) {
   constexpr int M = kRows * NVP;
   static_assert(M <= 32, "one value per lane group after the reduce-scatter");
+  rs_step<M, 16>(acc, threadIdx.x & 31);
+  return acc[0];
+}
+
+// Stores the reduced value of this lane's (row, vector). Plain: y[slot][rt *
+// kRows + row]. Gate/up fusion (kFlagGlu): rows 0..3 of the tile are gate rows
+// 4 rt .. 4 rt + 3 and rows 4..7 the matching up rows; the lane of gate row r
+// takes up row r from lane l + 16 and stores silu(g) * u at h[slot][4 rt + r]
+// (mlxcel-2178, "Problem / Background": gate, up and down per layer, SwiGLU
+// between them). All lanes of the warp call it.
+template <int FMT, int NVV, int NVP>
+__device__ __forceinline__ void store_lanes(const KParams& p, const Entry& e, int rt, float val) {
+  const int lane = threadIdx.x & 31;
+  constexpr int M = kRows * NVP;
   constexpr int S = 32 / M;
-  rs_step<M, 16>(acc, lane);
   const int idx = lane / S;
   const int r = idx / NVP, v = idx % NVP;
   if (p.flags & kFlagGlu) {
-    const float up = __shfl_xor_sync(0xffffffffu, acc[0], 16);   // row r + 4 (same vector) lives 16 lanes up
+    const float up = __shfl_xor_sync(0xffffffffu, val, 16);   // row r + 4 (same vector) lives 16 lanes up
     const int row = rt * (kRows / 2) + r;
     if (lane % S == 0 && r < kRows / 2 && v < NVV && row < p.out_n) {
-      store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, silu_f32(acc[0]) * up);
+      store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, silu_f32(val) * up);
     }
   } else {
     const int row = rt * kRows + r;
-    if (lane % S == 0 && v < NVV && row < p.out_n) store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, acc[0]);
+    if (lane % S == 0 && v < NVV && row < p.out_n) store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, val);
   }
 }
 
 // ---------------------------------------------------------------------------
-// One work item: all chunks of one row tile, applied to NVV vectors.
+// One task: chunks [c0, c1) of one row tile, applied to NVV vectors; then the
+// warp reduction and either the store (one K range per item) or the split-K
+// combine: the warp parks its reduced values in shared memory, and the warp
+// that completes an item's last range adds the ranges in range order (the
+// same order every run) and stores.
 // ---------------------------------------------------------------------------
 
 template <int FMT, int NVV, bool DBG, int ST>
-__device__ __forceinline__ bool run_item(const KParams& p, const Entry& e, int rt, int& q, const WarpPipe& wp,
-                                         const uint8_t* xs, const float* xinv) {
+__device__ __forceinline__ bool run_task(const KParams& p, const Entry& e, int rt, int k, int range, int c0,
+                                         int c1, int& q, WarpPipe& wp, const uint8_t* xs, const float* xinv,
+                                         float* part, int* cnt) {
   constexpr int NVP = (NVV == 3) ? 4 : NVV;
   const int lane = threadIdx.x & 31;
   float acc[kRows * NVP];
 #pragma unroll
   for (int i = 0; i < kRows * NVP; ++i) acc[i] = 0.f;
-  for (int c = 0; c < p.chunks; ++c, ++q) {
+  for (int c = c0; c < c1; ++c, ++q) {
     const int s = q % ST;
     const uint32_t parity = (uint32_t)(q / ST) & 1u;
     bool ok = mbar_wait_bounded(wp.bars + 8u * s, parity, kWaitLimitNs);
@@ -669,25 +730,53 @@ __device__ __forceinline__ bool run_item(const KParams& p, const Entry& e, int r
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) issue_tile<ST>(wp, q + ST);
+    if (lane == 0) issue_next<ST>(wp);
   }
-  reduce_store<FMT, NVV, NVP>(p, e, rt, acc);
+  float val = reduce_lanes<NVP>(acc);
+  if (p.splits > 1) {
+    constexpr int M = kRows * NVP;
+    constexpr int S = 32 / M;
+    volatile float* slot = part + (size_t)k * p.splits * kPartFloats;
+    if (lane % S == 0) slot[range * kPartFloats + lane / S] = val;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = (atomicAdd(&cnt[k], 1) == p.splits - 1) ? 1 : 0;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return true;
+    __threadfence_block();
+    val = 0.f;
+    for (int r = 0; r < p.splits; ++r) val += slot[r * kPartFloats + lane / S];
+  }
+  store_lanes<FMT, NVV, NVP>(p, e, rt, val);
   return true;
 }
 
-// All items of this warp. False if a tile wait gave up.
+// All tasks of this warp. False if a tile wait gave up.
 template <int FMT, int NV, bool DBG, int ST>
-__device__ __forceinline__ bool run_items(const KParams& p, int& q, const WarpPipe& wp, const uint8_t* xs,
-                                          const float* xinv) {
-  for (int item = wp.first; item < wp.n_items; item += wp.nw) {
+__device__ __forceinline__ bool run_tasks(const KParams& p, int& q, WarpPipe& wp, const uint8_t* xs,
+                                          const float* xinv, float* part, int* cnt) {
+  const int warp = threadIdx.x >> 5;
+  for (int lt = warp; lt < wp.n_tasks; lt += wp.warps) {
+    const int item = task_item(p, lt);
     const Entry& e = wp.ent[item / p.row_tiles];
     const int rt = item % p.row_tiles;
+    const int k = lt / p.splits, range = lt % p.splits;
+    int c0, c1;
+    task_chunks(p, lt, c0, c1);
     bool ok = true;
     switch (e.nv) {
-      case 1: ok = run_item<FMT, 1, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
-      case 2: if constexpr (NV >= 2) ok = run_item<FMT, 2, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
-      case 3: if constexpr (NV >= 3) ok = run_item<FMT, 3, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
-      case 4: if constexpr (NV >= 4) ok = run_item<FMT, 4, DBG, ST>(p, e, rt, q, wp, xs, xinv); break;
+      case 1: ok = run_task<FMT, 1, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt); break;
+      case 2:
+        if constexpr (NV >= 2) ok = run_task<FMT, 2, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
+        break;
+      case 3:
+        if constexpr (NV >= 3) ok = run_task<FMT, 3, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
+        break;
+      case 4:
+        if constexpr (NV >= 4) ok = run_task<FMT, 4, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
+        break;
       default: break;
     }
     if (!ok) return false;
@@ -695,13 +784,14 @@ __device__ __forceinline__ bool run_items(const KParams& p, int& q, const WarpPi
   return true;
 }
 
-// After a failed wait: let every copy this warp still has in flight (tiles
-// q .. q + ST - 1 of its sequence) land, bounded, before the CTA's shared
-// memory can be released.
+// After a failed wait: let every copy this warp still has in flight (tiles q
+// up to the number issued) land, bounded, before the CTA's shared memory can
+// be released. Lane 0 holds the issue count.
 template <int ST>
 __device__ __forceinline__ void drain_ring(const WarpPipe& wp, int q) {
   const int lane = threadIdx.x & 31;
-  for (int qq = q; qq < min(wp.nq, q + ST); ++qq) {
+  const int issued = __shfl_sync(0xffffffffu, wp.iss_n, 0);
+  for (int qq = q; qq < issued; ++qq) {
     const int s = qq % ST;
     if (!mbar_wait_bounded(wp.bars + 8u * s, (uint32_t)(qq / ST) & 1u, kDrainLimitNs)) {
       if (lane == 0) set_status(kStatusDrain);
@@ -717,18 +807,24 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K, W, ST);
+  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K, W, ST, p.splits,
+                                    p.items_per_cta);
   uint8_t* xs = smem + sl.x_off;
   float* xinv = reinterpret_cast<float*>(smem + sl.xinv_off);
   uint8_t* ring = smem + sl.ring_off;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sl.bar_off);
   Entry* ent = reinterpret_cast<Entry*>(smem + sl.ent_off);
+  float* part = reinterpret_cast<float*>(smem + sl.part_off);
+  int* cnt = reinterpret_cast<int*>(smem + sl.cnt_off);
   __shared__ int s_nent;
 
   __shared__ int s_ids[kMaxEntries];
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * ST; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
+  }
+  if (p.splits > 1) {
+    for (int i = threadIdx.x; i < p.items_per_cta; i += blockDim.x) cnt[i] = 0;
   }
   // Programmatic dependent launch. Activations may be produced by the kernel
   // that precedes this one in the stream, so they are read only after
@@ -747,22 +843,22 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   __syncthreads();
 
   WarpPipe wp;
-  // Items are dealt to CTAs first (item i -> CTA i % gridDim.x), so every CTA,
-  // and with a full grid every SM, gets the same number of items within one.
   wp.p = &p;
   wp.ent = ent;
-  wp.nw = gridDim.x * W;
-  wp.first = blockIdx.x + gridDim.x * warp;
-  wp.n_items = s_nent * p.row_tiles;
-  wp.nq = (wp.first < wp.n_items ? (wp.n_items - wp.first + wp.nw - 1) / wp.nw : 0) * p.chunks;
+  wp.warps = W;
+  const int n_items = s_nent * p.row_tiles;
+  const int items_here = ((int)blockIdx.x < n_items) ? (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  wp.n_tasks = items_here * p.splits;
   wp.ring_ptr = ring + (size_t)warp * ST * p.full_tile;
   wp.ring = smem_addr(wp.ring_ptr);
   wp.bars = smem_addr(&bars[warp * ST]);
   wp.policy = l2_evict_first_policy();
+  wp.iss_n = 0;
+  cursor_to(wp, warp);
   // Stage-major issue order (every warp's first tile, then every warp's
   // second, ...) so that each warp's first tile arrives early in the burst.
   for (int q = 0; q < ST; ++q) {
-    if (lane == 0) issue_tile<ST>(wp, q);
+    if (lane == 0) issue_next<ST>(wp);
     __syncthreads();
   }
   if (early) pdl_wait();
@@ -795,7 +891,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   __syncthreads();
 
   int q = 0;
-  if (!run_items<FMT, NV, DBG, ST>(p, q, wp, xs, xinv)) {
+  if (!run_tasks<FMT, NV, DBG, ST>(p, q, wp, xs, xinv, part, cnt)) {
     if (lane == 0) set_status(kStatusWaitTile);
     drain_ring<ST>(wp, q);
   }
@@ -812,6 +908,45 @@ struct KernelSet {
     return reinterpret_cast<void*>(&matvec_kernel<FMT, NV, DBG>);
   }
 };
+
+// Host plan of a launch: kernel (vectors per entry), launch shape, split-K
+// and shared memory. Items are upper-bounded by one entry per routed pair.
+// Split-K: when a full grid has at least 3 warps per item (or 2, for items of
+// 4 or more chunks), each item is cut into floor(warps / items) K ranges (at
+// most one per chunk, at most kMaxSplits), so that more warps stream at once.
+// Measured on GB300: dense CB4 2048x7168 7.7 -> 4.4 us, 7168x7168 11.9 ->
+// 9.5 us; splitting the 3-chunk items of a 1440-item gather in two was slower.
+struct LaunchPlan {
+  int nv, warps, stages;
+  long items;              // upper bound
+  long grid;               // CTAs of a full grid (kCtasPerSm per SM), at most `items`
+  int splits, split_chunks, items_per_cta;
+  SmemLayout smem;
+};
+
+inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm) {
+  const Geometry g = make_geometry(a.fmt, a.N, a.K);
+  LaunchPlan L;
+  L.nv = launch_vectors(a.ids != nullptr, a.ntok);
+  launch_shape(L.nv, L.warps, L.stages);
+  const long entries = a.ids ? (long)a.ntok * a.top_k : (a.ntok + L.nv - 1) / L.nv;
+  L.items = entries * g.row_tiles;
+  L.grid = (long)sm_count * ctas_per_sm;
+  if (L.grid > L.items) L.grid = L.items;
+  if (L.grid < 1) L.grid = 1;
+  const long warps_total = (long)sm_count * kCtasPerSm * L.warps;
+  long splits = warps_total / L.items;
+  if (splits < 3 && !(splits == 2 && g.chunks >= 4)) splits = 1;
+  if (splits > g.chunks) splits = g.chunks;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits < 1) splits = 1;
+  L.split_chunks = (int)((g.chunks + splits - 1) / splits);
+  L.splits = (g.chunks + L.split_chunks - 1) / L.split_chunks;
+  L.items_per_cta = (int)((L.items + L.grid - 1) / L.grid);
+  const uint32_t xvb = (a.fmt == MXFP4) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
+  L.smem = smem_layout(a.fmt, (uint32_t)a.nvec, xvb, g.full_tile, a.K, L.warps, L.stages, L.splits, L.items_per_cta);
+  return L;
+}
 
 inline KParams make_params(const MatvecArgs& a) {
   const Geometry g = make_geometry(a.fmt, a.N, a.K);
@@ -839,17 +974,20 @@ inline KParams make_params(const MatvecArgs& a) {
   for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i];
   p.flags = (a.prefetch ? kFlagPrefetch : 0u) | (a.glu ? kFlagGlu : 0u) | (a.x_f32 ? kFlagXF32 : 0u);
   p.out_n = a.out_n > 0 ? a.out_n : a.N;
+  p.splits = 1;
+  p.split_chunks = g.chunks;
+  p.items_per_cta = 0;
   return p;
 }
 
 template <int FMT>
 cudaError_t launch_matvec(const MatvecArgs& a) {
   constexpr int NVMAX = MaxVectors<FMT>::value;
-  const KParams p = make_params(a);
-  const int want_nv = a.ntok < NVMAX ? a.ntok : NVMAX;
-  int warps = 0, stages = 0;
-  launch_shape(want_nv, warps, stages);
-  const SmemLayout sl = smem_layout(a.fmt, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K, warps, stages);
+  static_assert(NVMAX == 4, "kernels exist for 1 to 4 vectors per entry");
+  KParams p = make_params(a);
+  LaunchPlan plan = plan_launch(a, device_sm_count(), kCtasPerSm);
+  const int want_nv = plan.nv;
+  const int warps = plan.warps;
   void* fn = nullptr;
   const bool dbg = a.dbg != nullptr;
   switch (want_nv) {
@@ -875,14 +1013,14 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   {
     std::lock_guard<std::mutex> lock(mu);
     size_t& have = configured[dev][want_nv][dbg ? 1 : 0];
-    if (have < sl.total) {
+    if (have < plan.smem.total) {
       // The opt-in limit covers static plus dynamic shared memory.
       cudaFuncAttributes fa;
       g_launch_stage = "cudaFuncGetAttributes";
       cudaError_t err = cudaFuncGetAttributes(&fa, fn);
       if (err != cudaSuccess) return err;
       const size_t target = device_max_smem_optin() - fa.sharedSizeBytes;
-      if (target < sl.total) {
+      if (target < plan.smem.total) {
         g_launch_stage = "shared memory limit";
         return cudaErrorInvalidValue;
       }
@@ -894,21 +1032,24 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   }
   int per_sm = 0;
   g_launch_stage = "cudaOccupancyMaxActiveBlocksPerMultiprocessor";
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, sl.total);
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, warps * 32, plan.smem.total);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  // Upper bound on work items: every routed pair its own entry.
-  const int entries_max = a.ids ? a.ntok * a.top_k : (a.ntok + want_nv - 1) / want_nv;
-  const long items = (long)entries_max * p.row_tiles;
-  // One wave, kCtasPerSm per SM; no CTA without an item.
-  long grid = (long)device_sm_count() * (per_sm < kCtasPerSm ? per_sm : kCtasPerSm);
-  if (grid > items) grid = items;
-  if (grid < 1) grid = 1;
+  if (per_sm < kCtasPerSm) {
+    // fewer CTAs fit: more items per CTA (the plan's smem only grows by the
+    // split-K slots, which the opt-in above already covers up to its limit)
+    plan = plan_launch(a, device_sm_count(), per_sm);
+    g_launch_stage = "shared memory limit";
+    if (plan.smem.total > device_max_smem_optin()) return cudaErrorInvalidValue;
+  }
+  p.splits = plan.splits;
+  p.split_chunks = plan.split_chunks;
+  p.items_per_cta = plan.items_per_cta;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)plan.grid);
   cfg.blockDim = dim3(warps * 32);
-  cfg.dynamicSmemBytes = sl.total;
+  cfg.dynamicSmemBytes = plan.smem.total;
   cfg.stream = a.stream;
   // Programmatic dependent launch lets this grid start while the previous
   // kernel in the stream drains; the kernel waits (griddepcontrol.wait) before
