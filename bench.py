@@ -292,7 +292,9 @@ def run_ours(args):
     g = qi.rng(1000 + rank)
     ids_host = np.stack([np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(L)]) for _ in range(total_steps)])
     ids_all = torch.from_numpy(ids_host).to(dev)               # [steps][layers][1][4]
-    ids_buf = torch.empty(L, 1, TOP_K, dtype=torch.int32, device=dev)
+    ids_sel = torch.empty(1, L, 1, TOP_K, dtype=torch.int32, device=dev)
+    ids_buf = ids_sel[0]                                       # the step's ids, [layers][1][4]
+    step_idx = torch.zeros(1, dtype=torch.long, device=dev)
     ws = torch.zeros(qmv.qmv_moe_layer_workspace_bytes(desc_gu, 1, TOP_K), dtype=torch.uint8, device=dev)
     layer_flags = qmv.QMV_FLAG_PREFETCH_INPUTS
     per_layer = 2
@@ -300,12 +302,22 @@ def run_ours(args):
 
     def step():
         """One decode token through all layers (fused gate/up/SwiGLU, then down).
-        The step's weights and ids are never written by a kernel of the step
-        (ids are copied in before it), so every layer may prefetch them while
-        the preceding kernel drains."""
+        The weights and the step's ids are not written by the kernel right
+        before any layer's launch, so every layer may prefetch them while the
+        preceding kernel drains."""
         for l in range(L):
             qmv.qmv_moe_layer(desc_gu, W_gu[l], desc_dn, W_dn[l], x_dev, ids_buf[l], 1, TOP_K, ws, y[l],
                               layer_flags)
+
+    def graph_step():
+        """The step as captured: the step's router ids are picked on the device
+        (ids_all[step_idx], standing in for the router producing them in the
+        same stream), then the counter advances -- in that order, so the
+        kernel right before the first layer does not write the ids -- then
+        the layers."""
+        torch.index_select(ids_all, 0, step_idx, out=ids_sel)
+        step_idx.add_(1).remainder_(total_steps)
+        step()
 
     # eager warm-up (sets kernel attributes), then capture one step in a CUDA graph
     ids_buf.copy_(ids_all[0])
@@ -323,19 +335,19 @@ def run_ours(args):
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        step()
+        graph_step()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     with torch.cuda.graph(graph):
-        step()
+        graph_step()
+    step_idx.zero_()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(gpu_uuid(dev))
     sampler.start()
     time.sleep(0.3)
     for i in range(args.warmup):
-        ids_buf.copy_(ids_all[i])
-        graph.replay()
+        graph.replay()                                 # steps 0 .. W-1
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -343,8 +355,7 @@ def run_ours(args):
     wall0 = time.time()
     ev0.record()
     for i in range(args.steps):
-        ids_buf.copy_(ids_all[args.warmup + i])
-        graph.replay()
+        graph.replay()                                 # steps W .. W+K-1
     ev1.record()
     torch.cuda.synchronize()
     barrier()
@@ -352,7 +363,6 @@ def run_ours(args):
     # keep the same work running until the sampler has seen >= 1.5 s of it
     while time.time() - wall0 < 1.5:
         for i in range(20):
-            ids_buf.copy_(ids_all[i % total_steps])
             graph.replay()
         torch.cuda.synchronize()
     wall2 = time.time()
@@ -385,11 +395,13 @@ def run_ours(args):
     y_host = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
     n_e2e = min(args.steps, 50)
     torch.cuda.synchronize()
+    cur = int(step_idx.item())                         # the id slot the next replay reads
     t0 = time.perf_counter()
     for i in range(n_e2e):
         x_dev.view(torch.int16).copy_(x_host, non_blocking=True)
-        ids_buf.copy_(ids_host_p[args.warmup + i], non_blocking=True)
+        ids_all[cur].copy_(ids_host_p[args.warmup + i], non_blocking=True)
         graph.replay()
+        cur = (cur + 1) % total_steps
         y_host.copy_(y, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     t_e2e = time.perf_counter() - t0
@@ -415,7 +427,7 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "layers": L, "experts": E, "top_k": TOP_K, "N": N, "K": K,
                        "ntok": 1, "weight_bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2: 1.27 GB of expert weights per step, fresh ids every step",
-                       "launch": f"CUDA graph of {2 * L} kernels per step ({L} fused gate/up/SwiGLU gathers + {L} down gathers, qmv_moe_layer), programmatic dependent launch with weight/id prefetch",
+                       "launch": f"one CUDA graph per step: the step's router ids picked on the device (index_select at a device step counter), then {2 * L} kernels ({L} fused gate/up/SwiGLU gathers + {L} down gathers, qmv_moe_layer), programmatic dependent launch with weight/id prefetch",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "clocks": clocks, "e2e": e2e,
             "gpu_launches": args.steps * L * per_layer, "cpu_baseline": cpu, "device_status": status,

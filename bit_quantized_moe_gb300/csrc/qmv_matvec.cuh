@@ -53,6 +53,17 @@ struct Shape {
 };
 constexpr int kCtasPerSm = 2;
 
+// Tile copies per warp issued before griddepcontrol.wait in a prefetching
+// launch; the rest follow the activation loads, which would otherwise queue
+// behind them. Measured best on GB300 (same-box timings of every workload
+// config): none for MXFP4 one- and two-vector kernels, one for the codebook
+// ones, all for three- and four-vector kernels (their 3-stage rings and
+// heavier arithmetic hide the activation latency).
+template <int FMT, int NV>
+struct EarlyTiles {
+  static constexpr int value = (NV >= 3) ? Shape<NV>::stages : (FMT == MXFP4 ? 0 : 1);
+};
+
 inline void launch_shape(int nv, int& warps, int& stages) {
   switch (nv) {
     case 1: warps = Shape<1>::warps; stages = Shape<1>::stages; break;
@@ -379,32 +390,48 @@ __device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* 
   *xinv_slot = pow2f(-sh);
 }
 
+// Each staging function issues the loads of its first round (every thread's
+// first units), then calls mid() -- uniformly, from every thread -- and only
+// then converts and stores: loads issued before the caller's tile copies sit
+// ahead of them in the memory queue.
+__device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, int g0, int n, int groups, uint32_t vec_bytes,
+                                                  uint32_t (&w)[kStageU][16]) {
+#pragma unroll
+  for (int u = 0; u < kStageU; ++u) {
+    const int gi = g0 + u * blockDim.x;
+    if (gi < n) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(gi / groups) * vec_bytes + (size_t)(gi % groups) * 64);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = src[q];
+        w[u][4 * q] = v.x; w[u][4 * q + 1] = v.y; w[u][4 * q + 2] = v.z; w[u][4 * q + 3] = v.w;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_groups_mxfp4(uint8_t* xs, float* xinv, int g0, int n, int groups,
+                                                   uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
+#pragma unroll
+  for (int u = 0; u < kStageU; ++u) {
+    const int gi = g0 + u * blockDim.x;
+    if (gi < n) convert_group_mxfp4(w[u], xs + (size_t)(gi / groups) * vec_bytes + (size_t)(gi % groups) * 64, xinv + gi);
+  }
+}
+
+template <class Mid>
 __device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, int nvec, int K,
-                                              uint32_t vec_bytes) {
+                                              uint32_t vec_bytes, Mid&& mid) {
   const int groups = K / 32;
   const int n = nvec * groups;
-  for (int g0 = threadIdx.x; g0 < n; g0 += kStageU * blockDim.x) {
-    uint32_t w[kStageU][16];
-#pragma unroll
-    for (int u = 0; u < kStageU; ++u) {
-      const int gi = g0 + u * blockDim.x;
-      if (gi < n) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(gi / groups) * vec_bytes +
-                                                          (size_t)(gi % groups) * 64);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = src[q];
-          w[u][4 * q] = v.x; w[u][4 * q + 1] = v.y; w[u][4 * q + 2] = v.z; w[u][4 * q + 3] = v.w;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kStageU; ++u) {
-      const int gi = g0 + u * blockDim.x;
-      if (gi < n) {
-        convert_group_mxfp4(w[u], xs + (size_t)(gi / groups) * vec_bytes + (size_t)(gi % groups) * 64, xinv + gi);
-      }
-    }
+  const int step = kStageU * blockDim.x;
+  uint32_t w[kStageU][16];
+  load_groups_mxfp4(x, threadIdx.x, n, groups, vec_bytes, w);
+  mid();
+  store_groups_mxfp4(xs, xinv, threadIdx.x, n, groups, vec_bytes, w);
+  for (int g0 = threadIdx.x + step; g0 < n; g0 += step) {
+    load_groups_mxfp4(x, g0, n, groups, vec_bytes, w);
+    store_groups_mxfp4(xs, xinv, g0, n, groups, vec_bytes, w);
   }
 }
 
@@ -438,50 +465,60 @@ __device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t*
   reinterpret_cast<__half*>(out + K)[blk] = __float2half_rn(d);
 }
 
-__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, int nvec, int K, uint32_t vec_bytes) {
+__device__ __forceinline__ void load_block_f32(const float* x, int bi, int n, int blocks, int K, float (&f)[32]) {
+  if (bi < n) {
+    const float4* src = reinterpret_cast<const float4*>(x + (size_t)(bi / blocks) * K + (size_t)(bi % blocks) * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = src[i];
+      f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
+    }
+  }
+}
+
+template <class Mid>
+__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, int nvec, int K, uint32_t vec_bytes,
+                                                  Mid&& mid) {
   const int blocks = K / 32;
   const int n = nvec * blocks;
-  constexpr int U = 1;
-  for (int b0 = threadIdx.x; b0 < n; b0 += U * blockDim.x) {
-    float f[U][32];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int bi = b0 + u * blockDim.x;
-      if (bi < n) {
-        const float4* src = reinterpret_cast<const float4*>(x + (size_t)(bi / blocks) * K + (size_t)(bi % blocks) * 32);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v = src[i];
-          f[u][4 * i] = v.x; f[u][4 * i + 1] = v.y; f[u][4 * i + 2] = v.z; f[u][4 * i + 3] = v.w;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int bi = b0 + u * blockDim.x;
-      if (bi < n) quantize_block_q8(f[u], xs + (size_t)(bi / blocks) * vec_bytes, K, bi % blocks);
-    }
+  float f[32];
+  int bi = threadIdx.x;
+  load_block_f32(x, bi, n, blocks, K, f);
+  mid();
+  for (;;) {
+    if (bi < n) quantize_block_q8(f, xs + (size_t)(bi / blocks) * vec_bytes, K, bi % blocks);
+    bi += blockDim.x;
+    if (bi >= n) break;
+    load_block_f32(x, bi, n, blocks, K, f);
   }
 }
 
 // Codebook activations (q8_1 vectors) are copied to shared memory as they are,
 // four 16-byte loads per thread in flight.
-__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, int nvec, uint32_t vec_bytes) {
+template <class Mid>
+__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, int nvec, uint32_t vec_bytes, Mid&& mid) {
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(xs);
   const int n = (int)((size_t)nvec * vec_bytes / 16);
-  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
-    uint4 v[4];
+  const int step = 4 * blockDim.x;
+  uint4 v[4];
+  bool first = true;
+  for (int i0 = threadIdx.x;; i0 += step) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * blockDim.x;
       if (i < n) v[u] = src[i];
+    }
+    if (first) {
+      mid();
+      first = false;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * blockDim.x;
       if (i < n) dst[i] = v[u];
     }
+    if (i0 + step >= n) break;
   }
 }
 
@@ -855,9 +892,12 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   wp.policy = l2_evict_first_policy();
   wp.iss_n = 0;
   cursor_to(wp, warp);
-  // Stage-major issue order (every warp's first tile, then every warp's
-  // second, ...) so that each warp's first tile arrives early in the burst.
-  for (int q = 0; q < ST; ++q) {
+  // Tile copies go out stage-major (every warp's first tile, then every
+  // warp's second, ...) so that each warp's first tile arrives early. With
+  // kFlagPrefetch the first kEarlyTiles per warp go out before the wait, the
+  // rest right after the activation loads (which must not queue behind them).
+  const int pre = early ? EarlyTiles<FMT, NV>::value : 0;
+  for (int q = 0; q < pre; ++q) {
     if (lane == 0) issue_next<ST>(wp);
     __syncthreads();
   }
@@ -881,12 +921,18 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
 
   // Activations: plain 16-byte loads by every thread (they do not queue
   // behind the tile copies), converted on the way for MXFP4.
+  auto issue_rest = [&]() {
+    for (int q = pre; q < ST; ++q) {
+      if (lane == 0) issue_next<ST>(wp);
+      __syncthreads();
+    }
+  };
   if constexpr (FMT == MXFP4) {
-    stage_x_mxfp4(p.x, xs, xinv, p.nvec, p.K, p.x_vec_bytes);
+    stage_x_mxfp4(p.x, xs, xinv, p.nvec, p.K, p.x_vec_bytes, issue_rest);
   } else if (p.flags & kFlagXF32) {
-    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, p.nvec, p.K, p.x_vec_bytes);
+    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, p.nvec, p.K, p.x_vec_bytes, issue_rest);
   } else {
-    stage_x_copy(p.x, xs, p.nvec, p.x_vec_bytes);
+    stage_x_copy(p.x, xs, p.nvec, p.x_vec_bytes, issue_rest);
   }
   __syncthreads();
 
