@@ -740,3 +740,32 @@ def test_x_f32_gather_equals_quantize_then_call(per_slot):
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
     assert torch.all(y2[2, 1] == 0)
     assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Split-K inside a CTA: uneven K ranges, sampled rows, run-to-run identity
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ntok", [1, 2, 3])
+def test_mxfp4_dense_split_k_uneven_ranges(ntok):
+    """6400 x 7168 MXFP4 (800 row tiles of 7 chunks): the one-vector kernel
+    cuts each row tile into 3 K ranges (3, 3, 1 chunks), the 2- and
+    3-vector kernels into 2 (4, 3). Sampled rows against the oracle; two runs
+    bit-identical."""
+    N, K = 6400, 7168
+    m = Matrices("mxfp4", N, K, 1, [0], seed=600)
+    g = qi.rng(601 + ntok)
+    x = qi.normal_bf16_bits(g, (ntok, K))
+    rows = np.unique(np.concatenate([g.choice(N, 96, replace=False), [0, 7, 8, N - 1]]))
+    outs = []
+    for _ in range(2):
+        y = torch.empty(ntok, N, dtype=torch.bfloat16, device=DEV)
+        qmv.qmv_dense(m.desc, m.w, to_dev(x), ntok, y)
+        outs.append(y.view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    got = bf16_to_np(torch.from_numpy(outs[0]).view(torch.bfloat16))[:, rows]
+    cs, ss = m.codes[0][rows], m.scales[0][rows]
+    ref = oracle.mxfp4_matvec(cs, ss, x)
+    absum = oracle.mxfp4_abs_products(cs, ss, x)
+    assert_close(got, ref, absum, True, f"mxfp4 dense split-K {N}x{K} ntok={ntok}")
+    assert status_clean()
