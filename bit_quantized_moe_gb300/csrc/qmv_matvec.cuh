@@ -217,18 +217,24 @@ __device__ int build_entries_warp(const KParams& p, Entry* ent, int* s_ids) {
 // Tile loads
 // ---------------------------------------------------------------------------
 
-// Work of a CTA: its items are b, b + G, b + 2G, ... (b = blockIdx.x, G =
-// gridDim.x: every CTA, and with a full grid every SM, gets the same number
-// within one); item k of the CTA is split into `splits` K ranges, and task
-// lt = k * splits + r (range r of item k) goes to warp lt % W. A warp streams
-// the tiles of its tasks, in order, through its ring. Lane 0 keeps the issue
-// cursor (the next task and chunk to copy).
+// Work of a CTA: its share of the n items, the same number within one for
+// every CTA (and, with a full grid, every SM). Calls whose vectors are shared
+// by all slots (dense, gate/up) deal items round-robin (CTA b: b, b + G,
+// ...), so that at any moment the grid streams neighbouring row tiles.
+// Per-slot gathers give each CTA a contiguous range, which lies within one or
+// two entries, so the CTA stages only those entries' vectors. Item k of the
+// CTA is split into `splits` K ranges, and task lt = k * splits + r (range r
+// of item k) goes to warp lt % W. A warp streams the tiles of its tasks, in
+// order, through its ring. Lane 0 keeps the issue cursor (the next task and
+// chunk to copy).
 struct WarpPipe {
   const KParams* p;   // the matrix (points into kernel parameter space)
   const Entry* ent;   // the work list
   uint32_t ring;      // shared address of this warp's stage 0
   uint32_t bars;      // shared address of this warp's mbarrier 0
   const uint8_t* ring_ptr;
+  int first;          // the CTA's first item
+  int stride;         // between the CTA's items (G round-robin, 1 contiguous)
   int n_tasks;        // tasks of this CTA
   int warps;          // W
   int iss_n;          // tiles issued so far
@@ -237,8 +243,23 @@ struct WarpPipe {
   uint64_t policy;
 };
 
-__device__ __forceinline__ int task_item(const KParams& p, int lt) {
-  return blockIdx.x + (lt / p.splits) * gridDim.x;
+__device__ __forceinline__ int task_item(const KParams& p, const WarpPipe& wp, int lt) {
+  return wp.first + (lt / p.splits) * wp.stride;
+}
+
+// The CTA's items first, first + stride, ... (count of them) out of n.
+__device__ __forceinline__ void cta_items(const KParams& p, int n, int& first, int& stride, int& count) {
+  const int b = blockIdx.x, G = gridDim.x;
+  if (p.per_slot) {
+    const int per = n / G, rem = n % G;
+    first = b * per + (b < rem ? b : rem);
+    count = per + (b < rem ? 1 : 0);
+    stride = 1;
+  } else {
+    first = b;
+    stride = G;
+    count = (b < n) ? (n - b + G - 1) / G : 0;
+  }
 }
 
 __device__ __forceinline__ void task_chunks(const KParams& p, int lt, int& c0, int& c1) {
@@ -252,7 +273,7 @@ __device__ __forceinline__ void cursor_to(WarpPipe& wp, int lt) {
   if (lt >= wp.n_tasks) return;
   const KParams& p = *wp.p;
   task_chunks(p, lt, wp.iss_c, wp.iss_c1);
-  const int item = task_item(p, lt);
+  const int item = task_item(p, wp, lt);
   const Entry& e = wp.ent[item / p.row_tiles];
   wp.iss_base = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)(item % p.row_tiles) * p.rowtile;
 }
@@ -394,13 +415,16 @@ __device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* 
 // first units), then calls mid() -- uniformly, from every thread -- and only
 // then converts and stores: loads issued before the caller's tile copies sit
 // ahead of them in the memory queue.
-__device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, int g0, int n, int groups, uint32_t vec_bytes,
-                                                  uint32_t (&w)[kStageU][16]) {
+// Units are numbered over the CTA's list of vectors: unit u is group (or
+// block, or piece) u % per_vec of vector vlist[u / per_vec].
+__device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, const int* vlist, int g0, int n, int groups,
+                                                  uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
 #pragma unroll
   for (int u = 0; u < kStageU; ++u) {
     const int gi = g0 + u * blockDim.x;
     if (gi < n) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(gi / groups) * vec_bytes + (size_t)(gi % groups) * 64);
+      const int v = vlist ? vlist[gi / groups] : gi / groups;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)v * vec_bytes + (size_t)(gi % groups) * 64);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 v = src[q];
@@ -410,28 +434,31 @@ __device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, int g0, int 
   }
 }
 
-__device__ __forceinline__ void store_groups_mxfp4(uint8_t* xs, float* xinv, int g0, int n, int groups,
-                                                   uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
+__device__ __forceinline__ void store_groups_mxfp4(uint8_t* xs, float* xinv, const int* vlist, int g0, int n,
+                                                   int groups, uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
 #pragma unroll
   for (int u = 0; u < kStageU; ++u) {
     const int gi = g0 + u * blockDim.x;
-    if (gi < n) convert_group_mxfp4(w[u], xs + (size_t)(gi / groups) * vec_bytes + (size_t)(gi % groups) * 64, xinv + gi);
+    if (gi < n) {
+      const int v = vlist ? vlist[gi / groups] : gi / groups, g = gi % groups;
+      convert_group_mxfp4(w[u], xs + (size_t)v * vec_bytes + (size_t)g * 64, xinv + v * groups + g);
+    }
   }
 }
 
 template <class Mid>
-__device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, int nvec, int K,
-                                              uint32_t vec_bytes, Mid&& mid) {
+__device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, const int* vlist, int nvl,
+                                              int K, uint32_t vec_bytes, Mid&& mid) {
   const int groups = K / 32;
-  const int n = nvec * groups;
+  const int n = nvl * groups;
   const int step = kStageU * blockDim.x;
   uint32_t w[kStageU][16];
-  load_groups_mxfp4(x, threadIdx.x, n, groups, vec_bytes, w);
+  load_groups_mxfp4(x, vlist, threadIdx.x, n, groups, vec_bytes, w);
   mid();
-  store_groups_mxfp4(xs, xinv, threadIdx.x, n, groups, vec_bytes, w);
+  store_groups_mxfp4(xs, xinv, vlist, threadIdx.x, n, groups, vec_bytes, w);
   for (int g0 = threadIdx.x + step; g0 < n; g0 += step) {
-    load_groups_mxfp4(x, g0, n, groups, vec_bytes, w);
-    store_groups_mxfp4(xs, xinv, g0, n, groups, vec_bytes, w);
+    load_groups_mxfp4(x, vlist, g0, n, groups, vec_bytes, w);
+    store_groups_mxfp4(xs, xinv, vlist, g0, n, groups, vec_bytes, w);
   }
 }
 
@@ -465,9 +492,11 @@ __device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t*
   reinterpret_cast<__half*>(out + K)[blk] = __float2half_rn(d);
 }
 
-__device__ __forceinline__ void load_block_f32(const float* x, int bi, int n, int blocks, int K, float (&f)[32]) {
+__device__ __forceinline__ void load_block_f32(const float* x, const int* vlist, int bi, int n, int blocks, int K,
+                                               float (&f)[32]) {
   if (bi < n) {
-    const float4* src = reinterpret_cast<const float4*>(x + (size_t)(bi / blocks) * K + (size_t)(bi % blocks) * 32);
+    const int v = vlist ? vlist[bi / blocks] : bi / blocks;
+    const float4* src = reinterpret_cast<const float4*>(x + (size_t)v * K + (size_t)(bi % blocks) * 32);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float4 v = src[i];
@@ -477,37 +506,44 @@ __device__ __forceinline__ void load_block_f32(const float* x, int bi, int n, in
 }
 
 template <class Mid>
-__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, int nvec, int K, uint32_t vec_bytes,
-                                                  Mid&& mid) {
+__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, const int* vlist, int nvl, int K,
+                                                  uint32_t vec_bytes, Mid&& mid) {
   const int blocks = K / 32;
-  const int n = nvec * blocks;
+  const int n = nvl * blocks;
   float f[32];
   int bi = threadIdx.x;
-  load_block_f32(x, bi, n, blocks, K, f);
+  load_block_f32(x, vlist, bi, n, blocks, K, f);
   mid();
   for (;;) {
-    if (bi < n) quantize_block_q8(f, xs + (size_t)(bi / blocks) * vec_bytes, K, bi % blocks);
+    if (bi < n) quantize_block_q8(f, xs + (size_t)(vlist ? vlist[bi / blocks] : bi / blocks) * vec_bytes, K, bi % blocks);
     bi += blockDim.x;
     if (bi >= n) break;
-    load_block_f32(x, bi, n, blocks, K, f);
+    load_block_f32(x, vlist, bi, n, blocks, K, f);
   }
 }
 
 // Codebook activations (q8_1 vectors) are copied to shared memory as they are,
 // four 16-byte loads per thread in flight.
 template <class Mid>
-__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, int nvec, uint32_t vec_bytes, Mid&& mid) {
+__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, const int* vlist, int nvl,
+                                             uint32_t vec_bytes, Mid&& mid) {
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(xs);
-  const int n = (int)((size_t)nvec * vec_bytes / 16);
+  const int per = (int)(vec_bytes / 16);
+  const int n = nvl * per;
   const int step = 4 * blockDim.x;
   uint4 v[4];
+  size_t at[4];
   bool first = true;
   for (int i0 = threadIdx.x;; i0 += step) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * blockDim.x;
-      if (i < n) v[u] = src[i];
+      at[u] = 0;
+      if (i < n) {
+        at[u] = vlist ? (size_t)vlist[i / per] * per + i % per : (size_t)i;
+        v[u] = src[at[u]];
+      }
     }
     if (first) {
       mid();
@@ -516,7 +552,7 @@ __device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, int 
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * blockDim.x;
-      if (i < n) dst[i] = v[u];
+      if (i < n) dst[at[u]] = v[u];
     }
     if (i0 + step >= n) break;
   }
@@ -796,7 +832,7 @@ __device__ __forceinline__ bool run_tasks(const KParams& p, int& q, WarpPipe& wp
                                           const float* xinv, float* part, int* cnt) {
   const int warp = threadIdx.x >> 5;
   for (int lt = warp; lt < wp.n_tasks; lt += wp.warps) {
-    const int item = task_item(p, lt);
+    const int item = task_item(p, wp, lt);
     const Entry& e = wp.ent[item / p.row_tiles];
     const int rt = item % p.row_tiles;
     const int k = lt / p.splits, range = lt % p.splits;
@@ -856,6 +892,8 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   __shared__ int s_nent;
 
   __shared__ int s_ids[kMaxEntries];
+  __shared__ int s_vlist[kMaxEntries];   // activation vectors this CTA's items use
+  __shared__ int s_nvl;
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * ST; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
@@ -883,8 +921,8 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   wp.p = &p;
   wp.ent = ent;
   wp.warps = W;
-  const int n_items = s_nent * p.row_tiles;
-  const int items_here = ((int)blockIdx.x < n_items) ? (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  int items_here = 0;
+  cta_items(p, s_nent * p.row_tiles, wp.first, wp.stride, items_here);
   wp.n_tasks = items_here * p.splits;
   wp.ring_ptr = ring + (size_t)warp * ST * p.full_tile;
   wp.ring = smem_addr(wp.ring_ptr);
@@ -901,6 +939,26 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     if (lane == 0) issue_next<ST>(wp);
     __syncthreads();
   }
+  // Per-slot gathers stage only the vectors of the entries the CTA's
+  // contiguous item range touches (listed here, after the first tile copies
+  // are out); other calls stage all vectors.
+  if (p.per_slot) {
+    if (warp == 0) {
+      uint32_t used = 0;
+      if (items_here > 0) {
+        const int e0 = wp.first / p.row_tiles, e1 = (wp.first + items_here - 1) / p.row_tiles;
+        for (int e = e0 + lane; e <= e1; e += 32) {
+          for (int m = 0; m < ent[e].nv; ++m) used |= 1u << ent[e].vec[m];
+        }
+      }
+      used = __reduce_or_sync(0xffffffffu, used);
+      if (used & (1u << lane)) s_vlist[__popc(used & ((1u << lane) - 1u))] = lane;
+      if (lane == 0) s_nvl = __popc(used);
+    }
+    __syncthreads();
+  }
+  const int* vlist = p.per_slot ? s_vlist : nullptr;
+  const int nvl = p.per_slot ? s_nvl : p.nvec;
   if (early) pdl_wait();
   // Dependents are released only after this kernel's own wait, so when one
   // starts, every kernel before this one is complete (what
@@ -928,11 +986,11 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     }
   };
   if constexpr (FMT == MXFP4) {
-    stage_x_mxfp4(p.x, xs, xinv, p.nvec, p.K, p.x_vec_bytes, issue_rest);
+    stage_x_mxfp4(p.x, xs, xinv, vlist, nvl, p.K, p.x_vec_bytes, issue_rest);
   } else if (p.flags & kFlagXF32) {
-    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, p.nvec, p.K, p.x_vec_bytes, issue_rest);
+    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, vlist, nvl, p.K, p.x_vec_bytes, issue_rest);
   } else {
-    stage_x_copy(p.x, xs, p.nvec, p.x_vec_bytes, issue_rest);
+    stage_x_copy(p.x, xs, vlist, nvl, p.x_vec_bytes, issue_rest);
   }
   __syncthreads();
 
