@@ -653,6 +653,64 @@ def run_configs(args):
     return 0
 
 
+def run_profile_config(args):
+    """A few eager calls of one config's call on a small resident expert set
+    (16 experts; full-size matrices), for ncu captures of the codebook and
+    dense kernels. Prints one status line, no JSON."""
+    import torch
+
+    import bit_quantized_moe_gb300 as qmv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = qi.rng(88)
+    cfg = args.profile_config
+    luts = {"cb2": qi.LUT_CB2, "cb3": qi.LUT_CB3, "cb4": qi.LUT_CB4}
+
+    def packed(fmt, n, N_, K_):
+        d = qmv.wdesc(fmt, N_, K_, n, luts.get(fmt))
+        c = qi.canonical_uniform_codes(g, (n, N_), K_, qi.FORMAT_BITS[fmt])
+        sc = qi.e8m0(g, (n, N_, K_ // qi.FORMAT_GROUP[fmt]))
+        return torch.from_numpy(qmv.qmv_pack_weights(d, c, sc)).to(dev), d
+
+    def q8(nvec, K_):
+        xq = torch.empty(qmv.qmv_act_q8_bytes(nvec, K_), dtype=torch.uint8, device=dev)
+        qmv.qmv_quantize_act_q8(torch.from_numpy(qi.normal_f32(g, (nvec, K_))).to(dev), nvec, K_, xq)
+        return xq
+
+    E, calls = 16, 6
+    if cfg == 0:
+        w, d = packed("mxfp4", 1, 2880, 2880)
+        x = torch.from_numpy(qi.normal_bf16_bits(g, (1, 2880)).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty(1, 2880, dtype=torch.bfloat16, device=dev)
+        fn = lambda i: qmv.qmv_dense(d, w, x, 1, y)
+    elif cfg == 2:
+        dg = qmv.wdesc("cb2", 2048, 7168, E, qi.LUT_CB2)
+        c1 = qi.canonical_uniform_codes(g, (E, 2048), 7168, 2)
+        c2 = qi.canonical_uniform_codes(g, (E, 2048), 7168, 2)
+        s1, s2 = qi.e8m0(g, (E, 2048, 7168 // 16)), qi.e8m0(g, (E, 2048, 7168 // 16))
+        w = torch.from_numpy(qmv.qmv_pack_gate_up(dg, c1, s1, c2, s2)).to(dev)
+        xq = q8(1, 7168)
+        ids = torch.from_numpy(np.stack([qi.topk_ids(g, 1, 4, E) for _ in range(calls)])).to(dev)
+        h = torch.empty(1, 4, 2048, dtype=torch.float32, device=dev)
+        fn = lambda i: qmv.qmv_moe_gate_up_swiglu(dg, w, xq, ids[i], 1, 4, h)
+    elif cfg == 3:
+        w, d = packed("cb3", E, 7168, 2048)
+        xq = q8(16, 2048)
+        ids = torch.from_numpy(np.stack([qi.topk_ids(g, 4, 4, E) for _ in range(calls)])).to(dev)
+        y = torch.empty(4, 4, 7168, dtype=torch.float32, device=dev)
+        fn = lambda i: qmv.qmv_moe_gather(d, w, xq, 1, ids[i], 4, 4, y)
+    else:
+        w, d = packed("cb4", 1, 7168, 7168)
+        xq = q8(1, 7168)
+        y = torch.empty(1, 7168, dtype=torch.float32, device=dev)
+        fn = lambda i: qmv.qmv_dense(d, w, xq, 1, y)
+    for i in range(calls):
+        fn(i)
+    torch.cuda.synchronize()
+    print(f"profile-config {cfg}: {calls} calls, device status {qmv.qmv_device_status(clear=True)}", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -667,6 +725,8 @@ def main(argv=None):
     ap.add_argument("--digest", action="store_true", help="print the kernel source digest and exit")
     ap.add_argument("--configs", action="store_true",
                     help="measure every config of the workload set (one JSON line per call type) and exit")
+    ap.add_argument("--profile-config", type=int, choices=[0, 2, 3, 4], default=None,
+                    help="a few eager calls of one config on a small resident set, for ncu captures")
     args = ap.parse_args(argv)
     if args.digest:
         print(kernel_source_digest())
@@ -677,6 +737,8 @@ def main(argv=None):
         return run_reference(args)
     if args.configs:
         return run_configs(args)
+    if args.profile_config is not None:
+        return run_profile_config(args)
     return run_ours(args)
 
 
