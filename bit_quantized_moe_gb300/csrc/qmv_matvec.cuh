@@ -3,16 +3,18 @@
 //
 // Work decomposition. A "work item" is one row tile (kRows rows) of one
 // matrix applied to up to NV activation vectors (the "entry": an expert and
-// the (token, slot) pairs routed to it). Items are dealt round-robin over the
-// CTAs of a one-wave grid, then over each CTA's warps. A warp streams its
-// items' tiles -- one tile per K chunk -- through a private ring of
-// shared-memory stages (Shape::stages) filled by bulk
-// asynchronous copies (one elected lane issues them, an mbarrier per stage
-// tracks completion). Lane l of the warp owns columns [32 l, 32 l + 32) of
-// every chunk for all kRows rows, so the activations it needs are loaded into
-// registers once per chunk and reused for kRows rows. After the last chunk a
-// warp reduce-scatter (shuffles) leaves each (row, vector) sum in one lane,
-// which applies nothing further and stores it.
+// the (token, slot) pairs routed to it). Items are shared out evenly over the
+// CTAs of a one-wave grid (round-robin, or contiguous ranges for per-slot
+// gathers), an item may be cut into K ranges (split-K, for calls with few
+// items), and the resulting tasks are dealt over each CTA's warps. A warp
+// streams its tasks' tiles -- one tile per K chunk -- through a private ring
+// of shared-memory stages (Shape::stages) filled by bulk asynchronous copies
+// (one elected lane issues them, an mbarrier per stage tracks completion).
+// Lane l of the warp owns columns [32 l, 32 l + 32) of every chunk for all
+// kRows rows, so the activations it needs are loaded into registers once per
+// chunk and reused for kRows rows. After the task's last chunk a warp
+// reduce-scatter (shuffles) leaves each (row, vector) sum in one lane group,
+// which stores it (or, under split-K, parks it for the item's last range).
 //
 // Per format (lane-block encodings are defined in qmv_layout.h):
 //   MXFP4: E2M1 nibbles -> f16x2 with cvt.rn.f16x2.e2m1x2, mixed-precision
