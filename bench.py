@@ -193,15 +193,25 @@ def make_pool(n: int, seed: int):
     return canon, scales, x
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed (string
+    literals kept), so that comment edits leave the digest unchanged."""
+    import re
+    pat = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'', re.S)
+    text = pat.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest() -> str:
-    """sha256 over the CUDA sources and headers of the library (kernel identity)."""
+    """sha256 over the code (comments stripped) of the library's CUDA sources
+    and headers: the kernel identity the committed ncu summary refers to."""
     import hashlib
     d = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_quantized_moe_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                d.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                d.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return d.hexdigest()
 
 
