@@ -32,8 +32,9 @@ Readings taken where the pages are silent (each is listed in the design doc):
     byte at bits [2j, 2j+2); CB3 code j of a 3-byte group at bits [3j, 3j+3)
     of the little-endian 24-bit word.
   * MoE layer: plain SwiGLU h = silu(g) * u between gate/up and down, no
-    biases, no clamp, per-slot outputs (no router-weighted combine); g, u, h
-    and y are rounded to bf16 where the GPU path stores bf16.
+    biases, no clamp, per-slot outputs; g, u, h and y are rounded to bf16
+    where the GPU path stores bf16. The optional combine weights the per-slot
+    outputs by the router's top-k weights and sums them (moe_combine).
 
 Parity status: every function below is pinned by the not-gpu tests in
 tests/test_oracle_pins.py except where a docstring says "parity unpinned".
@@ -456,3 +457,25 @@ def swiglu_tolerance(g, u, tol_g, tol_u):
     u = np.asarray(u, dtype=np.float64)
     return 1.1 * np.abs(u) * tol_g + np.abs(silu(g)) * tol_u + 1.1 * tol_g * tol_u
 
+
+
+def moe_combine(y_slots, weights, ids, n_experts: int):
+    """Router-weighted combine of a MoE layer's per-slot expert outputs:
+    out[t] = sum_j weights[t, j] * y_slots[t, j] over the slots j whose id is
+    in [0, n_experts) (an invalid id contributes nothing), in float64.
+
+    y_slots [ntok, top_k, N], weights and ids [ntok, top_k]. The pages print
+    the switch-GLU part of the gpt-oss layer (per-slot outputs of the top-k
+    experts) [mlxcel-2178, "Current Behavior": GptOssSwitchGLU]; weighting
+    those outputs by the router's top-k weights and summing them is the MoE
+    block's combine (a reading: the pages do not print it).
+    """
+    y_slots = np.asarray(y_slots, dtype=np.float64)
+    weights = np.asarray(weights, dtype=np.float64)
+    ntok, top_k, N = y_slots.shape
+    out = np.zeros((ntok, N), dtype=np.float64)
+    for t in range(ntok):
+        for j in range(top_k):
+            if 0 <= int(ids[t, j]) < n_experts:
+                out[t] += weights[t, j] * y_slots[t, j]
+    return out

@@ -546,3 +546,40 @@ def test_mutation_invalid_id_not_zeroed(monkeypatch):
         return real(matvec, n_experts, np.clip(ids, 0, n_experts - 1), per_slot, N)
     monkeypatch.setattr(O, "moe_gather", bad)
     assert _fails_some_pin([pin_gather])
+
+
+# ---------------------------------------------------------------------------
+# Router-weighted combine of per-slot outputs
+# ---------------------------------------------------------------------------
+
+def pin_combine():
+    """Exact rational check of out[t] = sum of w * y over valid slots, on a
+    small case with an invalid id (its slot must not contribute), plus the
+    one-hot special case (it selects a slot)."""
+    g = np.random.default_rng(5)
+    ntok, top_k, N, E = 2, 3, 5, 4
+    y = g.integers(-8, 9, size=(ntok, top_k, N)).astype(np.float64) / 4
+    w = g.integers(1, 9, size=(ntok, top_k)).astype(np.float64) / 8
+    ids = np.array([[0, 3, 1], [2, 7, 1]], dtype=np.int32)     # id 7 invalid
+    got = O.moe_combine(y, w, ids, E)
+    for t in range(ntok):
+        for n in range(N):
+            want = sum((Fraction(w[t, j]) * Fraction(y[t, j, n]) for j in range(top_k) if 0 <= ids[t, j] < E),
+                       Fraction(0))
+            assert Fraction(got[t, n]) == want
+    onehot = np.zeros((ntok, top_k))
+    onehot[:, 2] = 1.0
+    assert np.array_equal(O.moe_combine(y, onehot, ids, E), y[:, 2])
+
+
+def test_combine_pin():
+    pin_combine()
+
+
+def test_mutation_combine_ignores_invalid(monkeypatch):
+    real = O.moe_combine
+
+    def bad(y_slots, weights, ids, n_experts):
+        return real(y_slots, weights, np.clip(ids, 0, n_experts - 1), n_experts)
+    monkeypatch.setattr(O, "moe_combine", bad)
+    assert _fails_some_pin([pin_combine])
