@@ -660,6 +660,14 @@ def run_configs(args):
     t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgm, Wgm[l], ddm, Wdm[l], xm, idsm[l], 1, TOP_K, wsm,
                                                          ym[l], PF) for l in range(Lm)])
     emit(1, "qmv_moe_layer MXFP4 2880 E=32 top4 ntok=1 (2 launches)", LAYER_BYTES, t / Lm, {"calls_per_graph": Lm})
+    # the same layer with the router-weighted combine of its top-k outputs
+    rw = torch.from_numpy(np.stack([qi.router_weights(g, 1, TOP_K) for _ in range(Lm)])).to(dev)
+    wsc = torch.zeros(qmv.qmv_moe_layer_combine_workspace_bytes(dgm, ddm, 1, TOP_K), dtype=torch.uint8, device=dev)
+    yc = torch.empty(Lm, 1, K, dtype=torch.bfloat16, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer_combine(dgm, Wgm[l], ddm, Wdm[l], xm, idsm[l], rw[l], 1,
+                                                                 TOP_K, wsc, yc[l], PF) for l in range(Lm)])
+    emit(1, "qmv_moe_layer_combine MXFP4 2880 E=32 top4 ntok=1 (3 launches)", LAYER_BYTES, t / Lm,
+         {"calls_per_graph": Lm})
     return 0
 
 

@@ -43,7 +43,7 @@ EXPORTS = (
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
     "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
     "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
-    "qmv_moe_layer_noalloc",
+    "qmv_moe_layer_noalloc", "qmv_moe_combine", "qmv_moe_layer_combine_workspace_bytes", "qmv_moe_layer_combine",
     "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
@@ -99,6 +99,9 @@ def _load() -> ctypes.CDLL:
         "qmv_moe_layer_workspace_bytes": (SZ, [D, I32, I32]),
         "qmv_moe_layer": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, SZ, P, ctypes.c_uint32, P]),
         "qmv_moe_layer_noalloc": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
+        "qmv_moe_combine": (ctypes.c_int, [D, P, P, P, I32, I32, P, P]),
+        "qmv_moe_layer_combine_workspace_bytes": (SZ, [D, D, I32, I32]),
+        "qmv_moe_layer_combine": (ctypes.c_int, [D, P, D, P, P, P, P, I32, I32, P, SZ, P, ctypes.c_uint32, P]),
         "qmv_moe_gather_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
@@ -281,6 +284,23 @@ def qmv_moe_layer_noalloc(gate_up_desc: WDesc, w_gate_up, down_desc: WDesc, w_do
     _check(lib.qmv_moe_layer_noalloc(ctypes.byref(gate_up_desc), _ptr(w_gate_up), ctypes.byref(down_desc),
                                      _ptr(w_down), _ptr(x), _ptr(ids), ntok, top_k, _ptr(y), int(flags),
                                      _stream(stream)))
+
+
+def qmv_moe_combine(down_desc: WDesc, ys, weights, ids, ntok: int, top_k: int, y, stream=None) -> None:
+    _check(lib.qmv_moe_combine(ctypes.byref(down_desc), _ptr(ys), _ptr(weights), _ptr(ids), ntok, top_k, _ptr(y),
+                               _stream(stream)))
+
+
+def qmv_moe_layer_combine_workspace_bytes(gate_up_desc: WDesc, down_desc: WDesc, ntok: int, top_k: int) -> int:
+    return lib.qmv_moe_layer_combine_workspace_bytes(ctypes.byref(gate_up_desc), ctypes.byref(down_desc), ntok,
+                                                     top_k)
+
+
+def qmv_moe_layer_combine(gate_up_desc: WDesc, w_gate_up, down_desc: WDesc, w_down, x, ids, weights, ntok: int,
+                          top_k: int, workspace, y, flags: int = 0, stream=None) -> None:
+    _check(lib.qmv_moe_layer_combine(ctypes.byref(gate_up_desc), _ptr(w_gate_up), ctypes.byref(down_desc),
+                                     _ptr(w_down), _ptr(x), _ptr(ids), _ptr(weights), ntok, top_k,
+                                     _ptr(workspace), _nbytes(workspace), _ptr(y), int(flags), _stream(stream)))
 
 
 def qmv_swiglu_bf16(g, u, h, n: int, stream=None) -> None:

@@ -93,6 +93,62 @@ cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n,
 }
 
 // ---------------------------------------------------------------------------
+// Router-weighted combine of per-slot outputs: y[t][n] = sum over valid slots
+// j (ids[t][j] in [0, E)) of w[t][j] * ys[t][j][n], fp32 fma in slot order
+// (the same order every run), stored as T. Thread per output element.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float load_out(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float load_out(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ void store_val(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store_val(float* p, int64_t i, float v) { p[i] = v; }
+
+template <typename T>
+__global__ void combine_kernel(const T* __restrict__ ys, const float* __restrict__ w, const int32_t* __restrict__ ids,
+                               int ntok, int top_k, int n_experts, int N, T* __restrict__ y) {
+  pdl_wait();
+  const int64_t total = (int64_t)ntok * N;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / N);
+    const int n = (int)(i % N);
+    float acc = 0.0f;
+    for (int j = 0; j < top_k; ++j) {
+      const int s = t * top_k + j;
+      const int e = ids[s];
+      if (e < 0 || e >= n_experts) continue;
+      acc = fmaf(w[s], load_out(ys, (int64_t)s * N + n), acc);
+    }
+    store_val(y, i, acc);
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_combine(bool bf16, const void* ys, const float* w, const int32_t* ids, int ntok, int top_k,
+                           int n_experts, int N, void* y, cudaStream_t s) {
+  const int threads = 256;
+  const long total = (long)ntok * N;
+  long grid = (total + threads - 1) / threads;
+  const long cap = (long)device_sm_count() * 4;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  // Programmatic dependent launch after the down gather that produced ys.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (s != nullptr) ? 1 : 0;
+  if (bf16) {
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(ys), w, ids,
+                              ntok, top_k, n_experts, N, static_cast<__nv_bfloat16*>(y));
+  }
+  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, static_cast<const float*>(ys), w, ids, ntok, top_k,
+                            n_experts, N, static_cast<float*>(y));
+}
+
+// ---------------------------------------------------------------------------
 // Weight-layout decoder: one warp per tile, the matvec kernels' decode
 // routines, out[n][k] = value(code) * 2^(e-127).
 // ---------------------------------------------------------------------------

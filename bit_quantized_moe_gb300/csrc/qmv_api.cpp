@@ -405,6 +405,44 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   return run_matvec(down, w_down, ws, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
 }
 
+int qmv_moe_combine(const qmv_wdesc* down, const void* ys, const float* weights, const int32_t* ids, int32_t ntok,
+                    int32_t top_k, void* y, void* stream) {
+  const char* name = "qmv_moe_combine";
+  int rc = check_desc(down);
+  if (rc) return rc;
+  if (!ys || !weights || !ids || !y) return fail(QMV_EINVAL, "%s: NULL pointer", name);
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK)
+    return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
+  if (!aligned16(ys) || !aligned16(weights) || !aligned16(ids) || !aligned16(y))
+    return fail(QMV_EALIGN, "%s: pointers must be 16-byte aligned", name);
+  cudaError_t e = launch_combine(down->fmt == QMV_MXFP4, ys, weights, ids, ntok, top_k, down->n_experts, down->N, y,
+                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+size_t qmv_moe_layer_combine_workspace_bytes(const qmv_wdesc* gu, const qmv_wdesc* down, int32_t ntok, int32_t top_k) {
+  const size_t layer = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
+  if (layer == 0 || check_desc(down)) return 0;
+  const size_t elem = (down->fmt == QMV_MXFP4) ? 2 : 4;
+  return layer + ((size_t)ntok * top_k * down->N * elem + 255) / 256 * 256;
+}
+
+int qmv_moe_layer_combine(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, const void* w_down,
+                          const void* x, const int32_t* ids, const float* weights, int32_t ntok, int32_t top_k,
+                          void* ws, size_t ws_bytes, void* y, uint32_t flags, void* stream) {
+  const char* name = "qmv_moe_layer_combine";
+  const size_t need = qmv_moe_layer_combine_workspace_bytes(gu, down, ntok, top_k);
+  if (need == 0) return fail(QMV_EINVAL, "%s: invalid descriptors, ntok or top_k", name);
+  if (ws == nullptr || ws_bytes < need) return fail(QMV_ESIZE, "%s: workspace %zu bytes < %zu", name, ws_bytes, need);
+  if (!weights || !y) return fail(QMV_EINVAL, "%s: NULL pointer", name);
+  const size_t layer = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
+  void* ys = static_cast<uint8_t*>(ws) + layer;
+  int rc = qmv_moe_layer(gu, w_gu, down, w_down, x, ids, ntok, top_k, ws, layer, ys, flags, stream);
+  if (rc) return rc;
+  return qmv_moe_combine(down, ys, weights, ids, ntok, top_k, y, stream);
+}
+
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
                          const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
                          size_t sums_bytes, void* stream) {

@@ -42,6 +42,8 @@ cudaError_t launch_matvec_cb4(const MatvecArgs& a);
 
 cudaError_t launch_quantize_q8(const float* x, int nvec, int K, void* xq, cudaStream_t s);
 cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n, cudaStream_t s);
+cudaError_t launch_combine(bool bf16, const void* ys, const float* w, const int32_t* ids, int ntok, int top_k,
+                           int n_experts, int N, void* y, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t lut[4], float* out,
                            cudaStream_t s);
 

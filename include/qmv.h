@@ -273,6 +273,38 @@ int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, cons
                   void* workspace_dev, size_t workspace_bytes, void* y_dev, uint32_t flags, void* stream);
 
 /*
+ * Router-weighted combine of a MoE layer's per-slot outputs:
+ *   y[t][n] = sum over j with ids[t][j] in [0, E) of weights[t][j] * ys[t][j][n]
+ * (fp32 fma in slot order, the same order every run). The pages print the
+ * switch-GLU part of the gpt-oss layer (per-slot outputs of the top-k experts,
+ * "perf(rocm): add an mxfp4 arm to the warp-shared gather_qmv kernel for
+ * gpt-oss decode", "Current Behavior": GptOssSwitchGLU); weighting and summing
+ * them is the MoE block's combine (a reading: the pages do not print it).
+ * down_desc: the down projection (N outputs, n_experts, format: MXFP4 -> ys
+ * and y bf16, codebooks -> fp32). ys [ntok][top_k][N] (as qmv_moe_layer's
+ * y), weights fp32 [ntok][top_k], ids int32 [ntok][top_k], y [ntok][N]; all
+ * on the device, 16-byte aligned. One launch (dependent launch after the
+ * kernel that wrote ys).
+ * Errors: QMV_EINVAL, QMV_ESHAPE, QMV_EALIGN, QMV_ECUDA.
+ */
+int qmv_moe_combine(const qmv_wdesc* down_desc, const void* ys_dev, const float* weights_dev,
+                    const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, void* stream);
+
+/*
+ * qmv_moe_layer followed by qmv_moe_combine: the layer's combined output
+ * y [ntok][N_down] (MXFP4 bf16, codebooks fp32) for router weights
+ * weights_dev fp32 [ntok][top_k]. The per-slot outputs live in the workspace,
+ * which needs qmv_moe_layer_combine_workspace_bytes(...) bytes (the layer's
+ * workspace followed by ntok * top_k * N_down outputs). Three launches.
+ */
+size_t qmv_moe_layer_combine_workspace_bytes(const qmv_wdesc* gate_up_desc, const qmv_wdesc* down_desc,
+                                             int32_t ntok, int32_t top_k);
+int qmv_moe_layer_combine(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, const qmv_wdesc* down_desc,
+                          const void* w_down_dev, const void* x_dev, const int32_t* ids_dev,
+                          const float* weights_dev, int32_t ntok, int32_t top_k, void* workspace_dev,
+                          size_t workspace_bytes, void* y_dev, uint32_t flags, void* stream);
+
+/*
  * qmv_moe_layer for callers that cannot allocate device memory. (No
  * counterpart on the pages this library follows; it exists for how the
  * library is embedded.) Some callers may not allocate GPU memory while they

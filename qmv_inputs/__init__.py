@@ -80,6 +80,12 @@ def topk_ids(g: np.random.Generator, ntok: int, top_k: int, n_experts: int) -> n
     return out
 
 
+def router_weights(g: np.random.Generator, ntok: int, top_k: int) -> np.ndarray:
+    """[ntok][top_k] fp32 positive top-k router weights, each token's summing
+    to about 1 (a flat Dirichlet draw)."""
+    return g.dirichlet(np.ones(top_k), size=ntok).astype(np.float32)
+
+
 @dataclasses.dataclass(frozen=True)
 class Recipe:
     """One synthetic workload: matrix shape, format and routing."""

@@ -769,3 +769,103 @@ def test_mxfp4_dense_split_k_uneven_ranges(ntok):
     absum = oracle.mxfp4_abs_products(cs, ss, x)
     assert_close(got, ref, absum, True, f"mxfp4 dense split-K {N}x{K} ntok={ntok}")
     assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Router-weighted combine of the per-slot outputs
+# ---------------------------------------------------------------------------
+
+def _combine_tol(ys, w, ids, E, want, bf16_out, slot_tol=None):
+    """fp32 fma chain over top_k slots: each step rounds once (2^-24 relative
+    of the running magnitude, bounded by sum|w y|); a bf16 result adds one ulp
+    (2^-8 relative). slot_tol: the bound on each per-slot input, weighted."""
+    ntok, top_k, N = ys.shape
+    valid = ((ids >= 0) & (ids < E)).astype(np.float64)[..., None]
+    aw = np.abs(w.astype(np.float64))[..., None] * valid
+    mag = (aw * np.abs(ys)).sum(axis=1)
+    tol = mag * (top_k + 1) * 2.0 ** -24
+    if slot_tol is not None:
+        tol = tol + (aw * slot_tol).sum(axis=1)
+    if bf16_out:
+        tol = tol + np.abs(want) * 2.0 ** -8
+    return tol
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("ntok,top_k,N", [(1, 4, 2880), (4, 8, 7168), (3, 1, 17), (2, 8, 4096)])
+def test_combine(dtype, ntok, top_k, N):
+    """qmv_moe_combine on given per-slot outputs against the oracle's float64
+    combine; invalid ids (negative and >= E) contribute nothing."""
+    E = 64
+    g = qi.rng(500 + ntok * 37 + top_k + N)
+    ids = np.stack([g.permutation(E)[:top_k] for _ in range(ntok)]).astype(np.int32)
+    if top_k > 1:
+        ids[0, 1] = -1
+        ids[-1, 0] = E + 3
+    w = qi.router_weights(g, ntok, top_k)
+    fmt = "mxfp4" if dtype == "bf16" else "cb3"
+    desc = qmv.wdesc(fmt, N, 64, E, lut=LUTS.get(fmt))
+    if dtype == "bf16":
+        bits = qi.normal_bf16_bits(g, (ntok, top_k, N))
+        ys_np = oracle.bf16_bits_to_f64(bits)
+        ys = to_dev(bits).view(torch.bfloat16)
+        y = torch.full((ntok, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    else:
+        f = qi.normal_f32(g, (ntok, top_k, N))
+        ys_np = f.astype(np.float64)
+        ys = to_dev(f)
+        y = torch.full((ntok, N), 3.0, dtype=torch.float32, device=DEV)
+    qmv.qmv_moe_combine(desc, ys, to_dev(w), to_dev(ids), ntok, top_k, y)
+    want = oracle.moe_combine(ys_np, w, ids, E)
+    got = bf16_to_np(y) if dtype == "bf16" else y.cpu().numpy().astype(np.float64)
+    tol = _combine_tol(ys_np, w, ids, E, want, dtype == "bf16")
+    err = np.abs(got - want)
+    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined outputs outside tolerance"
+    assert status_clean()
+
+
+def test_combine_all_invalid_gives_zero():
+    E, ntok, top_k, N = 8, 2, 4, 256
+    g = qi.rng(520)
+    ids = np.full((ntok, top_k), -1, dtype=np.int32)
+    ids[1] = [E, E + 1, -7, 2 ** 31 - 1]
+    w = qi.router_weights(g, ntok, top_k)
+    ys = to_dev(qi.normal_f32(g, (ntok, top_k, N)))
+    y = torch.full((ntok, N), 9.0, dtype=torch.float32, device=DEV)
+    qmv.qmv_moe_combine(qmv.wdesc("cb4", N, 64, E, lut=qi.LUT_CB4), ys, to_dev(w), to_dev(ids), ntok, top_k, y)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y).item() == 0
+    assert status_clean()
+
+
+@pytest.mark.parametrize("pair", LAYER_PAIRS, ids=lambda p: f"{p[0]}-{p[1]}")
+@pytest.mark.parametrize("ntok,top_k", [(1, 4), (4, 2)])
+def test_layer_combine(pair, ntok, top_k):
+    """qmv_moe_layer_combine against the oracle chain (gate/up, SwiGLU, down,
+    combine), and bit for bit against qmv_moe_layer followed by
+    qmv_moe_combine."""
+    fmt_gu, fmt_dn, N, K, E = pair
+    ids, gu, down, x, xin, q, d, xf, dt = _layer_case(fmt_gu, fmt_dn, N, K, E, ntok, top_k, 600 + ntok * 10 + top_k)
+    g = qi.rng(650 + ntok + top_k)
+    w = qi.router_weights(g, ntok, top_k)
+    ids_d, w_d = to_dev(ids), to_dev(w)
+    nbytes = qmv.qmv_moe_layer_combine_workspace_bytes(gu.desc, down.desc, ntok, top_k)
+    assert nbytes >= qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k) + ntok * top_k * K * (2 if dt == torch.bfloat16 else 4)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    y = torch.full((ntok, K), 7.0, dtype=dt, device=DEV)
+    qmv.qmv_moe_layer_combine(gu.desc, gu.w, down.desc, down.w, xin, ids_d, w_d, ntok, top_k, ws, y)
+    slots, slot_tol = _layer_expected(gu, down, ids, x=x, q=q, d=d)
+    want = oracle.moe_combine(slots, w, ids, E)
+    tol = _combine_tol(slots, w, ids, E, want, dt == torch.bfloat16, slot_tol)
+    got = bf16_to_np(y) if dt == torch.bfloat16 else y.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined layer outputs outside tolerance"
+    ws2 = torch.empty(qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k), dtype=torch.uint8, device=DEV)
+    ys = torch.empty(ntok, top_k, K, dtype=dt, device=DEV)
+    qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xin, ids_d, ntok, top_k, ws2, ys)
+    y2 = torch.full_like(y, -7.0)
+    qmv.qmv_moe_combine(down.desc, ys, w_d, ids_d, ntok, top_k, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                       y2.view(torch.int16 if dt == torch.bfloat16 else torch.int32))
+    assert status_clean()

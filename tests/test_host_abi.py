@@ -257,3 +257,28 @@ def test_moe_layer_argument_errors():
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
     d = qmv.wdesc("mxfp4", 64, 64)
     assert qmv.lib.qmv_dense_ex(B(d), FAKE, FAKE, 1, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
+
+
+def test_combine_argument_errors():
+    B = qmv.ctypes.byref
+    dn = qmv.wdesc("mxfp4", 2880, 2880, 32)
+    C = qmv.lib.qmv_moe_combine
+    assert C(B(dn), None, FAKE, FAKE, 1, 4, FAKE, 0) == qmv.QMV_EINVAL
+    assert C(B(dn), FAKE, None, FAKE, 1, 4, FAKE, 0) == qmv.QMV_EINVAL
+    assert C(B(dn), FAKE, FAKE, FAKE, 0, 4, FAKE, 0) == qmv.QMV_EINVAL
+    assert C(B(dn), FAKE, FAKE, FAKE, 1, 9, FAKE, 0) == qmv.QMV_EINVAL
+    assert C(B(dn), FAKE, FAKE + 4, FAKE, 1, 4, FAKE, 0) == qmv.QMV_EALIGN
+    assert C(None, FAKE, FAKE, FAKE, 1, 4, FAKE, 0) == qmv.QMV_EINVAL
+    gu = qmv.wdesc("mxfp4", 2880, 2880, 32)
+    layer = qmv.qmv_moe_layer_workspace_bytes(gu, 2, 4)
+    need = qmv.qmv_moe_layer_combine_workspace_bytes(gu, dn, 2, 4)
+    assert need == layer + (2 * 4 * 2880 * 2 + 255) // 256 * 256
+    cg = qmv.wdesc("cb2", 2048, 7168, 64)
+    cd = qmv.wdesc("cb3", 7168, 2048, 64)
+    assert qmv.qmv_moe_layer_combine_workspace_bytes(cg, cd, 1, 4) == 4 * 2048 * 4 + 4 * 7168 * 4
+    assert qmv.qmv_moe_layer_combine_workspace_bytes(cg, cd, 0, 4) == 0
+    L = qmv.lib.qmv_moe_layer_combine
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need - 16, FAKE, 0, 0) == qmv.QMV_ESIZE
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, None, 2, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, None, need, FAKE, 0, 0) == qmv.QMV_ESIZE
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need, FAKE, 4, 0) == qmv.QMV_EINVAL
