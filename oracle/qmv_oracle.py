@@ -21,10 +21,15 @@ Sources (web pages, cited by title and section):
                  on RDNA" (lucebox-hub PR #19)
   [geo-31]       "DS4 H200: rocmfp2_mix MoE matvec 3.31x + ROCmFP4 dense matvec
                  1.53x (+42.6% decode)" (geo-lucebox PR #31)
+  [OCP-MX]       the OCP Microscaling Formats (MX) v1.0 specification, for the
+                 E4M3 element of MXFP8, which the pages name but do not define
 
 Readings taken where the pages are silent (each is listed in the design doc):
   * E2M1 value table {0,.5,1,1.5,2,3,4,6} with the sign in bit 3 and E8M0
     scale 2**(e-127), e = 255 -> NaN (OCP MX convention).
+  * MXFP8: E4M3 elements (bias 7, subnormals, S.1111.111 = NaN, no
+    infinities) with one E8M0 scale per 32 weights, one code per byte; the
+    f16-activation variants take fp16 activations and store fp16 outputs.
   * q8_1: per 32-block, d = amax/127 in fp32, codes round(x/d) half away from
     zero, clamped to [-127, 127]; d stored as fp16 (RNE). The block-sum field
     of q8_1 is not stored because no dot product here reads it.
@@ -72,6 +77,27 @@ def e8m0_decode(e: np.ndarray) -> np.ndarray:
     e = np.asarray(e).astype(np.int64)
     v = np.ldexp(1.0, e - 127)
     return np.where(e == 255, np.nan, v)
+
+
+# E4M3 element of MXFP8 [OCP-MX]: sign bit 7, exponent bits 6..3 with bias 7,
+# mantissa bits 2..0. Exponent field 0 is subnormal (m/8 * 2**-6); the two
+# codes with every exponent and mantissa bit set are NaN; there is no
+# infinity. The pages list f16 MXFP4 and MXFP8 gathers as the next scope
+# beyond the bf16 MXFP4 arm [mlxcel-2178, "Scope": out of scope].
+MXFP8_GROUP = 32
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Value of each E4M3 byte, float64 (NaN for 0x7F and 0xFF)."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = (c >> 7) & 1
+    ex = (c >> 3) & 15
+    man = c & 7
+    normal = np.ldexp(1.0 + man / 8.0, ex - 7)
+    subnormal = np.ldexp(man / 8.0, -6)
+    mag = np.where(ex == 0, subnormal, normal)
+    v = np.where(sign == 1, -mag, mag)
+    return np.where((ex == 15) & (man == 7), np.nan, v)
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -185,6 +211,8 @@ def unpack_cb3(packed: np.ndarray) -> np.ndarray:
 
 
 def pack_codes(fmt: str, codes: np.ndarray) -> np.ndarray:
+    if fmt == "mxfp8":
+        return np.array(codes, dtype=np.uint8)         # one code per byte
     if fmt in ("mxfp4", "cb4"):
         return pack_nibbles(codes)
     if fmt == "cb2":
@@ -195,6 +223,8 @@ def pack_codes(fmt: str, codes: np.ndarray) -> np.ndarray:
 
 
 def unpack_codes(fmt: str, packed: np.ndarray) -> np.ndarray:
+    if fmt == "mxfp8":
+        return np.array(packed, dtype=np.uint8)
     if fmt in ("mxfp4", "cb4"):
         return unpack_nibbles(packed)
     if fmt == "cb2":
@@ -217,6 +247,13 @@ def mxfp4_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     K = codes.shape[-1]
     g = np.arange(K) // MXFP4_GROUP
     return e2m1_decode(codes) * e8m0_decode(scales)[..., g]
+
+
+def mxfp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """W[n, k] = e4m3(code[n, k]) * 2**(scale[n, k // 32] - 127), float64."""
+    K = codes.shape[-1]
+    g = np.arange(K) // MXFP8_GROUP
+    return e4m3_decode(codes) * e8m0_decode(scales)[..., g]
 
 
 def cb_dequant(codes: np.ndarray, scales: np.ndarray, lut, group: int) -> np.ndarray:
@@ -267,6 +304,13 @@ def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 
 
+def f64_to_f16_bits(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to fp16 (nearest-even, straight from float64: numpy's
+    float64 -> float16 conversion), returned as bit patterns."""
+    with np.errstate(over="ignore"):
+        return np.asarray(v, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
 # ---------------------------------------------------------------------------
 # Dot products
 # ---------------------------------------------------------------------------
@@ -311,22 +355,63 @@ def cb_abs_products(codes, scales, lut, group: int, q, d_bits) -> np.ndarray:
     return xq @ W.T
 
 
-def mxfp4_matvec(codes, scales, x_bits) -> np.ndarray:
+def act_bits_to_f64(bits: np.ndarray, x_dtype: str = "bf16") -> np.ndarray:
+    """Exact value of bf16 or fp16 activation bit patterns."""
+    if x_dtype == "bf16":
+        return bf16_bits_to_f64(bits)
+    if x_dtype == "f16":
+        return f16_bits_to_f64(bits)
+    raise ValueError(x_dtype)
+
+
+def mxfp4_matvec(codes, scales, x_bits, x_dtype: str = "bf16") -> np.ndarray:
     """MXFP4 x bf16 matvec y[v, n] = sum_k W[n, k] * x[v, k] in float64.
 
     W decoded per mxfp4_dequant; x are bf16 activations [mlxcel-2178,
-    "Current Behavior": bf16 activations, group size 32, no biases].
-    codes [N, K], scales [N, K/32], x_bits [V, K] uint16. Returns [V, N].
+    "Current Behavior": bf16 activations, group size 32, no biases], or fp16
+    ones for the f16 variant ("Scope"). codes [N, K], scales [N, K/32],
+    x_bits [V, K] uint16. Returns [V, N].
     """
     W = mxfp4_dequant(codes, scales)
-    x = bf16_bits_to_f64(x_bits)
+    x = act_bits_to_f64(x_bits, x_dtype)
     return x @ W.T
 
 
-def mxfp4_abs_products(codes, scales, x_bits) -> np.ndarray:
+def mxfp4_abs_products(codes, scales, x_bits, x_dtype: str = "bf16") -> np.ndarray:
     W = np.abs(mxfp4_dequant(codes, scales))
-    x = np.abs(bf16_bits_to_f64(x_bits))
+    x = np.abs(act_bits_to_f64(x_bits, x_dtype))
     return x @ W.T
+
+
+def mxfp8_matvec(codes, scales, x_bits, x_dtype: str = "bf16") -> np.ndarray:
+    """MXFP8 matvec y[v, n] = sum_k W[n, k] * x[v, k] in float64, W decoded per
+    mxfp8_dequant. codes [N, K] (one E4M3 byte each), scales [N, K/32],
+    x_bits [V, K] bf16 or fp16. Returns [V, N]."""
+    W = mxfp8_dequant(codes, scales)
+    x = act_bits_to_f64(x_bits, x_dtype)
+    return x @ W.T
+
+
+def mxfp8_abs_products(codes, scales, x_bits, x_dtype: str = "bf16") -> np.ndarray:
+    W = np.abs(mxfp8_dequant(codes, scales))
+    x = np.abs(act_bits_to_f64(x_bits, x_dtype))
+    return x @ W.T
+
+
+def mx_matvec(fmt: str, codes, scales, x_bits, x_dtype: str = "bf16") -> np.ndarray:
+    if fmt == "mxfp4":
+        return mxfp4_matvec(codes, scales, x_bits, x_dtype)
+    if fmt == "mxfp8":
+        return mxfp8_matvec(codes, scales, x_bits, x_dtype)
+    raise ValueError(fmt)
+
+
+def mx_abs_products(fmt: str, codes, scales, x_bits, x_dtype: str = "bf16") -> np.ndarray:
+    if fmt == "mxfp4":
+        return mxfp4_abs_products(codes, scales, x_bits, x_dtype)
+    if fmt == "mxfp8":
+        return mxfp8_abs_products(codes, scales, x_bits, x_dtype)
+    raise ValueError(fmt)
 
 
 # ---------------------------------------------------------------------------
@@ -358,10 +443,17 @@ def moe_gather(matvec, n_experts: int, ids: np.ndarray, per_slot: bool, N: int) 
     return y
 
 
-def mxfp4_moe_gather(codes, scales, x_bits, ids, per_slot: bool):
+def mxfp4_moe_gather(codes, scales, x_bits, ids, per_slot: bool, x_dtype: str = "bf16"):
     """MXFP4 expert gather. codes [E, N, K], scales [E, N, K/32], x_bits [V, K]."""
     E, N, _ = codes.shape
-    return moe_gather(lambda e, v: mxfp4_matvec(codes[e], scales[e], x_bits[v:v + 1])[0],
+    return moe_gather(lambda e, v: mxfp4_matvec(codes[e], scales[e], x_bits[v:v + 1], x_dtype)[0],
+                      E, ids, per_slot, N)
+
+
+def mx_moe_gather(fmt: str, codes, scales, x_bits, ids, per_slot: bool, x_dtype: str = "bf16"):
+    """MXFP4 or MXFP8 expert gather. codes [E, N, K], scales [E, N, K/32], x_bits [V, K]."""
+    E, N, _ = codes.shape
+    return moe_gather(lambda e, v: mx_matvec(fmt, codes[e], scales[e], x_bits[v:v + 1], x_dtype)[0],
                       E, ids, per_slot, N)
 
 

@@ -23,8 +23,11 @@ from typing import Optional
 import numpy as np
 
 # Bits per code and E8M0 group length (weights per scale along K) per format.
-FORMAT_BITS = {"mxfp4": 4, "cb2": 2, "cb3": 3, "cb4": 4}
-FORMAT_GROUP = {"mxfp4": 32, "cb2": 16, "cb3": 16, "cb4": 32}
+FORMAT_BITS = {"mxfp4": 4, "cb2": 2, "cb3": 3, "cb4": 4, "mxfp8": 8}
+FORMAT_GROUP = {"mxfp4": 32, "cb2": 16, "cb3": 16, "cb4": 32, "mxfp8": 32}
+
+# MXFP8 codes that are NaN (never drawn: every synthetic weight is finite).
+E4M3_NAN_CODES = (0x7F, 0xFF)
 
 # Codebooks of the synthetic workloads (int8 values indexed by code).
 LUT_CB2 = (-3, -1, 1, 3)
@@ -41,13 +44,31 @@ def codes(g: np.random.Generator, shape, bits: int) -> np.ndarray:
     return g.integers(0, 1 << bits, size=shape, dtype=np.uint8)
 
 
+def finite_e4m3_codes(g: np.random.Generator, shape) -> np.ndarray:
+    """Uniform over the 254 E4M3 codes that are not NaN, one per uint8."""
+    c = g.integers(0, 254, size=shape, dtype=np.int32)
+    c = c + (c >= 0x7F)          # skip 0x7F; 0xFF lies beyond the drawn range
+    return c.astype(np.uint8)
+
+
+def format_codes(g: np.random.Generator, fmt: str, shape) -> np.ndarray:
+    """Synthetic codes of a format, one per uint8: uniform over every code,
+    except MXFP8, whose NaN codes are left out."""
+    if fmt == "mxfp8":
+        return finite_e4m3_codes(g, shape)
+    return codes(g, shape, FORMAT_BITS[fmt])
+
+
 def canonical_uniform_codes(g: np.random.Generator, lead_shape, K: int, bits: int) -> np.ndarray:
     """Canonical packed code bytes of uniform codes: [..., K * bits / 8] uniform bytes.
 
     Every canonical packing used here (two nibbles per byte, four 2-bit codes
     per byte, eight 3-bit codes per three bytes) maps uniform random bytes to
     independent uniform codes, so no packing step is needed to draw them.
+    8-bit codes are MXFP8 bytes and leave out its NaN codes.
     """
+    if bits == 8:
+        return finite_e4m3_codes(g, tuple(lead_shape) + (K,))
     return g.integers(0, 256, size=tuple(lead_shape) + (K * bits // 8,), dtype=np.uint8)
 
 
@@ -58,6 +79,12 @@ def e8m0(g: np.random.Generator, shape, lo: int = 120, hi: int = 130) -> np.ndar
 
 def normal_f32(g: np.random.Generator, shape) -> np.ndarray:
     return g.standard_normal(size=shape, dtype=np.float64).astype(np.float32)
+
+
+def normal_f16_bits(g: np.random.Generator, shape) -> np.ndarray:
+    """N(0,1) samples as fp16 bit patterns (uint16): the fp32 draw converted by
+    numpy (nearest-even)."""
+    return normal_f32(g, shape).astype(np.float16).view(np.uint16)
 
 
 def normal_bf16_bits(g: np.random.Generator, shape) -> np.ndarray:

@@ -64,6 +64,51 @@ def bf_fp16(bits: int) -> Fraction:
     return -v if s else v
 
 
+def bf_e4m3(code: int):
+    """E4M3: sign bit 7, 4-bit exponent (bias 7) in bits 6..3, 3-bit mantissa;
+    exponent 0 subnormal; S.1111.111 NaN (returned as None); no infinity."""
+    s = (code >> 7) & 1
+    e = (code >> 3) & 15
+    m = code & 7
+    if e == 15 and m == 7:
+        return None
+    if e == 0:
+        v = Fraction(m, 8) * Fraction(2) ** (-6)
+    else:
+        v = (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+    return -v if s else v
+
+
+def fp16_round_bits(x) -> int:
+    """Round an exact rational to fp16 (ties to even) by its definition; the
+    bit pattern, with overflow to infinity."""
+    v = Fraction(x)
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    if a == 0:
+        return sign
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -14) - 10)
+    n, rem = divmod(a, quantum)
+    n = int(n)
+    if rem > quantum / 2 or (rem == quantum / 2 and n % 2 == 1):
+        n += 1
+    r = n * quantum
+    if r > 65504:                      # rounded past the largest finite fp16
+        return sign | 0x7C00
+    if r < Fraction(2) ** -14:
+        return sign | int(r / Fraction(2) ** -24)
+    ee = r.numerator.bit_length() - r.denominator.bit_length()
+    if Fraction(2) ** ee > r:
+        ee -= 1
+    mant = int((r / Fraction(2) ** ee - 1) * 1024)
+    return sign | ((ee + 15) << 10) | mant
+
+
 def fp32_round(x) -> float:
     """Round an exact rational to the nearest fp32 (ties to even), no double rounding."""
     v = Fraction(x)
@@ -412,10 +457,93 @@ def pin_fused_gate_up():
                 assert abs(h[t, j, n] - want) <= 1e-12 * abs(want) + 1e-300
 
 
+def pin_e4m3_table():
+    torch = pytest.importorskip("torch")
+    got = O.e4m3_decode(np.arange(256))
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        want = bf_e4m3(c)
+        if want is None:
+            assert np.isnan(got[c]) and np.isnan(lib[c]), c
+            continue
+        assert Fraction(float(got[c])) == want, c
+        assert float(lib[c]) == float(got[c]), c
+        # every finite E4M3 value is exact in fp16 (the device decodes to f16)
+        assert float(np.float16(got[c])) == float(got[c]), c
+    # OCP MX E4M3 landmarks: largest normal 448, smallest normal 2**-6,
+    # smallest subnormal 2**-9, one, NaN only at S.1111.111
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0
+    assert got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+    assert [c for c in range(256) if np.isnan(got[c])] == [0x7F, 0xFF]
+    assert got[0x80] == 0 and np.signbit(got[0x80])
+
+
+def pin_f16_rounding():
+    g = qi.rng(16)
+    vals = g.standard_normal(3000) * np.exp2(g.integers(-30, 18, 3000))
+    got = O.f64_to_f16_bits(vals)
+    for v, b in zip(vals, got):
+        assert int(b) == fp16_round_bits(Fraction(float(v))), v
+    for v, b in ((1 + 2.0 ** -11, 0x3C00), (1 + 3 * 2.0 ** -11, 0x3C02), (65504.0, 0x7BFF),
+                 (65520.0, 0x7C00), (2.0 ** -25, 0x0000), (3 * 2.0 ** -26, 0x0001), (-(2.0 ** -24), 0x8001)):
+        assert int(O.f64_to_f16_bits(np.array([v]))[0]) == b, v
+    assert O.f16_bits_to_f64(np.array([0x3C00, 0x0001, 0xFBFF], dtype=np.uint16)).tolist() == [1.0, 2.0 ** -24, -65504.0]
+
+
+def brute_mx(fmt, codes, scales, x_bits, x_dtype, K):
+    elem = bf_e2m1 if fmt == "mxfp4" else bf_e4m3
+    act = bf_bf16 if x_dtype == "bf16" else bf_fp16
+    out = []
+    for r in range(codes.shape[0]):
+        acc = Fraction(0)
+        for k in range(K):
+            acc += elem(int(codes[r, k])) * bf_e8m0(int(scales[r, k // 32])) * act(int(x_bits[k]))
+        out.append(acc)
+    return out
+
+
+def pin_brute_force_mx_variants():
+    g = qi.rng(17)
+    for fmt in ("mxfp8", "mxfp4"):
+        for x_dtype in ("bf16", "f16"):
+            for N, K in ((1, 32), (4, 64)):
+                c = qi.format_codes(g, fmt, (N, K))
+                s = qi.e8m0(g, (N, K // 32))
+                x = qi.normal_bf16_bits(g, (1, K)) if x_dtype == "bf16" else qi.normal_f16_bits(g, (1, K))
+                codes = O.unpack_codes(fmt, O.pack_codes(fmt, c))
+                y = O.mx_matvec(fmt, codes, s, x, x_dtype)[0]
+                absum = O.mx_abs_products(fmt, codes, s, x, x_dtype)[0]
+                want = brute_mx(fmt, c, s, x[0], x_dtype, K)
+                for r in range(N):
+                    assert abs(Fraction(float(y[r])) - want[r]) <= Fraction(float(absum[r])) * Fraction(1, 10 ** 13)
+
+
+def pin_mx_gather_f16():
+    """mx_moe_gather: per-slot fp16 activations, an invalid id gives zeros, each
+    valid slot equals the brute-force product of its expert and its vector."""
+    g = qi.rng(18)
+    E, N, K = 3, 2, 32
+    c = qi.format_codes(g, "mxfp8", (E, N, K))
+    s = qi.e8m0(g, (E, N, 1))
+    ids = np.array([[2, 5], [0, 2]], dtype=np.int32)
+    x = qi.normal_f16_bits(g, (4, K))
+    y = O.mx_moe_gather("mxfp8", c, s, x, ids, True, "f16")
+    assert np.all(y[0, 1] == 0)
+    for t in range(2):
+        for j in range(2):
+            e = int(ids[t, j])
+            if e >= E:
+                continue
+            want = brute_mx("mxfp8", c[e], s[e], x[t * 2 + j], "f16", K)
+            for n in range(N):
+                assert abs(Fraction(float(y[t, j, n])) - want[n]) <= abs(want[n]) * Fraction(1, 10 ** 12) + Fraction(1, 10 ** 300)
+
+
 ALL_PINS = [pin_e2m1_table, pin_e2m1_stated_values, pin_e8m0, pin_bf16_conversions,
             pin_packings, pin_decode_contract, pin_brute_force_mxfp4, pin_brute_force_cb,
             pin_block_sums_exact, pin_identity_special_case, pin_q8_quantizer, pin_gather,
-            pin_silu, pin_swiglu_tolerance, pin_fused_gate_up]
+            pin_silu, pin_swiglu_tolerance, pin_fused_gate_up, pin_e4m3_table, pin_f16_rounding,
+            pin_brute_force_mx_variants, pin_mx_gather_f16]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -583,3 +711,34 @@ def test_mutation_combine_ignores_invalid(monkeypatch):
         return real(y_slots, weights, np.clip(ids, 0, n_experts - 1), n_experts)
     monkeypatch.setattr(O, "moe_combine", bad)
     assert _fails_some_pin([pin_combine])
+
+
+def test_mutation_e4m3_bias(monkeypatch):
+    real = O.e4m3_decode
+    monkeypatch.setattr(O, "e4m3_decode", lambda c: real(c) * 2.0)     # bias 6 instead of 7
+    assert _fails_some_pin([pin_e4m3_table, pin_brute_force_mx_variants])
+
+
+def test_mutation_e4m3_subnormal_as_normal(monkeypatch):
+    def bad(codes):
+        c = np.asarray(codes).astype(np.int64)
+        ex, man = (c >> 3) & 15, c & 7
+        mag = np.ldexp(1.0 + man / 8.0, ex - 7)
+        v = np.where((c >> 7) & 1, -mag, mag)
+        return np.where((ex == 15) & (man == 7), np.nan, v)
+    monkeypatch.setattr(O, "e4m3_decode", bad)
+    assert _fails_some_pin([pin_e4m3_table])
+
+
+def test_mutation_f16_read_as_bf16(monkeypatch):
+    monkeypatch.setattr(O, "act_bits_to_f64", lambda b, d="bf16": O.bf16_bits_to_f64(b))
+    assert _fails_some_pin([pin_brute_force_mx_variants, pin_mx_gather_f16])
+
+
+def test_mutation_mxfp8_group_16(monkeypatch):
+    def bad(codes, scales):
+        K = codes.shape[-1]
+        g = np.minimum(np.arange(K) // 16, scales.shape[-1] - 1)
+        return O.e4m3_decode(codes) * O.e8m0_decode(scales)[..., g]
+    monkeypatch.setattr(O, "mxfp8_dequant", bad)
+    assert _fails_some_pin([pin_brute_force_mx_variants])
