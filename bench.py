@@ -660,6 +660,15 @@ def run_configs(args):
     t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgm, Wgm[l], ddm, Wdm[l], xm, idsm[l], 1, TOP_K, wsm,
                                                          ym[l], PF) for l in range(Lm)])
     emit(1, "qmv_moe_layer MXFP4 2880 E=32 top4 ntok=1 (2 launches)", LAYER_BYTES, t / Lm, {"calls_per_graph": Lm})
+    # fp16 activations (QMV_FLAG_X_F16): same weights, x, h and y in fp16; x is
+    # scaled by 2^-10 so that h and y stay inside fp16's range with these weights
+    x16 = (qi.normal_f32(g, (1, K)) * np.float32(2.0 ** -10)).astype(np.float16)
+    xm16 = torch.from_numpy(x16.view(np.int16)).to(dev).view(torch.float16)
+    ym16 = torch.empty(Lm, 1, TOP_K, K, dtype=torch.float16, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgm, Wgm[l], ddm, Wdm[l], xm16, idsm[l], 1, TOP_K, wsm,
+                                                         ym16[l], PF | qmv.QMV_FLAG_X_F16) for l in range(Lm)])
+    emit("f4", "qmv_moe_layer MXFP4 2880 E=32 top4 ntok=1, fp16 x/h/y (2 launches)", LAYER_BYTES, t / Lm,
+         {"calls_per_graph": Lm})
     # the same layer with the router-weighted combine of its top-k outputs
     rw = torch.from_numpy(np.stack([qi.router_weights(g, 1, TOP_K) for _ in range(Lm)])).to(dev)
     wsc = torch.zeros(qmv.qmv_moe_layer_combine_workspace_bytes(dgm, ddm, 1, TOP_K), dtype=torch.uint8, device=dev)
@@ -667,6 +676,36 @@ def run_configs(args):
     t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer_combine(dgm, Wgm[l], ddm, Wdm[l], xm, idsm[l], rw[l], 1,
                                                                  TOP_K, wsc, yc[l], PF) for l in range(Lm)])
     emit(1, "qmv_moe_layer_combine MXFP4 2880 E=32 top4 ntok=1 (3 launches)", LAYER_BYTES, t / Lm,
+         {"calls_per_graph": Lm})
+    del Wgm, Wdm
+
+    # --- MXFP8 (E4M3 + E8M0/32): dense 2880x2880 and the gpt-oss-shaped layer
+    d8 = qmv.wdesc("mxfp8", N, K, 1)
+    b8 = qmv.qmv_packed_bytes(d8)
+    alg8 = N * K + N * (K // 32)
+    n8 = -(-4 * L2_BYTES // b8)
+    c8, s8 = canon("mxfp8", pool, N, K)
+    s8 = s8 - 8                                  # E4M3 magnitudes reach 448: scales 8 binades lower
+    W8 = _replicated(qmv, torch, dev, qmv.wdesc("mxfp8", N, K, pool),
+                     lambda: qmv.qmv_pack_weights(qmv.wdesc("mxfp8", N, K, pool), c8, s8), n8, b8)
+    y8 = torch.empty(n8, K, dtype=torch.bfloat16, device=dev)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_dense_ex(d8, W8[i], xm, 1, y8[i], PF) for i in range(n8)])
+    emit("f4", "qmv_dense MXFP8 2880x2880 ntok=1", alg8, t / n8, {"calls_per_graph": n8})
+    del W8
+    dg8, dd8 = qmv.wdesc("mxfp8", N, K, E), qmv.wdesc("mxfp8", K, N, E)
+    eg8, ed8 = qmv.qmv_packed_gate_up_expert_bytes(dg8), qmv.qmv_packed_expert_bytes(dd8)
+    gc, gs = canon("mxfp8", pool, N, K)
+    uc, us_ = canon("mxfp8", pool, N, K)
+    dc, ds = canon("mxfp8", pool, K, N)
+    Wg8 = _replicated(qmv, torch, dev, qmv.wdesc("mxfp8", N, K, pool),
+                      lambda: qmv.qmv_pack_gate_up(qmv.wdesc("mxfp8", N, K, pool), gc, gs - 8, uc, us_ - 8),
+                      Lm * E, eg8).view(Lm, -1)
+    Wd8 = _replicated(qmv, torch, dev, qmv.wdesc("mxfp8", K, N, pool),
+                      lambda: qmv.qmv_pack_weights(qmv.wdesc("mxfp8", K, N, pool), dc, ds - 8),
+                      Lm * E, ed8).view(Lm, -1)
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dg8, Wg8[l], dd8, Wd8[l], xm, idsm[l], 1, TOP_K, wsm,
+                                                         ym[l], PF) for l in range(Lm)])
+    emit("f4", "qmv_moe_layer MXFP8 2880 E=32 top4 ntok=1 (2 launches)", 12 * alg8, t / Lm,
          {"calls_per_graph": Lm})
     return 0
 

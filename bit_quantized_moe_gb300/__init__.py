@@ -29,10 +29,11 @@ QMV_ESIZE = -4
 QMV_ECUDA = -5
 QMV_FLAG_PREFETCH_INPUTS = 1
 QMV_FLAG_X_F32 = 2
+QMV_FLAG_X_F16 = 4
 QMV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
-MXFP4, CB2, CB3, CB4 = 0, 1, 2, 3
-FORMATS = {"mxfp4": MXFP4, "cb2": CB2, "cb3": CB3, "cb4": CB4}
+MXFP4, CB2, CB3, CB4, MXFP8 = 0, 1, 2, 3, 4
+FORMATS = {"mxfp4": MXFP4, "cb2": CB2, "cb3": CB3, "cb4": CB4, "mxfp8": MXFP8}
 MAX_NTOK = 4
 MAX_TOPK = 8
 
@@ -43,7 +44,7 @@ EXPORTS = (
     "qmv_act_q8_vec_bytes", "qmv_act_q8_bytes", "qmv_quantize_act_q8", "qmv_act_q8_unpack",
     "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
     "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
-    "qmv_moe_layer_noalloc", "qmv_moe_combine", "qmv_moe_layer_combine_workspace_bytes", "qmv_moe_layer_combine",
+    "qmv_moe_layer_noalloc", "qmv_moe_combine", "qmv_moe_combine_ex", "qmv_moe_layer_combine_workspace_bytes", "qmv_moe_layer_combine",
     "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
@@ -100,6 +101,7 @@ def _load() -> ctypes.CDLL:
         "qmv_moe_layer": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, SZ, P, ctypes.c_uint32, P]),
         "qmv_moe_layer_noalloc": (ctypes.c_int, [D, P, D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_moe_combine": (ctypes.c_int, [D, P, P, P, I32, I32, P, P]),
+        "qmv_moe_combine_ex": (ctypes.c_int, [D, P, P, P, I32, I32, P, ctypes.c_uint32, P]),
         "qmv_moe_layer_combine_workspace_bytes": (SZ, [D, D, I32, I32]),
         "qmv_moe_layer_combine": (ctypes.c_int, [D, P, D, P, P, P, P, I32, I32, P, SZ, P, ctypes.c_uint32, P]),
         "qmv_moe_gather_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, ctypes.c_uint32, P]),
@@ -289,6 +291,12 @@ def qmv_moe_layer_noalloc(gate_up_desc: WDesc, w_gate_up, down_desc: WDesc, w_do
 def qmv_moe_combine(down_desc: WDesc, ys, weights, ids, ntok: int, top_k: int, y, stream=None) -> None:
     _check(lib.qmv_moe_combine(ctypes.byref(down_desc), _ptr(ys), _ptr(weights), _ptr(ids), ntok, top_k, _ptr(y),
                                _stream(stream)))
+
+
+def qmv_moe_combine_ex(down_desc: WDesc, ys, weights, ids, ntok: int, top_k: int, y, flags: int,
+                       stream=None) -> None:
+    _check(lib.qmv_moe_combine_ex(ctypes.byref(down_desc), _ptr(ys), _ptr(weights), _ptr(ids), ntok, top_k,
+                                  _ptr(y), int(flags), _stream(stream)))
 
 
 def qmv_moe_layer_combine_workspace_bytes(gate_up_desc: WDesc, down_desc: WDesc, ntok: int, top_k: int) -> int:

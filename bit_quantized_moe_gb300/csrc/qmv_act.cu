@@ -98,8 +98,10 @@ cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n,
 // (the same order every run), stored as T. Thread per output element.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float load_out(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float load_out(const __half* p, int64_t i) { return __half2float(p[i]); }
 __device__ __forceinline__ float load_out(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ void store_val(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store_val(__half* p, int64_t i, float v) { p[i] = __float2half_rn(v); }
 __device__ __forceinline__ void store_val(float* p, int64_t i, float v) { p[i] = v; }
 
 template <typename T>
@@ -122,7 +124,7 @@ __global__ void combine_kernel(const T* __restrict__ ys, const float* __restrict
   pdl_launch_dependents();
 }
 
-cudaError_t launch_combine(bool bf16, const void* ys, const float* w, const int32_t* ids, int ntok, int top_k,
+cudaError_t launch_combine(int dtype, const void* ys, const float* w, const int32_t* ids, int ntok, int top_k,
                            int n_experts, int N, void* y, cudaStream_t s) {
   const int threads = 256;
   const long total = (long)ntok * N;
@@ -140,9 +142,13 @@ cudaError_t launch_combine(bool bf16, const void* ys, const float* w, const int3
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (s != nullptr) ? 1 : 0;
-  if (bf16) {
+  if (dtype == kOutBF16) {
     return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(ys), w, ids,
                               ntok, top_k, n_experts, N, static_cast<__nv_bfloat16*>(y));
+  }
+  if (dtype == kOutF16) {
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__half>, static_cast<const __half*>(ys), w, ids, ntok, top_k,
+                              n_experts, N, static_cast<__half*>(y));
   }
   return cudaLaunchKernelEx(&cfg, combine_kernel<float>, static_cast<const float*>(ys), w, ids, ntok, top_k,
                             n_experts, N, static_cast<float*>(y));
@@ -168,7 +174,20 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ w, int N, int K, uint
     const int row = rt * kRows + r;
     if (row >= N) break;
     float val[32];
-    if constexpr (FMT == MXFP4) {
+    if constexpr (FMT == MXFP8) {
+      const uint4* cp = reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 32);
+      const uint4 a = cp[0], b = cp[1];
+      const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      for (int q = 0; q < 8; ++q) {
+        uint32_t h[2];
+        e4m3x4_to_f16x2(w8[q], h);
+        for (int hb = 0; hb < 2; ++hb) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[hb]));
+          val[4 * q + 2 * hb] = f.x;
+          val[4 * q + 2 * hb + 1] = f.y;
+        }
+      }
+    } else if constexpr (FMT == MXFP4) {
       const uint4 cw = *reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 16);
       const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
       for (int q = 0; q < 4; ++q) {
@@ -214,6 +233,7 @@ cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t 
     case MXFP4: dequant_kernel<MXFP4><<<grid, 32, 0, s>>>(wp, N, K, lut[0], lut[1], lut[2], lut[3], out); break;
     case CB2: dequant_kernel<CB2><<<grid, 32, 0, s>>>(wp, N, K, lut[0], lut[1], lut[2], lut[3], out); break;
     case CB3: dequant_kernel<CB3><<<grid, 32, 0, s>>>(wp, N, K, lut[0], lut[1], lut[2], lut[3], out); break;
+    case MXFP8: dequant_kernel<MXFP8><<<grid, 32, 0, s>>>(wp, N, K, lut[0], lut[1], lut[2], lut[3], out); break;
     default: dequant_kernel<CB4><<<grid, 32, 0, s>>>(wp, N, K, lut[0], lut[1], lut[2], lut[3], out); break;
   }
   return cudaGetLastError();
@@ -243,7 +263,7 @@ cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t s) {
 QMV_DEFINE_STATUS_ACCESSOR(status_act)
 
 size_t matvec_smem_bytes(const MatvecArgs& a) {
-  const LaunchPlan plan = plan_launch(a, device_sm_count(), kCtasPerSm);
+  const LaunchPlan plan = plan_launch(a, device_sm_count(), kCtasPerSm, device_smem_per_sm());
   // room for the kernel's static shared variables (128 bytes with alignment)
   return (size_t)plan.smem.total + 256;
 }

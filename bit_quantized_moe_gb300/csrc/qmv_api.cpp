@@ -50,7 +50,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_desc(const qmv_wdesc* d) {
   if (d == nullptr) return fail(QMV_EINVAL, "descriptor is NULL");
-  if (d->fmt < QMV_MXFP4 || d->fmt > QMV_CB4) return fail(QMV_EINVAL, "unknown format %d", d->fmt);
+  if (d->fmt < QMV_MXFP4 || d->fmt > QMV_MXFP8) return fail(QMV_EINVAL, "unknown format %d", d->fmt);
   if (d->N < 1 || d->N > QMV_MAX_N) return fail(QMV_ESHAPE, "N=%d outside [1, %d]", d->N, QMV_MAX_N);
   if (d->K < 32 || d->K > QMV_MAX_K || d->K % 32 != 0)
     return fail(QMV_ESHAPE, "K=%d must be a multiple of 32 in [32, %d]", d->K, QMV_MAX_K);
@@ -69,6 +69,7 @@ void lut_words(const qmv_wdesc* d, uint32_t out[4]) {
 struct DevInfo {
   int sm_count = 0;
   size_t smem_optin = 0;
+  size_t smem_per_sm = 0;
 };
 
 std::mutex g_dev_mu;
@@ -80,12 +81,15 @@ const DevInfo* dev_info() {
   std::lock_guard<std::mutex> lock(g_dev_mu);
   DevInfo& di = g_dev[dev];
   if (di.sm_count == 0) {
-    int sms = 0, smem = 0;
+    int sms = 0, smem = 0, smem_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return nullptr;
+    if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+      return nullptr;
     di.sm_count = sms;
     di.smem_optin = (size_t)smem;
+    di.smem_per_sm = (size_t)smem_sm;
   }
   return &di;
 }
@@ -95,6 +99,7 @@ cudaError_t launch_for(const MatvecArgs& a) {
     case MXFP4: return launch_matvec_mxfp4(a);
     case CB2: return launch_matvec_cb2(a);
     case CB3: return launch_matvec_cb3(a);
+    case MXFP8: return launch_matvec_mxfp8(a);
     default: return launch_matvec_cb4(a);
   }
 }
@@ -116,10 +121,12 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
     glu_desc.N = gate_up_rows(desc_in->N);
     desc = &glu_desc;
   }
-  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32))
+  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16))
     return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
-  if ((flags & QMV_FLAG_X_F32) && (desc->fmt == QMV_MXFP4 || dbg != nullptr))
+  if ((flags & QMV_FLAG_X_F32) && (fmt_is_mx(desc->fmt) || dbg != nullptr))
     return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F32 applies to the codebook formats only (not block sums)", name);
+  if ((flags & QMV_FLAG_X_F16) && !fmt_is_mx(desc->fmt))
+    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F16 applies to the MX formats only", name);
   if (w == nullptr || x == nullptr || y == nullptr)
     return fail(QMV_EINVAL, "%s: weight, activation and output pointers must be non-NULL", name);
   if (ntok < 1 || ntok > QMV_MAX_NTOK) return fail(QMV_EINVAL, "%s: ntok=%d outside [1, %d]", name, ntok, QMV_MAX_NTOK);
@@ -133,7 +140,7 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   if (!aligned16(w) || !aligned16(x) || !aligned16(y) || (gather && !aligned16(ids)))
     return fail(QMV_EALIGN, "%s: device pointers must be 16-byte aligned", name);
   if (dbg != nullptr) {
-    if (desc->fmt == QMV_MXFP4) return fail(QMV_EINVAL, "%s: block sums exist only for codebook formats", name);
+    if (fmt_is_mx(desc->fmt)) return fail(QMV_EINVAL, "%s: block sums exist only for codebook formats", name);
     if (!aligned16(dbg)) return fail(QMV_EALIGN, "%s: sums pointer must be 16-byte aligned", name);
     const int span = fmt_group(desc->fmt);
     const size_t slots = gather ? (size_t)ntok * top_k : (size_t)ntok;
@@ -159,6 +166,7 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   lut_words(desc, a.lut);
   a.prefetch = (flags & QMV_FLAG_PREFETCH_INPUTS) != 0;
   a.x_f32 = (flags & QMV_FLAG_X_F32) != 0;
+  a.x_f16 = (flags & QMV_FLAG_X_F16) != 0;
   a.glu = glu;
   a.out_n = desc_in->N;
   a.stream = stream;
@@ -210,15 +218,20 @@ size_t device_max_smem_optin() {
   return di ? di->smem_optin : 0;
 }
 
+size_t device_smem_per_sm() {
+  const DevInfo* di = dev_info();
+  return di ? di->smem_per_sm : 0;
+}
+
 }  // namespace qmv
 
 using namespace qmv;
 
 extern "C" {
 
-int32_t qmv_scale_group(int32_t fmt) { return (fmt >= 0 && fmt <= 3) ? fmt_group(fmt) : 0; }
+int32_t qmv_scale_group(int32_t fmt) { return (fmt >= 0 && fmt < kNumFmts) ? fmt_group(fmt) : 0; }
 
-int32_t qmv_code_bits(int32_t fmt) { return (fmt >= 0 && fmt <= 3) ? fmt_bits(fmt) : 0; }
+int32_t qmv_code_bits(int32_t fmt) { return (fmt >= 0 && fmt < kNumFmts) ? fmt_bits(fmt) : 0; }
 
 size_t qmv_canonical_code_bytes(const qmv_wdesc* d) {
   if (check_desc(d)) return 0;
@@ -370,7 +383,7 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, 
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gu, int32_t ntok, int32_t top_k) {
   if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK) return 0;
   const size_t slots = (size_t)ntok * top_k;
-  if (gu->fmt == QMV_MXFP4) return (slots * gu->N * 2 + 255) / 256 * 256;
+  if (fmt_is_mx(gu->fmt)) return (slots * gu->N * 2 + 255) / 256 * 256;
   if (gu->N % 32) return 0;
   return (slots * gu->N * 4 + 255) / 256 * 256;
 }
@@ -384,8 +397,8 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   rc = check_desc(down);
   if (rc) return rc;
   if (!ids || !ws) return fail(QMV_EINVAL, "%s: ids and workspace must be non-NULL", name);
-  if ((gu->fmt == QMV_MXFP4) != (down->fmt == QMV_MXFP4))
-    return fail(QMV_EINVAL, "%s: gate/up and down must both be MXFP4 or both codebook formats", name);
+  if (fmt_is_mx(gu->fmt) != fmt_is_mx(down->fmt))
+    return fail(QMV_EINVAL, "%s: gate/up and down must both be MX formats or both codebook formats", name);
   if (down->K != gu->N) return fail(QMV_ESHAPE, "%s: down K=%d must equal gate/up N=%d", name, down->K, gu->N);
   if (down->n_experts != gu->n_experts)
     return fail(QMV_EINVAL, "%s: gate/up and down expert counts differ (%d, %d)", name, gu->n_experts, down->n_experts);
@@ -401,30 +414,40 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   // it stages it.
   rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, ws, nullptr, 0, s, name, flags, true);
   if (rc) return rc;
-  const uint32_t down_flags = QMV_FLAG_PREFETCH_INPUTS | (gu->fmt == QMV_MXFP4 ? 0u : (uint32_t)QMV_FLAG_X_F32);
+  const uint32_t down_flags = QMV_FLAG_PREFETCH_INPUTS | (flags & QMV_FLAG_X_F16) |
+                              (fmt_is_mx(gu->fmt) ? 0u : (uint32_t)QMV_FLAG_X_F32);
   return run_matvec(down, w_down, ws, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
 }
 
-int qmv_moe_combine(const qmv_wdesc* down, const void* ys, const float* weights, const int32_t* ids, int32_t ntok,
-                    int32_t top_k, void* y, void* stream) {
+int qmv_moe_combine_ex(const qmv_wdesc* down, const void* ys, const float* weights, const int32_t* ids,
+                       int32_t ntok, int32_t top_k, void* y, uint32_t flags, void* stream) {
   const char* name = "qmv_moe_combine";
   int rc = check_desc(down);
   if (rc) return rc;
+  if (flags & ~(uint32_t)QMV_FLAG_X_F16) return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  if ((flags & QMV_FLAG_X_F16) && !fmt_is_mx(down->fmt))
+    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F16 applies to the MX formats only", name);
   if (!ys || !weights || !ids || !y) return fail(QMV_EINVAL, "%s: NULL pointer", name);
   if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK)
     return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
   if (!aligned16(ys) || !aligned16(weights) || !aligned16(ids) || !aligned16(y))
     return fail(QMV_EALIGN, "%s: pointers must be 16-byte aligned", name);
-  cudaError_t e = launch_combine(down->fmt == QMV_MXFP4, ys, weights, ids, ntok, top_k, down->n_experts, down->N, y,
+  const int dtype = !fmt_is_mx(down->fmt) ? kOutF32 : ((flags & QMV_FLAG_X_F16) ? kOutF16 : kOutBF16);
+  cudaError_t e = launch_combine(dtype, ys, weights, ids, ntok, top_k, down->n_experts, down->N, y,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, name);
   return ok();
 }
 
+int qmv_moe_combine(const qmv_wdesc* down, const void* ys, const float* weights, const int32_t* ids, int32_t ntok,
+                    int32_t top_k, void* y, void* stream) {
+  return qmv_moe_combine_ex(down, ys, weights, ids, ntok, top_k, y, 0u, stream);
+}
+
 size_t qmv_moe_layer_combine_workspace_bytes(const qmv_wdesc* gu, const qmv_wdesc* down, int32_t ntok, int32_t top_k) {
   const size_t layer = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
   if (layer == 0 || check_desc(down)) return 0;
-  const size_t elem = (down->fmt == QMV_MXFP4) ? 2 : 4;
+  const size_t elem = fmt_is_mx(down->fmt) ? 2 : 4;
   return layer + ((size_t)ntok * top_k * down->N * elem + 255) / 256 * 256;
 }
 
@@ -440,7 +463,7 @@ int qmv_moe_layer_combine(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc
   void* ys = static_cast<uint8_t*>(ws) + layer;
   int rc = qmv_moe_layer(gu, w_gu, down, w_down, x, ids, ntok, top_k, ws, layer, ys, flags, stream);
   if (rc) return rc;
-  return qmv_moe_combine(down, ys, weights, ids, ntok, top_k, y, stream);
+  return qmv_moe_combine_ex(down, ys, weights, ids, ntok, top_k, y, flags & QMV_FLAG_X_F16, stream);
 }
 
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
@@ -483,8 +506,8 @@ int qmv_debug_dequant(const qmv_wdesc* desc, const void* w, int32_t expert, floa
 int qmv_device_status(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(QMV_EINVAL, "qmv_device_status: NULL pointer");
   uint32_t v = 0;
-  const uint32_t parts[5] = {status_mxfp4(clear), status_cb2(clear), status_cb3(clear), status_cb4(clear),
-                             status_act(clear)};
+  const uint32_t parts[6] = {status_mxfp4(clear), status_cb2(clear), status_cb3(clear),
+                             status_cb4(clear),   status_mxfp8(clear), status_act(clear)};
   for (uint32_t p : parts) {
     if (p == 0xffffffffu) return cuda_fail(cudaGetLastError(), "qmv_device_status");
     v |= p;

@@ -18,6 +18,7 @@ enum : uint32_t {
   kStatusWaitTile = 2u,   // weight tile copy did not complete
   kStatusDrain = 4u,      // a copy was still in flight when giving up
   kStatusWaitProbe = 8u,  // the wait probe's barrier (which nothing completes) timed out
+  kStatusPlan = 16u,      // a CTA needed more staged activation vectors than planned
 };
 
 // One status word per translation unit; read back by that unit's accessor.
@@ -147,6 +148,16 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
       " cvt.rn.f16x2.e2m1x2 %0, a;\n cvt.rn.f16x2.e2m1x2 %1, b;\n"
       " cvt.rn.f16x2.e2m1x2 %2, c;\n cvt.rn.f16x2.e2m1x2 %3, d;\n}"
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Four E4M3 codes (one 32-bit word, byte i = code i) -> two f16x2: h[0]
+// holds codes 0 (low half) and 1, h[1] codes 2 and 3. Every E4M3 value,
+// subnormals included, is exact in f16; the NaN codes give f16 NaN.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t (&h)[2]) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+      : "=r"(h[0]), "=r"(h[1])
       : "r"(w));
 }
 

@@ -24,6 +24,7 @@ struct MatvecArgs {
   uint32_t lut[4] = {0, 0, 0, 0}; // 16 int8 codebook bytes
   bool prefetch = false;          // QMV_FLAG_PREFETCH_INPUTS
   bool x_f32 = false;             // QMV_FLAG_X_F32: fp32 x, quantized to q8_1 in the kernel
+  bool x_f16 = false;             // QMV_FLAG_X_F16: MX formats, fp16 x and y
   bool glu = false;               // gate/up-interleaved matrix, store silu(gate) * up
   int out_n = 0;                  // output rows per slot (0: N)
   cudaStream_t stream = nullptr;
@@ -39,10 +40,13 @@ cudaError_t launch_matvec_mxfp4(const MatvecArgs& a);
 cudaError_t launch_matvec_cb2(const MatvecArgs& a);
 cudaError_t launch_matvec_cb3(const MatvecArgs& a);
 cudaError_t launch_matvec_cb4(const MatvecArgs& a);
+cudaError_t launch_matvec_mxfp8(const MatvecArgs& a);
 
 cudaError_t launch_quantize_q8(const float* x, int nvec, int K, void* xq, cudaStream_t s);
 cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n, cudaStream_t s);
-cudaError_t launch_combine(bool bf16, const void* ys, const float* w, const int32_t* ids, int ntok, int top_k,
+// Output types of the combine.
+enum : int { kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2 };
+cudaError_t launch_combine(int dtype, const void* ys, const float* w, const int32_t* ids, int ntok, int top_k,
                            int n_experts, int N, void* y, cudaStream_t s);
 cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t lut[4], float* out,
                            cudaStream_t s);
@@ -54,6 +58,7 @@ uint32_t status_mxfp4(int clear);
 uint32_t status_cb2(int clear);
 uint32_t status_cb3(int clear);
 uint32_t status_cb4(int clear);
+uint32_t status_mxfp8(int clear);
 
 // Sets the calling thread's qmv_last_error() message and returns `code`.
 int record_error(int code, const char* fmt, ...);
@@ -61,5 +66,6 @@ int record_error(int code, const char* fmt, ...);
 // Per-device cached properties.
 int device_sm_count();
 size_t device_max_smem_optin();
+size_t device_smem_per_sm();
 
 }  // namespace qmv

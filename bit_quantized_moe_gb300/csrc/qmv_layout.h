@@ -4,8 +4,8 @@
 // chunks of kChunkK columns. One (row tile, chunk) pair is a "tile": a
 // contiguous, 16-byte aligned block that one bulk copy moves into shared
 // memory. Inside a chunk, lane l of the consuming warp owns the 32 columns
-// [32 l, 32 l + 32) -- exactly one E8M0 group for MXFP4/CB4 and one q8_1
-// block of activations -- for all kRows rows of the tile.
+// [32 l, 32 l + 32) -- exactly one E8M0 group for MXFP4/MXFP8/CB4 and one
+// q8_1 block of activations -- for all kRows rows of the tile.
 //
 // Tile of a chunk with L active lanes (L = 32 except for a ragged last chunk):
 //   codes  : kRows x L lane blocks, row-major ([row][lane][lane block]);
@@ -31,7 +31,8 @@ constexpr int kLaneK = 32;         // columns per lane per chunk
 constexpr int kChunkK = 32 * kLaneK;  // columns per chunk (one warp)
 constexpr int kExpertAlign = 256;
 
-enum Fmt : int { MXFP4 = 0, CB2 = 1, CB3 = 2, CB4 = 3 };
+enum Fmt : int { MXFP4 = 0, CB2 = 1, CB3 = 2, CB4 = 3, MXFP8 = 4 };
+constexpr int kNumFmts = 5;
 
 #if defined(__CUDACC__)
 #define QMV_HD __host__ __device__
@@ -39,7 +40,9 @@ enum Fmt : int { MXFP4 = 0, CB2 = 1, CB3 = 2, CB4 = 3 };
 #define QMV_HD
 #endif
 
-QMV_HD constexpr int fmt_bits(int f) { return f == CB2 ? 2 : (f == CB3 ? 3 : 4); }
+QMV_HD constexpr int fmt_bits(int f) { return f == CB2 ? 2 : (f == CB3 ? 3 : (f == MXFP8 ? 8 : 4)); }
+// MX formats: floating-point elements times bf16 / fp16 activations
+QMV_HD constexpr bool fmt_is_mx(int f) { return f == MXFP4 || f == MXFP8; }
 QMV_HD constexpr int fmt_group(int f) { return (f == CB2 || f == CB3) ? 16 : 32; }
 // bytes of codes per lane per row (32 codes)
 QMV_HD constexpr int lane_code_bytes(int f) { return 32 * fmt_bits(f) / 8; }
@@ -96,6 +99,7 @@ QMV_HD inline uint64_t tile_offset(const Geometry& g, int rt, int c) {
 //
 // MXFP4 / CB4 (16 bytes): byte b = c[2b] | c[2b+1] << 4; word w holds c[8w..8w+7]
 //   in nibbles 0..7.
+// MXFP8 (32 bytes): byte i = c[i].
 // CB2 (8 bytes, words W0, W1): nibble n of W0 holds c[n] in bits 0-1 and
 //   c[n+8] in bits 2-3 (n = 0..7); W1 the same for c[16+n], c[24+n]. So
 //   (W >> 2s) & 0x33333333 has one code per nibble.
@@ -105,6 +109,10 @@ QMV_HD inline uint64_t tile_offset(const Geometry& g, int rt, int c) {
 // ---------------------------------------------------------------------------
 
 inline void encode_lane(int f, const uint8_t* c, uint8_t* out /* lane_code_bytes */) {
+  if (f == MXFP8) {
+    for (int i = 0; i < 32; ++i) out[i] = c[i];
+    return;
+  }
   if (f == MXFP4 || f == CB4) {
     for (int b = 0; b < 16; ++b) out[b] = (uint8_t)((c[2 * b] & 15) | ((c[2 * b + 1] & 15) << 4));
     return;
@@ -124,6 +132,10 @@ inline void encode_lane(int f, const uint8_t* c, uint8_t* out /* lane_code_bytes
 }
 
 inline void decode_lane(int f, const uint8_t* in, uint8_t* c /* 32 codes */) {
+  if (f == MXFP8) {
+    for (int i = 0; i < 32; ++i) c[i] = in[i];
+    return;
+  }
   if (f == MXFP4 || f == CB4) {
     for (int b = 0; b < 16; ++b) {
       c[2 * b] = in[b] & 15;

@@ -22,6 +22,16 @@
 //          staged as group-scaled f16, fp32 group sum times 2^(e-127) per 32
 //          weights ("perf(rocm): add an mxfp4 arm to the warp-shared
 //          gather_qmv kernel ...", "Proposed Solution" item 1).
+//   MXFP8: E4M3 bytes -> f16x2 with cvt.rn.f16x2.e4m3x2, then as MXFP4
+//          (the f16 MXFP4 and MXFP8 gathers the same page names as the next
+//          scope, "Scope"). The kernels' ALT variant of an MX format takes
+//          fp16 activations, staged as they are (unscaled), and stores fp16.
+//
+// Kernel variants: matvec_kernel<FMT, NV, ALT>. ALT is the integer block-sum
+// export (DBG) for the codebook formats and fp16 activations/outputs (XH)
+// for the MX formats: a compile-time choice, so the common kernels carry no
+// code for either (each launch runs its prologue from a cold instruction
+// cache).
 //   CB2/CB3/CB4: codes -> int8 through byte permutes (prmt) over the codebook
 //          held in registers, dp4a against q8_1 activations, integer sums per
 //          16-weight half-block (CB2, CB3) or 32-weight block (CB4), then
@@ -63,7 +73,7 @@ constexpr int kCtasPerSm = 2;
 // heavier arithmetic hide the activation latency).
 template <int FMT, int NV>
 struct EarlyTiles {
-  static constexpr int value = (NV >= 3) ? Shape<NV>::stages : (FMT == MXFP4 ? 0 : 1);
+  static constexpr int value = (NV >= 3) ? Shape<NV>::stages : (fmt_is_mx(FMT) ? 0 : 1);
 };
 
 inline void launch_shape(int nv, int& warps, int& stages) {
@@ -99,6 +109,7 @@ struct KParams {
   const uint8_t* x;
   uint32_t x_vec_bytes;   // bytes per activation vector (global and shared)
   int nvec;
+  int x_slots;            // vectors the shared activation region holds (<= nvec)
   const int32_t* ids;
   int ntok, top_k, per_slot, n_experts;
   int N, K, row_tiles, chunks, last_lanes;
@@ -138,15 +149,17 @@ struct SmemLayout {
 constexpr uint32_t kPartFloats = 32;
 constexpr int kMaxSplits = 8;
 
-// x region: the activation vectors as copied; for MXFP4 they are rewritten in
-// place as f16 (see stage_x_mxfp4) and xinv holds one float per 32-group.
+// x region: the staged activation vectors, x_slots of them (per-slot gathers
+// stage only the vectors of the CTA's items, at consecutive positions); for
+// the MX formats they are f16 (see stage_x_mxfp4) and xinv holds one float
+// per 32-group.
 __host__ __device__ inline SmemLayout smem_layout(int fmt, uint32_t nvec, uint32_t x_vec_bytes,
                                                   uint32_t full_tile, int K, int warps, int stages,
                                                   int splits, int items_per_cta) {
   SmemLayout L;
   L.x_off = 0;
   L.xinv_off = round_up_u32(nvec * x_vec_bytes, 16);
-  const uint32_t xinv_bytes = (fmt == MXFP4) ? nvec * (uint32_t)(K / 32) * 4u : 0u;
+  const uint32_t xinv_bytes = fmt_is_mx(fmt) ? nvec * (uint32_t)(K / 32) * 4u : 0u;
   L.ring_off = round_up_u32(L.xinv_off + xinv_bytes, 128);
   L.bar_off = L.ring_off + (uint32_t)(warps * stages) * full_tile;
   L.ent_off = round_up_u32(L.bar_off + (uint32_t)(warps * stages) * 8, 16);
@@ -418,7 +431,8 @@ __device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* 
 // then converts and stores: loads issued before the caller's tile copies sit
 // ahead of them in the memory queue.
 // Units are numbered over the CTA's list of vectors: unit u is group (or
-// block, or piece) u % per_vec of vector vlist[u / per_vec].
+// block, or piece) u % per_vec of vector vlist[u / per_vec], staged at that
+// vector's index, or at list position u / per_vec in a compact region.
 __device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, const int* vlist, int g0, int n, int groups,
                                                   uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
 #pragma unroll
@@ -436,31 +450,32 @@ __device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, const int* v
   }
 }
 
-__device__ __forceinline__ void store_groups_mxfp4(uint8_t* xs, float* xinv, const int* vlist, int g0, int n,
-                                                   int groups, uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
+__device__ __forceinline__ void store_groups_mxfp4(uint8_t* xs, float* xinv, const int* vlist, bool compact,
+                                                   int g0, int n, int groups, uint32_t vec_bytes,
+                                                   uint32_t (&w)[kStageU][16]) {
 #pragma unroll
   for (int u = 0; u < kStageU; ++u) {
     const int gi = g0 + u * blockDim.x;
     if (gi < n) {
-      const int v = vlist ? vlist[gi / groups] : gi / groups, g = gi % groups;
+      const int v = compact ? gi / groups : (vlist ? vlist[gi / groups] : gi / groups), g = gi % groups;
       convert_group_mxfp4(w[u], xs + (size_t)v * vec_bytes + (size_t)g * 64, xinv + v * groups + g);
     }
   }
 }
 
 template <class Mid>
-__device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, const int* vlist, int nvl,
-                                              int K, uint32_t vec_bytes, Mid&& mid) {
+__device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, const int* vlist,
+                                              bool compact, int nvl, int K, uint32_t vec_bytes, Mid&& mid) {
   const int groups = K / 32;
   const int n = nvl * groups;
   const int step = kStageU * blockDim.x;
   uint32_t w[kStageU][16];
   load_groups_mxfp4(x, vlist, threadIdx.x, n, groups, vec_bytes, w);
   mid();
-  store_groups_mxfp4(xs, xinv, vlist, threadIdx.x, n, groups, vec_bytes, w);
+  store_groups_mxfp4(xs, xinv, vlist, compact, threadIdx.x, n, groups, vec_bytes, w);
   for (int g0 = threadIdx.x + step; g0 < n; g0 += step) {
     load_groups_mxfp4(x, vlist, g0, n, groups, vec_bytes, w);
-    store_groups_mxfp4(xs, xinv, vlist, g0, n, groups, vec_bytes, w);
+    store_groups_mxfp4(xs, xinv, vlist, compact, g0, n, groups, vec_bytes, w);
   }
 }
 
@@ -508,8 +523,8 @@ __device__ __forceinline__ void load_block_f32(const float* x, const int* vlist,
 }
 
 template <class Mid>
-__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, const int* vlist, int nvl, int K,
-                                                  uint32_t vec_bytes, Mid&& mid) {
+__device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, const int* vlist, bool compact,
+                                                  int nvl, int K, uint32_t vec_bytes, Mid&& mid) {
   const int blocks = K / 32;
   const int n = nvl * blocks;
   float f[32];
@@ -517,18 +532,22 @@ __device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, c
   load_block_f32(x, vlist, bi, n, blocks, K, f);
   mid();
   for (;;) {
-    if (bi < n) quantize_block_q8(f, xs + (size_t)(vlist ? vlist[bi / blocks] : bi / blocks) * vec_bytes, K, bi % blocks);
+    if (bi < n) {
+      const int v = compact ? bi / blocks : (vlist ? vlist[bi / blocks] : bi / blocks);
+      quantize_block_q8(f, xs + (size_t)v * vec_bytes, K, bi % blocks);
+    }
     bi += blockDim.x;
     if (bi >= n) break;
     load_block_f32(x, vlist, bi, n, blocks, K, f);
   }
 }
 
-// Codebook activations (q8_1 vectors) are copied to shared memory as they are,
-// four 16-byte loads per thread in flight.
+// Codebook activations (q8_1 vectors), and fp16 activations of the MX
+// formats, are copied to shared memory as they are, four 16-byte loads per
+// thread in flight.
 template <class Mid>
-__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, const int* vlist, int nvl,
-                                             uint32_t vec_bytes, Mid&& mid) {
+__device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, const int* vlist, bool compact,
+                                             int nvl, uint32_t vec_bytes, Mid&& mid) {
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(xs);
   const int per = (int)(vec_bytes / 16);
@@ -554,7 +573,7 @@ __device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, cons
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * blockDim.x;
-      if (i < n) dst[at[u]] = v[u];
+      if (i < n) dst[compact ? (size_t)i : at[u]] = v[u];
     }
     if (i0 + step >= n) break;
   }
@@ -604,6 +623,63 @@ __device__ __forceinline__ void chunk_mxfp4(const KParams& p, const Entry& e, in
       for (int b = 0; b < 4; ++b) {
         const int k = 8 * q + 2 * b;
         const uint16_t wl = (uint16_t)(h[b] & 0xffffu), wh = (uint16_t)(h[b] >> 16);
+#pragma unroll
+        for (int v = 0; v < NVV; ++v) {
+          d0[v] = fma_f16_f32(wl, xv16[v][k], d0[v]);
+          d1[v] = fma_f16_f32(wh, xv16[v][k + 1], d1[v]);
+        }
+      }
+    }
+    const float s = e8m0_to_f32((scw[r >> 2] >> (8 * (r & 3))) & 0xffu);
+#pragma unroll
+    for (int v = 0; v < NVV; ++v) acc[r * NVP + v] = fmaf(s, (d0[v] + d1[v]) * inv[v], acc[r * NVP + v]);
+  }
+}
+
+// MXFP8: the lane's 32 E4M3 codes of a row are 32 bytes; each byte pair
+// becomes an f16x2 (exact), then the same mixed-precision FMA chains and
+// group scale as MXFP4.
+template <int NVV, int NVP>
+__device__ __forceinline__ void chunk_mxfp8(const KParams& p, const Entry& e, int c, int L,
+                                            const uint8_t* st, const uint8_t* xs, const float* xinv,
+                                            float* acc) {
+  const int lane = threadIdx.x & 31;
+  uint16_t xv16[NVV][32];
+  float inv[NVV];
+#pragma unroll
+  for (int v = 0; v < NVV; ++v) {
+    const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)e.vec[v] * p.x_vec_bytes +
+                                                     (size_t)(c * kChunkK + lane * kLaneK) * 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = xp[q];
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv16[v][8 * q + 2 * i] = (uint16_t)(w4[i] & 0xffffu);
+        xv16[v][8 * q + 2 * i + 1] = (uint16_t)(w4[i] >> 16);
+      }
+    }
+    inv[v] = xinv[e.vec[v] * (p.K / 32) + c * 32 + lane];
+  }
+  const uint2 sc = *reinterpret_cast<const uint2*>(st + tile_code_bytes(MXFP8, L) + lane * kRows);
+  const uint32_t scw[2] = {sc.x, sc.y};
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const uint4* cp = reinterpret_cast<const uint4*>(st + (size_t)(r * L + lane) * 32);
+    const uint4 a = cp[0], b = cp[1];
+    const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float d0[NVV], d1[NVV];
+#pragma unroll
+    for (int v = 0; v < NVV; ++v) d0[v] = d1[v] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t h[2];
+      e4m3x4_to_f16x2(w8[q], h);
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int k = 4 * q + 2 * hb;
+        const uint16_t wl = (uint16_t)(h[hb] & 0xffffu), wh = (uint16_t)(h[hb] >> 16);
 #pragma unroll
         for (int v = 0; v < NVV; ++v) {
           d0[v] = fma_f16_f32(wl, xv16[v][k], d0[v]);
@@ -728,9 +804,11 @@ __device__ __forceinline__ void rs_step(float* v, int lane) {
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
-template <int FMT>
+template <int FMT, bool XH>
 __device__ __forceinline__ void store_out(const KParams& p, size_t o, float val) {
-  if constexpr (FMT == MXFP4) {
+  if constexpr (fmt_is_mx(FMT) && XH) {
+    reinterpret_cast<__half*>(p.y)[o] = __float2half_rn(val);
+  } else if constexpr (fmt_is_mx(FMT)) {
     reinterpret_cast<__nv_bfloat16*>(p.y)[o] = __float2bfloat16_rn(val);
   } else {
     reinterpret_cast<float*>(p.y)[o] = val;
@@ -753,7 +831,7 @@ __device__ __forceinline__ float reduce_lanes(float* acc) {
 // takes up row r from lane l + 16 and stores silu(g) * u at h[slot][4 rt + r]
 // (mlxcel-2178, "Problem / Background": gate, up and down per layer, SwiGLU
 // between them). All lanes of the warp call it.
-template <int FMT, int NVV, int NVP>
+template <int FMT, int NVV, int NVP, bool XH>
 __device__ __forceinline__ void store_lanes(const KParams& p, const Entry& e, int rt, float val) {
   const int lane = threadIdx.x & 31;
   constexpr int M = kRows * NVP;
@@ -764,11 +842,11 @@ __device__ __forceinline__ void store_lanes(const KParams& p, const Entry& e, in
     const float up = __shfl_xor_sync(0xffffffffu, val, 16);   // row r + 4 (same vector) lives 16 lanes up
     const int row = rt * (kRows / 2) + r;
     if (lane % S == 0 && r < kRows / 2 && v < NVV && row < p.out_n) {
-      store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, silu_f32(val) * up);
+      store_out<FMT, XH>(p, (size_t)e.slot[v] * p.out_n + row, silu_f32(val) * up);
     }
   } else {
     const int row = rt * kRows + r;
-    if (lane % S == 0 && v < NVV && row < p.out_n) store_out<FMT>(p, (size_t)e.slot[v] * p.out_n + row, val);
+    if (lane % S == 0 && v < NVV && row < p.out_n) store_out<FMT, XH>(p, (size_t)e.slot[v] * p.out_n + row, val);
   }
 }
 
@@ -780,11 +858,13 @@ __device__ __forceinline__ void store_lanes(const KParams& p, const Entry& e, in
 // same order every run) and stores.
 // ---------------------------------------------------------------------------
 
-template <int FMT, int NVV, bool DBG, int ST>
+template <int FMT, int NVV, bool ALT, int ST>
 __device__ __forceinline__ bool run_task(const KParams& p, const Entry& e, int rt, int k, int range, int c0,
                                          int c1, int& q, WarpPipe& wp, const uint8_t* xs, const float* xinv,
                                          float* part, int* cnt) {
   constexpr int NVP = (NVV == 3) ? 4 : NVV;
+  constexpr bool DBG = ALT && !fmt_is_mx(FMT);
+  constexpr bool XH = ALT && fmt_is_mx(FMT);
   const int lane = threadIdx.x & 31;
   float acc[kRows * NVP];
 #pragma unroll
@@ -799,6 +879,8 @@ __device__ __forceinline__ bool run_task(const KParams& p, const Entry& e, int r
     if (lane < L) {
       if constexpr (FMT == MXFP4) {
         chunk_mxfp4<NVV, NVP>(p, e, c, L, st, xs, xinv, acc);
+      } else if constexpr (FMT == MXFP8) {
+        chunk_mxfp8<NVV, NVP>(p, e, c, L, st, xs, xinv, acc);
       } else {
         chunk_cb<FMT, NVV, NVP, DBG>(p, e, rt, c, L, st, xs, acc);
       }
@@ -824,12 +906,12 @@ __device__ __forceinline__ bool run_task(const KParams& p, const Entry& e, int r
     val = 0.f;
     for (int r = 0; r < p.splits; ++r) val += slot[r * kPartFloats + lane / S];
   }
-  store_lanes<FMT, NVV, NVP>(p, e, rt, val);
+  store_lanes<FMT, NVV, NVP, XH>(p, e, rt, val);
   return true;
 }
 
 // All tasks of this warp. False if a tile wait gave up.
-template <int FMT, int NV, bool DBG, int ST>
+template <int FMT, int NV, bool ALT, int ST>
 __device__ __forceinline__ bool run_tasks(const KParams& p, int& q, WarpPipe& wp, const uint8_t* xs,
                                           const float* xinv, float* part, int* cnt) {
   const int warp = threadIdx.x >> 5;
@@ -842,15 +924,15 @@ __device__ __forceinline__ bool run_tasks(const KParams& p, int& q, WarpPipe& wp
     task_chunks(p, lt, c0, c1);
     bool ok = true;
     switch (e.nv) {
-      case 1: ok = run_task<FMT, 1, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt); break;
+      case 1: ok = run_task<FMT, 1, ALT, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt); break;
       case 2:
-        if constexpr (NV >= 2) ok = run_task<FMT, 2, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
+        if constexpr (NV >= 2) ok = run_task<FMT, 2, ALT, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
         break;
       case 3:
-        if constexpr (NV >= 3) ok = run_task<FMT, 3, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
+        if constexpr (NV >= 3) ok = run_task<FMT, 3, ALT, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
         break;
       case 4:
-        if constexpr (NV >= 4) ok = run_task<FMT, 4, DBG, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
+        if constexpr (NV >= 4) ok = run_task<FMT, 4, ALT, ST>(p, e, rt, k, range, c0, c1, q, wp, xs, xinv, part, cnt);
         break;
       default: break;
     }
@@ -874,7 +956,7 @@ __device__ __forceinline__ void drain_ring(const WarpPipe& wp, int q) {
   }
 }
 
-template <int FMT, int NV, bool DBG>
+template <int FMT, int NV, bool ALT>
 __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     matvec_kernel(const __grid_constant__ KParams p) {
   constexpr int W = Shape<NV>::warps;
@@ -882,7 +964,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.nvec, p.x_vec_bytes, p.full_tile, p.K, W, ST, p.splits,
+  const SmemLayout sl = smem_layout(FMT, (uint32_t)p.x_slots, p.x_vec_bytes, p.full_tile, p.K, W, ST, p.splits,
                                     p.items_per_cta);
   uint8_t* xs = smem + sl.x_off;
   float* xinv = reinterpret_cast<float*>(smem + sl.xinv_off);
@@ -943,7 +1025,12 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   }
   // Per-slot gathers stage only the vectors of the entries the CTA's
   // contiguous item range touches (listed here, after the first tile copies
-  // are out); other calls stage all vectors.
+  // are out); other calls stage all vectors. A vector is staged at its own
+  // index, unless the host planned a compact region (x_slots < nvec: all
+  // vectors would not fit beside the tile ring); then the listed vectors sit
+  // at consecutive positions and the CTA's entries are pointed at them. The
+  // compact region holds the most vectors a CTA's range can touch; a longer
+  // list is recorded in the status word and cut (a planning error).
   if (p.per_slot) {
     if (warp == 0) {
       uint32_t used = 0;
@@ -954,13 +1041,30 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
         }
       }
       used = __reduce_or_sync(0xffffffffu, used);
-      if (used & (1u << lane)) s_vlist[__popc(used & ((1u << lane) - 1u))] = lane;
-      if (lane == 0) s_nvl = __popc(used);
+      int n_used = __popc(used);
+      if (n_used > p.x_slots) {
+        if (lane == 0) set_status(kStatusPlan);
+        n_used = p.x_slots;
+      }
+      const int pos = __popc(used & ((1u << lane) - 1u));
+      if ((used & (1u << lane)) && pos < n_used) s_vlist[pos] = lane;
+      if (lane == 0) s_nvl = n_used;
+      if (p.x_slots < p.nvec && items_here > 0) {
+        __syncwarp();
+        const int e0 = wp.first / p.row_tiles, e1 = (wp.first + items_here - 1) / p.row_tiles;
+        for (int e = e0 + lane; e <= e1; e += 32) {
+          for (int m = 0; m < 4; ++m) {
+            const int at = __popc(used & ((1u << ent[e].vec[m]) - 1u));
+            ent[e].vec[m] = at < n_used ? at : 0;
+          }
+        }
+      }
     }
     __syncthreads();
   }
   const int* vlist = p.per_slot ? s_vlist : nullptr;
   const int nvl = p.per_slot ? s_nvl : p.nvec;
+  const bool compact = p.x_slots < p.nvec;
   if (early) pdl_wait();
   // Dependents are released only after this kernel's own wait, so when one
   // starts, every kernel before this one is complete (what
@@ -974,7 +1078,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
       const int ex = s_ids[s];
       if (ex >= 0 && ex < p.n_experts) continue;
       for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < p.out_n; row += gridDim.x * blockDim.x) {
-        store_out<FMT>(p, (size_t)s * p.out_n + row, 0.f);
+        store_out<FMT, ALT>(p, (size_t)s * p.out_n + row, 0.f);
       }
     }
   }
@@ -987,17 +1091,20 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
       __syncthreads();
     }
   };
-  if constexpr (FMT == MXFP4) {
-    stage_x_mxfp4(p.x, xs, xinv, vlist, nvl, p.K, p.x_vec_bytes, issue_rest);
+  if constexpr (fmt_is_mx(FMT) && ALT) {
+    stage_x_copy(p.x, xs, vlist, compact, nvl, p.x_vec_bytes, issue_rest);
+    for (int i = threadIdx.x; i < p.x_slots * (p.K / 32); i += blockDim.x) xinv[i] = 1.0f;
+  } else if constexpr (fmt_is_mx(FMT)) {
+    stage_x_mxfp4(p.x, xs, xinv, vlist, compact, nvl, p.K, p.x_vec_bytes, issue_rest);
   } else if (p.flags & kFlagXF32) {
-    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, vlist, nvl, p.K, p.x_vec_bytes, issue_rest);
+    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, vlist, compact, nvl, p.K, p.x_vec_bytes, issue_rest);
   } else {
-    stage_x_copy(p.x, xs, vlist, nvl, p.x_vec_bytes, issue_rest);
+    stage_x_copy(p.x, xs, vlist, compact, nvl, p.x_vec_bytes, issue_rest);
   }
   __syncthreads();
 
   int q = 0;
-  if (!run_tasks<FMT, NV, DBG, ST>(p, q, wp, xs, xinv, part, cnt)) {
+  if (!run_tasks<FMT, NV, ALT, ST>(p, q, wp, xs, xinv, part, cnt)) {
     if (lane == 0) set_status(kStatusWaitTile);
     drain_ring<ST>(wp, q);
   }
@@ -1007,13 +1114,12 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
 // Host launcher
 // ---------------------------------------------------------------------------
 
-template <int FMT>
-struct KernelSet {
-  template <int NV, bool DBG>
-  static void* fn() {
-    return reinterpret_cast<void*>(&matvec_kernel<FMT, NV, DBG>);
-  }
-};
+// The kernel of a launch: NV vectors per entry, ALT variant or not.
+template <int FMT, int NV>
+void* kernel_for(bool alt) {
+  return alt ? reinterpret_cast<void*>(&matvec_kernel<FMT, NV, true>)
+             : reinterpret_cast<void*>(&matvec_kernel<FMT, NV, false>);
+}
 
 // Host plan of a launch: kernel (vectors per entry), launch shape, split-K
 // and shared memory. Items are upper-bounded by one entry per routed pair.
@@ -1022,15 +1128,20 @@ struct KernelSet {
 // most one per chunk, at most kMaxSplits), so that more warps stream at once.
 // Measured on GB300: dense CB4 2048x7168 7.7 -> 4.4 us, 7168x7168 11.9 ->
 // 9.5 us; splitting the 3-chunk items of a 1440-item gather in two was slower.
+// Shared memory per CTA beyond the dynamic region: the runtime's 1 KB
+// reserve plus the kernel's static variables, rounded up.
+constexpr size_t kSmemReserve = 1024 + 512;
+
 struct LaunchPlan {
   int nv, warps, stages;
   long items;              // upper bound
-  long grid;               // CTAs of a full grid (kCtasPerSm per SM), at most `items`
+  long grid;               // CTAs of a full grid (ctas_per_sm per SM), at most `items`
   int splits, split_chunks, items_per_cta;
+  int x_slots;             // activation vectors staged per CTA
   SmemLayout smem;
 };
 
-inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm) {
+inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm, size_t smem_per_sm) {
   const Geometry g = make_geometry(a.fmt, a.N, a.K);
   LaunchPlan L;
   L.nv = launch_vectors(a.ids != nullptr, a.ntok);
@@ -1040,7 +1151,7 @@ inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm
   L.grid = (long)sm_count * ctas_per_sm;
   if (L.grid > L.items) L.grid = L.items;
   if (L.grid < 1) L.grid = 1;
-  const long warps_total = (long)sm_count * kCtasPerSm * L.warps;
+  const long warps_total = (long)sm_count * ctas_per_sm * L.warps;
   long splits = warps_total / L.items;
   if (splits < 3 && !(splits == 2 && g.chunks >= 4)) splits = 1;
   if (splits > g.chunks) splits = g.chunks;
@@ -1049,8 +1160,24 @@ inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm
   L.split_chunks = (int)((g.chunks + splits - 1) / splits);
   L.splits = (g.chunks + L.split_chunks - 1) / L.split_chunks;
   L.items_per_cta = (int)((L.items + L.grid - 1) / L.grid);
-  const uint32_t xvb = (a.fmt == MXFP4) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
-  L.smem = smem_layout(a.fmt, (uint32_t)a.nvec, xvb, g.full_tile, a.K, L.warps, L.stages, L.splits, L.items_per_cta);
+  // Every vector gets its own slot of the activation region, unless that
+  // leaves a per-slot gather's CTA more than its share of the SM's shared
+  // memory: then the region holds only the most vectors a CTA's range can
+  // touch -- a range of at most items_per_cta items covers at most
+  // (items_per_cta - 1) / row_tiles + 2 entries of up to nv vectors.
+  const uint32_t xvb = fmt_is_mx(a.fmt) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
+  L.x_slots = a.nvec;
+  L.smem = smem_layout(a.fmt, (uint32_t)L.x_slots, xvb, g.full_tile, a.K, L.warps, L.stages, L.splits,
+                       L.items_per_cta);
+  const size_t share = smem_per_sm / (size_t)ctas_per_sm;
+  if (a.ids != nullptr && a.per_slot && (size_t)L.smem.total + kSmemReserve > share) {
+    const long touch = ((long)L.items_per_cta - 1) / g.row_tiles + 2;
+    if (touch * L.nv < L.x_slots) {
+      L.x_slots = (int)(touch * L.nv);
+      L.smem = smem_layout(a.fmt, (uint32_t)L.x_slots, xvb, g.full_tile, a.K, L.warps, L.stages, L.splits,
+                           L.items_per_cta);
+    }
+  }
   return L;
 }
 
@@ -1060,8 +1187,9 @@ inline KParams make_params(const MatvecArgs& a) {
   p.w = static_cast<const uint8_t*>(a.w);
   p.expert_stride = a.expert_stride;
   p.x = static_cast<const uint8_t*>(a.x);
-  p.x_vec_bytes = (a.fmt == MXFP4) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
+  p.x_vec_bytes = fmt_is_mx(a.fmt) ? (uint32_t)a.K * 2u : (uint32_t)q8_vec_bytes(a.K);
   p.nvec = a.nvec;
+  p.x_slots = a.nvec;
   p.ids = a.ids;
   p.ntok = a.ntok;
   p.top_k = a.ids ? a.top_k : 1;
@@ -1091,20 +1219,17 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   constexpr int NVMAX = MaxVectors<FMT>::value;
   static_assert(NVMAX == 4, "kernels exist for 1 to 4 vectors per entry");
   KParams p = make_params(a);
-  LaunchPlan plan = plan_launch(a, device_sm_count(), kCtasPerSm);
+  LaunchPlan plan = plan_launch(a, device_sm_count(), kCtasPerSm, device_smem_per_sm());
   const int want_nv = plan.nv;
   const int warps = plan.warps;
   void* fn = nullptr;
-  const bool dbg = a.dbg != nullptr;
+  // ALT: block sums (codebooks) or fp16 activations (MX formats)
+  const bool alt = fmt_is_mx(FMT) ? a.x_f16 : (a.dbg != nullptr);
   switch (want_nv) {
-    case 1: fn = dbg ? KernelSet<FMT>::template fn<1, true>() : KernelSet<FMT>::template fn<1, false>(); break;
-    case 2: fn = dbg ? KernelSet<FMT>::template fn<2, true>() : KernelSet<FMT>::template fn<2, false>(); break;
-    case 3:
-      if constexpr (NVMAX >= 3) fn = dbg ? KernelSet<FMT>::template fn<3, true>() : KernelSet<FMT>::template fn<3, false>();
-      break;
-    default:
-      if constexpr (NVMAX >= 4) fn = dbg ? KernelSet<FMT>::template fn<4, true>() : KernelSet<FMT>::template fn<4, false>();
-      break;
+    case 1: fn = kernel_for<FMT, 1>(alt); break;
+    case 2: fn = kernel_for<FMT, 2>(alt); break;
+    case 3: fn = kernel_for<FMT, 3>(alt); break;
+    default: fn = kernel_for<FMT, 4>(alt); break;
   }
   g_launch_stage = "kernel selection";
   if (fn == nullptr) return cudaErrorInvalidValue;
@@ -1118,7 +1243,7 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   {
     std::lock_guard<std::mutex> lock(mu);
-    size_t& have = configured[dev][want_nv][dbg ? 1 : 0];
+    size_t& have = configured[dev][want_nv][alt ? 1 : 0];
     if (have < plan.smem.total) {
       // The opt-in limit covers static plus dynamic shared memory.
       cudaFuncAttributes fa;
@@ -1144,13 +1269,14 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   if (per_sm < kCtasPerSm) {
     // fewer CTAs fit: more items per CTA (the plan's smem only grows by the
     // split-K slots, which the opt-in above already covers up to its limit)
-    plan = plan_launch(a, device_sm_count(), per_sm);
+    plan = plan_launch(a, device_sm_count(), per_sm, device_smem_per_sm());
     g_launch_stage = "shared memory limit";
     if (plan.smem.total > device_max_smem_optin()) return cudaErrorInvalidValue;
   }
   p.splits = plan.splits;
   p.split_chunks = plan.split_chunks;
   p.items_per_cta = plan.items_per_cta;
+  p.x_slots = plan.x_slots;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.grid);

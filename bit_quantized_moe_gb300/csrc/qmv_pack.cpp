@@ -1,7 +1,7 @@
 // qmv_pack.cpp -- host packer: canonical codes + E8M0 scales <-> GPU weight layout.
 //
-// Canonical storage order (per row): MXFP4/CB4 element k in byte k/2, low
-// nibble first; CB2 code j of a byte at bits [2j, 2j+2); CB3 eight codes per
+// Canonical storage order (per row): MXFP8 element k in byte k; MXFP4/CB4
+// element k in byte k/2, low nibble first; CB2 code j of a byte at bits [2j, 2j+2); CB3 eight codes per
 // three bytes, code j at bits [3j, 3j+3) of the little-endian 24-bit word.
 // The GPU layout is described in qmv_layout.h.
 #include <cstring>
@@ -13,6 +13,8 @@ namespace qmv {
 
 static inline uint8_t canon_get(int fmt, const uint8_t* row, int k) {
   switch (fmt) {
+    case MXFP8:
+      return row[k];
     case CB2:
       return (row[k >> 2] >> (2 * (k & 3))) & 3;
     case CB3: {
@@ -27,6 +29,9 @@ static inline uint8_t canon_get(int fmt, const uint8_t* row, int k) {
 
 static inline void canon_set(int fmt, uint8_t* row, int k, uint8_t c) {
   switch (fmt) {
+    case MXFP8:
+      row[k] = c;
+      return;
     case CB2:
       row[k >> 2] = (uint8_t)(row[k >> 2] | ((c & 3) << (2 * (k & 3))));
       return;
@@ -64,7 +69,7 @@ void pack_expert(const Geometry& g, const uint8_t* codes, const uint8_t* scales,
   const int spl = lane_scale_bytes(fmt);
   std::memset(out, 0, g.expert);
   uint8_t c32[32];
-  uint8_t lb[16];
+  uint8_t lb[32];
   for (int rt = 0; rt < g.row_tiles; ++rt) {
     for (int c = 0; c < g.chunks; ++c) {
       const int L = (c == g.chunks - 1) ? g.last_lanes : 32;
@@ -103,7 +108,7 @@ void unpack_expert(const Geometry& g, const uint8_t* in, uint8_t* codes, uint8_t
   const int spl = lane_scale_bytes(fmt);
   std::memset(codes, 0, row_code_bytes * g.N);
   uint8_t c32[32];
-  uint8_t lb[16];
+  uint8_t lb[32];
   for (int rt = 0; rt < g.row_tiles; ++rt) {
     for (int c = 0; c < g.chunks; ++c) {
       const int L = (c == g.chunks - 1) ? g.last_lanes : 32;

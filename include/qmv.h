@@ -10,6 +10,11 @@
  *              Source: "perf(rocm): add an mxfp4 arm to the warp-shared
  *              gather_qmv kernel for gpt-oss decode" (mlxcel #2178),
  *              "Current Behavior" and "Proposed Solution" item 1.
+ *   QMV_MXFP8  E4M3 8-bit codes (OCP MX: exponent bias 7, subnormals,
+ *              S.1111.111 = NaN, no infinity), one E8M0 scale per 32 weights,
+ *              otherwise as MXFP4. The page lists the f16 MXFP4 and the
+ *              MXFP8 gathers as the next scope beyond the bf16 MXFP4 arm
+ *              (mlxcel #2178, "Scope").
  *   QMV_CB2    2-bit codes into a 4-entry int8 codebook, E8M0 per 16 weights.
  *   QMV_CB3    3-bit codes into an 8-entry int8 codebook, E8M0 per 16 weights.
  *   QMV_CB4    4-bit codes into a 16-entry int8 codebook, E8M0 per 32 weights.
@@ -55,7 +60,7 @@ extern "C" {
 #define QMV_ESIZE (-4)   /* a caller buffer smaller than the required size */
 #define QMV_ECUDA (-5)   /* a CUDA runtime error (message in qmv_last_error) */
 
-typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3 } qmv_fmt;
+typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3, QMV_MXFP8 = 4 } qmv_fmt;
 
 /*
  * Launch flags of qmv_dense_ex, qmv_moe_gather_ex, qmv_moe_gate_up_swiglu and
@@ -82,6 +87,15 @@ typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3 } qmv_fmt;
  */
 #define QMV_FLAG_X_F32 2u
 
+/*
+ * QMV_FLAG_X_F16 (MX formats): activations are fp16 instead of bf16 and every
+ * output the call stores is fp16 (h and y of a layer, the combined output of
+ * qmv_moe_layer_combine). The products and sums are as for bf16 (exact
+ * products, fp32 sums). The f16 MXFP4 gather is the variant mlxcel #2178
+ * ("Scope") leaves out of the bf16 arm.
+ */
+#define QMV_FLAG_X_F16 4u
+
 /* Limits checked by every entry point. */
 #define QMV_MAX_NTOK 4      /* decode tokens per call */
 #define QMV_MAX_TOPK 8      /* experts per token */
@@ -101,15 +115,16 @@ typedef struct {
   int8_t lut[16];
 } qmv_wdesc;
 
-/* Weights per E8M0 scale along K: 32 for MXFP4 and CB4, 16 for CB2 and CB3. */
+/* Weights per E8M0 scale along K: 32 for MXFP4, MXFP8 and CB4, 16 for CB2 and CB3. */
 int32_t qmv_scale_group(int32_t fmt);
 
-/* Bits per weight code: 4, 2, 3, 4 for MXFP4, CB2, CB3, CB4. */
+/* Bits per weight code: 4, 2, 3, 4, 8 for MXFP4, CB2, CB3, CB4, MXFP8. */
 int32_t qmv_code_bits(int32_t fmt);
 
 /*
  * Canonical (storage-order) sizes of ONE expert matrix, in bytes:
  *   codes:  N * K * bits / 8, row-major, each row packed as
+ *           MXFP8: element k in byte k;
  *           MXFP4/CB4: element k in byte k/2, low nibble first (a
  *             little-endian uint32 at byte k/2 holds elements k..k+7; mlxcel
  *             #2178, "Proposed Solution" item 1);
@@ -178,8 +193,10 @@ int qmv_act_q8_unpack(const void* xq_host, int32_t nvec, int32_t K, int8_t* q_ho
 /*
  * Dense decode matvec: y[t] = W . x[t] for t < ntok (1..4).
  *   w_dev: GPU layout of one matrix (desc->n_experts must be 1).
- *   x_dev: MXFP4: bf16 [ntok][K]; CB formats: q8_1 buffer of ntok vectors.
- *   y_dev: MXFP4: bf16 [ntok][N]; CB formats: fp32 [ntok][N].
+ *   x_dev: MX formats (MXFP4, MXFP8): bf16 [ntok][K] (fp16 with
+ *          QMV_FLAG_X_F16); CB formats: q8_1 buffer of ntok vectors.
+ *   y_dev: MX formats: bf16 [ntok][N] (fp16 with QMV_FLAG_X_F16); CB
+ *          formats: fp32 [ntok][N].
  * The kernel streams every packed weight byte once per call and applies it
  * to all ntok tokens.
  * Errors: QMV_EINVAL, QMV_ESHAPE, QMV_EALIGN, QMV_ECUDA.
@@ -198,8 +215,10 @@ int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32
  *            [0, n_experts) writes a zero row block (mlxcel #2178,
  *            "Implementation Notes", edge cases). A matrix used by several
  *            (token, slot) pairs is streamed once per call for up to 4 of them.
- *   x_dev:   MXFP4: bf16 vectors of K; CB formats: q8_1 buffer.
- *   y_dev:   MXFP4: bf16 [ntok][top_k][N]; CB formats: fp32 [ntok][top_k][N].
+ *   x_dev:   MX formats: bf16 vectors of K (fp16 with QMV_FLAG_X_F16); CB
+ *            formats: q8_1 buffer.
+ *   y_dev:   MX formats: bf16 [ntok][top_k][N] (fp16 with QMV_FLAG_X_F16); CB
+ *            formats: fp32 [ntok][top_k][N].
  * Errors: QMV_EINVAL (ntok not in 1..4, top_k not in 1..8), QMV_ESHAPE,
  * QMV_EALIGN, QMV_ECUDA.
  */
@@ -233,7 +252,8 @@ int qmv_moe_gather_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_de
  * MoE layer's gate, up and SwiGLU: "perf(rocm): add an mxfp4 arm to the
  * warp-shared gather_qmv kernel for gpt-oss decode", "Problem / Background"
  * and "Current Behavior"). x and h follow qmv_moe_gather with per_slot_x = 0:
- * MXFP4: x bf16 [ntok][K], h bf16 [ntok][top_k][N]; CB formats: x q8_1, h fp32.
+ * MX formats: x bf16 [ntok][K], h bf16 [ntok][top_k][N] (both fp16 with
+ * QMV_FLAG_X_F16); CB formats: x q8_1, h fp32.
  * An invalid id gives a zero row of h. flags: QMV_FLAG_* (see below).
  * Errors: as qmv_moe_gather.
  */
@@ -253,19 +273,23 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w_gate_up_dev, con
  * "DS4 H200: rocmfp2_mix MoE matvec 3.31x + ROCmFP4 dense matvec 1.53x",
  * "Caveats", with h quantized to q8_1 in between).
  *   y[t][j] = W_down[ids[t][j]] . h[t][j],  h as qmv_moe_gate_up_swiglu.
- * gate_up_desc: one projection (N, K); down_desc: (N_down, K = N). Both MXFP4
- * or both codebook formats, same n_experts. x as qmv_moe_gate_up_swiglu.
- * y: MXFP4 bf16 [ntok][top_k][N_down]; codebooks fp32.
+ * gate_up_desc: one projection (N, K); down_desc: (N_down, K = N). Both MX
+ * formats (MXFP4 and MXFP8 may be mixed) or both codebook formats, same
+ * n_experts. x as qmv_moe_gate_up_swiglu.
+ * y: MX formats bf16 [ntok][top_k][N_down] (fp16 with QMV_FLAG_X_F16);
+ * codebooks fp32.
  * Two launches: the fused gate/up/SwiGLU gather stores h in the workspace
- * (MXFP4 bf16, codebooks fp32), then the down gather reads the per-slot h
+ * (MX formats bf16 or fp16, codebooks fp32), then the down gather reads the
+ * per-slot h
  * (codebooks: it quantizes h to q8_1 while staging it, as QMV_FLAG_X_F32).
  * workspace: caller-owned device scratch of at least
  * qmv_moe_layer_workspace_bytes(gate_up_desc, ntok, top_k) bytes, 16-byte
  * aligned; its contents on entry do not matter. Calls that share a workspace
  * must be ordered on one stream.
  * flags apply to the gate/up launch (QMV_FLAG_X_F32: a codebook layer's x is
- * fp32); the down gather always prefetches its weights and ids (they were
- * complete before the layer's first launch).
+ * fp32; QMV_FLAG_X_F16: an MX layer's x, h and y are fp16); the down gather
+ * always prefetches its weights and ids (they were complete before the
+ * layer's first launch).
  */
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gate_up_desc, int32_t ntok, int32_t top_k);
 int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, const qmv_wdesc* down_desc,
@@ -280,8 +304,8 @@ int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, cons
  * "perf(rocm): add an mxfp4 arm to the warp-shared gather_qmv kernel for
  * gpt-oss decode", "Current Behavior": GptOssSwitchGLU); weighting and summing
  * them is the MoE block's combine (a reading: the pages do not print it).
- * down_desc: the down projection (N outputs, n_experts, format: MXFP4 -> ys
- * and y bf16, codebooks -> fp32). ys [ntok][top_k][N] (as qmv_moe_layer's
+ * down_desc: the down projection (N outputs, n_experts, format: MX formats
+ * -> ys and y bf16, codebooks -> fp32). ys [ntok][top_k][N] (as qmv_moe_layer's
  * y), weights fp32 [ntok][top_k], ids int32 [ntok][top_k], y [ntok][N]; all
  * on the device, 16-byte aligned. One launch (dependent launch after the
  * kernel that wrote ys).
@@ -290,9 +314,16 @@ int qmv_moe_layer(const qmv_wdesc* gate_up_desc, const void* w_gate_up_dev, cons
 int qmv_moe_combine(const qmv_wdesc* down_desc, const void* ys_dev, const float* weights_dev,
                     const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, void* stream);
 
+/* qmv_moe_combine with flags: QMV_FLAG_X_F16 (MX formats) makes ys and y
+ * fp16; flags = 0 is qmv_moe_combine. */
+int qmv_moe_combine_ex(const qmv_wdesc* down_desc, const void* ys_dev, const float* weights_dev,
+                       const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, uint32_t flags,
+                       void* stream);
+
 /*
  * qmv_moe_layer followed by qmv_moe_combine: the layer's combined output
- * y [ntok][N_down] (MXFP4 bf16, codebooks fp32) for router weights
+ * y [ntok][N_down] (MX formats bf16, or fp16 with QMV_FLAG_X_F16; codebooks
+ * fp32) for router weights
  * weights_dev fp32 [ntok][top_k]. The per-slot outputs live in the workspace,
  * which needs qmv_moe_layer_combine_workspace_bytes(...) bytes (the layer's
  * workspace followed by ntok * top_k * N_down outputs). Three launches.
@@ -363,9 +394,11 @@ int qmv_debug_dequant(const qmv_wdesc* desc, const void* w_dev, int32_t expert, 
 /*
  * Device-side status: bit flags set by kernels whose bounded waits gave up:
  * 1 (not used), 2 weight tile copy, 4 copy still in flight when giving
- * up, 8 the wait probe. No kernel here waits on another kernel, so bits 1-4
- * indicate a lost asynchronous copy. Synchronizes the device; clear != 0
- * resets the flags.
+ * up, 8 the wait probe; and 16: a CTA of a per-slot gather needed more
+ * staged activation vectors than the launch planned for (a library bug; the
+ * outputs of that call are wrong). No kernel here waits on another kernel, so
+ * bits 1-4 indicate a lost asynchronous copy. Synchronizes the device;
+ * clear != 0 resets the flags.
  */
 int qmv_device_status(uint32_t* flags_host, int32_t clear);
 

@@ -23,6 +23,27 @@ def bf16_to_np(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
+# E8M0 ranges of the synthetic weights of the MX-variant tests, chosen so that
+# the rms weight is about 0.03 (rms E2M1 value 2.9, rms E4M3 value ~92): a
+# K = 2880 layer's g, u, h and y then stay O(1-10), far inside fp16's range
+# (65504), for fp16 and bf16 activations alike.
+MX_SCALES = {"mxfp4": (112, 122), "mxfp8": (107, 117)}
+
+
+def act_bits(g, x_dtype: str, shape) -> np.ndarray:
+    """N(0,1) activations as bf16 or fp16 bit patterns."""
+    return qi.normal_bf16_bits(g, shape) if x_dtype == "bf16" else qi.normal_f16_bits(g, shape)
+
+
+def act_to_dev(bits: np.ndarray, x_dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV)
+    return t.view(torch.bfloat16 if x_dtype == "bf16" else torch.float16)
+
+
+def mx_flags(x_dtype: str) -> int:
+    return qmv.QMV_FLAG_X_F16 if x_dtype == "f16" else 0
+
+
 class Matrices:
     """E expert matrices of one format; only `experts` hold drawn data, the
     rest of the device buffer is zero (the kernels never read them)."""
@@ -37,7 +58,7 @@ class Matrices:
         self.codes, self.scales = {}, {}
         self.w = torch.zeros(self.eb * E, dtype=torch.uint8, device=DEV)
         for e in sorted(set(int(v) for v in experts if 0 <= int(v) < E)):
-            c = qi.codes(g, (N, K), qi.FORMAT_BITS[fmt])
+            c = qi.format_codes(g, fmt, (N, K))
             s = qi.e8m0(g, (N, K // qi.FORMAT_GROUP[fmt]), scale_lo, scale_hi)
             self.set_expert(e, c, s)
 

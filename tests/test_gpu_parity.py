@@ -15,8 +15,8 @@ import qmv_inputs as qi
 pytestmark = pytest.mark.gpu
 
 qmv = pytest.importorskip("bit_quantized_moe_gb300")
-from qmv_testutil import (DEV, Matrices, assert_close, bf16_to_np, quantize_on_gpu,  # noqa: E402
-                          status_clean, to_dev)
+from qmv_testutil import (DEV, MX_SCALES, Matrices, act_bits, act_to_dev, assert_close,  # noqa: E402
+                          bf16_to_np, mx_flags, quantize_on_gpu, status_clean, to_dev)
 
 LUTS = {"cb2": qi.LUT_CB2, "cb3": qi.LUT_CB3, "cb4": qi.LUT_CB4}
 
@@ -25,7 +25,7 @@ LUTS = {"cb2": qi.LUT_CB2, "cb3": qi.LUT_CB3, "cb4": qi.LUT_CB4}
 # Decode of the packed layout and the activation quantizer (bit-exact)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "cb2", "cb3", "cb4"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "cb2", "cb3", "cb4", "mxfp8"])
 @pytest.mark.parametrize("N,K", [(17, 96), (516, 2880), (16, 2048)])
 def test_dequant_bit_exact(fmt, N, K):
     m = Matrices(fmt, N, K, 1, [0], seed=N + K, lut=LUTS.get(fmt), scale_lo=0, scale_hi=255)
@@ -34,6 +34,8 @@ def test_dequant_bit_exact(fmt, N, K):
     got = out.cpu().numpy()
     if fmt == "mxfp4":
         ref = oracle.mxfp4_dequant(m.codes[0], m.scales[0])
+    elif fmt == "mxfp8":
+        ref = oracle.mxfp8_dequant(m.codes[0], m.scales[0])
     else:
         ref = oracle.cb_dequant(m.codes[0], m.scales[0], m.lut, qi.FORMAT_GROUP[fmt])
     with np.errstate(over="ignore"):
@@ -443,18 +445,19 @@ class GateUp:
         bits, grp = qi.FORMAT_BITS[fmt], qi.FORMAT_GROUP[fmt]
         self.cg, self.sg, self.cu, self.su = {}, {}, {}, {}
         for e in sorted(set(int(v) for v in experts if 0 <= int(v) < E)):
-            self.cg[e], self.cu[e] = qi.codes(g, (N, K), bits), qi.codes(g, (N, K), bits)
+            self.cg[e], self.cu[e] = qi.format_codes(g, fmt, (N, K)), qi.format_codes(g, fmt, (N, K))
             self.sg[e] = qi.e8m0(g, (N, K // grp), scale_lo, scale_hi)
             self.su[e] = qi.e8m0(g, (N, K // grp), scale_lo, scale_hi)
             p = qmv.qmv_pack_gate_up(one, oracle.pack_codes(fmt, self.cg[e][None]), self.sg[e][None],
                                      oracle.pack_codes(fmt, self.cu[e][None]), self.su[e][None])
             self.w[e * eb:(e + 1) * eb] = torch.from_numpy(p).to(DEV)
 
-    def matvecs(self, xin, q=None, d=None):
+    def matvecs(self, xin, q=None, d=None, x_dtype="bf16"):
         """(gate, up, gate |w x|, up |w x|) callables of (expert, token) for the oracle."""
-        if self.fmt == "mxfp4":
-            mv = lambda c, s: (lambda e, t: oracle.mxfp4_matvec(c[e], s[e], xin[t:t + 1])[0])
-            ab = lambda c, s: (lambda e, t: oracle.mxfp4_abs_products(c[e], s[e], xin[t:t + 1])[0])
+        if self.fmt in ("mxfp4", "mxfp8"):
+            f = self.fmt
+            mv = lambda c, s: (lambda e, t: oracle.mx_matvec(f, c[e], s[e], xin[t:t + 1], x_dtype)[0])
+            ab = lambda c, s: (lambda e, t: oracle.mx_abs_products(f, c[e], s[e], xin[t:t + 1], x_dtype)[0])
         else:
             grp = qi.FORMAT_GROUP[self.fmt]
             mv = lambda c, s: (lambda e, t: oracle.cb_matvec(c[e], s[e], self.lut, grp, q[t:t + 1], d[t:t + 1])[0])
@@ -463,14 +466,14 @@ class GateUp:
         return mv(self.cg, self.sg), mv(self.cu, self.su), ab(self.cg, self.sg), ab(self.cu, self.su)
 
 
-def check_gate_up(m, ids, h_gpu, xin, q=None, d=None):
-    gm, um, ga, ua = m.matvecs(xin, q, d)
+def check_gate_up(m, ids, h_gpu, xin, q=None, d=None, x_dtype="bf16"):
+    gm, um, ga, ua = m.matvecs(xin, q, d, x_dtype)
     h, gv, uv = oracle.moe_gate_up_swiglu(gm, um, m.E, ids, m.N)
     tg = oracle.moe_gather(ga, m.E, ids, False, m.N) * 1e-3
     tu = oracle.moe_gather(ua, m.E, ids, False, m.N) * 1e-3
     tol = oracle.swiglu_tolerance(gv, uv, tg, tu)
-    if m.fmt == "mxfp4":
-        tol = tol + np.abs(h) * 2.0 ** -8
+    if m.fmt in ("mxfp4", "mxfp8"):
+        tol = tol + np.abs(h) * 2.0 ** -8 + 2.0 ** -24    # one bf16 ulp (fp16: also its subnormal quantum)
     err = np.abs(h_gpu - h)
     bad = ~(err <= tol + 1e-30)
     assert not bad.any(), f"{bad.sum()} fused outputs outside tolerance, first {np.argwhere(bad)[0]}"
@@ -509,23 +512,33 @@ def test_cb_gate_up_swiglu(fmt):
 # One MoE layer: fused gate/up/SwiGLU, then down on the per-slot h
 # ---------------------------------------------------------------------------
 
-def _layer_expected(gu, down, ids, x=None, q=None, d=None):
+MX = ("mxfp4", "mxfp8")
+
+
+def _mx_dequant(fmt, codes, scales):
+    return oracle.mxfp4_dequant(codes, scales) if fmt == "mxfp4" else oracle.mxfp8_dequant(codes, scales)
+
+
+def _layer_expected(gu, down, ids, x=None, q=None, d=None, x_dtype="bf16"):
     """Oracle chain and the per-output bound for y. h differs from the GPU's
-    by the propagated SwiGLU bound plus its storage rounding (a bf16 ulp for
-    MXFP4, one q8_1 quantum of its block for the codebooks)."""
-    gm, um, ga, ua = gu.matvecs(x, q, d)
+    by the propagated SwiGLU bound plus its storage rounding (a bf16 ulp, or
+    an fp16 one, for the MX formats; one q8_1 quantum of its block for the
+    codebooks)."""
+    gm, um, ga, ua = gu.matvecs(x, q, d, x_dtype)
     h, gv, uv = oracle.moe_gate_up_swiglu(gm, um, gu.E, ids, gu.N)
     tol_h = oracle.swiglu_tolerance(gv, uv, oracle.moe_gather(ga, gu.E, ids, False, gu.N) * 1e-3,
                                     oracle.moe_gather(ua, gu.E, ids, False, gu.N) * 1e-3)
     ntok, top_k = ids.shape
     rows = h.reshape(ntok * top_k, gu.N)
-    if gu.fmt == "mxfp4":
-        hb = oracle.f64_to_bf16_bits(rows)
-        hx = oracle.bf16_bits_to_f64(hb)
-        dh = tol_h.reshape(rows.shape) + np.abs(hx) * 2.0 ** -8 * 2
-        y = oracle.mxfp4_moe_gather(np.stack([down.codes.get(e, np.zeros((down.N, down.K), np.uint8)) for e in range(down.E)]),
-                                    np.stack([down.scales.get(e, np.zeros((down.N, down.K // 32), np.uint8)) for e in range(down.E)]),
-                                    hb, ids, True)
+    tiny = 2.0 ** -24 if x_dtype == "f16" else 0.0
+    if gu.fmt in MX:
+        hb = oracle.f64_to_bf16_bits(rows) if x_dtype == "bf16" else oracle.f64_to_f16_bits(rows)
+        hx = oracle.act_bits_to_f64(hb, x_dtype)
+        dh = tol_h.reshape(rows.shape) + np.abs(hx) * 2.0 ** -8 * 2 + tiny
+        y = oracle.mx_moe_gather(down.fmt,
+                                 np.stack([down.codes.get(e, np.zeros((down.N, down.K), np.uint8)) for e in range(down.E)]),
+                                 np.stack([down.scales.get(e, np.zeros((down.N, down.K // 32), np.uint8)) for e in range(down.E)]),
+                                 hb, ids, True, x_dtype)
     else:
         hq, hd = oracle.q8_1_quantize(rows.astype(np.float32))
         dq = oracle.f16_bits_to_f64(hd)
@@ -540,15 +553,15 @@ def _layer_expected(gu, down, ids, x=None, q=None, d=None):
             e, s = int(ids[t, j]), t * top_k + j
             if not (0 <= e < down.E):
                 continue
-            if down.fmt == "mxfp4":
-                Wabs = np.abs(oracle.mxfp4_dequant(down.codes[e], down.scales[e]))
-                base = Wabs @ np.abs(oracle.bf16_bits_to_f64(hb[s]))
+            if down.fmt in MX:
+                Wabs = np.abs(_mx_dequant(down.fmt, down.codes[e], down.scales[e]))
+                base = Wabs @ np.abs(oracle.act_bits_to_f64(hb[s], x_dtype))
             else:
                 Wabs = np.abs(oracle.cb_dequant(down.codes[e], down.scales[e], down.lut, grp))
                 base = Wabs @ np.abs(hq[s].astype(np.float64) * np.repeat(dq[s], 32))
             tol[t, j] = 1e-3 * base + Wabs @ dh[s]
-    if down.fmt == "mxfp4":
-        tol = tol + np.abs(y) * 2.0 ** -8
+    if down.fmt in MX:
+        tol = tol + np.abs(y) * 2.0 ** -8 + tiny
     return y, tol
 
 

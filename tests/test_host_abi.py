@@ -38,20 +38,21 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_format_constants():
     assert "sm_103a" in qmv.qmv_version()
-    assert [qmv.qmv_scale_group(f) for f in ("mxfp4", "cb2", "cb3", "cb4")] == [32, 16, 16, 32]
-    assert [qmv.qmv_code_bits(f) for f in ("mxfp4", "cb2", "cb3", "cb4")] == [4, 2, 3, 4]
+    assert [qmv.qmv_scale_group(f) for f in ("mxfp4", "cb2", "cb3", "cb4", "mxfp8")] == [32, 16, 16, 32, 32]
+    assert [qmv.qmv_code_bits(f) for f in ("mxfp4", "cb2", "cb3", "cb4", "mxfp8")] == [4, 2, 3, 4, 8]
+    assert qmv.qmv_code_bits(5) == 0
     assert qmv.qmv_scale_group(7) == 0
 
 
 SHAPES = [(1, 32), (5, 96), (16, 1024), (17, 1056), (40, 2048), (516, 2880)]
 
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "cb2", "cb3", "cb4"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "cb2", "cb3", "cb4", "mxfp8"])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_pack_roundtrip_bit_exact(fmt, N, K):
     E = 2
     g = qi.rng(100 + N + K)
-    codes = qi.codes(g, (E, N, K), qi.FORMAT_BITS[fmt])
+    codes = qi.codes(g, (E, N, K), qi.FORMAT_BITS[fmt])   # every byte value, NaN codes included
     scales = qi.e8m0(g, (E, N, K // qi.FORMAT_GROUP[fmt]), 0, 255)
     canon = oracle.pack_codes(fmt, codes)
     d = qmv.wdesc(fmt, N, K, E)
@@ -68,7 +69,7 @@ def test_pack_roundtrip_bit_exact(fmt, N, K):
 
 def test_pack_changes_with_every_code():
     """Every canonical code bit lands somewhere in the GPU layout (no dropped bits)."""
-    for fmt in ("mxfp4", "cb2", "cb3", "cb4"):
+    for fmt in ("mxfp4", "cb2", "cb3", "cb4", "mxfp8"):
         N, K = 3, 64
         d = qmv.wdesc(fmt, N, K)
         codes = np.zeros((1, N, K), dtype=np.uint8)
@@ -104,6 +105,10 @@ def test_packed_bytes_match_algorithmic_bytes():
     assert qmv.qmv_packed_expert_bytes(d) == 4587520
     d = qmv.wdesc("cb4", 7168, 7168)
     assert qmv.qmv_packed_expert_bytes(d) == 27295744
+    # MXFP8 2880 x 2880: 2880 code bytes + 90 scale bytes per row
+    d = qmv.wdesc("mxfp8", 2880, 2880)
+    alg = 2880 * 2880 + 2880 * 90
+    assert alg <= qmv.qmv_packed_expert_bytes(d) < alg + 256
 
 
 def test_q8_sizes_and_unpack():
@@ -205,7 +210,16 @@ def test_unknown_launch_flags_rejected():
     rc = qmv.lib.qmv_moe_gather_ex(qmv.ctypes.byref(d), FAKE, FAKE, 0, FAKE, 1, 4, FAKE, 6, 0)
     assert rc == qmv.QMV_EINVAL
     d = qmv.wdesc("cb2", 64, 64)
-    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 4, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 8, 0) == qmv.QMV_EINVAL
+    # fp16 activations exist only for the MX formats, fp32 ones only for the codebooks
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL
+    m8 = qmv.wdesc("mxfp8", 64, 64)
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(m8), FAKE, FAKE, 1, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(m8), FAKE, FAKE, 1, FAKE, 8, 0) == qmv.QMV_EINVAL
+    C = qmv.lib.qmv_moe_combine_ex
+    cb = qmv.wdesc("cb3", 64, 64, 4)
+    assert C(qmv.ctypes.byref(cb), FAKE, FAKE, FAKE, 1, 4, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL
+    assert C(qmv.ctypes.byref(m8), FAKE, FAKE, FAKE, 1, 4, FAKE, 1, 0) == qmv.QMV_EINVAL
 
 
 @pytest.mark.parametrize("fmt", ["mxfp4", "cb3"])
@@ -252,7 +266,7 @@ def test_moe_layer_argument_errors():
     cb = qmv.wdesc("cb3", 2880, 2880, 32)
     assert L(B(gu), FAKE, B(cb), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, None, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
-    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 4, 0) == qmv.QMV_EINVAL   # unknown flag
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 8, 0) == qmv.QMV_EINVAL   # unknown flag
     # fp32 activations exist only for the codebook formats
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
     d = qmv.wdesc("mxfp4", 64, 64)
@@ -281,4 +295,4 @@ def test_combine_argument_errors():
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need - 16, FAKE, 0, 0) == qmv.QMV_ESIZE
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, None, 2, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, None, need, FAKE, 0, 0) == qmv.QMV_ESIZE
-    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need, FAKE, 4, 0) == qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need, FAKE, 8, 0) == qmv.QMV_EINVAL
