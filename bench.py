@@ -712,8 +712,9 @@ def run_configs(args):
 
 def run_profile_config(args):
     """A few eager calls of one config's call on a small resident expert set
-    (16 experts; full-size matrices), for ncu captures of the codebook and
-    dense kernels. Prints one status line, no JSON."""
+    (16 experts, 32 for the MXFP8 layer; full-size matrices), for ncu
+    captures of the codebook, dense and MXFP8 kernels. Prints one status
+    line, no JSON."""
     import torch
 
     import bit_quantized_moe_gb300 as qmv
@@ -750,6 +751,20 @@ def run_profile_config(args):
         ids = torch.from_numpy(np.stack([qi.topk_ids(g, 1, 4, E) for _ in range(calls)])).to(dev)
         h = torch.empty(1, 4, 2048, dtype=torch.float32, device=dev)
         fn = lambda i: qmv.qmv_moe_gate_up_swiglu(dg, w, xq, ids[i], 1, 4, h)
+    elif cfg == 5:
+        # MXFP8 gpt-oss-shaped layer: fused gate/up/SwiGLU then down, 32 experts
+        E8, N8 = 32, 2880
+        dg = qmv.wdesc("mxfp8", N8, N8, E8)
+        c1 = qi.canonical_uniform_codes(g, (E8, N8), N8, 8)
+        c2 = qi.canonical_uniform_codes(g, (E8, N8), N8, 8)
+        s1, s2 = qi.e8m0(g, (E8, N8, N8 // 32), 112, 122), qi.e8m0(g, (E8, N8, N8 // 32), 112, 122)
+        wg = torch.from_numpy(qmv.qmv_pack_gate_up(dg, c1, s1, c2, s2)).to(dev)
+        w, d = packed("mxfp8", E8, N8, N8)
+        x = torch.from_numpy(qi.normal_bf16_bits(g, (1, N8)).view(np.int16)).to(dev).view(torch.bfloat16)
+        ids = torch.from_numpy(np.stack([qi.topk_ids(g, 1, 4, E8) for _ in range(calls)])).to(dev)
+        ws = torch.empty(qmv.qmv_moe_layer_workspace_bytes(dg, 1, 4), dtype=torch.uint8, device=dev)
+        y = torch.empty(1, 4, N8, dtype=torch.bfloat16, device=dev)
+        fn = lambda i: qmv.qmv_moe_layer(dg, wg, d, w, x, ids[i], 1, 4, ws, y, qmv.QMV_FLAG_PREFETCH_INPUTS)
     elif cfg == 3:
         w, d = packed("cb3", E, 7168, 2048)
         xq = q8(16, 2048)
@@ -782,8 +797,9 @@ def main(argv=None):
     ap.add_argument("--digest", action="store_true", help="print the kernel source digest and exit")
     ap.add_argument("--configs", action="store_true",
                     help="measure every config of the workload set (one JSON line per call type) and exit")
-    ap.add_argument("--profile-config", type=int, choices=[0, 2, 3, 4], default=None,
-                    help="a few eager calls of one config on a small resident set, for ncu captures")
+    ap.add_argument("--profile-config", type=int, choices=[0, 2, 3, 4, 5], default=None,
+                    help="a few eager calls of one config on a small resident set, for ncu captures "
+                         "(5: the MXFP8 layer)")
     args = ap.parse_args(argv)
     if args.digest:
         print(kernel_source_digest())
