@@ -641,6 +641,28 @@ def run_configs(args):
             emit(4, f"qmv_dense CB4 {N4}x{K4} ntok={ntok}", alg, t / n4, {"calls_per_graph": n4})
         del W4
 
+    # --- verify batches (f3): dense 8 and 16 tokens (one weight stream per 4 tokens, side by side)
+    for fmt, (Nv, Kv) in (("mxfp4", (2880, 2880)), ("cb4", (7168, 7168))):
+        dv = qmv.wdesc(fmt, Nv, Kv, 1, luts(fmt))
+        bv = qmv.qmv_packed_bytes(dv)
+        algv = Nv * Kv // 2 + Nv * (Kv // 32)
+        nv_ = -(-4 * L2_BYTES // bv)
+        cv, sv = canon(fmt, 2, Nv, Kv)
+        Wv = _replicated(qmv, torch, dev, qmv.wdesc(fmt, Nv, Kv, 2, luts(fmt)),
+                         lambda: qmv.qmv_pack_weights(qmv.wdesc(fmt, Nv, Kv, 2, luts(fmt)), cv, sv), nv_, bv)
+        for ntok in (8, 16):
+            if fmt == "mxfp4":
+                xv = torch.from_numpy(qi.normal_bf16_bits(g, (ntok, Kv)).view(np.int16)).to(dev).view(torch.bfloat16)
+                yv = torch.empty(nv_, ntok, Nv, dtype=torch.bfloat16, device=dev)
+            else:
+                xv = torch.empty(qmv.qmv_act_q8_bytes(ntok, Kv), dtype=torch.uint8, device=dev)
+                qmv.qmv_quantize_act_q8(torch.from_numpy(qi.normal_f32(g, (ntok, Kv))).to(dev), ntok, Kv, xv)
+                yv = torch.empty(nv_, ntok, Nv, dtype=torch.float32, device=dev)
+            t, _ = _graph_time(torch, lambda: [qmv.qmv_dense_ex(dv, Wv[i], xv, ntok, yv[i], PF) for i in range(nv_)])
+            emit("f3", f"qmv_dense {fmt.upper()} {Nv}x{Kv} verify ntok={ntok}", algv, t / nv_,
+                 {"calls_per_graph": nv_, "weights_x_tokens_per_s": Nv * Kv * ntok / (t / nv_)})
+        del Wv
+
     # --- config 1 layer, both launch structures (the headline bench line uses the default)
     dgm, ddm = qmv.wdesc("mxfp4", N, K, E), qmv.wdesc("mxfp4", K, N, E)
     egm, edm = qmv.qmv_packed_gate_up_expert_bytes(dgm), qmv.qmv_packed_expert_bytes(ddm)
@@ -660,6 +682,17 @@ def run_configs(args):
     t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgm, Wgm[l], ddm, Wdm[l], xm, idsm[l], 1, TOP_K, wsm,
                                                          ym[l], PF) for l in range(Lm)])
     emit(1, "qmv_moe_layer MXFP4 2880 E=32 top4 ntok=1 (2 launches)", LAYER_BYTES, t / Lm, {"calls_per_graph": Lm})
+    # an 8-token verify batch through the same layers (32 routed slots per layer)
+    ids8 = torch.from_numpy(np.stack([qi.topk_ids(g, 8, TOP_K, E) for _ in range(Lm)])).to(dev)
+    x8 = torch.from_numpy(qi.normal_bf16_bits(g, (8, K)).view(np.int16)).to(dev).view(torch.bfloat16)
+    ws8 = torch.zeros(qmv.qmv_moe_layer_workspace_bytes(dgm, 8, TOP_K), dtype=torch.uint8, device=dev)
+    y8m = torch.empty(Lm, 8, TOP_K, K, dtype=torch.bfloat16, device=dev)
+    distinct8 = [len(set(r.reshape(-1).tolist())) for r in ids8.cpu().numpy()]
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_layer(dgm, Wgm[l], ddm, Wdm[l], x8, ids8[l], 8, TOP_K, ws8,
+                                                         y8m[l], PF) for l in range(Lm)])
+    emit("f3", "qmv_moe_layer MXFP4 2880 E=32 top4 verify ntok=8 (32 routed slots, 2 launches)",
+         3 * MATRIX_BYTES * sum(distinct8) / Lm, t / Lm,
+         {"calls_per_graph": Lm, "distinct_experts_mean": sum(distinct8) / Lm})
     # fp16 activations (QMV_FLAG_X_F16): same weights, x, h and y in fp16; x is
     # scaled by 2^-10 so that h and y stay inside fp16's range with these weights
     x16 = (qi.normal_f32(g, (1, K)) * np.float32(2.0 ** -10)).astype(np.float16)

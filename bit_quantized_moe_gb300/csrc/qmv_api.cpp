@@ -134,6 +134,8 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   if (gather) {
     if (top_k < 1 || top_k > QMV_MAX_TOPK)
       return fail(QMV_EINVAL, "%s: top_k=%d outside [1, %d]", name, top_k, QMV_MAX_TOPK);
+    if (ntok * top_k > QMV_MAX_SLOTS)
+      return fail(QMV_EINVAL, "%s: ntok * top_k = %d routed slots > %d", name, ntok * top_k, QMV_MAX_SLOTS);
   } else if (desc->n_experts != 1) {
     return fail(QMV_EINVAL, "%s: a dense matvec needs n_experts == 1 (got %d)", name, desc->n_experts);
   }
@@ -298,8 +300,8 @@ size_t qmv_act_q8_bytes(int32_t nvec, int32_t K) {
 
 int qmv_quantize_act_q8(const float* x, int32_t nvec, int32_t K, void* xq, size_t xq_bytes, void* stream) {
   if (!x || !xq) return fail(QMV_EINVAL, "qmv_quantize_act_q8: NULL pointer");
-  if (nvec < 1 || nvec > QMV_MAX_NTOK * QMV_MAX_TOPK)
-    return fail(QMV_EINVAL, "qmv_quantize_act_q8: nvec=%d outside [1, %d]", nvec, QMV_MAX_NTOK * QMV_MAX_TOPK);
+  if (nvec < 1 || nvec > QMV_MAX_SLOTS)
+    return fail(QMV_EINVAL, "qmv_quantize_act_q8: nvec=%d outside [1, %d]", nvec, QMV_MAX_SLOTS);
   if (K < 32 || K > QMV_MAX_K || K % 32)
     return fail(QMV_ESHAPE, "qmv_quantize_act_q8: K=%d must be a multiple of 32 in [32, %d]", K, QMV_MAX_K);
   if (!aligned16(x) || !aligned16(xq)) return fail(QMV_EALIGN, "qmv_quantize_act_q8: pointers must be 16-byte aligned");
@@ -381,7 +383,9 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, 
 
 // Workspace of qmv_moe_layer: h (MXFP4: bf16; codebooks: fp32).
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gu, int32_t ntok, int32_t top_k) {
-  if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK) return 0;
+  if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK ||
+      ntok * top_k > QMV_MAX_SLOTS)
+    return 0;
   const size_t slots = (size_t)ntok * top_k;
   if (fmt_is_mx(gu->fmt)) return (slots * gu->N * 2 + 255) / 256 * 256;
   if (gu->N % 32) return 0;
@@ -402,7 +406,7 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   if (down->K != gu->N) return fail(QMV_ESHAPE, "%s: down K=%d must equal gate/up N=%d", name, down->K, gu->N);
   if (down->n_experts != gu->n_experts)
     return fail(QMV_EINVAL, "%s: gate/up and down expert counts differ (%d, %d)", name, gu->n_experts, down->n_experts);
-  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK)
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK || ntok * top_k > QMV_MAX_SLOTS)
     return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
   const size_t need = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
   if (ws_bytes < need) return fail(QMV_ESIZE, "%s: workspace %zu bytes < %zu", name, ws_bytes, need);
@@ -428,7 +432,7 @@ int qmv_moe_combine_ex(const qmv_wdesc* down, const void* ys, const float* weigh
   if ((flags & QMV_FLAG_X_F16) && !fmt_is_mx(down->fmt))
     return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F16 applies to the MX formats only", name);
   if (!ys || !weights || !ids || !y) return fail(QMV_EINVAL, "%s: NULL pointer", name);
-  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK)
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK || ntok * top_k > QMV_MAX_SLOTS)
     return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
   if (!aligned16(ys) || !aligned16(weights) || !aligned16(ids) || !aligned16(y))
     return fail(QMV_EALIGN, "%s: pointers must be 16-byte aligned", name);

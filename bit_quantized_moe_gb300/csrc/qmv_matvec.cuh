@@ -93,7 +93,7 @@ inline int launch_vectors(bool gather, int ntok) {
   const int cap = gather ? 2 : 4;
   return ntok < cap ? ntok : cap;
 }
-constexpr int kMaxEntries = 32;  // ntok * top_k <= 4 * 8
+constexpr int kMaxEntries = 32;  // routed slots (ntok * top_k) of a gather; dense entries <= 16 / 4
 constexpr int kMaxDevices = 64;
 
 struct Entry {
@@ -112,6 +112,7 @@ struct KParams {
   int x_slots;            // vectors the shared activation region holds (<= nvec)
   const int32_t* ids;
   int ntok, top_k, per_slot, n_experts;
+  int contig;             // deal contiguous item ranges and stage only the vectors they use
   int N, K, row_tiles, chunks, last_lanes;
   uint32_t full_tile, last_tile;
   uint64_t rowtile;
@@ -236,8 +237,11 @@ __device__ int build_entries_warp(const KParams& p, Entry* ent, int* s_ids) {
 // every CTA (and, with a full grid, every SM). Calls whose vectors are shared
 // by all slots (dense, gate/up) deal items round-robin (CTA b: b, b + G,
 // ...), so that at any moment the grid streams neighbouring row tiles.
-// Per-slot gathers give each CTA a contiguous range, which lies within one or
-// two entries, so the CTA stages only those entries' vectors. Item k of the
+// Per-slot gathers, and dense calls of more than one entry (over 4 tokens),
+// give each CTA a contiguous range (p.contig), which lies within one or two
+// entries, so the CTA stages only those entries' vectors; the entries of a
+// dense call then stream the same row tiles at about the same time, and all
+// but the first read them from L2. Item k of the
 // CTA is split into `splits` K ranges, and task lt = k * splits + r (range r
 // of item k) goes to warp lt % W. A warp streams the tiles of its tasks, in
 // order, through its ring. Lane 0 keeps the issue cursor (the next task and
@@ -265,7 +269,7 @@ __device__ __forceinline__ int task_item(const KParams& p, const WarpPipe& wp, i
 // The CTA's items first, first + stride, ... (count of them) out of n.
 __device__ __forceinline__ void cta_items(const KParams& p, int n, int& first, int& stride, int& count) {
   const int b = blockIdx.x, G = gridDim.x;
-  if (p.per_slot) {
+  if (p.contig) {
     const int per = n / G, rem = n % G;
     first = b * per + (b < rem ? b : rem);
     count = per + (b < rem ? 1 : 0);
@@ -1031,7 +1035,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   // at consecutive positions and the CTA's entries are pointed at them. The
   // compact region holds the most vectors a CTA's range can touch; a longer
   // list is recorded in the status word and cut (a planning error).
-  if (p.per_slot) {
+  if (p.contig) {
     if (warp == 0) {
       uint32_t used = 0;
       if (items_here > 0) {
@@ -1062,8 +1066,8 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     }
     __syncthreads();
   }
-  const int* vlist = p.per_slot ? s_vlist : nullptr;
-  const int nvl = p.per_slot ? s_nvl : p.nvec;
+  const int* vlist = p.contig ? s_vlist : nullptr;
+  const int nvl = p.contig ? s_nvl : p.nvec;
   const bool compact = p.x_slots < p.nvec;
   if (early) pdl_wait();
   // Dependents are released only after this kernel's own wait, so when one
@@ -1138,6 +1142,7 @@ struct LaunchPlan {
   long grid;               // CTAs of a full grid (ctas_per_sm per SM), at most `items`
   int splits, split_chunks, items_per_cta;
   int x_slots;             // activation vectors staged per CTA
+  int contig;              // contiguous dealing (per-slot gathers, dense calls of several entries)
   SmemLayout smem;
 };
 
@@ -1148,6 +1153,7 @@ inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm
   launch_shape(L.nv, L.warps, L.stages);
   const long entries = a.ids ? (long)a.ntok * a.top_k : (a.ntok + L.nv - 1) / L.nv;
   L.items = entries * g.row_tiles;
+  L.contig = (a.ids != nullptr) ? (a.per_slot ? 1 : 0) : (entries > 1 ? 1 : 0);
   L.grid = (long)sm_count * ctas_per_sm;
   if (L.grid > L.items) L.grid = L.items;
   if (L.grid < 1) L.grid = 1;
@@ -1161,7 +1167,7 @@ inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm
   L.splits = (g.chunks + L.split_chunks - 1) / L.split_chunks;
   L.items_per_cta = (int)((L.items + L.grid - 1) / L.grid);
   // Every vector gets its own slot of the activation region, unless that
-  // leaves a per-slot gather's CTA more than its share of the SM's shared
+  // leaves a contiguously dealt CTA more than its share of the SM's shared
   // memory: then the region holds only the most vectors a CTA's range can
   // touch -- a range of at most items_per_cta items covers at most
   // (items_per_cta - 1) / row_tiles + 2 entries of up to nv vectors.
@@ -1170,7 +1176,7 @@ inline LaunchPlan plan_launch(const MatvecArgs& a, int sm_count, int ctas_per_sm
   L.smem = smem_layout(a.fmt, (uint32_t)L.x_slots, xvb, g.full_tile, a.K, L.warps, L.stages, L.splits,
                        L.items_per_cta);
   const size_t share = smem_per_sm / (size_t)ctas_per_sm;
-  if (a.ids != nullptr && a.per_slot && (size_t)L.smem.total + kSmemReserve > share) {
+  if (L.contig && (size_t)L.smem.total + kSmemReserve > share) {
     const long touch = ((long)L.items_per_cta - 1) / g.row_tiles + 2;
     if (touch * L.nv < L.x_slots) {
       L.x_slots = (int)(touch * L.nv);
@@ -1194,6 +1200,7 @@ inline KParams make_params(const MatvecArgs& a) {
   p.ntok = a.ntok;
   p.top_k = a.ids ? a.top_k : 1;
   p.per_slot = a.per_slot;
+  p.contig = 0;
   p.n_experts = a.n_experts;
   p.N = a.N;
   p.K = a.K;
@@ -1277,6 +1284,7 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   p.split_chunks = plan.split_chunks;
   p.items_per_cta = plan.items_per_cta;
   p.x_slots = plan.x_slots;
+  p.contig = plan.contig;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.grid);

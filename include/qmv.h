@@ -3,7 +3,8 @@
  * NVIDIA GB300 (sm_103a), dense and MoE expert-gathered.
  *
  * Operation. For a weight matrix W (N rows x K columns) stored block-quantized
- * and 1..4 decode tokens, y = W . x per token. Weight formats:
+ * and 1..16 decode (or speculative-verify) tokens, y = W . x per token.
+ * Weight formats:
  *
  *   QMV_MXFP4  E2M1 4-bit codes, one E8M0 scale per 32 weights along K,
  *              times bf16 activations, fp32 accumulation, bf16 output.
@@ -97,8 +98,9 @@ typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3, QMV_MXFP8 =
 #define QMV_FLAG_X_F16 4u
 
 /* Limits checked by every entry point. */
-#define QMV_MAX_NTOK 4      /* decode tokens per call */
+#define QMV_MAX_NTOK 16     /* decode / verify tokens per call */
 #define QMV_MAX_TOPK 8      /* experts per token */
+#define QMV_MAX_SLOTS 32    /* routed (token, slot) pairs of a gather: ntok * top_k */
 #define QMV_MAX_N (1 << 20)
 #define QMV_MAX_K (1 << 16)
 
@@ -191,14 +193,19 @@ int qmv_quantize_act_q8(const float* x_dev, int32_t nvec, int32_t K, void* xq_de
 int qmv_act_q8_unpack(const void* xq_host, int32_t nvec, int32_t K, int8_t* q_host, uint16_t* d_host);
 
 /*
- * Dense decode matvec: y[t] = W . x[t] for t < ntok (1..4).
+ * Dense decode matvec: y[t] = W . x[t] for t < ntok (1..16; more than a
+ * few tokens is a speculative-decoding verify batch, which the pages run
+ * through a batched matmul: "perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on
+ * RDNA ...", "Depends on": the batched ROCmFPX MMQ).
  *   w_dev: GPU layout of one matrix (desc->n_experts must be 1).
  *   x_dev: MX formats (MXFP4, MXFP8): bf16 [ntok][K] (fp16 with
  *          QMV_FLAG_X_F16); CB formats: q8_1 buffer of ntok vectors.
  *   y_dev: MX formats: bf16 [ntok][N] (fp16 with QMV_FLAG_X_F16); CB
  *          formats: fp32 [ntok][N].
- * The kernel streams every packed weight byte once per call and applies it
- * to all ntok tokens.
+ * Up to 4 tokens the kernel streams every packed weight byte once per call
+ * and applies it to all of them; a call of more tokens streams the matrix
+ * once per group of 4 tokens, the groups side by side so that all but the
+ * first read it from L2 (the DRAM traffic stays about one matrix).
  * Errors: QMV_EINVAL, QMV_ESHAPE, QMV_EALIGN, QMV_ECUDA.
  */
 int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t ntok, void* y_dev,
@@ -219,7 +226,8 @@ int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32
  *            formats: q8_1 buffer.
  *   y_dev:   MX formats: bf16 [ntok][top_k][N] (fp16 with QMV_FLAG_X_F16); CB
  *            formats: fp32 [ntok][top_k][N].
- * Errors: QMV_EINVAL (ntok not in 1..4, top_k not in 1..8), QMV_ESHAPE,
+ * Errors: QMV_EINVAL (ntok not in 1..16, top_k not in 1..8, ntok * top_k >
+ * QMV_MAX_SLOTS), QMV_ESHAPE,
  * QMV_EALIGN, QMV_ECUDA.
  */
 int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,

@@ -1,0 +1,115 @@
+"""GPU parity of verify-batch calls: dense matvecs of 5 to 16 tokens (one
+weight stream per group of 4 tokens, groups dealt side by side) and gathers /
+layers with up to 32 routed (token, slot) pairs -- the speculative-decoding
+verify batch that "perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA ..."
+("Depends on": the batched ROCmFPX MMQ) runs beside the single-token path.
+Same bar as the decode tests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import qmv_inputs as qi
+
+pytestmark = pytest.mark.gpu
+
+qmv = pytest.importorskip("bit_quantized_moe_gb300")
+from qmv_testutil import (DEV, MX_SCALES, Matrices, assert_close, bf16_to_np,  # noqa: E402
+                          quantize_on_gpu, status_clean, to_dev)
+from test_gpu_parity import LUTS, GateUp, _combine_tol, _layer_expected  # noqa: E402
+
+
+@pytest.mark.parametrize("fmt,N,K", [("mxfp4", 2880, 2880), ("mxfp4", 516, 4096), ("mxfp8", 2880, 2880),
+                                     ("cb4", 2048, 7168), ("cb4", 7168, 7168), ("cb3", 1032, 2048)])
+@pytest.mark.parametrize("ntok", [5, 8, 13, 16])
+def test_verify_dense(fmt, N, K, ntok):
+    lo, hi = MX_SCALES.get(fmt, (120, 130))
+    m = Matrices(fmt, N, K, 1, [0], seed=N + K + ntok, lut=LUTS.get(fmt), scale_lo=lo, scale_hi=hi)
+    g = qi.rng(ntok * 31 + N)
+    if fmt in ("mxfp4", "mxfp8"):
+        x = qi.normal_bf16_bits(g, (ntok, K))
+        y = torch.empty(ntok, N, dtype=torch.bfloat16, device=DEV)
+        qmv.qmv_dense(m.desc, m.w, to_dev(x), ntok, y)
+        ref = oracle.mx_matvec(fmt, m.codes[0], m.scales[0], x)
+        absum = oracle.mx_abs_products(fmt, m.codes[0], m.scales[0], x)
+        assert_close(bf16_to_np(y), ref, absum, True, f"{fmt} dense {N}x{K} ntok={ntok}")
+    else:
+        xq, q, d = quantize_on_gpu(qi.normal_f32(g, (ntok, K)))
+        y = torch.empty(ntok, N, dtype=torch.float32, device=DEV)
+        qmv.qmv_dense(m.desc, m.w, xq, ntok, y)
+        grp = qi.FORMAT_GROUP[fmt]
+        ref = oracle.cb_matvec(m.codes[0], m.scales[0], m.lut, grp, q, d)
+        absum = oracle.cb_abs_products(m.codes[0], m.scales[0], m.lut, grp, q, d)
+        assert_close(y.cpu().numpy(), ref, absum, False, f"{fmt} dense {N}x{K} ntok={ntok}")
+    assert status_clean()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "cb3"])
+@pytest.mark.parametrize("ntok,top_k,per_slot", [(8, 4, True), (8, 4, False), (16, 2, True), (6, 5, False)])
+def test_verify_gather(fmt, ntok, top_k, per_slot):
+    E, N, K = 32, (2880 if fmt == "mxfp4" else 7168), (2880 if fmt == "mxfp4" else 2048)
+    g = qi.rng(ntok * 100 + top_k + per_slot)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    ids[1, 0] = ids[0, 0]
+    ids[-1, -1] = -1
+    m = Matrices(fmt, N, K, E, ids.reshape(-1), seed=ntok + top_k, lut=LUTS.get(fmt))
+    nvec = ntok * top_k if per_slot else ntok
+    if fmt == "mxfp4":
+        x = qi.normal_bf16_bits(g, (nvec, K))
+        y = torch.full((ntok, top_k, N), 5.0, dtype=torch.bfloat16, device=DEV)
+        qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), int(per_slot), to_dev(ids), ntok, top_k, y)
+        got = bf16_to_np(y)
+    else:
+        xq, q, d = quantize_on_gpu(qi.normal_f32(g, (nvec, K)))
+        y = torch.full((ntok, top_k, N), 5.0, dtype=torch.float32, device=DEV)
+        qmv.qmv_moe_gather(m.desc, m.w, xq, int(per_slot), to_dev(ids), ntok, top_k, y)
+        got = y.cpu().numpy().astype(np.float64)
+    for t in range(ntok):
+        for j in range(top_k):
+            e = int(ids[t, j])
+            if e < 0:
+                assert np.all(got[t, j] == 0)
+                continue
+            v = t * top_k + j if per_slot else t
+            if fmt == "mxfp4":
+                ref = oracle.mxfp4_matvec(m.codes[e], m.scales[e], x[v:v + 1])[0]
+                absum = oracle.mxfp4_abs_products(m.codes[e], m.scales[e], x[v:v + 1])[0]
+            else:
+                ref = oracle.cb_matvec(m.codes[e], m.scales[e], m.lut, 16, q[v:v + 1], d[v:v + 1])[0]
+                absum = oracle.cb_abs_products(m.codes[e], m.scales[e], m.lut, 16, q[v:v + 1], d[v:v + 1])[0]
+            assert_close(got[t, j], ref, absum, fmt == "mxfp4", f"slot ({t},{j}) expert {e}")
+    assert status_clean()
+
+
+@pytest.mark.parametrize("pair", [("mxfp4", "mxfp4", 2880, 2880, 32), ("cb2", "cb3", 2048, 7168, 64)],
+                         ids=lambda p: f"{p[0]}-{p[1]}")
+def test_verify_layer_combine(pair):
+    """An 8-token verify batch through the layer (32 routed slots) and the
+    router-weighted combine, against the oracle chain."""
+    fmt_gu, fmt_dn, N, K, E = pair
+    ntok, top_k = 8, 4
+    g = qi.rng(880)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    ids[2, 1] = ids[0, 0]
+    ids[5, 3] = E + 4
+    gu = GateUp(fmt_gu, N, K, E, ids.reshape(-1), seed=881, lut=LUTS.get(fmt_gu))
+    down = Matrices(fmt_dn, K, N, E, ids.reshape(-1), seed=882, lut=LUTS.get(fmt_dn))
+    w = qi.router_weights(g, ntok, top_k)
+    if fmt_gu == "mxfp4":
+        x = qi.normal_bf16_bits(g, (ntok, K))
+        xin, q, d, dt = to_dev(x), None, None, torch.bfloat16
+    else:
+        x = None
+        xin, q, d = quantize_on_gpu(qi.normal_f32(g, (ntok, K)))
+        dt = torch.float32
+    ws = torch.empty(qmv.qmv_moe_layer_combine_workspace_bytes(gu.desc, down.desc, ntok, top_k), dtype=torch.uint8,
+                     device=DEV)
+    y = torch.full((ntok, K), 7.0, dtype=dt, device=DEV)
+    qmv.qmv_moe_layer_combine(gu.desc, gu.w, down.desc, down.w, xin, to_dev(ids), to_dev(w), ntok, top_k, ws, y)
+    slots, slot_tol = _layer_expected(gu, down, ids, x=x, q=q, d=d)
+    want = oracle.moe_combine(slots, w, ids, E)
+    tol = _combine_tol(slots, w, ids, E, want, dt == torch.bfloat16, slot_tol)
+    got = bf16_to_np(y) if dt == torch.bfloat16 else y.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want)
+    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined outputs outside tolerance"
+    assert status_clean()

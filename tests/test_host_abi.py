@@ -130,7 +130,7 @@ FAKE = 1 << 40          # 16-byte aligned address that is never dereferenced
     ("K not multiple of 32", qmv.QMV_ESHAPE),
     ("N zero", qmv.QMV_ESHAPE),
     ("bad format", qmv.QMV_EINVAL),
-    ("ntok 5", qmv.QMV_EINVAL),
+    ("ntok 17", qmv.QMV_EINVAL),
     ("ntok 0", qmv.QMV_EINVAL),
     ("misaligned x", qmv.QMV_EALIGN),
     ("null y", qmv.QMV_EINVAL),
@@ -145,8 +145,8 @@ def test_dense_argument_errors(case, code):
         d.N = 0
     elif case == "bad format":
         d.fmt = 9
-    elif case == "ntok 5":
-        ntok = 5
+    elif case == "ntok 17":
+        ntok = 17
     elif case == "ntok 0":
         ntok = 0
     elif case == "misaligned x":
@@ -168,6 +168,22 @@ def test_gather_argument_errors(top_k, ids, code):
     with pytest.raises(qmv.QmvError) as ei:
         qmv.qmv_moe_gather(d, FAKE, FAKE, 0, ids, 1, top_k, FAKE, stream=0)
     assert ei.value.code == code
+
+
+def test_routed_slot_limit():
+    """A gather routes at most QMV_MAX_SLOTS (token, slot) pairs; 16 tokens
+    is the dense limit."""
+    assert qmv.MAX_SLOTS == 32 and qmv.MAX_NTOK == 16
+    d = qmv.wdesc("mxfp4", 64, 64, 8)
+    G = qmv.lib.qmv_moe_gather_ex
+    B = qmv.ctypes.byref
+    assert G(B(d), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) == qmv.QMV_EINVAL      # 64 slots
+    assert G(B(d), FAKE, FAKE, 1, FAKE, 16, 4, FAKE, 0, 0) == qmv.QMV_EINVAL     # 64 slots
+    assert G(B(d), FAKE, FAKE, 0, FAKE, 17, 1, FAKE, 0, 0) == qmv.QMV_EINVAL     # 17 tokens
+    gu = qmv.wdesc("mxfp4", 64, 64, 8)
+    assert qmv.qmv_moe_layer_workspace_bytes(gu, 8, 4) == (32 * 64 * 2 + 255) // 256 * 256
+    assert qmv.qmv_moe_layer_workspace_bytes(gu, 16, 4) == 0
+    assert qmv.lib.qmv_quantize_act_q8(FAKE, 33, 64, FAKE, 1 << 20, 0) == qmv.QMV_EINVAL
 
 
 def test_debug_sums_size_error():
