@@ -642,16 +642,19 @@ def run_configs(args):
         del W4
 
     # --- verify batches (f3): dense 8 and 16 tokens (one weight stream per 4 tokens, side by side)
-    for fmt, (Nv, Kv) in (("mxfp4", (2880, 2880)), ("cb4", (7168, 7168))):
+    for fmt, (Nv, Kv) in (("mxfp4", (2880, 2880)), ("mxfp8", (2880, 2880)), ("mxfp4", (7168, 7168)),
+                          ("cb4", (7168, 7168))):
         dv = qmv.wdesc(fmt, Nv, Kv, 1, luts(fmt))
         bv = qmv.qmv_packed_bytes(dv)
-        algv = Nv * Kv // 2 + Nv * (Kv // 32)
+        algv = Nv * Kv * qi.FORMAT_BITS[fmt] // 8 + Nv * (Kv // 32)
         nv_ = -(-4 * L2_BYTES // bv)
         cv, sv = canon(fmt, 2, Nv, Kv)
+        if fmt == "mxfp8":
+            sv = sv - 8
         Wv = _replicated(qmv, torch, dev, qmv.wdesc(fmt, Nv, Kv, 2, luts(fmt)),
                          lambda: qmv.qmv_pack_weights(qmv.wdesc(fmt, Nv, Kv, 2, luts(fmt)), cv, sv), nv_, bv)
         for ntok in (8, 16):
-            if fmt == "mxfp4":
+            if fmt in ("mxfp4", "mxfp8"):
                 xv = torch.from_numpy(qi.normal_bf16_bits(g, (ntok, Kv)).view(np.int16)).to(dev).view(torch.bfloat16)
                 yv = torch.empty(nv_, ntok, Nv, dtype=torch.bfloat16, device=dev)
             else:

@@ -174,6 +174,7 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   a.stream = stream;
   const DevInfo* di = dev_info();
   if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
+  if (verify_supported(a)) return QMV_OK;   // tensor-core path, fixed shared memory
   const size_t smem = matvec_smem_bytes(a);
   if (smem == 0 || smem > di->smem_optin)
     return fail(QMV_ESHAPE, "%s: %d activation vectors of K=%d do not fit in shared memory", name, a.nvec,
@@ -189,7 +190,7 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
                                 glu, a);
   if (rc) return rc;
   g_launch_stage = "";
-  cudaError_t e = launch_for(a);
+  cudaError_t e = verify_supported(a) ? launch_verify(a) : launch_for(a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(QMV_ECUDA, "%s: %s failed: %s (%s)", name, g_launch_stage, cudaGetErrorName(e),
@@ -510,8 +511,8 @@ int qmv_debug_dequant(const qmv_wdesc* desc, const void* w, int32_t expert, floa
 int qmv_device_status(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(QMV_EINVAL, "qmv_device_status: NULL pointer");
   uint32_t v = 0;
-  const uint32_t parts[6] = {status_mxfp4(clear), status_cb2(clear), status_cb3(clear),
-                             status_cb4(clear),   status_mxfp8(clear), status_act(clear)};
+  const uint32_t parts[7] = {status_mxfp4(clear), status_cb2(clear),   status_cb3(clear),   status_cb4(clear),
+                             status_mxfp8(clear), status_verify(clear), status_act(clear)};
   for (uint32_t p : parts) {
     if (p == 0xffffffffu) return cuda_fail(cudaGetLastError(), "qmv_device_status");
     v |= p;

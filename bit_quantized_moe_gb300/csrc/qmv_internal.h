@@ -42,6 +42,11 @@ cudaError_t launch_matvec_cb3(const MatvecArgs& a);
 cudaError_t launch_matvec_cb4(const MatvecArgs& a);
 cudaError_t launch_matvec_mxfp8(const MatvecArgs& a);
 
+// Dense verify batches of the MX formats (5..16 bf16 tokens) on the tensor
+// cores: whether a call takes that path, and its launcher.
+bool verify_supported(const MatvecArgs& a);
+cudaError_t launch_verify(const MatvecArgs& a);
+
 cudaError_t launch_quantize_q8(const float* x, int nvec, int K, void* xq, cudaStream_t s);
 cudaError_t launch_swiglu_bf16(const void* g, const void* u, void* h, int64_t n, cudaStream_t s);
 // Output types of the combine.
@@ -59,6 +64,7 @@ uint32_t status_cb2(int clear);
 uint32_t status_cb3(int clear);
 uint32_t status_cb4(int clear);
 uint32_t status_mxfp8(int clear);
+uint32_t status_verify(int clear);
 
 // Sets the calling thread's qmv_last_error() message and returns `code`.
 int record_error(int code, const char* fmt, ...);

@@ -113,3 +113,54 @@ def test_verify_layer_combine(pair):
     err = np.abs(got - want)
     assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined outputs outside tolerance"
     assert status_clean()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("N,K", [(1, 32), (17, 96), (130, 1056), (1032, 2048), (4099, 1024), (300, 7168)])
+@pytest.mark.parametrize("ntok", [5, 16])
+def test_verify_tensor_core_shapes(fmt, N, K, ntok):
+    """The tensor-core verify path over ragged row blocks (N not a multiple of
+    128), ragged K chunks, K ranges split across cluster ranks, and 5 tokens
+    (11 padding columns of the MMA)."""
+    lo, hi = MX_SCALES[fmt]
+    m = Matrices(fmt, N, K, 1, [0], seed=3 * N + K, scale_lo=lo, scale_hi=hi)
+    x = qi.normal_bf16_bits(qi.rng(N + K + ntok), (ntok, K))
+    y = torch.full((ntok, N), 9.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_dense(m.desc, m.w, to_dev(x), ntok, y)
+    ref = oracle.mx_matvec(fmt, m.codes[0], m.scales[0], x)
+    absum = oracle.mx_abs_products(fmt, m.codes[0], m.scales[0], x)
+    assert_close(bf16_to_np(y), ref, absum, True, f"{fmt} verify {N}x{K} ntok={ntok}")
+    assert status_clean()
+
+
+def test_verify_tensor_core_deterministic_and_chained():
+    """Two launches give identical bits; a launch on a side stream after
+    another kernel (programmatic dependent launch) and inside a CUDA graph
+    gives the same bits as the eager call."""
+    N, K, T = 2880, 2880, 12
+    m = Matrices("mxfp4", N, K, 1, [0], seed=77)
+    x = to_dev(qi.normal_bf16_bits(qi.rng(78), (T, K)))
+    y1 = torch.empty(T, N, dtype=torch.bfloat16, device=DEV)
+    y2 = torch.empty_like(y1)
+    qmv.qmv_dense(m.desc, m.w, x, T, y1)
+    qmv.qmv_dense(m.desc, m.w, x, T, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    x2 = torch.empty_like(x)
+    y3 = torch.empty_like(y1)
+    with torch.cuda.stream(s):
+        x2.copy_(x)                      # the verify launch depends on this kernel's output
+        qmv.qmv_dense(m.desc, m.w, x2, T, y3, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    y4 = torch.zeros_like(y1)
+    with torch.cuda.graph(g, stream=s):
+        qmv.qmv_dense(m.desc, m.w, x2, T, y4, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y4.view(torch.int16))
+    assert status_clean()
