@@ -17,13 +17,15 @@
 // layout) and one of `split` K ranges; the `split` CTAs of a row block form a
 // thread-block cluster and add their partial sums through distributed shared
 // memory in rank order (deterministic), each rank storing a share of the
-// outputs. Per CTA: 8 warps; thread (r, h) decodes row r for the h-th 32-group
-// of every 64-column step, with its weight loads issued kWindow steps ahead;
-// three A buffers let the decode of one step overlap the MMAs of the last.
+// outputs. Per CTA: 8 decoding warps -- thread (r, h) decodes row r for the
+// h-th 32-group of every 64-column step, its weight loads issued a window of
+// steps ahead -- and one warp that issues the MMAs. Three A buffers, each
+// with a "full" barrier (one arrival per decoding warp) and an "empty" one
+// (tcgen05.commit), let the warps decode ahead of the tensor core.
 //
 // Operand layouts (no swizzle, K-major "canonical" core matrices of 8 rows x
-// 16 bytes): A step buffer, core matrix (row group g, k group kk) at
-// kk * 2048 + g * 128; B (activations, tokens padded to 16 with zeros), core
+// 16 bytes): A step buffer (128 rows x 128 columns), core matrix (row group
+// g, k group kk) at kk * 2048 + g * 128; B (activations, tokens padded to 16 with zeros), core
 // matrix (token group g, k group kk) at kk * 256 + g * 128. Descriptor
 // leading byte offset = the K-direction stride, stride byte offset = the
 // row-direction stride.
@@ -46,13 +48,20 @@ namespace {
 
 constexpr int kVRows = 128;      // rows per CTA (MMA M)
 constexpr int kVTok = 16;        // MMA N: tokens, padded
-constexpr int kVThreads = 256;   // two threads per row
-constexpr int kVStepK = 64;      // columns per step (one A buffer)
+constexpr int kDecoders = 256;   // decoding threads: two per row
+constexpr int kVThreads = kDecoders + 32;   // plus one warp that issues the MMAs
+constexpr int kVStepK = 64;      // columns per step (one A buffer): 2 groups of 32
 constexpr int kVBufs = 3;        // A buffers
-constexpr int kWindow = 4;       // steps of weight loads in flight per thread
+// Steps of weight loads in flight per thread: 128 bytes (8 MXFP4 or 4
+// MXFP8 lane blocks), so two CTAs keep ~64 KB per SM in flight.
+template <int FMT>
+struct Window {
+  static constexpr int value = 128 / lane_code_bytes(FMT);
+};
 constexpr uint32_t kABytes = kVRows * kVStepK * 2;   // 16 KB
+constexpr uint32_t kALbo = kVRows / 8 * 128;          // A: k-group stride (16 row groups of 128 B)
 constexpr int kVMaxSplit = 8;    // cluster size limit (portable)
-constexpr int kVMaxSteps = 48;   // activation operand <= 96 KB
+constexpr int kVMaxSteps = 24;   // activation operand <= 48 KB (two CTAs per SM)
 
 struct VParams {
   const uint8_t* w;
@@ -65,6 +74,7 @@ struct VParams {
   int groups;   // K / 32
   int split;    // CTAs (cluster ranks) per row block
   int steps;    // steps of the longest K range
+  int prefetch; // weights were not written by the preceding kernel: load them before griddepcontrol.wait
 };
 
 __device__ __forceinline__ uint64_t mma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -89,6 +99,10 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -129,7 +143,8 @@ __device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t h2, float s) {
 }
 
 // 32 codes of a lane block -> 32 exact bf16 values (code value x 2^(e-127)),
-// written as four 16-byte core-matrix rows (k groups kk0 .. kk0 + 3).
+// written as four 16-byte core-matrix rows (k groups kk0 .. kk0 + 3, kALbo
+// bytes apart).
 template <int FMT>
 __device__ __forceinline__ void decode_store(const Block<FMT>& b, uint8_t* a_row, int kk0) {
   const float s = e8m0_to_f32(b.e);
@@ -153,15 +168,16 @@ __device__ __forceinline__ void decode_store(const Block<FMT>& b, uint8_t* a_row
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * 2048) =
+    *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
         make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
   }
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kVThreads) verify_kernel(const __grid_constant__ VParams p) {
+__global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_constant__ VParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kVBufs + 1];
+  __shared__ __align__(8) uint64_t bars[kVBufs + 1];   // empty (MMAs done) x kVBufs, final
+  __shared__ __align__(8) uint64_t full[kVBufs];        // A buffer written by all decoding warps
   __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)(blockIdx.x % (unsigned)p.split);
@@ -179,75 +195,102 @@ __global__ void __launch_bounds__(kVThreads) verify_kernel(const __grid_constant
   }
   if (tid == 0) {
     for (int i = 0; i <= kVBufs; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    for (int i = 0; i < kVBufs; ++i) mbar_init(smem_addr(&full[i]), kDecoders / 32);
     fence_mbar_init();
   }
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // Activation operand: tokens t < T of columns [32 g0, 32 g0 + 64 steps),
-  // zero beyond the CTA's range and for padding tokens.
-  {
-    const int kk_n = steps * (kVStepK / 8);
-    const int k_end = g1 * 32;
-    for (int u = tid; u < kk_n * kVTok; u += kVThreads) {
-      const int t = u % kVTok, kk = u / kVTok;
-      const int k = g0 * 32 + kk * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < p.T && k < k_end) v = *reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + k);
-      *reinterpret_cast<uint4*>(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16) = v;
-    }
-  }
-
   // Weight stream: thread (r, h) -> row r of the block, group 2 * step + h.
-  const int r = tid & (kVRows - 1), h = tid >> 7;
+  // The first window of loads goes out first (before griddepcontrol.wait
+  // when the caller guarantees the weights are not the preceding kernel's
+  // output), then the activations, whose loads are all issued before any of
+  // them is stored.
+  const bool decoder = tid < kDecoders;
+  const int r = tid & (kVRows - 1), h = (tid >> 7) & 1;
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
-  const bool row_ok = rt < p.row_tiles;
+  const bool row_ok = decoder && rt < p.row_tiles;
   uint8_t* a_row = abuf + (r >> 3) * 128 + (r & 7) * 16;
+  constexpr int kWindow = Window<FMT>::value;
   Block<FMT> win[kWindow];
+  if (!p.prefetch) pdl_wait();
 #pragma unroll
   for (int u = 0; u < kWindow; ++u) {
     const int g = g0 + 2 * u + h;
     load_block<FMT>(p, rt, r8, g, row_ok && u < steps && g < g1, win[u]);
   }
+  if (p.prefetch) pdl_wait();
+  pdl_launch_dependents();
 
+  // Activation operand: tokens t < T of columns [32 g0, 32 g0 + 64 steps),
+  // zero beyond the CTA's range and for padding tokens.
+  {
+    constexpr int kU = 4;
+    const int kk_n = steps * (kVStepK / 8);
+    const int k_end = g1 * 32;
+    const int n_units = decoder ? kk_n * kVTok : 0;
+    for (int u0 = tid; u0 < n_units; u0 += kU * kDecoders) {
+      uint4 v[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int u = u0 + j * kDecoders;
+        const int t = u % kVTok, kk = u / kVTok;
+        const int k = g0 * 32 + kk * 8;
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (u < n_units && t < p.T && k < k_end) v[j] = *reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + k);
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int u = u0 + j * kDecoders;
+        const int t = u % kVTok, kk = u / kVTok;
+        if (u < n_units) *reinterpret_cast<uint4*>(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16) = v[j];
+      }
+    }
+  }
+
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   bool ok = true;
 
-  for (int s0 = 0; s0 < steps; s0 += kWindow) {
+  if (decoder) {
+    for (int s0 = 0; s0 < steps; s0 += kWindow) {
 #pragma unroll
-    for (int u = 0; u < kWindow; ++u) {
-      const int st = s0 + u;
-      if (st < steps) {
-        const int b = st % kVBufs;
-        if (st >= kVBufs) {
-          // the MMAs that read this buffer kVBufs steps ago are done
-          ok &= mbar_wait_bounded(smem_addr(&bars[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
-        }
-        decode_store<FMT>(win[u], a_row + (size_t)b * kABytes, 4 * h);
-        const int gn = g0 + 2 * (st + kWindow) + h;
-        load_block<FMT>(p, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-          tc_fence_after();
-          const uint32_t a0 = smem_addr(abuf + (size_t)b * kABytes);
-          const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
-#pragma unroll
-          for (int j = 0; j < kVStepK / 16; ++j) {
-            mma_bf16(tmem, mma_desc(a0 + j * 2 * 2048, 2048, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                     (st > 0 || j > 0) ? 1u : 0u);
+      for (int u = 0; u < kWindow; ++u) {
+        const int st = s0 + u;
+        if (st < steps) {
+          const int b = st % kVBufs;
+          if (st >= kVBufs) {
+            // the MMAs that read this buffer kVBufs steps ago are done
+            ok &= mbar_wait_bounded(smem_addr(&bars[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
           }
-          mma_commit(smem_addr(&bars[b]));
+          decode_store<FMT>(win[u], a_row + (size_t)b * kABytes, 4 * h);
+          const int gn = g0 + 2 * (st + kWindow) + h;
+          load_block<FMT>(p, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&full[b]));
         }
       }
     }
+  } else if (lane == 0) {
+    // MMA issue: step st once every decoding warp has written its A buffer.
+    for (int st = 0; st < steps; ++st) {
+      const int b = st % kVBufs;
+      ok &= mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
+      tc_fence_after();
+      const uint32_t a0 = smem_addr(abuf + (size_t)b * kABytes);
+      const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
+#pragma unroll
+      for (int j = 0; j < kVStepK / 16; ++j) {
+        mma_bf16(tmem, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
+                 (st > 0 || j > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_addr(&bars[b]));
+    }
+    mma_commit(smem_addr(&bars[kVBufs]));
   }
-  if (tid == 0) mma_commit(smem_addr(&bars[kVBufs]));
+  __syncwarp();
   ok &= mbar_wait_bounded(smem_addr(&bars[kVBufs]), 0u, kWaitLimitNs);
   tc_fence_after();
   if (!__all_sync(0xffffffffu, ok) && lane == 0) set_status(kStatusWaitTile);
@@ -271,12 +314,16 @@ __global__ void __launch_bounds__(kVThreads) verify_kernel(const __grid_constant
   // K ranges meet in rank order; rank q stores outputs q, q + split, ...
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  for (int i = rank * kVThreads + tid; i < kVRows * p.T; i += p.split * kVThreads) {
+  for (int i = rank * kVThreads + tid; i < kVRows * p.T; i += p.split * kVThreads) {  // all 9 warps
     const int t = i / kVRows, rr = i % kVRows;
     const int orow = rb * kVRows + rr;
     if (orow >= p.N) continue;
+    float v[kVMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kVMaxSplit; ++q) v[q] = (q < p.split) ? cluster.map_shared_rank(part, q)[t * kVRows + rr] : 0.f;
     float acc = 0.f;
-    for (int q = 0; q < p.split; ++q) acc += cluster.map_shared_rank(part, q)[t * kVRows + rr];
+#pragma unroll
+    for (int q = 0; q < kVMaxSplit; ++q) acc += v[q];   // rank order; absent ranks add +0
     p.y[(size_t)t * p.N + orow] = __float2bfloat16_rn(acc);
   }
   cluster.sync();
@@ -316,13 +363,15 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.rowtile = g.rowtile;
   p.groups = a.K / 32;
   const int row_blocks = (a.N + kVRows - 1) / kVRows;
-  int split = (2 * device_sm_count() + row_blocks - 1) / row_blocks;
+  // one wave of at most two CTAs per SM
+  int split = (2 * device_sm_count()) / row_blocks;
   if (split > kVMaxSplit) split = kVMaxSplit;
   if (split > p.groups / 2) split = p.groups / 2;
   if (split < 1) split = 1;
   while ((p.groups + split - 1) / split > 2 * kVMaxSteps && split < kVMaxSplit) ++split;
   p.split = split;
   p.steps = ((p.groups + split - 1) / split + 1) / 2;
+  p.prefetch = a.prefetch ? 1 : 0;
   const size_t smem = verify_smem_bytes(p.steps);
   static size_t configured[64] = {};
   int dev = 0;
