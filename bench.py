@@ -202,16 +202,21 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
+# Sources that compile into the step's kernel (matvec_kernel<MXFP4, 1, false>).
+STEP_KERNEL_SOURCES = ("qmv_device.cuh", "qmv_internal.h", "qmv_layout.h", "qmv_matvec.cuh",
+                       "qmv_matvec_mxfp4.cu")
+
+
 def kernel_source_digest() -> str:
-    """sha256 over the code (comments stripped) of the library's CUDA sources
-    and headers: the kernel identity the committed ncu summary refers to."""
+    """sha256 over the code (comments stripped) of the sources that compile
+    into the step's kernel: the kernel identity the committed ncu summary
+    refers to."""
     import hashlib
     d = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_quantized_moe_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
-                d.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
+    for f in STEP_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            d.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return d.hexdigest()
 
 
