@@ -17,9 +17,10 @@
 // layout) and one of `split` K ranges; the `split` CTAs of a row block form a
 // thread-block cluster and add their partial sums through distributed shared
 // memory in rank order (deterministic), each rank storing a share of the
-// outputs. Per CTA: 8 decoding warps -- thread (r, h) decodes row r for the
-// h-th 32-group of every 64-column step, its weight loads issued a window of
-// steps ahead -- and one warp that issues the MMAs. Three A buffers, each
+// outputs. Per CTA: 8 decoding warps -- a warp decodes 16 rows (two row
+// tiles) of every 64-column step, a lane taking one row and one of the two
+// 32-groups, its weight loads issued a window of steps ahead -- and one warp
+// that issues the MMAs. Three A buffers, each
 // with a "full" barrier (one arrival per decoding warp) and an "empty" one
 // (tcgen05.commit), let the warps decode ahead of the tensor core.
 //
@@ -198,13 +199,17 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     for (int i = 0; i < kVBufs; ++i) mbar_init(smem_addr(&full[i]), kDecoders / 32);
     fence_mbar_init();
   }
-  // Weight stream: thread (r, h) -> row r of the block, group 2 * step + h.
+  // Weight stream: decoding warp w takes row tiles 2w and 2w + 1 of the
+  // block; lane (i, r8, h) takes row r8 of tile 2w + i and group
+  // 2 * step + h, so one warp load covers 16 rows x 32 contiguous bytes
+  // (16 full sectors).
   // The first window of loads goes out first (before griddepcontrol.wait
   // when the caller guarantees the weights are not the preceding kernel's
   // output), then the activations, whose loads are all issued before any of
   // them is stored.
   const bool decoder = tid < kDecoders;
-  const int r = tid & (kVRows - 1), h = (tid >> 7) & 1;
+  const int h = lane & 1;
+  const int r = (warp & 7) * 16 + (lane >> 1);   // row of the block: tile 2w + (lane >> 4), row (lane >> 1) & 7
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
