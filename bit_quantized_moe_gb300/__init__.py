@@ -35,7 +35,8 @@ QMV_NOALLOC_SCRATCH_BYTES = 1 << 20
 MXFP4, CB2, CB3, CB4, MXFP8 = 0, 1, 2, 3, 4
 FORMATS = {"mxfp4": MXFP4, "cb2": CB2, "cb3": CB3, "cb4": CB4, "mxfp8": MXFP8}
 MAX_NTOK = 16
-MAX_SLOTS = 32
+MAX_SLOTS = 128
+MAX_LAYER_SLOTS = 32
 MAX_TOPK = 8
 
 # Every symbol include/qmv.h declares.

@@ -172,9 +172,13 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   a.glu = glu;
   a.out_n = desc_in->N;
   a.stream = stream;
+  const bool verify = verify_supported(a);
+  if (gather && ntok * top_k > QMV_MAX_LAYER_SLOTS && !verify)
+    return fail(QMV_EINVAL, "%s: more than %d routed slots need an MX format with bf16 activations (the "
+                "sorted tensor-core gather)", name, QMV_MAX_LAYER_SLOTS);
   const DevInfo* di = dev_info();
   if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
-  if (verify_supported(a)) return QMV_OK;   // tensor-core path, fixed shared memory
+  if (verify) return QMV_OK;   // tensor-core path, fixed shared memory
   const size_t smem = matvec_smem_bytes(a);
   if (smem == 0 || smem > di->smem_optin)
     return fail(QMV_ESHAPE, "%s: %d activation vectors of K=%d do not fit in shared memory", name, a.nvec,
@@ -385,7 +389,7 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, 
 // Workspace of qmv_moe_layer: h (MXFP4: bf16; codebooks: fp32).
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gu, int32_t ntok, int32_t top_k) {
   if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK ||
-      ntok * top_k > QMV_MAX_SLOTS)
+      ntok * top_k > QMV_MAX_LAYER_SLOTS)
     return 0;
   const size_t slots = (size_t)ntok * top_k;
   if (fmt_is_mx(gu->fmt)) return (slots * gu->N * 2 + 255) / 256 * 256;
@@ -407,7 +411,7 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   if (down->K != gu->N) return fail(QMV_ESHAPE, "%s: down K=%d must equal gate/up N=%d", name, down->K, gu->N);
   if (down->n_experts != gu->n_experts)
     return fail(QMV_EINVAL, "%s: gate/up and down expert counts differ (%d, %d)", name, gu->n_experts, down->n_experts);
-  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK || ntok * top_k > QMV_MAX_SLOTS)
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK || ntok * top_k > QMV_MAX_LAYER_SLOTS)
     return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
   const size_t need = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
   if (ws_bytes < need) return fail(QMV_ESIZE, "%s: workspace %zu bytes < %zu", name, ws_bytes, need);

@@ -62,6 +62,7 @@ struct Window {
 constexpr uint32_t kABytes = kVRows * kVStepK * 2;   // 16 KB
 constexpr uint32_t kALbo = kVRows / 8 * 128;          // A: k-group stride (16 row groups of 128 B)
 constexpr int kVMaxSplit = 8;    // cluster size limit (portable)
+constexpr int kVMaxSlots = 128;  // routed slots of a sorted gather
 constexpr int kVMaxSteps = 24;   // activation operand <= 48 KB (two CTAs per SM)
 
 struct VParams {
@@ -76,6 +77,10 @@ struct VParams {
   int split;    // CTAs (cluster ranks) per row block
   int steps;    // steps of the longest K range
   int prefetch; // weights were not written by the preceding kernel: load them before griddepcontrol.wait
+  // sorted gather (ids != null): slots grouped by expert, <= 16 slots per work item
+  const int32_t* ids;
+  int top_k, nslots, per_slot, n_experts;
+  uint64_t expert_stride;
 };
 
 __device__ __forceinline__ uint64_t mma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -118,7 +123,8 @@ struct Block {
 };
 
 template <int FMT>
-__device__ __forceinline__ void load_block(const VParams& p, int rt, int r8, int g, bool valid, Block<FMT>& b) {
+__device__ __forceinline__ void load_block(const VParams& p, const uint8_t* w, int rt, int r8, int g, bool valid,
+                                           Block<FMT>& b) {
   if (!valid) {
 #pragma unroll
     for (int i = 0; i < Block<FMT>::kWords; ++i) b.c[i] = 0;
@@ -127,7 +133,7 @@ __device__ __forceinline__ void load_block(const VParams& p, int rt, int r8, int
   }
   const int c = g >> 5, l = g & 31;
   const int L = (c == p.chunks - 1) ? p.last_lanes : 32;
-  const uint8_t* tile = p.w + (uint64_t)rt * p.rowtile + (uint64_t)c * p.full_tile;
+  const uint8_t* tile = w + (uint64_t)rt * p.rowtile + (uint64_t)c * p.full_tile;
   const uint4* src = reinterpret_cast<const uint4*>(tile + (size_t)(r8 * L + l) * lane_code_bytes(FMT));
 #pragma unroll
   for (int q = 0; q < Block<FMT>::kWords / 4; ++q) {
@@ -186,6 +192,67 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   const int g0 = (int)((long)rank * p.groups / p.split);
   const int g1 = (int)((long)(rank + 1) * p.groups / p.split);
   const int steps = (g1 - g0 + 1) / 2;
+
+  // Sorted gather: work item blockIdx.y is the (expert, group of <= 16 of
+  // its slots) pair of that index, experts in order of their first slot and
+  // slots in slot order. Each CTA derives it from the ids in shared memory:
+  // thread s finds its expert's slot count and its rank among them; the
+  // first slot of each expert counts the work items of the experts before
+  // it. An index past the last item leaves the CTA idle (every CTA of a
+  // cluster shares blockIdx.y, so a cluster exits as a whole, before it
+  // allocates tensor memory). Slots with an invalid id get zero rows.
+  __shared__ int s_ids[kVMaxSlots];
+  __shared__ int s_cnt[kVMaxSlots];
+  __shared__ int s_slot[kVTok];
+  __shared__ int s_item[3];   // expert, first rank, tokens
+  int T = p.T;
+  const uint8_t* w = p.w;
+  if (p.ids != nullptr) {
+    if (!p.prefetch) pdl_wait();
+    if (tid == 0) s_item[0] = -1;
+    int e = -1;
+    if (tid < p.nslots) {
+      e = p.ids[tid];
+      if (e < 0 || e >= p.n_experts) e = -1;
+      s_ids[tid] = e;
+    }
+    __syncthreads();
+    int cnt = 0, rk = 0;
+    bool first = false;
+    if (tid < p.nslots && e >= 0) {
+      for (int q = 0; q < p.nslots; ++q) {
+        const int eq = s_ids[q];
+        cnt += (eq == e);
+        rk += (eq == e && q < tid);
+      }
+      first = (rk == 0);
+    }
+    if (tid < p.nslots) s_cnt[tid] = first ? cnt : 0;
+    __syncthreads();
+    if (first) {
+      int before = 0;
+      for (int q = 0; q < tid; ++q) before += (s_cnt[q] + kVTok - 1) / kVTok;
+      const int mine = (cnt + kVTok - 1) / kVTok;
+      const int y = (int)blockIdx.y;
+      if (y >= before && y < before + mine) {
+        s_item[0] = e;
+        s_item[1] = (y - before) * kVTok;
+        s_item[2] = min(kVTok, cnt - (y - before) * kVTok);
+      }
+    }
+    __syncthreads();
+    if (s_item[0] >= 0 && e == s_item[0] && rk >= s_item[1] && rk < s_item[1] + s_item[2]) s_slot[rk - s_item[1]] = tid;
+    if (blockIdx.y == 0) {
+      for (int i = rank * kVThreads + tid; i < p.nslots * kVRows; i += p.split * kVThreads) {
+        const int sl = i / kVRows, orow = rb * kVRows + i % kVRows;
+        if (s_ids[sl] < 0 && orow < p.N) p.y[(size_t)sl * p.N + orow] = __float2bfloat16_rn(0.f);
+      }
+    }
+    __syncthreads();
+    if (s_item[0] < 0) return;
+    T = s_item[2];
+    w = p.w + (uint64_t)s_item[0] * p.expert_stride;
+  }
   uint8_t* abuf = smem;                                   // kVBufs x 16 KB
   uint8_t* bbuf = smem + kVBufs * kABytes;                // steps x 64 columns x 16 tokens
   float* part = reinterpret_cast<float*>(smem);           // 16 x 128 fp32, after the MMAs
@@ -220,7 +287,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
 #pragma unroll
   for (int u = 0; u < kWindow; ++u) {
     const int g = g0 + 2 * u + h;
-    load_block<FMT>(p, rt, r8, g, row_ok && u < steps && g < g1, win[u]);
+    load_block<FMT>(p, w, rt, r8, g, row_ok && u < steps && g < g1, win[u]);
   }
   if (p.prefetch) pdl_wait();
   pdl_launch_dependents();
@@ -240,7 +307,10 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
         const int t = u % kVTok, kk = u / kVTok;
         const int k = g0 * 32 + kk * 8;
         v[j] = make_uint4(0, 0, 0, 0);
-        if (u < n_units && t < p.T && k < k_end) v[j] = *reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + k);
+        if (u < n_units && t < T && k < k_end) {
+          const int vec = (p.ids == nullptr) ? t : (p.per_slot ? s_slot[t] : s_slot[t] / p.top_k);
+          v[j] = *reinterpret_cast<const uint4*>(p.x + (size_t)vec * p.K + k);
+        }
       }
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
@@ -271,7 +341,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
           }
           decode_store<FMT>(win[u], a_row + (size_t)b * kABytes, 4 * h);
           const int gn = g0 + 2 * (st + kWindow) + h;
-          load_block<FMT>(p, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
+          load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&full[b]));
@@ -319,7 +389,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   // K ranges meet in rank order; rank q stores outputs q, q + split, ...
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
-  for (int i = rank * kVThreads + tid; i < kVRows * p.T; i += p.split * kVThreads) {  // all 9 warps
+  for (int i = rank * kVThreads + tid; i < kVRows * T; i += p.split * kVThreads) {  // all 9 warps
     const int t = i / kVRows, rr = i % kVRows;
     const int orow = rb * kVRows + rr;
     if (orow >= p.N) continue;
@@ -329,7 +399,8 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     float acc = 0.f;
 #pragma unroll
     for (int q = 0; q < kVMaxSplit; ++q) acc += v[q];   // rank order; absent ranks add +0
-    p.y[(size_t)t * p.N + orow] = __float2bfloat16_rn(acc);
+    const int oslot = (p.ids == nullptr) ? t : s_slot[t];
+    p.y[(size_t)oslot * p.N + orow] = __float2bfloat16_rn(acc);
   }
   cluster.sync();
   if (warp == 0) {
@@ -343,8 +414,14 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
 // Verify-batch plan: rows in blocks of 128, K cut into `split` ranges (one
 // cluster rank each) so that the grid covers about two CTAs per SM.
 bool verify_supported(const MatvecArgs& a) {
-  if (!fmt_is_mx(a.fmt) || a.ids != nullptr || a.x_f16 || a.glu || a.dbg != nullptr) return false;
-  if (a.ntok <= 4 || a.ntok > kVTok) return false;
+  if (!fmt_is_mx(a.fmt) || a.x_f16 || a.glu || a.dbg != nullptr) return false;
+  if (a.ids != nullptr) {
+    // sorted gather: beyond the decode gather's 32 routed slots
+    const int nslots = a.ntok * a.top_k;
+    if (nslots <= 32 || nslots > kVMaxSlots) return false;
+  } else if (a.ntok <= 4 || a.ntok > kVTok) {
+    return false;
+  }
   const int groups = a.K / 32;
   return (groups + kVMaxSplit - 1) / kVMaxSplit <= 2 * kVMaxSteps;
 }
@@ -368,8 +445,11 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.rowtile = g.rowtile;
   p.groups = a.K / 32;
   const int row_blocks = (a.N + kVRows - 1) / kVRows;
-  // one wave of at most two CTAs per SM
-  int split = (2 * device_sm_count()) / row_blocks;
+  // One wave of at most two CTAs per SM; a sorted gather has many work items
+  // (grid.y), so it splits K only as far as the activation operand needs.
+  const int nslots = a.ids ? a.ntok * a.top_k : 0;
+  const int items = a.ids ? (nslots + kVTok - 1) / kVTok + (a.n_experts < nslots ? a.n_experts : nslots) : 1;
+  int split = a.ids ? 1 : (2 * device_sm_count()) / row_blocks;
   if (split > kVMaxSplit) split = kVMaxSplit;
   if (split > p.groups / 2) split = p.groups / 2;
   if (split < 1) split = 1;
@@ -377,6 +457,12 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.split = split;
   p.steps = ((p.groups + split - 1) / split + 1) / 2;
   p.prefetch = a.prefetch ? 1 : 0;
+  p.ids = a.ids;
+  p.top_k = a.top_k;
+  p.nslots = nslots;
+  p.per_slot = a.per_slot;
+  p.n_experts = a.n_experts;
+  p.expert_stride = a.expert_stride;
   const size_t smem = verify_smem_bytes(p.steps);
   static size_t configured[64] = {};
   int dev = 0;
@@ -390,7 +476,7 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
     configured[dev] = smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(row_blocks * split));
+  cfg.gridDim = dim3((unsigned)(row_blocks * split), (unsigned)items);
   cfg.blockDim = dim3(kVThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;

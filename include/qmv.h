@@ -100,7 +100,8 @@ typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3, QMV_MXFP8 =
 /* Limits checked by every entry point. */
 #define QMV_MAX_NTOK 16     /* decode / verify tokens per call */
 #define QMV_MAX_TOPK 8      /* experts per token */
-#define QMV_MAX_SLOTS 32    /* routed (token, slot) pairs of a gather: ntok * top_k */
+#define QMV_MAX_SLOTS 128   /* routed (token, slot) pairs of a gather: ntok * top_k */
+#define QMV_MAX_LAYER_SLOTS 32  /* routed slots of the CUDA-core gather, the fused gate/up and layers */
 #define QMV_MAX_N (1 << 20)
 #define QMV_MAX_K (1 << 16)
 
@@ -222,12 +223,21 @@ int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32
  *            [0, n_experts) writes a zero row block (mlxcel #2178,
  *            "Implementation Notes", edge cases). A matrix used by several
  *            (token, slot) pairs is streamed once per call for up to 4 of them.
+ *   Up to QMV_MAX_LAYER_SLOTS (32) routed slots the call is the decode
+ *   gather above. 33..QMV_MAX_SLOTS (128) slots -- a verify or prefill batch
+ *   through a MoE projection -- need an MX format with bf16 activations and
+ *   run as the sorted gather ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ
+ *   on RDNA ...", "Depends on": the batched MMQ path): the slots are grouped
+ *   by expert (experts in order of their first slot, slots in slot order)
+ *   and each expert's weights are streamed once per 16 of its slots through
+ *   the tensor cores. Same results up to the order of fp32 additions.
  *   x_dev:   MX formats: bf16 vectors of K (fp16 with QMV_FLAG_X_F16); CB
  *            formats: q8_1 buffer.
  *   y_dev:   MX formats: bf16 [ntok][top_k][N] (fp16 with QMV_FLAG_X_F16); CB
  *            formats: fp32 [ntok][top_k][N].
  * Errors: QMV_EINVAL (ntok not in 1..16, top_k not in 1..8, ntok * top_k >
- * QMV_MAX_SLOTS), QMV_ESHAPE,
+ * QMV_MAX_SLOTS, or > QMV_MAX_LAYER_SLOTS outside the sorted gather's
+ * formats), QMV_ESHAPE,
  * QMV_EALIGN, QMV_ECUDA.
  */
 int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,

@@ -164,3 +164,40 @@ def test_verify_tensor_core_deterministic_and_chained():
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y4.view(torch.int16))
     assert status_clean()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("ntok,top_k,per_slot", [(16, 8, True), (16, 8, False), (8, 8, True), (12, 3, False)])
+def test_sorted_gather(fmt, ntok, top_k, per_slot):
+    """33..128 routed slots: the sorted tensor-core gather, against the oracle
+    per slot. Expert 5 takes 20 slots (two work items of <= 16), ids repeat
+    within a token, and invalid ids give zero rows."""
+    E, N, K = 32, 520, 2880
+    g = qi.rng(ntok * 1000 + top_k * 10 + per_slot)
+    ids = qi.topk_ids(g, ntok, top_k, E)
+    ids[:, 0] = 5
+    if top_k > 1:
+        ids[:4, 1] = 5
+        ids[-1, -1] = -3
+        ids[0, -1] = E
+    lo, hi = MX_SCALES[fmt]
+    m = Matrices(fmt, N, K, E, ids.reshape(-1), seed=ntok + top_k + 7, scale_lo=lo, scale_hi=hi)
+    nvec = ntok * top_k if per_slot else ntok
+    x = qi.normal_bf16_bits(g, (nvec, K))
+    y = torch.full((ntok, top_k, N), 5.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), int(per_slot), to_dev(ids), ntok, top_k, y)
+    got = bf16_to_np(y)
+    cache = {}
+    for t in range(ntok):
+        for j in range(top_k):
+            e = int(ids[t, j])
+            if not (0 <= e < E):
+                assert np.all(got[t, j] == 0), (t, j)
+                continue
+            v = t * top_k + j if per_slot else t
+            if (e, v) not in cache:
+                cache[(e, v)] = (oracle.mx_matvec(fmt, m.codes[e], m.scales[e], x[v:v + 1])[0],
+                                 oracle.mx_abs_products(fmt, m.codes[e], m.scales[e], x[v:v + 1])[0])
+            ref, absum = cache[(e, v)]
+            assert_close(got[t, j], ref, absum, True, f"slot ({t},{j}) expert {e}")
+    assert status_clean()

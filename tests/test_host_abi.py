@@ -171,19 +171,25 @@ def test_gather_argument_errors(top_k, ids, code):
 
 
 def test_routed_slot_limit():
-    """A gather routes at most QMV_MAX_SLOTS (token, slot) pairs; 16 tokens
-    is the dense limit."""
-    assert qmv.MAX_SLOTS == 32 and qmv.MAX_NTOK == 16
-    d = qmv.wdesc("mxfp4", 64, 64, 8)
-    G = qmv.lib.qmv_moe_gather_ex
+    """Gathers route at most QMV_MAX_SLOTS (128) (token, slot) pairs; beyond
+    QMV_MAX_LAYER_SLOTS (32) only the sorted tensor-core gather (MX formats,
+    bf16 activations) takes them; layers stop at 32; 16 tokens is the dense
+    limit. (No call here reaches a launch: every one fails validation.)"""
+    assert qmv.MAX_SLOTS == 128 and qmv.MAX_LAYER_SLOTS == 32 and qmv.MAX_NTOK == 16
     B = qmv.ctypes.byref
-    assert G(B(d), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) == qmv.QMV_EINVAL      # 64 slots
-    assert G(B(d), FAKE, FAKE, 1, FAKE, 16, 4, FAKE, 0, 0) == qmv.QMV_EINVAL     # 64 slots
-    assert G(B(d), FAKE, FAKE, 0, FAKE, 17, 1, FAKE, 0, 0) == qmv.QMV_EINVAL     # 17 tokens
+    G = qmv.lib.qmv_moe_gather_ex
+    cb = qmv.wdesc("cb3", 64, 64, 8, qi.LUT_CB3)
+    assert G(B(cb), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) == qmv.QMV_EINVAL      # 64 codebook slots
+    mx = qmv.wdesc("mxfp4", 64, 64, 8)
+    assert G(B(mx), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL   # fp16: no sorted path
+    assert G(B(mx), FAKE, FAKE, 0, FAKE, 17, 1, FAKE, 0, 0) == qmv.QMV_EINVAL     # 17 tokens
+    assert G(B(mx), FAKE, FAKE, 0, FAKE, 16, 9, FAKE, 0, 0) == qmv.QMV_EINVAL     # top_k 9
     gu = qmv.wdesc("mxfp4", 64, 64, 8)
     assert qmv.qmv_moe_layer_workspace_bytes(gu, 8, 4) == (32 * 64 * 2 + 255) // 256 * 256
-    assert qmv.qmv_moe_layer_workspace_bytes(gu, 16, 4) == 0
-    assert qmv.lib.qmv_quantize_act_q8(FAKE, 33, 64, FAKE, 1 << 20, 0) == qmv.QMV_EINVAL
+    assert qmv.qmv_moe_layer_workspace_bytes(gu, 16, 4) == 0                        # 64 slots: no layer
+    L = qmv.lib.qmv_moe_layer
+    assert L(B(gu), FAKE, B(gu), FAKE, FAKE, FAKE, 16, 4, FAKE, 1 << 20, FAKE, 0, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_quantize_act_q8(FAKE, 129, 64, FAKE, 1 << 22, 0) == qmv.QMV_EINVAL
 
 
 def test_debug_sums_size_error():
