@@ -701,6 +701,21 @@ def run_configs(args):
     emit("f3", "qmv_moe_layer MXFP4 2880 E=32 top4 verify ntok=8 (32 routed slots, 2 launches)",
          3 * MATRIX_BYTES * sum(distinct8) / Lm, t / Lm,
          {"calls_per_graph": Lm, "distinct_experts_mean": sum(distinct8) / Lm})
+    # sorted gathers (f3): 16 tokens x top-8 = 128 routed slots over the layer's 32 experts
+    ids16 = torch.from_numpy(np.stack([qi.topk_ids(g, 16, 8, E) for _ in range(Lm)])).to(dev)
+    x16b = torch.from_numpy(qi.normal_bf16_bits(g, (16, K)).view(np.int16)).to(dev).view(torch.bfloat16)
+    xs128 = torch.from_numpy(qi.normal_bf16_bits(g, (128, K)).view(np.int16)).to(dev).view(torch.bfloat16)
+    y128 = torch.empty(Lm, 16, 8, K, dtype=torch.bfloat16, device=dev)
+    distinct16 = [len(set(r.reshape(-1).tolist())) for r in ids16.cpu().numpy()]
+    sg_bytes = MATRIX_BYTES * sum(distinct16) / Lm
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_gather_ex(ddm, Wdm[l], x16b, 0, ids16[l], 16, 8, y128[l], PF)
+                                       for l in range(Lm)])
+    emit("f3", "qmv_moe_gather MXFP4 2880x2880 E=32 sorted, 16 tokens x top-8 (128 slots), shared x", sg_bytes,
+         t / Lm, {"calls_per_graph": Lm, "distinct_experts_mean": sum(distinct16) / Lm})
+    t, _ = _graph_time(torch, lambda: [qmv.qmv_moe_gather_ex(ddm, Wdm[l], xs128, 1, ids16[l], 16, 8, y128[l], PF)
+                                       for l in range(Lm)])
+    emit("f3", "qmv_moe_gather MXFP4 2880x2880 E=32 sorted, 16 tokens x top-8 (128 slots), per-slot x", sg_bytes,
+         t / Lm, {"calls_per_graph": Lm, "distinct_experts_mean": sum(distinct16) / Lm})
     # fp16 activations (QMV_FLAG_X_F16): same weights, x, h and y in fp16; x is
     # scaled by 2^-10 so that h and y stay inside fp16's range with these weights
     x16 = (qi.normal_f32(g, (1, K)) * np.float32(2.0 ** -10)).astype(np.float16)
