@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     __syncthreads();
     if (s_item[0] >= 0 && e == s_item[0] && rk >= s_item[1] && rk < s_item[1] + s_item[2]) s_slot[rk - s_item[1]] = tid;
     if (blockIdx.y == 0) {
+      if (p.prefetch) pdl_wait();   // outputs are written only after the preceding kernel completed
       for (int i = rank * kVThreads + tid; i < p.nslots * kVRows; i += p.split * kVThreads) {
         const int sl = i / kVRows, orow = rb * kVRows + i % kVRows;
         if (s_ids[sl] < 0 && orow < p.N) p.y[(size_t)sl * p.N + orow] = __float2bfloat16_rn(0.f);

@@ -201,3 +201,31 @@ def test_sorted_gather(fmt, ntok, top_k, per_slot):
             ref, absum = cache[(e, v)]
             assert_close(got[t, j], ref, absum, True, f"slot ({t},{j}) expert {e}")
     assert status_clean()
+
+
+def test_sorted_gather_prefetch_chain():
+    """The sorted gather with QMV_FLAG_PREFETCH_INPUTS after a kernel that
+    writes its activations, on a side stream (dependent launch): same bits as
+    the plain call; invalid ids still give zero rows."""
+    E, N, K, ntok, top_k = 16, 264, 1024, 8, 8
+    g = qi.rng(990)
+    ids = np.stack([g.permutation(E)[:top_k] for _ in range(ntok)]).astype(np.int32)
+    ids[3, 2] = -1
+    m = Matrices("mxfp4", N, K, E, ids.reshape(-1), seed=991)
+    x = to_dev(qi.normal_bf16_bits(g, (ntok, K)))
+    ids_d = to_dev(ids)
+    y1 = torch.full((ntok, top_k, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_moe_gather(m.desc, m.w, x, 0, ids_d, ntok, top_k, y1)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    x2 = torch.empty_like(x)
+    y2 = torch.full_like(y1, 4.0)
+    with torch.cuda.stream(s):
+        x2.copy_(x)
+        qmv.qmv_moe_gather_ex(m.desc, m.w, x2, 0, ids_d, ntok, top_k, y2, qmv.QMV_FLAG_PREFETCH_INPUTS, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.count_nonzero(y2[3, 2].float()).item() == 0
+    assert status_clean()
