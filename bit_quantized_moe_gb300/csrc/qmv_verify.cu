@@ -1,5 +1,6 @@
-// qmv_verify.cu -- dense verify-batch matvec of the MX formats on the
-// fifth-generation tensor cores (tcgen05), for 5..16 tokens.
+// qmv_verify.cu -- verify and batched products of the MX formats on the
+// fifth-generation tensor cores (tcgen05): dense matvecs of 5..16 tokens, and
+// sorted expert gathers of 33..128 routed slots.
 //
 // A speculative-decoding verify batch applies one weight matrix to several
 // tokens at once ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...",
@@ -20,14 +21,15 @@
 // outputs. Per CTA: 8 decoding warps -- a warp decodes 16 rows (two row
 // tiles) of every 64-column step, a lane taking one row and one of the two
 // 32-groups, its weight loads issued a window of steps ahead -- and one warp
-// that issues the MMAs. Three A buffers, each
-// with a "full" barrier (one arrival per decoding warp) and an "empty" one
-// (tcgen05.commit), let the warps decode ahead of the tensor core.
+// that issues the MMAs. Three A buffers, each with a "full" barrier (one
+// arrival per decoding warp) and an "empty" one (tcgen05.commit), let the
+// warps decode ahead of the tensor core. A sorted gather adds a second grid
+// dimension of work items, one (expert, up to 16 of its slots) pair each.
 //
 // Operand layouts (no swizzle, K-major "canonical" core matrices of 8 rows x
-// 16 bytes): A step buffer (128 rows x 128 columns), core matrix (row group
-// g, k group kk) at kk * 2048 + g * 128; B (activations, tokens padded to 16 with zeros), core
-// matrix (token group g, k group kk) at kk * 256 + g * 128. Descriptor
+// 16 bytes): A step buffer (128 rows x 64 columns), core matrix (row group
+// g, k group kk) at kk * 2048 + g * 128; B (activations, tokens padded to 16
+// with zeros), core matrix (token group g, k group kk) at kk * 256 + g * 128. Descriptor
 // leading byte offset = the K-direction stride, stride byte offset = the
 // row-direction stride.
 //
@@ -37,6 +39,8 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "qmv_device.cuh"
 #include "qmv_internal.h"
@@ -465,11 +469,13 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.n_experts = a.n_experts;
   p.expert_stride = a.expert_stride;
   const size_t smem = verify_smem_bytes(p.steps);
+  static std::mutex mu;
   static size_t configured[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
   if (configured[dev] < smem) {
     g_launch_stage = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
     err = cudaFuncSetAttribute(verify_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
