@@ -475,12 +475,14 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (configured[dev] < smem) {
-    g_launch_stage = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
-    err = cudaFuncSetAttribute(verify_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    configured[dev] = smem;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (configured[dev] < smem) {
+      g_launch_stage = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
+      err = cudaFuncSetAttribute(verify_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      configured[dev] = smem;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(row_blocks * split), (unsigned)items);
