@@ -47,7 +47,7 @@ EXPORTS = (
     "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
     "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
     "qmv_moe_layer_noalloc", "qmv_moe_combine", "qmv_moe_combine_ex", "qmv_moe_layer_combine_workspace_bytes", "qmv_moe_layer_combine",
-    "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant",
+    "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant", "qmv_debug_plan",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
 )
 
@@ -110,6 +110,8 @@ def _load() -> ctypes.CDLL:
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
         "qmv_debug_dequant": (ctypes.c_int, [D, P, I32, P, SZ, P]),
+        "qmv_debug_plan": (ctypes.c_int, [D, I32, I32, I32, I32, ctypes.c_uint32, I32, I32, I64,
+                                          ctypes.POINTER(I64), I32]),
         "qmv_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32]),
         "qmv_debug_wait_probe": (ctypes.c_int, [ctypes.c_uint64, P]),
         "qmv_last_error": (ctypes.c_char_p, []),
@@ -326,6 +328,19 @@ def qmv_debug_block_sums(desc: WDesc, w, x, per_slot_x: int, ids, ntok: int, top
 def qmv_debug_dequant(desc: WDesc, w, expert: int, out, stream=None) -> None:
     _check(lib.qmv_debug_dequant(ctypes.byref(desc), _ptr(w), expert, _ptr(out), _nbytes(out),
                                  _stream(stream)))
+
+
+PLAN_FIELDS = ("nv", "warps", "stages", "items", "grid", "splits", "split_chunks", "items_per_cta", "x_slots",
+               "contig", "smem", "row_tiles")
+
+
+def qmv_debug_plan(desc: WDesc, ntok: int, top_k: int, gather: bool, per_slot_x: bool, flags: int = 0,
+                   sm_count: int = 152, ctas_per_sm: int = 2, smem_per_sm: int = 233472) -> dict:
+    """The CUDA-core matvec's launch plan for a call and device shape (host only)."""
+    out = (ctypes.c_int64 * 12)()
+    _check(lib.qmv_debug_plan(ctypes.byref(desc), ntok, top_k, int(gather), int(per_slot_x), int(flags), sm_count,
+                              ctas_per_sm, smem_per_sm, out, 12))
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def qmv_device_status(clear: bool = False) -> int:

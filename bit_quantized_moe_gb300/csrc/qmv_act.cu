@@ -268,4 +268,14 @@ size_t matvec_smem_bytes(const MatvecArgs& a) {
   return (size_t)plan.smem.total + 256;
 }
 
+// The CUDA-core matvec's launch plan for an explicit device shape (no device
+// is queried): see qmv_debug_plan.
+void debug_plan(const MatvecArgs& a, int sm_count, int ctas_per_sm, size_t smem_per_sm, int64_t out[12]) {
+  const LaunchPlan L = plan_launch(a, sm_count, ctas_per_sm, smem_per_sm);
+  const Geometry g = make_geometry(a.fmt, a.N, a.K);
+  const int64_t v[12] = {L.nv, L.warps, L.stages, L.items, L.grid, L.splits, L.split_chunks, L.items_per_cta,
+                         L.x_slots, L.contig, (int64_t)L.smem.total, g.row_tiles};
+  for (int i = 0; i < 12; ++i) out[i] = v[i];
+}
+
 }  // namespace qmv

@@ -475,6 +475,37 @@ int qmv_moe_layer_combine(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc
   return qmv_moe_combine_ex(down, ys, weights, ids, ntok, top_k, y, flags & QMV_FLAG_X_F16, stream);
 }
 
+int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t gather, int32_t per_slot_x,
+                   uint32_t flags, int32_t sm_count, int32_t ctas_per_sm, int64_t smem_per_sm, int64_t* out,
+                   int32_t n_out) {
+  const char* name = "qmv_debug_plan";
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (!out || n_out < 12) return fail(QMV_ESIZE, "%s: out needs 12 entries", name);
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK ||
+      (gather && ntok * top_k > QMV_MAX_LAYER_SLOTS))
+    return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range for the CUDA-core matvec", name, ntok, top_k);
+  if (sm_count < 1 || ctas_per_sm < 1 || smem_per_sm < 1) return fail(QMV_EINVAL, "%s: bad device shape", name);
+  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16))
+    return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  MatvecArgs a;
+  a.fmt = desc->fmt;
+  a.N = desc->N;
+  a.K = desc->K;
+  a.n_experts = desc->n_experts;
+  static const int32_t dummy = 0;
+  a.ids = gather ? &dummy : nullptr;
+  a.per_slot = (gather && per_slot_x) ? 1 : 0;
+  a.ntok = ntok;
+  a.top_k = gather ? top_k : 1;
+  a.nvec = a.per_slot ? ntok * top_k : ntok;
+  a.prefetch = (flags & QMV_FLAG_PREFETCH_INPUTS) != 0;
+  a.x_f32 = (flags & QMV_FLAG_X_F32) != 0;
+  a.x_f16 = (flags & QMV_FLAG_X_F16) != 0;
+  debug_plan(a, sm_count, ctas_per_sm, (size_t)smem_per_sm, out);
+  return ok();
+}
+
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
                          const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
                          size_t sums_bytes, void* stream) {

@@ -36,6 +36,9 @@ extern thread_local const char* g_launch_stage;
 // Dynamic shared memory a launch of `a` needs (0 if it exceeds the device limit).
 size_t matvec_smem_bytes(const MatvecArgs& a);
 
+// Launch plan of `a` for an explicit device shape (qmv_debug_plan).
+void debug_plan(const MatvecArgs& a, int sm_count, int ctas_per_sm, size_t smem_per_sm, int64_t out[12]);
+
 cudaError_t launch_matvec_mxfp4(const MatvecArgs& a);
 cudaError_t launch_matvec_cb2(const MatvecArgs& a);
 cudaError_t launch_matvec_cb3(const MatvecArgs& a);

@@ -406,6 +406,20 @@ int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w_dev, const void* x
  * device decode routines to fp32 w_dev [N][K] = value(code) * 2^(e-127).
  * For the CB formats value(code) = lut[code].
  */
+/*
+ * Test export (host only, no device needed): the CUDA-core matvec's launch
+ * plan for a call shape and an explicit device shape (sm_count SMs,
+ * ctas_per_sm CTAs per SM, smem_per_sm bytes of shared memory per SM). out
+ * (>= 12 entries): vectors per entry, warps per CTA, ring stages, item upper
+ * bound, grid, K splits, chunks per split, items per CTA, activation vectors
+ * staged per CTA, contiguous dealing (0/1), dynamic shared memory bytes, row
+ * tiles. gather != 0 describes an expert gather (per_slot_x as there).
+ * Errors: QMV_EINVAL, QMV_ESHAPE, QMV_ESIZE.
+ */
+int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t gather, int32_t per_slot_x,
+                   uint32_t flags, int32_t sm_count, int32_t ctas_per_sm, int64_t smem_per_sm, int64_t* out,
+                   int32_t n_out);
+
 int qmv_debug_dequant(const qmv_wdesc* desc, const void* w_dev, int32_t expert, float* out_dev,
                       size_t out_bytes, void* stream);
 

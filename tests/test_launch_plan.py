@@ -1,0 +1,105 @@
+"""The CUDA-core matvec's launch planner, checked on the host against a
+simulation of the kernel's work dealing (no GPU): for every call the library
+accepts (validation rejects a call whose two-CTA plan does not fit the
+per-block shared-memory limit) and every entry count the call can produce,
+each CTA's items fit the split-K partial slots, a CTA of a contiguously
+dealt call touches no more activation vectors than its staged region holds
+(else the kernel records a planning error), and the plan the launcher may
+use -- two CTAs per SM, or one when two do not fit -- fits the device."""
+import itertools
+
+import pytest
+
+qmv = pytest.importorskip("bit_quantized_moe_gb300")
+
+SMS, SMEM_SM, OPTIN = 152, 233472, 232448
+
+
+def deal(n_items, grid, contig, b):
+    """Items of CTA b: (first, stride, count), as the kernel deals them."""
+    if contig:
+        per, rem = divmod(n_items, grid)
+        return b * per + min(b, rem), 1, per + (1 if b < rem else 0)
+    return b, grid, (n_items - b + grid - 1) // grid if b < n_items else 0
+
+
+def accepted(desc, ntok, top_k, gather, per_slot):
+    """The library's validation: the two-CTA plan plus the kernel's static
+    shared memory (256 bytes allowed) within the per-block limit."""
+    p2 = qmv.qmv_debug_plan(desc, ntok, top_k, gather, per_slot, sm_count=SMS, ctas_per_sm=2, smem_per_sm=SMEM_SM)
+    return p2["smem"] + 256 <= OPTIN
+
+
+def check_plan(desc, ntok, top_k, gather, per_slot, ctas):
+    p = qmv.qmv_debug_plan(desc, ntok, top_k, gather, per_slot, sm_count=SMS, ctas_per_sm=ctas,
+                           smem_per_sm=SMEM_SM)
+    if not accepted(desc, ntok, top_k, gather, per_slot):
+        return None
+    rt, nv = p["row_tiles"], p["nv"]
+    nvec = ntok * top_k if (gather and per_slot) else ntok
+    max_entries = p["items"] // rt
+    assert p["grid"] <= SMS * ctas and p["grid"] <= p["items"]
+    assert p["smem"] + 1024 <= OPTIN
+    if not p["contig"]:
+        assert p["x_slots"] == nvec
+    for n_ent in range(1, max_entries + 1):
+        n_items = n_ent * rt
+        for b in range(p["grid"]):
+            first, stride, count = deal(n_items, p["grid"], p["contig"], b)
+            assert count <= p["items_per_cta"], (n_ent, b)
+            if p["contig"] and count > 0:
+                e0, e1 = first // rt, (first + count - 1) // rt
+                assert (e1 - e0 + 1) * nv <= p["x_slots"] or p["x_slots"] == nvec, (n_ent, b, p)
+    return p
+
+
+FMTS = ["mxfp4", "mxfp8", "cb2", "cb3", "cb4"]
+SHAPES = [(1, 32), (17, 1056), (516, 2880), (2880, 2880), (7168, 2048), (2048, 7168)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_gather_plans(fmt, ctas):
+    for (N, K), (ntok, top_k), per_slot in itertools.product(SHAPES, [(1, 4), (4, 4), (4, 8), (8, 4), (16, 2)],
+                                                           [False, True]):
+        if fmt in ("cb2", "cb3") and K % 32:
+            continue
+        check_plan(qmv.wdesc(fmt, N, K, 64), ntok, top_k, True, per_slot, ctas)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_dense_plans(fmt, ctas):
+    for (N, K), ntok in itertools.product(SHAPES, [1, 3, 4, 5, 8, 13, 16]):
+        p = check_plan(qmv.wdesc(fmt, N, K, 1), ntok, 1, False, False, ctas)
+        if p is None:
+            continue
+        assert p["contig"] == (1 if ntok > 4 else 0)
+        assert p["nv"] == min(ntok, 4)
+
+
+def test_decode_shapes_are_accepted():
+    """Every decode-path configuration of the workloads passes validation."""
+    cases = [("mxfp4", 2880, 2880, 32, 1, 4, True, False), ("mxfp4", 2880, 2880, 32, 1, 4, True, True),
+             ("cb2", 4096, 7168, 256, 1, 4, True, False), ("cb3", 7168, 2048, 256, 4, 4, True, True),
+             ("cb4", 7168, 7168, 1, 4, 1, False, False), ("mxfp8", 5760, 2880, 32, 4, 8, True, False),
+             ("mxfp4", 5760, 2880, 32, 8, 4, True, False), ("cb2", 4096, 7168, 64, 8, 4, True, False)]
+    for fmt, N, K, E, ntok, top_k, gather, per_slot in cases:
+        assert accepted(qmv.wdesc(fmt, N, K, E), ntok, top_k, gather, per_slot), (fmt, N, K, ntok, top_k)
+
+
+def test_compact_region_only_when_needed():
+    # the MXFP4 down gather of the decode layer keeps every vector at its own index
+    p = qmv.qmv_debug_plan(qmv.wdesc("mxfp4", 2880, 2880, 32), 1, 4, True, True)
+    assert p["x_slots"] == 4 and p["contig"] == 1
+    # 32 per-slot vectors of K = 4096 cannot all sit beside the ring: compact
+    p = qmv.qmv_debug_plan(qmv.wdesc("mxfp4", 1032, 4096, 16), 4, 8, True, True)
+    assert p["x_slots"] < 32
+
+
+def test_plan_argument_errors():
+    d = qmv.wdesc("mxfp4", 64, 64, 8)
+    with pytest.raises(qmv.QmvError):
+        qmv.qmv_debug_plan(d, 8, 8, True, True)          # 64 slots: not a CUDA-core gather
+    with pytest.raises(qmv.QmvError):
+        qmv.qmv_debug_plan(d, 1, 4, True, True, sm_count=0)
