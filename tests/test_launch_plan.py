@@ -103,3 +103,37 @@ def test_plan_argument_errors():
         qmv.qmv_debug_plan(d, 8, 8, True, True)          # 64 slots: not a CUDA-core gather
     with pytest.raises(qmv.QmvError):
         qmv.qmv_debug_plan(d, 1, 4, True, True, sm_count=0)
+
+
+def sorted_gather_items(ids, n_experts, group=16):
+    """The sorted gather's work items in the kernel's order: experts by first
+    slot, each expert's slots (in slot order) cut into groups of <= 16."""
+    flat = [int(e) for e in ids.reshape(-1)]
+    items = []
+    for s, e in enumerate(flat):
+        if not (0 <= e < n_experts) or e in flat[:s]:
+            continue
+        slots = [q for q, eq in enumerate(flat) if eq == e]
+        for g0 in range(0, len(slots), group):
+            items.append((e, slots[g0:g0 + group]))
+    return items
+
+
+def test_sorted_gather_items_cover_slots_within_grid_bound():
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        ntok = int(rng.integers(1, 17))
+        top_k = int(rng.integers(1, 9))
+        E = int(rng.choice([1, 2, 8, 32, 256]))
+        ids = rng.integers(-2, E + 2, size=(ntok, top_k))
+        if trial % 3 == 0:
+            ids[:, 0] = 0                       # one expert in every token
+        n = ntok * top_k
+        items = sorted_gather_items(ids, E)
+        cap = (n + 15) // 16 + min(E, n)       # the launcher's grid.y
+        assert len(items) <= cap
+        covered = sorted(s for _, group in items for s in group)
+        valid = [s for s, e in enumerate(ids.reshape(-1)) if 0 <= e < E]
+        assert covered == valid                 # every valid slot exactly once
+        assert all(1 <= len(g) <= 16 for _, g in items)
