@@ -104,6 +104,17 @@ cudaError_t launch_for(const MatvecArgs& a) {
   }
 }
 
+// Launch flags valid for a call of format fmt (dbg: the block-sum export).
+int check_flags(int fmt, uint32_t flags, bool dbg, const char* name) {
+  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16))
+    return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  if ((flags & QMV_FLAG_X_F32) && (fmt_is_mx(fmt) || dbg))
+    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F32 applies to the codebook formats only (not block sums)", name);
+  if ((flags & QMV_FLAG_X_F16) && !fmt_is_mx(fmt))
+    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F16 applies to the MX formats only", name);
+  return QMV_OK;
+}
+
 // Rows of the gate/up-interleaved matrix of a projection with N rows.
 int gate_up_rows(int N) { return 2 * ((N + kRows / 2 - 1) / (kRows / 2) * (kRows / 2)); }
 
@@ -121,12 +132,8 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
     glu_desc.N = gate_up_rows(desc_in->N);
     desc = &glu_desc;
   }
-  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16))
-    return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
-  if ((flags & QMV_FLAG_X_F32) && (fmt_is_mx(desc->fmt) || dbg != nullptr))
-    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F32 applies to the codebook formats only (not block sums)", name);
-  if ((flags & QMV_FLAG_X_F16) && !fmt_is_mx(desc->fmt))
-    return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F16 applies to the MX formats only", name);
+  rc = check_flags(desc->fmt, flags, dbg != nullptr, name);
+  if (rc) return rc;
   if (w == nullptr || x == nullptr || y == nullptr)
     return fail(QMV_EINVAL, "%s: weight, activation and output pointers must be non-NULL", name);
   if (ntok < 1 || ntok > QMV_MAX_NTOK) return fail(QMV_EINVAL, "%s: ntok=%d outside [1, %d]", name, ntok, QMV_MAX_NTOK);
@@ -486,8 +493,8 @@ int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t g
       (gather && ntok * top_k > QMV_MAX_LAYER_SLOTS))
     return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range for the CUDA-core matvec", name, ntok, top_k);
   if (sm_count < 1 || ctas_per_sm < 1 || smem_per_sm < 1) return fail(QMV_EINVAL, "%s: bad device shape", name);
-  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16))
-    return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  rc = check_flags(desc->fmt, flags, false, name);
+  if (rc) return rc;
   MatvecArgs a;
   a.fmt = desc->fmt;
   a.N = desc->N;

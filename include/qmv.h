@@ -365,8 +365,12 @@ int qmv_moe_layer_combine(const qmv_wdesc* gate_up_desc, const void* w_gate_up_d
  * QMV_NOALLOC_SCRATCH_BYTES bytes compiled into the library instead; it calls
  * no allocator.
  *  - Every GPU that loads the library holds the array until the process exits.
- *  - The first call on a device looks up the array's device address (with that
- *    device current); make that first call before any stream capture.
+ *  - The array's device address belongs to a CUDA context. The first call in
+ *    each context (the device's primary context, a context the host
+ *    application made itself, or the primary context created again after
+ *    cudaDeviceReset) looks it up, with that context current, and keeps it
+ *    for later calls in the same context; make that first call before any
+ *    stream capture.
  *  - A layer whose qmv_moe_layer_workspace_bytes exceeds the array is rejected
  *    with QMV_ESIZE (use qmv_moe_layer with a workspace for it).
  *  - All calls share the one array and it keeps the last call's contents.
@@ -402,11 +406,6 @@ int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w_dev, const void* x
                          void* y_dev, int32_t* sums_dev, size_t sums_bytes, void* stream);
 
 /*
- * Test export: decode the GPU weight layout of one matrix with the kernels'
- * device decode routines to fp32 w_dev [N][K] = value(code) * 2^(e-127).
- * For the CB formats value(code) = lut[code].
- */
-/*
  * Test export (host only, no device needed): the CUDA-core matvec's launch
  * plan for a call shape and an explicit device shape (sm_count SMs,
  * ctas_per_sm CTAs per SM, smem_per_sm bytes of shared memory per SM). out
@@ -420,6 +419,11 @@ int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t g
                    uint32_t flags, int32_t sm_count, int32_t ctas_per_sm, int64_t smem_per_sm, int64_t* out,
                    int32_t n_out);
 
+/*
+ * Test export: decode the GPU weight layout of one matrix with the kernels'
+ * device decode routines to fp32 w_dev [N][K] = value(code) * 2^(e-127).
+ * For the CB formats value(code) = lut[code].
+ */
 int qmv_debug_dequant(const qmv_wdesc* desc, const void* w_dev, int32_t expert, float* out_dev,
                       size_t out_bytes, void* stream);
 

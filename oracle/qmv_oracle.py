@@ -24,7 +24,7 @@ Sources (web pages, cited by title and section):
   [OCP-MX]       the OCP Microscaling Formats (MX) v1.0 specification, for the
                  E4M3 element of MXFP8, which the pages name but do not define
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * E2M1 value table {0,.5,1,1.5,2,3,4,6} with the sign in bit 3 and E8M0
     scale 2**(e-127), e = 255 -> NaN (OCP MX convention).
   * MXFP8: E4M3 elements (bias 7, subnormals, S.1111.111 = NaN, no

@@ -68,25 +68,88 @@ class Matrices:
         self.w[e * self.eb:(e + 1) * self.eb] = torch.from_numpy(packed).to(DEV)
 
 
-def tolerance(absum: np.ndarray, ref: np.ndarray, bf16_out: bool) -> np.ndarray:
-    """1e-3 * sum|w x| per output, plus one bf16 ulp of the result when the
-    output is stored as bf16 (its rounding alone can exceed the first term
-    when |y| is close to sum|w x|)."""
-    tol = 1e-3 * absum
-    if bf16_out:
-        tol = tol + np.abs(ref) * 2.0 ** -8
-    return tol + 1e-30
+def round_out(v, out: str) -> np.ndarray:
+    """float64 values rounded to nearest (ties to even) in the output type
+    `out` ("bf16" or "f16"), returned as float64; "f32" returns v unchanged.
+    bf16 rounds straight from the float64 bits (no intermediate fp32), with
+    its subnormals on the 2^-133 grid and overflow to +-inf; fp16 uses numpy's
+    float64 -> float16 conversion (round to nearest even)."""
+    v = np.asarray(v, dtype=np.float64)
+    if out == "f32":
+        return v
+    if out == "f16":
+        with np.errstate(over="ignore"):
+            return v.astype(np.float16).astype(np.float64)
+    assert out == "bf16", out
+    c = np.ascontiguousarray(v)
+    b = c.view(np.uint64)
+    lsb = (b >> np.uint64(45)) & np.uint64(1)
+    r = ((b + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)).view(np.float64)
+    r = np.where(np.abs(r) > 3.3895313892515355e38, np.copysign(np.inf, c), r)
+    sub = np.rint(c * 2.0 ** 133) * 2.0 ** -133
+    r = np.where(np.abs(c) < 2.0 ** -126, sub, r)
+    return np.where(np.isfinite(c), r, c)
 
 
-def assert_close(got, ref, absum, bf16_out, what=""):
+def close_mask(got, ref, bound, out: str) -> np.ndarray:
+    """True where a stored output is consistent with the exact value `ref`:
+    the kernel's fp32 result lies within `bound` of ref, and a bf16 or fp16
+    output is that fp32 result rounded to nearest. Rounding is monotone, so
+    the stored value must lie between round(ref - bound) and
+    round(ref + bound); an fp32 output must lie within bound of ref."""
     got = np.asarray(got, dtype=np.float64)
-    err = np.abs(got - ref)
-    tol = tolerance(absum, ref, bf16_out)
-    bad = ~(err <= tol)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = np.asarray(bound, dtype=np.float64)
+    if out == "f32":
+        return np.abs(got - ref) <= bound
+    return (round_out(ref - bound, out) <= got) & (got <= round_out(ref + bound, out))
+
+
+def _out_name(out) -> str:
+    if out is True:
+        return "bf16"
+    if out is False:
+        return "f32"
+    return out
+
+
+def out_of(fmt: str, x_dtype: str = "bf16") -> str:
+    """Stored output type of a call: the activation type for the MX formats,
+    fp32 for the codebook formats."""
+    return x_dtype if fmt in ("mxfp4", "mxfp8") else "f32"
+
+
+def stored_err(v, bound, out: str) -> np.ndarray:
+    """Bound on |stored - v| when the kernel's fp32 result lies within `bound`
+    of v and is stored in `out`, rounded to nearest: bound plus half an ulp at
+    |v| + bound (bf16, 8 significant bits: 2^-8 relative, subnormal
+    half-quantum 2^-134; fp16, 11 bits: 2^-11, 2^-25)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    b = np.asarray(bound, dtype=np.float64)
+    if out == "bf16":
+        return b + (a + b) * 2.0 ** -8 + 2.0 ** -134
+    if out == "f16":
+        return b + (a + b) * 2.0 ** -11 + 2.0 ** -25
+    return b
+
+
+def assert_within(got, ref, bound, out, what=""):
+    """Every stored output consistent with ref within the fp32 bound (close_mask)."""
+    out = _out_name(out)
+    got = np.asarray(got, dtype=np.float64)
+    bound = np.broadcast_to(np.asarray(bound, dtype=np.float64), got.shape)
+    bad = ~close_mask(got, ref, bound, out)
     if bad.any():
-        i = np.argwhere(bad)[0]
-        raise AssertionError(f"{what}: {bad.sum()} outputs outside tolerance; first {tuple(i)}: "
-                             f"got {got[tuple(i)]!r} want {ref[tuple(i)]!r} tol {tol[tuple(i)]!r}")
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} outputs outside tolerance; first {i}: "
+                             f"got {got[i]!r} want {np.asarray(ref)[i]!r} bound {bound[i]!r} ({out})")
+
+
+def assert_close(got, ref, absum, out, what=""):
+    """Per output element: max|gpu - oracle| <= 1e-3 * sum|w x| for the
+    kernel's fp32 result, checked on the stored value as close_mask does.
+    out: "bf16", "f16" or "f32" (True / False mean bf16 / fp32)."""
+    assert_within(got, ref, 1e-3 * np.asarray(absum, dtype=np.float64), out, what)
 
 
 def quantize_on_gpu(x_f32: np.ndarray):

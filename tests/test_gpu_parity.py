@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 
 qmv = pytest.importorskip("bit_quantized_moe_gb300")
 from qmv_testutil import (DEV, MX_SCALES, Matrices, act_bits, act_to_dev, assert_close,  # noqa: E402
-                          bf16_to_np, mx_flags, quantize_on_gpu, status_clean, to_dev)
+                          assert_within, bf16_to_np, mx_flags, out_of, quantize_on_gpu, status_clean,
+                          stored_err, to_dev)
 
 LUTS = {"cb2": qi.LUT_CB2, "cb3": qi.LUT_CB3, "cb4": qi.LUT_CB4}
 
@@ -245,7 +246,8 @@ def test_swiglu(n):
     qmv.qmv_swiglu_bf16(to_dev(gb), to_dev(ub), h, n)
     ref = oracle.swiglu(oracle.bf16_bits_to_f64(gb), oracle.bf16_bits_to_f64(ub))
     got = bf16_to_np(h)
-    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+    # fp32 arithmetic (exp, add, divide, multiply: a few ulp), then bf16 rounding
+    assert_within(got, ref, 1e-6 * np.abs(ref), "bf16", "swiglu")
 
 
 def test_mxfp4_moe_layer_chain():
@@ -281,10 +283,21 @@ def test_mxfp4_moe_layer_chain():
             r = oracle.mxfp4_matvec(mm.codes[e], mm.scales[e], x)[0]
             absum = oracle.mxfp4_abs_products(mm.codes[e], mm.scales[e], x)[0]
             assert_close(bf16_to_np(got)[0, j], r, absum, True, f"{name} slot {j}")
-    # h: bf16 of silu(g)*u; g/u may differ from the oracle's by a bf16 rounding step
+    # h, stage-wise: the SwiGLU kernel on the GPU's own bf16 g and u (fp32
+    # arithmetic, then one bf16 rounding), every element
     hg = bf16_to_np(h)[0]
-    href = oracle.bf16_bits_to_f64(ref["h_bits"])[0]
-    assert np.mean(np.abs(hg - href) <= np.abs(href) * 2.0 ** -7 + 1e-6) > 0.999
+    stage = oracle.swiglu(bf16_to_np(yg)[0], bf16_to_np(yu)[0])
+    assert_within(hg, stage, 1e-6 * np.abs(stage), "bf16", "h stage-wise")
+    # h, chain-wise: against silu(g) * u of the exact g and u, their matvec
+    # bounds and bf16 storage propagated through SwiGLU, every element
+    gx = np.stack([oracle.mxfp4_matvec(gate.codes[int(e)], gate.scales[int(e)], x)[0] for e in ids[0]])
+    ux = np.stack([oracle.mxfp4_matvec(up.codes[int(e)], up.scales[int(e)], x)[0] for e in ids[0]])
+    eg = stored_err(gx, 1e-3 * np.stack([oracle.mxfp4_abs_products(gate.codes[int(e)], gate.scales[int(e)], x)[0]
+                                         for e in ids[0]]), "bf16")
+    eu = stored_err(ux, 1e-3 * np.stack([oracle.mxfp4_abs_products(up.codes[int(e)], up.scales[int(e)], x)[0]
+                                         for e in ids[0]]), "bf16")
+    hx = oracle.swiglu(gx, ux)
+    assert_within(hg, hx, oracle.swiglu_tolerance(gx, ux, eg, eu) + 1e-6 * np.abs(hx), "bf16", "h chain-wise")
     # down: against the oracle chain (its own h)
     for j in range(top_k):
         e = int(ids[0, j])
@@ -471,12 +484,10 @@ def check_gate_up(m, ids, h_gpu, xin, q=None, d=None, x_dtype="bf16"):
     h, gv, uv = oracle.moe_gate_up_swiglu(gm, um, m.E, ids, m.N)
     tg = oracle.moe_gather(ga, m.E, ids, False, m.N) * 1e-3
     tu = oracle.moe_gather(ua, m.E, ids, False, m.N) * 1e-3
-    tol = oracle.swiglu_tolerance(gv, uv, tg, tu)
-    if m.fmt in ("mxfp4", "mxfp8"):
-        tol = tol + np.abs(h) * 2.0 ** -8 + 2.0 ** -24    # one bf16 ulp (fp16: also its subnormal quantum)
-    err = np.abs(h_gpu - h)
-    bad = ~(err <= tol + 1e-30)
-    assert not bad.any(), f"{bad.sum()} fused outputs outside tolerance, first {np.argwhere(bad)[0]}"
+    # the matvec bounds propagated through SwiGLU, plus its fp32 arithmetic;
+    # the stored h (bf16 / fp16 for the MX formats) is that result rounded
+    tol = oracle.swiglu_tolerance(gv, uv, tg, tu) + 1e-6 * np.abs(h)
+    assert_within(h_gpu, h, tol, out_of(m.fmt, x_dtype), "fused gate/up")
 
 
 @pytest.mark.parametrize("N,ntok,top_k", [(2880, 1, 4), (516, 2, 4), (515, 1, 3), (64, 4, 2)])
@@ -520,21 +531,22 @@ def _mx_dequant(fmt, codes, scales):
 
 
 def _layer_expected(gu, down, ids, x=None, q=None, d=None, x_dtype="bf16"):
-    """Oracle chain and the per-output bound for y. h differs from the GPU's
-    by the propagated SwiGLU bound plus its storage rounding (a bf16 ulp, or
-    an fp16 one, for the MX formats; one q8_1 quantum of its block for the
-    codebooks)."""
+    """Oracle chain and the per-output bound on the kernel's fp32 y (before
+    its storage rounding, which the callers check with the stored type). h
+    differs from the GPU's by the propagated SwiGLU bound plus its storage
+    rounding (a bf16 ulp, or an fp16 one, for the MX formats; one q8_1
+    quantum of its block for the codebooks)."""
     gm, um, ga, ua = gu.matvecs(x, q, d, x_dtype)
     h, gv, uv = oracle.moe_gate_up_swiglu(gm, um, gu.E, ids, gu.N)
     tol_h = oracle.swiglu_tolerance(gv, uv, oracle.moe_gather(ga, gu.E, ids, False, gu.N) * 1e-3,
                                     oracle.moe_gather(ua, gu.E, ids, False, gu.N) * 1e-3)
     ntok, top_k = ids.shape
     rows = h.reshape(ntok * top_k, gu.N)
-    tiny = 2.0 ** -24 if x_dtype == "f16" else 0.0
     if gu.fmt in MX:
         hb = oracle.f64_to_bf16_bits(rows) if x_dtype == "bf16" else oracle.f64_to_f16_bits(rows)
-        hx = oracle.act_bits_to_f64(hb, x_dtype)
-        dh = tol_h.reshape(rows.shape) + np.abs(hx) * 2.0 ** -8 * 2 + tiny
+        # |GPU h - h| (its fp32 bound, stored rounded) + |hb - h| (the oracle's rounding)
+        dh = (stored_err(rows, tol_h.reshape(rows.shape) + 1e-6 * np.abs(rows), x_dtype)
+              + stored_err(rows, 0.0, x_dtype))
         y = oracle.mx_moe_gather(down.fmt,
                                  np.stack([down.codes.get(e, np.zeros((down.N, down.K), np.uint8)) for e in range(down.E)]),
                                  np.stack([down.scales.get(e, np.zeros((down.N, down.K // 32), np.uint8)) for e in range(down.E)]),
@@ -560,8 +572,6 @@ def _layer_expected(gu, down, ids, x=None, q=None, d=None, x_dtype="bf16"):
                 Wabs = np.abs(oracle.cb_dequant(down.codes[e], down.scales[e], down.lut, grp))
                 base = Wabs @ np.abs(hq[s].astype(np.float64) * np.repeat(dq[s], 32))
             tol[t, j] = 1e-3 * base + Wabs @ dh[s]
-    if down.fmt in MX:
-        tol = tol + np.abs(y) * 2.0 ** -8 + tiny
     return y, tol
 
 
@@ -577,8 +587,7 @@ def test_mxfp4_moe_layer():
         y = torch.empty(ntok, top_k, K, dtype=torch.bfloat16, device=DEV)
         qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, to_dev(x), to_dev(ids), ntok, top_k, ws, y)
         want, tol = _layer_expected(gu, down, ids, x=x)
-        err = np.abs(bf16_to_np(y) - want)
-        assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+        assert_within(bf16_to_np(y), want, tol, "bf16", "layer")
     assert status_clean()
 
 
@@ -594,8 +603,7 @@ def test_cb_moe_layer_ds4_shapes():
     y = torch.empty(ntok, top_k, 7168, dtype=torch.float32, device=DEV)
     qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xq, to_dev(ids), ntok, top_k, ws, y)
     want, tol = _layer_expected(gu, down, ids, q=q, d=d)
-    err = np.abs(y.cpu().numpy().astype(np.float64) - want)
-    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert_within(y.cpu().numpy(), want, tol, "f32", "layer")
     assert status_clean()
 
 
@@ -635,8 +643,7 @@ def test_layer_format_pairs(pair, ntok, top_k):
     qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xin, ids_d, ntok, top_k, ws, y)
     want, tol = _layer_expected(gu, down, ids, x=x, q=q, d=d)
     got = bf16_to_np(y) if dt == torch.bfloat16 else y.cpu().numpy().astype(np.float64)
-    err = np.abs(got - want)
-    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert_within(got, want, tol, out_of(fmt_dn), "layer")
     if xf is not None:
         y2 = torch.full_like(y, -7.0)
         qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xf, ids_d, ntok, top_k, ws, y2, qmv.QMV_FLAG_X_F32)
@@ -661,8 +668,7 @@ def test_layer_many_slots():
     want, tol = _layer_expected(gu, down, ids, x=x)
     got = bf16_to_np(y)
     assert np.all(got[3, 7] == 0) and np.all(got[2, 0] == 0)
-    err = np.abs(got - want)
-    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} layer outputs outside tolerance"
+    assert_within(got, want, tol, "bf16", "layer")
     assert status_clean()
 
 
@@ -788,19 +794,19 @@ def test_mxfp4_dense_split_k_uneven_ranges(ntok):
 # Router-weighted combine of the per-slot outputs
 # ---------------------------------------------------------------------------
 
-def _combine_tol(ys, w, ids, E, want, bf16_out, slot_tol=None):
-    """fp32 fma chain over top_k slots: each step rounds once (2^-24 relative
-    of the running magnitude, bounded by sum|w y|); a bf16 result adds one ulp
-    (2^-8 relative). slot_tol: the bound on each per-slot input, weighted."""
+def _combine_tol(ys, w, ids, E, slot_err=None):
+    """Bound on the combine's fp32 result: the fma chain over top_k slots
+    rounds once per step (2^-24 relative of the running magnitude, bounded by
+    sum|w y|); slot_err bounds each stored per-slot input, weighted. The
+    stored result (bf16, fp16 or fp32) is checked against it by rounding
+    interval."""
     ntok, top_k, N = ys.shape
     valid = ((ids >= 0) & (ids < E)).astype(np.float64)[..., None]
     aw = np.abs(w.astype(np.float64))[..., None] * valid
     mag = (aw * np.abs(ys)).sum(axis=1)
     tol = mag * (top_k + 1) * 2.0 ** -24
-    if slot_tol is not None:
-        tol = tol + (aw * slot_tol).sum(axis=1)
-    if bf16_out:
-        tol = tol + np.abs(want) * 2.0 ** -8
+    if slot_err is not None:
+        tol = tol + (aw * slot_err).sum(axis=1)
     return tol
 
 
@@ -831,9 +837,7 @@ def test_combine(dtype, ntok, top_k, N):
     qmv.qmv_moe_combine(desc, ys, to_dev(w), to_dev(ids), ntok, top_k, y)
     want = oracle.moe_combine(ys_np, w, ids, E)
     got = bf16_to_np(y) if dtype == "bf16" else y.cpu().numpy().astype(np.float64)
-    tol = _combine_tol(ys_np, w, ids, E, want, dtype == "bf16")
-    err = np.abs(got - want)
-    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined outputs outside tolerance"
+    assert_within(got, want, _combine_tol(ys_np, w, ids, E), dtype, "combine")
     assert status_clean()
 
 
@@ -869,10 +873,10 @@ def test_layer_combine(pair, ntok, top_k):
     qmv.qmv_moe_layer_combine(gu.desc, gu.w, down.desc, down.w, xin, ids_d, w_d, ntok, top_k, ws, y)
     slots, slot_tol = _layer_expected(gu, down, ids, x=x, q=q, d=d)
     want = oracle.moe_combine(slots, w, ids, E)
-    tol = _combine_tol(slots, w, ids, E, want, dt == torch.bfloat16, slot_tol)
+    out = out_of(fmt_dn)
+    tol = _combine_tol(slots, w, ids, E, stored_err(slots, slot_tol, out))
     got = bf16_to_np(y) if dt == torch.bfloat16 else y.cpu().numpy().astype(np.float64)
-    err = np.abs(got - want)
-    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined layer outputs outside tolerance"
+    assert_within(got, want, tol, out, "combined layer")
     ws2 = torch.empty(qmv.qmv_moe_layer_workspace_bytes(gu.desc, ntok, top_k), dtype=torch.uint8, device=DEV)
     ys = torch.empty(ntok, top_k, K, dtype=dt, device=DEV)
     qmv.qmv_moe_layer(gu.desc, gu.w, down.desc, down.w, xin, ids_d, ntok, top_k, ws2, ys)

@@ -14,8 +14,8 @@ import qmv_inputs as qi
 pytestmark = pytest.mark.gpu
 
 qmv = pytest.importorskip("bit_quantized_moe_gb300")
-from qmv_testutil import (DEV, MX_SCALES, Matrices, assert_close, bf16_to_np,  # noqa: E402
-                          quantize_on_gpu, status_clean, to_dev)
+from qmv_testutil import (DEV, MX_SCALES, Matrices, assert_close, assert_within, bf16_to_np,  # noqa: E402
+                          out_of, quantize_on_gpu, status_clean, stored_err, to_dev)
 from test_gpu_parity import LUTS, GateUp, _combine_tol, _layer_expected  # noqa: E402
 
 
@@ -77,7 +77,7 @@ def test_verify_gather(fmt, ntok, top_k, per_slot):
             else:
                 ref = oracle.cb_matvec(m.codes[e], m.scales[e], m.lut, 16, q[v:v + 1], d[v:v + 1])[0]
                 absum = oracle.cb_abs_products(m.codes[e], m.scales[e], m.lut, 16, q[v:v + 1], d[v:v + 1])[0]
-            assert_close(got[t, j], ref, absum, fmt == "mxfp4", f"slot ({t},{j}) expert {e}")
+            assert_close(got[t, j], ref, absum, out_of(fmt), f"slot ({t},{j}) expert {e}")
     assert status_clean()
 
 
@@ -108,10 +108,10 @@ def test_verify_layer_combine(pair):
     qmv.qmv_moe_layer_combine(gu.desc, gu.w, down.desc, down.w, xin, to_dev(ids), to_dev(w), ntok, top_k, ws, y)
     slots, slot_tol = _layer_expected(gu, down, ids, x=x, q=q, d=d)
     want = oracle.moe_combine(slots, w, ids, E)
-    tol = _combine_tol(slots, w, ids, E, want, dt == torch.bfloat16, slot_tol)
+    out = out_of(fmt_dn)
+    tol = _combine_tol(slots, w, ids, E, stored_err(slots, slot_tol, out))
     got = bf16_to_np(y) if dt == torch.bfloat16 else y.cpu().numpy().astype(np.float64)
-    err = np.abs(got - want)
-    assert np.all(err <= tol + 1e-30), f"{(err > tol).sum()} combined outputs outside tolerance"
+    assert_within(got, want, tol, out, "combined layer")
     assert status_clean()
 
 

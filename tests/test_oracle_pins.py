@@ -8,6 +8,7 @@ invariants. The mutation tests at the end plant plausible mistakes in the
 oracle (on the CPU) and check that at least one pin fails for each.
 """
 import os
+import re
 import struct
 from fractions import Fraction
 
@@ -742,3 +743,266 @@ def test_mutation_mxfp8_group_16(monkeypatch):
         return O.e4m3_decode(codes) * O.e8m0_decode(scales)[..., g]
     monkeypatch.setattr(O, "mxfp8_dequant", bad)
     assert _fails_some_pin([pin_brute_force_mx_variants])
+
+
+# ---------------------------------------------------------------------------
+# Tolerance bases, gathered block sums and the MoE layer chain
+# ---------------------------------------------------------------------------
+
+def bf16_round_fraction(v: Fraction) -> int:
+    """Bit pattern of the bf16 nearest to the exact rational v (ties to even),
+    written from the bf16 bit layout (8 significant bits, exponent bias 127)."""
+    if v == 0:
+        return 0
+    s = 0x8000 if v < 0 else 0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                       # subnormals share the smallest exponent
+    ulp = Fraction(2) ** (e - 7)
+    m, rem = divmod(a, ulp)
+    m = int(m)
+    if rem > ulp / 2 or (rem == ulp / 2 and m % 2 == 1):
+        m += 1
+    if e == -126 and m < 128:
+        return s | m                       # subnormal (or rounds up into the normals: m == 128)
+    if m == 256:
+        m, e = 128, e + 1
+    assert e <= 127, "bf16 overflow in a pin input"
+    return s | ((e + 127) << 7) | (m - 128)
+
+
+def pin_bf16_round_fraction_helper():
+    """The helper above against torch's fp32 -> bf16 rounding on values that
+    fp32 holds exactly (so no double rounding can occur)."""
+    torch = pytest.importorskip("torch")
+    g = qi.rng(40)
+    f = (g.standard_normal(4000) * np.exp2(g.integers(-30, 30, 4000))).astype(np.float32)
+    f[:4] = [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 2.0 ** -130]   # ties and a subnormal
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for x, w in zip(f.tolist(), want.tolist()):
+        assert bf16_round_fraction(Fraction(x)) == w, x
+
+
+def brute_abs(elem_values, scales_f, group, act_values):
+    """sum_k |elem[k] * scale[k // group] * act[k]| for one row, exact."""
+    return sum(abs(elem_values[k] * scales_f[k // group] * act_values[k]) for k in range(len(elem_values)))
+
+
+def pin_abs_products():
+    """The tolerance base of every float parity check, sum_k |w[n, k] * x[v, k]|,
+    against an exact rational brute force over the decoded elements, for every
+    format and activation type on 1x32 and 4x64 matrices with several vectors.
+    Checked term by term: |w| and |x| are exact in float64, and a sum of 64
+    non-negative float64 terms is within 64 * 2^-53 of the exact sum."""
+    g = qi.rng(41)
+    rel = Fraction(1, 10 ** 13)
+    for N, K in ((1, 32), (4, 64)):
+        V = 3
+        for fmt in ("mxfp4", "mxfp8"):
+            for x_dtype in ("bf16", "f16"):
+                c = qi.format_codes(g, fmt, (N, K))
+                s = qi.e8m0(g, (N, K // 32))
+                x = qi.normal_bf16_bits(g, (V, K)) if x_dtype == "bf16" else qi.normal_f16_bits(g, (V, K))
+                x[:, 0] ^= 0x8000                               # a negative activation in every vector
+                elem = bf_e2m1 if fmt == "mxfp4" else bf_e4m3
+                act = bf_bf16 if x_dtype == "bf16" else bf_fp16
+                got_mx = O.mx_abs_products(fmt, c, s, x, x_dtype)
+                got_fmt = (O.mxfp4_abs_products if fmt == "mxfp4" else O.mxfp8_abs_products)(c, s, x, x_dtype)
+                assert got_mx.shape == (V, N) and np.array_equal(got_mx, got_fmt)
+                for v in range(V):
+                    av = [act(int(b)) for b in x[v]]
+                    for n in range(N):
+                        want = brute_abs([elem(int(k)) for k in c[n]], [bf_e8m0(int(e)) for e in s[n]], 32, av)
+                        assert abs(Fraction(float(got_mx[v, n])) - want) <= want * rel
+        for fmt, lut in (("cb2", qi.LUT_CB2), ("cb3", qi.LUT_CB3), ("cb4", qi.LUT_CB4)):
+            group = qi.FORMAT_GROUP[fmt]
+            c = qi.codes(g, (N, K), qi.FORMAT_BITS[fmt])
+            s = qi.e8m0(g, (N, K // group))
+            q, d = O.q8_1_quantize(qi.normal_f32(g, (V, K)))
+            got = O.cb_abs_products(c, s, lut, group, q, d)
+            assert got.shape == (V, N)
+            for v in range(V):
+                av = [int(q[v, k]) * bf_fp16(int(d[v, k // 32])) for k in range(K)]
+                for n in range(N):
+                    want = brute_abs([Fraction(lut[int(k)]) for k in c[n]],
+                                     [bf_e8m0(int(e)) for e in s[n]], group, av)
+                    assert abs(Fraction(float(got[v, n])) - want) <= want * rel
+
+
+def pin_cb_moe_block_sums():
+    """Gathered integer block sums and the gathered codebook matvec, shared and
+    per-slot activations, with an invalid id: per (t, j) against Python-integer
+    sums over the slot's expert and vector (x[t] shared, x[t * top_k + j]
+    per-slot); an invalid slot is all zero."""
+    g = qi.rng(42)
+    E, N, K = 3, 4, 64
+    ids = np.array([[2, 0], [1, 5], [0, 2]], dtype=np.int32)       # 5 is invalid
+    ntok, top_k = ids.shape
+    for fmt, lut in (("cb2", qi.LUT_CB2), ("cb3", qi.LUT_CB3), ("cb4", qi.LUT_CB4)):
+        group = qi.FORMAT_GROUP[fmt]
+        c = qi.codes(g, (E, N, K), qi.FORMAT_BITS[fmt])
+        s = qi.e8m0(g, (E, N, K // group))
+        q, d = O.q8_1_quantize(qi.normal_f32(g, (ntok * top_k, K)))
+        for per_slot in (False, True):
+            sums = O.cb_moe_block_sums(c, lut, group, q, ids, per_slot)
+            y = O.cb_moe_gather(c, s, lut, group, q, d, ids, per_slot)
+            assert sums.shape == (ntok, top_k, N, K // group)
+            for t in range(ntok):
+                for j in range(top_k):
+                    e = int(ids[t, j])
+                    v = t * top_k + j if per_slot else t
+                    if not 0 <= e < E:
+                        assert np.all(sums[t, j] == 0) and np.all(y[t, j] == 0)
+                        continue
+                    for n in range(N):
+                        cs = codes_from_packed(fmt, bytes(O.pack_codes(fmt, c[e])[n]), K)
+                        exact_y = Fraction(0)
+                        for h in range(K // group):
+                            want = sum(lut[cs[i]] * int(q[v, i]) for i in range(h * group, (h + 1) * group))
+                            assert int(sums[t, j, n, h]) == want
+                            exact_y += (want * bf_e8m0(int(s[e, n, h]))
+                                        * bf_fp16(int(d[v, (h * group) // 32])))
+                        absum = sum(abs(lut[cs[i]] * bf_e8m0(int(s[e, n, i // group])) * int(q[v, i])
+                                        * bf_fp16(int(d[v, i // 32]))) for i in range(K))
+                        assert abs(Fraction(float(y[t, j, n])) - exact_y) <= absum * Fraction(1, 10 ** 13)
+
+
+def pin_mxfp4_moe_layer():
+    """The MoE layer chain g, u -> h -> y on E = 3, N = K = 64 with an invalid
+    id, stage by stage: g and u are the exact rational gate/up products rounded
+    to bf16 (nearest even, by the bit-layout helper above); h is
+    silu(g) * u of those bf16 values (Python float arithmetic, math.exp) and
+    h_bits its bf16 rounding; y is the exact rational product of the down
+    expert of each slot with that slot's own h_bits row."""
+    import math
+    g = qi.rng(43)
+    E, N, K = 3, 64, 64
+    mats = [(qi.codes(g, (E, N, K), 4), qi.e8m0(g, (E, N, K // 32))) for _ in range(3)]
+    x = qi.normal_bf16_bits(g, (2, K))
+    ids = np.array([[2, 0], [1, 4]], dtype=np.int32)                # 4 is invalid
+    out = O.mxfp4_moe_layer(mats[0], mats[1], mats[2], x, ids)
+
+    def exact_row(m, e, n, act_bits):
+        cc, ss = m
+        return sum(bf_e2m1(int(cc[e, n, k])) * bf_e8m0(int(ss[e, n, k // 32])) * bf_bf16(int(act_bits[k]))
+                   for k in range(K))
+
+    for t in range(2):
+        for j in range(2):
+            e = int(ids[t, j])
+            row = out["h_rows_bits"][t * 2 + j]
+            assert np.array_equal(row, out["h_bits"][t, j])
+            if not 0 <= e < E:
+                assert np.all(out["y"][t, j] == 0)
+                continue
+            for n in range(N):
+                gb = bf16_round_fraction(exact_row(mats[0], e, n, x[t]))
+                ub = bf16_round_fraction(exact_row(mats[1], e, n, x[t]))
+                assert int(out["g_bits"][t, j, n]) == gb and int(out["u_bits"][t, j, n]) == ub
+                gv, uv = float(bf_bf16(gb)), float(bf_bf16(ub))
+                hv = gv / (1.0 + math.exp(-gv)) * uv
+                assert abs(out["h"][t, j, n] - hv) <= 1e-15 * abs(hv) + 1e-300
+                assert int(out["h_bits"][t, j, n]) == bf16_round_fraction(Fraction(float(out["h"][t, j, n])))
+            for n in range(N):
+                want = exact_row(mats[2], e, n, row)
+                absum = sum(abs(bf_e2m1(int(mats[2][0][e, n, k])) * bf_e8m0(int(mats[2][1][e, n, k // 32]))
+                                * bf_bf16(int(row[k]))) for k in range(K))
+                assert abs(Fraction(float(out["y"][t, j, n])) - want) <= absum * Fraction(1, 10 ** 13)
+
+
+NEW_PINS = [pin_bf16_round_fraction_helper, pin_abs_products, pin_cb_moe_block_sums, pin_mxfp4_moe_layer]
+
+
+@pytest.mark.parametrize("pin", NEW_PINS, ids=lambda f: f.__name__)
+def test_pin_chain(pin):
+    pin()
+
+
+def test_mutation_abs_dropped_from_x(monkeypatch):
+    def bad(codes, scales, x_bits, x_dtype="bf16"):
+        return O.act_bits_to_f64(x_bits, x_dtype) @ np.abs(O.mxfp4_dequant(codes, scales)).T
+    monkeypatch.setattr(O, "mxfp4_abs_products", bad)
+    assert _fails_some_pin([pin_abs_products])
+
+
+def test_mutation_abs_of_sum(monkeypatch):
+    def bad(codes, scales, lut, group, q, d_bits):
+        return np.abs(O.cb_matvec(codes, scales, lut, group, q, d_bits))
+    monkeypatch.setattr(O, "cb_abs_products", bad)
+    assert _fails_some_pin([pin_abs_products])
+
+
+def test_mutation_abs_d_not_repeated(monkeypatch):
+    def bad(codes, scales, lut, group, q, d_bits):
+        W = np.abs(O.cb_dequant(codes, scales, lut, group))
+        d = O.f16_bits_to_f64(d_bits)
+        K = codes.shape[-1]
+        xq = np.abs(np.asarray(q).astype(np.float64) * np.tile(d, K // 32))     # block b's d on the wrong weights
+        return xq @ W.T
+    monkeypatch.setattr(O, "cb_abs_products", bad)
+    assert _fails_some_pin([pin_abs_products])
+
+
+def test_mutation_mxfp8_abs_scale_dropped(monkeypatch):
+    def bad(codes, scales, x_bits, x_dtype="bf16"):
+        W = np.abs(O.e4m3_decode(codes))
+        return np.abs(O.act_bits_to_f64(x_bits, x_dtype)) @ W.T
+    monkeypatch.setattr(O, "mxfp8_abs_products", bad)
+    assert _fails_some_pin([pin_abs_products])
+
+
+def test_mutation_block_sums_slot_index(monkeypatch):
+    real = O.gather_vectors
+
+    def bad(ids, per_slot):
+        ntok, top_k = ids.shape
+        return [[(j * ntok + t) if per_slot else t for j in range(top_k)] for t in range(ntok)]
+    monkeypatch.setattr(O, "gather_vectors", bad)
+    assert real is not bad
+    assert _fails_some_pin([pin_cb_moe_block_sums])
+
+
+def test_mutation_layer_h_unrounded(monkeypatch):
+    real = O.f64_to_bf16_bits
+    calls = {"n": 0}
+
+    def bad(v):
+        calls["n"] += 1
+        if calls["n"] % 3 == 0:                     # the third rounding of each layer is h's
+            return (np.asarray(v, dtype=np.float64).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        return real(v)
+    monkeypatch.setattr(O, "f64_to_bf16_bits", bad)
+    assert _fails_some_pin([pin_mxfp4_moe_layer])
+
+
+def test_mutation_layer_down_shared_x(monkeypatch):
+    real = O.mxfp4_moe_gather
+
+    def bad(codes, scales, x_bits, ids, per_slot, x_dtype="bf16"):
+        if per_slot:
+            ntok, top_k = ids.shape
+            x_bits = x_bits[::top_k]                  # one h row per token instead of per slot
+        return real(codes, scales, x_bits, ids, False, x_dtype)
+    monkeypatch.setattr(O, "mxfp4_moe_gather", bad)
+    assert _fails_some_pin([pin_mxfp4_moe_layer])
+
+
+def test_every_oracle_function_is_pinned():
+    """Each public function of the oracle is exercised by some pin: named in
+    a pin's source, or called (transitively) by a function a pin names."""
+    import inspect
+    pins = ALL_PINS + NEW_PINS + [pin_combine, test_page_tables_decode]
+    text = "\n".join(inspect.getsource(p) for p in pins)
+    funcs = {n: f for n, f in vars(O).items()
+             if inspect.isfunction(f) and not n.startswith("_") and f.__module__ == O.__name__}
+    covered = {n for n in funcs if f"O.{n}(" in text}
+    frontier = list(covered)
+    while frontier:
+        body = inspect.getsource(funcs[frontier.pop()])
+        for n in funcs:
+            if n not in covered and re.search(rf"\b{n}\(", body):
+                covered.add(n)
+                frontier.append(n)
+    assert sorted(set(funcs) - covered) == []
