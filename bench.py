@@ -845,6 +845,177 @@ def run_profile_config(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Secondary ALU roofline: the matvec inner loop's compute rate
+# ---------------------------------------------------------------------------
+
+# weight bytes per weight of each format (codes + E8M0 bytes)
+BYTES_PER_WEIGHT = {"mxfp4": 4.25 / 8, "mxfp8": 8.25 / 8, "cb2": 2.5 / 8, "cb3": 3.5 / 8, "cb4": 4.25 / 8}
+ALU_CASES = (("mxfp4", 1), ("mxfp4", 2), ("mxfp4", 4), ("mxfp8", 1), ("mxfp8", 4), ("cb2", 1), ("cb3", 1),
+             ("cb3", 2), ("cb4", 1), ("cb4", 3), ("cb4", 4))
+
+
+def run_alu(args):
+    """For each (format, vectors per entry): the chunk routine's weights per
+    clock per SM at the production launch shape (two CTAs per SM), with no
+    copies or waits (qmv_debug_chunk_rate), beside the rate the measured HBM
+    bandwidth delivers for that format. Clocks are sampled during the runs;
+    the rate uses the median sampled SM clock."""
+    import torch
+
+    import bit_quantized_moe_gb300 as qmv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    hbm, hbm_kind = peaks()
+    sampler = ClockSampler(gpu_uuid(dev))
+    sampler.start()
+    time.sleep(0.3)
+    iters = 256
+    rows = []
+    wall0 = time.time()
+    for fmt, nv in ALU_CASES:
+        w, th = qmv.qmv_debug_chunk_rate(fmt, nv, 2, iters)
+        sink = torch.empty(th, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            qmv.qmv_debug_chunk_rate(fmt, nv, 2, iters, sink)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        ev0.record()
+        for _ in range(reps):
+            qmv.qmv_debug_chunk_rate(fmt, nv, 2, iters, sink)
+        ev1.record()
+        torch.cuda.synchronize()
+        rows.append((fmt, nv, w * reps / (ev0.elapsed_time(ev1) * 1e-3)))
+    time.sleep(0.3)
+    wall1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+    mhz = clocks.get("sm_mhz") or 2070.0
+    out = []
+    for fmt, nv, wps in rows:
+        rate = wps / sms / (mhz * 1e6)
+        need = hbm * 1e9 / BYTES_PER_WEIGHT[fmt] / sms / (mhz * 1e6)
+        out.append({"fmt": fmt, "vectors": nv, "weights_per_clk_per_sm": round(rate, 2),
+                    "hbm_rate_weights_per_clk_per_sm": round(need, 2), "compute_over_hbm": round(rate / need, 3)})
+        print(f"{fmt:6s} nv={nv}  {rate:7.2f} weights/clk/SM (compute only)   HBM at {hbm:.0f} GB/s ({hbm_kind}) "
+              f"needs {need:6.2f}   ratio {rate / need:5.2f}", flush=True)
+    print(json.dumps({"alu_roofline": out, "sm_mhz": mhz, "clocks": clocks, "sms": sms,
+                      "launch": "2 CTAs per SM of the production shape, chunk routine on a resident tile, "
+                                f"{iters} iterations per warp"}), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Phase probe: where the time of each launch of the step goes
+# ---------------------------------------------------------------------------
+
+PROBE_LAYERS = (10, 11, 12, 13)    # 8 launches: the probe buffer's 8 slots
+
+
+def run_phase_probe(args):
+    """Builds the phase-probe variant of the library (build.py --phase-probe)
+    and runs the step's graph in a child process that loads it: the launches
+    of four consecutive layers record per-warp %globaltimer stamps at the
+    phases of the matvec kernel. Prints, per launch, each phase's min /
+    median / max over all warps in us from the first probed launch's start,
+    then one JSON line of per-launch spans."""
+    if not os.environ.get("QMV_LIB"):
+        import importlib.util
+        spec = importlib.util.spec_from_file_location(
+            "qmv_build", os.path.join(ROOT, "bit_quantized_moe_gb300", "build.py"))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        lib = mod.build(phase_probe=True)
+        env = dict(os.environ, QMV_LIB=lib)
+        cmd = [sys.executable, os.path.abspath(__file__), "--phase-probe", "--warmup", str(args.warmup),
+               "--layers", str(args.layers)]
+        return subprocess.call(cmd, env=env)
+    import torch
+
+    import bit_quantized_moe_gb300 as qmv
+    L = args.layers
+    assert L > max(PROBE_LAYERS), "the probed layers must exist"
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pool_n = 32
+    g_canon, g_scales, x_bits = make_pool(pool_n, qi.CONFIG1_GATE.seed)
+    u_canon, u_scales, _ = make_pool(pool_n, qi.CONFIG1_UP.seed + 100)
+    d_canon, d_scales, _ = make_pool(pool_n, qi.CONFIG1_DOWN.seed + 200)
+    desc_gu, desc_dn = qmv.wdesc("mxfp4", N, K, E), qmv.wdesc("mxfp4", K, N, E)
+    eb_gu, eb_dn = qmv.qmv_packed_gate_up_expert_bytes(desc_gu), qmv.qmv_packed_expert_bytes(desc_dn)
+    pool_gu = torch.from_numpy(qmv.qmv_pack_gate_up(qmv.wdesc("mxfp4", N, K, pool_n), g_canon, g_scales,
+                                                    u_canon, u_scales)).to(dev).view(pool_n, eb_gu)
+    pool_dn = torch.from_numpy(qmv.qmv_pack_weights(qmv.wdesc("mxfp4", K, N, pool_n), d_canon,
+                                                    d_scales)).to(dev).view(pool_n, eb_dn)
+    W_gu = torch.empty(L * E, eb_gu, dtype=torch.uint8, device=dev)
+    W_gu.view(-1, pool_n, eb_gu).copy_(pool_gu.unsqueeze(0).expand(L * E // pool_n, pool_n, eb_gu))
+    W_dn = torch.empty(L * E, eb_dn, dtype=torch.uint8, device=dev)
+    W_dn.view(-1, pool_n, eb_dn).copy_(pool_dn.unsqueeze(0).expand(L * E // pool_n, pool_n, eb_dn))
+    W_gu, W_dn = W_gu.view(L, E * eb_gu), W_dn.view(L, E * eb_dn)
+    x_dev = torch.from_numpy(x_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    g = qi.rng(1000)
+    ids = torch.from_numpy(np.stack([qi.topk_ids(g, 1, TOP_K, E) for _ in range(L)])).to(dev)
+    ws = torch.zeros(qmv.qmv_moe_layer_workspace_bytes(desc_gu, 1, TOP_K), dtype=torch.uint8, device=dev)
+    y = torch.empty(L, 1, TOP_K, K, dtype=torch.bfloat16, device=dev)
+
+    def step(probe):
+        for l in range(L):
+            if probe:
+                qmv.qmv_debug_phase_probe(l in PROBE_LAYERS)
+            qmv.qmv_moe_layer(desc_gu, W_gu[l], desc_dn, W_dn[l], x_dev, ids[l], 1, TOP_K, ws, y[l],
+                              qmv.QMV_FLAG_PREFETCH_INPUTS)
+        if probe:
+            qmv.qmv_debug_phase_probe(False)
+
+    step(False)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(False)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(True)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    qmv.qmv_debug_phase_read("mxfp4", clear=True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    graph.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    t = qmv.qmv_debug_phase_read("mxfp4", clear=True).astype(np.int64)
+    print(f"phase probe: {L} layers, step {ev0.elapsed_time(ev1) * 1e3:.1f} us "
+          f"({ev0.elapsed_time(ev1) * 1e3 / L:.2f} us per layer, probe build); layers {PROBE_LAYERS} probed, "
+          f"us from the first probed launch's earliest start; min / median / max over warps", flush=True)
+    starts = t[0, :, :, 0]
+    base = starts[starts > 0].min()
+    spans = []
+    for slot in range(8):
+        a = t[slot]
+        w = a[a[:, :, 0] > 0]
+        kind = "gate/up" if slot % 2 == 0 else "down"
+        print(f"launch {slot} ({kind}, layer {PROBE_LAYERS[slot // 2]}): {int((a[:, 0, 0] > 0).sum())} CTAs, "
+              f"{len(w)} warps")
+        row = {"launch": slot, "kind": kind}
+        for k, name in enumerate(qmv.PHASES):
+            c = w[:, k]
+            c = c[c > 0]
+            if len(c) == 0:
+                continue
+            lo, med, hi = (c.min() - base) / 1e3, (np.median(c) - base) / 1e3, (c.max() - base) / 1e3
+            row[name] = [round(lo, 2), round(med, 2), round(hi, 2)]
+            print(f"  {name:12s} n={len(c):5d} {lo:8.2f} {med:8.2f} {hi:8.2f}")
+        spans.append(row)
+    print(json.dumps({"phase_probe": spans}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -857,6 +1028,10 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers held on the device (the reported workload is 24; smaller for ncu captures)")
     ap.add_argument("--digest", action="store_true", help="print the kernel source digest and exit")
+    ap.add_argument("--alu", action="store_true",
+                    help="the chunk routine's compute rate per format (secondary ALU roofline) and exit")
+    ap.add_argument("--phase-probe", action="store_true",
+                    help="build the phase-probe variant and print where each launch's time goes")
     ap.add_argument("--configs", action="store_true",
                     help="measure every config of the workload set (one JSON line per call type) and exit")
     ap.add_argument("--profile-config", type=int, choices=[0, 2, 3, 4, 5, 6], default=None,
@@ -870,6 +1045,10 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.phase_probe:
+        return run_phase_probe(args)
+    if args.alu:
+        return run_alu(args)
     if args.configs:
         return run_configs(args)
     if args.profile_config is not None:

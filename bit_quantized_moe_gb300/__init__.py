@@ -19,7 +19,9 @@ import numpy as np
 import torch  # noqa: F401  (load PyTorch's CUDA runtime first; libqmv binds to the same one)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libqmv.so")
+# QMV_LIB selects another build of the same library (the phase-probe variant
+# that bench.py --phase-probe builds); the default is the in-tree product build.
+LIB_PATH = os.environ.get("QMV_LIB") or os.path.join(_PKG, "_build", "libqmv.so")
 
 QMV_OK = 0
 QMV_EINVAL = -1
@@ -48,7 +50,9 @@ EXPORTS = (
     "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
     "qmv_moe_layer_noalloc", "qmv_moe_combine", "qmv_moe_combine_ex", "qmv_moe_layer_combine_workspace_bytes", "qmv_moe_layer_combine",
     "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_dequant", "qmv_debug_plan",
-    "qmv_device_status", "qmv_debug_wait_probe", "qmv_last_error", "qmv_version",
+    "qmv_device_status", "qmv_debug_wait_probe", "qmv_debug_chunk_rate", "qmv_debug_phase_entries",
+    "qmv_debug_phase_probe",
+    "qmv_debug_phase_read", "qmv_last_error", "qmv_version",
 )
 
 
@@ -114,6 +118,11 @@ def _load() -> ctypes.CDLL:
                                           ctypes.POINTER(I64), I32]),
         "qmv_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32]),
         "qmv_debug_wait_probe": (ctypes.c_int, [ctypes.c_uint64, P]),
+        "qmv_debug_chunk_rate": (ctypes.c_int, [I32, I32, I32, I32, P, SZ, ctypes.POINTER(I64),
+                                                ctypes.POINTER(I64), P]),
+        "qmv_debug_phase_entries": (SZ, []),
+        "qmv_debug_phase_probe": (ctypes.c_int, [I32]),
+        "qmv_debug_phase_read": (ctypes.c_int, [I32, P, SZ, I32]),
         "qmv_last_error": (ctypes.c_char_p, []),
         "qmv_version": (ctypes.c_char_p, []),
     }
@@ -351,6 +360,36 @@ def qmv_device_status(clear: bool = False) -> int:
 
 def qmv_debug_wait_probe(limit_ns: int, stream=None) -> None:
     _check(lib.qmv_debug_wait_probe(int(limit_ns), _stream(stream)))
+
+
+def qmv_debug_chunk_rate(fmt, nv: int, ctas_per_sm: int, iters: int, sink=None, stream=None):
+    """Launches the compute-rate probe (or, with sink None, only sizes it);
+    returns (matrix weights per launch, threads = sink entries)."""
+    w, t = ctypes.c_int64(0), ctypes.c_int64(0)
+    f = FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib.qmv_debug_chunk_rate(f, nv, ctas_per_sm, iters, _ptr(sink), _nbytes(sink) if sink is not None else 0,
+                                    ctypes.byref(w), ctypes.byref(t), _stream(stream)))
+    return w.value, t.value
+
+
+PHASES = ("start", "work_list", "early_tiles", "dep_wait", "act_loads", "ring_issued", "act_staged",
+          "tile0_ready", "tile0_done", "tile1_ready", "tile2_ready", "last_done", "end")
+
+
+def qmv_debug_phase_probe(enable: bool) -> None:
+    """Record the phases of the matvec launches made from now on (phase-probe
+    build only; raises QmvError in the product build)."""
+    _check(lib.qmv_debug_phase_probe(1 if enable else 0))
+
+
+def qmv_debug_phase_read(fmt, clear: bool = True) -> np.ndarray:
+    """The format's phase stamps, uint64 ns [slot][cta][warp][phase] (0 = not
+    recorded). Synchronizes the device."""
+    n = lib.qmv_debug_phase_entries()
+    out = np.zeros(n, dtype=np.uint64)
+    f = FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib.qmv_debug_phase_read(f, out.ctypes.data, n, 1 if clear else 0))
+    return out.reshape(8, 512, 16, 16)
 
 
 def qmv_last_error() -> str:

@@ -54,7 +54,7 @@ cudaError_t launch_quantize_q8(const float* x, int nvec, int K, void* xq, cudaSt
 }
 
 // ---------------------------------------------------------------------------
-// SwiGLU: h = silu(g) * u, silu(z) = z / (1 + exp(-z)), fp32 arithmetic.
+// SwiGLU: h = silu(g) * u, silu(z) = z / (1 + exp(-z)), fp32 arithmetic (swiglu_f32).
 // ---------------------------------------------------------------------------
 __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ u,
                               __nv_bfloat16* __restrict__ h, int64_t n) {
@@ -70,12 +70,12 @@ __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ g, const __nv_bf
     __nv_bfloat16* he = reinterpret_cast<__nv_bfloat16*>(&hv);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      he[k] = __float2bfloat16_rn(silu_f32(__bfloat162float(ge[k])) * __bfloat162float(ue[k]));
+      he[k] = __float2bfloat16_rn(swiglu_f32(__bfloat162float(ge[k]), __bfloat162float(ue[k])));
     }
     reinterpret_cast<uint4*>(h)[i] = hv;
   }
   for (int64_t i = n8 * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    h[i] = __float2bfloat16_rn(silu_f32(__bfloat162float(g[i])) * __bfloat162float(u[i]));
+    h[i] = __float2bfloat16_rn(swiglu_f32(__bfloat162float(g[i]), __bfloat162float(u[i])));
   }
   pdl_launch_dependents();
 }

@@ -16,6 +16,7 @@
 
 namespace qmv {
 thread_local const char* g_launch_stage = "";
+bool g_phase_probe_on = false;
 
 void pack_expert(const Geometry& g, const uint8_t* codes, const uint8_t* scales, uint8_t* out);
 void pack_gate_up_expert(const Geometry& g, int N, const uint8_t* gate_codes, const uint8_t* gate_scales,
@@ -181,8 +182,9 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   a.stream = stream;
   const bool verify = verify_supported(a);
   if (gather && ntok * top_k > QMV_MAX_LAYER_SLOTS && !verify)
-    return fail(QMV_EINVAL, "%s: more than %d routed slots need an MX format with bf16 activations (the "
-                "sorted tensor-core gather)", name, QMV_MAX_LAYER_SLOTS);
+    return fail(QMV_EINVAL, "%s: more than %d routed slots run the sorted tensor-core gather, which takes "
+                "bf16 (MX) or q8_1 / fp32 (codebook) activations, not fp16 and not the gate/up fusion", name,
+                QMV_MAX_LAYER_SLOTS);
   const DevInfo* di = dev_info();
   if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
   if (verify) return QMV_OK;   // tensor-core path, fixed shared memory
@@ -561,6 +563,74 @@ int qmv_device_status(uint32_t* flags, int32_t clear) {
   }
   *flags = v;
   return ok();
+}
+
+int qmv_debug_chunk_rate(int32_t fmt, int32_t nv, int32_t ctas_per_sm, int32_t iters, float* sink,
+                         size_t sink_bytes, int64_t* weights, int64_t* threads, void* stream) {
+  const char* name = "qmv_debug_chunk_rate";
+  if (fmt < 0 || fmt >= kNumFmts) return fail(QMV_EINVAL, "%s: unknown format %d", name, fmt);
+  if (nv < 1 || nv > 4) return fail(QMV_EINVAL, "%s: nv=%d outside [1, 4]", name, nv);
+  if (ctas_per_sm < 1 || ctas_per_sm > 2) return fail(QMV_EINVAL, "%s: ctas_per_sm=%d outside [1, 2]", name, ctas_per_sm);
+  if (iters < 1 || iters > (1 << 20)) return fail(QMV_EINVAL, "%s: iters=%d outside [1, 2^20]", name, iters);
+  if (!weights || !threads) return fail(QMV_EINVAL, "%s: NULL output pointer", name);
+  if (sink != nullptr && !aligned16(sink)) return fail(QMV_EALIGN, "%s: sink must be 16-byte aligned", name);
+  if (dev_info() == nullptr) return cuda_fail(cudaGetLastError(), name);
+  int64_t w = 0, t = 0;
+  cudaError_t (*fn)(int, int, int, float*, int64_t*, int64_t*, cudaStream_t) = nullptr;
+  switch (fmt) {
+    case MXFP4: fn = launch_chunk_rate_mxfp4; break;
+    case MXFP8: fn = launch_chunk_rate_mxfp8; break;
+    case CB2: fn = launch_chunk_rate_cb2; break;
+    case CB3: fn = launch_chunk_rate_cb3; break;
+    default: fn = launch_chunk_rate_cb4; break;
+  }
+  cudaError_t e = fn(nv, ctas_per_sm, iters, nullptr, &w, &t, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  *weights = w;
+  *threads = t;
+  if (sink == nullptr) return ok();
+  if (sink_bytes < (size_t)t * sizeof(float)) return fail(QMV_ESIZE, "%s: sink %zu bytes < %zu", name, sink_bytes,
+                                                          (size_t)t * sizeof(float));
+  e = fn(nv, ctas_per_sm, iters, sink, &w, &t, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+size_t qmv_debug_phase_entries(void) { return (size_t)kProbeSlots * kProbeCtas * kProbeWarps * kPhases; }
+
+int qmv_debug_phase_probe(int32_t enable) {
+#ifdef QMV_PHASE_PROBE
+  g_phase_probe_on = enable != 0;
+  return ok();
+#else
+  (void)enable;
+  return fail(QMV_EINVAL, "qmv_debug_phase_probe: this library was built without the phase probe "
+              "(build.py --phase-probe builds the variant that has it)");
+#endif
+}
+
+int qmv_debug_phase_read(int32_t fmt, uint64_t* out, size_t n, int32_t clear) {
+  if (!out) return fail(QMV_EINVAL, "qmv_debug_phase_read: NULL pointer");
+  if (n < qmv_debug_phase_entries()) return fail(QMV_ESIZE, "qmv_debug_phase_read: %zu entries < %zu", n,
+                                                 qmv_debug_phase_entries());
+#ifdef QMV_PHASE_PROBE
+  unsigned long long* o = reinterpret_cast<unsigned long long*>(out);
+  int rc = -1;
+  switch (fmt) {
+    case QMV_MXFP4: rc = phase_mxfp4(o, n, clear); break;
+    case QMV_MXFP8: rc = phase_mxfp8(o, n, clear); break;
+    case QMV_CB2: rc = phase_cb2(o, n, clear); break;
+    case QMV_CB3: rc = phase_cb3(o, n, clear); break;
+    case QMV_CB4: rc = phase_cb4(o, n, clear); break;
+    default: return fail(QMV_EINVAL, "qmv_debug_phase_read: unknown format %d", fmt);
+  }
+  if (rc != 0) return cuda_fail(cudaGetLastError(), "qmv_debug_phase_read");
+  return ok();
+#else
+  (void)fmt;
+  (void)clear;
+  return fail(QMV_EINVAL, "qmv_debug_phase_read: this library was built without the phase probe");
+#endif
 }
 
 int qmv_debug_wait_probe(uint64_t limit_ns, void* stream) {

@@ -45,6 +45,18 @@ cudaError_t launch_matvec_cb3(const MatvecArgs& a);
 cudaError_t launch_matvec_cb4(const MatvecArgs& a);
 cudaError_t launch_matvec_mxfp8(const MatvecArgs& a);
 
+// Compute-rate probe of the chunk routine (qmv_debug_chunk_rate).
+cudaError_t launch_chunk_rate_mxfp4(int nv, int ctas_per_sm, int iters, float* sink, int64_t* weights,
+                                    int64_t* threads, cudaStream_t s);
+cudaError_t launch_chunk_rate_mxfp8(int nv, int ctas_per_sm, int iters, float* sink, int64_t* weights,
+                                    int64_t* threads, cudaStream_t s);
+cudaError_t launch_chunk_rate_cb2(int nv, int ctas_per_sm, int iters, float* sink, int64_t* weights,
+                                  int64_t* threads, cudaStream_t s);
+cudaError_t launch_chunk_rate_cb3(int nv, int ctas_per_sm, int iters, float* sink, int64_t* weights,
+                                  int64_t* threads, cudaStream_t s);
+cudaError_t launch_chunk_rate_cb4(int nv, int ctas_per_sm, int iters, float* sink, int64_t* weights,
+                                  int64_t* threads, cudaStream_t s);
+
 // Dense verify batches of the MX formats (5..16 bf16 tokens) on the tensor
 // cores: whether a call takes that path, and its launcher.
 bool verify_supported(const MatvecArgs& a);
@@ -60,6 +72,37 @@ cudaError_t launch_dequant(int fmt, int N, int K, const void* w, const uint32_t 
                            cudaStream_t s);
 
 cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t s);
+
+// Phase probe (build variant -DQMV_PHASE_PROBE, never the product build):
+// lane 0 of every warp records %globaltimer at the phases of a launch into
+// g_phase[launch slot][CTA][warp][phase], for the launches made while the
+// probe is enabled (qmv_debug_phase_probe), slots dealt in launch order. The
+// phases (kPh*) run from kernel start to the warp's end.
+enum : int {
+  kPhStart = 0,        // kernel entry
+  kPhWorkList = 1,     // work list built (first CTA barrier passed)
+  kPhEarlyTiles = 2,   // tile copies before griddepcontrol.wait issued
+  kPhDepWait = 3,      // griddepcontrol.wait returned
+  kPhActLoads = 4,     // first round of activation loads issued
+  kPhRingIssued = 5,   // every ring stage's first tile copy issued
+  kPhActStaged = 6,    // activations staged (CTA barrier passed)
+  kPhTile0Ready = 7,   // first tile landed
+  kPhTile0Done = 8,    // first tile computed
+  kPhTile1Ready = 9,
+  kPhTile2Ready = 10,
+  kPhLastDone = 11,    // last tile computed
+  kPhEnd = 12,         // warp done (after its stores)
+  kPhases = 16
+};
+constexpr int kProbeSlots = 8, kProbeCtas = 512, kProbeWarps = 16;
+
+// Phase probe (probe build only): launches made while on record their phases.
+extern bool g_phase_probe_on;
+int phase_mxfp4(unsigned long long* out, size_t n, int clear);
+int phase_mxfp8(unsigned long long* out, size_t n, int clear);
+int phase_cb2(unsigned long long* out, size_t n, int clear);
+int phase_cb3(unsigned long long* out, size_t n, int clear);
+int phase_cb4(unsigned long long* out, size_t n, int clear);
 
 uint32_t status_act(int clear);
 uint32_t status_mxfp4(int clear);

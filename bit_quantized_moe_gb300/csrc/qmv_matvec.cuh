@@ -43,6 +43,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "qmv_device.cuh"
@@ -94,6 +95,10 @@ inline int launch_vectors(bool gather, int ntok) {
   return ntok < cap ? ntok : cap;
 }
 constexpr int kMaxEntries = 32;  // routed slots (ntok * top_k) of a gather; dense entries <= 16 / 4
+
+#ifdef QMV_PHASE_PROBE
+static __device__ unsigned long long g_phase[kProbeSlots * kProbeCtas * kProbeWarps * kPhases];
+#endif
 constexpr int kMaxDevices = 64;
 
 struct Entry {
@@ -124,7 +129,22 @@ struct KParams {
   int splits;             // K ranges per item (split-K inside a CTA), >= 1
   int split_chunks;       // chunks per K range (the last may be shorter)
   int items_per_cta;      // upper bound on items per CTA (split-K partial slots)
+#ifdef QMV_PHASE_PROBE
+  int probe_slot;         // launch slot of the phase probe, -1 = not recorded
+#endif
 };
+
+__device__ __forceinline__ void probe_phase(const KParams& p, int k) {
+#ifdef QMV_PHASE_PROBE
+  if ((threadIdx.x & 31) == 0 && p.probe_slot >= 0 && blockIdx.x < kProbeCtas && (threadIdx.x >> 5) < kProbeWarps) {
+    g_phase[(((size_t)p.probe_slot * kProbeCtas + blockIdx.x) * kProbeWarps + (threadIdx.x >> 5)) * kPhases + k] =
+        global_timer_ns();
+  }
+#else
+  (void)p;
+  (void)k;
+#endif
+}
 
 // KParams::flags
 constexpr uint32_t kFlagPrefetch = 1u;   // weights and ids are not written by the preceding kernel
@@ -401,7 +421,9 @@ constexpr int kStageU = 2;
 // so every product w * x' (E2M1 times f16) and its fp32 accumulation match
 // fp32 arithmetic on the bf16 input, and dot * 2^-s undoes the shift exactly.
 // One thread converts one group (64 bytes of bf16).
-__device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* dst_bytes, float* xinv_slot) {
+// Converts one group (32 bf16 values in 16 words) in place to shifted f16
+// and returns 2^-s.
+__device__ __forceinline__ float shift_group_to_f16(uint32_t (&w)[16]) {
   uint32_t m8[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -424,10 +446,15 @@ __device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* 
     const __half2 h2 = __floats2half2_rn(lo, hi);
     w[i] = *reinterpret_cast<const uint32_t*>(&h2);
   }
+  return pow2f(-sh);
+}
+
+__device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* dst_bytes, float* xinv_slot) {
+  const float inv = shift_group_to_f16(w);
   uint4* dst = reinterpret_cast<uint4*>(dst_bytes);
 #pragma unroll
   for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-  *xinv_slot = pow2f(-sh);
+  *xinv_slot = inv;
 }
 
 // Each staging function issues the loads of its first round (every thread's
@@ -489,13 +516,12 @@ __device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, flo
 // q = round_half_away(x * (1 / d)) clamped to +-127, d stored as fp16 (RNE);
 // the same IEEE-rounded fp32 operations as the standalone quantizer, so the
 // result equals quantizing first and passing q8_1.
-__device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t* out, int K, int blk) {
+__device__ __forceinline__ float q8_block(const float (&f)[32], uint32_t (&qw)[8]) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
   const float d = __fdiv_rn(amax, 127.0f);
   const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-  uint32_t qw[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     uint32_t word = 0;
@@ -507,6 +533,12 @@ __device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t*
     }
     qw[i] = word;
   }
+  return d;
+}
+
+__device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t* out, int K, int blk) {
+  uint32_t qw[8];
+  const float d = q8_block(f, qw);
   uint4* dst = reinterpret_cast<uint4*>(out + (size_t)blk * 32);
   dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
   dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
@@ -806,7 +838,22 @@ __device__ __forceinline__ void rs_step(float* v, int lane) {
   }
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+// SwiGLU h = silu(z) * u, silu(z) = z / (1 + exp(-z)), in fp32 with no
+// intermediate that overflows or falls into fp32's subnormal range (where
+// exp(z) keeps only a few significant bits, and multiplying by z * u would
+// magnify that loss): for z < 0 as z * t / (1 + t) * u with t = exp(z); for
+// z <= -80, where 1 + t rounds to 1, as (z * exp(z + 80)) * (u * e^-80) --
+// z + 80 is exact (z <= -80 has an ulp of at least 2^-17, which z + 80 keeps)
+// and both factors stay normal, so only the final product rounds into the
+// subnormals.
+__device__ __forceinline__ float swiglu_f32(float z, float u) {
+  if (z >= 0.0f) return z / (1.0f + expf(-z)) * u;
+  if (z > -80.0f) {
+    const float t = expf(z);
+    return z * t / (1.0f + t) * u;
+  }
+  return (z * expf(z + 80.0f)) * (u * 1.8048513878454153e-35f);   // e^-80
+}
 
 template <int FMT, bool XH>
 __device__ __forceinline__ void store_out(const KParams& p, size_t o, float val) {
@@ -846,7 +893,7 @@ __device__ __forceinline__ void store_lanes(const KParams& p, const Entry& e, in
     const float up = __shfl_xor_sync(0xffffffffu, val, 16);   // row r + 4 (same vector) lives 16 lanes up
     const int row = rt * (kRows / 2) + r;
     if (lane % S == 0 && r < kRows / 2 && v < NVV && row < p.out_n) {
-      store_out<FMT, XH>(p, (size_t)e.slot[v] * p.out_n + row, silu_f32(val) * up);
+      store_out<FMT, XH>(p, (size_t)e.slot[v] * p.out_n + row, swiglu_f32(val, up));
     }
   } else {
     const int row = rt * kRows + r;
@@ -878,6 +925,9 @@ __device__ __forceinline__ bool run_task(const KParams& p, const Entry& e, int r
     const uint32_t parity = (uint32_t)(q / ST) & 1u;
     bool ok = mbar_wait_bounded(wp.bars + 8u * s, parity, kWaitLimitNs);
     if (!__all_sync(0xffffffffu, ok)) return false;
+    if (q == 0) probe_phase(p, kPhTile0Ready);
+    if (q == 1) probe_phase(p, kPhTile1Ready);
+    if (q == 2) probe_phase(p, kPhTile2Ready);
     const int L = (c == p.chunks - 1) ? p.last_lanes : 32;
     const uint8_t* st = wp.ring_ptr + (size_t)s * p.full_tile;
     if (lane < L) {
@@ -891,8 +941,10 @@ __device__ __forceinline__ bool run_task(const KParams& p, const Entry& e, int r
     }
     fence_proxy_async_smem();
     __syncwarp();
+    if (q == 0) probe_phase(p, kPhTile0Done);
     if (lane == 0) issue_next<ST>(wp);
   }
+  probe_phase(p, kPhLastDone);
   float val = reduce_lanes<NVP>(acc);
   if (p.splits > 1) {
     constexpr int M = kRows * NVP;
@@ -982,6 +1034,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   __shared__ int s_ids[kMaxEntries];
   __shared__ int s_vlist[kMaxEntries];   // activation vectors this CTA's items use
   __shared__ int s_nvl;
+  probe_phase(p, kPhStart);
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * ST; ++i) mbar_init(smem_addr(&bars[i]), 1);
     fence_mbar_init();
@@ -1004,6 +1057,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     if (lane == 0) s_nent = n;
   }
   __syncthreads();
+  probe_phase(p, kPhWorkList);
 
   WarpPipe wp;
   wp.p = &p;
@@ -1027,6 +1081,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     if (lane == 0) issue_next<ST>(wp);
     __syncthreads();
   }
+  probe_phase(p, kPhEarlyTiles);
   // Per-slot gathers stage only the vectors of the entries the CTA's
   // contiguous item range touches (listed here, after the first tile copies
   // are out); other calls stage all vectors. A vector is staged at its own
@@ -1070,6 +1125,7 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   const int nvl = p.contig ? s_nvl : p.nvec;
   const bool compact = p.x_slots < p.nvec;
   if (early) pdl_wait();
+  probe_phase(p, kPhDepWait);
   // Dependents are released only after this kernel's own wait, so when one
   // starts, every kernel before this one is complete (what
   // QMV_FLAG_PREFETCH_INPUTS relies on).
@@ -1090,10 +1146,12 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
   // Activations: plain 16-byte loads by every thread (they do not queue
   // behind the tile copies), converted on the way for MXFP4.
   auto issue_rest = [&]() {
+    probe_phase(p, kPhActLoads);
     for (int q = pre; q < ST; ++q) {
       if (lane == 0) issue_next<ST>(wp);
       __syncthreads();
     }
+    probe_phase(p, kPhRingIssued);
   };
   if constexpr (fmt_is_mx(FMT) && ALT) {
     stage_x_copy(p.x, xs, vlist, compact, nvl, p.x_vec_bytes, issue_rest);
@@ -1106,12 +1164,14 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     stage_x_copy(p.x, xs, vlist, compact, nvl, p.x_vec_bytes, issue_rest);
   }
   __syncthreads();
+  probe_phase(p, kPhActStaged);
 
   int q = 0;
   if (!run_tasks<FMT, NV, ALT, ST>(p, q, wp, xs, xinv, part, cnt)) {
     if (lane == 0) set_status(kStatusWaitTile);
     drain_ring<ST>(wp, q);
   }
+  probe_phase(p, kPhEnd);
 }
 
 // ---------------------------------------------------------------------------
@@ -1218,6 +1278,9 @@ inline KParams make_params(const MatvecArgs& a) {
   p.splits = 1;
   p.split_chunks = g.chunks;
   p.items_per_cta = 0;
+#ifdef QMV_PHASE_PROBE
+  p.probe_slot = -1;
+#endif
   return p;
 }
 
@@ -1280,6 +1343,12 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
     g_launch_stage = "shared memory limit";
     if (plan.smem.total > device_max_smem_optin()) return cudaErrorInvalidValue;
   }
+#ifdef QMV_PHASE_PROBE
+  {
+    static std::atomic<int> next_slot{0};
+    if (g_phase_probe_on) p.probe_slot = next_slot.fetch_add(1) % kProbeSlots;
+  }
+#endif
   p.splits = plan.splits;
   p.split_chunks = plan.split_chunks;
   p.items_per_cta = plan.items_per_cta;
@@ -1304,4 +1373,122 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// ---------------------------------------------------------------------------
+// Compute-rate probe (diagnostic export qmv_debug_chunk_rate): every warp
+// applies the format's chunk routine, `iters` times, to a tile resident in
+// shared memory -- the matvec's inner loop with no copies and no waits -- so
+// that the weights per clock per SM of the arithmetic alone can be set beside
+// the rate the HBM stream delivers. A compiler barrier per iteration keeps
+// the loads and the decode inside the loop.
+// ---------------------------------------------------------------------------
+
+template <int FMT, int NV>
+__global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
+    chunk_rate_kernel(const __grid_constant__ KParams p, int iters, float* sink) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NVP = (NV == 3) ? 4 : NV;
+  const int warp = threadIdx.x >> 5;
+  uint8_t* xs = smem;
+  float* xinv = reinterpret_cast<float*>(smem + NV * p.x_vec_bytes);
+  uint8_t* tiles = smem + round_up_u32(NV * p.x_vec_bytes + NV * 32 * 4, 128);
+  const uint32_t code_bytes = tile_code_bytes(FMT, 32);
+  for (uint32_t i = threadIdx.x; i < NV * p.x_vec_bytes; i += blockDim.x) {
+    // activations: f16 near 1 (MX formats), q8_1 codes in [-63, 63] and d = 1/64 (codebooks)
+    if constexpr (fmt_is_mx(FMT)) {
+      xs[i] = (i & 1) ? 0x3c : (uint8_t)(i * 29);
+    } else {
+      const uint32_t k = i % p.x_vec_bytes;
+      xs[i] = (k < (uint32_t)p.K) ? (uint8_t)((int8_t)((int)(k * 37 % 127) - 63)) : ((k & 1) ? 0x24 : 0x00);
+    }
+  }
+  for (int i = threadIdx.x; i < NV * 32; i += blockDim.x) xinv[i] = 1.0f / 16384.0f;
+  for (uint32_t i = threadIdx.x; i < Shape<NV>::warps * p.full_tile; i += blockDim.x) {
+    const uint32_t k = i % p.full_tile;
+    tiles[i] = (k >= code_bytes) ? 127 : (uint8_t)(i * 37 + 11);   // scale bytes 2^0
+  }
+  __syncthreads();
+  Entry e;
+  e.expert = 0;
+  e.nv = NV;
+  for (int v = 0; v < 4; ++v) e.vec[v] = e.slot[v] = (v < NV) ? v : 0;
+  float acc[kRows * NVP];
+#pragma unroll
+  for (int i = 0; i < kRows * NVP; ++i) acc[i] = 0.f;
+  const uint8_t* st = tiles + (size_t)warp * p.full_tile;
+  for (int it = 0; it < iters; ++it) {
+    if constexpr (FMT == MXFP4) {
+      chunk_mxfp4<NV, NVP>(p, e, 0, 32, st, xs, xinv, acc);
+    } else if constexpr (FMT == MXFP8) {
+      chunk_mxfp8<NV, NVP>(p, e, 0, 32, st, xs, xinv, acc);
+    } else {
+      chunk_cb<FMT, NV, NVP, false>(p, e, 0, 0, 32, st, xs, acc);
+    }
+    asm volatile("" ::: "memory");
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRows * NVP; ++i) sum += acc[i];
+  sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = sum;
+}
+
+// Launches sms x ctas_per_sm CTAs of the production launch shape for NV
+// vectors; *weights = matrix weights the launch processes (each applied to
+// NV vectors), *threads = threads launched (sink entries).
+template <int FMT, int NV>
+cudaError_t launch_chunk_rate_nv(int ctas_per_sm, int iters, float* sink, int64_t* weights, int64_t* threads,
+                                 cudaStream_t s) {
+  KParams p{};
+  const Geometry g = make_geometry(FMT, kRows, kChunkK);
+  p.K = kChunkK;
+  p.x_vec_bytes = fmt_is_mx(FMT) ? (uint32_t)kChunkK * 2u : (uint32_t)q8_vec_bytes(kChunkK);
+  p.full_tile = g.full_tile;
+  p.chunks = 1;
+  p.last_lanes = 32;
+  for (int i = 0; i < 4; ++i) p.lut[i] = 0xfd02fe01u * (uint32_t)(i + 1);   // int8 codebook values
+  constexpr int W = Shape<NV>::warps;
+  const size_t smem = round_up_u32(NV * p.x_vec_bytes + NV * 32 * 4, 128) + (size_t)W * p.full_tile;
+  cudaError_t err = cudaFuncSetAttribute(chunk_rate_kernel<FMT, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  const int grid = device_sm_count() * ctas_per_sm;
+  *weights = (int64_t)grid * W * iters * kRows * kChunkK;
+  *threads = (int64_t)grid * W * 32;
+  if (sink == nullptr) return cudaSuccess;
+  chunk_rate_kernel<FMT, NV><<<grid, W * 32, smem, s>>>(p, iters, sink);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_chunk_rate(int nv, int ctas_per_sm, int iters, float* sink, int64_t* weights, int64_t* threads,
+                              cudaStream_t s) {
+  switch (nv) {
+    case 1: return launch_chunk_rate_nv<FMT, 1>(ctas_per_sm, iters, sink, weights, threads, s);
+    case 2: return launch_chunk_rate_nv<FMT, 2>(ctas_per_sm, iters, sink, weights, threads, s);
+    case 3: return launch_chunk_rate_nv<FMT, 3>(ctas_per_sm, iters, sink, weights, threads, s);
+    default: return launch_chunk_rate_nv<FMT, 4>(ctas_per_sm, iters, sink, weights, threads, s);
+  }
+}
+
 }  // namespace qmv
+
+// Defines `int NAME(unsigned long long* out, size_t n, int clear)`: copies this
+// translation unit's phase-probe buffer (kProbeSlots x kProbeCtas x
+// kProbeWarps x kPhases stamps) to the host and optionally clears it; -1 in
+// a build without the probe.
+#ifdef QMV_PHASE_PROBE
+#define QMV_DEFINE_PHASE_ACCESSOR(NAME)                                                        \
+  int NAME(unsigned long long* out, size_t n, int clear) {                                     \
+    const size_t bytes = sizeof(qmv::g_phase);                                                 \
+    if (n * sizeof(unsigned long long) < bytes) return -1;                                     \
+    if (cudaMemcpyFromSymbol(out, qmv::g_phase, bytes) != cudaSuccess) return -1;               \
+    if (clear) {                                                                               \
+      void* a = nullptr;                                                                       \
+      if (cudaGetSymbolAddress(&a, qmv::g_phase) != cudaSuccess) return -1;                    \
+      if (cudaMemset(a, 0, bytes) != cudaSuccess) return -1;                                   \
+    }                                                                                          \
+    return 0;                                                                                  \
+  }
+#else
+#define QMV_DEFINE_PHASE_ACCESSOR(NAME) \
+  int NAME(unsigned long long*, size_t, int) { return -1; }
+#endif

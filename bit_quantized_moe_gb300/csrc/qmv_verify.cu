@@ -1,18 +1,39 @@
-// qmv_verify.cu -- verify and batched products of the MX formats on the
-// fifth-generation tensor cores (tcgen05): dense matvecs of 5..16 tokens, and
-// sorted expert gathers of 33..128 routed slots.
+// qmv_verify.cu -- batched products on the fifth-generation tensor cores
+// (tcgen05) for every weight format: dense calls of 5..16 tokens (a
+// speculative-decoding verify batch) and sorted expert gathers of 33..128
+// routed slots.
 //
-// A speculative-decoding verify batch applies one weight matrix to several
-// tokens at once ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...",
-// "Depends on": the batched ROCmFPX MMQ that runs the verify batch). With
-// more than a few tokens the product is a skinny GEMM, D[n][t] = sum_k W[n][k]
-// x[t][k], and the CUDA-core matvec becomes ALU-bound (one FMA per weight and
-// token). Here the CUDA cores only decode: each E2M1 / E4M3 code times its
-// group's 2^(e-127) is written as an exact bf16 into a shared-memory operand,
-// and one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128
-// rows, N = 16 tokens, K = 16) accumulating in tensor memory. Products of
-// bf16 values are exact in fp32, so the result differs from the CUDA-core
-// path only in the order of the fp32 additions.
+// A verify batch applies one weight matrix to several tokens at once
+// ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...", "Depends on":
+// the batched ROCmFPX MMQ that runs the verify batch). With more than a few
+// tokens the product is a skinny GEMM, D[n][t] = sum_k W[n][k] x[t][k], and
+// the CUDA-core matvec becomes ALU-bound (one FMA or dp4a lane per weight and
+// token). Here the CUDA cores only decode, and the block scales stay out of
+// the tensor-core operands:
+//   A (weights): the unscaled element values as f16, exact -- E2M1 and E4M3
+//      codes by cvt.rn.f16x2.e2m1x2 / e4m3x2, codebook codes through the byte
+//      permute table of the CUDA-core kernel into int8 and from there to f16
+//      (integers below 2^11 are exact in f16).
+//   B (activations): MX formats: the bf16 activations of each 32-group scaled
+//      by a power of two into f16 (the staging of the CUDA-core kernel: exact
+//      when the group's magnitudes span less than 2^31); codebook formats:
+//      the q8_1 codes as f16 (exact), their fp16 scale d kept aside.
+//   One tensor-memory accumulator per E8M0 group (32 columns; 16 for the
+//      half-block scales of CB2 / CB3): tcgen05.mma (kind::f16, f16 x f16 ->
+//      fp32, M = 128 rows, N = 16 tokens, K = 16). For the codebooks every
+//      product and partial sum is an integer below 2^24, so each accumulator
+//      is the exact integer block sum sum_{i in h} lut[c_i] * q_i.
+//   Drain: the decoding warps read each finished accumulator (tcgen05.ld) and
+//      apply the scales in fp32, as the CUDA-core path does --
+//        MX:        acc += 2^(e-127) * (sum * 2^-s)
+//        codebooks: acc += d_b * 2^(e-127) * isum  (two half-blocks:
+//                   d_b * (2^(e0-127) * isum0 + 2^(e1-127) * isum1))
+//      ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...", the
+//      review reply's dot structure; "perf(rocm): add an mxfp4 arm ...",
+//      "Current Behavior": E8M0 uint8 scales). So every legal scale byte
+//      0..254 is applied exactly (255 gives NaN), and the results differ from
+//      the CUDA-core path only in the order of fp32 additions; the integer
+//      block sums are bit-identical.
 //
 // Work decomposition: a CTA owns 128 rows (16 row tiles of the packed
 // layout) and one of `split` K ranges; the `split` CTAs of a row block form a
@@ -22,20 +43,20 @@
 // tiles) of every 64-column step, a lane taking one row and one of the two
 // 32-groups, its weight loads issued a window of steps ahead -- and one warp
 // that issues the MMAs. Three A buffers, each with a "full" barrier (one
-// arrival per decoding warp) and an "empty" one (tcgen05.commit), let the
-// warps decode ahead of the tensor core. A sorted gather adds a second grid
+// arrival per decoding warp) and an "empty" one (tcgen05.commit); the
+// accumulators of kAccSteps steps live in tensor memory, each step's with an
+// "accumulated" barrier (tcgen05.commit) and a "drained" one (one arrival
+// per decoding warp). A decoding warp drains step st - kLag after decoding
+// step st: warps w and w + 4 read tensor-memory lanes 32 (w % 4) .. + 31
+// (one row each), tokens 0..7 and 8..15. A sorted gather adds a second grid
 // dimension of work items, one (expert, up to 16 of its slots) pair each.
 //
 // Operand layouts (no swizzle, K-major "canonical" core matrices of 8 rows x
 // 16 bytes): A step buffer (128 rows x 64 columns), core matrix (row group
 // g, k group kk) at kk * 2048 + g * 128; B (activations, tokens padded to 16
-// with zeros), core matrix (token group g, k group kk) at kk * 256 + g * 128. Descriptor
-// leading byte offset = the K-direction stride, stride byte offset = the
-// row-direction stride.
-//
-// Range: a weight whose value exceeds bf16 / fp32 range (E8M0 254 with
-// |E2M1| >= 2, or E8M0 255 = NaN) decodes to inf / NaN here; the CUDA-core
-// path multiplies the scale into the fp32 sum instead.
+// with zeros), core matrix (token group g, k group kk) at kk * 256 + g * 128.
+// Descriptor leading byte offset = the K-direction stride, stride byte
+// offset = the row-direction stride.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -45,6 +66,7 @@
 #include "qmv_device.cuh"
 #include "qmv_internal.h"
 #include "qmv_layout.h"
+#include "qmv_matvec.cuh"
 
 namespace qmv {
 namespace cg = cooperative_groups;
@@ -57,26 +79,41 @@ constexpr int kDecoders = 256;   // decoding threads: two per row
 constexpr int kVThreads = kDecoders + 32;   // plus one warp that issues the MMAs
 constexpr int kVStepK = 64;      // columns per step (one A buffer): 2 groups of 32
 constexpr int kVBufs = 3;        // A buffers
-// Steps of weight loads in flight per thread: 128 bytes (8 MXFP4 or 4
-// MXFP8 lane blocks), so two CTAs keep ~64 KB per SM in flight.
-template <int FMT>
-struct Window {
-  static constexpr int value = 128 / lane_code_bytes(FMT);
-};
+constexpr int kAccSteps = 4;     // steps whose accumulators tensor memory holds at once
+constexpr int kLag = 2;          // a decoding warp drains step st - kLag after decoding step st
+constexpr int kScaleRing = 8;    // steps of E8M0 bytes kept for the drains
+static_assert(kLag < kVBufs && kLag < kAccSteps, "drain lag within the buffer and accumulator rings");
 constexpr uint32_t kABytes = kVRows * kVStepK * 2;   // 16 KB
 constexpr uint32_t kALbo = kVRows / 8 * 128;          // A: k-group stride (16 row groups of 128 B)
 constexpr int kVMaxSplit = 8;    // cluster size limit (portable)
 constexpr int kVMaxSlots = 128;  // routed slots of a sorted gather
 constexpr int kVMaxSteps = 24;   // activation operand <= 48 KB (two CTAs per SM)
 
+template <int FMT>
+struct VFmt {
+  static constexpr int span = fmt_group(FMT);                  // columns per accumulator (one E8M0 group)
+  static constexpr int blocks = kVStepK / span;                // accumulators per step: 2 or 4
+  static constexpr int acc_cols = kAccSteps * blocks * kVTok;  // tensor memory columns: 128 or 256
+  static constexpr int spl = lane_scale_bytes(FMT);            // E8M0 bytes per lane block: 1 or 2
+  // Weight loads in flight per thread: about 128 bytes of lane blocks for the
+  // MX formats, so two CTAs keep ~64 KB per SM in flight; fewer blocks for the
+  // codebooks, whose decode needs more registers (80-96 bytes in flight).
+  static constexpr int window = fmt_is_mx(FMT) ? 128 / lane_code_bytes(FMT) : (FMT == CB2 ? 8 : 6);
+  static constexpr int words = (FMT == CB3) ? 3 : lane_code_bytes(FMT) / 4;
+};
+
 struct VParams {
   const uint8_t* w;
-  const __nv_bfloat16* x;
-  __nv_bfloat16* y;
+  const uint8_t* x;        // bf16 vectors (MX), q8_1 vectors, or fp32 vectors (codebooks with x_f32)
+  void* y;                 // [slot][N]: bf16 (MX) or fp32 (codebooks)
+  int32_t* dbg;            // integer block sums (codebooks) or null
   int N, K, T;
   int row_tiles, chunks, last_lanes;
   uint32_t full_tile;
   uint64_t rowtile;
+  uint32_t x_vec_bytes;
+  int x_f32;               // codebooks: x is fp32, quantized to q8_1 while staged
+  uint32_t lut[4];         // codebook values + 128, one byte per code
   int groups;   // K / 32
   int split;    // CTAs (cluster ranks) per row block
   int steps;    // steps of the longest K range
@@ -95,12 +132,11 @@ __device__ __forceinline__ uint64_t mma_desc(uint32_t addr, uint32_t lbo, uint32
   return d;
 }
 
-// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both
-// K-major, N = 16, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kVTok >> 3) << 17) |
-                            ((uint32_t)(kVRows >> 4) << 24);
+// kind::f16 instruction descriptor: fp32 accumulator (bits 4-5 = 1), A and B
+// both f16 (bits 7-9 and 10-12 = 0), both K-major, N = 16, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kVTok >> 3) << 17) | ((uint32_t)(kVRows >> 4) << 24);
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
                :: "r"(tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate));
@@ -118,11 +154,23 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Lane block of one row and one 32-group: codes (LCB bytes) and scale.
+// Eight fp32 accumulator columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Lane block of one row and one 32-group: codes and E8M0 byte(s) (two, the
+// half-blocks, for CB2 / CB3).
 template <int FMT>
 struct Block {
-  static constexpr int kWords = lane_code_bytes(FMT) / 4;
-  uint32_t c[kWords];
+  uint32_t c[VFmt<FMT>::words];
   uint32_t e;
 };
 
@@ -131,34 +179,55 @@ __device__ __forceinline__ void load_block(const VParams& p, const uint8_t* w, i
                                            Block<FMT>& b) {
   if (!valid) {
 #pragma unroll
-    for (int i = 0; i < Block<FMT>::kWords; ++i) b.c[i] = 0;
-    b.e = 127;
+    for (int i = 0; i < VFmt<FMT>::words; ++i) b.c[i] = 0;
+    b.e = (VFmt<FMT>::spl == 2) ? 0x7f7fu : 0x7fu;
     return;
   }
   const int c = g >> 5, l = g & 31;
   const int L = (c == p.chunks - 1) ? p.last_lanes : 32;
   const uint8_t* tile = w + (uint64_t)rt * p.rowtile + (uint64_t)c * p.full_tile;
-  const uint4* src = reinterpret_cast<const uint4*>(tile + (size_t)(r8 * L + l) * lane_code_bytes(FMT));
-#pragma unroll
-  for (int q = 0; q < Block<FMT>::kWords / 4; ++q) {
-    const uint4 v = __ldg(src + q);
-    b.c[4 * q] = v.x; b.c[4 * q + 1] = v.y; b.c[4 * q + 2] = v.z; b.c[4 * q + 3] = v.w;
+  const size_t li = (size_t)(r8 * L + l);
+  if constexpr (FMT == MXFP4 || FMT == CB4) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(tile + li * 16));
+    b.c[0] = v.x; b.c[1] = v.y; b.c[2] = v.z; b.c[3] = v.w;
+  } else if constexpr (FMT == MXFP8) {
+    const uint4* src = reinterpret_cast<const uint4*>(tile + li * 32);
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    b.c[0] = v0.x; b.c[1] = v0.y; b.c[2] = v0.z; b.c[3] = v0.w;
+    b.c[4] = v1.x; b.c[5] = v1.y; b.c[6] = v1.z; b.c[7] = v1.w;
+  } else {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(tile + li * 8));
+    b.c[0] = v.x; b.c[1] = v.y;
+    if constexpr (FMT == CB3) b.c[2] = __ldg(reinterpret_cast<const uint32_t*>(tile + (size_t)kRows * L * 8 + li * 4));
   }
-  b.e = __ldg(tile + tile_code_bytes(FMT, L) + l * kRows + r8);
+  const uint8_t* sp = tile + tile_code_bytes(FMT, L) + (size_t)(l * kRows + r8) * VFmt<FMT>::spl;
+  if constexpr (VFmt<FMT>::spl == 2) {
+    b.e = __ldg(reinterpret_cast<const unsigned short*>(sp));
+  } else {
+    b.e = __ldg(sp);
+  }
 }
 
-__device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t h2, float s) {
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
-  return *reinterpret_cast<const uint32_t*>(&b);
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
-// 32 codes of a lane block -> 32 exact bf16 values (code value x 2^(e-127)),
+// Four int8 values stored with a bias of 128 (v + 128 in each byte) -> two
+// f16x2 holding exactly v: the byte under the f16 exponent of 1024 gives
+// 1024 + v + 128, and subtracting 1152 is exact.
+__device__ __forceinline__ void biased_i8x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  lo = sub_f16x2(prmt(v, 0x64646464u, 0x4140u), 0x64806480u);
+  hi = sub_f16x2(prmt(v, 0x64646464u, 0x4342u), 0x64806480u);
+}
+
+// 32 codes of a lane block -> 32 exact f16 element values (unscaled),
 // written as four 16-byte core-matrix rows (k groups kk0 .. kk0 + 3, kALbo
 // bytes apart).
 template <int FMT>
-__device__ __forceinline__ void decode_store(const Block<FMT>& b, uint8_t* a_row, int kk0) {
-  const float s = e8m0_to_f32(b.e);
+__device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t (&lut)[4], uint8_t* a_row,
+                                             int kk0) {
   uint32_t out[16];
   if constexpr (FMT == MXFP4) {
 #pragma unroll
@@ -166,16 +235,28 @@ __device__ __forceinline__ void decode_store(const Block<FMT>& b, uint8_t* a_row
       uint32_t h[4];
       e2m1x8_to_f16x2(b.c[q], h);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) out[4 * q + i] = scaled_bf16x2(h[i], s);
+      for (int i = 0; i < 4; ++i) out[4 * q + i] = h[i];
     }
-  } else {
+  } else if constexpr (FMT == MXFP8) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       uint32_t h[2];
       e4m3x4_to_f16x2(b.c[q], h);
-      out[2 * q] = scaled_bf16x2(h[0], s);
-      out[2 * q + 1] = scaled_bf16x2(h[1], s);
+      out[2 * q] = h[0];
+      out[2 * q + 1] = h[1];
     }
+  } else {
+    uint32_t v[8];
+    if constexpr (FMT == CB2) {
+      decode_cb2(b.c[0], b.c[1], lut[0], v);
+    } else if constexpr (FMT == CB3) {
+      decode_cb3(b.c[0], b.c[1], b.c[2], lut[0], lut[1], v);
+    } else {
+      const uint32_t w4[4] = {b.c[0], b.c[1], b.c[2], b.c[3]};
+      decode_cb4(w4, lut, v);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) biased_i8x4_to_f16x2(v[i], out[2 * i], out[2 * i + 1]);
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -184,11 +265,65 @@ __device__ __forceinline__ void decode_store(const Block<FMT>& b, uint8_t* a_row
   }
 }
 
+// Activation operand B: one (token t, local 32-group gl) unit -- 32 f16
+// values into four core-matrix rows -- and its factor for the drain (MX:
+// 2^-s of the group's shift; codebooks: the q8_1 scale d as fp32).
+template <int FMT>
+__device__ __forceinline__ void stage_unit(const VParams& p, int vec, int g, bool valid, uint8_t* bbuf, int gl,
+                                           int t, float* aux) {
+  uint32_t w[16];
+  float f = 0.0f;
+  if (!valid) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = 0;
+  } else if constexpr (fmt_is_mx(FMT)) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)vec * p.x_vec_bytes + (size_t)g * 64);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = src[q];
+      w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+    f = shift_group_to_f16(w);
+  } else {
+    uint32_t qw[8];
+    if (p.x_f32) {
+      float xf[32];
+      const float4* src = reinterpret_cast<const float4*>(p.x + (size_t)vec * p.x_vec_bytes + (size_t)g * 128);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = src[i];
+        xf[4 * i] = v.x; xf[4 * i + 1] = v.y; xf[4 * i + 2] = v.z; xf[4 * i + 3] = v.w;
+      }
+      f = __half2float(__float2half_rn(q8_block(xf, qw)));
+    } else {
+      const uint8_t* xv = p.x + (size_t)vec * p.x_vec_bytes;
+      const uint4* src = reinterpret_cast<const uint4*>(xv + (size_t)g * 32);
+      const uint4 a = src[0], b = src[1];
+      qw[0] = a.x; qw[1] = a.y; qw[2] = a.z; qw[3] = a.w;
+      qw[4] = b.x; qw[5] = b.y; qw[6] = b.z; qw[7] = b.w;
+      f = __half2float(reinterpret_cast<const __half*>(xv + p.K)[g]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) biased_i8x4_to_f16x2(qw[i] ^ 0x80808080u, w[2 * i], w[2 * i + 1]);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int kk = gl * 4 + q;
+    *reinterpret_cast<uint4*>(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+  aux[gl * kVTok + t] = f;
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_constant__ VParams p) {
+  using F = VFmt<FMT>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kVBufs + 1];   // empty (MMAs done) x kVBufs, final
-  __shared__ __align__(8) uint64_t full[kVBufs];        // A buffer written by all decoding warps
+  __shared__ __align__(8) uint64_t empty[kVBufs];      // A buffer read by the MMAs (tcgen05.commit)
+  __shared__ __align__(8) uint64_t full[kVBufs];       // A buffer written by all decoding warps
+  __shared__ __align__(8) uint64_t accd[kAccSteps];    // a step's accumulators complete (tcgen05.commit)
+  __shared__ __align__(8) uint64_t accf[kAccSteps];    // a step's accumulators drained (one arrival per decoding warp)
+  __shared__ __align__(8) uint64_t done;               // every MMA complete (tcgen05.commit)
   __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)(blockIdx.x % (unsigned)p.split);
@@ -250,7 +385,13 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       if (p.prefetch) pdl_wait();   // outputs are written only after the preceding kernel completed
       for (int i = rank * kVThreads + tid; i < p.nslots * kVRows; i += p.split * kVThreads) {
         const int sl = i / kVRows, orow = rb * kVRows + i % kVRows;
-        if (s_ids[sl] < 0 && orow < p.N) p.y[(size_t)sl * p.N + orow] = __float2bfloat16_rn(0.f);
+        if (s_ids[sl] < 0 && orow < p.N) {
+          if constexpr (fmt_is_mx(FMT)) {
+            static_cast<__nv_bfloat16*>(p.y)[(size_t)sl * p.N + orow] = __float2bfloat16_rn(0.f);
+          } else {
+            static_cast<float*>(p.y)[(size_t)sl * p.N + orow] = 0.f;
+          }
+        }
       }
     }
     __syncthreads();
@@ -258,27 +399,35 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     T = s_item[2];
     w = p.w + (uint64_t)s_item[0] * p.expert_stride;
   }
-  uint8_t* abuf = smem;                                   // kVBufs x 16 KB
-  uint8_t* bbuf = smem + kVBufs * kABytes;                // steps x 64 columns x 16 tokens
-  float* part = reinterpret_cast<float*>(smem);           // 16 x 128 fp32, after the MMAs
+  uint8_t* abuf = smem;                                               // kVBufs x 16 KB
+  uint8_t* bbuf = smem + kVBufs * kABytes;                            // steps x 64 columns x 16 tokens
+  uint16_t* sc = reinterpret_cast<uint16_t*>(bbuf + (size_t)p.steps * (kVStepK / 8) * 256);  // [ring][2][128]
+  float* aux = reinterpret_cast<float*>(sc + kScaleRing * 2 * kVRows);  // [2 steps][16]: 2^-s or d
+  float* part = reinterpret_cast<float*>(smem);                       // 16 x 128 fp32, after the MMAs
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" :: "r"(smem_addr(&tmem_slot)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(&tmem_slot)), "r"(F::acc_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int i = 0; i <= kVBufs; ++i) mbar_init(smem_addr(&bars[i]), 1);
-    for (int i = 0; i < kVBufs; ++i) mbar_init(smem_addr(&full[i]), kDecoders / 32);
+    for (int i = 0; i < kVBufs; ++i) {
+      mbar_init(smem_addr(&empty[i]), 1);
+      mbar_init(smem_addr(&full[i]), kDecoders / 32);
+    }
+    for (int i = 0; i < kAccSteps; ++i) {
+      mbar_init(smem_addr(&accd[i]), 1);
+      mbar_init(smem_addr(&accf[i]), kDecoders / 32);
+    }
+    mbar_init(smem_addr(&done), 1);
     fence_mbar_init();
   }
   // Weight stream: decoding warp w takes row tiles 2w and 2w + 1 of the
   // block; lane (i, r8, h) takes row r8 of tile 2w + i and group
-  // 2 * step + h, so one warp load covers 16 rows x 32 contiguous bytes
-  // (16 full sectors).
+  // 2 * step + h, so one warp load covers 16 rows x 2 adjacent lane blocks.
   // The first window of loads goes out first (before griddepcontrol.wait
   // when the caller guarantees the weights are not the preceding kernel's
-  // output), then the activations, whose loads are all issued before any of
-  // them is stored.
+  // output), then the activations.
   const bool decoder = tid < kDecoders;
   const int h = lane & 1;
   const int r = (warp & 7) * 16 + (lane >> 1);   // row of the block: tile 2w + (lane >> 4), row (lane >> 1) & 7
@@ -286,7 +435,8 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
   uint8_t* a_row = abuf + (r >> 3) * 128 + (r & 7) * 16;
-  constexpr int kWindow = Window<FMT>::value;
+  uint32_t lut[4] = {p.lut[0], p.lut[1], p.lut[2], p.lut[3]};
+  constexpr int kWindow = F::window;
   Block<FMT> win[kWindow];
   if (!p.prefetch) pdl_wait();
 #pragma unroll
@@ -297,32 +447,16 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   if (p.prefetch) pdl_wait();
   pdl_launch_dependents();
 
-  // Activation operand: tokens t < T of columns [32 g0, 32 g0 + 64 steps),
-  // zero beyond the CTA's range and for padding tokens.
-  {
-    constexpr int kU = 4;
-    const int kk_n = steps * (kVStepK / 8);
-    const int k_end = g1 * 32;
-    const int n_units = decoder ? kk_n * kVTok : 0;
-    for (int u0 = tid; u0 < n_units; u0 += kU * kDecoders) {
-      uint4 v[kU];
-#pragma unroll
-      for (int j = 0; j < kU; ++j) {
-        const int u = u0 + j * kDecoders;
-        const int t = u % kVTok, kk = u / kVTok;
-        const int k = g0 * 32 + kk * 8;
-        v[j] = make_uint4(0, 0, 0, 0);
-        if (u < n_units && t < T && k < k_end) {
-          const int vec = (p.ids == nullptr) ? t : (p.per_slot ? s_slot[t] : s_slot[t] / p.top_k);
-          v[j] = *reinterpret_cast<const uint4*>(p.x + (size_t)vec * p.K + k);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kU; ++j) {
-        const int u = u0 + j * kDecoders;
-        const int t = u % kVTok, kk = u / kVTok;
-        if (u < n_units) *reinterpret_cast<uint4*>(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16) = v[j];
-      }
+  // Activation operand: tokens t < T of groups [g0, g0 + 2 steps), zero
+  // beyond the CTA's range and for padding tokens.
+  if (decoder) {
+    const int n_units = 2 * steps * kVTok;
+    for (int u = tid; u < n_units; u += kDecoders) {
+      const int t = u % kVTok, gl = u / kVTok;
+      const int g = g0 + gl;
+      const bool valid = t < T && g < g1;
+      const int vec = (p.ids == nullptr) ? t : (p.per_slot ? s_slot[t < T ? t : 0] : s_slot[t < T ? t : 0] / p.top_k);
+      stage_unit<FMT>(p, vec, g, valid, bbuf, gl, t, aux);
     }
   }
 
@@ -333,61 +467,131 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   const uint32_t tmem = tmem_slot;
   bool ok = true;
 
+  // Drain of step sd by this decoding warp: rows 32 (warp % 4) + lane, tokens tq .. tq + 7.
+  const int tq = (warp >> 2) * 8;
+  const int rr = (warp & 3) * 32 + lane;
+  const int drow = rb * kVRows + rr;
+  const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  auto drain = [&](int sd) {
+    // the A-buffer barrier of step sd orders every decoding thread's scale
+    // bytes of that step before these reads; the accumulator barrier says
+    // the step's MMAs are complete
+    ok = ok && mbar_wait_bounded(smem_addr(&full[sd % kVBufs]), (uint32_t)(sd / kVBufs) & 1u, kWaitLimitNs);
+    ok = ok && mbar_wait_bounded(smem_addr(&accd[sd % kAccSteps]), (uint32_t)(sd / kAccSteps) & 1u, kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return;
+    tc_fence_after();
+    const uint16_t* scs = sc + (sd % kScaleRing) * 2 * kVRows + rr;
+    constexpr int per = F::blocks / 2;   // accumulators per 32-group: 1, or 2 half-blocks
+#pragma unroll
+    for (int gh = 0; gh < 2; ++gh) {
+      float v[per][8];
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        tmem_ld8(tlane + (uint32_t)(((sd % kAccSteps) * F::blocks + gh * per + j) * kVTok + tq), v[j]);
+      }
+      tmem_wait_ld();
+      const int gl = 2 * sd + gh;
+      const float* f = aux + gl * kVTok + tq;
+      const uint32_t eb = scs[gh * kVRows];
+      if constexpr (fmt_is_mx(FMT)) {
+        const float s = e8m0_to_f32(eb & 0xffu);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = fmaf(s, v[0][t] * f[t], acc[t]);
+      } else if constexpr (per == 2) {
+        const float s0 = e8m0_to_f32(eb & 0xffu), s1 = e8m0_to_f32(eb >> 8);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = fmaf(f[t], fmaf(s0, v[0][t], s1 * v[1][t]), acc[t]);
+      } else {
+        const float s = e8m0_to_f32(eb & 0xffu);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = fmaf(f[t], s * v[0][t], acc[t]);
+      }
+      if constexpr (!fmt_is_mx(FMT)) {
+        const int g = g0 + gl;
+        if (p.dbg != nullptr && drow < p.N && g < g1) {
+          const int nb = p.K / F::span;
+#pragma unroll
+          for (int j = 0; j < per; ++j) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int tt = tq + t;
+              if (tt < T) {
+                const int slot = (p.ids == nullptr) ? tt : s_slot[tt];
+                p.dbg[((size_t)slot * p.N + drow) * nb + g * per + j] = (int32_t)v[j][t];
+              }
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&accf[sd % kAccSteps]));
+  };
+
   if (decoder) {
-    for (int s0 = 0; s0 < steps; s0 += kWindow) {
+    for (int s0 = 0; s0 < steps && ok; s0 += kWindow) {
 #pragma unroll
       for (int u = 0; u < kWindow; ++u) {
         const int st = s0 + u;
-        if (st < steps) {
+        if (st < steps && ok) {
           const int b = st % kVBufs;
           if (st >= kVBufs) {
             // the MMAs that read this buffer kVBufs steps ago are done
-            ok &= mbar_wait_bounded(smem_addr(&bars[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
+            ok = ok && mbar_wait_bounded(smem_addr(&empty[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
           }
-          decode_store<FMT>(win[u], a_row + (size_t)b * kABytes, 4 * h);
+          decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
+          sc[(st % kScaleRing) * 2 * kVRows + h * kVRows + r] = (uint16_t)win[u].e;
           const int gn = g0 + 2 * (st + kWindow) + h;
           load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&full[b]));
+          if (st >= kLag) drain(st - kLag);
         }
       }
     }
+    for (int sd = steps - kLag > 0 ? steps - kLag : 0; sd < steps && ok; ++sd) drain(sd);
   } else if (lane == 0) {
-    // MMA issue: step st once every decoding warp has written its A buffer.
-    for (int st = 0; st < steps; ++st) {
+    // MMA issue: step st once every decoding warp has written its A buffer
+    // and the accumulators it reuses have been drained.
+    for (int st = 0; st < steps && ok; ++st) {
       const int b = st % kVBufs;
-      ok &= mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
+      ok = mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
+      if (ok && st >= kAccSteps) {
+        ok = mbar_wait_bounded(smem_addr(&accf[st % kAccSteps]), (uint32_t)((st / kAccSteps) - 1) & 1u, kWaitLimitNs);
+      }
+      if (!ok) break;
       tc_fence_after();
       const uint32_t a0 = smem_addr(abuf + (size_t)b * kABytes);
       const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
 #pragma unroll
       for (int j = 0; j < kVStepK / 16; ++j) {
-        mma_bf16(tmem, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                 (st > 0 || j > 0) ? 1u : 0u);
+        const int blk = j * 16 / F::span;
+        const uint32_t col = (uint32_t)(((st % kAccSteps) * F::blocks + blk) * kVTok);
+        mma_f16(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
+                (j * 16 % F::span) != 0 ? 1u : 0u);
       }
-      mma_commit(smem_addr(&bars[b]));
+      mma_commit(smem_addr(&empty[b]));
+      mma_commit(smem_addr(&accd[st % kAccSteps]));
     }
-    mma_commit(smem_addr(&bars[kVBufs]));
+    mma_commit(smem_addr(&done));
+    if (!mbar_wait_bounded(smem_addr(&done), 0u, kWaitLimitNs)) ok = false;
   }
-  __syncwarp();
-  ok &= mbar_wait_bounded(smem_addr(&bars[kVBufs]), 0u, kWaitLimitNs);
-  tc_fence_after();
-  if (!__all_sync(0xffffffffu, ok) && lane == 0) set_status(kStatusWaitTile);
+  if (!ok && lane == 0) set_status(kStatusWaitTile);
 
-  // Accumulator rows 32 w .. 32 w + 31 (tensor-memory lanes of warp w) ->
-  // partial sums part[t][row], t < 16. The A buffers are free: every MMA that
-  // read them has completed.
-  if (warp < 4) {
-    uint32_t v[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                   "=r"(v[15])
-                 : "r"(tmem + ((uint32_t)(warp * 32) << 16)));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  // Partial sums part[t][row] (the A buffers are free: every MMA that read
+  // them completed before the last drain).
+  __syncthreads();
+  if (decoder) {
 #pragma unroll
-    for (int t = 0; t < kVTok; ++t) part[t * kVRows + warp * 32 + lane] = __uint_as_float(v[t]);
+    for (int t = 0; t < 8; ++t) part[(tq + t) * kVRows + rr] = acc[t];
   }
   tc_fence_before();
 
@@ -395,31 +599,38 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   for (int i = rank * kVThreads + tid; i < kVRows * T; i += p.split * kVThreads) {  // all 9 warps
-    const int t = i / kVRows, rr = i % kVRows;
-    const int orow = rb * kVRows + rr;
+    const int t = i / kVRows, rw = i % kVRows;
+    const int orow = rb * kVRows + rw;
     if (orow >= p.N) continue;
     float v[kVMaxSplit];
 #pragma unroll
-    for (int q = 0; q < kVMaxSplit; ++q) v[q] = (q < p.split) ? cluster.map_shared_rank(part, q)[t * kVRows + rr] : 0.f;
-    float acc = 0.f;
+    for (int q = 0; q < kVMaxSplit; ++q) v[q] = (q < p.split) ? cluster.map_shared_rank(part, q)[t * kVRows + rw] : 0.f;
+    float a = 0.f;
 #pragma unroll
-    for (int q = 0; q < kVMaxSplit; ++q) acc += v[q];   // rank order; absent ranks add +0
+    for (int q = 0; q < kVMaxSplit; ++q) a += v[q];   // rank order; absent ranks add +0
     const int oslot = (p.ids == nullptr) ? t : s_slot[t];
-    p.y[(size_t)oslot * p.N + orow] = __float2bfloat16_rn(acc);
+    if constexpr (fmt_is_mx(FMT)) {
+      static_cast<__nv_bfloat16*>(p.y)[(size_t)oslot * p.N + orow] = __float2bfloat16_rn(a);
+    } else {
+      static_cast<float*>(p.y)[(size_t)oslot * p.N + orow] = a;
+    }
   }
   cluster.sync();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" :: "r"(tmem));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(F::acc_cols));
   }
 }
 
 }  // namespace
 
-// Verify-batch plan: rows in blocks of 128, K cut into `split` ranges (one
-// cluster rank each) so that the grid covers about two CTAs per SM.
+// Tensor-core plan: rows in blocks of 128, K cut into `split` ranges (one
+// cluster rank each) so that the grid covers about two CTAs per SM. Taken by
+// dense calls of 5..16 tokens and gathers of 33..128 routed slots, with bf16
+// (MX) or q8_1 / fp32 (codebook) activations, not the gate/up fusion.
 bool verify_supported(const MatvecArgs& a) {
-  if (!fmt_is_mx(a.fmt) || a.x_f16 || a.glu || a.dbg != nullptr) return false;
+  if (a.x_f16 || a.glu) return false;
+  if (fmt_is_mx(a.fmt) && a.dbg != nullptr) return false;
   if (a.ids != nullptr) {
     // sorted gather: beyond the decode gather's 32 routed slots
     const int nslots = a.ntok * a.top_k;
@@ -431,15 +642,19 @@ bool verify_supported(const MatvecArgs& a) {
   return (groups + kVMaxSplit - 1) / kVMaxSplit <= 2 * kVMaxSteps;
 }
 
-size_t verify_smem_bytes(int steps) { return (size_t)kVBufs * kABytes + (size_t)steps * (kVStepK / 8) * 256; }
+size_t verify_smem_bytes(int steps) {
+  return (size_t)kVBufs * kABytes + (size_t)steps * (kVStepK / 8) * 256 + (size_t)kScaleRing * 2 * kVRows * 2 +
+         (size_t)steps * 2 * kVTok * 4;
+}
 
 template <int FMT>
 static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   const Geometry g = make_geometry(a.fmt, a.N, a.K);
   VParams p;
   p.w = static_cast<const uint8_t*>(a.w);
-  p.x = static_cast<const __nv_bfloat16*>(a.x);
-  p.y = static_cast<__nv_bfloat16*>(a.y);
+  p.x = static_cast<const uint8_t*>(a.x);
+  p.y = a.y;
+  p.dbg = a.dbg;
   p.N = a.N;
   p.K = a.K;
   p.T = a.ntok;
@@ -448,6 +663,9 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.last_lanes = g.last_lanes;
   p.full_tile = g.full_tile;
   p.rowtile = g.rowtile;
+  p.x_f32 = a.x_f32 ? 1 : 0;
+  p.x_vec_bytes = fmt_is_mx(a.fmt) ? (uint32_t)a.K * 2u : (a.x_f32 ? (uint32_t)a.K * 4u : (uint32_t)q8_vec_bytes(a.K));
+  for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i] ^ 0x80808080u;
   p.groups = a.K / 32;
   const int row_blocks = (a.N + kVRows - 1) / kVRows;
   // One wave of at most two CTAs per SM; a sorted gather has many work items
@@ -508,7 +726,13 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
 }
 
 cudaError_t launch_verify(const MatvecArgs& a) {
-  return a.fmt == MXFP4 ? launch_verify_fmt<MXFP4>(a) : launch_verify_fmt<MXFP8>(a);
+  switch (a.fmt) {
+    case MXFP4: return launch_verify_fmt<MXFP4>(a);
+    case MXFP8: return launch_verify_fmt<MXFP8>(a);
+    case CB2: return launch_verify_fmt<CB2>(a);
+    case CB3: return launch_verify_fmt<CB3>(a);
+    default: return launch_verify_fmt<CB4>(a);
+  }
 }
 
 QMV_DEFINE_STATUS_ACCESSOR(status_verify)

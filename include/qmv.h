@@ -203,10 +203,15 @@ int qmv_act_q8_unpack(const void* xq_host, int32_t nvec, int32_t K, int8_t* q_ho
  *          QMV_FLAG_X_F16); CB formats: q8_1 buffer of ntok vectors.
  *   y_dev: MX formats: bf16 [ntok][N] (fp16 with QMV_FLAG_X_F16); CB
  *          formats: fp32 [ntok][N].
- * Up to 4 tokens the kernel streams every packed weight byte once per call
- * and applies it to all of them; a call of more tokens streams the matrix
- * once per group of 4 tokens, the groups side by side so that all but the
- * first read it from L2 (the DRAM traffic stays about one matrix).
+ * Up to 4 tokens the CUDA-core kernel streams every packed weight byte once
+ * per call and applies it to all of them. 5..16 tokens run on the tensor
+ * cores (every format; bf16, q8_1 or fp32 activations): the matrix is
+ * streamed once, its unscaled elements and the activations are multiplied as
+ * f16 with one fp32 accumulator per E8M0 group (exact integer block sums for
+ * the codebooks), and the scales are applied in fp32, so every scale byte
+ * 0..254 is exact. With fp16 activations (QMV_FLAG_X_F16) 5..16 tokens stream
+ * the matrix once per group of 4 tokens, side by side (the DRAM traffic stays
+ * about one matrix).
  * Errors: QMV_EINVAL, QMV_ESHAPE, QMV_EALIGN, QMV_ECUDA.
  */
 int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t ntok, void* y_dev,
@@ -225,19 +230,19 @@ int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32
  *            (token, slot) pairs is streamed once per call for up to 4 of them.
  *   Up to QMV_MAX_LAYER_SLOTS (32) routed slots the call is the decode
  *   gather above. 33..QMV_MAX_SLOTS (128) slots -- a verify or prefill batch
- *   through a MoE projection -- need an MX format with bf16 activations and
- *   run as the sorted gather ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ
- *   on RDNA ...", "Depends on": the batched MMQ path): the slots are grouped
- *   by expert (experts in order of their first slot, slots in slot order)
- *   and each expert's weights are streamed once per 16 of its slots through
- *   the tensor cores. Same results up to the order of fp32 additions.
+ *   through a MoE projection -- run as the sorted gather ("perf(ggml/hip):
+ *   optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...", "Depends on": the batched MMQ
+ *   path), for every format with bf16 (MX) or q8_1 / fp32 (codebook)
+ *   activations: the slots are grouped by expert (experts in order of their
+ *   first slot, slots in slot order) and each expert's weights are streamed
+ *   once per 16 of its slots through the tensor cores, as for qmv_dense. Same
+ *   results up to the order of fp32 additions; identical integer block sums.
  *   x_dev:   MX formats: bf16 vectors of K (fp16 with QMV_FLAG_X_F16); CB
  *            formats: q8_1 buffer.
  *   y_dev:   MX formats: bf16 [ntok][top_k][N] (fp16 with QMV_FLAG_X_F16); CB
  *            formats: fp32 [ntok][top_k][N].
  * Errors: QMV_EINVAL (ntok not in 1..16, top_k not in 1..8, ntok * top_k >
- * QMV_MAX_SLOTS, or > QMV_MAX_LAYER_SLOTS outside the sorted gather's
- * formats), QMV_ESHAPE,
+ * QMV_MAX_SLOTS, or > QMV_MAX_LAYER_SLOTS with fp16 activations), QMV_ESHAPE,
  * QMV_EALIGN, QMV_ECUDA.
  */
 int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,
@@ -445,6 +450,43 @@ int qmv_device_status(uint32_t* flags_host, int32_t clear);
  * context stays usable. Checks the timeout path without a fault or a hang.
  */
 int qmv_debug_wait_probe(uint64_t limit_ns, void* stream);
+
+/*
+ * Diagnostic export: the compute rate of the matvec's inner loop. Launches
+ * (SM count x ctas_per_sm) CTAs of the production launch shape for nv
+ * activation vectors (1..4) in which every warp applies the format's chunk
+ * routine (decode, products, block sums and scales of 8 rows x 1024 columns)
+ * `iters` times to a tile held in shared memory, with no copies or waits, so
+ * that its weights per clock per SM can be compared with the rate the weight
+ * stream delivers (the secondary ALU roofline). *weights_host = matrix
+ * weights one launch processes (each applied to nv vectors), *threads_host =
+ * threads launched; sink_dev (fp32 [threads], 16-byte aligned) receives one
+ * value per thread so that nothing is optimized away. sink_dev = NULL only
+ * reports the two counts. Time the launch with events on `stream`.
+ * Errors: QMV_EINVAL, QMV_EALIGN, QMV_ESIZE, QMV_ECUDA.
+ */
+int qmv_debug_chunk_rate(int32_t fmt, int32_t nv, int32_t ctas_per_sm, int32_t iters, float* sink_dev,
+                         size_t sink_bytes, int64_t* weights_host, int64_t* threads_host, void* stream);
+
+/*
+ * Diagnostic exports of the phase probe, a build variant of this library
+ * (bit_quantized_moe_gb300/build.py --phase-probe defines QMV_PHASE_PROBE):
+ * lane 0 of every warp of the CUDA-core matvec records %globaltimer (ns) at
+ * fixed phases of its launch -- kernel start, work list built, tile copies
+ * issued before griddepcontrol.wait, the wait returned, activation loads
+ * issued, every ring stage's first copy issued, activations staged, first
+ * tile landed and computed, second and third tiles landed, last tile
+ * computed, warp done -- into a per-format buffer of
+ * qmv_debug_phase_entries() uint64 values laid out [launch slot 0..7][CTA
+ * 0..511][warp 0..15][phase 0..15], 0 where nothing was recorded.
+ * qmv_debug_phase_probe(1) makes the following launches record (slots dealt
+ * in launch order, modulo 8; a CUDA graph keeps the slots of its capture);
+ * qmv_debug_phase_read copies one format's buffer to the host (synchronizes)
+ * and clears it if `clear`. In the product build both return QMV_EINVAL.
+ */
+size_t qmv_debug_phase_entries(void);
+int qmv_debug_phase_probe(int32_t enable);
+int qmv_debug_phase_read(int32_t fmt, uint64_t* out_host, size_t n, int32_t clear);
 
 /* Message of the last failure on the calling thread ("" if none). */
 const char* qmv_last_error(void);

@@ -99,6 +99,28 @@ def normal_bf16_bits(g: np.random.Generator, shape) -> np.ndarray:
     return u.astype(np.uint16)
 
 
+def scaled_normal_bf16_bits(g: np.random.Generator, shape, exp_shifts) -> np.ndarray:
+    """N(0,1) samples times 2**s as bf16 bit patterns, s = exp_shifts[i] for
+    row i of the leading axis: the fp32 draw scaled exactly by a power of two
+    (np.ldexp), then its upper half kept with round-to-nearest-even."""
+    f = normal_f32(g, shape)
+    s = np.asarray(exp_shifts, dtype=np.int64).reshape((-1,) + (1,) * (f.ndim - 1))
+    f = np.ldexp(f.astype(np.float64), s).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def e8m0_choice(g: np.random.Generator, shape, values) -> np.ndarray:
+    """E8M0 bytes drawn uniformly from the given values."""
+    return np.asarray(values, dtype=np.uint8)[g.integers(0, len(values), size=shape)]
+
+
+def e4m3_subnormal_codes(g: np.random.Generator, shape) -> np.ndarray:
+    """E4M3 codes with a zero exponent field (zero and the subnormals), either sign."""
+    return (g.integers(0, 8, size=shape) | (g.integers(0, 2, size=shape) << 7)).astype(np.uint8)
+
+
 def topk_ids(g: np.random.Generator, ntok: int, top_k: int, n_experts: int) -> np.ndarray:
     """[ntok][top_k] int32: distinct expert ids per token, uniform."""
     out = np.empty((ntok, top_k), dtype=np.int32)

@@ -229,3 +229,172 @@ def test_sorted_gather_prefetch_chain():
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert torch.count_nonzero(y2[3, 2].float()).item() == 0
     assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Every legal E8M0 byte on the tensor-core path (and the CUDA-core path at 4
+# tokens): the scales are applied in fp32 outside the f16 operands
+# ---------------------------------------------------------------------------
+
+EXTREME_E8M0 = (0, 1, 2, 3, 127, 253, 254)
+# per-token power-of-two magnitudes of the activations, so that rows of the
+# largest and the smallest scales both meet tokens that keep their products
+# inside fp32's finite range
+TOKEN_SHIFTS = (-100, -60, -30, -8, 0, 8, 30, 60, -80, -40, -20, 20, 40, 80, 100, 0)
+FP32_TINY = 2.0 ** -140     # fp32 subnormal arithmetic: a few quanta of 2^-149
+
+
+def _extreme_matrix(fmt, N, K, g):
+    """Rows with one scale byte each from EXTREME_E8M0, and rows mixing them
+    along K; MXFP8 also gets rows of subnormal E4M3 codes only."""
+    codes = qi.format_codes(g, fmt, (N, K))
+    scales = np.empty((N, K // 32), np.uint8)
+    for r in range(N):
+        kind = r % 9
+        scales[r] = EXTREME_E8M0[kind] if kind < len(EXTREME_E8M0) else qi.e8m0_choice(g, (K // 32,), EXTREME_E8M0)
+    if fmt == "mxfp8":
+        sub = np.arange(N) % 4 == 3
+        codes[sub] = qi.e4m3_subnormal_codes(g, (int(sub.sum()), K))
+    return codes, scales
+
+
+def _in_range(fmt, codes, scales, x):
+    """(token, row) pairs the fp32 kernels can represent: every 32-group's
+    sum|w x| and the whole row's stay below 2^120 (the float64 oracle has no
+    such limit). Returns the mask [T, N] and sum|w x| [T, N]."""
+    Wabs = np.abs(oracle.mxfp4_dequant(codes, scales) if fmt == "mxfp4" else oracle.mxfp8_dequant(codes, scales))
+    xa = np.abs(oracle.bf16_bits_to_f64(x))
+    N, K = codes.shape
+    per_group = np.einsum("ngk,tgk->tng", Wabs.reshape(N, K // 32, 32), xa.reshape(-1, K // 32, 32))
+    absum = per_group.sum(-1)
+    return (per_group.max(-1) < 2.0 ** 120) & (absum < 2.0 ** 120), absum
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("ntok", [4, 8, 16])
+def test_extreme_scales_dense(fmt, ntok):
+    N, K = 264, 1024
+    g = qi.rng(2000 + ntok + (7 if fmt == "mxfp8" else 0))
+    codes, scales = _extreme_matrix(fmt, N, K, g)
+    m = Matrices(fmt, N, K, 1, [], seed=1)
+    m.set_expert(0, codes, scales)
+    x = qi.scaled_normal_bf16_bits(g, (ntok, K), TOKEN_SHIFTS[:ntok])
+    y = torch.full((ntok, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_dense(m.desc, m.w, to_dev(x), ntok, y)
+    ref = oracle.mx_matvec(fmt, codes, scales, x)
+    mask, absum = _in_range(fmt, codes, scales, x)
+    got = bf16_to_np(y)
+    assert_within(got[mask], ref[mask], 1e-3 * absum[mask] + FP32_TINY, "bf16", f"{fmt} ntok={ntok}")
+    # every scale byte is checked somewhere
+    for e in EXTREME_E8M0:
+        rows = np.arange(N)[(np.arange(N) % 9) == EXTREME_E8M0.index(e)]
+        assert mask[:, rows].any(), e
+    assert status_clean()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8"])
+def test_extreme_scales_sorted_gather(fmt):
+    """40 routed slots (8 tokens x top-5) over 4 experts of extreme scales:
+    the sorted tensor-core gather, per slot against the oracle."""
+    E, N, K, ntok, top_k = 4, 136, 512, 8, 5
+    g = qi.rng(2100 + (7 if fmt == "mxfp8" else 0))
+    ids = np.stack([np.concatenate([g.permutation(E), [int(g.integers(0, E))]]) for _ in range(ntok)]).astype(np.int32)
+    m = Matrices(fmt, N, K, E, [], seed=2)
+    mats = {}
+    for e in range(E):
+        mats[e] = _extreme_matrix(fmt, N, K, g)
+        m.set_expert(e, *mats[e])
+    x = qi.scaled_normal_bf16_bits(g, (ntok, K), TOKEN_SHIFTS[:ntok])
+    y = torch.full((ntok, top_k, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), 0, to_dev(ids), ntok, top_k, y)
+    got = bf16_to_np(y)
+    for t in range(ntok):
+        for j in range(top_k):
+            c, s = mats[int(ids[t, j])]
+            ref = oracle.mx_matvec(fmt, c, s, x[t:t + 1])[0]
+            mask, absum = _in_range(fmt, c, s, x[t:t + 1])
+            assert_within(got[t, j][mask[0]], ref[mask[0]], 1e-3 * absum[0][mask[0]] + FP32_TINY, "bf16",
+                          f"slot ({t},{j})")
+    assert status_clean()
+
+
+# ---------------------------------------------------------------------------
+# Codebook formats on the tensor cores: exact integer block sums per
+# (half-)block, the d * 2^(e-127) epilogue in fp32
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,N,K", [("cb2", 1032, 2048), ("cb3", 7168, 2048), ("cb4", 520, 7168),
+                                     ("cb3", 136, 96)])
+@pytest.mark.parametrize("ntok", [5, 8, 16])
+def test_verify_codebook_block_sums(fmt, N, K, ntok):
+    """Dense verify batches of the codebook formats: every integer block sum
+    bit-exact against the oracle, y within the tolerance; fp32 activations
+    (quantized in the launch) give the same bits as the q8_1 input."""
+    grp = qi.FORMAT_GROUP[fmt]
+    m = Matrices(fmt, N, K, 1, [0], seed=N + K + ntok, lut=LUTS[fmt])
+    g = qi.rng(3000 + ntok + N)
+    xf = qi.normal_f32(g, (ntok, K))
+    xq, q, d = quantize_on_gpu(xf)
+    y = torch.full((ntok, N), 3.0, dtype=torch.float32, device=DEV)
+    sums = torch.full((ntok, N, K // grp), -7, dtype=torch.int32, device=DEV)
+    qmv.qmv_debug_block_sums(m.desc, m.w, xq, 0, None, ntok, 1, y, sums)
+    want = oracle.cb_block_sums(m.codes[0], m.lut, q, grp)
+    assert np.array_equal(sums.cpu().numpy(), want), "block sums differ from the oracle"
+    ref = oracle.cb_matvec(m.codes[0], m.scales[0], m.lut, grp, q, d)
+    absum = oracle.cb_abs_products(m.codes[0], m.scales[0], m.lut, grp, q, d)
+    assert_close(y.cpu().numpy(), ref, absum, "f32", f"{fmt} {N}x{K} ntok={ntok}")
+    y2 = torch.full_like(y, -3.0)
+    qmv.qmv_dense_ex(m.desc, m.w, to_dev(xf), ntok, y2, qmv.QMV_FLAG_X_F32)
+    y3 = torch.full_like(y, -4.0)
+    qmv.qmv_dense(m.desc, m.w, xq, ntok, y3)
+    torch.cuda.synchronize()
+    assert torch.equal(y2.view(torch.int32), y3.view(torch.int32))
+    assert torch.equal(y.view(torch.int32), y3.view(torch.int32))
+    assert status_clean()
+
+
+@pytest.mark.parametrize("fmt,N,K,E,ntok,top_k,per_slot", [
+    ("cb3", 7168, 2048, 64, 16, 4, True),     # a DS4 down projection over a 16-token verify batch
+    ("cb2", 2048, 7168, 64, 16, 4, False),    # its gate (shared activations)
+    ("cb4", 1032, 1024, 16, 16, 8, True),     # 128 slots, experts of up to 16 slots
+    ("cb3", 264, 512, 8, 12, 3, False),
+])
+def test_sorted_gather_codebook(fmt, N, K, E, ntok, top_k, per_slot):
+    """33..128 routed slots of a codebook format: the sorted tensor-core
+    gather, block sums bit-exact per slot and y within the tolerance;
+    repeated experts, an expert of more than 16 slots and invalid ids."""
+    grp = qi.FORMAT_GROUP[fmt]
+    g = qi.rng(4000 + N + ntok * 10 + top_k)
+    ids = np.stack([g.permutation(E)[:top_k] for _ in range(ntok)]).astype(np.int32)
+    ids[:, 0] = 1
+    ids[:3, 1] = 1 if top_k > 1 else ids[:3, 0]
+    ids[-1, -1] = -2
+    ids[2, -1] = E + 5
+    m = Matrices(fmt, N, K, E, ids.reshape(-1), seed=4001 + N, lut=LUTS[fmt])
+    nvec = ntok * top_k if per_slot else ntok
+    xf = qi.normal_f32(g, (nvec, K))
+    xq, q, d = quantize_on_gpu(xf)
+    y = torch.full((ntok, top_k, N), 5.0, dtype=torch.float32, device=DEV)
+    sums = torch.full((ntok, top_k, N, K // grp), -7, dtype=torch.int32, device=DEV)
+    ids_d = to_dev(ids)
+    qmv.qmv_debug_block_sums(m.desc, m.w, xq, int(per_slot), ids_d, ntok, top_k, y, sums)
+    got_sums, got = sums.cpu().numpy(), y.cpu().numpy()
+    for t in range(ntok):
+        for j in range(top_k):
+            e = int(ids[t, j])
+            if not (0 <= e < E):
+                assert np.all(got[t, j] == 0) and np.all(got_sums[t, j] == -7), (t, j)
+                continue
+            v = t * top_k + j if per_slot else t
+            assert np.array_equal(got_sums[t, j], oracle.cb_block_sums(m.codes[e], m.lut, q[v:v + 1], grp)[0]), (t, j)
+            ref = oracle.cb_matvec(m.codes[e], m.scales[e], m.lut, grp, q[v:v + 1], d[v:v + 1])[0]
+            absum = oracle.cb_abs_products(m.codes[e], m.scales[e], m.lut, grp, q[v:v + 1], d[v:v + 1])[0]
+            assert_close(got[t, j], ref, absum, "f32", f"slot ({t},{j}) expert {e}")
+    y2 = torch.full_like(y, -5.0)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, to_dev(xf), int(per_slot), ids_d, ntok, top_k, y2, qmv.QMV_FLAG_X_F32)
+    y3 = torch.full_like(y, -6.0)
+    qmv.qmv_moe_gather(m.desc, m.w, xq, int(per_slot), ids_d, ntok, top_k, y3)
+    torch.cuda.synchronize()
+    assert torch.equal(y2.view(torch.int32), y3.view(torch.int32))
+    assert torch.equal(y.view(torch.int32), y3.view(torch.int32))
+    assert status_clean()

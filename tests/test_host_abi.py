@@ -172,14 +172,17 @@ def test_gather_argument_errors(top_k, ids, code):
 
 def test_routed_slot_limit():
     """Gathers route at most QMV_MAX_SLOTS (128) (token, slot) pairs; beyond
-    QMV_MAX_LAYER_SLOTS (32) only the sorted tensor-core gather (MX formats,
-    bf16 activations) takes them; layers stop at 32; 16 tokens is the dense
-    limit. (No call here reaches a launch: every one fails validation.)"""
+    QMV_MAX_LAYER_SLOTS (32) only the sorted tensor-core gather takes them
+    (any format, not fp16 activations); layers stop at 32; 16 tokens is the
+    dense limit. (No call here reaches a launch: every one fails validation,
+    or, for the accepted 64-slot codebook gather, the device query of a
+    machine without a GPU.)"""
     assert qmv.MAX_SLOTS == 128 and qmv.MAX_LAYER_SLOTS == 32 and qmv.MAX_NTOK == 16
     B = qmv.ctypes.byref
     G = qmv.lib.qmv_moe_gather_ex
     cb = qmv.wdesc("cb3", 64, 64, 8, qi.LUT_CB3)
-    assert G(B(cb), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) == qmv.QMV_EINVAL      # 64 codebook slots
+    assert G(B(cb), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) != qmv.QMV_EINVAL      # 64 codebook slots: sorted gather
+    assert G(B(cb), FAKE, FAKE, 0, FAKE, 16, 9, FAKE, 0, 0) == qmv.QMV_EINVAL     # 144 slots
     mx = qmv.wdesc("mxfp4", 64, 64, 8)
     assert G(B(mx), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL   # fp16: no sorted path
     assert G(B(mx), FAKE, FAKE, 0, FAKE, 17, 1, FAKE, 0, 0) == qmv.QMV_EINVAL     # 17 tokens
