@@ -888,11 +888,27 @@ def run_alu(args):
         ev1.record()
         torch.cuda.synchronize()
         rows.append((fmt, nv, w * reps / (ev0.elapsed_time(ev1) * 1e-3)))
+    # the time must scale with the iteration count (a loop the compiler
+    # shortened would not): one case at 4x the iterations
+    scale = {}
+    for it in (iters, 4 * iters):
+        w, th = qmv.qmv_debug_chunk_rate("mxfp4", 1, 2, it)
+        sink = torch.empty(th, dtype=torch.float32, device=dev)
+        qmv.qmv_debug_chunk_rate("mxfp4", 1, 2, it, sink)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        qmv.qmv_debug_chunk_rate("mxfp4", 1, 2, it, sink)
+        ev1.record()
+        torch.cuda.synchronize()
+        scale[it] = ev0.elapsed_time(ev1) * 1e3
     time.sleep(0.3)
     wall1 = time.time()
     sampler.stop()
     clocks = sampler.summary(wall0, wall1)
     mhz = clocks.get("sm_mhz") or 2070.0
+    print(f"mxfp4 nv=1 launch time at {iters} / {4 * iters} iterations: {scale[iters]:.1f} / "
+          f"{scale[4 * iters]:.1f} us (ratio {scale[4 * iters] / scale[iters]:.2f})", flush=True)
     out = []
     for fmt, nv, wps in rows:
         rate = wps / sms / (mhz * 1e6)

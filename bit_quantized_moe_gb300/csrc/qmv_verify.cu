@@ -39,17 +39,18 @@
 // layout) and one of `split` K ranges; the `split` CTAs of a row block form a
 // thread-block cluster and add their partial sums through distributed shared
 // memory in rank order (deterministic), each rank storing a share of the
-// outputs. Per CTA: 8 decoding warps -- a warp decodes 16 rows (two row
-// tiles) of every 64-column step, a lane taking one row and one of the two
-// 32-groups, its weight loads issued a window of steps ahead -- and one warp
-// that issues the MMAs. Three A buffers, each with a "full" barrier (one
-// arrival per decoding warp) and an "empty" one (tcgen05.commit); the
-// accumulators of kAccSteps steps live in tensor memory, each step's with an
-// "accumulated" barrier (tcgen05.commit) and a "drained" one (one arrival
-// per decoding warp). A decoding warp drains step st - kLag after decoding
-// step st: warps w and w + 4 read tensor-memory lanes 32 (w % 4) .. + 31
-// (one row each), tokens 0..7 and 8..15. A sorted gather adds a second grid
-// dimension of work items, one (expert, up to 16 of its slots) pair each.
+// outputs. Per CTA: 8 decoding warps -- warp w decodes rows 32 (w % 4) ..
+// + 31 (one per lane) and 32-group w / 4 of every 64-column step, its
+// weight loads issued a window of steps ahead -- and one warp that issues
+// the MMAs. Three A buffers, each with a "full" barrier (one arrival per
+// decoding warp) and an "empty" one (tcgen05.commit); the accumulators of
+// kAccSteps steps live in tensor memory, each step's with an "accumulated"
+// barrier (tcgen05.commit) and a "drained" one (one arrival per decoding
+// warp). A decoding warp drains step st - kLag after decoding step st: the
+// rows it decoded are exactly the tensor-memory lanes 32 (w % 4) .. + 31 it
+// may read, so each lane drains its own row and group for all 16 tokens with
+// the scale byte it decoded. A sorted gather adds a second grid dimension of
+// work items, one (expert, up to 16 of its slots) pair each.
 //
 // Operand layouts (no swizzle, K-major "canonical" core matrices of 8 rows x
 // 16 bytes): A step buffer (128 rows x 64 columns), core matrix (row group
@@ -422,15 +423,16 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     mbar_init(smem_addr(&done), 1);
     fence_mbar_init();
   }
-  // Weight stream: decoding warp w takes row tiles 2w and 2w + 1 of the
-  // block; lane (i, r8, h) takes row r8 of tile 2w + i and group
-  // 2 * step + h, so one warp load covers 16 rows x 2 adjacent lane blocks.
-  // The first window of loads goes out first (before griddepcontrol.wait
-  // when the caller guarantees the weights are not the preceding kernel's
-  // output), then the activations.
+  // Decoding warp w takes rows 32 (w % 4) .. + 31 of the block -- the
+  // tensor-memory lanes its drains may read -- and group 2 * step + w / 4 of
+  // every step: lane l decodes row 32 (w % 4) + l, and later drains that
+  // row's accumulator of the same group for all 16 tokens, with the E8M0
+  // byte it decoded itself. The first window of loads goes out first (before
+  // griddepcontrol.wait when the caller guarantees the weights are not the
+  // preceding kernel's output), then the activations.
   const bool decoder = tid < kDecoders;
-  const int h = lane & 1;
-  const int r = (warp & 7) * 16 + (lane >> 1);   // row of the block: tile 2w + (lane >> 4), row (lane >> 1) & 7
+  const int h = (warp >> 2) & 1;                 // group of the step
+  const int r = (warp & 3) * 32 + lane;          // row of the block = tensor-memory lane
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
@@ -467,61 +469,54 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   const uint32_t tmem = tmem_slot;
   bool ok = true;
 
-  // Drain of step sd by this decoding warp: rows 32 (warp % 4) + lane, tokens tq .. tq + 7.
-  const int tq = (warp >> 2) * 8;
-  const int rr = (warp & 3) * 32 + lane;
-  const int drow = rb * kVRows + rr;
+  // Drain of step sd: this thread's row, its group 2 sd + h, 16 tokens in
+  // two halves of 8 columns; the scale byte is the one this thread stored
+  // when it decoded the block (its own earlier write, no barrier needed).
   const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  float acc[8];
+  float acc[kVTok];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < kVTok; ++i) acc[i] = 0.f;
+  uint16_t* my_sc = sc + warp * 32 + lane;       // [kScaleRing][256 decoding threads]
   auto drain = [&](int sd) {
-    // the A-buffer barrier of step sd orders every decoding thread's scale
-    // bytes of that step before these reads; the accumulator barrier says
-    // the step's MMAs are complete
-    ok = ok && mbar_wait_bounded(smem_addr(&full[sd % kVBufs]), (uint32_t)(sd / kVBufs) & 1u, kWaitLimitNs);
     ok = ok && mbar_wait_bounded(smem_addr(&accd[sd % kAccSteps]), (uint32_t)(sd / kAccSteps) & 1u, kWaitLimitNs);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
     tc_fence_after();
-    const uint16_t* scs = sc + (sd % kScaleRing) * 2 * kVRows + rr;
     constexpr int per = F::blocks / 2;   // accumulators per 32-group: 1, or 2 half-blocks
+    const uint32_t col0 = (uint32_t)(((sd % kAccSteps) * F::blocks + h * per) * kVTok);
+    const int gl = 2 * sd + h;
+    const float* f = aux + gl * kVTok;
+    const uint32_t eb = my_sc[(sd % kScaleRing) * kDecoders];
+    const float s0 = e8m0_to_f32(eb & 0xffu), s1 = e8m0_to_f32(eb >> 8);
 #pragma unroll
-    for (int gh = 0; gh < 2; ++gh) {
+    for (int th = 0; th < 2; ++th) {
       float v[per][8];
 #pragma unroll
-      for (int j = 0; j < per; ++j) {
-        tmem_ld8(tlane + (uint32_t)(((sd % kAccSteps) * F::blocks + gh * per + j) * kVTok + tq), v[j]);
-      }
+      for (int j = 0; j < per; ++j) tmem_ld8(tlane + col0 + (uint32_t)(j * kVTok + th * 8), v[j]);
       tmem_wait_ld();
-      const int gl = 2 * sd + gh;
-      const float* f = aux + gl * kVTok + tq;
-      const uint32_t eb = scs[gh * kVRows];
-      if constexpr (fmt_is_mx(FMT)) {
-        const float s = e8m0_to_f32(eb & 0xffu);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] = fmaf(s, v[0][t] * f[t], acc[t]);
-      } else if constexpr (per == 2) {
-        const float s0 = e8m0_to_f32(eb & 0xffu), s1 = e8m0_to_f32(eb >> 8);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] = fmaf(f[t], fmaf(s0, v[0][t], s1 * v[1][t]), acc[t]);
-      } else {
-        const float s = e8m0_to_f32(eb & 0xffu);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] = fmaf(f[t], s * v[0][t], acc[t]);
+      for (int t = 0; t < 8; ++t) {
+        const int tt = th * 8 + t;
+        if constexpr (fmt_is_mx(FMT)) {
+          acc[tt] = fmaf(s0, v[0][t] * f[tt], acc[tt]);
+        } else if constexpr (per == 2) {
+          acc[tt] = fmaf(f[tt], fmaf(s0, v[0][t], s1 * v[1][t]), acc[tt]);
+        } else {
+          acc[tt] = fmaf(f[tt], s0 * v[0][t], acc[tt]);
+        }
       }
       if constexpr (!fmt_is_mx(FMT)) {
         const int g = g0 + gl;
-        if (p.dbg != nullptr && drow < p.N && g < g1) {
+        if (p.dbg != nullptr && row < p.N && g < g1) {
           const int nb = p.K / F::span;
 #pragma unroll
           for (int j = 0; j < per; ++j) {
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-              const int tt = tq + t;
+              const int tt = th * 8 + t;
               if (tt < T) {
                 const int slot = (p.ids == nullptr) ? tt : s_slot[tt];
-                p.dbg[((size_t)slot * p.N + drow) * nb + g * per + j] = (int32_t)v[j][t];
+                p.dbg[((size_t)slot * p.N + row) * nb + g * per + j] = (int32_t)v[j][t];
               }
             }
           }
@@ -547,7 +542,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
             if (!ok) break;
           }
           decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
-          sc[(st % kScaleRing) * 2 * kVRows + h * kVRows + r] = (uint16_t)win[u].e;
+          my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
           const int gn = g0 + 2 * (st + kWindow) + h;
           load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
           fence_proxy_async_smem();
@@ -587,11 +582,17 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   if (!ok && lane == 0) set_status(kStatusWaitTile);
 
   // Partial sums part[t][row] (the A buffers are free: every MMA that read
-  // them completed before the last drain).
+  // them completed before the last drain): the even groups' sums (h = 0)
+  // first, then the odd groups' added in that order.
   __syncthreads();
-  if (decoder) {
+  if (decoder && h == 0) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) part[(tq + t) * kVRows + rr] = acc[t];
+    for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] = acc[t];
+  }
+  __syncthreads();
+  if (decoder && h == 1) {
+#pragma unroll
+    for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] += acc[t];
   }
   tc_fence_before();
 
