@@ -88,6 +88,26 @@ QMV_HD inline Geometry make_geometry(int f, int N, int K) {
   return g;
 }
 
+// Division by a divisor fixed for a launch, without a division instruction:
+// q = (n * m) >> 40 with m = ceil(2^40 / d). Writing m = (2^40 + r) / d
+// (0 <= r < d), n * m / 2^40 = n / d + n r / (d 2^40), so the floor is exact
+// whenever n * d <= 2^40; every quotient taken with it has n < 2^23 and
+// d < 2^17.
+struct FastDiv {
+  uint64_t m;
+  uint32_t d;
+};
+
+QMV_HD inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.m = ((1ull << 40) + d - 1) / d;
+  return f;
+}
+
+QMV_HD inline uint32_t fast_div(uint32_t n, const FastDiv& f) { return (uint32_t)(((uint64_t)n * f.m) >> 40); }
+QMV_HD inline uint32_t fast_mod(uint32_t n, const FastDiv& f) { return n - fast_div(n, f) * f.d; }
+
 // Byte offset of tile (row tile rt, chunk c) inside one expert.
 QMV_HD inline uint64_t tile_offset(const Geometry& g, int rt, int c) {
   return (uint64_t)rt * g.rowtile + (uint64_t)c * g.full_tile;

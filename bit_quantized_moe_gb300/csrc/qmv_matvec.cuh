@@ -134,6 +134,7 @@ struct KParams {
   int splits;             // K ranges per item (split-K inside a CTA), >= 1
   int split_chunks;       // chunks per K range (the last may be shorter)
   int items_per_cta;      // upper bound on items per CTA (split-K partial slots)
+  FastDiv fd_rt, fd_split, fd_grid, fd_grp, fd_per;   // row_tiles, splits, grid, K / 32, x_vec_bytes / 16
 #ifdef QMV_PHASE_PROBE
   int probe_slot;         // launch slot of the phase probe, -1 = not recorded
 #endif
@@ -288,26 +289,26 @@ struct WarpPipe {
 };
 
 __device__ __forceinline__ int task_item(const KParams& p, const WarpPipe& wp, int lt) {
-  return wp.first + (lt / p.splits) * wp.stride;
+  return wp.first + (int)fast_div((uint32_t)lt, p.fd_split) * wp.stride;
 }
 
 // The CTA's items first, first + stride, ... (count of them) out of n.
 __device__ __forceinline__ void cta_items(const KParams& p, int n, int& first, int& stride, int& count) {
   const int b = blockIdx.x, G = gridDim.x;
   if (p.contig) {
-    const int per = n / G, rem = n % G;
+    const int per = (int)fast_div((uint32_t)n, p.fd_grid), rem = n - per * G;
     first = b * per + (b < rem ? b : rem);
     count = per + (b < rem ? 1 : 0);
     stride = 1;
   } else {
     first = b;
     stride = G;
-    count = (b < n) ? (n - b + G - 1) / G : 0;
+    count = (b < n) ? (int)fast_div((uint32_t)(n - b + G - 1), p.fd_grid) : 0;
   }
 }
 
 __device__ __forceinline__ void task_chunks(const KParams& p, int lt, int& c0, int& c1) {
-  c0 = (lt % p.splits) * p.split_chunks;
+  c0 = (int)fast_mod((uint32_t)lt, p.fd_split) * p.split_chunks;
   c1 = min(p.chunks, c0 + p.split_chunks);
 }
 
@@ -318,8 +319,9 @@ __device__ __forceinline__ void cursor_to(WarpPipe& wp, int lt) {
   const KParams& p = *wp.p;
   task_chunks(p, lt, wp.iss_c, wp.iss_c1);
   const int item = task_item(p, wp, lt);
-  const Entry& e = wp.ent[item / p.row_tiles];
-  wp.iss_base = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)(item % p.row_tiles) * p.rowtile;
+  const int ei = (int)fast_div((uint32_t)item, p.fd_rt);
+  const Entry& e = wp.ent[ei];
+  wp.iss_base = p.w + (uint64_t)e.expert * p.expert_stride + (uint64_t)(item - ei * p.row_tiles) * p.rowtile;
 }
 
 // Lane 0: copies the next tile of this warp's task sequence into ring stage
@@ -469,14 +471,16 @@ __device__ __forceinline__ void convert_group_mxfp4(uint32_t (&w)[16], uint8_t* 
 // Units are numbered over the CTA's list of vectors: unit u is group (or
 // block, or piece) u % per_vec of vector vlist[u / per_vec], staged at that
 // vector's index, or at list position u / per_vec in a compact region.
-__device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, const int* vlist, int g0, int n, int groups,
-                                                  uint32_t vec_bytes, uint32_t (&w)[kStageU][16]) {
+__device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, const int* vlist, int g0, int n,
+                                                  const FastDiv& groups, uint32_t vec_bytes,
+                                                  uint32_t (&w)[kStageU][16]) {
 #pragma unroll
   for (int u = 0; u < kStageU; ++u) {
     const int gi = g0 + u * blockDim.x;
     if (gi < n) {
-      const int v = vlist ? vlist[gi / groups] : gi / groups;
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)v * vec_bytes + (size_t)(gi % groups) * 64);
+      const int vi = (int)fast_div((uint32_t)gi, groups), g = gi - vi * (int)groups.d;
+      const int v = vlist ? vlist[vi] : vi;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)v * vec_bytes + (size_t)g * 64);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 v = src[q];
@@ -487,23 +491,24 @@ __device__ __forceinline__ void load_groups_mxfp4(const uint8_t* x, const int* v
 }
 
 __device__ __forceinline__ void store_groups_mxfp4(uint8_t* xs, float* xinv, const int* vlist, bool compact,
-                                                   int g0, int n, int groups, uint32_t vec_bytes,
+                                                   int g0, int n, const FastDiv& groups, uint32_t vec_bytes,
                                                    uint32_t (&w)[kStageU][16]) {
 #pragma unroll
   for (int u = 0; u < kStageU; ++u) {
     const int gi = g0 + u * blockDim.x;
     if (gi < n) {
-      const int v = compact ? gi / groups : (vlist ? vlist[gi / groups] : gi / groups), g = gi % groups;
-      convert_group_mxfp4(w[u], xs + (size_t)v * vec_bytes + (size_t)g * 64, xinv + v * groups + g);
+      const int vi = (int)fast_div((uint32_t)gi, groups), g = gi - vi * (int)groups.d;
+      const int v = compact ? vi : (vlist ? vlist[vi] : vi);
+      convert_group_mxfp4(w[u], xs + (size_t)v * vec_bytes + (size_t)g * 64, xinv + v * (int)groups.d + g);
     }
   }
 }
 
 template <class Mid>
 __device__ __forceinline__ void stage_x_mxfp4(const uint8_t* x, uint8_t* xs, float* xinv, const int* vlist,
-                                              bool compact, int nvl, int K, uint32_t vec_bytes, Mid&& mid) {
-  const int groups = K / 32;
-  const int n = nvl * groups;
+                                              bool compact, int nvl, const FastDiv& groups, uint32_t vec_bytes,
+                                              Mid&& mid) {
+  const int n = nvl * (int)groups.d;
   const int step = kStageU * blockDim.x;
   uint32_t w[kStageU][16];
   load_groups_mxfp4(x, vlist, threadIdx.x, n, groups, vec_bytes, w);
@@ -550,11 +555,12 @@ __device__ __forceinline__ void quantize_block_q8(const float (&f)[32], uint8_t*
   reinterpret_cast<__half*>(out + K)[blk] = __float2half_rn(d);
 }
 
-__device__ __forceinline__ void load_block_f32(const float* x, const int* vlist, int bi, int n, int blocks, int K,
-                                               float (&f)[32]) {
+__device__ __forceinline__ void load_block_f32(const float* x, const int* vlist, int bi, int n,
+                                               const FastDiv& blocks, int K, float (&f)[32]) {
   if (bi < n) {
-    const int v = vlist ? vlist[bi / blocks] : bi / blocks;
-    const float4* src = reinterpret_cast<const float4*>(x + (size_t)v * K + (size_t)(bi % blocks) * 32);
+    const int vi = (int)fast_div((uint32_t)bi, blocks), b = bi - vi * (int)blocks.d;
+    const int v = vlist ? vlist[vi] : vi;
+    const float4* src = reinterpret_cast<const float4*>(x + (size_t)v * K + (size_t)b * 32);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float4 v = src[i];
@@ -565,17 +571,18 @@ __device__ __forceinline__ void load_block_f32(const float* x, const int* vlist,
 
 template <class Mid>
 __device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, const int* vlist, bool compact,
-                                                  int nvl, int K, uint32_t vec_bytes, Mid&& mid) {
-  const int blocks = K / 32;
-  const int n = nvl * blocks;
+                                                  int nvl, int K, const FastDiv& blocks, uint32_t vec_bytes,
+                                                  Mid&& mid) {
+  const int n = nvl * (int)blocks.d;
   float f[32];
   int bi = threadIdx.x;
   load_block_f32(x, vlist, bi, n, blocks, K, f);
   mid();
   for (;;) {
     if (bi < n) {
-      const int v = compact ? bi / blocks : (vlist ? vlist[bi / blocks] : bi / blocks);
-      quantize_block_q8(f, xs + (size_t)v * vec_bytes, K, bi % blocks);
+      const int vi = (int)fast_div((uint32_t)bi, blocks), b = bi - vi * (int)blocks.d;
+      const int v = compact ? vi : (vlist ? vlist[vi] : vi);
+      quantize_block_q8(f, xs + (size_t)v * vec_bytes, K, b);
     }
     bi += blockDim.x;
     if (bi >= n) break;
@@ -588,10 +595,10 @@ __device__ __forceinline__ void stage_q8_from_f32(const float* x, uint8_t* xs, c
 // thread in flight.
 template <class Mid>
 __device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, const int* vlist, bool compact,
-                                             int nvl, uint32_t vec_bytes, Mid&& mid) {
+                                             int nvl, const FastDiv& pieces, Mid&& mid) {
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(xs);
-  const int per = (int)(vec_bytes / 16);
+  const int per = (int)pieces.d;
   const int n = nvl * per;
   const int step = 4 * blockDim.x;
   uint4 v[4];
@@ -603,7 +610,12 @@ __device__ __forceinline__ void stage_x_copy(const uint8_t* x, uint8_t* xs, cons
       const int i = i0 + u * blockDim.x;
       at[u] = 0;
       if (i < n) {
-        at[u] = vlist ? (size_t)vlist[i / per] * per + i % per : (size_t)i;
+        if (vlist) {
+          const int vi = (int)fast_div((uint32_t)i, pieces);
+          at[u] = (size_t)vlist[vi] * per + (i - vi * per);
+        } else {
+          at[u] = (size_t)i;
+        }
         v[u] = src[at[u]];
       }
     }
@@ -978,9 +990,10 @@ __device__ __forceinline__ bool run_tasks(const KParams& p, int& q, WarpPipe& wp
   const int warp = threadIdx.x >> 5;
   for (int lt = warp; lt < wp.n_tasks; lt += wp.warps) {
     const int item = task_item(p, wp, lt);
-    const Entry& e = wp.ent[item / p.row_tiles];
-    const int rt = item % p.row_tiles;
-    const int k = lt / p.splits, range = lt % p.splits;
+    const int ei = (int)fast_div((uint32_t)item, p.fd_rt);
+    const Entry& e = wp.ent[ei];
+    const int rt = item - ei * p.row_tiles;
+    const int k = (int)fast_div((uint32_t)lt, p.fd_split), range = lt - k * p.splits;
     int c0, c1;
     task_chunks(p, lt, c0, c1);
     bool ok = true;
@@ -1099,7 +1112,8 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     if (warp == 0) {
       uint32_t used = 0;
       if (items_here > 0) {
-        const int e0 = wp.first / p.row_tiles, e1 = (wp.first + items_here - 1) / p.row_tiles;
+        const int e0 = (int)fast_div((uint32_t)wp.first, p.fd_rt);
+        const int e1 = (int)fast_div((uint32_t)(wp.first + items_here - 1), p.fd_rt);
         for (int e = e0 + lane; e <= e1; e += 32) {
           for (int m = 0; m < ent[e].nv; ++m) used |= 1u << ent[e].vec[m];
         }
@@ -1115,7 +1129,8 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
       if (lane == 0) s_nvl = n_used;
       if (p.x_slots < p.nvec && items_here > 0) {
         __syncwarp();
-        const int e0 = wp.first / p.row_tiles, e1 = (wp.first + items_here - 1) / p.row_tiles;
+        const int e0 = (int)fast_div((uint32_t)wp.first, p.fd_rt);
+        const int e1 = (int)fast_div((uint32_t)(wp.first + items_here - 1), p.fd_rt);
         for (int e = e0 + lane; e <= e1; e += 32) {
           for (int m = 0; m < 4; ++m) {
             const int at = __popc(used & ((1u << ent[e].vec[m]) - 1u));
@@ -1165,14 +1180,15 @@ __global__ void __launch_bounds__(Shape<NV>::warps * 32, kCtasPerSm)
     probe_phase(p, kPhRingIssued);
   };
   if constexpr (fmt_is_mx(FMT) && ALT) {
-    stage_x_copy(p.x, xs, vlist, compact, nvl, p.x_vec_bytes, issue_rest);
+    stage_x_copy(p.x, xs, vlist, compact, nvl, p.fd_per, issue_rest);
     for (int i = threadIdx.x; i < p.x_slots * (p.K / 32); i += blockDim.x) xinv[i] = 1.0f;
   } else if constexpr (fmt_is_mx(FMT)) {
-    stage_x_mxfp4(p.x, xs, xinv, vlist, compact, nvl, p.K, p.x_vec_bytes, issue_rest);
+    stage_x_mxfp4(p.x, xs, xinv, vlist, compact, nvl, p.fd_grp, p.x_vec_bytes, issue_rest);
   } else if (p.flags & kFlagXF32) {
-    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, vlist, compact, nvl, p.K, p.x_vec_bytes, issue_rest);
+    stage_q8_from_f32(reinterpret_cast<const float*>(p.x), xs, vlist, compact, nvl, p.K, p.fd_grp, p.x_vec_bytes,
+                      issue_rest);
   } else {
-    stage_x_copy(p.x, xs, vlist, compact, nvl, p.x_vec_bytes, issue_rest);
+    stage_x_copy(p.x, xs, vlist, compact, nvl, p.fd_per, issue_rest);
   }
   __syncthreads();
   for (int q = first_round; q < ST; ++q) {
@@ -1292,6 +1308,11 @@ inline KParams make_params(const MatvecArgs& a) {
   p.splits = 1;
   p.split_chunks = g.chunks;
   p.items_per_cta = 0;
+  p.fd_rt = make_fastdiv((uint32_t)g.row_tiles);
+  p.fd_split = make_fastdiv(1);
+  p.fd_grid = make_fastdiv(1);
+  p.fd_grp = make_fastdiv((uint32_t)(a.K / 32));
+  p.fd_per = make_fastdiv(p.x_vec_bytes / 16u);
 #ifdef QMV_PHASE_PROBE
   p.probe_slot = -1;
 #endif
@@ -1364,6 +1385,8 @@ cudaError_t launch_matvec(const MatvecArgs& a) {
   }
 #endif
   p.splits = plan.splits;
+  p.fd_split = make_fastdiv((uint32_t)plan.splits);
+  p.fd_grid = make_fastdiv((uint32_t)plan.grid);
   p.split_chunks = plan.split_chunks;
   p.items_per_cta = plan.items_per_cta;
   p.x_slots = plan.x_slots;
