@@ -101,6 +101,15 @@ struct VFmt {
   // codebooks, whose decode needs more registers (80-96 bytes in flight).
   static constexpr int window = fmt_is_mx(FMT) ? 128 / lane_code_bytes(FMT) : (FMT == CB2 ? 8 : 6);
   static constexpr int words = (FMT == CB3) ? 3 : lane_code_bytes(FMT) / 4;
+  // MX formats take the pre-scaled path: code x 2^(e-127) is exact in bf16
+  // for every E8M0 byte in [scale_lo, scale_hi] (MXFP4: 6 x 2^125 is below
+  // bf16's largest value and every product is a multiple of 2^-133, bf16's
+  // smallest subnormal; MXFP8: 448 x 2^119 and m / 8 x 2^-6 x 2^-124), so
+  // one accumulator per row sums bf16 x bf16 products for the whole K range
+  // and no per-group drain is needed; a row holding a scale byte outside the
+  // range is recomputed exactly on the CUDA cores afterwards.
+  static constexpr bool fast = fmt_is_mx(FMT);
+  static constexpr int alloc_cols = fast ? 32 : acc_cols;   // tensor memory allocation (32 at least)
 };
 
 struct VParams {
@@ -136,11 +145,15 @@ __device__ __forceinline__ uint64_t mma_desc(uint32_t addr, uint32_t lbo, uint32
 // kind::f16 instruction descriptor: fp32 accumulator (bits 4-5 = 1), A and B
 // both f16 (bits 7-9 and 10-12 = 0), both K-major, N = 16, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kVTok >> 3) << 17) | ((uint32_t)(kVRows >> 4) << 24);
+// The same with A and B both bf16 (bits 7-9 and 10-12 = 1), for the
+// pre-scaled path.
+constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
 
+template <bool BF16>
 __device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-               :: "r"(tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate));
+               :: "r"(tmem), "l"(a), "l"(b), "r"(BF16 ? kIdescBf16 : kIdesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -266,6 +279,51 @@ __device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t
   }
 }
 
+__device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t h2, float s) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Whether code x 2^(e-127) is exact in bf16 for every code of the format:
+// E8M0 bytes 0..252 (MXFP4), 3..246 (MXFP8).
+template <int FMT>
+__device__ __forceinline__ bool scale_in_bf16_range(uint32_t e) {
+  return (FMT == MXFP8) ? (e - 3u <= 243u) : (e <= 252u);
+}
+
+// Pre-scaled path (MX formats): 32 codes of a lane block -> 32 bf16 values
+// code x 2^(e-127) (exact for scale bytes in the format's safe range), four
+// 16-byte core-matrix rows. Returns whether the scale byte is outside it.
+template <int FMT>
+__device__ __forceinline__ bool decode_store_scaled(const Block<FMT>& b, uint8_t* a_row, int kk0) {
+  const float s = e8m0_to_f32(b.e);
+  uint32_t out[16];
+  if constexpr (FMT == MXFP4) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t h[4];
+      e2m1x8_to_f16x2(b.c[q], h);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[4 * q + i] = scaled_bf16x2(h[i], s);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t h[2];
+      e4m3x4_to_f16x2(b.c[q], h);
+      out[2 * q] = scaled_bf16x2(h[0], s);
+      out[2 * q + 1] = scaled_bf16x2(h[1], s);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
+        make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+  }
+  return !scale_in_bf16_range<FMT>(b.e);
+}
+
 // Activation operand B: one (token t, local 32-group gl) unit -- 32 f16
 // values into four core-matrix rows -- and its factor for the drain (MX:
 // 2^-s of the group's shift; codebooks: the q8_1 scale d as fp32).
@@ -284,7 +342,11 @@ __device__ __forceinline__ void stage_unit(const VParams& p, int vec, int g, boo
       const uint4 v = src[q];
       w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
     }
-    f = shift_group_to_f16(w);
+    if constexpr (VFmt<FMT>::fast) {
+      f = 1.0f;                          // bf16 as it is
+    } else {
+      f = shift_group_to_f16(w);
+    }
   } else {
     uint32_t qw[8];
     if (p.x_f32) {
@@ -326,6 +388,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   __shared__ __align__(8) uint64_t accf[kAccSteps];    // a step's accumulators drained (one arrival per decoding warp)
   __shared__ __align__(8) uint64_t done;               // every MMA complete (tcgen05.commit)
   __shared__ uint32_t tmem_slot;
+  __shared__ uint8_t s_unsafe[kVRows];                 // pre-scaled path: row has a scale byte outside the range
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)(blockIdx.x % (unsigned)p.split);
   const int rb = (int)(blockIdx.x / (unsigned)p.split);
@@ -408,7 +471,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_addr(&tmem_slot)), "r"(F::acc_cols));
+                 :: "r"(smem_addr(&tmem_slot)), "r"(F::alloc_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
@@ -423,16 +486,20 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     mbar_init(smem_addr(&done), 1);
     fence_mbar_init();
   }
-  // Decoding warp w takes rows 32 (w % 4) .. + 31 of the block -- the
-  // tensor-memory lanes its drains may read -- and group 2 * step + w / 4 of
-  // every step: lane l decodes row 32 (w % 4) + l, and later drains that
-  // row's accumulator of the same group for all 16 tokens, with the E8M0
-  // byte it decoded itself. The first window of loads goes out first (before
-  // griddepcontrol.wait when the caller guarantees the weights are not the
-  // preceding kernel's output), then the activations.
+  // Drained path: decoding warp w takes rows 32 (w % 4) .. + 31 of the block
+  // -- the tensor-memory lanes its drains may read -- and group 2 * step +
+  // w / 4 of every step: lane l decodes row 32 (w % 4) + l, and later drains
+  // that row's accumulator of the same group for all 16 tokens, with the
+  // E8M0 byte it decoded itself. The first window of loads goes out first
+  // (before griddepcontrol.wait when the caller guarantees the weights are
+  // not the preceding kernel's output), then the activations.
   const bool decoder = tid < kDecoders;
-  const int h = (warp >> 2) & 1;                 // group of the step
-  const int r = (warp & 3) * 32 + lane;          // row of the block = tensor-memory lane
+  // Pre-scaled path: lane pairs take the two groups of one row (warp w: rows
+  // 16 w .. 16 w + 15), so a warp load covers 16 rows x 32 contiguous bytes;
+  // drained path: warp w takes rows 32 (w % 4) .. + 31 (its tensor-memory
+  // lanes) and group w / 4.
+  const int h = F::fast ? (lane & 1) : ((warp >> 2) & 1);                              // group of the step
+  const int r = F::fast ? ((warp & 7) * 16 + (lane >> 1)) : ((warp & 3) * 32 + lane);  // row of the block
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
@@ -462,6 +529,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     }
   }
 
+  if (tid < kVRows) s_unsafe[tid] = 0;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -541,25 +609,33 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
-          decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
-          my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
+          if constexpr (F::fast) {
+            if (decode_store_scaled<FMT>(win[u], a_row + (size_t)b * kABytes, 4 * h)) s_unsafe[r] = 1;
+          } else {
+            decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
+            my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
+          }
           const int gn = g0 + 2 * (st + kWindow) + h;
           load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&full[b]));
-          if (st >= kLag) drain(st - kLag);
+          if constexpr (!F::fast) {
+            if (st >= kLag) drain(st - kLag);
+          }
         }
       }
     }
-    for (int sd = steps - kLag > 0 ? steps - kLag : 0; sd < steps && ok; ++sd) drain(sd);
+    if constexpr (!F::fast) {
+      for (int sd = steps - kLag > 0 ? steps - kLag : 0; sd < steps && ok; ++sd) drain(sd);
+    }
   } else if (lane == 0) {
     // MMA issue: step st once every decoding warp has written its A buffer
     // and the accumulators it reuses have been drained.
     for (int st = 0; st < steps && ok; ++st) {
       const int b = st % kVBufs;
       ok = mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
-      if (ok && st >= kAccSteps) {
+      if (!F::fast && ok && st >= kAccSteps) {
         ok = mbar_wait_bounded(smem_addr(&accf[st % kAccSteps]), (uint32_t)((st / kAccSteps) - 1) & 1u, kWaitLimitNs);
       }
       if (!ok) break;
@@ -568,13 +644,19 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
 #pragma unroll
       for (int j = 0; j < kVStepK / 16; ++j) {
-        const int blk = j * 16 / F::span;
-        const uint32_t col = (uint32_t)(((st % kAccSteps) * F::blocks + blk) * kVTok);
-        mma_f16(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                (j * 16 % F::span) != 0 ? 1u : 0u);
+        if constexpr (F::fast) {
+          // one accumulator for the whole K range
+          mma_f16<true>(tmem, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
+                        (st > 0 || j > 0) ? 1u : 0u);
+        } else {
+          const int blk = j * 16 / F::span;
+          const uint32_t col = (uint32_t)(((st % kAccSteps) * F::blocks + blk) * kVTok);
+          mma_f16<false>(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128),
+                         mma_desc(b0 + j * 2 * 256, 256, 128), (j * 16 % F::span) != 0 ? 1u : 0u);
+        }
       }
       mma_commit(smem_addr(&empty[b]));
-      mma_commit(smem_addr(&accd[st % kAccSteps]));
+      if constexpr (!F::fast) mma_commit(smem_addr(&accd[st % kAccSteps]));
     }
     mma_commit(smem_addr(&done));
     if (!mbar_wait_bounded(smem_addr(&done), 0u, kWaitLimitNs)) ok = false;
@@ -582,17 +664,87 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   if (!ok && lane == 0) set_status(kStatusWaitTile);
 
   // Partial sums part[t][row] (the A buffers are free: every MMA that read
-  // them completed before the last drain): the even groups' sums (h = 0)
-  // first, then the odd groups' added in that order.
+  // them completed before the MMA warp passed `done`, or before the last
+  // drain).
   __syncthreads();
-  if (decoder && h == 0) {
+  if constexpr (F::fast) {
+    // the accumulator: warps w and w + 4 read lanes 32 (w % 4) .., tokens 8 (w / 4) ..
+    tc_fence_after();
+    if (decoder && ok) {
+      const int th = (warp >> 2) & 1, tr = (warp & 3) * 32 + lane;
+      float v[8];
+      tmem_ld8(tlane + (uint32_t)(th * 8), v);
+      tmem_wait_ld();
 #pragma unroll
-    for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] = acc[t];
-  }
-  __syncthreads();
-  if (decoder && h == 1) {
+      for (int t = 0; t < 8; ++t) part[(th * 8 + t) * kVRows + tr] = v[t];
+    }
+    __syncthreads();
+    // rows holding a scale byte outside the pre-scaled range: recomputed on
+    // the CUDA cores, sum over groups of 2^(e-127) * (sum of code x x) in
+    // fp32 (the CUDA-core path's formula), one warp per row, the lanes
+    // taking groups and adding their sums in a fixed shuffle order
+    for (int rr = warp; rr < kVRows; rr += kVThreads / 32) {
+      if (!s_unsafe[rr]) continue;
+      const int orow = rb * kVRows + rr;
+      if (orow >= p.N) continue;
+      float sum[kVTok];
 #pragma unroll
-    for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] += acc[t];
+      for (int t = 0; t < kVTok; ++t) sum[t] = 0.f;
+      for (int g = g0 + lane; g < g1; g += 32) {
+        Block<FMT> bk;
+        load_block<FMT>(p, w, orow >> 3, orow & 7, g, true, bk);
+        const float sc = e8m0_to_f32(bk.e);
+        uint32_t hw[16];
+        if constexpr (FMT == MXFP4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t hq[4];
+            e2m1x8_to_f16x2(bk.c[q], hq);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hw[4 * q + i] = hq[i];
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t hq[2];
+            e4m3x4_to_f16x2(bk.c[q], hq);
+            hw[2 * q] = hq[0];
+            hw[2 * q + 1] = hq[1];
+          }
+        }
+        const int kl0 = (g - g0) * 32;
+        for (int t = 0; t < T; ++t) {
+          const uint8_t* xt = bbuf + (t >> 3) * 128 + (t & 7) * 16;
+          float d = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&hw[i]));
+            const int k = kl0 + 2 * i;
+            const uint32_t xb = *reinterpret_cast<const uint32_t*>(xt + (size_t)(k >> 3) * 256 + (k & 7) * 2);
+            d = fmaf(wf.x, __uint_as_float(xb << 16), d);
+            d = fmaf(wf.y, __uint_as_float(xb & 0xffff0000u), d);
+          }
+          sum[t] = fmaf(sc, d, sum[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kVTok; ++t) {
+        float v = sum[t];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) part[t * kVRows + rr] = v;
+      }
+    }
+  } else {
+    if (decoder && h == 0) {
+#pragma unroll
+      for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] = acc[t];
+    }
+    __syncthreads();
+    if (decoder && h == 1) {
+#pragma unroll
+      for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] += acc[t];
+    }
   }
   tc_fence_before();
 
@@ -619,7 +771,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   cluster.sync();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(F::acc_cols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(F::alloc_cols));
   }
 }
 
