@@ -107,8 +107,11 @@ cudaError_t launch_for(const MatvecArgs& a) {
 
 // Launch flags valid for a call of format fmt (dbg: the block-sum export).
 int check_flags(int fmt, uint32_t flags, bool dbg, const char* name) {
-  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16))
+  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_X_F32 | QMV_FLAG_X_F16 | QMV_FLAG_PATH_TENSOR |
+                          QMV_FLAG_PATH_CUDA_CORES))
     return fail(QMV_EINVAL, "%s: unknown flags 0x%x", name, flags);
+  if ((flags & QMV_FLAG_PATH_TENSOR) && (flags & QMV_FLAG_PATH_CUDA_CORES))
+    return fail(QMV_EINVAL, "%s: QMV_FLAG_PATH_TENSOR and QMV_FLAG_PATH_CUDA_CORES together", name);
   if ((flags & QMV_FLAG_X_F32) && (fmt_is_mx(fmt) || dbg))
     return fail(QMV_EINVAL, "%s: QMV_FLAG_X_F32 applies to the codebook formats only (not block sums)", name);
   if ((flags & QMV_FLAG_X_F16) && !fmt_is_mx(fmt))
@@ -118,6 +121,72 @@ int check_flags(int fmt, uint32_t flags, bool dbg, const char* name) {
 
 // Rows of the gate/up-interleaved matrix of a projection with N rows.
 int gate_up_rows(int N) { return 2 * ((N + kRows / 2 - 1) / (kRows / 2) * (kRows / 2)); }
+
+// A gather of more than QMV_MAX_LAYER_SLOTS routed slots takes the sorted
+// tensor-core gather when its slots share experts: the tensor-core work item
+// decodes an expert's weights once for up to 16 of its slots, so it pays
+// when experts carry several slots each. With few slots per expert (many
+// experts, a uniform router) the CUDA-core gather streams the same weights
+// and decodes them more cheaply, so the call runs as CUDA-core gathers of
+// whole tokens, QMV_MAX_LAYER_SLOTS slots at a time (an expert shared by two
+// of them is streamed by each). Measured on GB300 (2880^2 MXFP4 and
+// 7168 x 2048 / 2048 x 7168 codebook experts, 64-128 slots): the MX tensor
+// path breaks even at 4 slots per expert; the codebooks' (one accumulator
+// per block, drained on the CUDA cores) at about 12.
+constexpr int kSortedMinSlotsPerExpertMx = 4;
+constexpr int kSortedMinSlotsPerExpertCb = 12;
+
+bool sorted_gather_pays(const MatvecArgs& a) {
+  const int nslots = a.ntok * a.top_k;
+  const int experts = a.n_experts < nslots ? a.n_experts : nslots;
+  const int need = fmt_is_mx(a.fmt) ? kSortedMinSlotsPerExpertMx : kSortedMinSlotsPerExpertCb;
+  return nslots >= need * experts;
+}
+
+// Codebook dense verify batches take the tensor cores only when the
+// CUDA-core path's weight streams (one per 4 tokens, side by side) would
+// overflow the L2 cache: below that the repeated streams hit L2 and the
+// CUDA cores are faster (measured on GB300: 7168 x 2048 CB3 and 2048 x 7168
+// CB2 at 16 tokens 10.4 / 11.3 us on the CUDA cores against 14.9 / 19.1 us
+// on the tensor cores; 7168^2 CB4 47.0 against 39.6 us).
+constexpr uint64_t kCbDenseTensorBytes = 64ull << 20;
+
+bool dense_tensor_pays(const MatvecArgs& a) {
+  if (fmt_is_mx(a.fmt)) return true;
+  const uint64_t streams = (uint64_t)(a.ntok + 3) / 4;
+  return streams * make_geometry(a.fmt, a.N, a.K).expert > kCbDenseTensorBytes;
+}
+
+// Whether the call runs on the tensor cores (dense verify batch or sorted
+// gather), else on the CUDA-core matvec (one launch, or one per token range
+// for a gather of more than QMV_MAX_LAYER_SLOTS slots).
+bool use_tensor_cores(const MatvecArgs& a) {
+  if (a.path == 2 || !verify_supported(a)) return false;
+  return a.path == 1 || (a.ids == nullptr ? dense_tensor_pays(a) : sorted_gather_pays(a));
+}
+
+// Tokens per CUDA-core launch of a gather (all of them up to
+// QMV_MAX_LAYER_SLOTS routed slots).
+int gather_launch_tokens(const MatvecArgs& a) {
+  return (a.ids != nullptr && a.ntok * a.top_k > QMV_MAX_LAYER_SLOTS) ? QMV_MAX_LAYER_SLOTS / a.top_k : a.ntok;
+}
+
+// The CUDA-core gather of tokens [t0, t0 + n): ids, activations, outputs and
+// block sums offset to the range's first slot.
+MatvecArgs token_range(const MatvecArgs& a, int t0, int n) {
+  MatvecArgs b = a;
+  const int s0 = t0 * a.top_k;
+  const size_t xvec = fmt_is_mx(a.fmt) ? (size_t)a.K * 2
+                                       : (a.x_f32 ? (size_t)a.K * 4 : (size_t)q8_vec_bytes(a.K));
+  const size_t ysz = fmt_is_mx(a.fmt) ? 2 : 4;
+  b.ntok = n;
+  b.ids = a.ids + s0;
+  b.x = static_cast<const uint8_t*>(a.x) + (size_t)(a.per_slot ? s0 : t0) * xvec;
+  b.nvec = a.per_slot ? n * a.top_k : n;
+  b.y = static_cast<uint8_t*>(a.y) + (size_t)s0 * a.out_n * ysz;
+  if (a.dbg != nullptr) b.dbg = a.dbg + (size_t)s0 * a.N * (a.K / fmt_group(a.fmt));
+  return b;
+}
 
 // Validates one matvec call and fills `a` (no launch).
 int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_slot, const int32_t* ids,
@@ -179,16 +248,12 @@ int prepare_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int p
   a.x_f16 = (flags & QMV_FLAG_X_F16) != 0;
   a.glu = glu;
   a.out_n = desc_in->N;
+  a.path = (flags & QMV_FLAG_PATH_TENSOR) ? 1 : ((flags & QMV_FLAG_PATH_CUDA_CORES) ? 2 : 0);
   a.stream = stream;
-  const bool verify = verify_supported(a);
-  if (gather && ntok * top_k > QMV_MAX_LAYER_SLOTS && !verify)
-    return fail(QMV_EINVAL, "%s: more than %d routed slots run the sorted tensor-core gather, which takes "
-                "bf16 (MX) or q8_1 / fp32 (codebook) activations, not fp16 and not the gate/up fusion", name,
-                QMV_MAX_LAYER_SLOTS);
   const DevInfo* di = dev_info();
   if (di == nullptr) return cuda_fail(cudaGetLastError(), name);
-  if (verify) return QMV_OK;   // tensor-core path, fixed shared memory
-  const size_t smem = matvec_smem_bytes(a);
+  if (use_tensor_cores(a)) return QMV_OK;   // tensor-core path, fixed shared memory
+  const size_t smem = matvec_smem_bytes(token_range(a, 0, gather_launch_tokens(a)));
   if (smem == 0 || smem > di->smem_optin)
     return fail(QMV_ESHAPE, "%s: %d activation vectors of K=%d do not fit in shared memory", name, a.nvec,
                 desc->K);
@@ -203,7 +268,15 @@ int run_matvec(const qmv_wdesc* desc_in, const void* w, const void* x, int per_s
                                 glu, a);
   if (rc) return rc;
   g_launch_stage = "";
-  cudaError_t e = verify_supported(a) ? launch_verify(a) : launch_for(a);
+  cudaError_t e = cudaSuccess;
+  if (use_tensor_cores(a)) {
+    e = launch_verify(a);
+  } else {
+    const int per = gather_launch_tokens(a);
+    for (int t0 = 0; t0 < a.ntok && e == cudaSuccess; t0 += per) {
+      e = launch_for(per < a.ntok ? token_range(a, t0, a.ntok - t0 < per ? a.ntok - t0 : per) : a);
+    }
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(QMV_ECUDA, "%s: %s failed: %s (%s)", name, g_launch_stage, cudaGetErrorName(e),
@@ -398,7 +471,7 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w, const void* x, 
 // Workspace of qmv_moe_layer: h (MXFP4: bf16; codebooks: fp32).
 size_t qmv_moe_layer_workspace_bytes(const qmv_wdesc* gu, int32_t ntok, int32_t top_k) {
   if (check_desc(gu) || ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK ||
-      ntok * top_k > QMV_MAX_LAYER_SLOTS)
+      ntok * top_k > QMV_MAX_SLOTS)
     return 0;
   const size_t slots = (size_t)ntok * top_k;
   if (fmt_is_mx(gu->fmt)) return (slots * gu->N * 2 + 255) / 256 * 256;
@@ -420,7 +493,7 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   if (down->K != gu->N) return fail(QMV_ESHAPE, "%s: down K=%d must equal gate/up N=%d", name, down->K, gu->N);
   if (down->n_experts != gu->n_experts)
     return fail(QMV_EINVAL, "%s: gate/up and down expert counts differ (%d, %d)", name, gu->n_experts, down->n_experts);
-  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK || ntok * top_k > QMV_MAX_LAYER_SLOTS)
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK || ntok * top_k > QMV_MAX_SLOTS)
     return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d out of range", name, ntok, top_k);
   const size_t need = qmv_moe_layer_workspace_bytes(gu, ntok, top_k);
   if (ws_bytes < need) return fail(QMV_ESIZE, "%s: workspace %zu bytes < %zu", name, ws_bytes, need);
@@ -432,7 +505,8 @@ int qmv_moe_layer(const qmv_wdesc* gu, const void* w_gu, const qmv_wdesc* down, 
   // it stages it.
   rc = run_matvec(gu, w_gu, x, 0, ids, ntok, top_k, ws, nullptr, 0, s, name, flags, true);
   if (rc) return rc;
-  const uint32_t down_flags = QMV_FLAG_PREFETCH_INPUTS | (flags & QMV_FLAG_X_F16) |
+  const uint32_t down_flags = QMV_FLAG_PREFETCH_INPUTS | (flags & (QMV_FLAG_X_F16 | QMV_FLAG_PATH_TENSOR |
+                                                                    QMV_FLAG_PATH_CUDA_CORES)) |
                               (fmt_is_mx(gu->fmt) ? 0u : (uint32_t)QMV_FLAG_X_F32);
   return run_matvec(down, w_down, ws, 1, ids, ntok, top_k, y, nullptr, 0, s, name, down_flags);
 }
@@ -518,9 +592,17 @@ int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t g
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
                          const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
                          size_t sums_bytes, void* stream) {
+  return qmv_debug_block_sums_ex(desc, w, x, per_slot_x, ids, ntok, top_k, y, sums, sums_bytes, 0u, stream);
+}
+
+int qmv_debug_block_sums_ex(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
+                            const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
+                            size_t sums_bytes, uint32_t flags, void* stream) {
   if (sums == nullptr) return fail(QMV_EINVAL, "qmv_debug_block_sums: sums must be non-NULL");
+  if (flags & ~(uint32_t)(QMV_FLAG_PREFETCH_INPUTS | QMV_FLAG_PATH_TENSOR | QMV_FLAG_PATH_CUDA_CORES))
+    return fail(QMV_EINVAL, "qmv_debug_block_sums: flags 0x%x (prefetch and path flags only)", flags);
   return run_matvec(desc, w, x, per_slot_x, ids, ntok, top_k, y, sums, sums_bytes,
-                    static_cast<cudaStream_t>(stream), "qmv_debug_block_sums");
+                    static_cast<cudaStream_t>(stream), "qmv_debug_block_sums", flags);
 }
 
 int qmv_swiglu_bf16(const void* g, const void* u, void* h, int64_t n, void* stream) {

@@ -27,6 +27,7 @@ struct MatvecArgs {
   bool x_f16 = false;             // QMV_FLAG_X_F16: MX formats, fp16 x and y
   bool glu = false;               // gate/up-interleaved matrix, store silu(gate) * up
   int out_n = 0;                  // output rows per slot (0: N)
+  int path = 0;                   // 0: cost model, 1: tensor cores where possible, 2: CUDA cores
   cudaStream_t stream = nullptr;
 };
 

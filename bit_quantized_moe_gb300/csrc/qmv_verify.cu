@@ -8,49 +8,58 @@
 // the batched ROCmFPX MMQ that runs the verify batch). With more than a few
 // tokens the product is a skinny GEMM, D[n][t] = sum_k W[n][k] x[t][k], and
 // the CUDA-core matvec becomes ALU-bound (one FMA or dp4a lane per weight and
-// token). Here the CUDA cores only decode, and the block scales stay out of
-// the tensor-core operands:
-//   A (weights): the unscaled element values as f16, exact -- E2M1 and E4M3
-//      codes by cvt.rn.f16x2.e2m1x2 / e4m3x2, codebook codes through the byte
-//      permute table of the CUDA-core kernel into int8 and from there to f16
-//      (integers below 2^11 are exact in f16).
-//   B (activations): MX formats: the bf16 activations of each 32-group scaled
-//      by a power of two into f16 (the staging of the CUDA-core kernel: exact
-//      when the group's magnitudes span less than 2^31); codebook formats:
-//      the q8_1 codes as f16 (exact), their fp16 scale d kept aside.
-//   One tensor-memory accumulator per E8M0 group (32 columns; 16 for the
-//      half-block scales of CB2 / CB3): tcgen05.mma (kind::f16, f16 x f16 ->
-//      fp32, M = 128 rows, N = 16 tokens, K = 16). For the codebooks every
-//      product and partial sum is an integer below 2^24, so each accumulator
-//      is the exact integer block sum sum_{i in h} lut[c_i] * q_i.
-//   Drain: the decoding warps read each finished accumulator (tcgen05.ld) and
-//      apply the scales in fp32, as the CUDA-core path does --
-//        MX:        acc += 2^(e-127) * (sum * 2^-s)
-//        codebooks: acc += d_b * 2^(e-127) * isum  (two half-blocks:
-//                   d_b * (2^(e0-127) * isum0 + 2^(e1-127) * isum1))
-//      ("perf(ggml/hip): optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...", the
-//      review reply's dot structure; "perf(rocm): add an mxfp4 arm ...",
-//      "Current Behavior": E8M0 uint8 scales). So every legal scale byte
-//      0..254 is applied exactly (255 gives NaN), and the results differ from
-//      the CUDA-core path only in the order of fp32 additions; the integer
-//      block sums are bit-identical.
+// token). Here the CUDA cores only decode and one thread issues tcgen05.mma
+// (kind::f16, M = 128 rows, N = 16 tokens, K = 16) into tensor memory.
+//
+// MX formats (verify_mx_kernel) -- bf16 operands, one accumulator per row:
+//   A (weights): code x 2^(e - e_ref) as bf16, where e_ref is the row's
+//      first E8M0 byte in the CTA's K range plus kRefMargin (at most 254).
+//      The factor 2^(e - e_ref) (e - e_ref in [-24, 0]) is an exact f16, so
+//      one mixed-precision FMA
+//      (fma.rn.f32.f16, f16 inputs, fp32 result) makes each product exactly
+//      and cvt.rn.bf16x2.f32 packs it without rounding (E2M1: two
+//      significant bits, E4M3: four, far above bf16's smallest subnormal).
+//   B (activations): the bf16 vectors as they are.
+//   Products of bf16 values are exact in fp32, so the accumulator holds
+//      sum_k code x 2^(e - e_ref) x x in fp32, and the epilogue multiplies it
+//      by 2^(e_ref - 127) ("perf(rocm): add an mxfp4 arm ...", "Current
+//      Behavior": E8M0 scale 2^(e-127)): a power of two, exact unless the
+//      product leaves fp32's normal range. The result differs from the
+//      CUDA-core path only in the order of the fp32 additions. A row holding
+//      a scale byte outside [e_ref - 24, e_ref] (its bytes spread wider than
+//      the margin allows, or the NaN byte 255) is flagged while it is decoded
+//      and recomputed exactly on the CUDA cores after the MMAs (sum over
+//      groups of 2^(e-127) x sum(code x x) in fp32).
+//
+// Codebook formats (verify_kernel) -- exact integer block sums:
+//   A (weights): codebook values through the byte permute table of the
+//      CUDA-core kernel into int8 and from there to f16 (exact).
+//   B (activations): the q8_1 codes as f16 (exact), their fp16 scale d kept
+//      aside.
+//   One tensor-memory accumulator per E8M0 group (16 columns per half-block
+//      scale of CB2 / CB3): every product and partial sum is an integer below
+//      2^24, so each accumulator is the exact integer block sum
+//      sum_{i in h} lut[c_i] * q_i. The decoding warps drain each finished
+//      accumulator (tcgen05.ld) and apply d_b * 2^(e-127) in fp32 (two
+//      half-blocks: d_b * (2^(e0-127) * isum0 + 2^(e1-127) * isum1)), the dot
+//      structure of the review reply in "perf(ggml/hip): optimize ROCMFPX
+//      fp3/fp2 MMVQ on RDNA ...".
 //
 // Work decomposition: a CTA owns 128 rows (16 row tiles of the packed
 // layout) and one of `split` K ranges; the `split` CTAs of a row block form a
 // thread-block cluster and add their partial sums through distributed shared
 // memory in rank order (deterministic), each rank storing a share of the
-// outputs. Per CTA: 8 decoding warps -- warp w decodes rows 32 (w % 4) ..
-// + 31 (one per lane) and 32-group w / 4 of every 64-column step, its
-// weight loads issued a window of steps ahead -- and one warp that issues
-// the MMAs. Three A buffers, each with a "full" barrier (one arrival per
-// decoding warp) and an "empty" one (tcgen05.commit); the accumulators of
-// kAccSteps steps live in tensor memory, each step's with an "accumulated"
-// barrier (tcgen05.commit) and a "drained" one (one arrival per decoding
-// warp). A decoding warp drains step st - kLag after decoding step st: the
-// rows it decoded are exactly the tensor-memory lanes 32 (w % 4) .. + 31 it
-// may read, so each lane drains its own row and group for all 16 tokens with
-// the scale byte it decoded. A sorted gather adds a second grid dimension of
-// work items, one (expert, up to 16 of its slots) pair each.
+// outputs. Per CTA: 8 decoding warps, their weight loads issued a window of
+// steps ahead, and one warp that issues the MMAs. Three A buffers of 64
+// columns, each with a "full" barrier (one arrival per decoding warp) and an
+// "empty" one (tcgen05.commit). MX: lane pairs take the two 32-groups of one
+// row (warp w: rows 16 w .. 16 w + 15), so a warp load covers 16 rows x 32
+// contiguous bytes. Codebooks: warp w decodes rows 32 (w % 4) .. + 31 (the
+// tensor-memory lanes it may read) and group w / 4 of every step; the
+// accumulators of kAccSteps steps live in tensor memory, each step's with an
+// "accumulated" barrier (tcgen05.commit) and a "drained" one, and a warp
+// drains step st - kLag after decoding step st. A sorted gather adds a second
+// grid dimension of work items, one (expert, up to 16 of its slots) pair each.
 //
 // Operand layouts (no swizzle, K-major "canonical" core matrices of 8 rows x
 // 16 bytes): A step buffer (128 rows x 64 columns), core matrix (row group
@@ -80,36 +89,34 @@ constexpr int kDecoders = 256;   // decoding threads: two per row
 constexpr int kVThreads = kDecoders + 32;   // plus one warp that issues the MMAs
 constexpr int kVStepK = 64;      // columns per step (one A buffer): 2 groups of 32
 constexpr int kVBufs = 3;        // A buffers
-constexpr int kAccSteps = 4;     // steps whose accumulators tensor memory holds at once
-constexpr int kLag = 2;          // a decoding warp drains step st - kLag after decoding step st
-constexpr int kScaleRing = 8;    // steps of E8M0 bytes kept for the drains
+constexpr int kAccSteps = 4;     // codebooks: steps whose accumulators tensor memory holds at once
+constexpr int kLag = 2;          // codebooks: a decoding warp drains step st - kLag after decoding step st
+constexpr int kScaleRing = 8;    // codebooks: steps of E8M0 bytes kept for the drains
 static_assert(kLag < kVBufs && kLag < kAccSteps, "drain lag within the buffer and accumulator rings");
 constexpr uint32_t kABytes = kVRows * kVStepK * 2;   // 16 KB
 constexpr uint32_t kALbo = kVRows / 8 * 128;          // A: k-group stride (16 row groups of 128 B)
 constexpr int kVMaxSplit = 8;    // cluster size limit (portable)
 constexpr int kVMaxSlots = 128;  // routed slots of a sorted gather
 constexpr int kVMaxSteps = 24;   // activation operand <= 48 KB (two CTAs per SM)
+constexpr int kMaxSpread = 24;   // MX: e - e_ref down to -24 (2^-24: f16's smallest subnormal)
+constexpr int kRefMargin = 12;   // MX: e_ref = first scale byte + 12: bytes within -12 .. +12 of the first
+
+// Codebooks: accumulators per step and tensor-memory columns.
+template <int FMT>
+struct CbAcc {
+  static constexpr int span = fmt_group(FMT);                  // columns per accumulator (one scale)
+  static constexpr int blocks = kVStepK / span;                // accumulators per step: 2 or 4
+  static constexpr int acc_cols = kAccSteps * blocks * kVTok;  // tensor memory columns: 128 or 256
+};
 
 template <int FMT>
 struct VFmt {
-  static constexpr int span = fmt_group(FMT);                  // columns per accumulator (one E8M0 group)
-  static constexpr int blocks = kVStepK / span;                // accumulators per step: 2 or 4
-  static constexpr int acc_cols = kAccSteps * blocks * kVTok;  // tensor memory columns: 128 or 256
   static constexpr int spl = lane_scale_bytes(FMT);            // E8M0 bytes per lane block: 1 or 2
-  // Weight loads in flight per thread: about 128 bytes of lane blocks for the
-  // MX formats, so two CTAs keep ~64 KB per SM in flight; fewer blocks for the
-  // codebooks, whose decode needs more registers (80-96 bytes in flight).
+  // Weight loads in flight per thread: 128 bytes of lane blocks for the MX
+  // formats, so two CTAs keep ~64 KB per SM in flight; fewer blocks for the
+  // codebooks, whose decode needs more registers.
   static constexpr int window = fmt_is_mx(FMT) ? 128 / lane_code_bytes(FMT) : (FMT == CB2 ? 8 : 6);
   static constexpr int words = (FMT == CB3) ? 3 : lane_code_bytes(FMT) / 4;
-  // MX formats take the pre-scaled path: code x 2^(e-127) is exact in bf16
-  // for every E8M0 byte in [scale_lo, scale_hi] (MXFP4: 6 x 2^125 is below
-  // bf16's largest value and every product is a multiple of 2^-133, bf16's
-  // smallest subnormal; MXFP8: 448 x 2^119 and m / 8 x 2^-6 x 2^-124), so
-  // one accumulator per row sums bf16 x bf16 products for the whole K range
-  // and no per-group drain is needed; a row holding a scale byte outside the
-  // range is recomputed exactly on the CUDA cores afterwards.
-  static constexpr bool fast = fmt_is_mx(FMT);
-  static constexpr int alloc_cols = fast ? 32 : acc_cols;   // tensor memory allocation (32 at least)
 };
 
 struct VParams {
@@ -145,8 +152,7 @@ __device__ __forceinline__ uint64_t mma_desc(uint32_t addr, uint32_t lbo, uint32
 // kind::f16 instruction descriptor: fp32 accumulator (bits 4-5 = 1), A and B
 // both f16 (bits 7-9 and 10-12 = 0), both K-major, N = 16, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kVTok >> 3) << 17) | ((uint32_t)(kVRows >> 4) << 24);
-// The same with A and B both bf16 (bits 7-9 and 10-12 = 1), for the
-// pre-scaled path.
+// The same with A and B both bf16 (bits 7-9 and 10-12 = 1): MX formats.
 constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
 
 template <bool BF16>
@@ -180,6 +186,9 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// MX: scale of a lane block outside the matrix (its codes are zero).
+constexpr uint32_t kNoScale = 0x100u;
+
 // Lane block of one row and one 32-group: codes and E8M0 byte(s) (two, the
 // half-blocks, for CB2 / CB3).
 template <int FMT>
@@ -194,7 +203,7 @@ __device__ __forceinline__ void load_block(const VParams& p, const uint8_t* w, i
   if (!valid) {
 #pragma unroll
     for (int i = 0; i < VFmt<FMT>::words; ++i) b.c[i] = 0;
-    b.e = (VFmt<FMT>::spl == 2) ? 0x7f7fu : 0x7fu;
+    b.e = (VFmt<FMT>::spl == 2) ? 0x7f7fu : (fmt_is_mx(FMT) ? kNoScale : 0x7fu);
     return;
   }
   const int c = g >> 5, l = g & 31;
@@ -236,42 +245,26 @@ __device__ __forceinline__ void biased_i8x4_to_f16x2(uint32_t v, uint32_t& lo, u
   hi = sub_f16x2(prmt(v, 0x64646464u, 0x4342u), 0x64806480u);
 }
 
-// 32 codes of a lane block -> 32 exact f16 element values (unscaled),
-// written as four 16-byte core-matrix rows (k groups kk0 .. kk0 + 3, kALbo
-// bytes apart).
+
+// Codebooks: 32 codes of a lane block -> 32 exact f16 element values
+// (unscaled integers), written as four 16-byte core-matrix rows (k groups
+// kk0 .. kk0 + 3, kALbo bytes apart).
 template <int FMT>
 __device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t (&lut)[4], uint8_t* a_row,
                                              int kk0) {
-  uint32_t out[16];
-  if constexpr (FMT == MXFP4) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t h[4];
-      e2m1x8_to_f16x2(b.c[q], h);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) out[4 * q + i] = h[i];
-    }
-  } else if constexpr (FMT == MXFP8) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      uint32_t h[2];
-      e4m3x4_to_f16x2(b.c[q], h);
-      out[2 * q] = h[0];
-      out[2 * q + 1] = h[1];
-    }
+  static_assert(!fmt_is_mx(FMT), "codebook decode");
+  uint32_t v[8];
+  if constexpr (FMT == CB2) {
+    decode_cb2(b.c[0], b.c[1], lut[0], v);
+  } else if constexpr (FMT == CB3) {
+    decode_cb3(b.c[0], b.c[1], b.c[2], lut[0], lut[1], v);
   } else {
-    uint32_t v[8];
-    if constexpr (FMT == CB2) {
-      decode_cb2(b.c[0], b.c[1], lut[0], v);
-    } else if constexpr (FMT == CB3) {
-      decode_cb3(b.c[0], b.c[1], b.c[2], lut[0], lut[1], v);
-    } else {
-      const uint32_t w4[4] = {b.c[0], b.c[1], b.c[2], b.c[3]};
-      decode_cb4(w4, lut, v);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) biased_i8x4_to_f16x2(v[i], out[2 * i], out[2 * i + 1]);
+    const uint32_t w4[4] = {b.c[0], b.c[1], b.c[2], b.c[3]};
+    decode_cb4(w4, lut, v);
   }
+  uint32_t out[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) biased_i8x4_to_f16x2(v[i], out[2 * i], out[2 * i + 1]);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
@@ -279,25 +272,38 @@ __device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t
   }
 }
 
-__device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t h2, float s) {
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
-  return *reinterpret_cast<const uint32_t*>(&b);
+// f16 bits of 2^d for -24 <= d <= 0 (normal down to 2^-14, subnormal below;
+// the fp32 power of two converts exactly).
+__device__ __forceinline__ uint16_t pow2_f16(int d) {
+  return __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)(d + 127) << 23)));
 }
 
-// Whether code x 2^(e-127) is exact in bf16 for every code of the format:
-// E8M0 bytes 0..252 (MXFP4), 3..246 (MXFP8).
-template <int FMT>
-__device__ __forceinline__ bool scale_in_bf16_range(uint32_t e) {
-  return (FMT == MXFP8) ? (e - 3u <= 243u) : (e <= 252u);
+// Two f16 element values times the f16 power of two m -> bf16x2: each
+// product made exactly in fp32 by the mixed-precision FMA (f16 inputs, fp32
+// sum with +0), then packed (low half = first element). Exact whenever the
+// product is a bf16 value, which holds for every E2M1 / E4M3 code times
+// 2^-24 .. 1.
+__device__ __forceinline__ uint32_t scaled_pair_bf16(uint32_t h2, uint16_t m) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n .reg .f32 a, b;\n mov.b32 {lo, hi}, %1;\n"
+      " fma.rn.f32.f16 a, lo, %2, %3;\n fma.rn.f32.f16 b, hi, %2, %3;\n"
+      " cvt.rn.bf16x2.f32 %0, b, a;\n}"
+      : "=r"(r)
+      : "r"(h2), "h"(m), "f"(0.0f));
+  return r;
 }
 
-// Pre-scaled path (MX formats): 32 codes of a lane block -> 32 bf16 values
-// code x 2^(e-127) (exact for scale bytes in the format's safe range), four
-// 16-byte core-matrix rows. Returns whether the scale byte is outside it.
+// MX: 32 codes of a lane block -> 32 bf16 values code x 2^(e - e_ref), four
+// 16-byte core-matrix rows. e - e_ref is clamped to [-24, 0]; returns whether
+// that changed it (or the byte is 255), in which case the row is recomputed
+// on the CUDA cores and its accumulator is not used. A block outside the
+// matrix (scale kNoScale, zero codes) is never flagged.
 template <int FMT>
-__device__ __forceinline__ bool decode_store_scaled(const Block<FMT>& b, uint8_t* a_row, int kk0) {
-  const float s = e8m0_to_f32(b.e);
+__device__ __forceinline__ bool decode_store_ref(const Block<FMT>& b, int eref, uint8_t* a_row, int kk0) {
+  int d = (int)b.e - eref;
+  const bool bad = (d < -kMaxSpread || d > 0) && b.e != kNoScale;
+  d = d < -kMaxSpread ? -kMaxSpread : (d > 0 ? 0 : d);
+  const uint16_t m = pow2_f16(d);
   uint32_t out[16];
   if constexpr (FMT == MXFP4) {
 #pragma unroll
@@ -305,15 +311,16 @@ __device__ __forceinline__ bool decode_store_scaled(const Block<FMT>& b, uint8_t
       uint32_t h[4];
       e2m1x8_to_f16x2(b.c[q], h);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) out[4 * q + i] = scaled_bf16x2(h[i], s);
+      for (int i = 0; i < 4; ++i) out[4 * q + i] = scaled_pair_bf16(h[i], m);
     }
   } else {
+    static_assert(FMT == MXFP8, "MX decode");
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       uint32_t h[2];
       e4m3x4_to_f16x2(b.c[q], h);
-      out[2 * q] = scaled_bf16x2(h[0], s);
-      out[2 * q + 1] = scaled_bf16x2(h[1], s);
+      out[2 * q] = scaled_pair_bf16(h[0], m);
+      out[2 * q + 1] = scaled_pair_bf16(h[1], m);
     }
   }
 #pragma unroll
@@ -321,32 +328,20 @@ __device__ __forceinline__ bool decode_store_scaled(const Block<FMT>& b, uint8_t
     *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
         make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
   }
-  return !scale_in_bf16_range<FMT>(b.e);
+  return bad;
 }
 
-// Activation operand B: one (token t, local 32-group gl) unit -- 32 f16
-// values into four core-matrix rows -- and its factor for the drain (MX:
-// 2^-s of the group's shift; codebooks: the q8_1 scale d as fp32).
+// Codebooks, activation operand B: one (token t, local 32-group gl) unit --
+// the 32 q8_1 codes as f16 into four core-matrix rows -- and its fp16 scale
+// d (as fp32) for the drain.
 template <int FMT>
-__device__ __forceinline__ void stage_unit(const VParams& p, int vec, int g, bool valid, uint8_t* bbuf, int gl,
-                                           int t, float* aux) {
+__device__ __forceinline__ void stage_unit_q8(const VParams& p, int vec, int g, bool valid, uint8_t* bbuf, int gl,
+                                              int t, float* aux) {
   uint32_t w[16];
   float f = 0.0f;
   if (!valid) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = 0;
-  } else if constexpr (fmt_is_mx(FMT)) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)vec * p.x_vec_bytes + (size_t)g * 64);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = src[q];
-      w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-    }
-    if constexpr (VFmt<FMT>::fast) {
-      f = 1.0f;                          // bf16 as it is
-    } else {
-      f = shift_group_to_f16(w);
-    }
   } else {
     uint32_t qw[8];
     if (p.x_f32) {
@@ -378,17 +373,218 @@ __device__ __forceinline__ void stage_unit(const VParams& p, int vec, int g, boo
   aux[gl * kVTok + t] = f;
 }
 
+// MX, activation operand B: the bf16 columns [32 g0, 32 g0 + 64 steps) of
+// tokens t < T, zero beyond the CTA's range and for padding tokens. Units of
+// 8 columns (16 bytes); each thread issues four loads before it stores.
+__device__ __forceinline__ void stage_x_bf16(const VParams& p, int T, int g0, int g1, int steps, int tid,
+                                             const int* slot, uint8_t* bbuf) {
+  constexpr int kU = 4;
+  const int n_units = steps * (kVStepK / 8) * kVTok;
+  const int k_end = g1 * 32;
+  for (int u0 = tid; u0 < n_units; u0 += kU * kDecoders) {
+    uint4 v[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int u = u0 + j * kDecoders;
+      const int t = u % kVTok, kk = u / kVTok;
+      const int k = g0 * 32 + kk * 8;
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (u < n_units && t < T && k < k_end) {
+        const int vec = (p.ids == nullptr) ? t : (p.per_slot ? slot[t] : slot[t] / p.top_k);
+        v[j] = *reinterpret_cast<const uint4*>(p.x + (size_t)vec * p.x_vec_bytes + (size_t)k * 2);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int u = u0 + j * kDecoders;
+      const int t = u % kVTok, kk = u / kVTok;
+      if (u < n_units) *reinterpret_cast<uint4*>(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16) = v[j];
+    }
+  }
+}
+
+// Shared-memory state of a sorted gather's work item.
+struct GatherSmem {
+  int ids[kVMaxSlots];
+  int cnt[kVMaxSlots];
+  int slot[kVTok];   // slot of each of the item's tokens
+  int item[3];       // expert, first rank, tokens
+};
+
+// Sorted gather: work item blockIdx.y is the (expert, group of <= 16 of its
+// slots) pair of that index, experts in order of their first slot and slots
+// in slot order. Each CTA derives it from the ids in shared memory: thread s
+// finds its expert's slot count and its rank among them; the first slot of
+// each expert counts the work items of the experts before it. Slots with an
+// invalid id get zero rows (written by the CTAs of work item 0). Returns the
+// item's token count, or -1 for an index past the last item (every CTA of a
+// cluster shares blockIdx.y, so a cluster exits as a whole, before it
+// allocates tensor memory). Called by every thread of the CTA.
 template <int FMT>
-__global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_constant__ VParams p) {
+__device__ int gather_work_item(const VParams& p, int tid, int rank, int rb, GatherSmem& gs) {
+  if (!p.prefetch) pdl_wait();
+  if (tid == 0) gs.item[0] = -1;
+  int e = -1;
+  if (tid < p.nslots) {
+    e = p.ids[tid];
+    if (e < 0 || e >= p.n_experts) e = -1;
+    gs.ids[tid] = e;
+  }
+  __syncthreads();
+  int cnt = 0, rk = 0;
+  bool first = false;
+  if (tid < p.nslots && e >= 0) {
+    for (int q = 0; q < p.nslots; ++q) {
+      const int eq = gs.ids[q];
+      cnt += (eq == e);
+      rk += (eq == e && q < tid);
+    }
+    first = (rk == 0);
+  }
+  if (tid < p.nslots) gs.cnt[tid] = first ? cnt : 0;
+  __syncthreads();
+  if (first) {
+    int before = 0;
+    for (int q = 0; q < tid; ++q) before += (gs.cnt[q] + kVTok - 1) / kVTok;
+    const int mine = (cnt + kVTok - 1) / kVTok;
+    const int y = (int)blockIdx.y;
+    if (y >= before && y < before + mine) {
+      gs.item[0] = e;
+      gs.item[1] = (y - before) * kVTok;
+      gs.item[2] = min(kVTok, cnt - (y - before) * kVTok);
+    }
+  }
+  __syncthreads();
+  if (gs.item[0] >= 0 && e == gs.item[0] && rk >= gs.item[1] && rk < gs.item[1] + gs.item[2]) {
+    gs.slot[rk - gs.item[1]] = tid;
+  }
+  if (blockIdx.y == 0) {
+    if (p.prefetch) pdl_wait();   // outputs are written only after the preceding kernel completed
+    for (int i = rank * kVThreads + tid; i < p.nslots * kVRows; i += p.split * kVThreads) {
+      const int sl = i / kVRows, orow = rb * kVRows + i % kVRows;
+      if (gs.ids[sl] < 0 && orow < p.N) {
+        if constexpr (fmt_is_mx(FMT)) {
+          static_cast<__nv_bfloat16*>(p.y)[(size_t)sl * p.N + orow] = __float2bfloat16_rn(0.f);
+        } else {
+          static_cast<float*>(p.y)[(size_t)sl * p.N + orow] = 0.f;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  return gs.item[0] < 0 ? -1 : gs.item[2];
+}
+
+// The partial sums part[t][row] of the `split` CTAs of a row block meet in
+// rank order through distributed shared memory; rank q stores outputs q,
+// q + split, ... (bf16 for MX, fp32 for the codebooks). Called by every
+// thread of every CTA of the cluster.
+template <int FMT>
+__device__ void cluster_store(const VParams& p, const float* part, int rank, int rb, int T, const int* slot,
+                              int tid) {
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  for (int i = rank * kVThreads + tid; i < kVRows * T; i += p.split * kVThreads) {  // all 9 warps
+    const int t = i / kVRows, rw = i % kVRows;
+    const int orow = rb * kVRows + rw;
+    if (orow >= p.N) continue;
+    float v[kVMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kVMaxSplit; ++q) {
+      v[q] = (q < p.split) ? cluster.map_shared_rank(const_cast<float*>(part), q)[t * kVRows + rw] : 0.f;
+    }
+    float a = 0.f;
+#pragma unroll
+    for (int q = 0; q < kVMaxSplit; ++q) a += v[q];   // rank order; absent ranks add +0
+    const int oslot = (p.ids == nullptr) ? t : slot[t];
+    if constexpr (fmt_is_mx(FMT)) {
+      static_cast<__nv_bfloat16*>(p.y)[(size_t)oslot * p.N + orow] = __float2bfloat16_rn(a);
+    } else {
+      static_cast<float*>(p.y)[(size_t)oslot * p.N + orow] = a;
+    }
+  }
+  cluster.sync();
+}
+
+// MX: the rows whose reference byte is -1 (scale bytes spanning more than
+// kMaxSpread octaves, or the NaN byte 255), recomputed on the CUDA cores: sum
+// over groups of 2^(e-127) * (sum of code x x) in fp32 (the CUDA-core path's
+// formula), one warp per row, the lanes taking groups and adding their sums
+// in a fixed shuffle order; the result replaces part[.][row]. The activations
+// are read from the staged operand B.
+template <int FMT>
+__device__ void recompute_rows(const VParams& p, const uint8_t* w, int rb, int g0, int g1, int T,
+                               const uint8_t* bbuf, const int* s_eref, float* part, int warp, int lane) {
+  for (int rr = warp; rr < kVRows; rr += kVThreads / 32) {
+    if (s_eref[rr] >= 0) continue;
+    const int orow = rb * kVRows + rr;
+    if (orow >= p.N) continue;
+    float sum[kVTok];
+#pragma unroll
+    for (int t = 0; t < kVTok; ++t) sum[t] = 0.f;
+    for (int g = g0 + lane; g < g1; g += 32) {
+      Block<FMT> bk;
+      load_block<FMT>(p, w, orow >> 3, orow & 7, g, true, bk);
+      const float sc = e8m0_to_f32(bk.e);
+      uint32_t hw[16];
+      if constexpr (FMT == MXFP4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hq[4];
+          e2m1x8_to_f16x2(bk.c[q], hq);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) hw[4 * q + i] = hq[i];
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t hq[2];
+          e4m3x4_to_f16x2(bk.c[q], hq);
+          hw[2 * q] = hq[0];
+          hw[2 * q + 1] = hq[1];
+        }
+      }
+      const int kl0 = (g - g0) * 32;
+#pragma unroll 1
+      for (int t = 0; t < kVTok; ++t) {
+        if (t < T) {
+          const uint8_t* xt = bbuf + (t >> 3) * 128 + (t & 7) * 16;
+          float d = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&hw[i]));
+            const int k = kl0 + 2 * i;
+            const uint32_t xb = *reinterpret_cast<const uint32_t*>(xt + (size_t)(k >> 3) * 256 + (k & 7) * 2);
+            d = fmaf(wf.x, __uint_as_float(xb << 16), d);
+            d = fmaf(wf.y, __uint_as_float(xb & 0xffff0000u), d);
+          }
+          sum[t] = fmaf(sc, d, sum[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kVTok; ++t) {
+      float v = sum[t];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) part[t * kVRows + rr] = v;
+    }
+  }
+}
+
+// MX formats: bf16 operands code x 2^(e - e_ref), one accumulator per row
+// for the CTA's whole K range, 2^(e_ref - 127) applied in the epilogue.
+template <int FMT>
+__global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_constant__ VParams p) {
   using F = VFmt<FMT>;
+  static_assert(fmt_is_mx(FMT), "MX formats");
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t empty[kVBufs];      // A buffer read by the MMAs (tcgen05.commit)
-  __shared__ __align__(8) uint64_t full[kVBufs];       // A buffer written by all decoding warps
-  __shared__ __align__(8) uint64_t accd[kAccSteps];    // a step's accumulators complete (tcgen05.commit)
-  __shared__ __align__(8) uint64_t accf[kAccSteps];    // a step's accumulators drained (one arrival per decoding warp)
-  __shared__ __align__(8) uint64_t done;               // every MMA complete (tcgen05.commit)
+  __shared__ __align__(8) uint64_t empty[kVBufs];   // A buffer read by the MMAs (tcgen05.commit)
+  __shared__ __align__(8) uint64_t full[kVBufs];    // A buffer written by all decoding warps
+  __shared__ __align__(8) uint64_t done;            // every MMA complete (tcgen05.commit)
   __shared__ uint32_t tmem_slot;
-  __shared__ uint8_t s_unsafe[kVRows];                 // pre-scaled path: row has a scale byte outside the range
+  __shared__ int s_eref[kVRows];                    // row reference byte e_ref; -1: recomputed
+  __shared__ GatherSmem gs;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)(blockIdx.x % (unsigned)p.split);
   const int rb = (int)(blockIdx.x / (unsigned)p.split);
@@ -396,72 +592,170 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   const int g1 = (int)((long)(rank + 1) * p.groups / p.split);
   const int steps = (g1 - g0 + 1) / 2;
 
-  // Sorted gather: work item blockIdx.y is the (expert, group of <= 16 of
-  // its slots) pair of that index, experts in order of their first slot and
-  // slots in slot order. Each CTA derives it from the ids in shared memory:
-  // thread s finds its expert's slot count and its rank among them; the
-  // first slot of each expert counts the work items of the experts before
-  // it. An index past the last item leaves the CTA idle (every CTA of a
-  // cluster shares blockIdx.y, so a cluster exits as a whole, before it
-  // allocates tensor memory). Slots with an invalid id get zero rows.
-  __shared__ int s_ids[kVMaxSlots];
-  __shared__ int s_cnt[kVMaxSlots];
-  __shared__ int s_slot[kVTok];
-  __shared__ int s_item[3];   // expert, first rank, tokens
   int T = p.T;
   const uint8_t* w = p.w;
   if (p.ids != nullptr) {
-    if (!p.prefetch) pdl_wait();
-    if (tid == 0) s_item[0] = -1;
-    int e = -1;
-    if (tid < p.nslots) {
-      e = p.ids[tid];
-      if (e < 0 || e >= p.n_experts) e = -1;
-      s_ids[tid] = e;
+    T = gather_work_item<FMT>(p, tid, rank, rb, gs);
+    if (T < 0) return;
+    w = p.w + (uint64_t)gs.item[0] * p.expert_stride;
+  }
+  uint8_t* abuf = smem;                                 // kVBufs x 16 KB
+  uint8_t* bbuf = smem + kVBufs * kABytes;              // steps x 64 columns x 16 tokens
+  float* part = reinterpret_cast<float*>(smem);         // 16 x 128 fp32, after the MMAs
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" :: "r"(smem_addr(&tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kVBufs; ++i) {
+      mbar_init(smem_addr(&empty[i]), 1);
+      mbar_init(smem_addr(&full[i]), kDecoders / 32);
     }
-    __syncthreads();
-    int cnt = 0, rk = 0;
-    bool first = false;
-    if (tid < p.nslots && e >= 0) {
-      for (int q = 0; q < p.nslots; ++q) {
-        const int eq = s_ids[q];
-        cnt += (eq == e);
-        rk += (eq == e && q < tid);
-      }
-      first = (rk == 0);
-    }
-    if (tid < p.nslots) s_cnt[tid] = first ? cnt : 0;
-    __syncthreads();
-    if (first) {
-      int before = 0;
-      for (int q = 0; q < tid; ++q) before += (s_cnt[q] + kVTok - 1) / kVTok;
-      const int mine = (cnt + kVTok - 1) / kVTok;
-      const int y = (int)blockIdx.y;
-      if (y >= before && y < before + mine) {
-        s_item[0] = e;
-        s_item[1] = (y - before) * kVTok;
-        s_item[2] = min(kVTok, cnt - (y - before) * kVTok);
-      }
-    }
-    __syncthreads();
-    if (s_item[0] >= 0 && e == s_item[0] && rk >= s_item[1] && rk < s_item[1] + s_item[2]) s_slot[rk - s_item[1]] = tid;
-    if (blockIdx.y == 0) {
-      if (p.prefetch) pdl_wait();   // outputs are written only after the preceding kernel completed
-      for (int i = rank * kVThreads + tid; i < p.nslots * kVRows; i += p.split * kVThreads) {
-        const int sl = i / kVRows, orow = rb * kVRows + i % kVRows;
-        if (s_ids[sl] < 0 && orow < p.N) {
-          if constexpr (fmt_is_mx(FMT)) {
-            static_cast<__nv_bfloat16*>(p.y)[(size_t)sl * p.N + orow] = __float2bfloat16_rn(0.f);
-          } else {
-            static_cast<float*>(p.y)[(size_t)sl * p.N + orow] = 0.f;
+    mbar_init(smem_addr(&done), 1);
+    fence_mbar_init();
+  }
+  // Lane pairs take the two groups of one row: warp w rows 16 w .. + 15,
+  // lane l row 16 w + l / 2 and group 2 step + l % 2, so one warp load
+  // covers 16 rows x 32 contiguous bytes. The first window of loads goes out
+  // first (before griddepcontrol.wait when the caller guarantees the weights
+  // are not the preceding kernel's output), then the activations.
+  const bool decoder = tid < kDecoders;
+  const int h = lane & 1;
+  const int r = (warp & 7) * 16 + (lane >> 1);
+  const int row = rb * kVRows + r;
+  const int rt = row >> 3, r8 = row & 7;
+  const bool row_ok = decoder && rt < p.row_tiles;
+  uint8_t* a_row = abuf + (r >> 3) * 128 + (r & 7) * 16;
+  Block<FMT> win[F::window];
+  if (!p.prefetch) pdl_wait();
+#pragma unroll
+  for (int u = 0; u < F::window; ++u) {
+    const int g = g0 + 2 * u + h;
+    load_block<FMT>(p, w, rt, r8, g, row_ok && u < steps && g < g1, win[u]);
+  }
+  if (p.prefetch) pdl_wait();
+  pdl_launch_dependents();
+  if (decoder) stage_x_bf16(p, T, g0, g1, steps, tid, gs.slot, bbuf);
+
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool ok = true;
+  bool any_bad = false;
+
+  if (decoder) {
+    // the row's reference byte: its first block's (the pair's even lane) + kRefMargin
+    const int e_first = __shfl_sync(0xffffffffu, (int)win[0].e, lane & ~1);
+    const int eref = min((e_first == (int)kNoScale ? 127 : e_first) + kRefMargin, 254);
+    bool bad = false;
+    for (int s0 = 0; s0 < steps; s0 += F::window) {
+#pragma unroll
+      for (int u = 0; u < F::window; ++u) {
+        const int st = s0 + u;
+        if (st < steps) {
+          const int b = st % kVBufs;
+          if (st >= kVBufs) {
+            // the MMAs that read this buffer kVBufs steps ago are done
+            ok &= mbar_wait_bounded(smem_addr(&empty[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
           }
+          bad |= decode_store_ref<FMT>(win[u], eref, a_row + (size_t)b * kABytes, 4 * h);
+          const int gn = g0 + 2 * (st + F::window) + h;
+          load_block<FMT>(p, w, rt, r8, gn, row_ok && st + F::window < steps && gn < g1, win[u]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&full[b]));
         }
       }
     }
+    bad |= __shfl_xor_sync(0xffffffffu, (int)bad, 1) != 0;
+    if (h == 0) s_eref[r] = bad ? -1 : eref;
+    any_bad = bad;
+  } else if (lane == 0) {
+    // MMA issue: step st once every decoding warp has written its A buffer;
+    // one accumulator for the whole K range.
+    for (int st = 0; st < steps; ++st) {
+      const int b = st % kVBufs;
+      ok &= mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
+      tc_fence_after();
+      const uint32_t a0 = smem_addr(abuf + (size_t)b * kABytes);
+      const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
+#pragma unroll
+      for (int j = 0; j < kVStepK / 16; ++j) {
+        mma_f16<true>(tmem, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
+                      (st > 0 || j > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_addr(&empty[b]));
+    }
+    mma_commit(smem_addr(&done));
+  }
+  __syncwarp();
+  ok &= mbar_wait_bounded(smem_addr(&done), 0u, kWaitLimitNs);
+  if (!__all_sync(0xffffffffu, ok) && lane == 0) set_status(kStatusWaitTile);
+  tc_fence_before();
+  any_bad = __syncthreads_or(any_bad) != 0;   // every row's e_ref is in s_eref
+  tc_fence_after();
+
+  // Accumulator rows 32 w .. 32 w + 31 (tensor-memory lanes of warp w) ->
+  // partial sums part[t][row] = D x 2^(e_ref - 127). The A buffers are free:
+  // every MMA that read them has completed.
+  if (warp < 4) {
+    float v0[8], v1[8];
+    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+    tmem_ld8(ta, v0);
+    tmem_ld8(ta + 8u, v1);
+    tmem_wait_ld();
+    const int rr = warp * 32 + lane;
+    const int er = s_eref[rr];
+    const float f = e8m0_to_f32(er < 0 ? 127u : (uint32_t)er);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      part[t * kVRows + rr] = v0[t] * f;
+      part[(t + 8) * kVRows + rr] = v1[t] * f;
+    }
+  }
+  tc_fence_before();
+  if (any_bad) {
     __syncthreads();
-    if (s_item[0] < 0) return;
-    T = s_item[2];
-    w = p.w + (uint64_t)s_item[0] * p.expert_stride;
+    recompute_rows<FMT>(p, w, rb, g0, g1, T, bbuf, s_eref, part, warp, lane);
+  }
+  cluster_store<FMT>(p, part, rank, rb, T, gs.slot, tid);
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" :: "r"(tmem));
+  }
+}
+
+// Codebook formats: f16 integer operands, one tensor-memory accumulator per
+// (half-)block scale, drained by the decoding warps into fp32 row sums.
+template <int FMT>
+__global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_constant__ VParams p) {
+  using F = VFmt<FMT>;
+  using C = CbAcc<FMT>;
+  static_assert(!fmt_is_mx(FMT), "codebook formats");
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t empty[kVBufs];      // A buffer read by the MMAs (tcgen05.commit)
+  __shared__ __align__(8) uint64_t full[kVBufs];       // A buffer written by all decoding warps
+  __shared__ __align__(8) uint64_t accd[kAccSteps];    // a step's accumulators complete (tcgen05.commit)
+  __shared__ __align__(8) uint64_t accf[kAccSteps];    // a step's accumulators drained (one arrival per decoding warp)
+  __shared__ __align__(8) uint64_t done;               // every MMA complete (tcgen05.commit)
+  __shared__ uint32_t tmem_slot;
+  __shared__ GatherSmem gs;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)(blockIdx.x % (unsigned)p.split);
+  const int rb = (int)(blockIdx.x / (unsigned)p.split);
+  const int g0 = (int)((long)rank * p.groups / p.split);
+  const int g1 = (int)((long)(rank + 1) * p.groups / p.split);
+  const int steps = (g1 - g0 + 1) / 2;
+
+  int T = p.T;
+  const uint8_t* w = p.w;
+  if (p.ids != nullptr) {
+    T = gather_work_item<FMT>(p, tid, rank, rb, gs);
+    if (T < 0) return;
+    w = p.w + (uint64_t)gs.item[0] * p.expert_stride;
   }
   uint8_t* abuf = smem;                                               // kVBufs x 16 KB
   uint8_t* bbuf = smem + kVBufs * kABytes;                            // steps x 64 columns x 16 tokens
@@ -471,7 +765,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_addr(&tmem_slot)), "r"(F::alloc_cols));
+                 :: "r"(smem_addr(&tmem_slot)), "r"(C::acc_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
@@ -486,7 +780,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     mbar_init(smem_addr(&done), 1);
     fence_mbar_init();
   }
-  // Drained path: decoding warp w takes rows 32 (w % 4) .. + 31 of the block
+  // Decoding warp w takes rows 32 (w % 4) .. + 31 of the block
   // -- the tensor-memory lanes its drains may read -- and group 2 * step +
   // w / 4 of every step: lane l decodes row 32 (w % 4) + l, and later drains
   // that row's accumulator of the same group for all 16 tokens, with the
@@ -494,12 +788,8 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   // (before griddepcontrol.wait when the caller guarantees the weights are
   // not the preceding kernel's output), then the activations.
   const bool decoder = tid < kDecoders;
-  // Pre-scaled path: lane pairs take the two groups of one row (warp w: rows
-  // 16 w .. 16 w + 15), so a warp load covers 16 rows x 32 contiguous bytes;
-  // drained path: warp w takes rows 32 (w % 4) .. + 31 (its tensor-memory
-  // lanes) and group w / 4.
-  const int h = F::fast ? (lane & 1) : ((warp >> 2) & 1);                              // group of the step
-  const int r = F::fast ? ((warp & 7) * 16 + (lane >> 1)) : ((warp & 3) * 32 + lane);  // row of the block
+  const int h = (warp >> 2) & 1;                 // group of the step
+  const int r = (warp & 3) * 32 + lane;          // row of the block
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
@@ -524,12 +814,11 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       const int t = u % kVTok, gl = u / kVTok;
       const int g = g0 + gl;
       const bool valid = t < T && g < g1;
-      const int vec = (p.ids == nullptr) ? t : (p.per_slot ? s_slot[t < T ? t : 0] : s_slot[t < T ? t : 0] / p.top_k);
-      stage_unit<FMT>(p, vec, g, valid, bbuf, gl, t, aux);
+      const int vec = (p.ids == nullptr) ? t : (p.per_slot ? gs.slot[t < T ? t : 0] : gs.slot[t < T ? t : 0] / p.top_k);
+      stage_unit_q8<FMT>(p, vec, g, valid, bbuf, gl, t, aux);
     }
   }
 
-  if (tid < kVRows) s_unsafe[tid] = 0;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -550,8 +839,8 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
     tc_fence_after();
-    constexpr int per = F::blocks / 2;   // accumulators per 32-group: 1, or 2 half-blocks
-    const uint32_t col0 = (uint32_t)(((sd % kAccSteps) * F::blocks + h * per) * kVTok);
+    constexpr int per = C::blocks / 2;   // accumulators per 32-group: 1, or 2 half-blocks
+    const uint32_t col0 = (uint32_t)(((sd % kAccSteps) * C::blocks + h * per) * kVTok);
     const int gl = 2 * sd + h;
     const float* f = aux + gl * kVTok;
     const uint32_t eb = my_sc[(sd % kScaleRing) * kDecoders];
@@ -565,27 +854,23 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int tt = th * 8 + t;
-        if constexpr (fmt_is_mx(FMT)) {
-          acc[tt] = fmaf(s0, v[0][t] * f[tt], acc[tt]);
-        } else if constexpr (per == 2) {
+        if constexpr (per == 2) {
           acc[tt] = fmaf(f[tt], fmaf(s0, v[0][t], s1 * v[1][t]), acc[tt]);
         } else {
           acc[tt] = fmaf(f[tt], s0 * v[0][t], acc[tt]);
         }
       }
-      if constexpr (!fmt_is_mx(FMT)) {
-        const int g = g0 + gl;
-        if (p.dbg != nullptr && row < p.N && g < g1) {
-          const int nb = p.K / F::span;
+      const int g = g0 + gl;
+      if (p.dbg != nullptr && row < p.N && g < g1) {
+        const int nb = p.K / C::span;
 #pragma unroll
-          for (int j = 0; j < per; ++j) {
+        for (int j = 0; j < per; ++j) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int tt = th * 8 + t;
-              if (tt < T) {
-                const int slot = (p.ids == nullptr) ? tt : s_slot[tt];
-                p.dbg[((size_t)slot * p.N + row) * nb + g * per + j] = (int32_t)v[j][t];
-              }
+          for (int t = 0; t < 8; ++t) {
+            const int tt = th * 8 + t;
+            if (tt < T) {
+              const int slot = (p.ids == nullptr) ? tt : gs.slot[tt];
+              p.dbg[((size_t)slot * p.N + row) * nb + g * per + j] = (int32_t)v[j][t];
             }
           }
         }
@@ -609,33 +894,25 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
-          if constexpr (F::fast) {
-            if (decode_store_scaled<FMT>(win[u], a_row + (size_t)b * kABytes, 4 * h)) s_unsafe[r] = 1;
-          } else {
-            decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
-            my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
-          }
+          decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
+          my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
           const int gn = g0 + 2 * (st + kWindow) + h;
           load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&full[b]));
-          if constexpr (!F::fast) {
-            if (st >= kLag) drain(st - kLag);
-          }
+          if (st >= kLag) drain(st - kLag);
         }
       }
     }
-    if constexpr (!F::fast) {
-      for (int sd = steps - kLag > 0 ? steps - kLag : 0; sd < steps && ok; ++sd) drain(sd);
-    }
+    for (int sd = steps - kLag > 0 ? steps - kLag : 0; sd < steps && ok; ++sd) drain(sd);
   } else if (lane == 0) {
     // MMA issue: step st once every decoding warp has written its A buffer
     // and the accumulators it reuses have been drained.
     for (int st = 0; st < steps && ok; ++st) {
       const int b = st % kVBufs;
       ok = mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
-      if (!F::fast && ok && st >= kAccSteps) {
+      if (ok && st >= kAccSteps) {
         ok = mbar_wait_bounded(smem_addr(&accf[st % kAccSteps]), (uint32_t)((st / kAccSteps) - 1) & 1u, kWaitLimitNs);
       }
       if (!ok) break;
@@ -644,19 +921,13 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
 #pragma unroll
       for (int j = 0; j < kVStepK / 16; ++j) {
-        if constexpr (F::fast) {
-          // one accumulator for the whole K range
-          mma_f16<true>(tmem, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                        (st > 0 || j > 0) ? 1u : 0u);
-        } else {
-          const int blk = j * 16 / F::span;
-          const uint32_t col = (uint32_t)(((st % kAccSteps) * F::blocks + blk) * kVTok);
-          mma_f16<false>(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128),
-                         mma_desc(b0 + j * 2 * 256, 256, 128), (j * 16 % F::span) != 0 ? 1u : 0u);
-        }
+        const int blk = j * 16 / C::span;
+        const uint32_t col = (uint32_t)(((st % kAccSteps) * C::blocks + blk) * kVTok);
+        mma_f16<false>(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
+                       (j * 16 % C::span) != 0 ? 1u : 0u);
       }
       mma_commit(smem_addr(&empty[b]));
-      if constexpr (!F::fast) mma_commit(smem_addr(&accd[st % kAccSteps]));
+      mma_commit(smem_addr(&accd[st % kAccSteps]));
     }
     mma_commit(smem_addr(&done));
     if (!mbar_wait_bounded(smem_addr(&done), 0u, kWaitLimitNs)) ok = false;
@@ -667,111 +938,21 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   // them completed before the MMA warp passed `done`, or before the last
   // drain).
   __syncthreads();
-  if constexpr (F::fast) {
-    // the accumulator: warps w and w + 4 read lanes 32 (w % 4) .., tokens 8 (w / 4) ..
-    tc_fence_after();
-    if (decoder && ok) {
-      const int th = (warp >> 2) & 1, tr = (warp & 3) * 32 + lane;
-      float v[8];
-      tmem_ld8(tlane + (uint32_t)(th * 8), v);
-      tmem_wait_ld();
+  if (decoder && h == 0) {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) part[(th * 8 + t) * kVRows + tr] = v[t];
-    }
-    __syncthreads();
-    // rows holding a scale byte outside the pre-scaled range: recomputed on
-    // the CUDA cores, sum over groups of 2^(e-127) * (sum of code x x) in
-    // fp32 (the CUDA-core path's formula), one warp per row, the lanes
-    // taking groups and adding their sums in a fixed shuffle order
-    for (int rr = warp; rr < kVRows; rr += kVThreads / 32) {
-      if (!s_unsafe[rr]) continue;
-      const int orow = rb * kVRows + rr;
-      if (orow >= p.N) continue;
-      float sum[kVTok];
+    for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] = acc[t];
+  }
+  __syncthreads();
+  if (decoder && h == 1) {
 #pragma unroll
-      for (int t = 0; t < kVTok; ++t) sum[t] = 0.f;
-      for (int g = g0 + lane; g < g1; g += 32) {
-        Block<FMT> bk;
-        load_block<FMT>(p, w, orow >> 3, orow & 7, g, true, bk);
-        const float sc = e8m0_to_f32(bk.e);
-        uint32_t hw[16];
-        if constexpr (FMT == MXFP4) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t hq[4];
-            e2m1x8_to_f16x2(bk.c[q], hq);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) hw[4 * q + i] = hq[i];
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint32_t hq[2];
-            e4m3x4_to_f16x2(bk.c[q], hq);
-            hw[2 * q] = hq[0];
-            hw[2 * q + 1] = hq[1];
-          }
-        }
-        const int kl0 = (g - g0) * 32;
-        for (int t = 0; t < T; ++t) {
-          const uint8_t* xt = bbuf + (t >> 3) * 128 + (t & 7) * 16;
-          float d = 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&hw[i]));
-            const int k = kl0 + 2 * i;
-            const uint32_t xb = *reinterpret_cast<const uint32_t*>(xt + (size_t)(k >> 3) * 256 + (k & 7) * 2);
-            d = fmaf(wf.x, __uint_as_float(xb << 16), d);
-            d = fmaf(wf.y, __uint_as_float(xb & 0xffff0000u), d);
-          }
-          sum[t] = fmaf(sc, d, sum[t]);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kVTok; ++t) {
-        float v = sum[t];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) part[t * kVRows + rr] = v;
-      }
-    }
-  } else {
-    if (decoder && h == 0) {
-#pragma unroll
-      for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] = acc[t];
-    }
-    __syncthreads();
-    if (decoder && h == 1) {
-#pragma unroll
-      for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] += acc[t];
-    }
+    for (int t = 0; t < kVTok; ++t) part[t * kVRows + r] += acc[t];
   }
   tc_fence_before();
 
-  // K ranges meet in rank order; rank q stores outputs q, q + split, ...
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
-  for (int i = rank * kVThreads + tid; i < kVRows * T; i += p.split * kVThreads) {  // all 9 warps
-    const int t = i / kVRows, rw = i % kVRows;
-    const int orow = rb * kVRows + rw;
-    if (orow >= p.N) continue;
-    float v[kVMaxSplit];
-#pragma unroll
-    for (int q = 0; q < kVMaxSplit; ++q) v[q] = (q < p.split) ? cluster.map_shared_rank(part, q)[t * kVRows + rw] : 0.f;
-    float a = 0.f;
-#pragma unroll
-    for (int q = 0; q < kVMaxSplit; ++q) a += v[q];   // rank order; absent ranks add +0
-    const int oslot = (p.ids == nullptr) ? t : s_slot[t];
-    if constexpr (fmt_is_mx(FMT)) {
-      static_cast<__nv_bfloat16*>(p.y)[(size_t)oslot * p.N + orow] = __float2bfloat16_rn(a);
-    } else {
-      static_cast<float*>(p.y)[(size_t)oslot * p.N + orow] = a;
-    }
-  }
-  cluster.sync();
+  cluster_store<FMT>(p, part, rank, rb, T, gs.slot, tid);
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(F::alloc_cols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::acc_cols));
   }
 }
 
@@ -795,9 +976,11 @@ bool verify_supported(const MatvecArgs& a) {
   return (groups + kVMaxSplit - 1) / kVMaxSplit <= 2 * kVMaxSteps;
 }
 
-size_t verify_smem_bytes(int steps) {
-  return (size_t)kVBufs * kABytes + (size_t)steps * (kVStepK / 8) * 256 + (size_t)kScaleRing * 2 * kVRows * 2 +
-         (size_t)steps * 2 * kVTok * 4;
+// Dynamic shared memory: the A buffers and the activation operand, plus for
+// the codebooks the ring of scale bytes and the per-group activation scales.
+size_t verify_smem_bytes(bool mx, int steps) {
+  const size_t base = (size_t)kVBufs * kABytes + (size_t)steps * (kVStepK / 8) * 256;
+  return mx ? base : base + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4;
 }
 
 template <int FMT>
@@ -821,11 +1004,13 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   for (int i = 0; i < 4; ++i) p.lut[i] = a.lut[i] ^ 0x80808080u;
   p.groups = a.K / 32;
   const int row_blocks = (a.N + kVRows - 1) / kVRows;
-  // One wave of at most two CTAs per SM; a sorted gather has many work items
-  // (grid.y), so it splits K only as far as the activation operand needs.
+  // About one wave of two CTAs per SM: a sorted gather's grid.y is an upper
+  // bound of its work items (ceil(slots / 16) + distinct experts, known only
+  // on the device); K is split for about one item per expert that can occur.
   const int nslots = a.ids ? a.ntok * a.top_k : 0;
-  const int items = a.ids ? (nslots + kVTok - 1) / kVTok + (a.n_experts < nslots ? a.n_experts : nslots) : 1;
-  int split = a.ids ? 1 : (2 * device_sm_count()) / row_blocks;
+  const int experts = a.ids ? (a.n_experts < nslots ? a.n_experts : nslots) : 1;
+  const int items = a.ids ? (nslots + kVTok - 1) / kVTok + experts : 1;
+  int split = (2 * device_sm_count()) / (row_blocks * experts);
   if (split > kVMaxSplit) split = kVMaxSplit;
   if (split > p.groups / 2) split = p.groups / 2;
   if (split < 1) split = 1;
@@ -839,7 +1024,15 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.per_slot = a.per_slot;
   p.n_experts = a.n_experts;
   p.expert_stride = a.expert_stride;
-  const size_t smem = verify_smem_bytes(p.steps);
+  constexpr bool kMx = fmt_is_mx(FMT);
+  auto kernel = [] {
+    if constexpr (kMx) {
+      return verify_mx_kernel<FMT>;
+    } else {
+      return verify_kernel<FMT>;
+    }
+  }();
+  const size_t smem = verify_smem_bytes(kMx, p.steps);
   static std::mutex mu;
   static size_t configured[64] = {};
   int dev = 0;
@@ -850,7 +1043,7 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
     std::lock_guard<std::mutex> lock(mu);
     if (configured[dev] < smem) {
       g_launch_stage = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
-      err = cudaFuncSetAttribute(verify_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (err != cudaSuccess) return err;
       configured[dev] = smem;
     }
@@ -875,7 +1068,7 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   cfg.attrs = attr;
   cfg.numAttrs = na;
   g_launch_stage = "cudaLaunchKernelEx(verify)";
-  return cudaLaunchKernelEx(&cfg, verify_kernel<FMT>, p);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 cudaError_t launch_verify(const MatvecArgs& a) {

@@ -97,11 +97,29 @@ typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3, QMV_MXFP8 =
  */
 #define QMV_FLAG_X_F16 4u
 
+/*
+ * QMV_FLAG_PATH_TENSOR / QMV_FLAG_PATH_CUDA_CORES: override the library's
+ * choice between the tcgen05 tensor-core path (dense calls of 5..16 tokens,
+ * gathers of 33..QMV_MAX_SLOTS routed slots) and the CUDA-core matvec (one
+ * launch, or one per token range of at most QMV_MAX_LAYER_SLOTS slots).
+ * Without them the choice follows a cost model measured on GB300: MX dense
+ * verify batches and MX gathers of >= 4 slots per distinct expert take the
+ * tensor cores; codebook dense batches do when their CUDA-core weight
+ * streams (one per 4 tokens) exceed 64 MB, codebook gathers at >= 12 slots
+ * per expert. PATH_TENSOR applies to calls that have a tensor-core form
+ * (5..16 dense tokens or 33..128 slots, not fp16 activations, not the
+ * gate/up fusion) and is ignored by the others. Not both. Results differ
+ * between the two paths only in the order of fp32 additions (integer block
+ * sums are identical). For testing and tuning.
+ */
+#define QMV_FLAG_PATH_TENSOR 8u
+#define QMV_FLAG_PATH_CUDA_CORES 16u
+
 /* Limits checked by every entry point. */
 #define QMV_MAX_NTOK 16     /* decode / verify tokens per call */
 #define QMV_MAX_TOPK 8      /* experts per token */
 #define QMV_MAX_SLOTS 128   /* routed (token, slot) pairs of a gather: ntok * top_k */
-#define QMV_MAX_LAYER_SLOTS 32  /* routed slots of the CUDA-core gather, the fused gate/up and layers */
+#define QMV_MAX_LAYER_SLOTS 32  /* routed slots per launch of the CUDA-core gather and gate/up fusion */
 #define QMV_MAX_N (1 << 20)
 #define QMV_MAX_K (1 << 16)
 
@@ -232,18 +250,22 @@ int qmv_dense(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32
  *   gather above. 33..QMV_MAX_SLOTS (128) slots -- a verify or prefill batch
  *   through a MoE projection -- run as the sorted gather ("perf(ggml/hip):
  *   optimize ROCMFPX fp3/fp2 MMVQ on RDNA ...", "Depends on": the batched MMQ
- *   path), for every format with bf16 (MX) or q8_1 / fp32 (codebook)
- *   activations: the slots are grouped by expert (experts in order of their
+ *   path) when the slots share experts (ntok * top_k >= 3 * min(n_experts,
+ *   ntok * top_k)) and the activations are bf16 (MX) or q8_1 / fp32
+ *   (codebooks): the slots are grouped by expert (experts in order of their
  *   first slot, slots in slot order) and each expert's weights are streamed
  *   once per 16 of its slots through the tensor cores, as for qmv_dense. Same
  *   results up to the order of fp32 additions; identical integer block sums.
+ *   Otherwise (about one or two slots per expert, or fp16 activations) the
+ *   call runs as the decode gather on consecutive token ranges of at most
+ *   QMV_MAX_LAYER_SLOTS slots, one launch each (the same bits as those calls
+ *   made one by one; an expert used in two ranges is streamed by each).
  *   x_dev:   MX formats: bf16 vectors of K (fp16 with QMV_FLAG_X_F16); CB
  *            formats: q8_1 buffer.
  *   y_dev:   MX formats: bf16 [ntok][top_k][N] (fp16 with QMV_FLAG_X_F16); CB
  *            formats: fp32 [ntok][top_k][N].
  * Errors: QMV_EINVAL (ntok not in 1..16, top_k not in 1..8, ntok * top_k >
- * QMV_MAX_SLOTS, or > QMV_MAX_LAYER_SLOTS with fp16 activations), QMV_ESHAPE,
- * QMV_EALIGN, QMV_ECUDA.
+ * QMV_MAX_SLOTS), QMV_ESHAPE, QMV_EALIGN, QMV_ECUDA.
  */
 int qmv_moe_gather(const qmv_wdesc* desc, const void* w_dev, const void* x_dev, int32_t per_slot_x,
                    const int32_t* ids_dev, int32_t ntok, int32_t top_k, void* y_dev, void* stream);
@@ -277,7 +299,9 @@ int qmv_moe_gather_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_de
  * and "Current Behavior"). x and h follow qmv_moe_gather with per_slot_x = 0:
  * MX formats: x bf16 [ntok][K], h bf16 [ntok][top_k][N] (both fp16 with
  * QMV_FLAG_X_F16); CB formats: x q8_1, h fp32.
- * An invalid id gives a zero row of h. flags: QMV_FLAG_* (see below).
+ * An invalid id gives a zero row of h. flags: QMV_FLAG_* (see below). More
+ * than QMV_MAX_LAYER_SLOTS routed slots run as one launch per token range of
+ * at most that many slots.
  * Errors: as qmv_moe_gather.
  */
 size_t qmv_packed_gate_up_expert_bytes(const qmv_wdesc* desc);
@@ -301,9 +325,10 @@ int qmv_moe_gate_up_swiglu(const qmv_wdesc* desc, const void* w_gate_up_dev, con
  * n_experts. x as qmv_moe_gate_up_swiglu.
  * y: MX formats bf16 [ntok][top_k][N_down] (fp16 with QMV_FLAG_X_F16);
  * codebooks fp32.
- * Two launches: the fused gate/up/SwiGLU gather stores h in the workspace
- * (MX formats bf16 or fp16, codebooks fp32), then the down gather reads the
- * per-slot h
+ * Two launches (more for more than QMV_MAX_LAYER_SLOTS routed slots, up to
+ * QMV_MAX_SLOTS, as qmv_moe_gather and qmv_moe_gate_up_swiglu split them):
+ * the fused gate/up/SwiGLU gather stores h in the workspace (MX formats bf16
+ * or fp16, codebooks fp32), then the down gather reads the per-slot h
  * (codebooks: it quantizes h to q8_1 while staging it, as QMV_FLAG_X_F32).
  * workspace: caller-owned device scratch of at least
  * qmv_moe_layer_workspace_bytes(gate_up_desc, ntok, top_k) bytes, 16-byte
@@ -409,6 +434,11 @@ int qmv_swiglu_bf16(const void* g_dev, const void* u_dev, void* h_dev, int64_t n
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w_dev, const void* x_dev,
                          int32_t per_slot_x, const int32_t* ids_dev, int32_t ntok, int32_t top_k,
                          void* y_dev, int32_t* sums_dev, size_t sums_bytes, void* stream);
+/* qmv_debug_block_sums with launch flags (QMV_FLAG_PREFETCH_INPUTS,
+ * QMV_FLAG_PATH_*). */
+int qmv_debug_block_sums_ex(const qmv_wdesc* desc, const void* w_dev, const void* x_dev,
+                            int32_t per_slot_x, const int32_t* ids_dev, int32_t ntok, int32_t top_k,
+                            void* y_dev, int32_t* sums_dev, size_t sums_bytes, uint32_t flags, void* stream);
 
 /*
  * Test export (host only, no device needed): the CUDA-core matvec's launch

@@ -185,7 +185,7 @@ def test_sorted_gather(fmt, ntok, top_k, per_slot):
     nvec = ntok * top_k if per_slot else ntok
     x = qi.normal_bf16_bits(g, (nvec, K))
     y = torch.full((ntok, top_k, N), 5.0, dtype=torch.bfloat16, device=DEV)
-    qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), int(per_slot), to_dev(ids), ntok, top_k, y)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, to_dev(x), int(per_slot), to_dev(ids), ntok, top_k, y, qmv.QMV_FLAG_PATH_TENSOR)
     got = bf16_to_np(y)
     cache = {}
     for t in range(ntok):
@@ -215,7 +215,7 @@ def test_sorted_gather_prefetch_chain():
     x = to_dev(qi.normal_bf16_bits(g, (ntok, K)))
     ids_d = to_dev(ids)
     y1 = torch.full((ntok, top_k, N), 3.0, dtype=torch.bfloat16, device=DEV)
-    qmv.qmv_moe_gather(m.desc, m.w, x, 0, ids_d, ntok, top_k, y1)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, x, 0, ids_d, ntok, top_k, y1, qmv.QMV_FLAG_PATH_TENSOR)
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -223,7 +223,8 @@ def test_sorted_gather_prefetch_chain():
     y2 = torch.full_like(y1, 4.0)
     with torch.cuda.stream(s):
         x2.copy_(x)
-        qmv.qmv_moe_gather_ex(m.desc, m.w, x2, 0, ids_d, ntok, top_k, y2, qmv.QMV_FLAG_PREFETCH_INPUTS, stream=s)
+        qmv.qmv_moe_gather_ex(m.desc, m.w, x2, 0, ids_d, ntok, top_k, y2,
+                              qmv.QMV_FLAG_PREFETCH_INPUTS | qmv.QMV_FLAG_PATH_TENSOR, stream=s)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
@@ -306,7 +307,7 @@ def test_extreme_scales_sorted_gather(fmt):
         m.set_expert(e, *mats[e])
     x = qi.scaled_normal_bf16_bits(g, (ntok, K), TOKEN_SHIFTS[:ntok])
     y = torch.full((ntok, top_k, N), 3.0, dtype=torch.bfloat16, device=DEV)
-    qmv.qmv_moe_gather(m.desc, m.w, to_dev(x), 0, to_dev(ids), ntok, top_k, y)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, to_dev(x), 0, to_dev(ids), ntok, top_k, y, qmv.QMV_FLAG_PATH_TENSOR)
     got = bf16_to_np(y)
     for t in range(ntok):
         for j in range(top_k):
@@ -315,6 +316,54 @@ def test_extreme_scales_sorted_gather(fmt):
             mask, absum = _in_range(fmt, c, s, x[t:t + 1])
             assert_within(got[t, j][mask[0]], ref[mask[0]], 1e-3 * absum[0][mask[0]] + FP32_TINY, "bf16",
                           f"slot ({t},{j})")
+    assert status_clean()
+
+
+SPREAD_SETS = (
+    (100, 124),        # 24 octaves: 2^-24, f16's smallest subnormal, as the factor of the smaller scale
+    (110, 118, 125),   # factors 2^-15 (subnormal) and 2^-7
+    (99, 124),         # 25 octaves: recomputed on the CUDA cores
+    (230, 254),        # the largest legal scales, 24 octaves apart
+    (0, 1, 20),        # the smallest legal scales
+    (112, 122),        # the usual range
+)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("ntok", [8, 16])
+def test_verify_scale_spread(fmt, ntok):
+    """Rows whose scale bytes span up to 24 octaves take the tensor cores with
+    factors 2^(e - e_ref) down to 2^-24; wider rows and rows holding the NaN
+    byte 255 are recomputed on the CUDA cores. Per (token, row) against the
+    oracle wherever the products stay inside fp32's range."""
+    N, K = 264, 2048
+    g = qi.rng(2200 + ntok + (7 if fmt == "mxfp8" else 0))
+    codes = qi.format_codes(g, fmt, (N, K))
+    scales = np.empty((N, K // 32), np.uint8)
+    kinds = len(SPREAD_SETS) + 1
+    for r in range(N):
+        kind = r % kinds
+        if kind < len(SPREAD_SETS):
+            scales[r] = qi.e8m0_choice(g, (K // 32,), SPREAD_SETS[kind])
+        else:
+            scales[r] = qi.e8m0_choice(g, (K // 32,), (118, 120))
+            scales[r, int(g.integers(0, K // 32))] = 255
+    m = Matrices(fmt, N, K, 1, [], seed=3)
+    m.set_expert(0, codes, scales)
+    x = qi.scaled_normal_bf16_bits(g, (ntok, K), TOKEN_SHIFTS[:ntok])
+    y = torch.full((ntok, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    qmv.qmv_dense(m.desc, m.w, to_dev(x), ntok, y)
+    got = bf16_to_np(y)
+    nan_rows = np.arange(N) % kinds == len(SPREAD_SETS)
+    assert np.isnan(got[:, nan_rows]).all()
+    keep = ~nan_rows
+    ref = oracle.mx_matvec(fmt, codes[keep], scales[keep], x)
+    mask, absum = _in_range(fmt, codes[keep], scales[keep], x)
+    sub = got[:, keep]
+    assert_within(sub[mask], ref[mask], 1e-3 * absum[mask] + FP32_TINY, "bf16", f"{fmt} ntok={ntok}")
+    for kind in range(len(SPREAD_SETS)):
+        rows = (np.arange(N)[keep] % kinds) == kind
+        assert mask[:, rows].any(), SPREAD_SETS[kind]
     assert status_clean()
 
 
@@ -337,17 +386,23 @@ def test_verify_codebook_block_sums(fmt, N, K, ntok):
     xq, q, d = quantize_on_gpu(xf)
     y = torch.full((ntok, N), 3.0, dtype=torch.float32, device=DEV)
     sums = torch.full((ntok, N, K // grp), -7, dtype=torch.int32, device=DEV)
-    qmv.qmv_debug_block_sums(m.desc, m.w, xq, 0, None, ntok, 1, y, sums)
+    qmv.qmv_debug_block_sums(m.desc, m.w, xq, 0, None, ntok, 1, y, sums, flags=qmv.QMV_FLAG_PATH_TENSOR)
     want = oracle.cb_block_sums(m.codes[0], m.lut, q, grp)
     assert np.array_equal(sums.cpu().numpy(), want), "block sums differ from the oracle"
     ref = oracle.cb_matvec(m.codes[0], m.scales[0], m.lut, grp, q, d)
     absum = oracle.cb_abs_products(m.codes[0], m.scales[0], m.lut, grp, q, d)
     assert_close(y.cpu().numpy(), ref, absum, "f32", f"{fmt} {N}x{K} ntok={ntok}")
     y2 = torch.full_like(y, -3.0)
-    qmv.qmv_dense_ex(m.desc, m.w, to_dev(xf), ntok, y2, qmv.QMV_FLAG_X_F32)
+    qmv.qmv_dense_ex(m.desc, m.w, to_dev(xf), ntok, y2, qmv.QMV_FLAG_X_F32 | qmv.QMV_FLAG_PATH_TENSOR)
     y3 = torch.full_like(y, -4.0)
-    qmv.qmv_dense(m.desc, m.w, xq, ntok, y3)
+    qmv.qmv_dense_ex(m.desc, m.w, xq, ntok, y3, qmv.QMV_FLAG_PATH_TENSOR)
+    # the CUDA-core path (one weight stream per 4 tokens): the same block sums
+    y4 = torch.full_like(y, -5.0)
+    sums4 = torch.full_like(sums, -8)
+    qmv.qmv_debug_block_sums(m.desc, m.w, xq, 0, None, ntok, 1, y4, sums4, flags=qmv.QMV_FLAG_PATH_CUDA_CORES)
     torch.cuda.synchronize()
+    assert torch.equal(sums4, sums)
+    assert_close(y4.cpu().numpy(), ref, absum, "f32", f"{fmt} {N}x{K} ntok={ntok} CUDA cores")
     assert torch.equal(y2.view(torch.int32), y3.view(torch.int32))
     assert torch.equal(y.view(torch.int32), y3.view(torch.int32))
     assert status_clean()
@@ -377,7 +432,7 @@ def test_sorted_gather_codebook(fmt, N, K, E, ntok, top_k, per_slot):
     y = torch.full((ntok, top_k, N), 5.0, dtype=torch.float32, device=DEV)
     sums = torch.full((ntok, top_k, N, K // grp), -7, dtype=torch.int32, device=DEV)
     ids_d = to_dev(ids)
-    qmv.qmv_debug_block_sums(m.desc, m.w, xq, int(per_slot), ids_d, ntok, top_k, y, sums)
+    qmv.qmv_debug_block_sums(m.desc, m.w, xq, int(per_slot), ids_d, ntok, top_k, y, sums, flags=qmv.QMV_FLAG_PATH_TENSOR)
     got_sums, got = sums.cpu().numpy(), y.cpu().numpy()
     for t in range(ntok):
         for j in range(top_k):
@@ -391,9 +446,10 @@ def test_sorted_gather_codebook(fmt, N, K, E, ntok, top_k, per_slot):
             absum = oracle.cb_abs_products(m.codes[e], m.scales[e], m.lut, grp, q[v:v + 1], d[v:v + 1])[0]
             assert_close(got[t, j], ref, absum, "f32", f"slot ({t},{j}) expert {e}")
     y2 = torch.full_like(y, -5.0)
-    qmv.qmv_moe_gather_ex(m.desc, m.w, to_dev(xf), int(per_slot), ids_d, ntok, top_k, y2, qmv.QMV_FLAG_X_F32)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, to_dev(xf), int(per_slot), ids_d, ntok, top_k, y2,
+                          qmv.QMV_FLAG_X_F32 | qmv.QMV_FLAG_PATH_TENSOR)
     y3 = torch.full_like(y, -6.0)
-    qmv.qmv_moe_gather(m.desc, m.w, xq, int(per_slot), ids_d, ntok, top_k, y3)
+    qmv.qmv_moe_gather_ex(m.desc, m.w, xq, int(per_slot), ids_d, ntok, top_k, y3, qmv.QMV_FLAG_PATH_TENSOR)
     torch.cuda.synchronize()
     assert torch.equal(y2.view(torch.int32), y3.view(torch.int32))
     assert torch.equal(y.view(torch.int32), y3.view(torch.int32))

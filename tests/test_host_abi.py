@@ -171,27 +171,29 @@ def test_gather_argument_errors(top_k, ids, code):
 
 
 def test_routed_slot_limit():
-    """Gathers route at most QMV_MAX_SLOTS (128) (token, slot) pairs; beyond
-    QMV_MAX_LAYER_SLOTS (32) only the sorted tensor-core gather takes them
-    (any format, not fp16 activations); layers stop at 32; 16 tokens is the
-    dense limit. (No call here reaches a launch: every one fails validation,
-    or, for the accepted 64-slot codebook gather, the device query of a
-    machine without a GPU.)"""
+    """Gathers and layers route at most QMV_MAX_SLOTS (128) (token, slot)
+    pairs, any format and activation type (beyond QMV_MAX_LAYER_SLOTS (32)
+    they run as the sorted tensor-core gather or as CUDA-core gathers of 32
+    slots each); 16 tokens and top-8 are the limits. (No call here reaches a
+    launch: every one fails validation, or, for the accepted calls, the
+    device query of a machine without a GPU.)"""
     assert qmv.MAX_SLOTS == 128 and qmv.MAX_LAYER_SLOTS == 32 and qmv.MAX_NTOK == 16
     B = qmv.ctypes.byref
     G = qmv.lib.qmv_moe_gather_ex
     cb = qmv.wdesc("cb3", 64, 64, 8, qi.LUT_CB3)
-    assert G(B(cb), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) != qmv.QMV_EINVAL      # 64 codebook slots: sorted gather
+    assert G(B(cb), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, 0, 0) != qmv.QMV_EINVAL      # 64 codebook slots
     assert G(B(cb), FAKE, FAKE, 0, FAKE, 16, 9, FAKE, 0, 0) == qmv.QMV_EINVAL     # 144 slots
     mx = qmv.wdesc("mxfp4", 64, 64, 8)
-    assert G(B(mx), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL   # fp16: no sorted path
+    assert G(B(mx), FAKE, FAKE, 0, FAKE, 8, 8, FAKE, qmv.QMV_FLAG_X_F16, 0) != qmv.QMV_EINVAL   # fp16, 64 slots
     assert G(B(mx), FAKE, FAKE, 0, FAKE, 17, 1, FAKE, 0, 0) == qmv.QMV_EINVAL     # 17 tokens
     assert G(B(mx), FAKE, FAKE, 0, FAKE, 16, 9, FAKE, 0, 0) == qmv.QMV_EINVAL     # top_k 9
     gu = qmv.wdesc("mxfp4", 64, 64, 8)
     assert qmv.qmv_moe_layer_workspace_bytes(gu, 8, 4) == (32 * 64 * 2 + 255) // 256 * 256
-    assert qmv.qmv_moe_layer_workspace_bytes(gu, 16, 4) == 0                        # 64 slots: no layer
+    assert qmv.qmv_moe_layer_workspace_bytes(gu, 16, 8) == (128 * 64 * 2 + 255) // 256 * 256
+    assert qmv.qmv_moe_layer_workspace_bytes(gu, 16, 9) == 0                        # 144 slots
     L = qmv.lib.qmv_moe_layer
-    assert L(B(gu), FAKE, B(gu), FAKE, FAKE, FAKE, 16, 4, FAKE, 1 << 20, FAKE, 0, 0) == qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(gu), FAKE, FAKE, FAKE, 16, 4, FAKE, 1 << 20, FAKE, 0, 0) != qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(gu), FAKE, FAKE, FAKE, 16, 9, FAKE, 1 << 20, FAKE, 0, 0) == qmv.QMV_EINVAL
     assert qmv.lib.qmv_quantize_act_q8(FAKE, 129, 64, FAKE, 1 << 22, 0) == qmv.QMV_EINVAL
 
 
@@ -235,12 +237,18 @@ def test_unknown_launch_flags_rejected():
     rc = qmv.lib.qmv_moe_gather_ex(qmv.ctypes.byref(d), FAKE, FAKE, 0, FAKE, 1, 4, FAKE, 6, 0)
     assert rc == qmv.QMV_EINVAL
     d = qmv.wdesc("cb2", 64, 64)
-    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 8, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, 32, 0) == qmv.QMV_EINVAL
+    # the two path overrides are exclusive; block sums take only prefetch and path flags
+    both = qmv.QMV_FLAG_PATH_TENSOR | qmv.QMV_FLAG_PATH_CUDA_CORES
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 8, FAKE, both, 0) == qmv.QMV_EINVAL
+    S = qmv.lib.qmv_debug_block_sums_ex
+    assert S(qmv.ctypes.byref(d), FAKE, FAKE, 0, None, 1, 1, FAKE, FAKE, 1 << 20, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
+    assert S(qmv.ctypes.byref(d), FAKE, FAKE, 0, None, 1, 1, FAKE, FAKE, 1 << 20, both, 0) == qmv.QMV_EINVAL
     # fp16 activations exist only for the MX formats, fp32 ones only for the codebooks
     assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(d), FAKE, FAKE, 1, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL
     m8 = qmv.wdesc("mxfp8", 64, 64)
     assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(m8), FAKE, FAKE, 1, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
-    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(m8), FAKE, FAKE, 1, FAKE, 8, 0) == qmv.QMV_EINVAL
+    assert qmv.lib.qmv_dense_ex(qmv.ctypes.byref(m8), FAKE, FAKE, 1, FAKE, 64, 0) == qmv.QMV_EINVAL
     C = qmv.lib.qmv_moe_combine_ex
     cb = qmv.wdesc("cb3", 64, 64, 4)
     assert C(qmv.ctypes.byref(cb), FAKE, FAKE, FAKE, 1, 4, FAKE, qmv.QMV_FLAG_X_F16, 0) == qmv.QMV_EINVAL
@@ -291,7 +299,7 @@ def test_moe_layer_argument_errors():
     cb = qmv.wdesc("cb3", 2880, 2880, 32)
     assert L(B(gu), FAKE, B(cb), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, None, 1, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
-    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 8, 0) == qmv.QMV_EINVAL   # unknown flag
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, 32, 0) == qmv.QMV_EINVAL   # unknown flag
     # fp32 activations exist only for the codebook formats
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, 1, 4, FAKE, need, FAKE, qmv.QMV_FLAG_X_F32, 0) == qmv.QMV_EINVAL
     d = qmv.wdesc("mxfp4", 64, 64)
@@ -320,4 +328,4 @@ def test_combine_argument_errors():
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need - 16, FAKE, 0, 0) == qmv.QMV_ESIZE
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, None, 2, 4, FAKE, need, FAKE, 0, 0) == qmv.QMV_EINVAL
     assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, None, need, FAKE, 0, 0) == qmv.QMV_ESIZE
-    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need, FAKE, 8, 0) == qmv.QMV_EINVAL
+    assert L(B(gu), FAKE, B(dn), FAKE, FAKE, FAKE, FAKE, 2, 4, FAKE, need, FAKE, 32, 0) == qmv.QMV_EINVAL
