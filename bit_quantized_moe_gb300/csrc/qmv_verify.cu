@@ -373,33 +373,31 @@ __device__ __forceinline__ void stage_unit_q8(const VParams& p, int vec, int g, 
   aux[gl * kVTok + t] = f;
 }
 
+// 16 bytes global -> shared without a register round trip (cp.async, L2
+// only); src_bytes = 0 writes zeros (and reads nothing).
+__device__ __forceinline__ void cp_async16(uint8_t* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // MX, activation operand B: the bf16 columns [32 g0, 32 g0 + 64 steps) of
 // tokens t < T, zero beyond the CTA's range and for padding tokens. Units of
-// 8 columns (16 bytes); each thread issues four loads before it stores.
-__device__ __forceinline__ void stage_x_bf16(const VParams& p, int T, int g0, int g1, int steps, int tid,
-                                             const int* slot, uint8_t* bbuf) {
-  constexpr int kU = 4;
+// 8 columns (16 bytes), every one of a thread's copies in flight at once
+// (cp.async); the caller waits for them (cp_async_wait_all) before the
+// barrier that publishes the operand.
+__device__ __forceinline__ void stage_x_bf16_async(const VParams& p, int T, int g0, int g1, int steps, int tid,
+                                                   const int* slot, uint8_t* bbuf) {
   const int n_units = steps * (kVStepK / 8) * kVTok;
   const int k_end = g1 * 32;
-  for (int u0 = tid; u0 < n_units; u0 += kU * kDecoders) {
-    uint4 v[kU];
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int u = u0 + j * kDecoders;
-      const int t = u % kVTok, kk = u / kVTok;
-      const int k = g0 * 32 + kk * 8;
-      v[j] = make_uint4(0, 0, 0, 0);
-      if (u < n_units && t < T && k < k_end) {
-        const int vec = (p.ids == nullptr) ? t : (p.per_slot ? slot[t] : slot[t] / p.top_k);
-        v[j] = *reinterpret_cast<const uint4*>(p.x + (size_t)vec * p.x_vec_bytes + (size_t)k * 2);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int u = u0 + j * kDecoders;
-      const int t = u % kVTok, kk = u / kVTok;
-      if (u < n_units) *reinterpret_cast<uint4*>(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16) = v[j];
-    }
+  for (int u = tid; u < n_units; u += kDecoders) {
+    const int t = u % kVTok, kk = u / kVTok;
+    const int k = g0 * 32 + kk * 8;
+    const bool valid = t < T && k < k_end;
+    const int vec = (p.ids == nullptr) ? t : (p.per_slot ? slot[t < T ? t : 0] : slot[t < T ? t : 0] / p.top_k);
+    const uint8_t* src = valid ? p.x + (size_t)vec * p.x_vec_bytes + (size_t)k * 2 : p.x;
+    cp_async16(bbuf + (size_t)kk * 256 + (t >> 3) * 128 + (t & 7) * 16, src, valid ? 16u : 0u);
   }
 }
 
@@ -617,9 +615,10 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
   }
   // Lane pairs take the two groups of one row: warp w rows 16 w .. + 15,
   // lane l row 16 w + l / 2 and group 2 step + l % 2, so one warp load
-  // covers 16 rows x 32 contiguous bytes. The first window of loads goes out
-  // first (before griddepcontrol.wait when the caller guarantees the weights
-  // are not the preceding kernel's output), then the activations.
+  // covers 16 rows x 32 contiguous bytes. The activation copies and the
+  // first window of weight loads go out together: the weights first when the
+  // caller guarantees that they are not the preceding kernel's output (they
+  // are loaded before griddepcontrol.wait), else the activations first.
   const bool decoder = tid < kDecoders;
   const int h = lane & 1;
   const int r = (warp & 7) * 16 + (lane >> 1);
@@ -628,16 +627,21 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
   const bool row_ok = decoder && rt < p.row_tiles;
   uint8_t* a_row = abuf + (r >> 3) * 128 + (r & 7) * 16;
   Block<FMT> win[F::window];
-  if (!p.prefetch) pdl_wait();
+  if (!p.prefetch) {
+    pdl_wait();
+    if (decoder) stage_x_bf16_async(p, T, g0, g1, steps, tid, gs.slot, bbuf);
+  }
 #pragma unroll
   for (int u = 0; u < F::window; ++u) {
     const int g = g0 + 2 * u + h;
     load_block<FMT>(p, w, rt, r8, g, row_ok && u < steps && g < g1, win[u]);
   }
-  if (p.prefetch) pdl_wait();
+  if (p.prefetch) {
+    pdl_wait();
+    if (decoder) stage_x_bf16_async(p, T, g0, g1, steps, tid, gs.slot, bbuf);
+  }
   pdl_launch_dependents();
-  if (decoder) stage_x_bf16(p, T, g0, g1, steps, tid, gs.slot, bbuf);
-
+  cp_async_wait_all();
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
