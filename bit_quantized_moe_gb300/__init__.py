@@ -51,7 +51,7 @@ EXPORTS = (
     "qmv_dense", "qmv_moe_gather", "qmv_dense_ex", "qmv_moe_gather_ex", "qmv_packed_gate_up_expert_bytes",
     "qmv_pack_gate_up", "qmv_moe_gate_up_swiglu", "qmv_moe_layer_workspace_bytes", "qmv_moe_layer",
     "qmv_moe_layer_noalloc", "qmv_moe_combine", "qmv_moe_combine_ex", "qmv_moe_layer_combine_workspace_bytes", "qmv_moe_layer_combine",
-    "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_block_sums_ex", "qmv_debug_dequant", "qmv_debug_plan",
+    "qmv_swiglu_bf16", "qmv_debug_block_sums", "qmv_debug_block_sums_ex", "qmv_debug_path", "qmv_debug_dequant", "qmv_debug_plan",
     "qmv_device_status", "qmv_debug_wait_probe", "qmv_debug_chunk_rate", "qmv_debug_phase_entries",
     "qmv_debug_phase_probe",
     "qmv_debug_phase_read", "qmv_last_error", "qmv_version",
@@ -116,6 +116,7 @@ def _load() -> ctypes.CDLL:
         "qmv_swiglu_bf16": (ctypes.c_int, [P, P, P, I64, P]),
         "qmv_debug_block_sums": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, P]),
         "qmv_debug_block_sums_ex": (ctypes.c_int, [D, P, P, I32, P, I32, I32, P, P, SZ, ctypes.c_uint32, P]),
+        "qmv_debug_path": (ctypes.c_int, [D, I32, I32, I32, I32, ctypes.c_uint32, P, I32]),
         "qmv_debug_dequant": (ctypes.c_int, [D, P, I32, P, SZ, P]),
         "qmv_debug_plan": (ctypes.c_int, [D, I32, I32, I32, I32, ctypes.c_uint32, I32, I32, I64,
                                           ctypes.POINTER(I64), I32]),
@@ -335,6 +336,15 @@ def qmv_debug_block_sums(desc: WDesc, w, x, per_slot_x: int, ids, ntok: int, top
                          stream=None, flags: int = 0) -> None:
     _check(lib.qmv_debug_block_sums_ex(ctypes.byref(desc), _ptr(w), _ptr(x), int(per_slot_x), _ptr(ids), ntok,
                                        top_k, _ptr(y), _ptr(sums), _nbytes(sums), int(flags), _stream(stream)))
+
+
+def qmv_debug_path(desc: WDesc, ntok: int, top_k: int = 1, gather: bool = False, glu: bool = False,
+                   flags: int = 0):
+    """(tensor cores?, tokens per CUDA-core launch) of a call (host only)."""
+    out = (ctypes.c_int64 * 2)()
+    _check(lib.qmv_debug_path(ctypes.byref(desc), int(ntok), int(top_k), int(bool(gather)), int(bool(glu)),
+                              int(flags), out, 2))
+    return bool(out[0]), int(out[1])
 
 
 def qmv_debug_dequant(desc: WDesc, w, expert: int, out, stream=None) -> None:

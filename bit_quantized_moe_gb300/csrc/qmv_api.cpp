@@ -589,6 +589,37 @@ int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t g
   return ok();
 }
 
+int qmv_debug_path(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t gather, int32_t glu,
+                   uint32_t flags, int64_t* out, int32_t n_out) {
+  const char* name = "qmv_debug_path";
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (!out || n_out < 2) return fail(QMV_ESIZE, "%s: out needs 2 entries", name);
+  if (ntok < 1 || ntok > QMV_MAX_NTOK || top_k < 1 || top_k > QMV_MAX_TOPK ||
+      (gather && ntok * top_k > QMV_MAX_SLOTS) || (glu && !gather))
+    return fail(QMV_EINVAL, "%s: ntok=%d / top_k=%d / gather=%d / glu=%d out of range", name, ntok, top_k, gather,
+                glu);
+  rc = check_flags(desc->fmt, flags, false, name);
+  if (rc) return rc;
+  MatvecArgs a;
+  a.fmt = desc->fmt;
+  a.N = glu ? gate_up_rows(desc->N) : desc->N;
+  a.K = desc->K;
+  a.n_experts = desc->n_experts;
+  static const int32_t dummy = 0;
+  a.ids = gather ? &dummy : nullptr;
+  a.ntok = ntok;
+  a.top_k = gather ? top_k : 1;
+  a.x_f32 = (flags & QMV_FLAG_X_F32) != 0;
+  a.x_f16 = (flags & QMV_FLAG_X_F16) != 0;
+  a.glu = glu != 0;
+  a.out_n = desc->N;
+  a.path = (flags & QMV_FLAG_PATH_TENSOR) ? 1 : ((flags & QMV_FLAG_PATH_CUDA_CORES) ? 2 : 0);
+  out[0] = use_tensor_cores(a) ? 1 : 0;
+  out[1] = gather_launch_tokens(a);
+  return ok();
+}
+
 int qmv_debug_block_sums(const qmv_wdesc* desc, const void* w, const void* x, int32_t per_slot_x,
                          const int32_t* ids, int32_t ntok, int32_t top_k, void* y, int32_t* sums,
                          size_t sums_bytes, void* stream) {

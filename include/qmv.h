@@ -455,6 +455,18 @@ int qmv_debug_plan(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t g
                    int32_t n_out);
 
 /*
+ * Test export (host only, no device needed): the path a call of this shape
+ * and these flags takes (QMV_FLAG_PATH_* included). out (>= 2 entries):
+ * out[0] = 1 for the tcgen05 tensor-core kernels (verify batch or sorted
+ * gather), 0 for the CUDA-core matvec; out[1] = tokens per CUDA-core launch
+ * (ntok, or QMV_MAX_LAYER_SLOTS / top_k for a gather of more routed slots).
+ * gather != 0 describes an expert gather; glu != 0 the fused gate/up
+ * (qmv_moe_gate_up_swiglu). Errors: QMV_EINVAL, QMV_ESIZE.
+ */
+int qmv_debug_path(const qmv_wdesc* desc, int32_t ntok, int32_t top_k, int32_t gather, int32_t glu,
+                   uint32_t flags, int64_t* out, int32_t n_out);
+
+/*
  * Test export: decode the GPU weight layout of one matrix with the kernels'
  * device decode routines to fp32 w_dev [N][K] = value(code) * 2^(e-127).
  * For the CB formats value(code) = lut[code].

@@ -137,3 +137,69 @@ def test_sorted_gather_items_cover_slots_within_grid_bound():
         valid = [s for s, e in enumerate(ids.reshape(-1)) if 0 <= e < E]
         assert covered == valid                 # every valid slot exactly once
         assert all(1 <= len(g) <= 16 for _, g in items)
+
+
+# ---------------------------------------------------------------------------
+# Tensor cores or CUDA cores: the cost model of the verify batch and of
+# gathers beyond 32 routed slots, and the QMV_FLAG_PATH_* overrides
+# ---------------------------------------------------------------------------
+
+def test_path_dense_verify_batches():
+    """MX dense calls of 5..16 bf16 tokens take the tensor cores (not 1..4
+    tokens, not fp16 activations); codebook ones only when their CUDA-core
+    weight streams (one per 4 tokens) exceed 64 MB."""
+    P = qmv.qmv_debug_path
+    mx = qmv.wdesc("mxfp4", 2880, 2880)
+    assert [P(mx, n)[0] for n in range(1, 17)] == [False] * 4 + [True] * 12
+    assert P(mx, 16, flags=qmv.QMV_FLAG_X_F16) == (False, 16)
+    assert P(mx, 16, flags=qmv.QMV_FLAG_PATH_CUDA_CORES) == (False, 16)
+    assert P(mx, 4, flags=qmv.QMV_FLAG_PATH_TENSOR) == (False, 4)   # no tensor-core form at 4 tokens
+    cb4 = qmv.wdesc("cb4", 7168, 7168)                                # 27.3 MB per stream
+    assert P(cb4, 16)[0] and P(cb4, 9)[0] and not P(cb4, 8)[0] and not P(cb4, 5)[0]   # 3 streams: 82 MB
+    cb3 = qmv.wdesc("cb3", 7168, 2048)
+    assert not P(cb3, 16)[0]
+    assert P(cb3, 16, flags=qmv.QMV_FLAG_PATH_TENSOR)[0]
+    assert P(cb3, 16, flags=qmv.QMV_FLAG_PATH_TENSOR | qmv.QMV_FLAG_X_F32)[0]
+
+
+@pytest.mark.parametrize("fmt,E,ntok,top_k,tensor", [
+    ("mxfp4", 32, 16, 8, True),     # 128 slots, 4 per expert
+    ("mxfp4", 32, 16, 4, False),    # 64 slots, 2 per expert
+    ("mxfp4", 16, 16, 4, True),     # 64 slots, 4 per expert
+    ("mxfp4", 256, 16, 8, False),   # 128 slots, 1 per expert
+    ("mxfp8", 8, 9, 4, True),       # 36 slots, 4.5 per expert
+    ("cb3", 8, 16, 8, True),        # 128 slots, 16 per expert
+    ("cb3", 16, 16, 8, False),      # 128 slots, 8 per expert
+    ("cb2", 2, 16, 2, True),        # 32 slots: the decode gather
+])
+def test_path_gathers(fmt, E, ntok, top_k, tensor):
+    """Gathers of 33..128 routed slots: the sorted tensor-core gather at >= 4
+    (MX) or >= 12 (codebooks) slots per expert that can occur, else CUDA-core
+    gathers of 32-slot token ranges; 32 slots or fewer are always the decode
+    gather in one launch."""
+    lut = {"cb2": [0] * 4, "cb3": [0] * 8, "cb4": [0] * 16}.get(fmt)
+    d = qmv.wdesc(fmt, 1024, 2048, E, lut)
+    slots = ntok * top_k
+    if slots <= 32:
+        assert qmv.qmv_debug_path(d, ntok, top_k, gather=True) == (False, ntok)
+        return
+    assert qmv.qmv_debug_path(d, ntok, top_k, gather=True) == (tensor, 32 // top_k)
+    assert qmv.qmv_debug_path(d, ntok, top_k, gather=True, flags=qmv.QMV_FLAG_PATH_TENSOR)[0]
+    assert qmv.qmv_debug_path(d, ntok, top_k, gather=True, flags=qmv.QMV_FLAG_PATH_CUDA_CORES) == (False,
+                                                                                                  32 // top_k)
+
+
+def test_path_gate_up_and_fp16_have_no_tensor_form():
+    """The fused gate/up and fp16 activations run on the CUDA cores at any slot
+    count, split into launches of at most 32 slots; the overrides are
+    exclusive."""
+    d = qmv.wdesc("mxfp4", 2880, 2880, 32)
+    assert qmv.qmv_debug_path(d, 16, 8, gather=True, glu=True) == (False, 4)
+    assert qmv.qmv_debug_path(d, 16, 8, gather=True, glu=True, flags=qmv.QMV_FLAG_PATH_TENSOR) == (False, 4)
+    assert qmv.qmv_debug_path(d, 16, 8, gather=True, flags=qmv.QMV_FLAG_X_F16) == (False, 4)
+    assert qmv.qmv_debug_path(d, 5, 7, gather=True) == (False, 4)   # 35 slots, top-7: 4 tokens per launch
+    with pytest.raises(qmv.QmvError):
+        qmv.qmv_debug_path(d, 16, 8, gather=True,
+                           flags=qmv.QMV_FLAG_PATH_TENSOR | qmv.QMV_FLAG_PATH_CUDA_CORES)
+    with pytest.raises(qmv.QmvError):
+        qmv.qmv_debug_path(d, 16, 9, gather=True)
