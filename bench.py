@@ -648,7 +648,7 @@ def run_configs(args):
 
     # --- verify batches (f3): dense 8 and 16 tokens (one weight stream per 4 tokens, side by side)
     for fmt, (Nv, Kv) in (("mxfp4", (2880, 2880)), ("mxfp8", (2880, 2880)), ("mxfp4", (7168, 7168)),
-                          ("cb4", (7168, 7168))):
+                          ("mxfp8", (7168, 7168)), ("cb4", (7168, 7168))):
         dv = qmv.wdesc(fmt, Nv, Kv, 1, luts(fmt))
         bv = qmv.qmv_packed_bytes(dv)
         algv = Nv * Kv * qi.FORMAT_BITS[fmt] // 8 + Nv * (Kv // 32)
