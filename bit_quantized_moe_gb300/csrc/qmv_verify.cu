@@ -12,7 +12,8 @@
 // (kind::f16, M = 128 rows, N = 16 tokens, K = 16) into tensor memory.
 //
 // MX formats (verify_mx_kernel) -- bf16 operands, one accumulator per row:
-//   A (weights): code x 2^(e - e_ref) as bf16, where e_ref is the row's
+//   A (weights, in tensor memory: lane = row, bf16 pairs along the columns):
+//      code x 2^(e - e_ref) as bf16, where e_ref is the row's
 //      first E8M0 byte in the CTA's K range plus kRefMargin (at most 254).
 //      The factor 2^(e - e_ref) (e - e_ref in [-24, 0]) is an exact f16, so
 //      one mixed-precision FMA
@@ -50,11 +51,13 @@
 // thread-block cluster and add their partial sums through distributed shared
 // memory in rank order (deterministic), each rank storing a share of the
 // outputs. Per CTA: 8 decoding warps, their weight loads issued a window of
-// steps ahead, and one warp that issues the MMAs. Three A buffers of 64
-// columns, each with a "full" barrier (one arrival per decoding warp) and an
-// "empty" one (tcgen05.commit). MX: lane pairs take the two 32-groups of one
-// row (warp w: rows 16 w .. 16 w + 15), so a warp load covers 16 rows x 32
-// contiguous bytes. Codebooks: warp w decodes rows 32 (w % 4) .. + 31 (the
+// steps ahead, and one warp that issues the MMAs. A stages of 64 columns,
+// each with a "full" barrier (one arrival per decoding warp that writes it)
+// and an "empty" one (tcgen05.commit). MX: six stages in tensor memory; warp
+// w writes rows 32 (w % 4) .. + 31 (its quadrant of lanes) of the steps of
+// parity w / 4, both 32-groups of the step for its row (one tcgen05.st of 16
+// columns each). Codebooks: three stages in shared memory; warp w decodes
+// rows 32 (w % 4) .. + 31 (the
 // tensor-memory lanes it may read) and group w / 4 of every step; the
 // accumulators of kAccSteps steps live in tensor memory, each step's with an
 // "accumulated" barrier (tcgen05.commit) and a "drained" one, and a warp
@@ -570,18 +573,76 @@ __device__ void recompute_rows(const VParams& p, const uint8_t* w, int rb, int g
   }
 }
 
+// MX: 16 fp32 tensor-memory columns x 32 lanes of this warp's quadrant from
+// 16 registers per thread (thread l -> lane base + l).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                  "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// MMA with A read from tensor memory (M = 128 lanes, K = 16 bf16 in 8
+// columns), B from shared memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+               " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(kIdescBf16), "r"(accumulate));
+}
+
+// MX: 32 codes of a lane block -> 16 bf16x2 words code x 2^(e - e_ref) (as
+// decode_store_ref, into registers). Returns whether the block's scale byte
+// is outside [e_ref - 24, e_ref].
+template <int FMT>
+__device__ __forceinline__ bool decode_ref(const Block<FMT>& b, int eref, uint32_t (&out)[16]) {
+  int d = (int)b.e - eref;
+  const bool bad = (d < -kMaxSpread || d > 0) && b.e != kNoScale;
+  d = d < -kMaxSpread ? -kMaxSpread : (d > 0 ? 0 : d);
+  const uint16_t m = pow2_f16(d);
+  if constexpr (FMT == MXFP4) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t h[4];
+      e2m1x8_to_f16x2(b.c[q], h);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[4 * q + i] = scaled_pair_bf16(h[i], m);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t h[2];
+      e4m3x4_to_f16x2(b.c[q], h);
+      out[2 * q] = scaled_pair_bf16(h[0], m);
+      out[2 * q + 1] = scaled_pair_bf16(h[1], m);
+    }
+  }
+  return bad;
+}
+
+constexpr int kTmAStages = 6;          // MX: A operand stages in tensor memory (32 columns each)
+constexpr uint32_t kTmACol0 = 32;      // MX: first A column (the accumulator takes columns 0..15)
+constexpr uint32_t kTmCols = 256;      // MX: tensor-memory columns per CTA (two CTAs per SM)
+
 // MX formats: bf16 operands code x 2^(e - e_ref), one accumulator per row
-// for the CTA's whole K range, 2^(e_ref - 127) applied in the epilogue.
+// for the CTA's whole K range, 2^(e_ref - 127) applied in the epilogue. The
+// A operand lives in tensor memory: lane = row, a step's 64 columns in 32
+// columns of bf16 pairs; warp w decodes rows 32 (w % 4) .. + 31 (its
+// quadrant of lanes) and the steps of parity w / 4, both lane blocks of the
+// step for its row, and writes them with one tcgen05.st each.
 template <int FMT>
 __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_constant__ VParams p) {
   using F = VFmt<FMT>;
   static_assert(fmt_is_mx(FMT), "MX formats");
+  constexpr int kWin = F::window / 2;   // steps of loads in flight per thread (two lane blocks each)
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t empty[kVBufs];   // A buffer read by the MMAs (tcgen05.commit)
-  __shared__ __align__(8) uint64_t full[kVBufs];    // A buffer written by all decoding warps
-  __shared__ __align__(8) uint64_t done;            // every MMA complete (tcgen05.commit)
+  __shared__ __align__(8) uint64_t empty[kTmAStages];   // A stage read by the MMAs (tcgen05.commit)
+  __shared__ __align__(8) uint64_t full[kTmAStages];    // A stage written by the 4 warps of its parity
+  __shared__ __align__(8) uint64_t done;                // every MMA complete (tcgen05.commit)
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_eref[kVRows];                    // row reference byte e_ref; -1: recomputed
+  __shared__ int s_eref[kVRows];                        // row reference byte e_ref; -1: recomputed
+  __shared__ uint8_t s_bad[2][kVRows];                  // per parity: a block outside the window
   __shared__ GatherSmem gs;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)(blockIdx.x % (unsigned)p.split);
@@ -597,44 +658,42 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
     if (T < 0) return;
     w = p.w + (uint64_t)gs.item[0] * p.expert_stride;
   }
-  uint8_t* abuf = smem;                                 // kVBufs x 16 KB
-  uint8_t* bbuf = smem + kVBufs * kABytes;              // steps x 64 columns x 16 tokens
-  float* part = reinterpret_cast<float*>(smem);         // 16 x 128 fp32, after the MMAs
+  uint8_t* bbuf = smem;                                  // steps x 64 columns x 16 tokens
+  float* part = reinterpret_cast<float*>(smem + (size_t)p.steps * (kVStepK / 8) * 256);  // 16 x 128 fp32
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" :: "r"(smem_addr(&tmem_slot)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(&tmem_slot)), "r"(kTmCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int i = 0; i < kVBufs; ++i) {
+    for (int i = 0; i < kTmAStages; ++i) {
       mbar_init(smem_addr(&empty[i]), 1);
-      mbar_init(smem_addr(&full[i]), kDecoders / 32);
+      mbar_init(smem_addr(&full[i]), 4);
     }
     mbar_init(smem_addr(&done), 1);
     fence_mbar_init();
   }
-  // Lane pairs take the two groups of one row: warp w rows 16 w .. + 15,
-  // lane l row 16 w + l / 2 and group 2 step + l % 2, so one warp load
-  // covers 16 rows x 32 contiguous bytes. The activation copies and the
-  // first window of weight loads go out together: the weights first when the
-  // caller guarantees that they are not the preceding kernel's output (they
-  // are loaded before griddepcontrol.wait), else the activations first.
   const bool decoder = tid < kDecoders;
-  const int h = lane & 1;
-  const int r = (warp & 7) * 16 + (lane >> 1);
+  const int quad = warp & 3, par = (warp >> 2) & 1;
+  const int r = quad * 32 + lane;                       // row of the block (= tensor-memory lane)
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
-  uint8_t* a_row = abuf + (r >> 3) * 128 + (r & 7) * 16;
-  Block<FMT> win[F::window];
+  // this thread's steps: st = par, par + 2, ...; step k of them loads groups
+  // g0 + 2 st and g0 + 2 st + 1 of its row
+  Block<FMT> win[kWin][2];
   if (!p.prefetch) {
     pdl_wait();
     if (decoder) stage_x_bf16_async(p, T, g0, g1, steps, tid, gs.slot, bbuf);
   }
+  Block<FMT> first;
+  load_block<FMT>(p, w, rt, r8, g0, row_ok, first);   // the row's reference scale byte
 #pragma unroll
-  for (int u = 0; u < F::window; ++u) {
-    const int g = g0 + 2 * u + h;
-    load_block<FMT>(p, w, rt, r8, g, row_ok && u < steps && g < g1, win[u]);
+  for (int u = 0; u < kWin; ++u) {
+    const int st = par + 2 * u, g = g0 + 2 * st;
+    load_block<FMT>(p, w, rt, r8, g, row_ok && st < steps && g < g1, win[u][0]);
+    load_block<FMT>(p, w, rt, r8, g + 1, row_ok && st < steps && g + 1 < g1, win[u][1]);
   }
   if (p.prefetch) {
     pdl_wait();
@@ -651,47 +710,54 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
   bool any_bad = false;
 
   if (decoder) {
-    // the row's reference byte: its first block's (the pair's even lane) + kRefMargin
-    const int e_first = __shfl_sync(0xffffffffu, (int)win[0].e, lane & ~1);
+    const int e_first = (int)first.e;
     const int eref = min((e_first == (int)kNoScale ? 127 : e_first) + kRefMargin, 254);
     bool bad = false;
-    for (int s0 = 0; s0 < steps; s0 += F::window) {
+    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);   // this warp's lane quadrant
+    for (int k0 = 0; par + 2 * k0 < steps; k0 += kWin) {
 #pragma unroll
-      for (int u = 0; u < F::window; ++u) {
-        const int st = s0 + u;
+      for (int u = 0; u < kWin; ++u) {
+        const int k = k0 + u, st = par + 2 * k;
         if (st < steps) {
-          const int b = st % kVBufs;
-          if (st >= kVBufs) {
-            // the MMAs that read this buffer kVBufs steps ago are done
-            ok &= mbar_wait_bounded(smem_addr(&empty[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
+          const int sa = st % kTmAStages;
+          if (st >= kTmAStages) {
+            // the MMAs that read this stage kTmAStages steps ago are done
+            ok &= mbar_wait_bounded(smem_addr(&empty[sa]), (uint32_t)((st / kTmAStages) - 1) & 1u, kWaitLimitNs);
           }
-          bad |= decode_store_ref<FMT>(win[u], eref, a_row + (size_t)b * kABytes, 4 * h);
-          const int gn = g0 + 2 * (st + F::window) + h;
-          load_block<FMT>(p, w, rt, r8, gn, row_ok && st + F::window < steps && gn < g1, win[u]);
-          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t col = tq + kTmACol0 + (uint32_t)sa * 32;
+          uint32_t v[16];
+          bad |= decode_ref<FMT>(win[u][0], eref, v);
+          tmem_st16(col, v);
+          bad |= decode_ref<FMT>(win[u][1], eref, v);
+          tmem_st16(col + 16, v);
+          const int stn = st + 2 * kWin, gn = g0 + 2 * stn;
+          load_block<FMT>(p, w, rt, r8, gn, row_ok && stn < steps && gn < g1, win[u][0]);
+          load_block<FMT>(p, w, rt, r8, gn + 1, row_ok && stn < steps && gn + 1 < g1, win[u][1]);
+          tmem_wait_st();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&full[b]));
+          if (lane == 0) mbar_arrive(smem_addr(&full[sa]));
         }
       }
     }
-    bad |= __shfl_xor_sync(0xffffffffu, (int)bad, 1) != 0;
-    if (h == 0) s_eref[r] = bad ? -1 : eref;
+    s_bad[par][r] = bad ? 1 : 0;
+    if (par == 0) s_eref[r] = eref;
     any_bad = bad;
   } else if (lane == 0) {
-    // MMA issue: step st once every decoding warp has written its A buffer;
-    // one accumulator for the whole K range.
+    // MMA issue: step st once the 4 warps of its parity have written its A
+    // stage; one accumulator for the whole K range.
     for (int st = 0; st < steps; ++st) {
-      const int b = st % kVBufs;
-      ok &= mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
+      const int sa = st % kTmAStages;
+      ok &= mbar_wait_bounded(smem_addr(&full[sa]), (uint32_t)(st / kTmAStages) & 1u, kWaitLimitNs);
       tc_fence_after();
-      const uint32_t a0 = smem_addr(abuf + (size_t)b * kABytes);
+      const uint32_t a0 = tmem + kTmACol0 + (uint32_t)sa * 32;
       const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
 #pragma unroll
       for (int j = 0; j < kVStepK / 16; ++j) {
-        mma_f16<true>(tmem, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                      (st > 0 || j > 0) ? 1u : 0u);
+        mma_bf16_ts(tmem, a0 + (uint32_t)j * 8, mma_desc(b0 + j * 2 * 256, 256, 128), (st > 0 || j > 0) ? 1u : 0u);
       }
-      mma_commit(smem_addr(&empty[b]));
+      mma_commit(smem_addr(&empty[sa]));
     }
     mma_commit(smem_addr(&done));
   }
@@ -699,12 +765,12 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
   ok &= mbar_wait_bounded(smem_addr(&done), 0u, kWaitLimitNs);
   if (!__all_sync(0xffffffffu, ok) && lane == 0) set_status(kStatusWaitTile);
   tc_fence_before();
-  any_bad = __syncthreads_or(any_bad) != 0;   // every row's e_ref is in s_eref
+  any_bad = __syncthreads_or(any_bad) != 0;   // every row's e_ref and flags are in shared memory
   tc_fence_after();
 
   // Accumulator rows 32 w .. 32 w + 31 (tensor-memory lanes of warp w) ->
-  // partial sums part[t][row] = D x 2^(e_ref - 127). The A buffers are free:
-  // every MMA that read them has completed.
+  // partial sums part[t][row] = D x 2^(e_ref - 127); a flagged row gets
+  // e_ref = -1 here (this thread's own row) and is recomputed below.
   if (warp < 4) {
     float v0[8], v1[8];
     const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
@@ -712,7 +778,11 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
     tmem_ld8(ta + 8u, v1);
     tmem_wait_ld();
     const int rr = warp * 32 + lane;
-    const int er = s_eref[rr];
+    int er = s_eref[rr];
+    if (s_bad[0][rr] | s_bad[1][rr]) {
+      er = -1;
+      s_eref[rr] = -1;
+    }
     const float f = e8m0_to_f32(er < 0 ? 127u : (uint32_t)er);
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
@@ -721,14 +791,15 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_co
     }
   }
   tc_fence_before();
+  __syncthreads();
   if (any_bad) {
-    __syncthreads();
     recompute_rows<FMT>(p, w, rb, g0, g1, T, bbuf, s_eref, part, warp, lane);
+    __syncthreads();
   }
   cluster_store<FMT>(p, part, rank, rb, T, gs.slot, tid);
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" :: "r"(tmem));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmCols));
   }
 }
 
@@ -983,8 +1054,9 @@ bool verify_supported(const MatvecArgs& a) {
 // Dynamic shared memory: the A buffers and the activation operand, plus for
 // the codebooks the ring of scale bytes and the per-group activation scales.
 size_t verify_smem_bytes(bool mx, int steps) {
+  if (mx) return (size_t)steps * (kVStepK / 8) * 256 + (size_t)kVTok * kVRows * 4;   // B, then part
   const size_t base = (size_t)kVBufs * kABytes + (size_t)steps * (kVStepK / 8) * 256;
-  return mx ? base : base + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4;
+  return base + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4;
 }
 
 template <int FMT>
