@@ -53,7 +53,7 @@
 // outputs. Per CTA: 8 decoding warps, their weight loads issued a window of
 // steps ahead, and one warp that issues the MMAs. A stages of 64 columns,
 // each with a "full" barrier (one arrival per decoding warp that writes it)
-// and an "empty" one (tcgen05.commit). MX: six stages in tensor memory; warp
+// and an "empty" one (tcgen05.commit). MX: three stages in tensor memory; warp
 // w writes rows 32 (w % 4) .. + 31 (its quadrant of lanes) of the steps of
 // parity w / 4, both 32-groups of the step for its row (one tcgen05.st of 16
 // columns each). Codebooks: three stages in shared memory; warp w decodes
@@ -115,10 +115,11 @@ struct CbAcc {
 template <int FMT>
 struct VFmt {
   static constexpr int spl = lane_scale_bytes(FMT);            // E8M0 bytes per lane block: 1 or 2
-  // Weight loads in flight per thread: 128 bytes of lane blocks for the MX
-  // formats, so two CTAs keep ~64 KB per SM in flight; fewer blocks for the
-  // codebooks, whose decode needs more registers.
-  static constexpr int window = fmt_is_mx(FMT) ? 128 / lane_code_bytes(FMT) : (FMT == CB2 ? 8 : 6);
+  // Weight loads in flight per thread: MX formats, 4 lane blocks (the two
+  // 32-groups of 2 steps; measured on GB300: 2 steps beat 1, 3 and 4 steps
+  // for MXFP4 and equal 4 for MXFP8); fewer blocks for the codebooks, whose
+  // decode needs more registers.
+  static constexpr int window = fmt_is_mx(FMT) ? 4 : (FMT == CB2 ? 8 : 6);
   static constexpr int words = (FMT == CB3) ? 3 : lane_code_bytes(FMT) / 4;
 };
 
@@ -621,9 +622,9 @@ __device__ __forceinline__ bool decode_ref(const Block<FMT>& b, int eref, uint32
   return bad;
 }
 
-constexpr int kTmAStages = 6;          // MX: A operand stages in tensor memory (32 columns each)
+constexpr int kTmAStages = 3;          // MX: A operand stages in tensor memory (32 columns each)
 constexpr uint32_t kTmACol0 = 32;      // MX: first A column (the accumulator takes columns 0..15)
-constexpr uint32_t kTmCols = 256;      // MX: tensor-memory columns per CTA (two CTAs per SM)
+constexpr uint32_t kTmCols = 128;      // MX: tensor-memory columns per CTA (accumulator + 3 stages)
 
 // MX formats: bf16 operands code x 2^(e - e_ref), one accumulator per row
 // for the CTA's whole K range, 2^(e_ref - 127) applied in the epilogue. The
