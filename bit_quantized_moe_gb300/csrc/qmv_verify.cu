@@ -622,6 +622,7 @@ __device__ __forceinline__ bool decode_ref(const Block<FMT>& b, int eref, uint32
   return bad;
 }
 
+constexpr int kShortKSteps = 8;         // MX: steps per CTA up to which the 3-CTA build runs
 constexpr int kTmAStages = 3;          // MX: A operand stages in tensor memory (32 columns each)
 constexpr uint32_t kTmACol0 = 32;      // MX: first A column (the accumulator takes columns 0..15)
 constexpr uint32_t kTmCols = 128;      // MX: tensor-memory columns per CTA (accumulator + 3 stages)
@@ -631,9 +632,11 @@ constexpr uint32_t kTmCols = 128;      // MX: tensor-memory columns per CTA (acc
 // A operand lives in tensor memory: lane = row, a step's 64 columns in 32
 // columns of bf16 pairs; warp w decodes rows 32 (w % 4) .. + 31 (its
 // quadrant of lanes) and the steps of parity w / 4, both lane blocks of the
-// step for its row, and writes them with one tcgen05.st each.
-template <int FMT>
-__global__ void __launch_bounds__(kVThreads, 2) verify_mx_kernel(const __grid_constant__ VParams p) {
+// step for its row, and writes them with one tcgen05.st each. CTAS: the CTAs
+// per SM the registers are sized for (3 for short K ranges, where it measured
+// faster; 2 otherwise).
+template <int FMT, int CTAS>
+__global__ void __launch_bounds__(kVThreads, CTAS) verify_mx_kernel(const __grid_constant__ VParams p) {
   using F = VFmt<FMT>;
   static_assert(fmt_is_mx(FMT), "MX formats");
   constexpr int kWin = F::window / 2;   // steps of loads in flight per thread (two lane blocks each)
@@ -1102,27 +1105,31 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
   p.n_experts = a.n_experts;
   p.expert_stride = a.expert_stride;
   constexpr bool kMx = fmt_is_mx(FMT);
-  auto kernel = [] {
+  // MX: the build sized for three CTAs per SM (72 registers) when each CTA's
+  // K range is short (measured on GB300: 2880^2 x 8-16 tokens, 6 steps per
+  // CTA, 7-9% faster; 7168^2, 23 steps, slower)
+  const int variant = (kMx && p.steps <= kShortKSteps) ? 1 : 0;
+  auto kernel = [variant] {
     if constexpr (kMx) {
-      return verify_mx_kernel<FMT>;
+      return variant ? verify_mx_kernel<FMT, 3> : verify_mx_kernel<FMT, 2>;
     } else {
       return verify_kernel<FMT>;
     }
   }();
   const size_t smem = verify_smem_bytes(kMx, p.steps);
   static std::mutex mu;
-  static size_t configured[64] = {};
+  static size_t configured[2][64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (configured[dev] < smem) {
+    if (configured[variant][dev] < smem) {
       g_launch_stage = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
       err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (err != cudaSuccess) return err;
-      configured[dev] = smem;
+      configured[variant][dev] = smem;
     }
   }
   cudaLaunchConfig_t cfg = {};
