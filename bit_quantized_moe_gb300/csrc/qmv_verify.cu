@@ -109,7 +109,15 @@ template <int FMT>
 struct CbAcc {
   static constexpr int span = fmt_group(FMT);                  // columns per accumulator (one scale)
   static constexpr int blocks = kVStepK / span;                // accumulators per step: 2 or 4
-  static constexpr int acc_cols = kAccSteps * blocks * kVTok;  // tensor memory columns: 128 or 256
+  static constexpr int acc_cols = kAccSteps * blocks * kVTok;  // accumulator columns: 128 or 256
+  // CB4 (128 accumulator columns) keeps its A operand in tensor memory too:
+  // a_bufs stages of 32 columns from column acc_cols; CB2 / CB3 stage it in
+  // kVBufs shared-memory buffers.
+  static constexpr bool tm_a = (FMT == CB4);
+  static constexpr int a_bufs = tm_a ? 4 : kVBufs;
+  static constexpr uint32_t tm_cols = tm_a ? 256u : (uint32_t)acc_cols;
+  static_assert(!tm_a || acc_cols + a_bufs * 32 <= 256, "A stages beside the accumulators");
+  static_assert(kLag < a_bufs && a_bufs <= 4, "drain lag within the A ring");
 };
 
 template <int FMT>
@@ -117,9 +125,11 @@ struct VFmt {
   static constexpr int spl = lane_scale_bytes(FMT);            // E8M0 bytes per lane block: 1 or 2
   // Weight loads in flight per thread: MX formats, 4 lane blocks (the two
   // 32-groups of 2 steps; measured on GB300: 2 steps beat 1, 3 and 4 steps
-  // for MXFP4 and equal 4 for MXFP8); fewer blocks for the codebooks, whose
-  // decode needs more registers.
-  static constexpr int window = fmt_is_mx(FMT) ? 4 : (FMT == CB2 ? 8 : 6);
+  // for MXFP4 and equal 4 for MXFP8); CB2 8 and CB3 6 (4 and 5 measured
+  // slower); CB4, whose kernel is bound by issue rather than load latency,
+  // 1 (7168^2 x 16 tokens: 29.2 us against 30.9 with 2, 33.2 with 4 and 39.7
+  // with 6, where ptxas spills).
+  static constexpr int window = fmt_is_mx(FMT) ? 4 : (FMT == CB2 ? 8 : (FMT == CB4 ? 1 : 6));
   static constexpr int words = (FMT == CB3) ? 3 : lane_code_bytes(FMT) / 4;
 };
 
@@ -251,11 +261,9 @@ __device__ __forceinline__ void biased_i8x4_to_f16x2(uint32_t v, uint32_t& lo, u
 
 
 // Codebooks: 32 codes of a lane block -> 32 exact f16 element values
-// (unscaled integers), written as four 16-byte core-matrix rows (k groups
-// kk0 .. kk0 + 3, kALbo bytes apart).
+// (unscaled integers) as 16 f16x2 words in K order (low half first).
 template <int FMT>
-__device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t (&lut)[4], uint8_t* a_row,
-                                             int kk0) {
+__device__ __forceinline__ void decode_words(const Block<FMT>& b, const uint32_t (&lut)[4], uint32_t (&out)[16]) {
   static_assert(!fmt_is_mx(FMT), "codebook decode");
   uint32_t v[8];
   if constexpr (FMT == CB2) {
@@ -266,9 +274,17 @@ __device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t
     const uint32_t w4[4] = {b.c[0], b.c[1], b.c[2], b.c[3]};
     decode_cb4(w4, lut, v);
   }
-  uint32_t out[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) biased_i8x4_to_f16x2(v[i], out[2 * i], out[2 * i + 1]);
+}
+
+// The same values written as four 16-byte core-matrix rows (k groups
+// kk0 .. kk0 + 3, kALbo bytes apart) of a shared-memory A operand.
+template <int FMT>
+__device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t (&lut)[4], uint8_t* a_row,
+                                             int kk0) {
+  uint32_t out[16];
+  decode_words<FMT>(b, lut, out);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
@@ -585,12 +601,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// MMA with A read from tensor memory (M = 128 lanes, K = 16 bf16 in 8
-// columns), B from shared memory.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
+// MMA with A read from tensor memory (M = 128 lanes, K = 16 bf16 or f16
+// in 8 columns), B from shared memory.
+template <bool BF16>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
-               :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(kIdescBf16), "r"(accumulate));
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(BF16 ? kIdescBf16 : kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
+  mma_ts<true>(d_tmem, a_tmem, b, accumulate);
 }
 
 // MX: 32 codes of a lane block -> 16 bf16x2 words code x 2^(e - e_ref) (as
@@ -808,15 +829,20 @@ __global__ void __launch_bounds__(kVThreads, CTAS) verify_mx_kernel(const __grid
 }
 
 // Codebook formats: f16 integer operands, one tensor-memory accumulator per
-// (half-)block scale, drained by the decoding warps into fp32 row sums.
+// (half-)block scale, drained by the decoding warps into fp32 row sums. The
+// A operand is a ring of steps, in tensor memory for CB4 (lane = row,
+// a step's 64 columns in 32 columns of f16 pairs, each decoding warp writing
+// its quadrant of lanes and its 32-group with one tcgen05.st) and in shared
+// memory for CB2 / CB3, whose accumulators fill the columns.
 template <int FMT>
 __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_constant__ VParams p) {
   using F = VFmt<FMT>;
   using C = CbAcc<FMT>;
   static_assert(!fmt_is_mx(FMT), "codebook formats");
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t empty[kVBufs];      // A buffer read by the MMAs (tcgen05.commit)
-  __shared__ __align__(8) uint64_t full[kVBufs];       // A buffer written by all decoding warps
+  constexpr int kBufs = C::a_bufs;
+  __shared__ __align__(8) uint64_t empty[kBufs];       // A buffer read by the MMAs (tcgen05.commit)
+  __shared__ __align__(8) uint64_t full[kBufs];        // A buffer written by all decoding warps
   __shared__ __align__(8) uint64_t accd[kAccSteps];    // a step's accumulators complete (tcgen05.commit)
   __shared__ __align__(8) uint64_t accf[kAccSteps];    // a step's accumulators drained (one arrival per decoding warp)
   __shared__ __align__(8) uint64_t done;               // every MMA complete (tcgen05.commit)
@@ -836,19 +862,21 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     if (T < 0) return;
     w = p.w + (uint64_t)gs.item[0] * p.expert_stride;
   }
-  uint8_t* abuf = smem;                                               // kVBufs x 16 KB
-  uint8_t* bbuf = smem + kVBufs * kABytes;                            // steps x 64 columns x 16 tokens
+  constexpr bool kTmA = C::tm_a;
+  uint8_t* abuf = smem;                                               // kVBufs x 16 KB (shared-memory A)
+  uint8_t* bbuf = smem + (kTmA ? 0 : kVBufs * kABytes);               // steps x 64 columns x 16 tokens
   uint16_t* sc = reinterpret_cast<uint16_t*>(bbuf + (size_t)p.steps * (kVStepK / 8) * 256);  // [ring][2][128]
   float* aux = reinterpret_cast<float*>(sc + kScaleRing * 2 * kVRows);  // [2 steps][16]: 2^-s or d
-  float* part = reinterpret_cast<float*>(smem);                       // 16 x 128 fp32, after the MMAs
+  // 16 x 128 fp32 partial sums: after aux, or over the A buffers once the MMAs are done
+  float* part = kTmA ? aux + (size_t)p.steps * 2 * kVTok : reinterpret_cast<float*>(smem);
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_addr(&tmem_slot)), "r"(C::acc_cols));
+                 :: "r"(smem_addr(&tmem_slot)), "r"(C::tm_cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int i = 0; i < kVBufs; ++i) {
+    for (int i = 0; i < kBufs; ++i) {
       mbar_init(smem_addr(&empty[i]), 1);
       mbar_init(smem_addr(&full[i]), kDecoders / 32);
     }
@@ -966,18 +994,30 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       for (int u = 0; u < kWindow; ++u) {
         const int st = s0 + u;
         if (st < steps && ok) {
-          const int b = st % kVBufs;
-          if (st >= kVBufs) {
-            // the MMAs that read this buffer kVBufs steps ago are done
-            ok = ok && mbar_wait_bounded(smem_addr(&empty[b]), (uint32_t)((st / kVBufs) - 1) & 1u, kWaitLimitNs);
+          const int b = st % kBufs;
+          if (st >= kBufs) {
+            // the MMAs that read this buffer kBufs steps ago are done
+            ok = ok && mbar_wait_bounded(smem_addr(&empty[b]), (uint32_t)((st / kBufs) - 1) & 1u, kWaitLimitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
-          decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
+          if constexpr (kTmA) {
+            tc_fence_after();   // after the MMAs that read the stage
+            uint32_t v[16];
+            decode_words<FMT>(win[u], lut, v);
+            tmem_st16(tlane + (uint32_t)C::acc_cols + (uint32_t)b * 32u + (uint32_t)h * 16u, v);
+          } else {
+            decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
+          }
           my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
           const int gn = g0 + 2 * (st + kWindow) + h;
           load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
-          fence_proxy_async_smem();
+          if constexpr (kTmA) {
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            fence_proxy_async_smem();
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&full[b]));
           if (st >= kLag) drain(st - kLag);
@@ -989,8 +1029,8 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     // MMA issue: step st once every decoding warp has written its A buffer
     // and the accumulators it reuses have been drained.
     for (int st = 0; st < steps && ok; ++st) {
-      const int b = st % kVBufs;
-      ok = mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kVBufs) & 1u, kWaitLimitNs);
+      const int b = st % kBufs;
+      ok = mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kBufs) & 1u, kWaitLimitNs);
       if (ok && st >= kAccSteps) {
         ok = mbar_wait_bounded(smem_addr(&accf[st % kAccSteps]), (uint32_t)((st / kAccSteps) - 1) & 1u, kWaitLimitNs);
       }
@@ -1002,8 +1042,14 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       for (int j = 0; j < kVStepK / 16; ++j) {
         const int blk = j * 16 / C::span;
         const uint32_t col = (uint32_t)(((st % kAccSteps) * C::blocks + blk) * kVTok);
-        mma_f16<false>(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                       (j * 16 % C::span) != 0 ? 1u : 0u);
+        const uint32_t acc = (j * 16 % C::span) != 0 ? 1u : 0u;
+        if constexpr (kTmA) {
+          mma_ts<false>(tmem + col, tmem + (uint32_t)C::acc_cols + (uint32_t)b * 32u + (uint32_t)j * 8u,
+                        mma_desc(b0 + j * 2 * 256, 256, 128), acc);
+        } else {
+          mma_f16<false>(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
+                         acc);
+        }
       }
       mma_commit(smem_addr(&empty[b]));
       mma_commit(smem_addr(&accd[st % kAccSteps]));
@@ -1013,9 +1059,9 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   }
   if (!ok && lane == 0) set_status(kStatusWaitTile);
 
-  // Partial sums part[t][row] (the A buffers are free: every MMA that read
-  // them completed before the MMA warp passed `done`, or before the last
-  // drain).
+  // Partial sums part[t][row] (shared-memory A buffers are free: every MMA
+  // that read them completed before the MMA warp passed `done`, or before
+  // the last drain).
   __syncthreads();
   if (decoder && h == 0) {
 #pragma unroll
@@ -1031,7 +1077,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   cluster_store<FMT>(p, part, rank, rb, T, gs.slot, tid);
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::acc_cols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::tm_cols));
   }
 }
 
@@ -1055,12 +1101,14 @@ bool verify_supported(const MatvecArgs& a) {
   return (groups + kVMaxSplit - 1) / kVMaxSplit <= 2 * kVMaxSteps;
 }
 
-// Dynamic shared memory: the A buffers and the activation operand, plus for
-// the codebooks the ring of scale bytes and the per-group activation scales.
-size_t verify_smem_bytes(bool mx, int steps) {
-  if (mx) return (size_t)steps * (kVStepK / 8) * 256 + (size_t)kVTok * kVRows * 4;   // B, then part
-  const size_t base = (size_t)kVBufs * kABytes + (size_t)steps * (kVStepK / 8) * 256;
-  return base + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4;
+// Dynamic shared memory: the activation operand and the partial sums; for
+// the codebooks also the ring of scale bytes, the per-group activation
+// scales and (CB2 / CB3) the A buffers, which the partial sums reuse.
+size_t verify_smem_bytes(int fmt, int steps) {
+  const size_t b = (size_t)steps * (kVStepK / 8) * 256, part = (size_t)kVTok * kVRows * 4;
+  if (fmt_is_mx(fmt)) return b + part;
+  const size_t cb = b + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4;
+  return fmt == CB4 ? cb + part : cb + (size_t)kVBufs * kABytes;
 }
 
 template <int FMT>
@@ -1116,7 +1164,7 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
       return verify_kernel<FMT>;
     }
   }();
-  const size_t smem = verify_smem_bytes(kMx, p.steps);
+  const size_t smem = verify_smem_bytes(FMT, p.steps);
   static std::mutex mu;
   static size_t configured[2][64] = {};
   int dev = 0;

@@ -105,8 +105,8 @@ typedef enum { QMV_MXFP4 = 0, QMV_CB2 = 1, QMV_CB3 = 2, QMV_CB4 = 3, QMV_MXFP8 =
  * Without them the choice follows a cost model measured on GB300: MX dense
  * verify batches and MX gathers of >= 4 slots per distinct expert take the
  * tensor cores; codebook dense batches do when their CUDA-core weight
- * streams (one per 4 tokens) exceed 64 MB, codebook gathers at >= 12 slots
- * per expert. PATH_TENSOR applies to calls that have a tensor-core form
+ * streams (one per 4 tokens) exceed 64 MB, CB4 gathers at >= 8 slots per
+ * expert, CB2 / CB3 gathers at >= 12. PATH_TENSOR applies to calls that have a tensor-core form
  * (5..16 dense tokens or 33..128 slots, not fp16 activations, not the
  * gate/up fusion) and is ignored by the others. Not both. Results differ
  * between the two paths only in the order of fp32 additions (integer block

@@ -170,11 +170,13 @@ def test_path_dense_verify_batches():
     ("mxfp8", 8, 9, 4, True),       # 36 slots, 4.5 per expert
     ("cb3", 8, 16, 8, True),        # 128 slots, 16 per expert
     ("cb3", 16, 16, 8, False),      # 128 slots, 8 per expert
+    ("cb4", 16, 16, 8, True),       # 128 slots, 8 per expert (A in tensor memory: cheaper per item)
+    ("cb4", 32, 16, 8, False),      # 128 slots, 4 per expert
     ("cb2", 2, 16, 2, True),        # 32 slots: the decode gather
 ])
 def test_path_gathers(fmt, E, ntok, top_k, tensor):
     """Gathers of 33..128 routed slots: the sorted tensor-core gather at >= 4
-    (MX) or >= 12 (codebooks) slots per expert that can occur, else CUDA-core
+    (MX), >= 8 (CB4) or >= 12 (CB2, CB3) slots per expert that can occur, else CUDA-core
     gathers of 32-slot token ranges; 32 slots or fewer are always the decode
     gather in one launch."""
     lut = {"cb2": [0] * 4, "cb3": [0] * 8, "cb4": [0] * 16}.get(fmt)
