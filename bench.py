@@ -827,6 +827,12 @@ def run_profile_config(args):
         x = torch.from_numpy(qi.normal_bf16_bits(g, (16, 7168)).view(np.int16)).to(dev).view(torch.bfloat16)
         y = torch.empty(16, 7168, dtype=torch.bfloat16, device=dev)
         fn = lambda i: qmv.qmv_dense_ex(d, w, x, 16, y, qmv.QMV_FLAG_PREFETCH_INPUTS)
+    elif cfg == 7:
+        # verify batch: dense CB4 7168 x 7168, 16 q8_1 tokens (tensor-core path)
+        w, d = packed("cb4", 1, 7168, 7168)
+        xq = q8(16, 7168)
+        y = torch.empty(16, 7168, dtype=torch.float32, device=dev)
+        fn = lambda i: qmv.qmv_dense_ex(d, w, xq, 16, y, qmv.QMV_FLAG_PREFETCH_INPUTS)
     elif cfg == 3:
         w, d = packed("cb3", E, 7168, 2048)
         xq = q8(16, 2048)
@@ -1050,9 +1056,9 @@ def main(argv=None):
                     help="build the phase-probe variant and print where each launch's time goes")
     ap.add_argument("--configs", action="store_true",
                     help="measure every config of the workload set (one JSON line per call type) and exit")
-    ap.add_argument("--profile-config", type=int, choices=[0, 2, 3, 4, 5, 6], default=None,
+    ap.add_argument("--profile-config", type=int, choices=[0, 2, 3, 4, 5, 6, 7], default=None,
                     help="a few eager calls of one config on a small resident set, for ncu captures "
-                         "(5: the MXFP8 layer; 6: a 16-token MXFP4 7168x7168 verify batch)")
+                         "(5: the MXFP8 layer; 6 / 7: a 16-token MXFP4 / CB4 7168x7168 verify batch)")
     args = ap.parse_args(argv)
     if args.digest:
         print(kernel_source_digest())

@@ -132,9 +132,9 @@ int gate_up_rows(int N) { return 2 * ((N + kRows / 2 - 1) / (kRows / 2) * (kRows
 // of them is streamed by each). Measured on GB300 (2880^2 MXFP4 and
 // 7168 x 2048 / 2048 x 7168 codebook experts, 64-128 slots): the MX tensor
 // path breaks even at 4 slots per expert; CB4's (one accumulator per block,
-// drained on the CUDA cores; A in tensor memory) at about 7 (8 per expert:
-// 150 against 195 us, 6.4: 186 against 191, 4: 283 against 208); CB2 /
-// CB3's (A in shared memory) at about 12.
+// drained on the CUDA cores) at about 7 (8 per expert: 150 against 195 us,
+// 6.4: 186 against 191, 4: 283 against 208); CB2 / CB3's (two accumulators
+// per 32-group) at about 12.
 constexpr int kSortedMinSlotsPerExpertMx = 4;
 constexpr int kSortedMinSlotsPerExpertCb4 = 8;
 constexpr int kSortedMinSlotsPerExpertCb = 12;
@@ -151,7 +151,7 @@ bool sorted_gather_pays(const MatvecArgs& a) {
 // CUDA-core path's weight streams (one per 4 tokens, side by side) would
 // overflow the L2 cache: below that the repeated streams hit L2 and the
 // CUDA cores are faster (measured on GB300: 7168 x 2048 CB3 and 2048 x 7168
-// CB2 at 16 tokens 10.4 / 11.3 us on the CUDA cores against 14.9 / 19.1 us
+// CB2 at 16 tokens 10.4 / 11.3 us on the CUDA cores against 13.4 / 17.9 us
 // on the tensor cores; 7168^2 CB4 47.0 against 29.2 us).
 constexpr uint64_t kCbDenseTensorBytes = 64ull << 20;
 

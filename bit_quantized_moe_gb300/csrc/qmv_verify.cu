@@ -56,18 +56,21 @@
 // and an "empty" one (tcgen05.commit). MX: three stages in tensor memory; warp
 // w writes rows 32 (w % 4) .. + 31 (its quadrant of lanes) of the steps of
 // parity w / 4, both 32-groups of the step for its row (one tcgen05.st of 16
-// columns each). Codebooks: three stages in shared memory; warp w decodes
-// rows 32 (w % 4) .. + 31 (the
-// tensor-memory lanes it may read) and group w / 4 of every step; the
-// accumulators of kAccSteps steps live in tensor memory, each step's with an
-// "accumulated" barrier (tcgen05.commit) and a "drained" one, and a warp
-// drains step st - kLag after decoding step st. A sorted gather adds a second
-// grid dimension of work items, one (expert, up to 16 of its slots) pair each.
+// columns each). Codebooks: stages in tensor memory after the accumulators
+// (four for CB4, two for CB2 / CB3); warp w decodes rows 32 (w % 4) .. + 31
+// (the tensor-memory lanes it may read and write) and group w / 4 of every
+// step, one tcgen05.st of 16 columns per block; the accumulators of a few
+// steps (four, or three when a step has four blocks) live in tensor memory,
+// each step's with an "accumulated" barrier (tcgen05.commit) and a
+// "drained" one, and a warp drains step st - kLag after decoding step st. A
+// sorted gather adds a second grid dimension of work items, one (expert, up
+// to 16 of its slots) pair each.
 //
-// Operand layouts (no swizzle, K-major "canonical" core matrices of 8 rows x
-// 16 bytes): A step buffer (128 rows x 64 columns), core matrix (row group
-// g, k group kk) at kk * 2048 + g * 128; B (activations, tokens padded to 16
-// with zeros), core matrix (token group g, k group kk) at kk * 256 + g * 128.
+// Operand layouts: A in tensor memory, lane = row, column j of a stage =
+// elements 2j and 2j + 1 of the step (low half first); B (activations,
+// tokens padded to 16 with zeros) in shared memory as no-swizzle K-major
+// "canonical" core matrices of 8 rows x 16 bytes, core matrix (token group
+// g, k group kk) at kk * 256 + g * 128.
 // Descriptor leading byte offset = the K-direction stride, stride byte
 // offset = the row-direction stride.
 #include <cooperative_groups.h>
@@ -90,14 +93,9 @@ constexpr int kVRows = 128;      // rows per CTA (MMA M)
 constexpr int kVTok = 16;        // MMA N: tokens, padded
 constexpr int kDecoders = 256;   // decoding threads: two per row
 constexpr int kVThreads = kDecoders + 32;   // plus one warp that issues the MMAs
-constexpr int kVStepK = 64;      // columns per step (one A buffer): 2 groups of 32
-constexpr int kVBufs = 3;        // A buffers
-constexpr int kAccSteps = 4;     // codebooks: steps whose accumulators tensor memory holds at once
+constexpr int kVStepK = 64;      // columns per step (one A stage): 2 groups of 32
 constexpr int kLag = 2;          // codebooks: a decoding warp drains step st - kLag after decoding step st
 constexpr int kScaleRing = 8;    // codebooks: steps of E8M0 bytes kept for the drains
-static_assert(kLag < kVBufs && kLag < kAccSteps, "drain lag within the buffer and accumulator rings");
-constexpr uint32_t kABytes = kVRows * kVStepK * 2;   // 16 KB
-constexpr uint32_t kALbo = kVRows / 8 * 128;          // A: k-group stride (16 row groups of 128 B)
 constexpr int kVMaxSplit = 8;    // cluster size limit (portable)
 constexpr int kVMaxSlots = 128;  // routed slots of a sorted gather
 constexpr int kVMaxSteps = 24;   // activation operand <= 48 KB (two CTAs per SM)
@@ -109,15 +107,18 @@ template <int FMT>
 struct CbAcc {
   static constexpr int span = fmt_group(FMT);                  // columns per accumulator (one scale)
   static constexpr int blocks = kVStepK / span;                // accumulators per step: 2 or 4
-  static constexpr int acc_cols = kAccSteps * blocks * kVTok;  // accumulator columns: 128 or 256
-  // CB4 (128 accumulator columns) keeps its A operand in tensor memory too:
-  // a_bufs stages of 32 columns from column acc_cols; CB2 / CB3 stage it in
-  // kVBufs shared-memory buffers.
-  static constexpr bool tm_a = (FMT == CB4);
-  static constexpr int a_bufs = tm_a ? 4 : kVBufs;
-  static constexpr uint32_t tm_cols = tm_a ? 256u : (uint32_t)acc_cols;
-  static_assert(!tm_a || acc_cols + a_bufs * 32 <= 256, "A stages beside the accumulators");
-  static_assert(kLag < a_bufs && a_bufs <= 4, "drain lag within the A ring");
+  // Tensor memory (256 columns): the accumulators of acc_steps steps, then
+  // a_bufs stages of the A operand (32 columns each): CB4 4 steps (128
+  // columns) and 4 stages; CB2 / CB3 3 steps (192 columns) and 2 stages.
+  static constexpr int acc_steps = blocks == 4 ? 3 : 4;
+  static constexpr int acc_cols = acc_steps * blocks * kVTok;
+  static constexpr int a_bufs = (256 - acc_cols) / 32;
+  static constexpr uint32_t tm_cols = 256u;
+  // A stage b of step st is rewritten at step st + a_bufs once MMA(st) is
+  // done; the drain of st runs after decoding st + kLag: with a_bufs >= kLag
+  // neither waits on the other in a cycle. (A lag of 3 for CB4 measured the
+  // same as 2 on GB300.)
+  static_assert(a_bufs >= 2 && a_bufs <= 4 && kLag <= a_bufs && kLag < acc_steps, "A and accumulator rings");
 };
 
 template <int FMT>
@@ -125,11 +126,12 @@ struct VFmt {
   static constexpr int spl = lane_scale_bytes(FMT);            // E8M0 bytes per lane block: 1 or 2
   // Weight loads in flight per thread: MX formats, 4 lane blocks (the two
   // 32-groups of 2 steps; measured on GB300: 2 steps beat 1, 3 and 4 steps
-  // for MXFP4 and equal 4 for MXFP8); CB2 8 and CB3 6 (4 and 5 measured
-  // slower); CB4, whose kernel is bound by issue rather than load latency,
-  // 1 (7168^2 x 16 tokens: 29.2 us against 30.9 with 2, 33.2 with 4 and 39.7
-  // with 6, where ptxas spills).
-  static constexpr int window = fmt_is_mx(FMT) ? 4 : (FMT == CB2 ? 8 : (FMT == CB4 ? 1 : 6));
+  // for MXFP4 and equal 4 for MXFP8). The codebook kernels are bound by
+  // issue rather than load latency, and fewer blocks leave registers to the
+  // drains: CB4 1 (7168^2 x 16 tokens: 29.2 us against 30.9 with 2, 33.2
+  // with 4, 39.7 with 6), CB2 / CB3 2 (128-slot gathers 78.7 / 89.0 us
+  // against 94.6 / 99.6 with 4 and 100.7 / 101.6 with 8 / 6).
+  static constexpr int window = fmt_is_mx(FMT) ? 4 : (FMT == CB4 ? 1 : 2);
   static constexpr int words = (FMT == CB3) ? 3 : lane_code_bytes(FMT) / 4;
 };
 
@@ -168,13 +170,6 @@ __device__ __forceinline__ uint64_t mma_desc(uint32_t addr, uint32_t lbo, uint32
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kVTok >> 3) << 17) | ((uint32_t)(kVRows >> 4) << 24);
 // The same with A and B both bf16 (bits 7-9 and 10-12 = 1): MX formats.
 constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
-
-template <bool BF16>
-__device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
-  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-               " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-               :: "r"(tmem), "l"(a), "l"(b), "r"(BF16 ? kIdescBf16 : kIdesc), "r"(accumulate));
-}
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar)
@@ -278,20 +273,6 @@ __device__ __forceinline__ void decode_words(const Block<FMT>& b, const uint32_t
   for (int i = 0; i < 8; ++i) biased_i8x4_to_f16x2(v[i], out[2 * i], out[2 * i + 1]);
 }
 
-// The same values written as four 16-byte core-matrix rows (k groups
-// kk0 .. kk0 + 3, kALbo bytes apart) of a shared-memory A operand.
-template <int FMT>
-__device__ __forceinline__ void decode_store(const Block<FMT>& b, const uint32_t (&lut)[4], uint8_t* a_row,
-                                             int kk0) {
-  uint32_t out[16];
-  decode_words<FMT>(b, lut, out);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
-        make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-  }
-}
-
 // f16 bits of 2^d for -24 <= d <= 0 (normal down to 2^-14, subnormal below;
 // the fp32 power of two converts exactly).
 __device__ __forceinline__ uint16_t pow2_f16(int d) {
@@ -311,44 +292,6 @@ __device__ __forceinline__ uint32_t scaled_pair_bf16(uint32_t h2, uint16_t m) {
       : "=r"(r)
       : "r"(h2), "h"(m), "f"(0.0f));
   return r;
-}
-
-// MX: 32 codes of a lane block -> 32 bf16 values code x 2^(e - e_ref), four
-// 16-byte core-matrix rows. e - e_ref is clamped to [-24, 0]; returns whether
-// that changed it (or the byte is 255), in which case the row is recomputed
-// on the CUDA cores and its accumulator is not used. A block outside the
-// matrix (scale kNoScale, zero codes) is never flagged.
-template <int FMT>
-__device__ __forceinline__ bool decode_store_ref(const Block<FMT>& b, int eref, uint8_t* a_row, int kk0) {
-  int d = (int)b.e - eref;
-  const bool bad = (d < -kMaxSpread || d > 0) && b.e != kNoScale;
-  d = d < -kMaxSpread ? -kMaxSpread : (d > 0 ? 0 : d);
-  const uint16_t m = pow2_f16(d);
-  uint32_t out[16];
-  if constexpr (FMT == MXFP4) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t h[4];
-      e2m1x8_to_f16x2(b.c[q], h);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) out[4 * q + i] = scaled_pair_bf16(h[i], m);
-    }
-  } else {
-    static_assert(FMT == MXFP8, "MX decode");
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      uint32_t h[2];
-      e4m3x4_to_f16x2(b.c[q], h);
-      out[2 * q] = scaled_pair_bf16(h[0], m);
-      out[2 * q + 1] = scaled_pair_bf16(h[1], m);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    *reinterpret_cast<uint4*>(a_row + (size_t)(kk0 + j) * kALbo) =
-        make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-  }
-  return bad;
 }
 
 // Codebooks, activation operand B: one (token t, local 32-group gl) unit --
@@ -614,9 +557,11 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
   mma_ts<true>(d_tmem, a_tmem, b, accumulate);
 }
 
-// MX: 32 codes of a lane block -> 16 bf16x2 words code x 2^(e - e_ref) (as
-// decode_store_ref, into registers). Returns whether the block's scale byte
-// is outside [e_ref - 24, e_ref].
+// MX: 32 codes of a lane block -> 16 bf16x2 words code x 2^(e - e_ref) in K
+// order. e - e_ref is clamped to [-24, 0]; returns whether that changed it
+// (or the byte is 255), in which case the row is recomputed on the CUDA
+// cores and its accumulator is not used. A block outside the matrix (scale
+// kNoScale, zero codes) is never flagged.
 template <int FMT>
 __device__ __forceinline__ bool decode_ref(const Block<FMT>& b, int eref, uint32_t (&out)[16]) {
   int d = (int)b.e - eref;
@@ -830,10 +775,9 @@ __global__ void __launch_bounds__(kVThreads, CTAS) verify_mx_kernel(const __grid
 
 // Codebook formats: f16 integer operands, one tensor-memory accumulator per
 // (half-)block scale, drained by the decoding warps into fp32 row sums. The
-// A operand is a ring of steps, in tensor memory for CB4 (lane = row,
-// a step's 64 columns in 32 columns of f16 pairs, each decoding warp writing
-// its quadrant of lanes and its 32-group with one tcgen05.st) and in shared
-// memory for CB2 / CB3, whose accumulators fill the columns.
+// A operand is a ring of steps in tensor memory after the accumulators (lane
+// = row, a step's 64 columns in 32 columns of f16 pairs, each decoding warp
+// writing its quadrant of lanes and its 32-group with one tcgen05.st).
 template <int FMT>
 __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_constant__ VParams p) {
   using F = VFmt<FMT>;
@@ -841,10 +785,11 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   static_assert(!fmt_is_mx(FMT), "codebook formats");
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int kBufs = C::a_bufs;
-  __shared__ __align__(8) uint64_t empty[kBufs];       // A buffer read by the MMAs (tcgen05.commit)
-  __shared__ __align__(8) uint64_t full[kBufs];        // A buffer written by all decoding warps
-  __shared__ __align__(8) uint64_t accd[kAccSteps];    // a step's accumulators complete (tcgen05.commit)
-  __shared__ __align__(8) uint64_t accf[kAccSteps];    // a step's accumulators drained (one arrival per decoding warp)
+  __shared__ __align__(8) uint64_t empty[kBufs];       // A stage read by the MMAs (tcgen05.commit)
+  __shared__ __align__(8) uint64_t full[kBufs];        // A stage written by all decoding warps
+  constexpr int kAcc = C::acc_steps;
+  __shared__ __align__(8) uint64_t accd[kAcc];         // a step's accumulators complete (tcgen05.commit)
+  __shared__ __align__(8) uint64_t accf[kAcc];         // a step's accumulators drained (one arrival per decoding warp)
   __shared__ __align__(8) uint64_t done;               // every MMA complete (tcgen05.commit)
   __shared__ uint32_t tmem_slot;
   __shared__ GatherSmem gs;
@@ -862,13 +807,10 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     if (T < 0) return;
     w = p.w + (uint64_t)gs.item[0] * p.expert_stride;
   }
-  constexpr bool kTmA = C::tm_a;
-  uint8_t* abuf = smem;                                               // kVBufs x 16 KB (shared-memory A)
-  uint8_t* bbuf = smem + (kTmA ? 0 : kVBufs * kABytes);               // steps x 64 columns x 16 tokens
+  uint8_t* bbuf = smem;                                               // steps x 64 columns x 16 tokens
   uint16_t* sc = reinterpret_cast<uint16_t*>(bbuf + (size_t)p.steps * (kVStepK / 8) * 256);  // [ring][2][128]
   float* aux = reinterpret_cast<float*>(sc + kScaleRing * 2 * kVRows);  // [2 steps][16]: 2^-s or d
-  // 16 x 128 fp32 partial sums: after aux, or over the A buffers once the MMAs are done
-  float* part = kTmA ? aux + (size_t)p.steps * 2 * kVTok : reinterpret_cast<float*>(smem);
+  float* part = aux + (size_t)p.steps * 2 * kVTok;                    // 16 x 128 fp32 partial sums
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -880,7 +822,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
       mbar_init(smem_addr(&empty[i]), 1);
       mbar_init(smem_addr(&full[i]), kDecoders / 32);
     }
-    for (int i = 0; i < kAccSteps; ++i) {
+    for (int i = 0; i < kAcc; ++i) {
       mbar_init(smem_addr(&accd[i]), 1);
       mbar_init(smem_addr(&accf[i]), kDecoders / 32);
     }
@@ -900,7 +842,6 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   const int row = rb * kVRows + r;
   const int rt = row >> 3, r8 = row & 7;
   const bool row_ok = decoder && rt < p.row_tiles;
-  uint8_t* a_row = abuf + (r >> 3) * 128 + (r & 7) * 16;
   uint32_t lut[4] = {p.lut[0], p.lut[1], p.lut[2], p.lut[3]};
   constexpr int kWindow = F::window;
   Block<FMT> win[kWindow];
@@ -942,12 +883,12 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
   for (int i = 0; i < kVTok; ++i) acc[i] = 0.f;
   uint16_t* my_sc = sc + warp * 32 + lane;       // [kScaleRing][256 decoding threads]
   auto drain = [&](int sd) {
-    ok = ok && mbar_wait_bounded(smem_addr(&accd[sd % kAccSteps]), (uint32_t)(sd / kAccSteps) & 1u, kWaitLimitNs);
+    ok = ok && mbar_wait_bounded(smem_addr(&accd[sd % kAcc]), (uint32_t)(sd / kAcc) & 1u, kWaitLimitNs);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
     tc_fence_after();
     constexpr int per = C::blocks / 2;   // accumulators per 32-group: 1, or 2 half-blocks
-    const uint32_t col0 = (uint32_t)(((sd % kAccSteps) * C::blocks + h * per) * kVTok);
+    const uint32_t col0 = (uint32_t)(((sd % kAcc) * C::blocks + h * per) * kVTok);
     const int gl = 2 * sd + h;
     const float* f = aux + gl * kVTok;
     const uint32_t eb = my_sc[(sd % kScaleRing) * kDecoders];
@@ -985,7 +926,7 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&accf[sd % kAccSteps]));
+    if (lane == 0) mbar_arrive(smem_addr(&accf[sd % kAcc]));
   };
 
   if (decoder) {
@@ -996,28 +937,20 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
         if (st < steps && ok) {
           const int b = st % kBufs;
           if (st >= kBufs) {
-            // the MMAs that read this buffer kBufs steps ago are done
+            // the MMAs that read this stage kBufs steps ago are done
             ok = ok && mbar_wait_bounded(smem_addr(&empty[b]), (uint32_t)((st / kBufs) - 1) & 1u, kWaitLimitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
-          if constexpr (kTmA) {
-            tc_fence_after();   // after the MMAs that read the stage
-            uint32_t v[16];
-            decode_words<FMT>(win[u], lut, v);
-            tmem_st16(tlane + (uint32_t)C::acc_cols + (uint32_t)b * 32u + (uint32_t)h * 16u, v);
-          } else {
-            decode_store<FMT>(win[u], lut, a_row + (size_t)b * kABytes, 4 * h);
-          }
+          tc_fence_after();   // after the MMAs that read the stage
+          uint32_t v[16];
+          decode_words<FMT>(win[u], lut, v);
+          tmem_st16(tlane + (uint32_t)C::acc_cols + (uint32_t)b * 32u + (uint32_t)h * 16u, v);
           my_sc[(st % kScaleRing) * kDecoders] = (uint16_t)win[u].e;
           const int gn = g0 + 2 * (st + kWindow) + h;
           load_block<FMT>(p, w, rt, r8, gn, row_ok && st + kWindow < steps && gn < g1, win[u]);
-          if constexpr (kTmA) {
-            tmem_wait_st();
-            tc_fence_before();
-          } else {
-            fence_proxy_async_smem();
-          }
+          tmem_wait_st();
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&full[b]));
           if (st >= kLag) drain(st - kLag);
@@ -1026,42 +959,34 @@ __global__ void __launch_bounds__(kVThreads, 2) verify_kernel(const __grid_const
     }
     for (int sd = steps - kLag > 0 ? steps - kLag : 0; sd < steps && ok; ++sd) drain(sd);
   } else if (lane == 0) {
-    // MMA issue: step st once every decoding warp has written its A buffer
+    // MMA issue: step st once every decoding warp has written its A stage
     // and the accumulators it reuses have been drained.
     for (int st = 0; st < steps && ok; ++st) {
       const int b = st % kBufs;
       ok = mbar_wait_bounded(smem_addr(&full[b]), (uint32_t)(st / kBufs) & 1u, kWaitLimitNs);
-      if (ok && st >= kAccSteps) {
-        ok = mbar_wait_bounded(smem_addr(&accf[st % kAccSteps]), (uint32_t)((st / kAccSteps) - 1) & 1u, kWaitLimitNs);
+      if (ok && st >= kAcc) {
+        ok = mbar_wait_bounded(smem_addr(&accf[st % kAcc]), (uint32_t)((st / kAcc) - 1) & 1u, kWaitLimitNs);
       }
       if (!ok) break;
       tc_fence_after();
-      const uint32_t a0 = smem_addr(abuf + (size_t)b * kABytes);
+      const uint32_t a0 = tmem + (uint32_t)C::acc_cols + (uint32_t)b * 32u;
       const uint32_t b0 = smem_addr(bbuf + (size_t)st * (kVStepK / 8) * 256);
 #pragma unroll
       for (int j = 0; j < kVStepK / 16; ++j) {
         const int blk = j * 16 / C::span;
-        const uint32_t col = (uint32_t)(((st % kAccSteps) * C::blocks + blk) * kVTok);
-        const uint32_t acc = (j * 16 % C::span) != 0 ? 1u : 0u;
-        if constexpr (kTmA) {
-          mma_ts<false>(tmem + col, tmem + (uint32_t)C::acc_cols + (uint32_t)b * 32u + (uint32_t)j * 8u,
-                        mma_desc(b0 + j * 2 * 256, 256, 128), acc);
-        } else {
-          mma_f16<false>(tmem + col, mma_desc(a0 + j * 2 * kALbo, kALbo, 128), mma_desc(b0 + j * 2 * 256, 256, 128),
-                         acc);
-        }
+        const uint32_t col = (uint32_t)(((st % kAcc) * C::blocks + blk) * kVTok);
+        mma_ts<false>(tmem + col, a0 + (uint32_t)j * 8u, mma_desc(b0 + j * 2 * 256, 256, 128),
+                      (j * 16 % C::span) != 0 ? 1u : 0u);
       }
       mma_commit(smem_addr(&empty[b]));
-      mma_commit(smem_addr(&accd[st % kAccSteps]));
+      mma_commit(smem_addr(&accd[st % kAcc]));
     }
     mma_commit(smem_addr(&done));
     if (!mbar_wait_bounded(smem_addr(&done), 0u, kWaitLimitNs)) ok = false;
   }
   if (!ok && lane == 0) set_status(kStatusWaitTile);
 
-  // Partial sums part[t][row] (shared-memory A buffers are free: every MMA
-  // that read them completed before the MMA warp passed `done`, or before
-  // the last drain).
+  // Partial sums part[t][row].
   __syncthreads();
   if (decoder && h == 0) {
 #pragma unroll
@@ -1102,13 +1027,12 @@ bool verify_supported(const MatvecArgs& a) {
 }
 
 // Dynamic shared memory: the activation operand and the partial sums; for
-// the codebooks also the ring of scale bytes, the per-group activation
-// scales and (CB2 / CB3) the A buffers, which the partial sums reuse.
-size_t verify_smem_bytes(int fmt, int steps) {
+// the codebooks also the ring of scale bytes and the per-group activation
+// scales.
+static size_t verify_smem_bytes(bool mx, int steps) {
   const size_t b = (size_t)steps * (kVStepK / 8) * 256, part = (size_t)kVTok * kVRows * 4;
-  if (fmt_is_mx(fmt)) return b + part;
-  const size_t cb = b + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4;
-  return fmt == CB4 ? cb + part : cb + (size_t)kVBufs * kABytes;
+  if (mx) return b + part;
+  return b + (size_t)kScaleRing * 2 * kVRows * 2 + (size_t)steps * 2 * kVTok * 4 + part;
 }
 
 template <int FMT>
@@ -1164,7 +1088,7 @@ static cudaError_t launch_verify_fmt(const MatvecArgs& a) {
       return verify_kernel<FMT>;
     }
   }();
-  const size_t smem = verify_smem_bytes(FMT, p.steps);
+  const size_t smem = verify_smem_bytes(kMx, p.steps);
   static std::mutex mu;
   static size_t configured[2][64] = {};
   int dev = 0;
