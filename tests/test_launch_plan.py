@@ -172,6 +172,7 @@ def test_path_dense_verify_batches():
     ("cb3", 16, 16, 8, False),      # 128 slots, 8 per expert
     ("cb4", 16, 16, 8, True),       # 128 slots, 8 per expert (A in tensor memory: cheaper per item)
     ("cb4", 32, 16, 8, False),      # 128 slots, 4 per expert
+    ("cb2", 8, 16, 8, True),        # 128 slots, 16 per expert
     ("cb2", 2, 16, 2, True),        # 32 slots: the decode gather
 ])
 def test_path_gathers(fmt, E, ntok, top_k, tensor):
